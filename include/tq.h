@@ -1,0 +1,279 @@
+/*
+ * tq.h -- C ABI of the GB300 TurboQuant compressed-KV library (libtq.so).
+ *
+ * TurboQuant stores each key/value vector of a KV cache as its norm plus the
+ * Lloyd-Max codebook indices of its randomly rotated unit vector, bit-packed
+ * into uint32 words; "prod" keys add a 1-bit QJL sign sketch of the rotated
+ * residual and the residual norm; values may instead use per-group affine
+ * quantisation. Decode attention reads that compressed cache directly.
+ *
+ * Sources, by page title:
+ *   "lightning-mlx/plan.md"               -- codec outline (rotation, Lloyd-Max,
+ *       norm separation, group denormalise, inverse rotation `rotated @ Q` in
+ *       fp32), incremental append for decode, the fused decode-attention kernel
+ *       over Lloyd-Max codes, and the bandwidth-bound decode model.
+ *   "omlx/turboquant_kv.py"               -- packed_width = ceil(head_dim*bits/32),
+ *       prod keys pack bits-1 index bits, codecs rebuilt from (head_dim, bits,
+ *       seed) with the value codec on seed+1, append at the written end rather
+ *       than the allocated capacity, refusal to batch caches of mixed (bits,
+ *       seed), state fields of MSE and prod states.
+ *   "turboquant/validate_moe_phase2.py"   -- TurboQuantProd fields (mse_indices,
+ *       qjl_signs, residual_norms, norms; norms in float32), head_dim x head_dim
+ *       fp32 rotation Pi and QJL matrix S, value group quantisation with
+ *       scales and zeros, attention scale 1/sqrt(head_dim), direct scoring of
+ *       queries against compressed keys (attention_score).
+ *
+ * Conventions for every call:
+ *   - Pointers named "device" are CUDA device pointers on the device that was
+ *     current when the codecs were created; "host" pointers are host memory.
+ *   - Calls that take a stream only enqueue work on it (asynchronous, no host
+ *     synchronisation, no allocation); arguments are checked on the host first.
+ *   - Errors are returned as tq_status; nothing is thrown across the ABI.
+ *     Violations that only the GPU can see (a sequence longer than its block
+ *     table, a block id outside the pool) skip the offending access and set
+ *     bits in a per-device error word read by tq_device_error().
+ *   - Shapes are row-major and contiguous.
+ */
+#ifndef TQ_H
+#define TQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define TQ_ABI_VERSION 1
+
+/* A cudaStream_t; 0 is the legacy default stream. */
+typedef struct CUstream_st *tq_stream_t;
+
+typedef enum { TQ_MODE_MSE = 0, TQ_MODE_PROD = 1, TQ_MODE_GROUP = 2 } tq_mode;
+typedef enum { TQ_F32 = 0, TQ_BF16 = 1, TQ_F16 = 2 } tq_dtype;
+
+typedef enum {
+    TQ_OK = 0,
+    TQ_ERR_INVALID_ARG = 1,     /* null pointer, negative size, misaligned buffer  */
+    TQ_ERR_UNSUPPORTED = 2,     /* head_dim/bits/mode combination not built         */
+    TQ_ERR_CONFIG_MISMATCH = 3, /* codec does not match the cache descriptor         */
+    TQ_ERR_CAPACITY = 4,        /* pool or workspace too small for the request       */
+    TQ_ERR_OOM = 5,             /* codec table allocation failed                      */
+    TQ_ERR_CUDA = 6,            /* a CUDA runtime call or kernel launch failed        */
+    TQ_ERR_DEVICE_BOUNDS = 7    /* reported by tq_device_error: GPU saw a bad index   */
+} tq_status;
+
+/* Device error bits (tq_device_error). */
+#define TQ_DEVERR_CAPACITY 1u   /* append past a sequence's block-table capacity */
+#define TQ_DEVERR_BLOCK 2u      /* block id outside [0, num_blocks)              */
+#define TQ_DEVERR_SEQLEN 4u     /* decode seq_len outside [q_len, capacity]      */
+
+/* ------------------------------------------------------------------ */
+/* Codecs                                                               */
+/* ------------------------------------------------------------------ */
+
+typedef struct tq_codec tq_codec; /* opaque; immutable after creation */
+
+typedef struct {
+    int head_dim;
+    int bits;          /* total bits per coordinate (prod: MSE bits + 1)      */
+    int mode;          /* tq_mode                                              */
+    int group_size;    /* group mode only                                      */
+    uint64_t seed;
+    int index_bits;    /* bits per packed index: bits, or bits-1 for prod      */
+    int index_words;   /* packed_width = ceil(head_dim * index_bits / 32)      */
+    int sign_words;    /* prod: head_dim/32 QJL sign words, else 0             */
+    int record_bytes;  /* bytes stored per token for this codec                */
+    int device;        /* CUDA device holding the tables                       */
+} tq_codec_info_t;
+
+/*
+ * Build an MSE or prod codec from (head_dim, bits, seed) alone, as the codec
+ * rebuild of "omlx/turboquant_kv.py" (_rebuild_codecs) requires:
+ *   rotation R (head_dim x head_dim, fp32): Q factor with positive diagonal of
+ *     the QR factorisation of a seeded Gaussian matrix (SplitMix64 stream
+ *     2*seed, Box-Muller normals, Householder QR in fp64), y = R x;
+ *   QJL matrix S (prod only, fp32): i.i.d. N(0,1), stream 2*seed+1;
+ *   codebook: 2^index_bits Lloyd-Max levels for the density of one coordinate
+ *     of a uniform unit vector in R^head_dim, (1-t^2)^((head_dim-3)/2), with
+ *     the midpoints between levels as decision thresholds.
+ * head_dim in {64, 128, 256}; MSE bits 1..4; prod bits 2..5. The tables live
+ * on the current CUDA device (plus a host copy). Returns TQ_ERR_UNSUPPORTED
+ * for other values. *out receives a codec owned by the caller
+ * (tq_codec_destroy). Thread-safe.
+ */
+tq_status tq_codec_create(int head_dim, int bits, tq_mode mode, uint64_t seed, tq_codec **out);
+
+/*
+ * Group codec ("turboquant/validate_moe_phase2.py", quantize_values): per
+ * group of group_size consecutive coordinates an fp16 scale
+ * (max-min)/(2^bits-1) and an fp16 minimum; codes round((x-min)/scale)
+ * clamped to [0, 2^bits-1]; no rotation. bits in {2, 4}; group_size in
+ * {32, 64, 128} dividing head_dim.
+ */
+tq_status tq_codec_create_group(int head_dim, int bits, int group_size, tq_codec **out);
+
+void tq_codec_destroy(tq_codec *codec);
+tq_status tq_codec_info(const tq_codec *codec, tq_codec_info_t *out);
+
+/*
+ * Build the fp32 tables of an MSE or prod codec on the host only, without a
+ * CUDA device (the same construction as tq_codec_create): R and S are
+ * head_dim*head_dim row-major (S only for prod, may be NULL), centroids
+ * 2^index_bits, midpoints 2^index_bits - 1. Lets a table be reproduced and
+ * inspected offline.
+ */
+tq_status tq_codec_build_host(int head_dim, int bits, tq_mode mode, uint64_t seed, float *rotation,
+                              float *qjl, float *centroids, float *midpoints);
+
+/* Host copies of the fp32 tables. Any pointer may be NULL. R and S are
+ * head_dim*head_dim row-major; centroids 2^index_bits; midpoints
+ * 2^index_bits - 1. Group codecs have no tables (TQ_ERR_INVALID_ARG). */
+tq_status tq_codec_export(const tq_codec *codec, float *rotation, float *qjl, float *centroids,
+                          float *midpoints);
+
+/* ------------------------------------------------------------------ */
+/* Cache layout                                                         */
+/* ------------------------------------------------------------------ */
+
+/*
+ * Paged compressed cache. Each layer owns a pool of num_blocks blocks; a
+ * block holds block_tokens consecutive tokens of one sequence for every KV
+ * head. The (block p, head h) sub-block starts at byte
+ *     (p * num_kv_heads + h) * subblock_bytes
+ * of the layer pool and stores its streams one after another, each
+ * token-major: key indices [BT][index_words] u32, key QJL signs
+ * [BT][head_dim/32] u32 (prod), key norms [BT] f32, key residual norms [BT]
+ * f32 (prod), value indices [BT][index_words] u32, then value norms [BT] f32
+ * (MSE) or value scales and minima [BT][head_dim/group] f16 (group).
+ * A contiguous cache is the special case of one sequence whose block table
+ * is the identity (or NULL, see below).
+ */
+typedef struct {
+    void *pool;              /* device, 16-byte aligned: pool of layer 0             */
+    int64_t layer_stride;    /* bytes between consecutive layer pools               */
+    int num_layers;
+    int num_blocks;          /* physical blocks per layer pool                      */
+    int block_tokens;        /* power of two, 16..65536                             */
+    int num_kv_heads;
+    int head_dim;
+    int key_mode, key_bits;
+    uint64_t key_seed;
+    int value_mode, value_bits, value_group;
+    uint64_t value_seed;
+    int64_t subblock_bytes;  /* block_tokens * (key + value record bytes)           */
+    int64_t stream_offset[7];/* byte offsets of the streams in a sub-block (-1 = none):
+                                key idx, key signs, key norm, key rnorm,
+                                value idx, value norm | value scale, value min     */
+} tq_cache_desc;
+
+/*
+ * Fill *desc for a pool of num_layers layers laid out back to back
+ * (layer_stride = num_blocks * num_kv_heads * subblock_bytes). If pool_bytes
+ * is smaller than that total, returns TQ_ERR_CAPACITY. pool may be NULL to
+ * query sizes only (pool_bytes is then ignored); *required_bytes (optional)
+ * receives the total.
+ */
+tq_status tq_cache_desc_init(tq_cache_desc *desc, const tq_codec *key_codec,
+                             const tq_codec *value_codec, int num_layers, int num_blocks,
+                             int block_tokens, int num_kv_heads, void *pool, size_t pool_bytes,
+                             size_t *required_bytes);
+
+/* ------------------------------------------------------------------ */
+/* Encode                                                               */
+/* ------------------------------------------------------------------ */
+
+/*
+ * Append n_new tokens per sequence to layer `layer` of the cache: compress
+ * keys with key_codec and values with value_codec and write them at
+ * positions seq_lens[b] .. seq_lens[b]+n_new-1 -- the written end of each
+ * sequence, never the allocated capacity ("omlx/turboquant_kv.py",
+ * BatchTurboQuantKVCache._phys_end) -- incremental per-token append as
+ * "lightning-mlx/plan.md" asks of update_and_fetch.
+ *   k, v        device [batch][num_kv_heads][n_new][head_dim], dtype f32/bf16/f16
+ *   seq_lens    device int32 [batch], tokens already cached (not modified)
+ *   block_table device int32 [batch][max_blocks] of physical block ids, or NULL:
+ *               then sequence b owns blocks b*max_blocks .. b*max_blocks+max_blocks-1
+ * Encoding is bit-exact with the fp32 specification (sequential fused
+ * multiply-adds, IEEE division and square root): norm = sqrt(sum x_k^2),
+ * y = (R x)/norm, index_i = #{midpoints < y_i}; prod residual r = y - c[index],
+ * rnorm = |r|, sign_j = ((S r)_j >= 0). Tokens past a sequence's capacity
+ * are skipped and flagged (TQ_DEVERR_CAPACITY).
+ * Errors: TQ_ERR_CONFIG_MISMATCH if a codec's (head_dim, bits, mode, seed,
+ * group) differs from the descriptor (the mixed-config guard of
+ * BatchTurboQuantKVCache.merge); TQ_ERR_CAPACITY if n_new exceeds
+ * max_blocks*block_tokens; TQ_ERR_INVALID_ARG for bad pointers or sizes.
+ */
+tq_status tq_encode_append(const tq_codec *key_codec, const tq_codec *value_codec,
+                           const tq_cache_desc *cache, int layer, const void *k, const void *v,
+                           tq_dtype dtype, int batch, int n_new, const int32_t *seq_lens,
+                           const int32_t *block_table, int max_blocks, tq_stream_t stream);
+
+/*
+ * Codec-only quantise of n vectors x (device [n][head_dim]) into plain record
+ * arrays (the codec's quantize): idx [n][index_words] u32; for MSE norm [n]
+ * f32; for prod also signs [n][head_dim/32] u32 and rnorm [n] f32; for group
+ * scale and min [n][head_dim/group] f16 (passed in aux0/aux1). Unused
+ * outputs may be NULL. Same arithmetic as tq_encode_append.
+ *   mse : aux0 = norm,  aux1 = unused, aux2 = unused
+ *   prod: aux0 = norm,  aux1 = signs,  aux2 = rnorm
+ *   group: aux0 = scale, aux1 = min,   aux2 = unused
+ */
+tq_status tq_quantize(const tq_codec *codec, const void *x, tq_dtype dtype, int64_t n,
+                      uint32_t *idx, void *aux0, void *aux1, void *aux2, tq_stream_t stream);
+
+/* ------------------------------------------------------------------ */
+/* Decode attention                                                     */
+/* ------------------------------------------------------------------ */
+
+/* Workspace (device bytes) tq_decode_attention needs for these sizes. */
+tq_status tq_decode_workspace_bytes(const tq_cache_desc *cache, int batch, int num_q_heads,
+                                    int q_len, int max_seq_len, size_t *bytes);
+
+/*
+ * Decode attention over layer `layer` of the compressed cache
+ * ("lightning-mlx/plan.md": fused attention over Lloyd-Max codes;
+ * "turboquant/validate_moe_phase2.py": attention_score scores queries against
+ * compressed keys). For every sequence b, query head hq (KV head
+ * hq / (num_q_heads/num_kv_heads)) and query position l < q_len:
+ *   q' = R_k q, q'' = S_k q' (once per query);
+ *   score_t = scale * n_t * (<q', c_k[idx_t]> + sqrt(pi/2)/D * rnorm_t <q'', sign_t>)
+ *             (the second term for prod keys only), for keys t <= N - q_len + l
+ *             where N = seq_lens[b] (the q_len query tokens are the newest,
+ *             already appended);
+ *   out = softmax(score) . V, with MSE values accumulated in the rotated domain
+ *         as n^v_t c_v[idx^v_t] and rotated back once (x = (sum) @ R_v), group
+ *         values as code*scale+min.
+ *   q    device [batch][num_q_heads][q_len][head_dim], f32/bf16/f16
+ *   out  device [batch][num_q_heads][q_len][head_dim] f32
+ *   seq_lens device int32 [batch] in [q_len, capacity]; max_seq_len (host) must
+ *        bound every seq_lens[b]; it sizes the split-K grid.
+ *   scale 0 means 1/sqrt(head_dim).
+ *   workspace device, >= tq_decode_workspace_bytes(...), 256-byte aligned;
+ *        only this call uses it while it runs (calls that overlap on the GPU
+ *        must use distinct workspaces).
+ * (num_q_heads/num_kv_heads) * q_len <= 64.
+ */
+tq_status tq_decode_attention(const tq_codec *key_codec, const tq_codec *value_codec,
+                              const tq_cache_desc *cache, int layer, const void *q,
+                              tq_dtype q_dtype, int batch, int num_q_heads, int q_len,
+                              const int32_t *seq_lens, const int32_t *block_table, int max_blocks,
+                              int max_seq_len, float scale, float *out, void *workspace,
+                              size_t workspace_bytes, tq_stream_t stream);
+
+/* ------------------------------------------------------------------ */
+/* Diagnostics                                                          */
+/* ------------------------------------------------------------------ */
+
+const char *tq_status_string(tq_status status);
+/* Synchronises the current device, returns its error word in *flags and
+ * clears it. Returns TQ_ERR_DEVICE_BOUNDS if any bit was set. */
+tq_status tq_device_error(uint32_t *flags);
+/* Number of kernels this library has launched since it was loaded. */
+uint64_t tq_launch_count(void);
+int tq_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* TQ_H */

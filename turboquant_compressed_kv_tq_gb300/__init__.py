@@ -1,0 +1,231 @@
+"""GB300 TurboQuant compressed KV cache: Python binding of libtq.so.
+
+The functions below carry the names of the C ABI (include/tq.h) and only
+marshal arguments: tensors become device pointers, the current torch stream
+becomes the cudaStream_t. Every step of encode and decode runs in the
+library's CUDA kernels. PyTorch provides device memory and streams.
+"""
+from __future__ import annotations
+
+import ctypes
+from typing import Optional
+
+import numpy as np
+
+from ._lib import (TQ_BF16, TQ_DEVERR_BLOCK, TQ_DEVERR_CAPACITY, TQ_DEVERR_SEQLEN, TQ_F16,
+                   TQ_F32, TQ_MODE_GROUP, TQ_MODE_MSE, TQ_MODE_PROD, TQ_OK, TQError, check,
+                   lib, library_path, status_string, tq_cache_desc, tq_codec_info_t)
+
+__all__ = [
+    "tq_codec_create", "tq_codec_create_group", "tq_codec_destroy", "tq_codec_info",
+    "tq_codec_build_host", "tq_codec_export", "tq_cache_desc_init", "tq_encode_append",
+    "tq_quantize", "tq_decode_workspace_bytes", "tq_decode_attention", "tq_device_error",
+    "tq_launch_count", "tq_abi_version", "Codec", "CompressedKVCache", "TQError",
+    "TQ_MODE_MSE", "TQ_MODE_PROD", "TQ_MODE_GROUP", "TQ_F32", "TQ_BF16", "TQ_F16",
+]
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _dtype_code(t) -> int:
+    torch = _torch()
+    if t.dtype == torch.float32:
+        return TQ_F32
+    if t.dtype == torch.bfloat16:
+        return TQ_BF16
+    if t.dtype == torch.float16:
+        return TQ_F16
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def _ptr(t) -> Optional[int]:
+    if t is None:
+        return None
+    if not t.is_contiguous():
+        raise ValueError("tensor must be contiguous")
+    return t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        return _torch().cuda.current_stream().cuda_stream
+    return stream if isinstance(stream, int) else stream.cuda_stream
+
+
+# ----------------------------------------------------------------- raw ABI
+
+def tq_abi_version() -> int:
+    return lib().tq_abi_version()
+
+
+def tq_launch_count() -> int:
+    return int(lib().tq_launch_count())
+
+
+def tq_codec_create(head_dim: int, bits: int, mode: int, seed: int) -> int:
+    h = ctypes.c_void_p()
+    check(lib().tq_codec_create(head_dim, bits, mode, seed, ctypes.byref(h)), "tq_codec_create")
+    return h.value
+
+
+def tq_codec_create_group(head_dim: int, bits: int, group_size: int) -> int:
+    h = ctypes.c_void_p()
+    check(lib().tq_codec_create_group(head_dim, bits, group_size, ctypes.byref(h)),
+          "tq_codec_create_group")
+    return h.value
+
+
+def tq_codec_destroy(handle: int) -> None:
+    lib().tq_codec_destroy(handle)
+
+
+def tq_codec_info(handle: int) -> dict:
+    info = tq_codec_info_t()
+    check(lib().tq_codec_info(handle, ctypes.byref(info)), "tq_codec_info")
+    return {k: getattr(info, k) for k, _ in info._fields_}
+
+
+def _tables(D: int, ib: int, with_s: bool):
+    R = np.empty((D, D), np.float32)
+    S = np.empty((D, D), np.float32) if with_s else None
+    c = np.empty(1 << ib, np.float32)
+    m = np.empty((1 << ib) - 1, np.float32)
+    return R, S, c, m
+
+
+def _np_ptr(a):
+    return None if a is None else a.ctypes.data
+
+
+def tq_codec_build_host(head_dim: int, bits: int, mode: int, seed: int):
+    ib = bits - 1 if mode == TQ_MODE_PROD else bits
+    R, S, c, m = _tables(head_dim, ib, mode == TQ_MODE_PROD)
+    check(lib().tq_codec_build_host(head_dim, bits, mode, seed, _np_ptr(R), _np_ptr(S), _np_ptr(c),
+                                    _np_ptr(m)), "tq_codec_build_host")
+    return R, S, c, m
+
+
+def tq_codec_export(handle: int):
+    info = tq_codec_info(handle)
+    R, S, c, m = _tables(info["head_dim"], info["index_bits"], info["mode"] == TQ_MODE_PROD)
+    check(lib().tq_codec_export(handle, _np_ptr(R), _np_ptr(S), _np_ptr(c), _np_ptr(m)),
+          "tq_codec_export")
+    return R, S, c, m
+
+
+def tq_cache_desc_init(key_codec: int, value_codec: int, num_layers: int, num_blocks: int,
+                       block_tokens: int, num_kv_heads: int, pool=None):
+    """Returns (desc, required_bytes). ``pool`` is a device tensor or None."""
+    d = tq_cache_desc()
+    req = ctypes.c_size_t()
+    ptr = None if pool is None else pool.data_ptr()
+    nbytes = 0 if pool is None else pool.numel() * pool.element_size()
+    check(lib().tq_cache_desc_init(ctypes.byref(d), key_codec, value_codec, num_layers, num_blocks,
+                                   block_tokens, num_kv_heads, ptr, nbytes, ctypes.byref(req)),
+          "tq_cache_desc_init")
+    return d, req.value
+
+
+def tq_encode_append(key_codec: int, value_codec: int, desc: tq_cache_desc, layer: int, k, v,
+                     seq_lens, block_table=None, max_blocks: int = 0, stream=None) -> None:
+    batch, _, n_new, _ = k.shape
+    check(lib().tq_encode_append(key_codec, value_codec, ctypes.byref(desc), layer, _ptr(k), _ptr(v),
+                                 _dtype_code(k), batch, n_new, _ptr(seq_lens), _ptr(block_table),
+                                 max_blocks, _stream(stream)), "tq_encode_append")
+
+
+def tq_quantize(codec: int, x, idx, aux0=None, aux1=None, aux2=None, stream=None) -> None:
+    n = x.shape[0]
+    check(lib().tq_quantize(codec, _ptr(x), _dtype_code(x), n, _ptr(idx), _ptr(aux0), _ptr(aux1),
+                            _ptr(aux2), _stream(stream)), "tq_quantize")
+
+
+def tq_decode_workspace_bytes(desc: tq_cache_desc, batch: int, num_q_heads: int, q_len: int,
+                              max_seq_len: int) -> int:
+    out = ctypes.c_size_t()
+    check(lib().tq_decode_workspace_bytes(ctypes.byref(desc), batch, num_q_heads, q_len, max_seq_len,
+                                          ctypes.byref(out)), "tq_decode_workspace_bytes")
+    return out.value
+
+
+def tq_decode_attention(key_codec: int, value_codec: int, desc: tq_cache_desc, layer: int, q,
+                        seq_lens, block_table, max_blocks: int, max_seq_len: int, out, workspace,
+                        scale: float = 0.0, stream=None) -> None:
+    batch, hq, lq, _ = q.shape
+    ws_bytes = workspace.numel() * workspace.element_size()
+    check(lib().tq_decode_attention(key_codec, value_codec, ctypes.byref(desc), layer, _ptr(q),
+                                    _dtype_code(q), batch, hq, lq, _ptr(seq_lens), _ptr(block_table),
+                                    max_blocks, max_seq_len, scale, _ptr(out), _ptr(workspace),
+                                    ws_bytes, _stream(stream)), "tq_decode_attention")
+
+
+def tq_device_error() -> int:
+    flags = ctypes.c_uint32()
+    st = lib().tq_device_error(ctypes.byref(flags))
+    if st not in (TQ_OK, 7):
+        check(st, "tq_device_error")
+    return flags.value
+
+
+# ----------------------------------------------------------------- helpers
+
+class Codec:
+    """Owns one codec handle."""
+
+    def __init__(self, head_dim: int, bits: int, mode: int, seed: int = 0, group: int = 0):
+        if mode == TQ_MODE_GROUP:
+            self.handle = tq_codec_create_group(head_dim, bits, group)
+        else:
+            self.handle = tq_codec_create(head_dim, bits, mode, seed)
+        self.info = tq_codec_info(self.handle)
+
+    def __del__(self):
+        h = getattr(self, "handle", None)
+        if h:
+            try:
+                tq_codec_destroy(h)
+            except Exception:
+                pass
+            self.handle = None
+
+    @property
+    def record_bytes(self) -> int:
+        return self.info["record_bytes"]
+
+    def export(self):
+        return tq_codec_export(self.handle)
+
+
+class CompressedKVCache:
+    """A device pool plus its descriptor (all layers), allocated through torch."""
+
+    def __init__(self, key: Codec, value: Codec, num_layers: int, num_blocks: int,
+                 block_tokens: int, num_kv_heads: int, device="cuda"):
+        torch = _torch()
+        self.key, self.value = key, value
+        _, req = tq_cache_desc_init(key.handle, value.handle, num_layers, num_blocks, block_tokens,
+                                    num_kv_heads, None)
+        self.pool = torch.zeros(req, dtype=torch.uint8, device=device)
+        self.desc, _ = tq_cache_desc_init(key.handle, value.handle, num_layers, num_blocks,
+                                          block_tokens, num_kv_heads, self.pool)
+        self.num_layers, self.num_blocks = num_layers, num_blocks
+        self.block_tokens, self.num_kv_heads = block_tokens, num_kv_heads
+
+    @property
+    def nbytes(self) -> int:
+        return self.pool.numel()
+
+    def append(self, layer, k, v, seq_lens, block_table=None, max_blocks=0, stream=None):
+        tq_encode_append(self.key.handle, self.value.handle, self.desc, layer, k, v, seq_lens,
+                         block_table, max_blocks, stream)
+
+    def workspace_bytes(self, batch, num_q_heads, q_len, max_seq_len):
+        return tq_decode_workspace_bytes(self.desc, batch, num_q_heads, q_len, max_seq_len)
+
+    def decode(self, layer, q, seq_lens, block_table, max_blocks, max_seq_len, out, workspace,
+               scale=0.0, stream=None):
+        tq_decode_attention(self.key.handle, self.value.handle, self.desc, layer, q, seq_lens,
+                            block_table, max_blocks, max_seq_len, out, workspace, scale, stream)

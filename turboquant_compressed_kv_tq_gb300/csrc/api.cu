@@ -1,0 +1,452 @@
+// C ABI of libtq: codec lifetime, cache layout, argument checks and launches.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+#include <mutex>
+#include <new>
+
+#include "tq_internal.h"
+
+namespace tq {
+
+std::atomic<uint64_t> g_launches{0};
+
+namespace {
+
+// Per-device error word written by the kernels (see tq_device_error).
+__device__ unsigned int g_device_error;
+
+constexpr int kMaxDevices = 64;
+unsigned* g_err_ptr[kMaxDevices] = {};
+int g_num_sms[kMaxDevices] = {};
+std::mutex g_dev_mu;
+
+tq_status device_state(unsigned** err, int* num_sms) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return TQ_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    if (!g_err_ptr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return TQ_ERR_CUDA;
+        int sms = 0;
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return TQ_ERR_CUDA;
+        g_err_ptr[dev] = static_cast<unsigned*>(p);
+        g_num_sms[dev] = sms;
+    }
+    if (err) *err = g_err_ptr[dev];
+    if (num_sms) *num_sms = g_num_sms[dev];
+    return TQ_OK;
+}
+
+int index_bits_of(int bits, int mode) { return mode == TQ_MODE_PROD ? bits - 1 : bits; }
+
+int record_bytes_of(int D, int bits, int mode, int group) {
+    const int w = (D * index_bits_of(bits, mode) + 31) / 32;
+    if (mode == TQ_MODE_MSE) return 4 * w + 4;
+    if (mode == TQ_MODE_PROD) return 4 * w + 4 * (D / 32) + 8;
+    return 4 * w + 4 * (D / group);
+}
+
+bool head_dim_ok(int D) { return D == 64 || D == 128 || D == 256; }
+
+void free_codec(tq_codec* c) {
+    if (!c) return;
+    int prev = -1;
+    cudaGetDevice(&prev);
+    if (c->device >= 0) cudaSetDevice(c->device);
+    cudaFree(c->d_R);
+    cudaFree(c->d_Rt);
+    cudaFree(c->d_St);
+    cudaFree(c->d_c);
+    cudaFree(c->d_m);
+    if (prev >= 0) cudaSetDevice(prev);
+    delete c;
+}
+
+template <typename T>
+tq_status upload(T** dst, const std::vector<T>& src) {
+    if (src.empty()) return TQ_OK;
+    if (cudaMalloc(reinterpret_cast<void**>(dst), src.size() * sizeof(T)) != cudaSuccess) return TQ_ERR_OOM;
+    if (cudaMemcpy(*dst, src.data(), src.size() * sizeof(T), cudaMemcpyHostToDevice) != cudaSuccess)
+        return TQ_ERR_CUDA;
+    return TQ_OK;
+}
+
+std::vector<float> transpose(const std::vector<float>& a, int D) {
+    std::vector<float> t(a.size());
+    for (int i = 0; i < D; ++i)
+        for (int k = 0; k < D; ++k) t[static_cast<size_t>(k) * D + i] = a[static_cast<size_t>(i) * D + k];
+    return t;
+}
+
+CodecDev dev_view(const tq_codec* c) {
+    CodecDev d{};
+    d.R = c->d_R;
+    d.Rt = c->d_Rt;
+    d.St = c->d_St;
+    d.c = c->d_c;
+    d.m = c->d_m;
+    d.D = c->head_dim;
+    d.mode = c->mode;
+    d.bits = c->bits;
+    d.ib = c->index_bits;
+    d.W = c->index_words;
+    d.Ws = c->sign_words;
+    d.group = c->group;
+    return d;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+tq_status check_codecs_vs_cache(const tq_codec* kc, const tq_codec* vc, const tq_cache_desc* d) {
+    if (!kc || !vc || !d) return TQ_ERR_INVALID_ARG;
+    if (kc->mode == TQ_MODE_GROUP || vc->mode == TQ_MODE_PROD) return TQ_ERR_UNSUPPORTED;
+    if (kc->head_dim != d->head_dim || vc->head_dim != d->head_dim) return TQ_ERR_CONFIG_MISMATCH;
+    if (kc->mode != d->key_mode || kc->bits != d->key_bits || kc->seed != d->key_seed)
+        return TQ_ERR_CONFIG_MISMATCH;
+    if (vc->mode != d->value_mode || vc->bits != d->value_bits) return TQ_ERR_CONFIG_MISMATCH;
+    if (vc->mode == TQ_MODE_GROUP ? vc->group != d->value_group : vc->seed != d->value_seed)
+        return TQ_ERR_CONFIG_MISMATCH;
+    if (!d->pool || !aligned16(d->pool) || d->num_blocks <= 0 || d->num_kv_heads <= 0) return TQ_ERR_INVALID_ARG;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return TQ_ERR_CUDA;
+    if (kc->device != dev || vc->device != dev) return TQ_ERR_INVALID_ARG;
+    return TQ_OK;
+}
+
+PoolDev pool_view(const tq_cache_desc* d, int layer) {
+    PoolDev p{};
+    p.base = static_cast<char*>(d->pool) + d->layer_stride * layer;
+    p.sub_bytes = d->subblock_bytes;
+    for (int i = 0; i < 7; ++i) p.off[i] = d->stream_offset[i];
+    p.Hkv = d->num_kv_heads;
+    p.BT = d->block_tokens;
+    p.num_blocks = d->num_blocks;
+    return p;
+}
+
+}  // namespace
+}  // namespace tq
+
+using namespace tq;
+
+extern "C" {
+
+int tq_abi_version(void) { return TQ_ABI_VERSION; }
+
+uint64_t tq_launch_count(void) { return g_launches.load(); }
+
+const char* tq_status_string(tq_status s) {
+    switch (s) {
+        case TQ_OK: return "ok";
+        case TQ_ERR_INVALID_ARG: return "invalid argument";
+        case TQ_ERR_UNSUPPORTED: return "unsupported head_dim/bits/mode";
+        case TQ_ERR_CONFIG_MISMATCH: return "codec does not match the cache descriptor";
+        case TQ_ERR_CAPACITY: return "capacity exceeded";
+        case TQ_ERR_OOM: return "out of device memory";
+        case TQ_ERR_CUDA: return "CUDA error";
+        case TQ_ERR_DEVICE_BOUNDS: return "device reported an out-of-range index";
+    }
+    return "unknown status";
+}
+
+tq_status tq_codec_create(int head_dim, int bits, tq_mode mode, uint64_t seed, tq_codec** out) {
+    if (!out) return TQ_ERR_INVALID_ARG;
+    *out = nullptr;
+    if (!head_dim_ok(head_dim)) return TQ_ERR_UNSUPPORTED;
+    if (mode == TQ_MODE_MSE) {
+        if (bits < 1 || bits > 4) return TQ_ERR_UNSUPPORTED;
+    } else if (mode == TQ_MODE_PROD) {
+        if (bits < 2 || bits > 5) return TQ_ERR_UNSUPPORTED;
+    } else {
+        return TQ_ERR_UNSUPPORTED;
+    }
+    tq_codec* c = new (std::nothrow) tq_codec();
+    if (!c) return TQ_ERR_OOM;
+    c->head_dim = head_dim;
+    c->bits = bits;
+    c->mode = mode;
+    c->seed = seed;
+    c->index_bits = index_bits_of(bits, mode);
+    c->index_words = (head_dim * c->index_bits + 31) / 32;
+    c->sign_words = mode == TQ_MODE_PROD ? head_dim / 32 : 0;
+    c->record_bytes = record_bytes_of(head_dim, bits, mode, 0);
+    if (cudaGetDevice(&c->device) != cudaSuccess) {
+        delete c;
+        return TQ_ERR_CUDA;
+    }
+    build_codec_tables(head_dim, c->index_bits, mode == TQ_MODE_PROD, seed, c->host);
+    tq_status st = upload(&c->d_R, c->host.rotation);
+    if (st == TQ_OK) st = upload(&c->d_Rt, transpose(c->host.rotation, head_dim));
+    if (st == TQ_OK && mode == TQ_MODE_PROD) st = upload(&c->d_St, transpose(c->host.qjl, head_dim));
+    if (st == TQ_OK) st = upload(&c->d_c, c->host.centroids);
+    if (st == TQ_OK) st = upload(&c->d_m, c->host.midpoints);
+    if (st == TQ_OK && device_state(nullptr, nullptr) != TQ_OK) st = TQ_ERR_CUDA;
+    if (st != TQ_OK) {
+        free_codec(c);
+        return st;
+    }
+    *out = c;
+    return TQ_OK;
+}
+
+tq_status tq_codec_create_group(int head_dim, int bits, int group_size, tq_codec** out) {
+    if (!out) return TQ_ERR_INVALID_ARG;
+    *out = nullptr;
+    if (!head_dim_ok(head_dim)) return TQ_ERR_UNSUPPORTED;
+    if (bits != 2 && bits != 4) return TQ_ERR_UNSUPPORTED;
+    if (group_size != 32 && group_size != 64 && group_size != 128) return TQ_ERR_UNSUPPORTED;
+    if (head_dim % group_size != 0) return TQ_ERR_UNSUPPORTED;
+    tq_codec* c = new (std::nothrow) tq_codec();
+    if (!c) return TQ_ERR_OOM;
+    c->head_dim = head_dim;
+    c->bits = bits;
+    c->mode = TQ_MODE_GROUP;
+    c->group = group_size;
+    c->index_bits = bits;
+    c->index_words = (head_dim * bits + 31) / 32;
+    c->record_bytes = record_bytes_of(head_dim, bits, TQ_MODE_GROUP, group_size);
+    if (cudaGetDevice(&c->device) != cudaSuccess || device_state(nullptr, nullptr) != TQ_OK) {
+        delete c;
+        return TQ_ERR_CUDA;
+    }
+    *out = c;
+    return TQ_OK;
+}
+
+void tq_codec_destroy(tq_codec* codec) { free_codec(codec); }
+
+tq_status tq_codec_info(const tq_codec* c, tq_codec_info_t* out) {
+    if (!c || !out) return TQ_ERR_INVALID_ARG;
+    out->head_dim = c->head_dim;
+    out->bits = c->bits;
+    out->mode = c->mode;
+    out->group_size = c->group;
+    out->seed = c->seed;
+    out->index_bits = c->index_bits;
+    out->index_words = c->index_words;
+    out->sign_words = c->sign_words;
+    out->record_bytes = c->record_bytes;
+    out->device = c->device;
+    return TQ_OK;
+}
+
+tq_status tq_codec_build_host(int head_dim, int bits, tq_mode mode, uint64_t seed, float* rotation, float* qjl,
+                              float* centroids, float* midpoints) {
+    if (!head_dim_ok(head_dim)) return TQ_ERR_UNSUPPORTED;
+    if (mode == TQ_MODE_MSE ? (bits < 1 || bits > 4) : mode == TQ_MODE_PROD ? (bits < 2 || bits > 5) : true)
+        return TQ_ERR_UNSUPPORTED;
+    HostTables t;
+    build_codec_tables(head_dim, index_bits_of(bits, mode), mode == TQ_MODE_PROD, seed, t);
+    if (rotation) std::memcpy(rotation, t.rotation.data(), t.rotation.size() * sizeof(float));
+    if (qjl && !t.qjl.empty()) std::memcpy(qjl, t.qjl.data(), t.qjl.size() * sizeof(float));
+    if (centroids) std::memcpy(centroids, t.centroids.data(), t.centroids.size() * sizeof(float));
+    if (midpoints) std::memcpy(midpoints, t.midpoints.data(), t.midpoints.size() * sizeof(float));
+    return TQ_OK;
+}
+
+tq_status tq_codec_export(const tq_codec* c, float* rotation, float* qjl, float* centroids, float* midpoints) {
+    if (!c || c->mode == TQ_MODE_GROUP) return TQ_ERR_INVALID_ARG;
+    const auto& h = c->host;
+    if (rotation) std::memcpy(rotation, h.rotation.data(), h.rotation.size() * sizeof(float));
+    if (qjl) {
+        if (h.qjl.empty()) return TQ_ERR_INVALID_ARG;
+        std::memcpy(qjl, h.qjl.data(), h.qjl.size() * sizeof(float));
+    }
+    if (centroids) std::memcpy(centroids, h.centroids.data(), h.centroids.size() * sizeof(float));
+    if (midpoints) std::memcpy(midpoints, h.midpoints.data(), h.midpoints.size() * sizeof(float));
+    return TQ_OK;
+}
+
+tq_status tq_cache_desc_init(tq_cache_desc* d, const tq_codec* kc, const tq_codec* vc, int num_layers,
+                             int num_blocks, int block_tokens, int num_kv_heads, void* pool,
+                             size_t pool_bytes, size_t* required_bytes) {
+    if (!d || !kc || !vc) return TQ_ERR_INVALID_ARG;
+    if (kc->head_dim != vc->head_dim) return TQ_ERR_CONFIG_MISMATCH;
+    if (kc->mode == TQ_MODE_GROUP || vc->mode == TQ_MODE_PROD) return TQ_ERR_UNSUPPORTED;
+    if (num_layers <= 0 || num_blocks <= 0 || num_kv_heads <= 0) return TQ_ERR_INVALID_ARG;
+    if (block_tokens < 16 || block_tokens > 65536 || (block_tokens & (block_tokens - 1)) != 0)
+        return TQ_ERR_INVALID_ARG;
+    if (pool && !aligned16(pool)) return TQ_ERR_INVALID_ARG;
+    std::memset(d, 0, sizeof(*d));
+    const int D = kc->head_dim;
+    const int64_t BT = block_tokens;
+    int64_t o = 0;
+    for (int i = 0; i < 7; ++i) d->stream_offset[i] = -1;
+    d->stream_offset[0] = o;
+    o += BT * 4 * kc->index_words;
+    if (kc->mode == TQ_MODE_PROD) {
+        d->stream_offset[1] = o;
+        o += BT * 4 * kc->sign_words;
+    }
+    d->stream_offset[2] = o;
+    o += BT * 4;
+    if (kc->mode == TQ_MODE_PROD) {
+        d->stream_offset[3] = o;
+        o += BT * 4;
+    }
+    d->stream_offset[4] = o;
+    o += BT * 4 * vc->index_words;
+    if (vc->mode == TQ_MODE_MSE) {
+        d->stream_offset[5] = o;
+        o += BT * 4;
+    } else {
+        const int64_t ng = D / vc->group;
+        d->stream_offset[5] = o;
+        o += BT * 2 * ng;
+        d->stream_offset[6] = o;
+        o += BT * 2 * ng;
+    }
+    d->subblock_bytes = o;
+    d->layer_stride = o * num_kv_heads * static_cast<int64_t>(num_blocks);
+    d->num_layers = num_layers;
+    d->num_blocks = num_blocks;
+    d->block_tokens = block_tokens;
+    d->num_kv_heads = num_kv_heads;
+    d->head_dim = D;
+    d->key_mode = kc->mode;
+    d->key_bits = kc->bits;
+    d->key_seed = kc->seed;
+    d->value_mode = vc->mode;
+    d->value_bits = vc->bits;
+    d->value_group = vc->group;
+    d->value_seed = vc->seed;
+    d->pool = pool;
+    const size_t total = static_cast<size_t>(d->layer_stride) * num_layers;
+    if (required_bytes) *required_bytes = total;
+    if (pool && pool_bytes < total) return TQ_ERR_CAPACITY;
+    return TQ_OK;
+}
+
+tq_status tq_encode_append(const tq_codec* kc, const tq_codec* vc, const tq_cache_desc* cache, int layer,
+                           const void* k, const void* v, tq_dtype dtype, int batch, int n_new,
+                           const int32_t* seq_lens, const int32_t* block_table, int max_blocks,
+                           tq_stream_t stream) {
+    tq_status st = check_codecs_vs_cache(kc, vc, cache);
+    if (st != TQ_OK) return st;
+    if (layer < 0 || layer >= cache->num_layers || batch < 0 || n_new < 0 || max_blocks <= 0)
+        return TQ_ERR_INVALID_ARG;
+    if (dtype != TQ_F32 && dtype != TQ_BF16 && dtype != TQ_F16) return TQ_ERR_INVALID_ARG;
+    if (static_cast<int64_t>(n_new) > static_cast<int64_t>(max_blocks) * cache->block_tokens) return TQ_ERR_CAPACITY;
+    if (!block_table && static_cast<int64_t>(batch) * max_blocks > cache->num_blocks) return TQ_ERR_CAPACITY;
+    if (batch == 0 || n_new == 0) return TQ_OK;
+    if (!k || !v || !seq_lens) return TQ_ERR_INVALID_ARG;
+    if (batch > 32767) return TQ_ERR_INVALID_ARG;
+    unsigned* err = nullptr;
+    if (device_state(&err, nullptr) != TQ_OK) return TQ_ERR_CUDA;
+    EncodeAppendArgs a{};
+    a.kc = dev_view(kc);
+    a.vc = dev_view(vc);
+    a.pool = pool_view(cache, layer);
+    a.k = k;
+    a.v = v;
+    a.dtype = dtype;
+    a.batch = batch;
+    a.n_new = n_new;
+    a.seq_lens = seq_lens;
+    a.table = block_table;
+    a.max_blocks = max_blocks;
+    a.err = err;
+    return launch_encode_append(a, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
+}
+
+tq_status tq_quantize(const tq_codec* c, const void* x, tq_dtype dtype, int64_t n, uint32_t* idx, void* aux0,
+                      void* aux1, void* aux2, tq_stream_t stream) {
+    if (!c || n < 0) return TQ_ERR_INVALID_ARG;
+    if (dtype != TQ_F32 && dtype != TQ_BF16 && dtype != TQ_F16) return TQ_ERR_INVALID_ARG;
+    if (n == 0) return TQ_OK;
+    if (!x) return TQ_ERR_INVALID_ARG;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return TQ_ERR_CUDA;
+    if (dev != c->device) return TQ_ERR_INVALID_ARG;
+    if (n > static_cast<int64_t>(65535) * 65535) return TQ_ERR_INVALID_ARG;
+    QuantizeArgs a{};
+    a.cd = dev_view(c);
+    a.x = x;
+    a.dtype = dtype;
+    a.n = n;
+    a.idx = idx;
+    a.aux0 = aux0;
+    a.aux1 = aux1;
+    a.aux2 = aux2;
+    return launch_quantize(a, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
+}
+
+tq_status tq_decode_workspace_bytes(const tq_cache_desc* cache, int batch, int num_q_heads, int q_len,
+                                    int max_seq_len, size_t* bytes) {
+    if (!cache || !bytes || batch < 0 || q_len <= 0 || max_seq_len < q_len) return TQ_ERR_INVALID_ARG;
+    if (num_q_heads <= 0 || num_q_heads % cache->num_kv_heads != 0) return TQ_ERR_INVALID_ARG;
+    const int G = num_q_heads / cache->num_kv_heads;
+    if (G * q_len > 64) return TQ_ERR_UNSUPPORTED;
+    int sms = 0;
+    if (device_state(nullptr, &sms) != TQ_OK) return TQ_ERR_CUDA;
+    *bytes = make_decode_plan(cache->head_dim, batch, cache->num_kv_heads, G, q_len, max_seq_len, sms).total;
+    return TQ_OK;
+}
+
+tq_status tq_decode_attention(const tq_codec* kc, const tq_codec* vc, const tq_cache_desc* cache, int layer,
+                              const void* q, tq_dtype q_dtype, int batch, int num_q_heads, int q_len,
+                              const int32_t* seq_lens, const int32_t* block_table, int max_blocks,
+                              int max_seq_len, float scale, float* out, void* workspace,
+                              size_t workspace_bytes, tq_stream_t stream) {
+    tq_status st = check_codecs_vs_cache(kc, vc, cache);
+    if (st != TQ_OK) return st;
+    if (layer < 0 || layer >= cache->num_layers || batch < 0 || q_len <= 0 || max_blocks <= 0)
+        return TQ_ERR_INVALID_ARG;
+    if (q_dtype != TQ_F32 && q_dtype != TQ_BF16 && q_dtype != TQ_F16) return TQ_ERR_INVALID_ARG;
+    if (num_q_heads <= 0 || num_q_heads % cache->num_kv_heads != 0) return TQ_ERR_INVALID_ARG;
+    if (max_seq_len < q_len) return TQ_ERR_INVALID_ARG;
+    if (static_cast<int64_t>(max_seq_len) > static_cast<int64_t>(max_blocks) * cache->block_tokens)
+        return TQ_ERR_CAPACITY;
+    if (!block_table && static_cast<int64_t>(batch) * max_blocks > cache->num_blocks) return TQ_ERR_CAPACITY;
+    const int G = num_q_heads / cache->num_kv_heads;
+    if (G * q_len > 64) return TQ_ERR_UNSUPPORTED;
+    if (batch == 0) return TQ_OK;
+    if (batch > 65535) return TQ_ERR_INVALID_ARG;
+    if (!q || !out || !seq_lens || !workspace) return TQ_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return TQ_ERR_INVALID_ARG;
+    unsigned* err = nullptr;
+    int sms = 0;
+    if (device_state(&err, &sms) != TQ_OK) return TQ_ERR_CUDA;
+    const DecodePlan plan = make_decode_plan(cache->head_dim, batch, cache->num_kv_heads, G, q_len, max_seq_len, sms);
+    if (workspace_bytes < plan.total) return TQ_ERR_CAPACITY;
+    DecodeArgs a{};
+    a.kc = dev_view(kc);
+    a.vc = dev_view(vc);
+    a.pool = pool_view(cache, layer);
+    a.q = q;
+    a.q_dtype = q_dtype;
+    a.batch = batch;
+    a.Hq = num_q_heads;
+    a.Lq = q_len;
+    a.G = G;
+    a.seq_lens = seq_lens;
+    a.table = block_table;
+    a.max_blocks = max_blocks;
+    a.scale = scale == 0.0f ? 1.0f / std::sqrt(static_cast<float>(cache->head_dim)) : scale;
+    a.out = out;
+    char* ws = static_cast<char*>(workspace);
+    a.qrot = reinterpret_cast<float*>(ws);
+    a.qjl = reinterpret_cast<float*>(ws + plan.q_bytes);
+    a.part = reinterpret_cast<float*>(ws + 2 * plan.q_bytes);
+    a.ml = reinterpret_cast<float*>(ws + 2 * plan.q_bytes + plan.part_bytes);
+    a.plan = plan;
+    a.err = err;
+    return launch_decode(a, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
+}
+
+tq_status tq_device_error(uint32_t* flags) {
+    unsigned* err = nullptr;
+    if (device_state(&err, nullptr) != TQ_OK) return TQ_ERR_CUDA;
+    if (cudaDeviceSynchronize() != cudaSuccess) return TQ_ERR_CUDA;
+    unsigned v = 0;
+    if (cudaMemcpy(&v, err, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return TQ_ERR_CUDA;
+    const unsigned zero = 0;
+    if (cudaMemcpy(err, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return TQ_ERR_CUDA;
+    if (flags) *flags = v;
+    return v ? TQ_ERR_DEVICE_BOUNDS : TQ_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,358 @@
+// TurboQuant decode attention over the compressed cache.
+//
+// "lightning-mlx/plan.md" asks for a fused attention kernel that works on the
+// Lloyd-Max codes directly instead of dequantising the cache; the validation
+// script of "turboquant/validate_moe_phase2.py" scores queries against
+// compressed keys (attention_score). In the rotated domain, with q' = R_k q
+// and q'' = S_k q',
+//   <q, k_hat_t> = n_t (<q', c[idx_t]> + sqrt(pi/2)/D * rnorm_t <q'', sign_t>)
+// and for MSE values sum_t p_t v_hat_t = (sum_t p_t n_t c_v[idx_t]) @ R_v, so the
+// cache is never rotated back: the query is rotated once and the output once.
+//
+// Three kernels per call:
+//   qprep  : q' (and q'' for prod keys) for every query row, fp32;
+//   split  : one CTA per (token split, kv head x row group, sequence) runs an
+//            online softmax over its tokens and writes (max, sum, acc[D]);
+//   merge  : log-sum-exp merge of the splits, 1/sum, inverse value rotation.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include <cfloat>
+#include <cmath>
+
+#include "tq_internal.h"
+
+namespace tq {
+namespace {
+
+constexpr int kTile = 32;   // tokens per tile
+constexpr int kRows = 16;   // query rows per CTA (one row group)
+constexpr int kThreads = 128;
+
+__device__ __forceinline__ float load_q(const void* p, int dtype, int64_t i) {
+    if (dtype == TQ_F32) return static_cast<const float*>(p)[i];
+    if (dtype == TQ_BF16) return __bfloat162float(static_cast<const __nv_bfloat16*>(p)[i]);
+    return __half2float(static_cast<const __half*>(p)[i]);
+}
+
+__device__ __forceinline__ unsigned extract_code(const uint32_t* words, int i, int b) {
+    const int p = i * b;
+    const int w = p >> 5;
+    const int sh = p & 31;
+    uint32_t v = words[w] >> sh;
+    if (sh + b > 32) v |= words[w + 1] << (32 - sh);
+    return v & ((1u << b) - 1u);
+}
+
+// q' = R q and q'' = S q' for the 16 rows of one (sequence, kv head, row group).
+template <int D>
+__global__ void qprep_kernel(DecodeArgs a) {
+    __shared__ float qs[D];
+    __shared__ float q1[D];
+    const int Hkv = a.pool.Hkv;
+    const int bh = blockIdx.x;
+    const int b = bh / Hkv, h = bh % Hkv;
+    const int rg = blockIdx.y;
+    const int RG = a.plan.row_groups;
+    const int i = threadIdx.x;
+    for (int rr = 0; rr < kRows; ++rr) {
+        const int r = rg * kRows + rr;
+        const int64_t o = ((static_cast<int64_t>(bh) * RG + rg) * kRows + rr) * D + i;
+        if (r >= a.plan.rows) {
+            a.qrot[o] = 0.0f;
+            a.qjl[o] = 0.0f;
+            continue;
+        }
+        const int g = r / a.Lq, l = r % a.Lq;
+        const int hq = h * a.G + g;
+        qs[i] = load_q(a.q, a.q_dtype, ((static_cast<int64_t>(b) * a.Hq + hq) * a.Lq + l) * D + i);
+        __syncthreads();
+        float t = 0.0f;
+        for (int k = 0; k < D; ++k) t = fmaf(__ldg(a.kc.Rt + k * D + i), qs[k], t);
+        q1[i] = t;
+        a.qrot[o] = t;
+        __syncthreads();
+        if (a.kc.mode == TQ_MODE_PROD) {
+            float z = 0.0f;
+            for (int k = 0; k < D; ++k) z = fmaf(__ldg(a.kc.St + k * D + i), q1[k], z);
+            a.qjl[o] = z;
+        } else {
+            a.qjl[o] = 0.0f;
+        }
+        __syncthreads();
+    }
+}
+
+template <int D>
+struct SplitSmem {
+    float qr[kRows][D];
+    float qj[kRows][D];
+    float kh[kTile][D + 1];
+    float vh[kTile][D + 1];
+    uint32_t sg[kTile][D / 32];
+    float kn[kTile], kr[kTile], vn[kTile];
+    float sc[kRows][kTile + 1];
+    float m[kRows], l[kRows], alpha[kRows];
+};
+
+template <int D>
+__global__ void __launch_bounds__(kThreads) split_kernel(DecodeArgs a) {
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    SplitSmem<D>& sm = *reinterpret_cast<SplitSmem<D>*>(smem_raw);
+    constexpr int kDPer = (D + kThreads - 1) / kThreads;
+    const int tid = threadIdx.x;
+    const int Hkv = a.pool.Hkv;
+    const int RG = a.plan.row_groups;
+    const int split = blockIdx.x;
+    const int h = blockIdx.y % Hkv;
+    const int rg = blockIdx.y / Hkv;
+    const int b = blockIdx.z;
+    const int bh = b * Hkv + h;
+    const int rows = a.plan.rows;
+    const int BT = a.pool.BT;
+    const float kappa = 1.2533141373155003f / static_cast<float>(D);  // sqrt(pi/2)/D
+
+    const int N = a.seq_lens[b];
+    const int cap = a.max_blocks * BT;
+    const bool bad = N < a.Lq || N > cap;
+    if (bad && split == 0 && tid == 0 && rg == 0 && h == 0) atomicOr(a.err, TQ_DEVERR_SEQLEN);
+    const int t_begin = split * a.plan.chunk;
+    int t_end = t_begin + a.plan.chunk;
+    const int n_eff = bad ? 0 : N;
+    if (t_end > n_eff) t_end = n_eff;
+
+    for (int e = tid; e < kRows * D; e += kThreads) {
+        const int rr = e / D, i = e % D;
+        const int64_t o = ((static_cast<int64_t>(bh) * RG + rg) * kRows + rr) * D + i;
+        sm.qr[rr][i] = a.qrot[o];
+        sm.qj[rr][i] = a.qjl[o];
+    }
+    if (tid < kRows) {
+        sm.m[tid] = -INFINITY;
+        sm.l[tid] = 0.0f;
+    }
+    float acc[kRows][kDPer];
+#pragma unroll
+    for (int r = 0; r < kRows; ++r)
+#pragma unroll
+        for (int j = 0; j < kDPer; ++j) acc[r][j] = 0.0f;
+    __syncthreads();
+
+    const int kb = a.kc.ib, vb = a.vc.mode == TQ_MODE_GROUP ? a.vc.bits : a.vc.ib;
+    // A tile never crosses a block: TT divides BT and every split starts on a
+    // multiple of kTile.
+    const int TT = BT < kTile ? BT : kTile;
+    for (int tile = t_begin; tile < t_end; tile += TT) {
+        const int nt = min(TT, t_end - tile);
+        const int lb = tile / BT;
+        const int slot0 = tile - lb * BT;
+        const int64_t pb = a.table ? static_cast<int64_t>(a.table[static_cast<int64_t>(b) * a.max_blocks + lb])
+                                   : static_cast<int64_t>(b) * a.max_blocks + lb;
+        const bool pb_ok = pb >= 0 && pb < a.pool.num_blocks;
+        if (!pb_ok && tid == 0) atomicOr(a.err, TQ_DEVERR_BLOCK);
+        const char* base = a.pool.base + (pb_ok ? (pb * Hkv + h) * a.pool.sub_bytes : 0);
+        const uint32_t* kidx = reinterpret_cast<const uint32_t*>(base + a.pool.off[0]) + static_cast<int64_t>(slot0) * a.kc.W;
+        const uint32_t* vidx = reinterpret_cast<const uint32_t*>(base + a.pool.off[4]) + static_cast<int64_t>(slot0) * a.vc.W;
+        for (int e = tid; e < nt * D; e += kThreads) {
+            const int t = e / D, i = e % D;
+            sm.kh[t][i] = __ldg(a.kc.c + extract_code(kidx + t * a.kc.W, i, kb));
+            const unsigned vcode = extract_code(vidx + t * a.vc.W, i, vb);
+            if (a.vc.mode == TQ_MODE_GROUP) {
+                const int ng = D / a.vc.group;
+                const __half* sc = reinterpret_cast<const __half*>(base + a.pool.off[5]) + static_cast<int64_t>(slot0 + t) * ng;
+                const __half* mn = reinterpret_cast<const __half*>(base + a.pool.off[6]) + static_cast<int64_t>(slot0 + t) * ng;
+                sm.vh[t][i] = fmaf(static_cast<float>(vcode), __half2float(sc[i / a.vc.group]),
+                                   __half2float(mn[i / a.vc.group]));
+            } else {
+                sm.vh[t][i] = __ldg(a.vc.c + vcode);
+            }
+        }
+        if (a.kc.mode == TQ_MODE_PROD) {
+            const uint32_t* sgn = reinterpret_cast<const uint32_t*>(base + a.pool.off[1]) + static_cast<int64_t>(slot0) * a.kc.Ws;
+            for (int e = tid; e < nt * (D / 32); e += kThreads) sm.sg[e / (D / 32)][e % (D / 32)] = sgn[e];
+        }
+        if (tid < nt) {
+            sm.kn[tid] = reinterpret_cast<const float*>(base + a.pool.off[2])[slot0 + tid];
+            sm.kr[tid] = a.kc.mode == TQ_MODE_PROD ? reinterpret_cast<const float*>(base + a.pool.off[3])[slot0 + tid] : 0.0f;
+            sm.vn[tid] = a.vc.mode == TQ_MODE_GROUP ? 1.0f : reinterpret_cast<const float*>(base + a.pool.off[5])[slot0 + tid];
+        }
+        __syncthreads();
+        // scores
+        {
+            const int t = tid & (kTile - 1);
+            for (int rr = tid / kTile; rr < kRows; rr += kThreads / kTile) {
+                const int r = rg * kRows + rr;
+                float s = -INFINITY;
+                if (t < nt && r < rows && pb_ok) {
+                    const int l = r % a.Lq;
+                    const int pos = tile + t;
+                    if (pos <= N - a.Lq + l) {
+                        float dot = 0.0f;
+                        for (int i = 0; i < D; ++i) dot = fmaf(sm.qr[rr][i], sm.kh[t][i], dot);
+                        if (a.kc.mode == TQ_MODE_PROD) {
+                            float sd = 0.0f;
+                            for (int i = 0; i < D; ++i) {
+                                const float qv = sm.qj[rr][i];
+                                sd += ((sm.sg[t][i >> 5] >> (i & 31)) & 1u) ? qv : -qv;
+                            }
+                            dot = fmaf(kappa * sm.kr[t], sd, dot);
+                        }
+                        s = a.scale * sm.kn[t] * dot;
+                    }
+                }
+                sm.sc[rr][t] = s;
+            }
+        }
+        __syncthreads();
+        if (tid < kRows) {
+            const int rr = tid;
+            float mt = -INFINITY;
+            for (int t = 0; t < kTile; ++t) mt = fmaxf(mt, sm.sc[rr][t]);
+            const float mo = sm.m[rr];
+            const float mn = fmaxf(mo, mt);
+            float alpha = 1.0f, sum = 0.0f;
+            if (mn != -INFINITY) {
+                alpha = expf(mo - mn);
+                for (int t = 0; t < kTile; ++t) {
+                    const float p = expf(sm.sc[rr][t] - mn);
+                    sum += p;
+                    sm.sc[rr][t] = p * sm.vn[t < nt ? t : 0];
+                }
+            } else {
+                for (int t = 0; t < kTile; ++t) sm.sc[rr][t] = 0.0f;
+            }
+            sm.l[rr] = sm.l[rr] * alpha + sum;
+            sm.m[rr] = mn;
+            sm.alpha[rr] = alpha;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int j = 0; j < kDPer; ++j) {
+            const int d = tid + j * kThreads;
+            if (d < D) {
+#pragma unroll
+                for (int r = 0; r < kRows; ++r) {
+                    float v = acc[r][j] * sm.alpha[r];
+                    for (int t = 0; t < nt; ++t) v = fmaf(sm.sc[r][t], sm.vh[t][d], v);
+                    acc[r][j] = v;
+                }
+            }
+        }
+        __syncthreads();
+    }
+    const int64_t pbase = ((static_cast<int64_t>(bh) * RG + rg) * a.plan.splits + split) * kRows;
+#pragma unroll
+    for (int j = 0; j < kDPer; ++j) {
+        const int d = tid + j * kThreads;
+        if (d < D) {
+#pragma unroll
+            for (int r = 0; r < kRows; ++r) a.part[(pbase + r) * D + d] = acc[r][j];
+        }
+    }
+    if (tid < kRows) {
+        a.ml[(pbase + tid) * 2] = sm.m[tid];
+        a.ml[(pbase + tid) * 2 + 1] = sm.l[tid];
+    }
+}
+
+// Merge the splits of one (sequence, kv head, row group) and rotate back.
+template <int D>
+__global__ void merge_kernel(DecodeArgs a) {
+    __shared__ float orot[D];
+    const int Hkv = a.pool.Hkv;
+    const int bh = blockIdx.x;
+    const int b = bh / Hkv, h = bh % Hkv;
+    const int rg = blockIdx.y;
+    const int RG = a.plan.row_groups;
+    const int S = a.plan.splits;
+    const int i = threadIdx.x;
+    for (int rr = 0; rr < kRows; ++rr) {
+        const int r = rg * kRows + rr;
+        if (r >= a.plan.rows) break;
+        const int64_t base = (static_cast<int64_t>(bh) * RG + rg) * S;
+        float M = -INFINITY;
+        for (int s = 0; s < S; ++s) M = fmaxf(M, a.ml[((base + s) * kRows + rr) * 2]);
+        float L = 0.0f, o = 0.0f;
+        if (M != -INFINITY) {
+            for (int s = 0; s < S; ++s) {
+                const float ms = a.ml[((base + s) * kRows + rr) * 2];
+                if (ms == -INFINITY) continue;
+                const float w = expf(ms - M);
+                L = fmaf(w, a.ml[((base + s) * kRows + rr) * 2 + 1], L);
+                o = fmaf(w, a.part[((base + s) * kRows + rr) * D + i], o);
+            }
+        }
+        orot[i] = L > 0.0f ? o / L : 0.0f;
+        __syncthreads();
+        float res = orot[i];
+        if (a.vc.mode != TQ_MODE_GROUP) {
+            res = 0.0f;
+            for (int k = 0; k < D; ++k) res = fmaf(orot[k], __ldg(a.vc.R + k * D + i), res);
+        }
+        const int g = r / a.Lq, l = r % a.Lq;
+        a.out[((static_cast<int64_t>(b) * a.Hq + h * a.G + g) * a.Lq + l) * D + i] = res;
+        __syncthreads();
+    }
+}
+
+template <int D>
+cudaError_t launch_decode_d(const DecodeArgs& a, cudaStream_t s) {
+    const int B = a.batch, Hkv = a.pool.Hkv, RG = a.plan.row_groups;
+    qprep_kernel<D><<<dim3(B * Hkv, RG), D, 0, s>>>(a);
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    const size_t smem = sizeof(SplitSmem<D>);
+    static std::atomic<uint64_t> attr_set{0};  // one bit per device
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const uint64_t bit = 1ull << (dev & 63);
+    if (!(attr_set.load() & bit)) {
+        cudaError_t e = cudaFuncSetAttribute(split_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(smem));
+        if (e != cudaSuccess) return e;
+        attr_set.fetch_or(bit);
+    }
+    split_kernel<D><<<dim3(a.plan.splits, Hkv * RG, B), kThreads, smem, s>>>(a);
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    merge_kernel<D><<<dim3(B * Hkv, RG), D, 0, s>>>(a);
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+DecodePlan make_decode_plan(int D, int batch, int Hkv, int G, int Lq, int max_seq_len, int num_sms) {
+    DecodePlan p{};
+    p.rows = G * Lq;
+    p.row_groups = (p.rows + kRows - 1) / kRows;
+    const int64_t units = static_cast<int64_t>(batch) * Hkv * p.row_groups;
+    const int64_t target = static_cast<int64_t>(num_sms) * 4;
+    const int64_t max_splits = (max_seq_len + kTile - 1) / kTile;
+    int64_t splits = (target + units - 1) / units;
+    if (splits > max_splits) splits = max_splits;
+    if (splits < 1) splits = 1;
+    int64_t chunk = (max_seq_len + splits - 1) / splits;
+    chunk = (chunk + kTile - 1) / kTile * kTile;
+    if (chunk < kTile) chunk = kTile;
+    splits = (max_seq_len + chunk - 1) / chunk;
+    if (splits < 1) splits = 1;
+    p.splits = static_cast<int>(splits);
+    p.chunk = static_cast<int>(chunk);
+    auto al = [](size_t x) { return (x + 255) / 256 * 256; };
+    p.q_bytes = al(static_cast<size_t>(batch) * Hkv * p.row_groups * kRows * D * sizeof(float));
+    p.part_bytes = al(static_cast<size_t>(batch) * Hkv * p.row_groups * p.splits * kRows * D * sizeof(float));
+    p.ml_bytes = al(static_cast<size_t>(batch) * Hkv * p.row_groups * p.splits * kRows * 2 * sizeof(float));
+    p.total = 2 * p.q_bytes + p.part_bytes + p.ml_bytes;
+    return p;
+}
+
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s) {
+    if (a.batch == 0) return cudaSuccess;
+    switch (a.kc.D) {
+        case 64: return launch_decode_d<64>(a, s);
+        case 128: return launch_decode_d<128>(a, s);
+        case 256: return launch_decode_d<256>(a, s);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace tq

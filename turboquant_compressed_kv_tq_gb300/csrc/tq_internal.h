@@ -1,0 +1,137 @@
+// Internal declarations shared by the libtq translation units.
+#pragma once
+
+#include <atomic>
+#include <cstdint>
+#include <vector>
+
+#include "tq.h"
+
+#ifdef __CUDACC__
+#include <cuda_runtime.h>
+#endif
+
+namespace tq {
+
+struct HostTables {
+    std::vector<float> rotation;   // D x D row-major, y = R x
+    std::vector<float> qjl;        // D x D row-major (prod only)
+    std::vector<float> centroids;  // 2^index_bits, ascending, antisymmetric
+    std::vector<float> midpoints;  // 2^index_bits - 1
+};
+
+// Deterministic codec tables from (D, index bits, seed) (host, fp64 -> fp32).
+void build_codec_tables(int D, int index_bits, bool with_qjl, uint64_t seed, HostTables& out);
+
+// Device view of one codec.
+struct CodecDev {
+    const float* R;    // [D][D] row-major
+    const float* Rt;   // [D][D] transposed rotation (Rt[k*D+i] = R[i][k])
+    const float* St;   // [D][D] transposed QJL matrix (prod) or nullptr
+    const float* c;    // centroids
+    const float* m;    // midpoints
+    int D;
+    int mode;          // tq_mode
+    int bits;          // total bits
+    int ib;            // index bits
+    int W;             // index words
+    int Ws;            // sign words (prod)
+    int group;         // group size (group mode)
+};
+
+// Device view of one layer pool.
+struct PoolDev {
+    char* base;          // layer pool
+    int64_t sub_bytes;   // bytes per (block, head) sub-block
+    int64_t off[7];      // stream offsets inside a sub-block
+    int Hkv;
+    int BT;              // tokens per block
+    int num_blocks;
+};
+
+struct EncodeAppendArgs {
+    CodecDev kc, vc;
+    PoolDev pool;
+    const void* k;
+    const void* v;
+    int dtype;
+    int batch, n_new;
+    const int32_t* seq_lens;
+    const int32_t* table;
+    int max_blocks;
+    unsigned* err;
+};
+
+struct QuantizeArgs {
+    CodecDev cd;
+    const void* x;
+    int dtype;
+    int64_t n;
+    uint32_t* idx;
+    void* aux0;
+    void* aux1;
+    void* aux2;
+};
+
+// Decode plan shared by workspace sizing and the launch.
+struct DecodePlan {
+    int rows;         // G * Lq
+    int row_groups;   // ceil(rows / 16)
+    int splits;       // token splits per (sequence, kv head, row group)
+    int chunk;        // tokens per split (multiple of the tile)
+    size_t q_bytes;   // prepared queries
+    size_t part_bytes;// partial accumulators
+    size_t ml_bytes;  // partial (max, sum)
+    size_t total;
+};
+
+struct DecodeArgs {
+    CodecDev kc, vc;
+    PoolDev pool;
+    const void* q;
+    int q_dtype;
+    int batch, Hq, Lq, G;
+    const int32_t* seq_lens;
+    const int32_t* table;
+    int max_blocks;
+    float scale;
+    float* out;
+    float* qrot;   // [B][Hkv][RG*16][D]
+    float* qjl;    // [B][Hkv][RG*16][D]
+    float* part;   // [B][Hkv][RG][splits][16][D]
+    float* ml;     // [B][Hkv][RG][splits][16][2]
+    DecodePlan plan;
+    unsigned* err;
+};
+
+DecodePlan make_decode_plan(int D, int batch, int Hkv, int G, int Lq, int max_seq_len, int num_sms);
+
+#ifdef __CUDACC__
+cudaError_t launch_encode_append(const EncodeAppendArgs& a, cudaStream_t s);
+cudaError_t launch_quantize(const QuantizeArgs& a, cudaStream_t s);
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);
+#endif
+
+extern std::atomic<uint64_t> g_launches;
+
+}  // namespace tq
+
+// Opaque codec handle behind the C ABI.
+struct tq_codec {
+    int head_dim = 0;
+    int bits = 0;
+    int mode = 0;
+    int group = 0;
+    uint64_t seed = 0;
+    int index_bits = 0;
+    int index_words = 0;
+    int sign_words = 0;
+    int record_bytes = 0;
+    int device = -1;
+    tq::HostTables host;
+    float* d_R = nullptr;
+    float* d_Rt = nullptr;
+    float* d_St = nullptr;
+    float* d_c = nullptr;
+    float* d_m = nullptr;
+};
