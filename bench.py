@@ -1,0 +1,399 @@
+"""Benchmark: TurboQuant compressed-KV decode attention at 256k context.
+
+Workload (one replica per GPU): 64 layers, 8 KV heads, 64 query heads,
+head_dim 128, keys 3-bit prod, values 3-bit MSE, 262,144 tokens prefilled by
+chunked encode (8192-token chunks), then decode steps that each append 2
+tokens per layer and attend with query length 2 over every layer.
+
+A step = for each of the 64 layers: tq_encode_append (2 tokens x 8 heads)
+followed by tq_decode_attention (q_len 2). `value` is the compressed bytes the
+step's decode reads (valid tokens x heads x layers x record bytes) divided by
+the step time, summed over ranks. Inputs are resident in HBM before the timed
+region; the cache (14.5 GB) is far larger than L2, so no flush is needed.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "compressed-KV decode-attn HBM GB/s (% of peak) and steps/s @256k; encode Mtok/s"
+UNIT = "GB/s"
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clock and throttle reasons during a region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._t = threading.Thread(target=self._read, daemon=True)
+            self._t.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self._t.join(timeout=2)
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ distributed
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def reduce_max(x: float, world: int, device=None) -> float:
+    """Max of a float over ranks (identity for a single process)."""
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ------------------------------------------------------------------ oracle baseline
+
+def cpu_baseline(w, kv_heads=2, rows=16, device="cuda"):
+    """Time the oracle's decode on the host cores on a bounded sample: layer 0,
+    `kv_heads` KV heads at the full prefill length, all query rows of those
+    heads. Returns (GB/s of compressed bytes, cores, sample text, seconds)."""
+    import numpy as np
+    import torch
+
+    import oracle as O
+    from turboquant_compressed_kv_tq_gb300 import workloads as wl
+
+    D = w.head_dim
+    N = w.seq_lens[0]
+    kc = O.Codec(D, w.key.bits, w.key.mode, w.key.seed)
+    vc = O.Codec(D, w.value.bits, w.value.mode, w.value.seed)
+    K = wl.kv_chunk(w, 0, 0, 0, N, "k", device)[:kv_heads].float().cpu().numpy()
+    V = wl.kv_chunk(w, 0, 0, 0, N, "v", device)[:kv_heads].float().cpu().numpy()
+    q = wl.queries(w, 0, 0, device)[0].double().cpu().numpy()
+    recs = [(kc.encode(K[h]), vc.encode(V[h])) for h in range(kv_heads)]
+    G = w.gqa
+    t0 = time.perf_counter()
+    for h in range(kv_heads):
+        O.decode_rotated(q[h * G:(h + 1) * G], kc, recs[h][0], vc, recs[h][1], 1 / math.sqrt(D), w.q_len)
+    dt = time.perf_counter() - t0
+    nbytes = kv_heads * N * (kc.record_bytes + vc.record_bytes)
+    sample = (f"oracle rotated-domain decode (fp64), layer 0, {kv_heads} KV heads x {G * w.q_len} "
+              f"query rows, N={N}, {nbytes / 1e6:.1f} MB of compressed records")
+    return nbytes / dt / 1e9, O.num_threads(), sample, dt
+
+
+def run_reference(args):
+    rank, world, local = dist_env()
+    if rank != 0:
+        return 0
+    import torch
+    from turboquant_compressed_kv_tq_gb300 import workloads as wl
+    import oracle as O
+    O.build()
+    w = wl.long_256k()
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    vals = []
+    cores = sample = None
+    for _ in range(max(1, args.warmup // 3)):
+        cpu_baseline(w, kv_heads=1, device=dev)
+    for _ in range(args.steps):
+        v, cores, sample, _ = cpu_baseline(w, kv_heads=1, device=dev)
+        vals.append(v)
+    val = statistics.median(vals)
+    line = {"impl": "reference", "metric": METRIC, "value": val, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": _workload_text(w)},
+            "cpu_baseline": {"value": val, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def _workload_text(w):
+    return (f"{w.name}: {w.num_layers} layers, {w.num_kv_heads} KV heads, {w.num_q_heads} query "
+            f"heads, head_dim {w.head_dim}, batch {w.batch}, N={w.seq_lens[0]} prefilled in "
+            f"{w.prefill_chunk}-token chunks then +{w.append_per_step} tokens per step, q_len "
+            f"{w.q_len}; keys {w.key.bits}-bit prod, values {w.value.bits}-bit MSE; bf16 inputs N(0,1)")
+
+
+# ------------------------------------------------------------------ GPU arm
+
+def run_gpu(args):
+    import numpy as np
+    import torch
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    from turboquant_compressed_kv_tq_gb300 import build as tqbuild
+    if rank == 0 or not os.path.exists(tqbuild.LIB):
+        tqbuild.build()
+    barrier(world)
+    import turboquant_compressed_kv_tq_gb300 as tq
+    from turboquant_compressed_kv_tq_gb300 import workloads as wl
+
+    w = wl.long_256k()
+    L, Hkv, Hq, D, Lq = w.num_layers, w.num_kv_heads, w.num_q_heads, w.head_dim, w.q_len
+    N0 = w.seq_lens[0]
+    A = w.append_per_step
+    total_steps = args.warmup + args.steps
+    cap = N0 + A * total_steps
+    BT = w.block_tokens
+    nblk = (cap + BT - 1) // BT
+    kc = tq.Codec(D, w.key.bits, w.key.mode, w.key.seed)
+    vc = tq.Codec(D, w.value.bits, w.value.mode, w.value.seed)
+    cache = tq.CompressedKVCache(kc, vc, L, nblk, BT, Hkv, dev)
+    rec_bytes = kc.record_bytes + vc.record_bytes
+
+    stream = torch.cuda.current_stream(dev)
+    # ---------------- prefill: chunked encode of every layer (timed per layer)
+    zero = torch.zeros(1, dtype=torch.int32, device=dev)
+    enc_ms = 0.0
+    chunk = w.prefill_chunk
+    nchunks = (N0 + chunk - 1) // chunk
+    starts = torch.arange(0, N0, chunk, dtype=torch.int32, device=dev)
+    for layer in range(L):
+        ks = [wl.kv_chunk(w, layer, rank, c * chunk, min(chunk, N0 - c * chunk), "k", dev).unsqueeze(0)
+              for c in range(nchunks)]
+        vs = [wl.kv_chunk(w, layer, rank, c * chunk, min(chunk, N0 - c * chunk), "v", dev).unsqueeze(0)
+              for c in range(nchunks)]
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for c in range(nchunks):
+            cache.append(layer, ks[c], vs[c], starts[c:c + 1], None, nblk)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        enc_ms += e0.elapsed_time(e1)
+        del ks, vs
+    assert tq.tq_device_error() == 0
+
+    # ---------------- decode-step inputs, resident on the device
+    steps_in = []
+    for s in range(total_steps):
+        k_new = torch.stack([wl.kv_chunk(w, layer, rank, N0 + A * s, A, "k", dev) for layer in range(L)])
+        v_new = torch.stack([wl.kv_chunk(w, layer, rank, N0 + A * s, A, "v", dev) for layer in range(L)])
+        q = torch.stack([wl.queries(w, layer, s, dev)[0] for layer in range(L)])
+        steps_in.append((k_new.unsqueeze(1).contiguous(), v_new.unsqueeze(1).contiguous(),
+                         q.unsqueeze(1).contiguous()))
+    lens_pre = torch.tensor([N0 + A * s for s in range(total_steps)], dtype=torch.int32, device=dev)
+    lens_post = lens_pre + A
+    ws = torch.empty(cache.workspace_bytes(1, Hq, Lq, cap), dtype=torch.uint8, device=dev)
+    out = torch.empty(L, 1, Hq, Lq, D, dtype=torch.float32, device=dev)
+
+    def step(s, ev=None):
+        k_new, v_new, q = steps_in[s]
+        for layer in range(L):
+            cache.append(layer, k_new[layer], v_new[layer], lens_pre[s:s + 1], None, nblk)
+            if ev is not None:
+                ev[layer][0].record(stream)
+            cache.decode(layer, q[layer], lens_post[s:s + 1], None, nblk, cap, out[layer], ws)
+            if ev is not None:
+                ev[layer][1].record(stream)
+
+    for s in range(args.warmup):
+        step(s)
+    torch.cuda.synchronize(dev)
+    # ---------------- timed region
+    n_launch0 = tq.tq_launch_count()
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        t_start.record(stream)
+        for s in range(args.warmup, total_steps):
+            step(s)
+        t_end.record(stream)
+        torch.cuda.synchronize(dev)
+    barrier(world)
+    launches = tq.tq_launch_count() - n_launch0
+    step_ms = t_start.elapsed_time(t_end) / args.steps
+    step_ms_max = reduce_max(step_ms, world, dev)
+    # bytes the decode of step s reads: valid tokens x heads x layers x record bytes
+    dec_bytes = [sum(L * Hkv * (N0 + A * s + A) * rec_bytes for _ in [0])
+                 for s in range(args.warmup, total_steps)]
+    bytes_per_step = sum(dec_bytes) / args.steps
+    value = world * bytes_per_step / (step_ms_max * 1e-3) / 1e9
+
+    # ---------------- roofline pass: per-launch decode timing on the launching stream
+    evs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            for _ in range(L)] for _ in range(args.steps)]
+    torch.cuda.synchronize(dev)
+    for i, s in enumerate(range(args.warmup, total_steps)):
+        step(s, evs[i])
+    torch.cuda.synchronize(dev)
+    durs = [a.elapsed_time(b) for row in evs for a, b in row]
+    dec_ms = sum(durs) / len(durs)
+    per_launch_bytes = bytes_per_step / L
+    peak, peak_kind = _peaks()
+    achieved = per_launch_bytes / (dec_ms * 1e-3) / 1e9
+
+    # ---------------- end to end through the API with host buffers
+    pin_in = []
+    for s in range(args.warmup, total_steps):
+        pin_in.append(tuple(t.cpu().pin_memory() for t in steps_in[s]))
+    out_host = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    dk = torch.empty_like(steps_in[0][0])
+    dv = torch.empty_like(steps_in[0][1])
+    dq = torch.empty_like(steps_in[0][2])
+    h2d = sum(t.numel() * t.element_size() for t in pin_in[0])
+    d2h = out_host.numel() * out_host.element_size()
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    t0 = time.perf_counter()
+    for i, s in enumerate(range(args.warmup, total_steps)):
+        hk, hv, hq = pin_in[i]
+        dk.copy_(hk, non_blocking=True)
+        dv.copy_(hv, non_blocking=True)
+        dq.copy_(hq, non_blocking=True)
+        for layer in range(L):
+            cache.append(layer, dk[layer], dv[layer], lens_pre[s:s + 1], None, nblk)
+            cache.decode(layer, dq[layer], lens_post[s:s + 1], None, nblk, cap, out[layer], ws)
+        out_host.copy_(out, non_blocking=True)
+        torch.cuda.current_stream(dev).synchronize()
+    e2e_s = (time.perf_counter() - t0) / args.steps
+    e2e_s = reduce_max(e2e_s, world, dev)
+    e2e_value = world * bytes_per_step / e2e_s / 1e9
+    assert tq.tq_device_error() == 0
+
+    enc_tokens = N0 * L * Hkv
+    result = None
+    if rank == 0:
+        cpu = None
+        if world == 1 and not args.no_cpu_baseline:
+            v, cores, sample, secs = cpu_baseline(w, device=dev)
+            cpu = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample,
+                   "seconds": round(secs, 2)}
+        clocks = clk.summary()
+        result = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": step_ms_max, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": _workload_text(w),
+                       "bytes_per_step": bytes_per_step, "record_bytes_per_token_head": rec_bytes,
+                       "l2": "inputs larger than L2: each step reads a 14.5 GB compressed cache",
+                       "block_tokens": BT, "replicas": world},
+            "steps_per_s": 1000.0 / step_ms_max,
+            "hbm_frac_of_measured": value / world / peak,
+            "encode": {"prefill_s": enc_ms / 1e3,
+                       "mtok_s": enc_tokens / (enc_ms * 1e-3) / 1e6,
+                       "unit": "M token-head-layers/s",
+                       "model_tokens_per_s": N0 / (enc_ms * 1e-3),
+                       "gb_s_in_out": (enc_tokens * (2 * 2 * D + rec_bytes)) / (enc_ms * 1e-3) / 1e9},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "traffic": None, "peak_kind": peak_kind,
+                         "kernel": "tq_decode_attention (query prep + split + merge), per layer",
+                         "avg_launch_ms": dec_ms, "algorithmic_bytes_per_launch": per_launch_bytes},
+            "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "ms_per_step": e2e_s * 1e3},
+            "gpu_launches": launches,
+            "clocks": clocks,
+        }
+        if cpu:
+            result["cpu_baseline"] = cpu
+        print(json.dumps(result), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=32)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3 and args.impl != "reference":
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

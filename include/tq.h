@@ -67,6 +67,7 @@ typedef enum {
 #define TQ_DEVERR_CAPACITY 1u   /* append past a sequence's block-table capacity */
 #define TQ_DEVERR_BLOCK 2u      /* block id outside [0, num_blocks)              */
 #define TQ_DEVERR_SEQLEN 4u     /* decode seq_len outside [q_len, capacity]      */
+#define TQ_DEVERR_TIMEOUT 8u    /* a bounded wait for a bulk copy ran out         */
 
 /* ------------------------------------------------------------------ */
 /* Codecs                                                               */

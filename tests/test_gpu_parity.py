@@ -262,3 +262,28 @@ def test_empty_batch_is_noop():
     k = torch.zeros(0, 1, 2, D, dtype=torch.bfloat16, device=DEV)
     cache.append(0, k, k, torch.zeros(0, dtype=torch.int32, device=DEV), None, 4)
     assert tq.tq_launch_count() == n0
+
+
+KEYS = [("prod", 2), ("prod", 3), ("prod", 4), ("mse", 2), ("mse", 3), ("mse", 4)]
+VALUES = [("mse", 2), ("mse", 3), ("mse", 4), ("group", 2, 32), ("group", 4, 64), ("group", 4, 128)]
+
+
+@pytest.mark.parametrize("key", KEYS)
+@pytest.mark.parametrize("value", VALUES)
+def test_decode_codec_combinations(key, value):
+    # every tensor-core kernel instantiation: ragged length, two query positions
+    w = dataclasses.replace(_small_paged(key=key, value=value, lens=(203,), Lq=2, G=8, bt=64, Hkv=2),
+                            append_per_step=0)
+    _check_decode(w, [0])
+
+
+@pytest.mark.parametrize("bt", [16, 32, 128])
+def test_decode_block_sizes(bt):
+    w = dataclasses.replace(_small_paged(lens=(300, 77, 1000), Lq=1, G=4, bt=bt), append_per_step=0)
+    _check_decode(w, [1])
+
+
+def test_decode_head_dim_64():
+    w = dataclasses.replace(_small_paged(key=("prod", 3), value=("mse", 4), D=64, lens=(150,), Lq=2, G=4),
+                            append_per_step=0)
+    _check_decode(w, [0])

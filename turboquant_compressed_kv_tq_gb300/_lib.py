@@ -32,6 +32,7 @@ TQ_F16 = 2
 TQ_DEVERR_CAPACITY = 1
 TQ_DEVERR_BLOCK = 2
 TQ_DEVERR_SEQLEN = 4
+TQ_DEVERR_TIMEOUT = 8
 
 
 class TQError(RuntimeError):

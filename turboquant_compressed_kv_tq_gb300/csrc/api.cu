@@ -382,7 +382,7 @@ tq_status tq_decode_workspace_bytes(const tq_cache_desc* cache, int batch, int n
     if (G * q_len > 64) return TQ_ERR_UNSUPPORTED;
     int sms = 0;
     if (device_state(nullptr, &sms) != TQ_OK) return TQ_ERR_CUDA;
-    *bytes = make_decode_plan(cache->head_dim, batch, cache->num_kv_heads, G, q_len, max_seq_len, sms).total;
+    *bytes = make_decode_plan(cache, batch, G, q_len, max_seq_len, sms).total;
     return TQ_OK;
 }
 
@@ -407,10 +407,11 @@ tq_status tq_decode_attention(const tq_codec* kc, const tq_codec* vc, const tq_c
     if (batch > 65535) return TQ_ERR_INVALID_ARG;
     if (!q || !out || !seq_lens || !workspace) return TQ_ERR_INVALID_ARG;
     if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return TQ_ERR_INVALID_ARG;
+    if (!aligned16(out)) return TQ_ERR_INVALID_ARG;
     unsigned* err = nullptr;
     int sms = 0;
     if (device_state(&err, &sms) != TQ_OK) return TQ_ERR_CUDA;
-    const DecodePlan plan = make_decode_plan(cache->head_dim, batch, cache->num_kv_heads, G, q_len, max_seq_len, sms);
+    const DecodePlan plan = make_decode_plan(cache, batch, G, q_len, max_seq_len, sms);
     if (workspace_bytes < plan.total) return TQ_ERR_CAPACITY;
     DecodeArgs a{};
     a.kc = dev_view(kc);
@@ -432,6 +433,7 @@ tq_status tq_decode_attention(const tq_codec* kc, const tq_codec* vc, const tq_c
     a.qjl = reinterpret_cast<float*>(ws + plan.q_bytes);
     a.part = reinterpret_cast<float*>(ws + 2 * plan.q_bytes);
     a.ml = reinterpret_cast<float*>(ws + 2 * plan.q_bytes + plan.part_bytes);
+    a.ws = workspace;
     a.plan = plan;
     a.err = err;
     return launch_decode(a, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;

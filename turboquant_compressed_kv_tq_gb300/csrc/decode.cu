@@ -320,33 +320,127 @@ cudaError_t launch_decode_d(const DecodeArgs& a, cudaStream_t s) {
 
 }  // namespace
 
-DecodePlan make_decode_plan(int D, int batch, int Hkv, int G, int Lq, int max_seq_len, int num_sms) {
-    DecodePlan p{};
-    p.rows = G * Lq;
-    p.row_groups = (p.rows + kRows - 1) / kRows;
-    const int64_t units = static_cast<int64_t>(batch) * Hkv * p.row_groups;
-    const int64_t target = static_cast<int64_t>(num_sms) * 4;
-    const int64_t max_splits = (max_seq_len + kTile - 1) / kTile;
-    int64_t splits = (target + units - 1) / units;
+namespace mmadec {
+struct MmaArgs;
+}
+
+}  // namespace tq
+#include "decode_mma_impl.cuh"
+namespace tq {
+namespace mmadec {
+bool dispatch_a(int, bool, bool, int, const MmaArgs&, size_t, cudaStream_t, cudaError_t*);
+bool dispatch_b(int, bool, bool, int, const MmaArgs&, size_t, cudaStream_t, cudaError_t*);
+bool dispatch_c(int, bool, bool, int, const MmaArgs&, size_t, cudaStream_t, cudaError_t*);
+}  // namespace mmadec
+
+namespace {
+
+size_t al256(size_t x) { return (x + 255) / 256 * 256; }
+
+// Token splits: enough CTAs to cover the GPU, split length a multiple of the
+// tile, and at most `max_chunk` tokens so that many short units still balance.
+void choose_splits(DecodePlan& p, int64_t units, int64_t target_ctas, int max_seq_len, int tile, int max_chunk) {
+    const int64_t max_splits = (max_seq_len + tile - 1) / tile;
+    int64_t splits = (target_ctas + units - 1) / units;
     if (splits > max_splits) splits = max_splits;
     if (splits < 1) splits = 1;
     int64_t chunk = (max_seq_len + splits - 1) / splits;
-    chunk = (chunk + kTile - 1) / kTile * kTile;
-    if (chunk < kTile) chunk = kTile;
+    chunk = (chunk + tile - 1) / tile * tile;
+    if (chunk > max_chunk) chunk = max_chunk;
+    if (chunk < tile) chunk = tile;
     splits = (max_seq_len + chunk - 1) / chunk;
-    if (splits < 1) splits = 1;
-    p.splits = static_cast<int>(splits);
+    p.splits = static_cast<int>(splits < 1 ? 1 : splits);
     p.chunk = static_cast<int>(chunk);
-    auto al = [](size_t x) { return (x + 255) / 256 * 256; };
-    p.q_bytes = al(static_cast<size_t>(batch) * Hkv * p.row_groups * kRows * D * sizeof(float));
-    p.part_bytes = al(static_cast<size_t>(batch) * Hkv * p.row_groups * p.splits * kRows * D * sizeof(float));
-    p.ml_bytes = al(static_cast<size_t>(batch) * Hkv * p.row_groups * p.splits * kRows * 2 * sizeof(float));
-    p.total = 2 * p.q_bytes + p.part_bytes + p.ml_bytes;
+}
+
+bool mma_supported(const tq_cache_desc* d, DecodePlan& p) {
+    if (d->head_dim != mmadec::kD) return false;
+    p.kprod = d->key_mode == TQ_MODE_PROD;
+    p.kb = p.kprod ? d->key_bits - 1 : d->key_bits;
+    if (p.kprod ? (p.kb < 1 || p.kb > 3) : (p.kb < 2 || p.kb > 4)) return false;
+    p.vgroup = d->value_mode == TQ_MODE_GROUP;
+    p.vb = d->value_bits;
+    if (p.vgroup) {
+        if ((p.vb != 2 && p.vb != 4) || d->value_group < 32) return false;
+    } else if (p.vb < 2 || p.vb > 4) {
+        return false;
+    }
+    return true;
+}
+
+}  // namespace
+
+DecodePlan make_decode_plan(const tq_cache_desc* d, int batch, int G, int Lq, int max_seq_len, int num_sms) {
+    DecodePlan p{};
+    const int D = d->head_dim;
+    const int Hkv = d->num_kv_heads;
+    p.rows = G * Lq;
+    p.row_groups = (p.rows + kRows - 1) / kRows;
+    const int64_t units = static_cast<int64_t>(batch) * Hkv * p.row_groups;
+    if (mma_supported(d, p)) {
+        p.kind = 1;
+        p.tile = d->block_tokens < mmadec::kMaxTile ? d->block_tokens : mmadec::kMaxTile;
+        choose_splits(p, units, num_sms, max_seq_len, p.tile, 16384);
+        int o = 0;
+        for (int k = 0; k < 7; ++k) {
+            const int64_t so = d->stream_offset[k];
+            int64_t next = d->subblock_bytes;
+            for (int k2 = k + 1; k2 < 7; ++k2)
+                if (d->stream_offset[k2] >= 0) { next = d->stream_offset[k2]; break; }
+            if (so < 0) {
+                p.st_off[k] = -1;
+                p.st_field[k] = 0;
+                continue;
+            }
+            p.st_field[k] = static_cast<int>((next - so) / d->block_tokens);
+            p.st_off[k] = o;
+            o += p.tile * p.st_field[k];
+        }
+        p.st_bytes = (o + 127) / 128 * 128;
+        const size_t ring = static_cast<size_t>(mmadec::kWarps) * mmadec::kStages * p.st_bytes;
+        const size_t combine = sizeof(float) * (2 * mmadec::kWarps * kRows + mmadec::kWarps * kRows * (D + 1));
+        const size_t body = ((ring > combine ? ring : combine) + 127) / 128 * 128;
+        p.bar_off = static_cast<int>(body);
+        p.smem = body + sizeof(uint64_t) * mmadec::kWarps * mmadec::kStages;
+        p.q_bytes = al256(static_cast<size_t>(units) * 2 * 8 * 32 * 16);
+        p.cnt_bytes = al256(static_cast<size_t>(units) * sizeof(unsigned));
+    } else {
+        p.kind = 0;
+        p.tile = kTile;
+        choose_splits(p, units, static_cast<int64_t>(num_sms) * 4, max_seq_len, kTile, 1 << 30);
+        p.q_bytes = al256(static_cast<size_t>(units) * kRows * D * sizeof(float));
+        p.cnt_bytes = 0;
+    }
+    p.part_bytes = al256(static_cast<size_t>(units) * p.splits * kRows * D * sizeof(float));
+    p.ml_bytes = al256(static_cast<size_t>(units) * p.splits * kRows * 2 * sizeof(float));
+    p.total = (p.kind ? p.q_bytes + p.cnt_bytes : 2 * p.q_bytes) + p.part_bytes + p.ml_bytes;
     return p;
 }
 
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s) {
     if (a.batch == 0) return cudaSuccess;
+    if (a.plan.kind == 1) {
+        mmadec::MmaArgs m{};
+        m.a = a;
+        m.st.tt = a.plan.tile;
+        m.st.bytes = a.plan.st_bytes;
+        m.st.bar_off = a.plan.bar_off;
+        for (int k = 0; k < 7; ++k) {
+            m.st.off[k] = a.plan.st_off[k];
+            m.st.field[k] = a.plan.st_field[k];
+        }
+        char* ws = static_cast<char*>(a.ws);
+        m.qfrag = reinterpret_cast<const uint4*>(ws);
+        m.cnt = reinterpret_cast<unsigned*>(ws + a.plan.q_bytes);
+        m.part = reinterpret_cast<float*>(ws + a.plan.q_bytes + a.plan.cnt_bytes);
+        m.ml = reinterpret_cast<float*>(ws + a.plan.q_bytes + a.plan.cnt_bytes + a.plan.part_bytes);
+        cudaError_t e = cudaErrorInvalidValue;
+        const DecodePlan& p = a.plan;
+        if (mmadec::dispatch_a(p.kb, p.kprod, p.vgroup, p.vb, m, p.smem, s, &e)) return e;
+        if (mmadec::dispatch_b(p.kb, p.kprod, p.vgroup, p.vb, m, p.smem, s, &e)) return e;
+        if (mmadec::dispatch_c(p.kb, p.kprod, p.vgroup, p.vb, m, p.smem, s, &e)) return e;
+        return cudaErrorInvalidValue;
+    }
     switch (a.kc.D) {
         case 64: return launch_decode_d<64>(a, s);
         case 128: return launch_decode_d<128>(a, s);

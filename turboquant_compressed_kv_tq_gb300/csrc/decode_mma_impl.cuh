@@ -1,0 +1,524 @@
+// Kernel templates of the tensor-core decode path (see decode_mma.cuh).
+#pragma once
+
+#include "decode_mma.cuh"
+
+namespace tq {
+namespace mmadec {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kSqrtHalfPi = 1.2533141373155003f;  // sqrt(pi/2)
+
+// Per-launch layout of one shared-memory stage (TT tokens of every stream).
+struct StageLayout {
+    int tt;                 // tokens per stage (= tile), 16..64, divides block_tokens
+    int bytes;              // stage bytes rounded up to 128
+    int off[7];             // stream offsets inside a stage (-1 = absent)
+    int field[7];           // bytes per token of each stream
+    int bar_off;            // byte offset of the mbarriers (past ring and merge areas)
+};
+
+struct MmaArgs {
+    DecodeArgs a;
+    StageLayout st;
+    const uint4* qfrag;     // [unit][2][8][32] uint4
+    unsigned* cnt;          // [unit]
+    float* part;            // [unit][splits][16][128]
+    float* ml;              // [unit][splits][16][2]
+};
+
+// ------------------------------------------------------------------ query fragments
+
+// q' = R_k q * scale * log2(e) and q'' = S_k q' * sqrt(pi/2)/D (same scale),
+// written as fp16 A fragments of mma.m16n8k16 in the decoders' coordinate order.
+template <int KB>
+__global__ void __launch_bounds__(kD) qfrag_kernel(MmaArgs m) {
+    __shared__ float q1[kRows][kD];
+    __shared__ float q2[kRows][kD];
+    __shared__ float qs[kD];
+    const DecodeArgs& a = m.a;
+    const int Hkv = a.pool.Hkv;
+    const int bh = blockIdx.x;
+    const int b = bh / Hkv, h = bh % Hkv;
+    const int rg = blockIdx.y;
+    const int RG = a.plan.row_groups;
+    const int unit = bh * RG + rg;
+    const int i = threadIdx.x;
+    const float s1 = a.scale * kLog2e;
+    const float s2 = s1 * kSqrtHalfPi / static_cast<float>(kD);
+    for (int rr = 0; rr < kRows; ++rr) {
+        const int r = rg * kRows + rr;
+        if (r >= a.plan.rows) {
+            q1[rr][i] = 0.0f;
+            q2[rr][i] = 0.0f;
+            continue;
+        }
+        const int g = r / a.Lq, l = r % a.Lq;
+        const int64_t src = ((static_cast<int64_t>(b) * a.Hq + h * a.G + g) * a.Lq + l) * kD + i;
+        float qv;
+        if (a.q_dtype == TQ_F32) qv = static_cast<const float*>(a.q)[src];
+        else if (a.q_dtype == TQ_BF16) qv = __bfloat162float(static_cast<const __nv_bfloat16*>(a.q)[src]);
+        else qv = __half2float(static_cast<const __half*>(a.q)[src]);
+        __syncthreads();
+        qs[i] = qv;
+        __syncthreads();
+        float t = 0.0f;
+        for (int k = 0; k < kD; ++k) t = fmaf(__ldg(a.kc.Rt + k * kD + i), qs[k], t);
+        q1[rr][i] = t;
+        __syncthreads();
+        float z = 0.0f;
+        if (a.kc.mode == TQ_MODE_PROD)
+            for (int k = 0; k < kD; ++k) z = fmaf(__ldg(a.kc.St + k * kD + i), q1[rr][k], z);
+        q2[rr][i] = z;
+    }
+    __syncthreads();
+    uint32_t* dst = reinterpret_cast<uint32_t*>(const_cast<uint4*>(m.qfrag)) + static_cast<int64_t>(unit) * 2 * 8 * 32 * 4;
+    for (int idx = i; idx < 2 * 8 * 32 * 4; idx += kD) {
+        const int reg = idx & 3;
+        const int lane = (idx >> 2) & 31;
+        const int ks = (idx >> 7) & 7;
+        const int which = idx >> 10;
+        const int g = lane >> 2, j = lane & 3;
+        const int row = (reg & 1) ? g + 8 : g;
+        const int e = reg >> 1;
+        int pa, pb;
+        mse_pair(which ? 1 : KB, 2 * ks + e, pa, pb);
+        const float* q = which ? q2[row] : q1[row];
+        const float sc = which ? s2 : s1;
+        dst[idx] = pack_half2(q[32 * j + pa] * sc, q[32 * j + pb] * sc);
+    }
+    if (i == 0) m.cnt[unit] = 0u;
+}
+
+// ------------------------------------------------------------------ split kernel
+
+template <int NW>
+__device__ __forceinline__ void load_words(const uint32_t* p, uint32_t (&w)[NW]) {
+    if constexpr (NW == 4) {
+        const uint4 v = *reinterpret_cast<const uint4*>(p);
+        w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
+    } else if constexpr (NW == 2) {
+        const uint2 v = *reinterpret_cast<const uint2*>(p);
+        w[0] = v.x; w[1] = v.y;
+    } else {
+#pragma unroll
+        for (int k = 0; k < NW; ++k) w[k] = p[k];
+    }
+}
+
+template <int B>
+struct MseTable {
+    using type = Tab8;
+};
+template <>
+struct MseTable<1> {
+    using type = Tab4;
+};
+template <>
+struct MseTable<2> {
+    using type = Tab4;
+};
+
+// Register tables for an MSE codebook of 2^B centroids.
+template <int B>
+__device__ inline typename MseTable<B>::type mse_table(const float* cg) {
+    float c[16];
+    for (int k = 0; k < (1 << B); ++k) c[k] = __ldg(cg + k);
+    if constexpr (B == 1) {
+        const uint32_t h = h_bits(c[0]);
+        return Tab4{h | (h << 16), 0u};
+    } else if constexpr (B == 2) {
+        return make_tab4(c);
+    } else if constexpr (B == 3) {
+        return make_tab8(c);
+    } else {
+        return make_tab8(c + 8);  // magnitudes of the positive half
+    }
+}
+
+template <int B>
+__device__ __forceinline__ void mse_chunk(const uint32_t* w, const typename MseTable<B>::type& t, uint32_t (&h)[16]) {
+    MseChunk<B>::run(w, t, h);
+}
+
+template <int KB, bool KPROD, bool VGROUP, int VB>
+__global__ void __launch_bounds__(kThreads, 1) split_mma_kernel(MmaArgs m) {
+    extern __shared__ __align__(128) unsigned char smem[];
+    const DecodeArgs& a = m.a;
+    const StageLayout& st = m.st;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = lane >> 2, j = lane & 3;
+    const int Hkv = a.pool.Hkv;
+    const int RG = a.plan.row_groups;
+    const int split = blockIdx.x;
+    const int h = blockIdx.y % Hkv;
+    const int rg = blockIdx.y / Hkv;
+    const int b = blockIdx.z;
+    const int unit = (b * Hkv + h) * RG + rg;
+    const int BT = a.pool.BT;
+    const int TT = st.tt;
+
+    unsigned char* ring = smem + static_cast<size_t>(warp) * kStages * st.bytes;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + st.bar_off) + warp * kStages;
+
+    const int N = a.seq_lens[b];
+    const bool bad = N < a.Lq || N > a.max_blocks * BT;
+    if (bad && split == 0 && threadIdx.x == 0 && rg == 0 && h == 0) atomicOr(a.err, TQ_DEVERR_SEQLEN);
+    const int t_begin = split * a.plan.chunk;
+    const int t_end = min(t_begin + a.plan.chunk, bad ? 0 : N);
+    const int ntiles = t_end > t_begin ? (t_end - t_begin + TT - 1) / TT : 0;
+    const int my_n = ntiles > warp ? (ntiles - warp + kWarps - 1) / kWarps : 0;
+
+    if (lane == 0) {
+        for (int s = 0; s < kStages; ++s) mbar_init(&bars[s], 1);
+        mbar_fence_init();
+    }
+    __syncwarp();
+
+    // query fragments
+    uint32_t qa[8][4];
+    uint32_t qj[KPROD ? 8 : 1][4];
+    {
+        const uint4* qf = m.qfrag + static_cast<int64_t>(unit) * 2 * 8 * 32;
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+            const uint4 v = qf[ks * 32 + lane];
+            qa[ks][0] = v.x; qa[ks][1] = v.y; qa[ks][2] = v.z; qa[ks][3] = v.w;
+        }
+        if constexpr (KPROD) {
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) {
+                const uint4 v = qf[(8 + ks) * 32 + lane];
+                qj[ks][0] = v.x; qj[ks][1] = v.y; qj[ks][2] = v.z; qj[ks][3] = v.w;
+            }
+        }
+    }
+    const auto ktab = mse_table<KB>(a.kc.c);
+    typename MseTable<VGROUP ? 2 : VB>::type vtab{};
+    if constexpr (!VGROUP) vtab = mse_table<VB>(a.vc.c);
+
+    // causal limits of this thread's two rows (padding rows see everything)
+    const int r0 = rg * kRows + g, r1 = r0 + 8;
+    const int lim0 = r0 < a.plan.rows ? N - a.Lq + (r0 % a.Lq) : N - 1;
+    const int lim1 = r1 < a.plan.rows ? N - a.Lq + (r1 % a.Lq) : N - 1;
+
+    float o[16][4];
+#pragma unroll
+    for (int p = 0; p < 16; ++p) o[p][0] = o[p][1] = o[p][2] = o[p][3] = 0.0f;
+    float mrow0 = -INFINITY, mrow1 = -INFINITY, lrow0 = 0.0f, lrow1 = 0.0f;
+    bool failed = false;
+
+    auto issue = [&](int i) {
+        const int t0 = t_begin + (warp + i * kWarps) * TT;
+        const int lb = t0 / BT;
+        const int slot0 = t0 - lb * BT;
+        int64_t pb = a.table ? static_cast<int64_t>(a.table[static_cast<int64_t>(b) * a.max_blocks + lb])
+                             : static_cast<int64_t>(b) * a.max_blocks + lb;
+        if (pb < 0 || pb >= a.pool.num_blocks) pb = 0;  // flagged and masked when computed
+        const char* base = a.pool.base + (pb * Hkv + h) * a.pool.sub_bytes;
+        unsigned char* dst = ring + static_cast<size_t>(i % kStages) * st.bytes;
+        uint64_t* bar = &bars[i % kStages];
+        if (lane == 0) {
+            unsigned total = 0;
+            for (int k = 0; k < 7; ++k)
+                if (st.off[k] >= 0) total += TT * st.field[k];
+            mbar_expect_tx(bar, total);
+            for (int k = 0; k < 7; ++k)
+                if (st.off[k] >= 0)
+                    bulk_g2s(dst + st.off[k], base + a.pool.off[k] + static_cast<int64_t>(slot0) * st.field[k],
+                             TT * st.field[k], bar);
+        }
+    };
+
+    const int pre = my_n < kStages - 1 ? my_n : kStages - 1;
+    for (int i = 0; i < pre; ++i) issue(i);
+    int waited = 0;
+    for (int i = 0; i < my_n; ++i) {
+        if (i + kStages - 1 < my_n) {
+            __syncwarp();
+            issue(i + kStages - 1);
+        }
+        if (!mbar_wait(&bars[i % kStages], (i / kStages) & 1)) {
+            failed = true;
+            break;
+        }
+        waited = i + 1;
+        const unsigned char* sp = ring + static_cast<size_t>(i % kStages) * st.bytes;
+        const uint32_t* kidx = reinterpret_cast<const uint32_t*>(sp + st.off[0]);
+        const uint32_t* ksgn = KPROD ? reinterpret_cast<const uint32_t*>(sp + st.off[1]) : nullptr;
+        const float* knorm = reinterpret_cast<const float*>(sp + st.off[2]);
+        const float* krn = KPROD ? reinterpret_cast<const float*>(sp + st.off[3]) : nullptr;
+        const uint32_t* vidx = reinterpret_cast<const uint32_t*>(sp + st.off[4]);
+        const float* vnorm = VGROUP ? nullptr : reinterpret_cast<const float*>(sp + st.off[5]);
+        const __half* vsc = VGROUP ? reinterpret_cast<const __half*>(sp + st.off[5]) : nullptr;
+        const __half* vmn = VGROUP ? reinterpret_cast<const __half*>(sp + st.off[6]) : nullptr;
+
+        const int t0 = t_begin + (warp + i * kWarps) * TT;
+        int valid = min(TT, t_end - t0);
+        {
+            const int lb = t0 / BT;
+            const int64_t pb = a.table ? static_cast<int64_t>(a.table[static_cast<int64_t>(b) * a.max_blocks + lb])
+                                       : static_cast<int64_t>(b) * a.max_blocks + lb;
+            if (pb < 0 || pb >= a.pool.num_blocks) {
+                if (lane == 0) atomicOr(a.err, TQ_DEVERR_BLOCK);
+                valid = 0;
+            }
+        }
+
+        for (int u = 0; u < TT / 16; ++u) {
+            if (16 * u >= valid) break;
+            // ---------------- scores for 16 tokens (two n8 tiles)
+            float sc[2][4];
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+                sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.0f;
+                const int tau = 16 * u + 8 * nt + g;
+                uint32_t kw[KB];
+                load_words<KB>(kidx + tau * (4 * KB) + j * KB, kw);
+                uint32_t hk[16];
+                mse_chunk<KB>(kw, ktab, hk);
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks) mma16816(sc[nt], qa[ks], hk[2 * ks], hk[2 * ks + 1]);
+                if constexpr (KPROD) {
+                    const uint32_t sw = ksgn[tau * 4 + j];
+                    const uint32_t hg = h_bits(-krn[tau]);
+                    const uint32_t neg2 = hg | (hg << 16);
+#pragma unroll
+                    for (int ks = 0; ks < 8; ++ks)
+                        mma16816(sc[nt], qj[ks], dec1(sw, 15 - ks, neg2), dec1(sw, 7 - ks, neg2));
+                }
+            }
+            // ---------------- scale, mask, online softmax (log2 domain)
+            float x[2][4];
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+                const int tl = 16 * u + 8 * nt + 2 * j;
+                const float2 kn = *reinterpret_cast<const float2*>(knorm + tl);
+                const int pos = t0 + tl;
+                const bool v0 = tl < valid, v1 = tl + 1 < valid;
+                x[nt][0] = (v0 && pos <= lim0) ? sc[nt][0] * kn.x : -INFINITY;
+                x[nt][1] = (v1 && pos + 1 <= lim0) ? sc[nt][1] * kn.y : -INFINITY;
+                x[nt][2] = (v0 && pos <= lim1) ? sc[nt][2] * kn.x : -INFINITY;
+                x[nt][3] = (v1 && pos + 1 <= lim1) ? sc[nt][3] * kn.y : -INFINITY;
+            }
+            float mx0 = fmaxf(fmaxf(x[0][0], x[0][1]), fmaxf(x[1][0], x[1][1]));
+            float mx1 = fmaxf(fmaxf(x[0][2], x[0][3]), fmaxf(x[1][2], x[1][3]));
+            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+            const float mn0 = fmaxf(mrow0, mx0), mn1 = fmaxf(mrow1, mx1);
+            if (__any_sync(0xffffffffu, mn0 != mrow0 || mn1 != mrow1)) {
+                const float al0 = mn0 == -INFINITY ? 1.0f : ex2(mrow0 - mn0);
+                const float al1 = mn1 == -INFINITY ? 1.0f : ex2(mrow1 - mn1);
+                lrow0 *= al0;
+                lrow1 *= al1;
+#pragma unroll
+                for (int p = 0; p < 16; ++p) {
+                    o[p][0] *= al0; o[p][1] *= al0;
+                    o[p][2] *= al1; o[p][3] *= al1;
+                }
+                mrow0 = mn0;
+                mrow1 = mn1;
+            }
+            float pr[2][4];
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+                pr[nt][0] = mrow0 == -INFINITY ? 0.0f : ex2(x[nt][0] - mrow0);
+                pr[nt][1] = mrow0 == -INFINITY ? 0.0f : ex2(x[nt][1] - mrow0);
+                pr[nt][2] = mrow1 == -INFINITY ? 0.0f : ex2(x[nt][2] - mrow1);
+                pr[nt][3] = mrow1 == -INFINITY ? 0.0f : ex2(x[nt][3] - mrow1);
+                lrow0 += pr[nt][0] + pr[nt][1];
+                lrow1 += pr[nt][2] + pr[nt][3];
+                if constexpr (!VGROUP) {
+                    const float2 nv = *reinterpret_cast<const float2*>(vnorm + 16 * u + 8 * nt + 2 * j);
+                    pr[nt][0] = pr[nt][0] != 0.0f ? pr[nt][0] * nv.x : 0.0f;
+                    pr[nt][1] = pr[nt][1] != 0.0f ? pr[nt][1] * nv.y : 0.0f;
+                    pr[nt][2] = pr[nt][2] != 0.0f ? pr[nt][2] * nv.x : 0.0f;
+                    pr[nt][3] = pr[nt][3] != 0.0f ? pr[nt][3] * nv.y : 0.0f;
+                }
+            }
+            uint32_t pa[4];
+            pa[0] = pack_half2(pr[0][0], pr[0][1]);
+            pa[1] = pack_half2(pr[0][2], pr[0][3]);
+            pa[2] = pack_half2(pr[1][0], pr[1][1]);
+            pa[3] = pack_half2(pr[1][2], pr[1][3]);
+            // ---------------- values: decode two tokens per thread, transpose, O += P' V
+            uint32_t hA[16], hB[16];
+            {
+                const int tA = 16 * u + g, tB = tA + 8;
+                uint32_t wA[VB], wB[VB];
+                load_words<VB>(vidx + tA * (4 * VB) + j * VB, wA);
+                load_words<VB>(vidx + tB * (4 * VB) + j * VB, wB);
+                if constexpr (VGROUP) {
+                    const int ng = kD / a.vc.group;
+                    const int gi = (32 * j) / a.vc.group;
+                    const float mulf = VB == 4 ? 16.0f : 4.0f;
+                    const bool okA = tA < valid, okB = tB < valid;
+                    const float sA = okA ? __half2float(vsc[tA * ng + gi]) : 0.0f;
+                    const float mA = okA ? __half2float(vmn[tA * ng + gi]) : 0.0f;
+                    const float sB = okB ? __half2float(vsc[tB * ng + gi]) : 0.0f;
+                    const float mB = okB ? __half2float(vmn[tB * ng + gi]) : 0.0f;
+                    const uint32_t mulA = pack_half2(sA * mulf, sA * mulf);
+                    const uint32_t addA = pack_half2(mA - sA * mulf, mA - sA * mulf);
+                    const uint32_t mulB = pack_half2(sB * mulf, sB * mulf);
+                    const uint32_t addB = pack_half2(mB - sB * mulf, mB - sB * mulf);
+                    GroupChunk<VB>::run(wA, mulA, addA, hA);
+                    GroupChunk<VB>::run(wB, mulB, addB, hB);
+                } else {
+                    mse_chunk<VB>(wA, vtab, hA);
+                    mse_chunk<VB>(wB, vtab, hB);
+                }
+            }
+#pragma unroll
+            for (int p = 0; p < 16; ++p) mma16816(o[p], pa, movmatrix_t(hA[p]), movmatrix_t(hB[p]));
+        }
+    }
+    if (failed && lane == 0) atomicOr(a.err, TQ_DEVERR_TIMEOUT);
+    // drain copies that were issued but never waited for (only after a timeout)
+    if (failed) {
+        const int issued = my_n < waited + kStages - 1 ? my_n : waited + kStages - 1;
+        for (int i = waited; i < issued; ++i) (void)mbar_wait(&bars[i % kStages], (i / kStages) & 1);
+    }
+
+    __syncwarp();
+    if (lane == 0)
+        for (int s = 0; s < kStages; ++s) mbar_inval(&bars[s]);
+
+    // ---------------- merge the warps of this CTA
+    lrow0 += __shfl_xor_sync(0xffffffffu, lrow0, 1);
+    lrow0 += __shfl_xor_sync(0xffffffffu, lrow0, 2);
+    lrow1 += __shfl_xor_sync(0xffffffffu, lrow1, 1);
+    lrow1 += __shfl_xor_sync(0xffffffffu, lrow1, 2);
+    __syncthreads();
+    constexpr int kStride = kD + 1;
+    float* cm = reinterpret_cast<float*>(smem);
+    float* cl = cm + kWarps * kRows;
+    float* co = cl + kWarps * kRows;
+    if (j == 0) {
+        cm[warp * kRows + g] = mrow0;
+        cm[warp * kRows + g + 8] = mrow1;
+        cl[warp * kRows + g] = lrow0;
+        cl[warp * kRows + g + 8] = lrow1;
+    }
+#pragma unroll
+    for (int p = 0; p < 16; ++p) {
+        int pa_, pb_;
+        if constexpr (VGROUP) group_pair(VB, p, pa_, pb_);
+        else mse_pair(VB, p, pa_, pb_);
+        const int d0 = 32 * j + pa_, d1 = 32 * j + pb_;
+        co[(warp * kRows + g) * kStride + d0] = o[p][0];
+        co[(warp * kRows + g) * kStride + d1] = o[p][1];
+        co[(warp * kRows + g + 8) * kStride + d0] = o[p][2];
+        co[(warp * kRows + g + 8) * kStride + d1] = o[p][3];
+    }
+    __syncthreads();
+    const int S = a.plan.splits;
+    const int tid = threadIdx.x;
+    const int r = tid >> 4;
+    const int dbase = (tid & 15) * 8;
+    {
+        float M = -INFINITY;
+        for (int w = 0; w < kWarps; ++w) M = fmaxf(M, cm[w * kRows + r]);
+        float L = 0.0f, acc[8] = {};
+        if (M != -INFINITY) {
+            for (int w = 0; w < kWarps; ++w) {
+                const float mw = cm[w * kRows + r];
+                if (mw == -INFINITY) continue;
+                const float wt = ex2(mw - M);
+                L = fmaf(wt, cl[w * kRows + r], L);
+                for (int k = 0; k < 8; ++k) acc[k] = fmaf(wt, co[(w * kRows + r) * kStride + dbase + k], acc[k]);
+            }
+        }
+        float* dst = m.part + ((static_cast<int64_t>(unit) * S + split) * kRows + r) * kD + dbase;
+        reinterpret_cast<float4*>(dst)[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+        reinterpret_cast<float4*>(dst)[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+        if ((tid & 15) == 0) {
+            float* mlp = m.ml + ((static_cast<int64_t>(unit) * S + split) * kRows + r) * 2;
+            mlp[0] = M;
+            mlp[1] = L;
+        }
+    }
+    // ---------------- the last CTA of this unit merges the splits
+    __threadfence();
+    __syncthreads();
+    __shared__ unsigned s_ticket;
+    if (tid == 0) s_ticket = atomicAdd(m.cnt + unit, 1u);
+    __syncthreads();
+    if (s_ticket != static_cast<unsigned>(S - 1)) return;
+    __threadfence();
+    float* orot = cm;  // [16][kStride]
+    {
+        float M = -INFINITY;
+        const float* mlu = m.ml + static_cast<int64_t>(unit) * S * kRows * 2;
+        for (int s = 0; s < S; ++s) M = fmaxf(M, __ldcg(mlu + (s * kRows + r) * 2));
+        float L = 0.0f, acc[8] = {};
+        if (M != -INFINITY) {
+            for (int s = 0; s < S; ++s) {
+                const float ms = __ldcg(mlu + (s * kRows + r) * 2);
+                if (ms == -INFINITY) continue;
+                const float wt = ex2(ms - M);
+                L = fmaf(wt, __ldcg(mlu + (s * kRows + r) * 2 + 1), L);
+                const float4* src = reinterpret_cast<const float4*>(
+                    m.part + ((static_cast<int64_t>(unit) * S + s) * kRows + r) * kD + dbase);
+                const float4 v0 = __ldcg(src), v1 = __ldcg(src + 1);
+                acc[0] = fmaf(wt, v0.x, acc[0]); acc[1] = fmaf(wt, v0.y, acc[1]);
+                acc[2] = fmaf(wt, v0.z, acc[2]); acc[3] = fmaf(wt, v0.w, acc[3]);
+                acc[4] = fmaf(wt, v1.x, acc[4]); acc[5] = fmaf(wt, v1.y, acc[5]);
+                acc[6] = fmaf(wt, v1.z, acc[6]); acc[7] = fmaf(wt, v1.w, acc[7]);
+            }
+        }
+        const float inv = L > 0.0f ? 1.0f / L : 0.0f;
+        for (int k = 0; k < 8; ++k) orot[r * kStride + dbase + k] = acc[k] * inv;
+    }
+    __syncthreads();
+    const int row = rg * kRows + r;
+    if (row < a.plan.rows) {
+        float res[8];
+        if constexpr (!VGROUP) {
+            for (int k = 0; k < 8; ++k) res[k] = 0.0f;
+            const float* R = a.vc.R;
+            for (int i2 = 0; i2 < kD; ++i2) {
+                const float ov = orot[r * kStride + i2];
+                const float4 r0 = __ldg(reinterpret_cast<const float4*>(R + i2 * kD + dbase));
+                const float4 r1 = __ldg(reinterpret_cast<const float4*>(R + i2 * kD + dbase) + 1);
+                res[0] = fmaf(ov, r0.x, res[0]); res[1] = fmaf(ov, r0.y, res[1]);
+                res[2] = fmaf(ov, r0.z, res[2]); res[3] = fmaf(ov, r0.w, res[3]);
+                res[4] = fmaf(ov, r1.x, res[4]); res[5] = fmaf(ov, r1.y, res[5]);
+                res[6] = fmaf(ov, r1.z, res[6]); res[7] = fmaf(ov, r1.w, res[7]);
+            }
+        } else {
+            for (int k = 0; k < 8; ++k) res[k] = orot[r * kStride + dbase + k];
+        }
+        const int gq = row / a.Lq, l = row % a.Lq;
+        float* dst = a.out + ((static_cast<int64_t>(b) * a.Hq + h * a.G + gq) * a.Lq + l) * kD + dbase;
+        reinterpret_cast<float4*>(dst)[0] = make_float4(res[0], res[1], res[2], res[3]);
+        reinterpret_cast<float4*>(dst)[1] = make_float4(res[4], res[5], res[6], res[7]);
+    }
+    if (tid == 0) m.cnt[unit] = 0u;
+}
+
+template <int KB, bool KPROD, bool VGROUP, int VB>
+cudaError_t launch_mma(const MmaArgs& m, size_t smem, cudaStream_t s) {
+    const DecodeArgs& a = m.a;
+    static std::atomic<uint64_t> attr_set{0};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const uint64_t bit = 1ull << (dev & 63);
+    if (!(attr_set.load() & bit)) {
+        cudaError_t e = cudaFuncSetAttribute(split_mma_kernel<KB, KPROD, VGROUP, VB>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+        if (e != cudaSuccess) return e;
+        attr_set.fetch_or(bit);
+    }
+    const int RG = a.plan.row_groups;
+    qfrag_kernel<KB><<<dim3(a.batch * a.pool.Hkv, RG), kD, 0, s>>>(m);
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    split_mma_kernel<KB, KPROD, VGROUP, VB>
+        <<<dim3(a.plan.splits, a.pool.Hkv * RG, a.batch), kThreads, smem, s>>>(m);
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    return cudaGetLastError();
+}
+
+}  // namespace mmadec
+}  // namespace tq

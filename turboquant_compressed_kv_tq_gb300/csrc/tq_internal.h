@@ -75,11 +75,21 @@ struct QuantizeArgs {
 
 // Decode plan shared by workspace sizing and the launch.
 struct DecodePlan {
+    int kind;         // 0: SIMT kernels (any shape), 1: tensor-core kernels (head_dim 128)
     int rows;         // G * Lq
     int row_groups;   // ceil(rows / 16)
     int splits;       // token splits per (sequence, kv head, row group)
     int chunk;        // tokens per split (multiple of the tile)
-    size_t q_bytes;   // prepared queries
+    int tile;         // tokens per tile / shared-memory stage
+    int kb, vb;       // key / value index bits (tensor-core path)
+    bool kprod, vgroup;
+    int st_off[7];    // stage layout (tensor-core path)
+    int st_field[7];
+    int st_bytes;
+    int bar_off;      // shared-memory offset of the stage barriers
+    size_t smem;      // dynamic shared memory of the split kernel
+    size_t q_bytes;   // SIMT: q' and q'' buffers (each); tensor cores: query fragments
+    size_t cnt_bytes; // tensor cores: per-unit arrival counters
     size_t part_bytes;// partial accumulators
     size_t ml_bytes;  // partial (max, sum)
     size_t total;
@@ -100,11 +110,12 @@ struct DecodeArgs {
     float* qjl;    // [B][Hkv][RG*16][D]
     float* part;   // [B][Hkv][RG][splits][16][D]
     float* ml;     // [B][Hkv][RG][splits][16][2]
+    void* ws;      // workspace base
     DecodePlan plan;
     unsigned* err;
 };
 
-DecodePlan make_decode_plan(int D, int batch, int Hkv, int G, int Lq, int max_seq_len, int num_sms);
+DecodePlan make_decode_plan(const tq_cache_desc* d, int batch, int G, int Lq, int max_seq_len, int num_sms);
 
 #ifdef __CUDACC__
 cudaError_t launch_encode_append(const EncodeAppendArgs& a, cudaStream_t s);
