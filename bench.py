@@ -127,35 +127,58 @@ def barrier(world: int):
         dist.barrier()
 
 
+def aggregate(bytes_per_step: float, step_ms_local: float, world: int, device=None):
+    """Whole-job throughput of `world` replicas: every rank processed
+    `bytes_per_step` per step; the job's step time is the slowest rank's.
+    Returns (GB/s over all ranks, max step ms)."""
+    step_ms = reduce_max(step_ms_local, world, device)
+    return world * bytes_per_step / (step_ms * 1e-3) / 1e9, step_ms
+
+
 # ------------------------------------------------------------------ oracle baseline
 
-def cpu_baseline(w, kv_heads=2, rows=16, device="cuda"):
-    """Time the oracle's decode on the host cores on a bounded sample: layer 0,
-    `kv_heads` KV heads at the full prefill length, all query rows of those
-    heads. Returns (GB/s of compressed bytes, cores, sample text, seconds)."""
-    import numpy as np
-    import torch
+class OracleSample:
+    """Oracle records of a bounded sample of the bench workload: layer 0,
+    `kv_heads` KV heads at the full prefill length (encoded once, by the
+    oracle, from the same device-generated inputs the GPU arm encodes)."""
 
-    import oracle as O
-    from turboquant_compressed_kv_tq_gb300 import workloads as wl
+    def __init__(self, w, kv_heads=1, device="cuda"):
+        import oracle as O
+        from turboquant_compressed_kv_tq_gb300 import workloads as wl
+        O.build()
+        self.O, self.w, self.kv_heads = O, w, kv_heads
+        D, N = w.head_dim, w.seq_lens[0]
+        self.kc = O.Codec(D, w.key.bits, w.key.mode, w.key.seed)
+        self.vc = O.Codec(D, w.value.bits, w.value.mode, w.value.seed)
+        K = wl.kv_chunk(w, 0, 0, 0, N, "k", device)[:kv_heads].float().cpu().numpy()
+        V = wl.kv_chunk(w, 0, 0, 0, N, "v", device)[:kv_heads].float().cpu().numpy()
+        self.q = wl.queries(w, 0, 0, device)[0].double().cpu().numpy()
+        self.recs = [(self.kc.encode(K[h]), self.vc.encode(V[h])) for h in range(kv_heads)]
+        self.nbytes = kv_heads * N * (self.kc.record_bytes + self.vc.record_bytes)
 
-    D = w.head_dim
-    N = w.seq_lens[0]
-    kc = O.Codec(D, w.key.bits, w.key.mode, w.key.seed)
-    vc = O.Codec(D, w.value.bits, w.value.mode, w.value.seed)
-    K = wl.kv_chunk(w, 0, 0, 0, N, "k", device)[:kv_heads].float().cpu().numpy()
-    V = wl.kv_chunk(w, 0, 0, 0, N, "v", device)[:kv_heads].float().cpu().numpy()
-    q = wl.queries(w, 0, 0, device)[0].double().cpu().numpy()
-    recs = [(kc.encode(K[h]), vc.encode(V[h])) for h in range(kv_heads)]
-    G = w.gqa
-    t0 = time.perf_counter()
-    for h in range(kv_heads):
-        O.decode_rotated(q[h * G:(h + 1) * G], kc, recs[h][0], vc, recs[h][1], 1 / math.sqrt(D), w.q_len)
-    dt = time.perf_counter() - t0
-    nbytes = kv_heads * N * (kc.record_bytes + vc.record_bytes)
-    sample = (f"oracle rotated-domain decode (fp64), layer 0, {kv_heads} KV heads x {G * w.q_len} "
-              f"query rows, N={N}, {nbytes / 1e6:.1f} MB of compressed records")
-    return nbytes / dt / 1e9, O.num_threads(), sample, dt
+    def decode_seconds(self):
+        """Wall time of the oracle's rotated-domain decode of the sample."""
+        w, G = self.w, self.w.gqa
+        t0 = time.perf_counter()
+        for h in range(self.kv_heads):
+            self.O.decode_rotated(self.q[h * G:(h + 1) * G], self.kc, self.recs[h][0], self.vc,
+                                  self.recs[h][1], 1 / math.sqrt(w.head_dim), w.q_len)
+        return time.perf_counter() - t0
+
+    def describe(self):
+        w = self.w
+        return (f"oracle rotated-domain decode (fp64, OpenMP over query rows), layer 0, "
+                f"{self.kv_heads} KV head(s) x {w.gqa * w.q_len} query rows, N={w.seq_lens[0]}, "
+                f"{self.nbytes / 1e6:.1f} MB of compressed records per sample")
+
+
+def cpu_baseline(w, kv_heads=2, device="cuda", repeats=3):
+    """Oracle decode throughput on the host cores (GB/s of compressed bytes),
+    median of `repeats` timed samples. Returns (value, cores, sample, seconds)."""
+    smp = OracleSample(w, kv_heads, device)
+    times = [smp.decode_seconds() for _ in range(repeats)]
+    t = statistics.median(times)
+    return smp.nbytes / t / 1e9, smp.O.num_threads(), smp.describe(), sum(times)
 
 
 def run_reference(args):
@@ -164,24 +187,20 @@ def run_reference(args):
         return 0
     import torch
     from turboquant_compressed_kv_tq_gb300 import workloads as wl
-    import oracle as O
-    O.build()
     w = wl.long_256k()
     dev = "cuda" if torch.cuda.is_available() else "cpu"
-    vals = []
-    cores = sample = None
-    for _ in range(max(1, args.warmup // 3)):
-        cpu_baseline(w, kv_heads=1, device=dev)
-    for _ in range(args.steps):
-        v, cores, sample, _ = cpu_baseline(w, kv_heads=1, device=dev)
-        vals.append(v)
-    val = statistics.median(vals)
+    smp = OracleSample(w, 1, dev)
+    for _ in range(args.warmup):
+        smp.decode_seconds()
+    times = [smp.decode_seconds() for _ in range(args.steps)]
+    total = sum(times)
+    val = smp.nbytes * args.steps / total / 1e9
     line = {"impl": "reference", "metric": METRIC, "value": val, "unit": UNIT, "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": _workload_text(w)},
-            "cpu_baseline": {"value": val, "unit": UNIT, "cores": cores, "kind": "oracle",
-                             "sample": sample},
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": _workload_text(w)},
+            "cpu_baseline": {"value": val, "unit": UNIT, "cores": smp.O.num_threads(), "kind": "oracle",
+                             "sample": smp.describe()},
             "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
@@ -290,12 +309,10 @@ def run_gpu(args):
     barrier(world)
     launches = tq.tq_launch_count() - n_launch0
     step_ms = t_start.elapsed_time(t_end) / args.steps
-    step_ms_max = reduce_max(step_ms, world, dev)
     # bytes the decode of step s reads: valid tokens x heads x layers x record bytes
-    dec_bytes = [sum(L * Hkv * (N0 + A * s + A) * rec_bytes for _ in [0])
-                 for s in range(args.warmup, total_steps)]
+    dec_bytes = [L * Hkv * (N0 + A * s + A) * rec_bytes for s in range(args.warmup, total_steps)]
     bytes_per_step = sum(dec_bytes) / args.steps
-    value = world * bytes_per_step / (step_ms_max * 1e-3) / 1e9
+    value, step_ms_max = aggregate(bytes_per_step, step_ms, world, dev)
 
     # ---------------- roofline pass: per-launch decode timing on the launching stream
     evs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
@@ -343,7 +360,7 @@ def run_gpu(args):
     if rank == 0:
         cpu = None
         if world == 1 and not args.no_cpu_baseline:
-            v, cores, sample, secs = cpu_baseline(w, device=dev)
+            v, cores, sample, secs = cpu_baseline(w, kv_heads=2, device=dev)
             cpu = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample,
                    "seconds": round(secs, 2)}
         clocks = clk.summary()
