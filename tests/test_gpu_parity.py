@@ -119,11 +119,21 @@ def _small_paged(name="small_paged", key=("prod", 3), value=("group", 4, 64), D=
                        prefill_chunk=64)
 
 
-@pytest.mark.parametrize("value", [("group", 4, 64), ("mse", 3), ("group", 2, 32)])
-def test_append_into_paged_pool_bit_exact(value):
-    w = _small_paged(value=value)
+@pytest.mark.parametrize("value,key,D,chunk,lens", [
+    (("group", 4, 64), ("prod", 3), 128, 24, (37, 100, 16, 1)),
+    (("mse", 3), ("prod", 3), 128, 24, (37, 100, 16, 1)),
+    (("group", 2, 32), ("prod", 3), 128, 24, (37, 100, 16, 1)),
+    # chunks of >= 32 tokens take the register-blocked encoder (ragged tails included)
+    (("mse", 3), ("prod", 3), 128, 300, (700, 45, 333)),
+    (("group", 4, 64), ("mse", 4), 128, 257, (600, 33)),
+    (("mse", 2), ("prod", 4), 64, 500, (530, 129)),
+    (("group", 2, 32), ("prod", 3), 256, 100, (230, 64)),
+    (("mse", 4), ("mse", 1), 256, 64, (100,)),
+])
+def test_append_into_paged_pool_bit_exact(value, key, D, chunk, lens):
+    w = _small_paged(value=value, key=key, D=D, lens=lens)
     case = GpuCase(w, layers=[0, 1], seq_lens=w.seq_lens)
-    case.prefill(chunk=24)          # several calls, crossing block boundaries
+    case.prefill(chunk=chunk)       # several calls, crossing block boundaries
     # incremental appends of `append_per_step` tokens at the written end
     B = w.batch
     n_new = w.append_per_step

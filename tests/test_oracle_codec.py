@@ -143,3 +143,15 @@ def test_codec_determinism_and_seed_separation(oracle_lib):
     # prod uses bits-1 index bits; its codebook is the (bits-1)-bit MSE codebook
     mse2 = O.Codec(128, 2, O.MSE, 5)
     assert a.ib == 2 and np.array_equal(a.c, mse2.c) and np.array_equal(a.R, mse2.R)
+
+
+@pytest.mark.parametrize("D,bits,mode", [(128, 3, O.PROD), (128, 4, O.MSE), (256, 3, O.MSE), (64, 1, O.MSE)])
+def test_stored_levels_are_nearest_halves(oracle_lib, D, bits, mode):
+    # the stored codebook is the IEEE half rounding of the fp64 Lloyd-Max levels
+    # and the thresholds are the exact midpoints of adjacent stored levels
+    cd = O.Codec(D, bits, mode, 1)
+    c64, _, _ = O.lloyd_max(D, cd.ib)
+    assert np.array_equal(cd.c.astype(np.float64), c64.astype(np.float16).astype(np.float64))
+    mid = (cd.c[:-1].astype(np.float64) + cd.c[1:].astype(np.float64)) / 2
+    assert np.array_equal(cd.m.astype(np.float64), mid)
+    assert np.array_equal(cd.c[::-1], -cd.c)

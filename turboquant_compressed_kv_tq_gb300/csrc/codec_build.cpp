@@ -10,7 +10,8 @@
 //   rotation: Householder QR of the Gaussian matrix (row-major fill), every
 //            sum in ascending index order without fused multiply-add, then
 //            the columns signed so that R's diagonal is positive;
-//   codebook: Lloyd iteration on (1-t^2)^((D-3)/2) over [-1, 1].
+//   codebook: Lloyd iteration on (1-t^2)^((D-3)/2) over [-1, 1], levels
+//            stored as the nearest half-precision numbers.
 // This file must be compiled without floating-point contraction.
 #include "tq_internal.h"
 
@@ -202,6 +203,15 @@ void lloyd_max_levels(int D, int b, std::vector<double>& c, std::vector<double>&
     for (int j = 0; j + 1 < L; ++j) m[j] = 0.5 * (c[j] + c[j + 1]);
 }
 
+// Nearest binary16 number to x, ties to even: spacing 2^(ilogb(x) - 10) in
+// the normal half range and 2^-24 below it.
+double nearest_half(double x) {
+    if (x == 0.0) return x;
+    int q = std::ilogb(x) - 10;
+    if (q < -24) q = -24;
+    return std::scalbn(std::nearbyint(std::scalbn(x, -q)), q);
+}
+
 }  // namespace
 
 void build_codec_tables(int D, int index_bits, bool with_qjl, uint64_t seed, HostTables& out) {
@@ -229,10 +239,15 @@ void build_codec_tables(int D, int index_bits, bool with_qjl, uint64_t seed, Hos
         out.qjl.resize(S.size());
         for (size_t i = 0; i < S.size(); ++i) out.qjl[i] = static_cast<float>(S[i]);
     }
+    // Stored levels: the nearest half-precision numbers to the fp64 levels
+    // (exact fp16 operands for the tensor-core decode); thresholds: exact
+    // midpoints of adjacent stored levels.
     out.centroids.resize(c.size());
-    for (size_t i = 0; i < c.size(); ++i) out.centroids[i] = static_cast<float>(c[i]);
+    for (size_t i = 0; i < c.size(); ++i) out.centroids[i] = static_cast<float>(nearest_half(c[i]));
     out.midpoints.resize(m.size());
-    for (size_t i = 0; i < m.size(); ++i) out.midpoints[i] = static_cast<float>(m[i]);
+    for (size_t i = 0; i < m.size(); ++i)
+        out.midpoints[i] = static_cast<float>((static_cast<double>(out.centroids[i]) +
+                                               static_cast<double>(out.centroids[i + 1])) * 0.5);
 }
 
 }  // namespace tq

@@ -308,7 +308,10 @@ cudaError_t launch_decode_d(const DecodeArgs& a, cudaStream_t s) {
     if (!(attr_set.load() & bit)) {
         cudaError_t e = cudaFuncSetAttribute(split_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              static_cast<int>(smem));
-        if (e != cudaSuccess) return e;
+        if (e != cudaSuccess) {
+            (void)cudaGetLastError();
+            return e;
+        }
         attr_set.fetch_or(bit);
     }
     split_kernel<D><<<dim3(a.plan.splits, Hkv * RG, B), kThreads, smem, s>>>(a);

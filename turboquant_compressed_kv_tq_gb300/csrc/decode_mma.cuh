@@ -308,9 +308,11 @@ __host__ __device__ inline void mse_pair(int bits, int p, int& a, int& b) {
     }
 }
 
-// Group-quantised values: q*scale + min through the fp16 exponent trick.
-// 4-bit: pair (i, i+4) of word wi -> p = 4*wi + i; value 1 + q/16 scaled by
-// 16*scale plus (min - 16*scale). 2-bit: pair (i, i+8) of word w -> p = 8*w + i.
+// Group-quantised values: q*scale + min with one rounding. The code is placed
+// in the mantissa of 1.0 (exact 1 + q/16 for 4 bits, 1 + q/4 for 2 bits), 1.0 is
+// subtracted exactly, and one fused multiply-add gives (q/16)*(16*scale) + min.
+// 4-bit: pair (i, i+4) of word wi -> p = 4*wi + i; 2-bit: pair (i, i+8) of
+// word w -> p = 8*w + i.
 __host__ __device__ inline void group_pair(int bits, int p, int& a, int& b) {
     if (bits == 4) {
         a = 8 * (p >> 2) + (p & 3);
@@ -337,7 +339,8 @@ struct GroupChunk<4> {
                 const int sh = 6 - 4 * i;
                 const uint32_t x = sh >= 0 ? (w[wi] << sh) : (w[wi] >> (-sh));
                 const uint32_t v = (x & 0x03C003C0u) | 0x3C003C00u;  // 1 + q/16 in each half
-                const __half2 r = __hfma2(*reinterpret_cast<const __half2*>(&v), m, c);
+                const __half2 f = __hsub2(*reinterpret_cast<const __half2*>(&v), __float2half2_rn(1.0f));
+                const __half2 r = __hfma2(f, m, c);
                 h[4 * wi + i] = *reinterpret_cast<const uint32_t*>(&r);
             }
         }
@@ -357,7 +360,8 @@ struct GroupChunk<2> {
                 const int sh = 8 - 2 * i;
                 const uint32_t x = sh >= 0 ? (w[wi] << sh) : (w[wi] >> (-sh));
                 const uint32_t v = (x & 0x03000300u) | 0x3C003C00u;  // 1 + q/4 in each half
-                const __half2 r = __hfma2(*reinterpret_cast<const __half2*>(&v), m, c);
+                const __half2 f = __hsub2(*reinterpret_cast<const __half2*>(&v), __float2half2_rn(1.0f));
+                const __half2 r = __hfma2(f, m, c);
                 h[8 * wi + i] = *reinterpret_cast<const uint32_t*>(&r);
             }
         }

@@ -31,6 +31,9 @@ struct MmaArgs {
 
 // q' = R_k q * scale * log2(e) and q'' = S_k q' * sqrt(pi/2)/D (same scale),
 // written as fp16 A fragments of mma.m16n8k16 in the decoders' coordinate order.
+// Slot 0 holds fp16(q'); slot 1 holds q'' for prod keys, and for MSE keys the
+// rounding remainder fp16(q' - fp16(q')), so that two MMAs against the exact
+// fp16 codebook operand carry q' to about 22 bits.
 template <int KB>
 __global__ void __launch_bounds__(kD) qfrag_kernel(MmaArgs m) {
     __shared__ float q1[kRows][kD];
@@ -82,10 +85,16 @@ __global__ void __launch_bounds__(kD) qfrag_kernel(MmaArgs m) {
         const int row = (reg & 1) ? g + 8 : g;
         const int e = reg >> 1;
         int pa, pb;
-        mse_pair(which ? 1 : KB, 2 * ks + e, pa, pb);
-        const float* q = which ? q2[row] : q1[row];
-        const float sc = which ? s2 : s1;
-        dst[idx] = pack_half2(q[32 * j + pa] * sc, q[32 * j + pb] * sc);
+        const bool qjl = which && a.kc.mode == TQ_MODE_PROD;
+        mse_pair(qjl ? 1 : KB, 2 * ks + e, pa, pb);
+        const float* q = qjl ? q2[row] : q1[row];
+        const float sc = qjl ? s2 : s1;
+        float va = q[32 * j + pa] * sc, vb = q[32 * j + pb] * sc;
+        if (which && !qjl) {
+            va -= __half2float(__float2half_rn(va));
+            vb -= __half2float(__float2half_rn(vb));
+        }
+        dst[idx] = pack_half2(va, vb);
     }
     if (i == 0) m.cnt[unit] = 0u;
 }
@@ -177,7 +186,7 @@ __global__ void __launch_bounds__(kThreads, 1) split_mma_kernel(MmaArgs m) {
 
     // query fragments
     uint32_t qa[8][4];
-    uint32_t qj[KPROD ? 8 : 1][4];
+    uint32_t qj[8][4];  // QJL query (prod keys) or low half of the split query (MSE keys)
     {
         const uint4* qf = m.qfrag + static_cast<int64_t>(unit) * 2 * 8 * 32;
 #pragma unroll
@@ -185,12 +194,10 @@ __global__ void __launch_bounds__(kThreads, 1) split_mma_kernel(MmaArgs m) {
             const uint4 v = qf[ks * 32 + lane];
             qa[ks][0] = v.x; qa[ks][1] = v.y; qa[ks][2] = v.z; qa[ks][3] = v.w;
         }
-        if constexpr (KPROD) {
 #pragma unroll
-            for (int ks = 0; ks < 8; ++ks) {
-                const uint4 v = qf[(8 + ks) * 32 + lane];
-                qj[ks][0] = v.x; qj[ks][1] = v.y; qj[ks][2] = v.z; qj[ks][3] = v.w;
-            }
+        for (int ks = 0; ks < 8; ++ks) {
+            const uint4 v = qf[(8 + ks) * 32 + lane];
+            qj[ks][0] = v.x; qj[ks][1] = v.y; qj[ks][2] = v.z; qj[ks][3] = v.w;
         }
     }
     const auto ktab = mse_table<KB>(a.kc.c);
@@ -279,6 +286,10 @@ __global__ void __launch_bounds__(kThreads, 1) split_mma_kernel(MmaArgs m) {
                 mse_chunk<KB>(kw, ktab, hk);
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks) mma16816(sc[nt], qa[ks], hk[2 * ks], hk[2 * ks + 1]);
+                if constexpr (!KPROD) {
+#pragma unroll
+                    for (int ks = 0; ks < 8; ++ks) mma16816(sc[nt], qj[ks], hk[2 * ks], hk[2 * ks + 1]);
+                }
                 if constexpr (KPROD) {
                     const uint32_t sw = ksgn[tau * 4 + j];
                     const uint32_t hg = h_bits(-krn[tau]);
@@ -328,21 +339,34 @@ __global__ void __launch_bounds__(kThreads, 1) split_mma_kernel(MmaArgs m) {
                 pr[nt][1] = mrow0 == -INFINITY ? 0.0f : ex2(x[nt][1] - mrow0);
                 pr[nt][2] = mrow1 == -INFINITY ? 0.0f : ex2(x[nt][2] - mrow1);
                 pr[nt][3] = mrow1 == -INFINITY ? 0.0f : ex2(x[nt][3] - mrow1);
-                lrow0 += pr[nt][0] + pr[nt][1];
-                lrow1 += pr[nt][2] + pr[nt][3];
+            }
+            // P' = fp16(p * value norm); the row sums add the weights actually
+            // multiplied (P' / norm), so the rounding of P' cancels in o = sum/L
+            // (a zero-norm value contributes its p directly).
+            uint32_t pa[4];
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+                float w0 = pr[nt][0], w1 = pr[nt][1], w2 = pr[nt][2], w3 = pr[nt][3];
+                float r0 = 1.0f, r1 = 1.0f;
                 if constexpr (!VGROUP) {
                     const float2 nv = *reinterpret_cast<const float2*>(vnorm + 16 * u + 8 * nt + 2 * j);
-                    pr[nt][0] = pr[nt][0] != 0.0f ? pr[nt][0] * nv.x : 0.0f;
-                    pr[nt][1] = pr[nt][1] != 0.0f ? pr[nt][1] * nv.y : 0.0f;
-                    pr[nt][2] = pr[nt][2] != 0.0f ? pr[nt][2] * nv.x : 0.0f;
-                    pr[nt][3] = pr[nt][3] != 0.0f ? pr[nt][3] * nv.y : 0.0f;
+                    const bool z0 = !(nv.x > 0.0f), z1 = !(nv.y > 0.0f);
+                    r0 = z0 ? 0.0f : __frcp_rn(nv.x);
+                    r1 = z1 ? 0.0f : __frcp_rn(nv.y);
+                    w0 = (w0 != 0.0f && !z0) ? w0 * nv.x : 0.0f;
+                    w1 = (w1 != 0.0f && !z1) ? w1 * nv.y : 0.0f;
+                    w2 = (w2 != 0.0f && !z0) ? w2 * nv.x : 0.0f;
+                    w3 = (w3 != 0.0f && !z1) ? w3 * nv.y : 0.0f;
+                    if (z0) { lrow0 += pr[nt][0]; lrow1 += pr[nt][2]; }
+                    if (z1) { lrow0 += pr[nt][1]; lrow1 += pr[nt][3]; }
                 }
+                pa[2 * nt] = pack_half2(w0, w1);
+                pa[2 * nt + 1] = pack_half2(w2, w3);
+                const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&pa[2 * nt]));
+                const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&pa[2 * nt + 1]));
+                lrow0 += f0.x * r0 + f0.y * r1;
+                lrow1 += f1.x * r0 + f1.y * r1;
             }
-            uint32_t pa[4];
-            pa[0] = pack_half2(pr[0][0], pr[0][1]);
-            pa[1] = pack_half2(pr[0][2], pr[0][3]);
-            pa[2] = pack_half2(pr[1][0], pr[1][1]);
-            pa[3] = pack_half2(pr[1][2], pr[1][3]);
             // ---------------- values: decode two tokens per thread, transpose, O += P' V
             uint32_t hA[16], hB[16];
             {
@@ -360,9 +384,9 @@ __global__ void __launch_bounds__(kThreads, 1) split_mma_kernel(MmaArgs m) {
                     const float sB = okB ? __half2float(vsc[tB * ng + gi]) : 0.0f;
                     const float mB = okB ? __half2float(vmn[tB * ng + gi]) : 0.0f;
                     const uint32_t mulA = pack_half2(sA * mulf, sA * mulf);
-                    const uint32_t addA = pack_half2(mA - sA * mulf, mA - sA * mulf);
+                    const uint32_t addA = pack_half2(mA, mA);
                     const uint32_t mulB = pack_half2(sB * mulf, sB * mulf);
-                    const uint32_t addB = pack_half2(mB - sB * mulf, mB - sB * mulf);
+                    const uint32_t addB = pack_half2(mB, mB);
                     GroupChunk<VB>::run(wA, mulA, addA, hA);
                     GroupChunk<VB>::run(wB, mulB, addB, hB);
                 } else {
@@ -502,15 +526,29 @@ template <int KB, bool KPROD, bool VGROUP, int VB>
 cudaError_t launch_mma(const MmaArgs& m, size_t smem, cudaStream_t s) {
     const DecodeArgs& a = m.a;
     static std::atomic<uint64_t> attr_set{0};
+    static std::atomic<int> max_dyn[64];
     int dev = 0;
     cudaGetDevice(&dev);
     const uint64_t bit = 1ull << (dev & 63);
     if (!(attr_set.load() & bit)) {
-        cudaError_t e = cudaFuncSetAttribute(split_mma_kernel<KB, KPROD, VGROUP, VB>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-        if (e != cudaSuccess) return e;
+        // opt in once to the largest dynamic size the device allows next to the
+        // kernel's static shared memory: later calls may need larger stages
+        int optin = 0;
+        cudaFuncAttributes fa{};
+        cudaError_t e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+        if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, split_mma_kernel<KB, KPROD, VGROUP, VB>);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(split_mma_kernel<KB, KPROD, VGROUP, VB>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     optin - static_cast<int>(fa.sharedSizeBytes));
+        if (e != cudaSuccess) {
+            (void)cudaGetLastError();  // do not leave the error for the next launch
+            return e;
+        }
         attr_set.fetch_or(bit);
+        max_dyn[dev & 63].store(optin - static_cast<int>(fa.sharedSizeBytes));
     }
+    if (static_cast<int>(smem) > max_dyn[dev & 63].load()) return cudaErrorInvalidValue;
     const int RG = a.plan.row_groups;
     qfrag_kernel<KB><<<dim3(a.batch * a.pool.Hkv, RG), kD, 0, s>>>(m);
     g_launches.fetch_add(1, std::memory_order_relaxed);

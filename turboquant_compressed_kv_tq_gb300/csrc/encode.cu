@@ -123,12 +123,13 @@ __device__ void encode_vector(const CodecDev& cd, VecSmem& sm, const RecordOut& 
     }
 }
 
-__global__ void encode_append_kernel(EncodeAppendArgs a) {
+// which: 0 = keys and values (grid z = 2 * batch), 1 = keys only, 2 = values only.
+__global__ void encode_append_kernel(EncodeAppendArgs a, int which) {
     __shared__ VecSmem sm;
     const int t = blockIdx.x;
     const int h = blockIdx.y;
-    const int bq = blockIdx.z >> 1;
-    const bool is_v = blockIdx.z & 1;
+    const int bq = which == 0 ? (blockIdx.z >> 1) : blockIdx.z;
+    const bool is_v = which == 0 ? (blockIdx.z & 1) : which == 2;
     const CodecDev& cd = is_v ? a.vc : a.kc;
     const int D = cd.D;
     const int i = threadIdx.x;
@@ -201,10 +202,24 @@ __global__ void quantize_kernel(QuantizeArgs a) {
 
 cudaError_t launch_encode_append(const EncodeAppendArgs& a, cudaStream_t s) {
     if (a.batch == 0 || a.n_new == 0) return cudaSuccess;
-    dim3 grid(a.n_new, a.pool.Hkv, a.batch * 2);
-    encode_append_kernel<<<grid, a.kc.D, 0, s>>>(a);
-    g_launches.fetch_add(1, std::memory_order_relaxed);
-    return cudaGetLastError();
+    // Short appends (decode steps): one CTA per vector. Long appends (prefill
+    // chunks): the register-blocked kernel for rotated codecs.
+    constexpr int kBlockedFrom = 32;
+    if (a.n_new < kBlockedFrom) {
+        dim3 grid(a.n_new, a.pool.Hkv, a.batch * 2);
+        encode_append_kernel<<<grid, a.kc.D, 0, s>>>(a, 0);
+        g_launches.fetch_add(1, std::memory_order_relaxed);
+        return cudaGetLastError();
+    }
+    cudaError_t e = launch_encode_block(a, 0, s);
+    if (e != cudaSuccess) return e;
+    if (a.vc.mode == TQ_MODE_GROUP) {
+        dim3 grid(a.n_new, a.pool.Hkv, a.batch);
+        encode_append_kernel<<<grid, a.vc.D, 0, s>>>(a, 2);
+        g_launches.fetch_add(1, std::memory_order_relaxed);
+        return cudaGetLastError();
+    }
+    return launch_encode_block(a, 1, s);
 }
 
 cudaError_t launch_quantize(const QuantizeArgs& a, cudaStream_t s) {

@@ -119,6 +119,7 @@ DecodePlan make_decode_plan(const tq_cache_desc* d, int batch, int G, int Lq, in
 
 #ifdef __CUDACC__
 cudaError_t launch_encode_append(const EncodeAppendArgs& a, cudaStream_t s);
+cudaError_t launch_encode_block(const EncodeAppendArgs& a, int is_v, cudaStream_t s);
 cudaError_t launch_quantize(const QuantizeArgs& a, cudaStream_t s);
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);
 #endif
