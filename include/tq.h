@@ -262,6 +262,33 @@ tq_status tq_decode_attention(const tq_codec *key_codec, const tq_codec *value_c
                               int max_seq_len, float scale, float *out, void *workspace,
                               size_t workspace_bytes, tq_stream_t stream);
 
+/*
+ * Decode attention without a caller-provided workspace. (The pages have no
+ * counterpart; this exists for callers of this library.)
+ *
+ * For callers that cannot allocate device memory: hosts that own all of the
+ * GPU's memory and expose no allocator to plug-ins, and serving loops that must
+ * not allocate once running (an allocation can block on the device or fail
+ * under memory pressure mid-request). Arguments and results are those of
+ * tq_decode_attention; the scratch it needs lives instead in a fixed device
+ * array of TQ_NOALLOC_SCRATCH_BYTES that every GPU loading this library keeps
+ * until the process exits. Nothing is allocated by this call.
+ *   - Returns TQ_ERR_CAPACITY when tq_decode_workspace_bytes() for these sizes
+ *     exceeds TQ_NOALLOC_SCRATCH_BYTES (use tq_decode_attention instead).
+ *   - The first call on a device looks up the array's device address (with
+ *     that device current); make that first call before any stream capture.
+ *   - All calls on a device share the one array, which keeps the last call's
+ *     contents: calls that overlap on the GPU (other streams, or other host
+ *     threads) race and corrupt each other's results. Serialise them.
+ */
+#define TQ_NOALLOC_SCRATCH_BYTES (16u << 20)
+tq_status tq_decode_attention_noalloc(const tq_codec *key_codec, const tq_codec *value_codec,
+                                      const tq_cache_desc *cache, int layer, const void *q,
+                                      tq_dtype q_dtype, int batch, int num_q_heads, int q_len,
+                                      const int32_t *seq_lens, const int32_t *block_table,
+                                      int max_blocks, int max_seq_len, float scale, float *out,
+                                      tq_stream_t stream);
+
 /* ------------------------------------------------------------------ */
 /* Diagnostics                                                          */
 /* ------------------------------------------------------------------ */

@@ -19,7 +19,8 @@ from ._lib import (TQ_BF16, TQ_DEVERR_BLOCK, TQ_DEVERR_CAPACITY, TQ_DEVERR_SEQLE
 __all__ = [
     "tq_codec_create", "tq_codec_create_group", "tq_codec_destroy", "tq_codec_info",
     "tq_codec_build_host", "tq_codec_export", "tq_cache_desc_init", "tq_encode_append",
-    "tq_quantize", "tq_decode_workspace_bytes", "tq_decode_attention", "tq_device_error",
+    "tq_quantize", "tq_decode_workspace_bytes", "tq_decode_attention", "tq_decode_attention_noalloc",
+    "tq_device_error",
     "tq_launch_count", "tq_abi_version", "Codec", "CompressedKVCache", "TQError",
     "TQ_MODE_MSE", "TQ_MODE_PROD", "TQ_MODE_GROUP", "TQ_F32", "TQ_BF16", "TQ_F16",
 ]
@@ -160,6 +161,18 @@ def tq_decode_attention(key_codec: int, value_codec: int, desc: tq_cache_desc, l
                                     _dtype_code(q), batch, hq, lq, _ptr(seq_lens), _ptr(block_table),
                                     max_blocks, max_seq_len, scale, _ptr(out), _ptr(workspace),
                                     ws_bytes, _stream(stream)), "tq_decode_attention")
+
+
+def tq_decode_attention_noalloc(key_codec: int, value_codec: int, desc: tq_cache_desc, layer: int, q,
+                                seq_lens, block_table, max_blocks: int, max_seq_len: int, out,
+                                scale: float = 0.0, stream=None) -> None:
+    """tq_decode_attention with its scratch in the library's fixed device array
+    (for callers that cannot allocate device memory); see include/tq.h."""
+    batch, hq, lq, _ = q.shape
+    check(lib().tq_decode_attention_noalloc(key_codec, value_codec, ctypes.byref(desc), layer, _ptr(q),
+                                            _dtype_code(q), batch, hq, lq, _ptr(seq_lens),
+                                            _ptr(block_table), max_blocks, max_seq_len, scale, _ptr(out),
+                                            _stream(stream)), "tq_decode_attention_noalloc")
 
 
 def tq_device_error() -> int:

@@ -34,6 +34,8 @@ TQ_DEVERR_BLOCK = 2
 TQ_DEVERR_SEQLEN = 4
 TQ_DEVERR_TIMEOUT = 8
 
+TQ_NOALLOC_SCRATCH_BYTES = 16 << 20
+
 
 class TQError(RuntimeError):
     def __init__(self, status: int, what: str):
@@ -87,6 +89,8 @@ SIGNATURES = {
                                         ctypes.POINTER(_SZ)]),
     "tq_decode_attention": (_ST, [_P, _P, ctypes.POINTER(tq_cache_desc), _I, _P, _I, _I, _I, _I, _P,
                                   _P, _I, _I, _F, _P, _P, _SZ, _P]),
+    "tq_decode_attention_noalloc": (_ST, [_P, _P, ctypes.POINTER(tq_cache_desc), _I, _P, _I, _I, _I, _I,
+                                          _P, _P, _I, _I, _F, _P, _P]),
     "tq_device_error": (_ST, [ctypes.POINTER(ctypes.c_uint32)]),
 }
 
