@@ -36,67 +36,63 @@ struct MmaArgs {
 // fp16 codebook operand carry q' to about 22 bits.
 template <int KB>
 __global__ void __launch_bounds__(kD) qfrag_kernel(MmaArgs m) {
-    __shared__ float q1[kRows][kD];
-    __shared__ float q2[kRows][kD];
+    // one CTA per (sequence x kv head, row group, row): the row's q' and q''
+    // in fp32, then the 128 fragment registers that hold this row
+    __shared__ float q1[kD];
+    __shared__ float q2[kD];
     __shared__ float qs[kD];
     const DecodeArgs& a = m.a;
     const int Hkv = a.pool.Hkv;
     const int bh = blockIdx.x;
     const int b = bh / Hkv, h = bh % Hkv;
     const int rg = blockIdx.y;
+    const int rr = blockIdx.z;
     const int RG = a.plan.row_groups;
     const int unit = bh * RG + rg;
     const int i = threadIdx.x;
     const float s1 = a.scale * kLog2e;
     const float s2 = s1 * kSqrtHalfPi / static_cast<float>(kD);
-    for (int rr = 0; rr < kRows; ++rr) {
-        const int r = rg * kRows + rr;
-        if (r >= a.plan.rows) {
-            q1[rr][i] = 0.0f;
-            q2[rr][i] = 0.0f;
-            continue;
-        }
+    const int r = rg * kRows + rr;
+    if (r < a.plan.rows) {
         const int g = r / a.Lq, l = r % a.Lq;
         const int64_t src = ((static_cast<int64_t>(b) * a.Hq + h * a.G + g) * a.Lq + l) * kD + i;
-        float qv;
-        if (a.q_dtype == TQ_F32) qv = static_cast<const float*>(a.q)[src];
-        else if (a.q_dtype == TQ_BF16) qv = __bfloat162float(static_cast<const __nv_bfloat16*>(a.q)[src]);
-        else qv = __half2float(static_cast<const __half*>(a.q)[src]);
-        __syncthreads();
-        qs[i] = qv;
+        if (a.q_dtype == TQ_F32) qs[i] = static_cast<const float*>(a.q)[src];
+        else if (a.q_dtype == TQ_BF16) qs[i] = __bfloat162float(static_cast<const __nv_bfloat16*>(a.q)[src]);
+        else qs[i] = __half2float(static_cast<const __half*>(a.q)[src]);
         __syncthreads();
         float t = 0.0f;
+#pragma unroll 32
         for (int k = 0; k < kD; ++k) t = fmaf(__ldg(a.kc.Rt + k * kD + i), qs[k], t);
-        q1[rr][i] = t;
+        q1[i] = t;
         __syncthreads();
         float z = 0.0f;
-        if (a.kc.mode == TQ_MODE_PROD)
-            for (int k = 0; k < kD; ++k) z = fmaf(__ldg(a.kc.St + k * kD + i), q1[rr][k], z);
-        q2[rr][i] = z;
+        if (a.kc.mode == TQ_MODE_PROD) {
+#pragma unroll 32
+            for (int k = 0; k < kD; ++k) z = fmaf(__ldg(a.kc.St + k * kD + i), q1[k], z);
+        }
+        q2[i] = z;
+    } else {
+        q1[i] = 0.0f;
+        q2[i] = 0.0f;
     }
     __syncthreads();
-    uint32_t* dst = reinterpret_cast<uint32_t*>(const_cast<uint4*>(m.qfrag)) + static_cast<int64_t>(unit) * 2 * 8 * 32 * 4;
-    for (int idx = i; idx < 2 * 8 * 32 * 4; idx += kD) {
-        const int reg = idx & 3;
-        const int lane = (idx >> 2) & 31;
-        const int ks = (idx >> 7) & 7;
-        const int which = idx >> 10;
-        const int g = lane >> 2, j = lane & 3;
-        const int row = (reg & 1) ? g + 8 : g;
-        const int e = reg >> 1;
-        int pa, pb;
-        const bool qjl = which && a.kc.mode == TQ_MODE_PROD;
-        mse_pair(qjl ? 1 : KB, 2 * ks + e, pa, pb);
-        const float* q = qjl ? q2[row] : q1[row];
-        const float sc = qjl ? s2 : s1;
-        float va = q[32 * j + pa] * sc, vb = q[32 * j + pb] * sc;
-        if (which && !qjl) {
-            va -= __half2float(__float2half_rn(va));
-            vb -= __half2float(__float2half_rn(vb));
-        }
-        dst[idx] = pack_half2(va, vb);
+    // entry (which, ks, j, e) of this row: lane 4*(rr%8)+j, register 2e + (rr >= 8)
+    const int which = i >> 6, ks = (i >> 3) & 7, j = (i >> 1) & 3, e = i & 1;
+    const int lane = 4 * (rr & 7) + j;
+    const int reg = 2 * e + (rr >= 8 ? 1 : 0);
+    int pa, pb;
+    const bool qjl = which && a.kc.mode == TQ_MODE_PROD;
+    mse_pair(qjl ? 1 : KB, 2 * ks + e, pa, pb);
+    const float* q = qjl ? q2 : q1;
+    const float sc = qjl ? s2 : s1;
+    float va = q[32 * j + pa] * sc, vb = q[32 * j + pb] * sc;
+    if (which && !qjl) {
+        va -= __half2float(__float2half_rn(va));
+        vb -= __half2float(__float2half_rn(vb));
     }
-    if (i == 0) m.cnt[unit] = 0u;
+    uint32_t* dst = reinterpret_cast<uint32_t*>(const_cast<uint4*>(m.qfrag)) + static_cast<int64_t>(unit) * 2 * 8 * 32 * 4;
+    dst[((which * 8 + ks) * 32 + lane) * 4 + reg] = pack_half2(va, vb);
+    if (i == 0 && rr == 0) m.cnt[unit] = 0u;
 }
 
 // ------------------------------------------------------------------ split kernel
@@ -275,28 +271,66 @@ __global__ void __launch_bounds__(kThreads, 1) split_mma_kernel(MmaArgs m) {
         for (int u = 0; u < TT / 16; ++u) {
             if (16 * u >= valid) break;
             // ---------------- scores for 16 tokens (two n8 tiles)
-            float sc[2][4];
+            // two n8 tiles x two independent accumulator chains (codebook part;
+            // QJL part or low half of the split query) keep four MMAs in flight
+            float sc[2][4], sd[2][4];
+            uint32_t hk[2][16];
+            uint32_t sw[2], neg2[2];
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt) {
                 sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.0f;
+                sd[nt][0] = sd[nt][1] = sd[nt][2] = sd[nt][3] = 0.0f;
                 const int tau = 16 * u + 8 * nt + g;
                 uint32_t kw[KB];
                 load_words<KB>(kidx + tau * (4 * KB) + j * KB, kw);
-                uint32_t hk[16];
-                mse_chunk<KB>(kw, ktab, hk);
-#pragma unroll
-                for (int ks = 0; ks < 8; ++ks) mma16816(sc[nt], qa[ks], hk[2 * ks], hk[2 * ks + 1]);
-                if constexpr (!KPROD) {
-#pragma unroll
-                    for (int ks = 0; ks < 8; ++ks) mma16816(sc[nt], qj[ks], hk[2 * ks], hk[2 * ks + 1]);
-                }
+                mse_chunk<KB>(kw, ktab, hk[nt]);
                 if constexpr (KPROD) {
-                    const uint32_t sw = ksgn[tau * 4 + j];
+                    sw[nt] = ksgn[tau * 4 + j];
                     const uint32_t hg = h_bits(-krn[tau]);
-                    const uint32_t neg2 = hg | (hg << 16);
+                    neg2[nt] = hg | (hg << 16);
+                }
+            }
 #pragma unroll
-                    for (int ks = 0; ks < 8; ++ks)
-                        mma16816(sc[nt], qj[ks], dec1(sw, 15 - ks, neg2), dec1(sw, 7 - ks, neg2));
+            for (int ks = 0; ks < 8; ++ks) {
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt) {
+                    mma16816(sc[nt], qa[ks], hk[nt][2 * ks], hk[nt][2 * ks + 1]);
+                    if constexpr (KPROD)
+                        mma16816(sd[nt], qj[ks], dec1(sw[nt], 15 - ks, neg2[nt]), dec1(sw[nt], 7 - ks, neg2[nt]));
+                    else
+                        mma16816(sd[nt], qj[ks], hk[nt][2 * ks], hk[nt][2 * ks + 1]);
+                }
+            }
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) sc[nt][e] += sd[nt][e];
+            // ---------------- values of the same 16 tokens: decoded while the score MMAs
+            // are in flight (independent of the scores)
+            uint32_t hA[16], hB[16];
+            {
+                const int tA = 16 * u + g, tB = tA + 8;
+                uint32_t wA[VB], wB[VB];
+                load_words<VB>(vidx + tA * (4 * VB) + j * VB, wA);
+                load_words<VB>(vidx + tB * (4 * VB) + j * VB, wB);
+                if constexpr (VGROUP) {
+                    const int ng = kD / a.vc.group;
+                    const int gi = (32 * j) / a.vc.group;
+                    const float mulf = VB == 4 ? 16.0f : 4.0f;
+                    const bool okA = tA < valid, okB = tB < valid;
+                    const float sA = okA ? __half2float(vsc[tA * ng + gi]) : 0.0f;
+                    const float mA = okA ? __half2float(vmn[tA * ng + gi]) : 0.0f;
+                    const float sB = okB ? __half2float(vsc[tB * ng + gi]) : 0.0f;
+                    const float mB = okB ? __half2float(vmn[tB * ng + gi]) : 0.0f;
+                    const uint32_t mulA = pack_half2(sA * mulf, sA * mulf);
+                    const uint32_t addA = pack_half2(mA, mA);
+                    const uint32_t mulB = pack_half2(sB * mulf, sB * mulf);
+                    const uint32_t addB = pack_half2(mB, mB);
+                    GroupChunk<VB>::run(wA, mulA, addA, hA);
+                    GroupChunk<VB>::run(wB, mulB, addB, hB);
+                } else {
+                    mse_chunk<VB>(wA, vtab, hA);
+                    mse_chunk<VB>(wB, vtab, hB);
                 }
             }
             // ---------------- scale, mask, online softmax (log2 domain)
@@ -351,8 +385,8 @@ __global__ void __launch_bounds__(kThreads, 1) split_mma_kernel(MmaArgs m) {
                 if constexpr (!VGROUP) {
                     const float2 nv = *reinterpret_cast<const float2*>(vnorm + 16 * u + 8 * nt + 2 * j);
                     const bool z0 = !(nv.x > 0.0f), z1 = !(nv.y > 0.0f);
-                    r0 = z0 ? 0.0f : __frcp_rn(nv.x);
-                    r1 = z1 ? 0.0f : __frcp_rn(nv.y);
+                    r0 = z0 ? 0.0f : __fdividef(1.0f, nv.x);
+                    r1 = z1 ? 0.0f : __fdividef(1.0f, nv.y);
                     w0 = (w0 != 0.0f && !z0) ? w0 * nv.x : 0.0f;
                     w1 = (w1 != 0.0f && !z1) ? w1 * nv.y : 0.0f;
                     w2 = (w2 != 0.0f && !z0) ? w2 * nv.x : 0.0f;
@@ -366,33 +400,6 @@ __global__ void __launch_bounds__(kThreads, 1) split_mma_kernel(MmaArgs m) {
                 const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&pa[2 * nt + 1]));
                 lrow0 += f0.x * r0 + f0.y * r1;
                 lrow1 += f1.x * r0 + f1.y * r1;
-            }
-            // ---------------- values: decode two tokens per thread, transpose, O += P' V
-            uint32_t hA[16], hB[16];
-            {
-                const int tA = 16 * u + g, tB = tA + 8;
-                uint32_t wA[VB], wB[VB];
-                load_words<VB>(vidx + tA * (4 * VB) + j * VB, wA);
-                load_words<VB>(vidx + tB * (4 * VB) + j * VB, wB);
-                if constexpr (VGROUP) {
-                    const int ng = kD / a.vc.group;
-                    const int gi = (32 * j) / a.vc.group;
-                    const float mulf = VB == 4 ? 16.0f : 4.0f;
-                    const bool okA = tA < valid, okB = tB < valid;
-                    const float sA = okA ? __half2float(vsc[tA * ng + gi]) : 0.0f;
-                    const float mA = okA ? __half2float(vmn[tA * ng + gi]) : 0.0f;
-                    const float sB = okB ? __half2float(vsc[tB * ng + gi]) : 0.0f;
-                    const float mB = okB ? __half2float(vmn[tB * ng + gi]) : 0.0f;
-                    const uint32_t mulA = pack_half2(sA * mulf, sA * mulf);
-                    const uint32_t addA = pack_half2(mA, mA);
-                    const uint32_t mulB = pack_half2(sB * mulf, sB * mulf);
-                    const uint32_t addB = pack_half2(mB, mB);
-                    GroupChunk<VB>::run(wA, mulA, addA, hA);
-                    GroupChunk<VB>::run(wB, mulB, addB, hB);
-                } else {
-                    mse_chunk<VB>(wA, vtab, hA);
-                    mse_chunk<VB>(wB, vtab, hB);
-                }
             }
 #pragma unroll
             for (int p = 0; p < 16; ++p) mma16816(o[p], pa, movmatrix_t(hA[p]), movmatrix_t(hB[p]));
@@ -550,7 +557,7 @@ cudaError_t launch_mma(const MmaArgs& m, size_t smem, cudaStream_t s) {
     }
     if (static_cast<int>(smem) > max_dyn[dev & 63].load()) return cudaErrorInvalidValue;
     const int RG = a.plan.row_groups;
-    qfrag_kernel<KB><<<dim3(a.batch * a.pool.Hkv, RG), kD, 0, s>>>(m);
+    qfrag_kernel<KB><<<dim3(a.batch * a.pool.Hkv, RG, kRows), kD, 0, s>>>(m);
     g_launches.fetch_add(1, std::memory_order_relaxed);
     split_mma_kernel<KB, KPROD, VGROUP, VB>
         <<<dim3(a.plan.splits, a.pool.Hkv * RG, a.batch), kThreads, smem, s>>>(m);

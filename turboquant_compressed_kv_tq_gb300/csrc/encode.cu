@@ -86,6 +86,7 @@ __device__ void encode_vector(const CodecDev& cd, VecSmem& sm, const RecordOut& 
         for (int k = 0; k < D; ++k) n2 = __fmaf_rn(sm.x[k], sm.x[k], n2);
         const float n = __fsqrt_rn(n2);
         float t = 0.0f;
+#pragma unroll 32
         for (int k = 0; k < D; ++k) t = __fmaf_rn(__ldg(cd.Rt + k * D + i), sm.x[k], t);
         const float y = (n > 0.0f) ? __fdiv_rn(t, n) : 0.0f;
         const int nm = (1 << b) - 1;
@@ -100,6 +101,7 @@ __device__ void encode_vector(const CodecDev& cd, VecSmem& sm, const RecordOut& 
             for (int k = 0; k < D; ++k) g2 = __fmaf_rn(sm.r[k], sm.r[k], g2);
             if (i == 0 && out.rnorm) *out.rnorm = __fsqrt_rn(g2);
             float z = 0.0f;
+#pragma unroll 32
             for (int k = 0; k < D; ++k) z = __fmaf_rn(__ldg(cd.St + k * D + i), sm.r[k], z);
             const unsigned bal = __ballot_sync(0xffffffffu, z >= 0.0f);
             if ((i & 31) == 0 && out.sgn) out.sgn[i >> 5] = bal;
