@@ -44,13 +44,19 @@
 extern "C" {
 #endif
 
-#define TQ_ABI_VERSION 1
+#define TQ_ABI_VERSION 2
 
 /* A cudaStream_t; 0 is the legacy default stream. */
 typedef struct CUstream_st *tq_stream_t;
 
 typedef enum { TQ_MODE_MSE = 0, TQ_MODE_PROD = 1, TQ_MODE_GROUP = 2 } tq_mode;
 typedef enum { TQ_F32 = 0, TQ_BF16 = 1, TQ_F16 = 2 } tq_dtype;
+
+/* How tq_encode_append rotates long appends (tq_cache_desc.encode_policy). */
+typedef enum {
+    TQ_ENCODE_AUTO = 0,  /* tensor cores for appends of >= 64 tokens (see tq_encode_append) */
+    TQ_ENCODE_EXACT = 1  /* always the sequential fp32 specification, bit for bit          */
+} tq_encode_policy;
 
 typedef enum {
     TQ_OK = 0,
@@ -166,6 +172,7 @@ typedef struct {
     int64_t stream_offset[7];/* byte offsets of the streams in a sub-block (-1 = none):
                                 key idx, key signs, key norm, key rnorm,
                                 value idx, value norm | value scale, value min     */
+    int encode_policy;       /* tq_encode_policy; tq_cache_desc_init sets AUTO      */
 } tq_cache_desc;
 
 /*
@@ -195,15 +202,24 @@ tq_status tq_cache_desc_init(tq_cache_desc *desc, const tq_codec *key_codec,
  *   seq_lens    device int32 [batch], tokens already cached (not modified)
  *   block_table device int32 [batch][max_blocks] of physical block ids, or NULL:
  *               then sequence b owns blocks b*max_blocks .. b*max_blocks+max_blocks-1
- * Encoding is bit-exact with the fp32 specification (sequential fused
- * multiply-adds, IEEE division and square root): norm = sqrt(sum x_k^2),
- * y = (R x)/norm, index_i = #{midpoints < y_i}; prod residual r = y - c[index],
- * rnorm = |r|, sign_j = ((S r)_j >= 0). Tokens past a sequence's capacity
+ * The fp32 specification (sequential fused multiply-adds, IEEE division and
+ * square root): norm = sqrt(sum x_k^2), y = (R x)/norm,
+ * index_i = #{midpoints < y_i}; prod residual r = y - c[index], rnorm = |r|,
+ * sign_j = ((S r)_j >= 0). Short appends (decode steps), group codecs, f32
+ * inputs, head_dim 256 and TQ_ENCODE_EXACT follow it bit for bit. With
+ * TQ_ENCODE_AUTO, appends of >= 64 tokens of bf16/f16 MSE or prod vectors
+ * with head_dim 64 or 128 rotate on the tensor cores, as the pages plan for
+ * chunked prefill: norms stay bit-exact, y and S r are computed with errors
+ * far below the specification's own fp32 rounding bound, so an index or a
+ * sign differs from the specification only where the exact value lies within
+ * that bound of a decision threshold (a midpoint, or 0), and the residual
+ * norm then follows the differing index. Tokens past a sequence's capacity
  * are skipped and flagged (TQ_DEVERR_CAPACITY).
  * Errors: TQ_ERR_CONFIG_MISMATCH if a codec's (head_dim, bits, mode, seed,
  * group) differs from the descriptor (the mixed-config guard of
  * BatchTurboQuantKVCache.merge); TQ_ERR_CAPACITY if n_new exceeds
- * max_blocks*block_tokens; TQ_ERR_INVALID_ARG for bad pointers or sizes.
+ * max_blocks*block_tokens; TQ_ERR_INVALID_ARG for bad pointers or sizes or an
+ * unknown encode_policy.
  */
 tq_status tq_encode_append(const tq_codec *key_codec, const tq_codec *value_codec,
                            const tq_cache_desc *cache, int layer, const void *k, const void *v,

@@ -44,7 +44,7 @@ def compare_decode(gpu: np.ndarray, ref: np.ndarray, atol: float = ATOL, cos_min
 class GpuCase:
     """One workload slice on the GPU: codecs, pool, block table, inputs."""
 
-    def __init__(self, w: wl.Workload, layers, seq_lens=None, device="cuda"):
+    def __init__(self, w: wl.Workload, layers, seq_lens=None, device="cuda", exact_encode=True):
         self.w = w
         self.layers = list(layers)
         self.D = w.head_dim
@@ -55,7 +55,8 @@ class GpuCase:
         self.table, nblocks = wl.block_table(w, cap)
         self.max_blocks = self.table.shape[1]
         self.cache = tq.CompressedKVCache(self.kc, self.vc, len(self.layers), nblocks,
-                                          w.block_tokens, w.num_kv_heads, device)
+                                          w.block_tokens, w.num_kv_heads, device,
+                                          exact_encode=exact_encode)
         self.table_d = self.table.to(device)
         self.device = device
 
@@ -109,3 +110,47 @@ def oracle_decode(w: wl.Workload, K: np.ndarray, V: np.ndarray, q: np.ndarray, s
     kc, vc = oracle_codec(w.key, D), oracle_codec(w.value, D)
     kr, vr = kc.encode(K), vc.encode(V)
     return O.decode_rotated(q, kc, kr, vc, vr, scale or 1 / math.sqrt(D), w.q_len)
+
+
+def read_records(layer_pool: np.ndarray, kc: O.Codec, vc: O.Codec, Hkv: int, BT: int, table, max_blocks: int,
+                 seq: int, h: int, t0: int, n: int):
+    """Key and value records of tokens [t0, t0+n) of (seq, head h) from a layer pool.
+
+    The sub-block layout is the oracle's (subblock_layout); ``table`` is the
+    block table (numpy) or None for the identity.
+    """
+    sub, off = O.subblock_layout(kc, vc, BT)
+    Wk, Wv, Ws = kc.W, vc.W, kc.D // 32
+    ng = vc.D // vc.group if vc.mode == O.GROUP else 0
+    rows = {"k_idx": [], "k_sgn": [], "k_norm": [], "k_rnorm": [], "v_idx": [], "v_norm": [],
+            "v_scale": [], "v_min": []}
+    for t in range(t0, t0 + n):
+        lb, slot = t // BT, t % BT
+        pb = int(table[seq, lb]) if table is not None else seq * max_blocks + lb
+        base = (pb * Hkv + h) * sub
+
+        def take(o, count, dt):
+            size = np.dtype(dt).itemsize * count
+            a = base + o + slot * size
+            return layer_pool[a:a + size].view(dt)
+        rows["k_idx"].append(take(off[0], Wk, np.uint32))
+        rows["k_norm"].append(take(off[2], 1, np.float32))
+        if kc.mode == O.PROD:
+            rows["k_sgn"].append(take(off[1], Ws, np.uint32))
+            rows["k_rnorm"].append(take(off[3], 1, np.float32))
+        rows["v_idx"].append(take(off[4], Wv, np.uint32))
+        if vc.mode == O.GROUP:
+            rows["v_scale"].append(take(off[5], ng, np.uint16))
+            rows["v_min"].append(take(off[6], ng, np.uint16))
+        else:
+            rows["v_norm"].append(take(off[5], 1, np.float32))
+    out = {k: np.stack(v) for k, v in rows.items() if v}
+    krec = {"idx": out["k_idx"], "norm": out["k_norm"][:, 0]}
+    if kc.mode == O.PROD:
+        krec["sgn"], krec["rnorm"] = out["k_sgn"], out["k_rnorm"][:, 0]
+    vrec = {"idx": out["v_idx"]}
+    if vc.mode == O.GROUP:
+        vrec["scale"], vrec["min"] = out["v_scale"], out["v_min"]
+    else:
+        vrec["norm"] = out["v_norm"][:, 0]
+    return krec, vrec

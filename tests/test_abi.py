@@ -43,16 +43,24 @@ def test_header_symbols_exported(libtq):
 
 
 def test_abi_version_and_status_strings(libtq):
-    assert tq.tq_abi_version() == 1
+    assert tq.tq_abi_version() == 2
     for s in range(8):
         assert _lib.status_string(s)
 
 
-def test_struct_layout_matches_header(libtq):
+def test_struct_layout_matches_header(libtq, tmp_path):
     # offsets the C compiler gives the descriptor must match the ctypes mirror
-    assert ctypes.sizeof(_lib.tq_cache_desc) == 8 + 8 + 4 * 7 + 4 + 8 + 12 + 4 + 8 + 8 + 56
-    assert _lib.tq_cache_desc.key_seed.offset == 48
-    assert _lib.tq_cache_desc.stream_offset.offset == 88
+    fields = [f for f, _ in _lib.tq_cache_desc._fields_]
+    src = tmp_path / "layout.c"
+    src.write_text('#include <stddef.h>\n#include <stdio.h>\n#include "tq.h"\nint main(void) {\n'
+                   '  printf("%zu\\n", sizeof(tq_cache_desc));\n' +
+                   "".join(f'  printf("%zu\\n", offsetof(tq_cache_desc, {f}));\n' for f in fields) +
+                   "  return 0;\n}\n")
+    exe = tmp_path / "layout"
+    subprocess.check_call(["gcc", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)])
+    got = [int(v) for v in subprocess.check_output([str(exe)]).split()]
+    assert got[0] == ctypes.sizeof(_lib.tq_cache_desc)
+    assert got[1:] == [getattr(_lib.tq_cache_desc, f).offset for f in fields]
 
 
 def test_unsupported_codecs_rejected_without_device(libtq):

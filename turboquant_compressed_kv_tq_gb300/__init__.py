@@ -12,8 +12,8 @@ from typing import Optional
 
 import numpy as np
 
-from ._lib import (TQ_BF16, TQ_DEVERR_BLOCK, TQ_DEVERR_CAPACITY, TQ_DEVERR_SEQLEN, TQ_F16,
-                   TQ_F32, TQ_MODE_GROUP, TQ_MODE_MSE, TQ_MODE_PROD, TQ_OK, TQError, check,
+from ._lib import (TQ_BF16, TQ_DEVERR_BLOCK, TQ_DEVERR_CAPACITY, TQ_DEVERR_SEQLEN, TQ_ENCODE_AUTO,
+                   TQ_ENCODE_EXACT, TQ_F16, TQ_F32, TQ_MODE_GROUP, TQ_MODE_MSE, TQ_MODE_PROD, TQ_OK, TQError, check,
                    lib, library_path, status_string, tq_cache_desc, tq_codec_info_t)
 
 __all__ = [
@@ -23,6 +23,7 @@ __all__ = [
     "tq_device_error",
     "tq_launch_count", "tq_abi_version", "Codec", "CompressedKVCache", "TQError",
     "TQ_MODE_MSE", "TQ_MODE_PROD", "TQ_MODE_GROUP", "TQ_F32", "TQ_BF16", "TQ_F16",
+    "TQ_ENCODE_AUTO", "TQ_ENCODE_EXACT",
 ]
 
 
@@ -216,7 +217,7 @@ class CompressedKVCache:
     """A device pool plus its descriptor (all layers), allocated through torch."""
 
     def __init__(self, key: Codec, value: Codec, num_layers: int, num_blocks: int,
-                 block_tokens: int, num_kv_heads: int, device="cuda"):
+                 block_tokens: int, num_kv_heads: int, device="cuda", exact_encode: bool = False):
         torch = _torch()
         self.key, self.value = key, value
         _, req = tq_cache_desc_init(key.handle, value.handle, num_layers, num_blocks, block_tokens,
@@ -224,6 +225,9 @@ class CompressedKVCache:
         self.pool = torch.zeros(req, dtype=torch.uint8, device=device)
         self.desc, _ = tq_cache_desc_init(key.handle, value.handle, num_layers, num_blocks,
                                           block_tokens, num_kv_heads, self.pool)
+        # TQ_ENCODE_EXACT: every append in the sequential fp32 order; AUTO lets
+        # long appends rotate on the tensor cores
+        self.desc.encode_policy = TQ_ENCODE_EXACT if exact_encode else TQ_ENCODE_AUTO
         self.num_layers, self.num_blocks = num_layers, num_blocks
         self.block_tokens, self.num_kv_heads = block_tokens, num_kv_heads
 

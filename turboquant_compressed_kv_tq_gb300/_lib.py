@@ -29,6 +29,9 @@ TQ_F32 = 0
 TQ_BF16 = 1
 TQ_F16 = 2
 
+TQ_ENCODE_AUTO = 0
+TQ_ENCODE_EXACT = 1
+
 TQ_DEVERR_CAPACITY = 1
 TQ_DEVERR_BLOCK = 2
 TQ_DEVERR_SEQLEN = 4
@@ -59,7 +62,7 @@ class tq_cache_desc(ctypes.Structure):
                 ("key_seed", ctypes.c_uint64), ("value_mode", ctypes.c_int),
                 ("value_bits", ctypes.c_int), ("value_group", ctypes.c_int),
                 ("value_seed", ctypes.c_uint64), ("subblock_bytes", ctypes.c_int64),
-                ("stream_offset", ctypes.c_int64 * 7)]
+                ("stream_offset", ctypes.c_int64 * 7), ("encode_policy", ctypes.c_int)]
 
 
 _P = ctypes.c_void_p

@@ -17,10 +17,10 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libtq.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-CU_SOURCES = ["api.cu", "encode.cu", "encode_block.cu", "decode.cu", "decode_mma_a.cu", "decode_mma_b.cu", "decode_mma_c.cu", "decode_noalloc.cu"]
+CU_SOURCES = ["api.cu", "encode.cu", "encode_block.cu", "encode_tc.cu", "decode.cu", "decode_mma_a.cu", "decode_mma_b.cu", "decode_mma_c.cu", "decode_noalloc.cu"]
 CXX_SOURCES = ["codec_build.cpp"]
-HEADERS = [os.path.join(CSRC, "tq_internal.h"), os.path.join(CSRC, "decode_mma.cuh"),
-           os.path.join(CSRC, "decode_mma_impl.cuh"), os.path.join(INCLUDE, "tq.h")]
+HEADERS = sorted(os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".h", ".cuh"))) + \
+    [os.path.join(INCLUDE, "tq.h")]
 
 
 def _nvcc() -> str:

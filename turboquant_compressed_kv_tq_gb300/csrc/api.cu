@@ -61,6 +61,8 @@ void free_codec(tq_codec* c) {
     cudaFree(c->d_St);
     cudaFree(c->d_c);
     cudaFree(c->d_m);
+    cudaFree(c->d_Rtc);
+    cudaFree(c->d_Stc);
     if (prev >= 0) cudaSetDevice(prev);
     delete c;
 }
@@ -88,6 +90,8 @@ CodecDev dev_view(const tq_codec* c) {
     d.St = c->d_St;
     d.c = c->d_c;
     d.m = c->d_m;
+    d.Rtc = c->d_Rtc;
+    d.Stc = c->d_Stc;
     d.D = c->head_dim;
     d.mode = c->mode;
     d.bits = c->bits;
@@ -183,6 +187,16 @@ tq_status tq_codec_create(int head_dim, int bits, tq_mode mode, uint64_t seed, t
     if (st == TQ_OK && mode == TQ_MODE_PROD) st = upload(&c->d_St, transpose(c->host.qjl, head_dim));
     if (st == TQ_OK) st = upload(&c->d_c, c->host.centroids);
     if (st == TQ_OK) st = upload(&c->d_m, c->host.midpoints);
+    if (st == TQ_OK && head_dim <= 128) {
+        // tensor-core operands for the chunked-prefill encoder: 16 R and S, fp16 hi + lo
+        std::vector<uint16_t> op;
+        build_tc_operand(c->host.rotation, head_dim, 16.0, op);
+        st = upload(&c->d_Rtc, op);
+        if (st == TQ_OK && mode == TQ_MODE_PROD) {
+            build_tc_operand(c->host.qjl, head_dim, 1.0, op);
+            st = upload(&c->d_Stc, op);
+        }
+    }
     if (st == TQ_OK && device_state(nullptr, nullptr) != TQ_OK) st = TQ_ERR_CUDA;
     if (st != TQ_OK) {
         free_codec(c);
@@ -274,6 +288,7 @@ tq_status tq_cache_desc_init(tq_cache_desc* d, const tq_codec* kc, const tq_code
     const int D = kc->head_dim;
     const int64_t BT = block_tokens;
     int64_t o = 0;
+    d->encode_policy = TQ_ENCODE_AUTO;
     for (int i = 0; i < 7; ++i) d->stream_offset[i] = -1;
     d->stream_offset[0] = o;
     o += BT * 4 * kc->index_words;
@@ -329,6 +344,7 @@ tq_status tq_encode_append(const tq_codec* kc, const tq_codec* vc, const tq_cach
     if (layer < 0 || layer >= cache->num_layers || batch < 0 || n_new < 0 || max_blocks <= 0)
         return TQ_ERR_INVALID_ARG;
     if (dtype != TQ_F32 && dtype != TQ_BF16 && dtype != TQ_F16) return TQ_ERR_INVALID_ARG;
+    if (cache->encode_policy != TQ_ENCODE_AUTO && cache->encode_policy != TQ_ENCODE_EXACT) return TQ_ERR_INVALID_ARG;
     if (static_cast<int64_t>(n_new) > static_cast<int64_t>(max_blocks) * cache->block_tokens) return TQ_ERR_CAPACITY;
     if (!block_table && static_cast<int64_t>(batch) * max_blocks > cache->num_blocks) return TQ_ERR_CAPACITY;
     if (batch == 0 || n_new == 0) return TQ_OK;
@@ -348,6 +364,7 @@ tq_status tq_encode_append(const tq_codec* kc, const tq_codec* vc, const tq_cach
     a.seq_lens = seq_lens;
     a.table = block_table;
     a.max_blocks = max_blocks;
+    a.exact = cache->encode_policy == TQ_ENCODE_EXACT;
     a.err = err;
     return launch_encode_append(a, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
 }

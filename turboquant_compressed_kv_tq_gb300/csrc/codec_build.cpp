@@ -212,7 +212,32 @@ double nearest_half(double x) {
     return std::scalbn(std::nearbyint(std::scalbn(x, -q)), q);
 }
 
+// IEEE half bits of a value already on the fp16 grid (|h| < 65520).
+uint16_t half_bits_of(double h) {
+    const uint16_t sign = std::signbit(h) ? 0x8000u : 0u;
+    const double a = std::fabs(h);
+    if (a == 0.0) return sign;
+    const int e = std::ilogb(a);
+    if (e < -14) return static_cast<uint16_t>(sign | std::lround(std::scalbn(a, 24)));  // subnormal
+    const long mant = std::lround(std::scalbn(a, 10 - e));                              // 1024..2047
+    return static_cast<uint16_t>(sign | ((e + 15) << 10) | (mant - 1024));
+}
+
 }  // namespace
+
+void build_tc_operand(const std::vector<float>& M, int D, double scale, std::vector<uint16_t>& out) {
+    out.assign(static_cast<size_t>(2) * D * D, 0);
+    const size_t lo_base = static_cast<size_t>(D) * D;
+    for (int row = 0; row < D; ++row)
+        for (int k = 0; k < D; ++k) {
+            const double v = scale * static_cast<double>(M[static_cast<size_t>(row) * D + k]);
+            const double hi = nearest_half(v);
+            const double lo = nearest_half(v - hi);
+            const size_t at = (static_cast<size_t>(row / 8) * (D / 8) + k / 8) * 64 + (row % 8) * 8 + (k % 8);
+            out[at] = half_bits_of(hi);
+            out[lo_base + at] = half_bits_of(lo);
+        }
+}
 
 void build_codec_tables(int D, int index_bits, bool with_qjl, uint64_t seed, HostTables& out) {
     static std::mutex mu;

@@ -213,7 +213,12 @@ cudaError_t launch_encode_append(const EncodeAppendArgs& a, cudaStream_t s) {
         g_launches.fetch_add(1, std::memory_order_relaxed);
         return cudaGetLastError();
     }
-    cudaError_t e = launch_encode_block(a, 0, s);
+    // Chunks of >= 64 tokens rotate on the tensor cores unless the caller asked
+    // for the sequential fp32 order (inputs must be 16-byte aligned rows).
+    constexpr int kTensorFrom = 64;
+    const bool aligned = (reinterpret_cast<uintptr_t>(a.k) % 16 == 0) && (reinterpret_cast<uintptr_t>(a.v) % 16 == 0);
+    const bool tc_ok = !a.exact && a.n_new >= kTensorFrom && aligned;
+    cudaError_t e = (tc_ok && encode_tc_supported(a, 0)) ? launch_encode_tc(a, 0, s) : launch_encode_block(a, 0, s);
     if (e != cudaSuccess) return e;
     if (a.vc.mode == TQ_MODE_GROUP) {
         dim3 grid(a.n_new, a.pool.Hkv, a.batch);
@@ -221,7 +226,7 @@ cudaError_t launch_encode_append(const EncodeAppendArgs& a, cudaStream_t s) {
         g_launches.fetch_add(1, std::memory_order_relaxed);
         return cudaGetLastError();
     }
-    return launch_encode_block(a, 1, s);
+    return (tc_ok && encode_tc_supported(a, 1)) ? launch_encode_tc(a, 1, s) : launch_encode_block(a, 1, s);
 }
 
 cudaError_t launch_quantize(const QuantizeArgs& a, cudaStream_t s) {

@@ -23,6 +23,11 @@ struct HostTables {
 // Deterministic codec tables from (D, index bits, seed) (host, fp64 -> fp32).
 void build_codec_tables(int D, int index_bits, bool with_qjl, uint64_t seed, HostTables& out);
 
+// Tensor-core operand of scale * M (D x D row-major): fp16 bits of the hi part
+// then of the lo remainder, each in the no-swizzle K-major core-matrix layout
+// (row = output coordinate, K = input coordinate).
+void build_tc_operand(const std::vector<float>& M, int D, double scale, std::vector<uint16_t>& out);
+
 // Device view of one codec.
 struct CodecDev {
     const float* R;    // [D][D] row-major
@@ -30,6 +35,8 @@ struct CodecDev {
     const float* St;   // [D][D] transposed QJL matrix (prod) or nullptr
     const float* c;    // centroids
     const float* m;    // midpoints
+    const uint16_t* Rtc;  // tensor-core operand of 16 R (hi, lo), or nullptr
+    const uint16_t* Stc;  // tensor-core operand of S (hi, lo) (prod), or nullptr
     int D;
     int mode;          // tq_mode
     int bits;          // total bits
@@ -59,6 +66,7 @@ struct EncodeAppendArgs {
     const int32_t* seq_lens;
     const int32_t* table;
     int max_blocks;
+    int exact;           // 1: sequential fp32 order only (no tensor-core rotation)
     unsigned* err;
 };
 
@@ -120,6 +128,8 @@ DecodePlan make_decode_plan(const tq_cache_desc* d, int batch, int G, int Lq, in
 #ifdef __CUDACC__
 cudaError_t launch_encode_append(const EncodeAppendArgs& a, cudaStream_t s);
 cudaError_t launch_encode_block(const EncodeAppendArgs& a, int is_v, cudaStream_t s);
+bool encode_tc_supported(const EncodeAppendArgs& a, int is_v);
+cudaError_t launch_encode_tc(const EncodeAppendArgs& a, int is_v, cudaStream_t s);
 cudaError_t launch_quantize(const QuantizeArgs& a, cudaStream_t s);
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);
 #endif
@@ -146,4 +156,6 @@ struct tq_codec {
     float* d_St = nullptr;
     float* d_c = nullptr;
     float* d_m = nullptr;
+    uint16_t* d_Rtc = nullptr;
+    uint16_t* d_Stc = nullptr;
 };

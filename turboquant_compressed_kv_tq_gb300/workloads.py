@@ -200,3 +200,27 @@ def block_table(w: Workload, capacity_tokens: Sequence[int], device="cpu"):
         table[b, :k] = phys[o:o + k].to(torch.int32)
         o += k
     return table.to(device), total
+
+
+def encoder_stress(seed: int, batch: int, num_kv_heads: int, n: int, head_dim: int,
+                   dtype=torch.bfloat16, device="cpu") -> torch.Tensor:
+    """Vectors [batch, Hkv, n, D] that stress an encoder's arithmetic.
+
+    Mostly N(0,1) rows times a per-row scale 2^u, u ~ U[-12, 12]; among them
+    all-zero rows, one-hot rows, constant rows, rows with one dominant
+    coordinate and a tail 2^-20 below it, and rows at 2^-100 (tiny but normal
+    in bf16). Seeded; drawn on the host, then moved to ``device``.
+    """
+    g = torch.Generator().manual_seed(derive_seed(seed, "stress", batch, num_kv_heads, n, head_dim))
+    x = torch.randn(batch, num_kv_heads, n, head_dim, generator=g, dtype=torch.float32)
+    u = torch.randint(-12, 13, (batch, num_kv_heads, n, 1), generator=g).to(torch.float32)
+    x = x * torch.pow(2.0, u)
+    kind = torch.randint(0, 40, (batch, num_kv_heads, n), generator=g)
+    spike = torch.randint(0, head_dim, (batch, num_kv_heads, n), generator=g)
+    onehot = torch.nn.functional.one_hot(spike, head_dim).to(torch.float32)
+    x = torch.where((kind == 0).unsqueeze(-1), torch.zeros_like(x), x)
+    x = torch.where((kind == 1).unsqueeze(-1), onehot * 3.0, x)
+    x = torch.where((kind == 2).unsqueeze(-1), torch.full_like(x, -0.75), x)
+    x = torch.where((kind == 3).unsqueeze(-1), onehot * 5.0 + x * 2.0 ** -20, x)
+    x = torch.where((kind == 4).unsqueeze(-1), x * 2.0 ** -100, x)
+    return x.to(dtype).to(device).contiguous()
