@@ -12,7 +12,8 @@ checked here is:
     the division and the tensor-core side's own rounding;
   * for prod keys whose indices all agree, a QJL sign may differ only where
     the exact (S r)_j lies within the propagated band of 0, and the residual
-    norms differ by at most the propagated band;
+    norms differ by at most the propagated band plus the fp32 bound of a sum
+    of D squares in any order;
   * group-quantised values are not rotated and stay bit-exact.
 Expected values come from the oracle alone; the exact y and S r are recomputed
 here in fp64 from the oracle's fp32 tables.
@@ -85,7 +86,9 @@ def check_rotated(codec: O.Codec, X: np.ndarray, got: dict, want: dict):
         for t, j in zip(*np.nonzero(sd)):
             assert abs(z[t, j]) <= bz[t, j], f"token {t} sign {j}: z={z[t, j]:.9g}, band {bz[t, j]:.3g}"
         sflips = int(sd.sum())
-        rband = 2.0 * np.sqrt((band * band).sum(1)) + 2.0 ** -22 * want["rnorm"]
+        # both sides sum D squares in fp32 (in their own order): relative error
+        # <= gamma_D/2 each, plus the square roots' rounding
+        rband = 2.0 * np.sqrt((band * band).sum(1)) + (gD + 2.0 ** -22) * want["rnorm"]
         dr = np.abs(got["rnorm"].astype(np.float64) - want["rnorm"].astype(np.float64))
         assert np.all(dr[same] <= rband[same]), f"max rnorm excess {(dr - rband)[same].max():.3g}"
     return int(diff.sum()), sflips

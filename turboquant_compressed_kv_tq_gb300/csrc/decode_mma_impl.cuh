@@ -34,65 +34,114 @@ struct MmaArgs {
 // Slot 0 holds fp16(q'); slot 1 holds q'' for prod keys, and for MSE keys the
 // rounding remainder fp16(q' - fp16(q')), so that two MMAs against the exact
 // fp16 codebook operand carry q' to about 22 bits.
+constexpr int kQThreads = 256;
+
+__host__ __device__ constexpr size_t qfrag_smem_bytes(bool prod) {
+    return (prod ? 2u : 1u) * kD * kD * 4u + 3u * kRows * kD * 4u + 16u;
+}
+
 template <int KB>
-__global__ void __launch_bounds__(kD) qfrag_kernel(MmaArgs m) {
-    // one CTA per (sequence x kv head, row group, row): the row's q' and q''
-    // in fp32, then the 128 fragment registers that hold this row
-    __shared__ float q1[kD];
-    __shared__ float q2[kD];
-    __shared__ float qs[kD];
+__global__ void __launch_bounds__(kQThreads) qfrag_kernel(MmaArgs m) {
+    // one CTA per (sequence x kv head, row group): the 16 rows' q' and q'' in
+    // fp32 from tables staged in shared memory by one bulk copy; thread
+    // (i, half) runs 8 independent row chains for output coordinate i
+    extern __shared__ __align__(16) unsigned char qsm[];
     const DecodeArgs& a = m.a;
+    const bool prod = a.kc.mode == TQ_MODE_PROD;
+    float* Rt = reinterpret_cast<float*>(qsm);   // [k][i] = R[i][k]
+    float* St = Rt + kD * kD;                    // prod
+    float* qs = St + (prod ? kD * kD : 0);       // [16][kD] query rows
+    float* q1 = qs + kRows * kD;                 // [16][kD] q'
+    float* q2 = q1 + kRows * kD;                 // [16][kD] q'' (prod)
+    uint64_t* bar = reinterpret_cast<uint64_t*>(q2 + kRows * kD);
     const int Hkv = a.pool.Hkv;
     const int bh = blockIdx.x;
     const int b = bh / Hkv, h = bh % Hkv;
     const int rg = blockIdx.y;
-    const int rr = blockIdx.z;
     const int RG = a.plan.row_groups;
     const int unit = bh * RG + rg;
-    const int i = threadIdx.x;
-    const float s1 = a.scale * kLog2e;
-    const float s2 = s1 * kSqrtHalfPi / static_cast<float>(kD);
-    const int r = rg * kRows + rr;
-    if (r < a.plan.rows) {
-        const int g = r / a.Lq, l = r % a.Lq;
-        const int64_t src = ((static_cast<int64_t>(b) * a.Hq + h * a.G + g) * a.Lq + l) * kD + i;
-        if (a.q_dtype == TQ_F32) qs[i] = static_cast<const float*>(a.q)[src];
-        else if (a.q_dtype == TQ_BF16) qs[i] = __bfloat162float(static_cast<const __nv_bfloat16*>(a.q)[src]);
-        else qs[i] = __half2float(static_cast<const __half*>(a.q)[src]);
-        __syncthreads();
-        float t = 0.0f;
-#pragma unroll 32
-        for (int k = 0; k < kD; ++k) t = fmaf(__ldg(a.kc.Rt + k * kD + i), qs[k], t);
-        q1[i] = t;
-        __syncthreads();
-        float z = 0.0f;
-        if (a.kc.mode == TQ_MODE_PROD) {
-#pragma unroll 32
-            for (int k = 0; k < kD; ++k) z = fmaf(__ldg(a.kc.St + k * kD + i), q1[k], z);
+    const int tid = threadIdx.x;
+    const int i = tid & (kD - 1), half = tid >> 7;
+
+    if (tid == 0) {
+        mbar_init(bar, 1);
+        mbar_fence_init();
+        mbar_expect_tx(bar, (prod ? 2u : 1u) * kD * kD * 4u);
+        bulk_g2s(Rt, a.kc.Rt, kD * kD * 4, bar);
+        if (prod) bulk_g2s(St, a.kc.St, kD * kD * 4, bar);
+    }
+    for (int e = tid; e < kRows * kD; e += kQThreads) {
+        const int rr = e / kD, k = e % kD;
+        const int r = rg * kRows + rr;
+        float v = 0.0f;
+        if (r < a.plan.rows) {
+            const int g = r / a.Lq, l = r % a.Lq;
+            const int64_t src = ((static_cast<int64_t>(b) * a.Hq + h * a.G + g) * a.Lq + l) * kD + k;
+            if (a.q_dtype == TQ_F32) v = static_cast<const float*>(a.q)[src];
+            else if (a.q_dtype == TQ_BF16) v = __bfloat162float(static_cast<const __nv_bfloat16*>(a.q)[src]);
+            else v = __half2float(static_cast<const __half*>(a.q)[src]);
         }
-        q2[i] = z;
-    } else {
-        q1[i] = 0.0f;
-        q2[i] = 0.0f;
+        qs[e] = v;
+    }
+    const bool ok = mbar_wait(bar, 0);
+    if (__syncthreads_or(!ok)) {
+        if (tid == 0) atomicOr(a.err, TQ_DEVERR_TIMEOUT);
+        (void)mbar_wait(bar, 0);
+        return;
+    }
+    {
+        float acc[8];
+#pragma unroll
+        for (int r = 0; r < 8; ++r) acc[r] = 0.0f;
+#pragma unroll 4
+        for (int k = 0; k < kD; ++k) {
+            const float rt = Rt[k * kD + i];
+#pragma unroll
+            for (int r = 0; r < 8; ++r) acc[r] = fmaf(rt, qs[(8 * half + r) * kD + k], acc[r]);
+        }
+#pragma unroll
+        for (int r = 0; r < 8; ++r) q1[(8 * half + r) * kD + i] = acc[r];
     }
     __syncthreads();
-    // entry (which, ks, j, e) of this row: lane 4*(rr%8)+j, register 2e + (rr >= 8)
-    const int which = i >> 6, ks = (i >> 3) & 7, j = (i >> 1) & 3, e = i & 1;
-    const int lane = 4 * (rr & 7) + j;
-    const int reg = 2 * e + (rr >= 8 ? 1 : 0);
-    int pa, pb;
-    const bool qjl = which && a.kc.mode == TQ_MODE_PROD;
-    mse_pair(qjl ? 1 : KB, 2 * ks + e, pa, pb);
-    const float* q = qjl ? q2 : q1;
-    const float sc = qjl ? s2 : s1;
-    float va = q[32 * j + pa] * sc, vb = q[32 * j + pb] * sc;
-    if (which && !qjl) {
-        va -= __half2float(__float2half_rn(va));
-        vb -= __half2float(__float2half_rn(vb));
+    if (prod) {
+        float acc[8];
+#pragma unroll
+        for (int r = 0; r < 8; ++r) acc[r] = 0.0f;
+#pragma unroll 4
+        for (int k = 0; k < kD; ++k) {
+            const float st = St[k * kD + i];
+#pragma unroll
+            for (int r = 0; r < 8; ++r) acc[r] = fmaf(st, q1[(8 * half + r) * kD + k], acc[r]);
+        }
+#pragma unroll
+        for (int r = 0; r < 8; ++r) q2[(8 * half + r) * kD + i] = acc[r];
+        __syncthreads();
     }
+    // entry (row rr, which, ks, j, e): lane 4*(rr%8)+j, register 2e + (rr >= 8)
+    const float s1 = a.scale * kLog2e;
+    const float s2 = s1 * kSqrtHalfPi / static_cast<float>(kD);
     uint32_t* dst = reinterpret_cast<uint32_t*>(const_cast<uint4*>(m.qfrag)) + static_cast<int64_t>(unit) * 2 * 8 * 32 * 4;
-    dst[((which * 8 + ks) * 32 + lane) * 4 + reg] = pack_half2(va, vb);
-    if (i == 0 && rr == 0) m.cnt[unit] = 0u;
+    for (int e = tid; e < kRows * 128; e += kQThreads) {
+        const int rr = e >> 7, x = e & 127;
+        const int which = x >> 6, ks = (x >> 3) & 7, j = (x >> 1) & 3, ee = x & 1;
+        const int lane = 4 * (rr & 7) + j;
+        const int reg = 2 * ee + (rr >= 8 ? 1 : 0);
+        int pa, pb;
+        const bool qjl = which && prod;
+        mse_pair(qjl ? 1 : KB, 2 * ks + ee, pa, pb);
+        const float* q = (qjl ? q2 : q1) + rr * kD;
+        const float sc = qjl ? s2 : s1;
+        float va = q[32 * j + pa] * sc, vb = q[32 * j + pb] * sc;
+        if (which && !qjl) {
+            va -= __half2float(__float2half_rn(va));
+            vb -= __half2float(__float2half_rn(vb));
+        }
+        dst[((which * 8 + ks) * 32 + lane) * 4 + reg] = pack_half2(va, vb);
+    }
+    if (tid == 0) {
+        m.cnt[unit] = 0u;
+        mbar_inval(bar);
+    }
 }
 
 // ------------------------------------------------------------------ split kernel
@@ -556,8 +605,18 @@ cudaError_t launch_mma(const MmaArgs& m, size_t smem, cudaStream_t s) {
         max_dyn[dev & 63].store(optin - static_cast<int>(fa.sharedSizeBytes));
     }
     if (static_cast<int>(smem) > max_dyn[dev & 63].load()) return cudaErrorInvalidValue;
+    static std::atomic<uint64_t> qattr_set{0};
+    if (!(qattr_set.load() & bit)) {
+        cudaError_t e = cudaFuncSetAttribute(qfrag_kernel<KB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(qfrag_smem_bytes(true)));
+        if (e != cudaSuccess) {
+            (void)cudaGetLastError();
+            return e;
+        }
+        qattr_set.fetch_or(bit);
+    }
     const int RG = a.plan.row_groups;
-    qfrag_kernel<KB><<<dim3(a.batch * a.pool.Hkv, RG, kRows), kD, 0, s>>>(m);
+    qfrag_kernel<KB><<<dim3(a.batch * a.pool.Hkv, RG), kQThreads, qfrag_smem_bytes(KPROD), s>>>(m);
     g_launches.fetch_add(1, std::memory_order_relaxed);
     split_mma_kernel<KB, KPROD, VGROUP, VB>
         <<<dim3(a.plan.splits, a.pool.Hkv * RG, a.batch), kThreads, smem, s>>>(m);

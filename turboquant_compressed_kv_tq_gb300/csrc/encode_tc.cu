@@ -82,14 +82,18 @@ __device__ __forceinline__ void store8(unsigned char* a0, unsigned char* a1, int
     if (a1) *reinterpret_cast<uint4*>(a1 + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
 }
 
+// N words at dst (dst aligned to the widest access that divides N words).
 template <int N>
 __device__ __forceinline__ void store_words(uint32_t* dst, const uint32_t (&w)[N]) {
     if constexpr (N % 4 == 0) {
 #pragma unroll
         for (int i = 0; i < N; i += 4) reinterpret_cast<uint4*>(dst)[i / 4] = make_uint4(w[i], w[i + 1], w[i + 2], w[i + 3]);
-    } else {
+    } else if constexpr (N % 2 == 0) {
 #pragma unroll
         for (int i = 0; i < N; i += 2) reinterpret_cast<uint2*>(dst)[i / 2] = make_uint2(w[i], w[i + 1]);
+    } else {
+#pragma unroll
+        for (int i = 0; i < N; ++i) dst[i] = w[i];
     }
 }
 
@@ -149,6 +153,20 @@ __global__ void __launch_bounds__(kThreads, 1) encode_tc_kernel(EncodeAppendArgs
     unsigned char* A0 = smem + L::oA0;
     unsigned char* A1 = smem + L::oA1;
 
+    // inputs of this thread's token in a tile, loaded one tile ahead
+    uint4 nraw[D / 8];
+    auto load_row = [&](int64_t tl) {
+        const int ts = static_cast<int>(tl % tiles_per_seq);
+        const int bh = static_cast<int>(tl / tiles_per_seq);
+        const int t = ts * kTileRows + tid;
+        const bool ok_row = tl < ntiles && t < a.n_new;
+        const int64_t row = (static_cast<int64_t>(bh / Hkv) * Hkv + bh % Hkv) * a.n_new + t;
+        const uint4* p = reinterpret_cast<const uint4*>(src + row * D * 2);
+#pragma unroll
+        for (int c8 = 0; c8 < D / 8; ++c8) nraw[c8] = ok_row ? __ldg(p + c8) : make_uint4(0, 0, 0, 0);
+    };
+    load_row(blockIdx.x);
+
     for (int64_t tile = blockIdx.x; tile < ntiles && !failed; tile += gridDim.x) {
         const int ts = static_cast<int>(tile % tiles_per_seq);
         const int bh = static_cast<int>(tile / tiles_per_seq);
@@ -156,15 +174,11 @@ __global__ void __launch_bounds__(kThreads, 1) encode_tc_kernel(EncodeAppendArgs
         const int t = ts * kTileRows + tid;
         const bool valid = t < a.n_new;
 
-        // ---------------- this thread's token: norm (sequential fma) and the
-        // scaled fp16 operand row
+        // ---------------- this thread's token (loaded during the previous tile):
+        // norm in the sequential fma order, scaled fp16 operand row
         uint4 raw[D / 8];
-        {
-            const int64_t row = (static_cast<int64_t>(b) * Hkv + h) * a.n_new + t;
-            const uint4* p = reinterpret_cast<const uint4*>(src + row * D * 2);
 #pragma unroll
-            for (int c8 = 0; c8 < D / 8; ++c8) raw[c8] = valid ? __ldg(p + c8) : make_uint4(0, 0, 0, 0);
-        }
+        for (int c8 = 0; c8 < D / 8; ++c8) raw[c8] = nraw[c8];
         float n2 = 0.0f;
 #pragma unroll
         for (int c8 = 0; c8 < D / 8; ++c8)
@@ -199,6 +213,7 @@ __global__ void __launch_bounds__(kThreads, 1) encode_tc_kernel(EncodeAppendArgs
             }
             tc::mma_commit(bar_mma);
         }
+        load_row(tile + gridDim.x);  // next tile's row, in flight during this tile
         ok = tc::mbar_wait(bar_mma, phase);
         if (__syncthreads_or(!ok)) {
             failed = true;  // the commit of `phase` is still outstanding
@@ -207,42 +222,9 @@ __global__ void __launch_bounds__(kThreads, 1) encode_tc_kernel(EncodeAppendArgs
         phase ^= 1;
         tc::tc_fence_after();
 
-        // ---------------- epilogue 1: indices (and residual operands for prod)
+        // ---------------- epilogue 1: indices (and residual operands for prod),
+        // 32 columns at a time; their KB index words are stored directly
         const float inv = n > 0.0f ? __fdiv_rn(scalbnf(1.0f, ex - 4), n) : 0.0f;
-        uint32_t words[W];
-#pragma unroll
-        for (int i = 0; i < W; ++i) words[i] = 0u;
-        float g2 = 0.0f;
-#pragma unroll
-        for (int ch = 0; ch < D / 32; ++ch) {
-            float v[32];
-            tc::tmem_ld32(tmem_row + 32 * ch, v);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                const int k = 32 * ch + i;
-                const float y = v[i] * inv;
-                int code = 0;
-#pragma unroll
-                for (int j = 0; j < NM; ++j) code += y > mreg[j] ? 1 : 0;
-                const int bit = k * KB;
-                words[bit >> 5] |= static_cast<uint32_t>(code) << (bit & 31);
-                if ((bit & 31) + KB > 32) words[(bit >> 5) + 1] |= static_cast<uint32_t>(code) >> (32 - (bit & 31));
-                if constexpr (PROD) {
-                    const float r = __fsub_rn(y, s_c[code]);
-                    g2 = __fmaf_rn(r, r, g2);
-                    v[i] = r * 256.0f;
-                }
-            }
-            if constexpr (PROD) {
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    float f[8];
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) f[e] = v[8 * q + e];
-                    store8<D>(A0, A1, tid, 32 * ch + 8 * q, f);
-                }
-            }
-        }
 
         // destination of this token in the pool
         char* sub = nullptr;
@@ -261,10 +243,43 @@ __global__ void __launch_bounds__(kThreads, 1) encode_tc_kernel(EncodeAppendArgs
                 else sub = a.pool.base + (pb * Hkv + h) * a.pool.sub_bytes;
             }
         }
-        if (sub) {
-            store_words<W>(reinterpret_cast<uint32_t*>(sub + o_idx) + static_cast<int64_t>(slot) * W, words);
-            reinterpret_cast<float*>(sub + o_norm)[slot] = n;
+        uint32_t* widx = sub ? reinterpret_cast<uint32_t*>(sub + o_idx) + static_cast<int64_t>(slot) * W : nullptr;
+
+        float g2 = 0.0f;
+#pragma unroll 1
+        for (int ch = 0; ch < D / 32; ++ch) {
+            float v[32];
+            tc::tmem_ld32(tmem_row + 32 * ch, v);
+            uint32_t cw[KB];
+#pragma unroll
+            for (int q = 0; q < KB; ++q) cw[q] = 0u;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                const float y = v[i] * inv;
+                int code = 0;
+#pragma unroll
+                for (int j = 0; j < NM; ++j) code += y > mreg[j] ? 1 : 0;
+                const int bit = i * KB;
+                cw[bit >> 5] |= static_cast<uint32_t>(code) << (bit & 31);
+                if ((bit & 31) + KB > 32) cw[(bit >> 5) + 1] |= static_cast<uint32_t>(code) >> (32 - (bit & 31));
+                if constexpr (PROD) {
+                    const float r = __fsub_rn(y, s_c[code]);
+                    g2 = __fmaf_rn(r, r, g2);
+                    v[i] = r * 256.0f;
+                }
+            }
+            if (widx) store_words<KB>(widx + KB * ch, cw);
+            if constexpr (PROD) {
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    float f[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) f[e] = v[8 * q + e];
+                    store8<D>(A0, A1, tid, 32 * ch + 8 * q, f);
+                }
+            }
         }
+        if (sub) reinterpret_cast<float*>(sub + o_norm)[slot] = n;
 
         if constexpr (PROD) {
             // ---------------- GEMM 2: Z = r~ S^T in three fp16 parts
