@@ -16,6 +16,7 @@ region; the cache (14.5 GB) is far larger than L2, so no flush is needed.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import json
 import math
 import os
@@ -59,7 +60,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self._t = threading.Thread(target=self._read, daemon=True)
             self._t.start()
@@ -234,6 +235,10 @@ def run_gpu(args):
     from turboquant_compressed_kv_tq_gb300 import workloads as wl
 
     w = wl.long_256k()
+    if args.layers:
+        # fewer layers of the same workload: a small case for profiler captures,
+        # never a headline number (the layer count is in config.workload)
+        w = dataclasses.replace(w, num_layers=args.layers)
     L, Hkv, Hq, D, Lq = w.num_layers, w.num_kv_heads, w.num_q_heads, w.head_dim, w.q_len
     N0 = w.seq_lens[0]
     A = w.append_per_step
@@ -367,7 +372,7 @@ def run_gpu(args):
         result = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": step_ms_max, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "scaling": "weak", "vs_baseline": None, "dtype": "f16+f32", "data": "synthetic",
             "config": {"workload": _workload_text(w),
                        "bytes_per_step": bytes_per_step, "record_bytes_per_token_head": rec_bytes,
                        "l2": "inputs larger than L2: each step reads a 14.5 GB compressed cache",
@@ -400,10 +405,12 @@ def run_gpu(args):
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=32)
+    ap.add_argument("--steps", type=int, default=256)  # the workload's 256 decode steps
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--layers", type=int, default=0,
+                    help="run only the first L layers (profiling case; default: all 64)")
     args = ap.parse_args(argv)
     if args.warmup < 3 and args.impl != "reference":
         args.warmup = 3

@@ -35,86 +35,137 @@ struct MmaArgs {
 // rounding remainder fp16(q' - fp16(q')), so that two MMAs against the exact
 // fp16 codebook operand carry q' to about 22 bits.
 constexpr int kQThreads = 256;
+constexpr int kQStride = kD + 8;  // fp16 row stride of the query operand tiles (conflict-free fragments)
 
-__host__ __device__ constexpr size_t qfrag_smem_bytes(bool prod) {
-    return (prod ? 2u : 1u) * kD * kD * 4u + 3u * kRows * kD * 4u + 16u;
+struct QSmem {
+    uint16_t R[2][kD * kD];         // 16 R_k, fp16 hi / lo, core-matrix layout
+    uint16_t S[2][kD * kD];         // S_k, fp16 hi / lo (prod keys)
+    uint16_t A[2][kRows * kQStride];  // scaled operand rows, fp16 hi / lo
+    float q1[kRows][kD];            // q' (fp32)
+    float q2[kRows][kD];            // q'' (fp32, prod keys)
+    float ex[kRows];                // per-row power-of-two scale exponents
+    uint64_t bar;
+};
+
+// Rows of the A tiles from fp32 values v[16][kD] scaled by 2^-ex[row]: hi and lo fp16.
+__device__ __forceinline__ void q_split_rows(QSmem& sm, const float* v, int tid) {
+    for (int e = tid; e < kRows * kD / 2; e += kQThreads) {
+        const int r = e / (kD / 2), k = 2 * (e % (kD / 2));
+        const float sc = scalbnf(1.0f, -static_cast<int>(sm.ex[r]));
+        const float a = v[r * kD + k] * sc, b = v[r * kD + k + 1] * sc;
+        const __half2 hi = __floats2half2_rn(a, b);
+        const float2 back = __half22float2(hi);
+        const __half2 lo = __floats2half2_rn(a - back.x, b - back.y);
+        *reinterpret_cast<__half2*>(&sm.A[0][r * kQStride + k]) = hi;
+        *reinterpret_cast<__half2*>(&sm.A[1][r * kQStride + k]) = lo;
+    }
+}
+
+// out[16][kD] = (A_hi + A_lo) (T_hi + T_lo)^T without the lo*lo term, times
+// 2^ex[row] / tscale: warp w computes output columns 16w .. 16w+15.
+__device__ __forceinline__ void q_gemm(QSmem& sm, const uint16_t (*T)[kD * kD], float tscale, float* out, int warp,
+                                       int lane) {
+    const int g = lane >> 2, j = lane & 3;
+    float acc[2][4] = {};
+#pragma unroll
+    for (int ks = 0; ks < kD / 16; ++ks) {
+        uint32_t ah[4], al[4];
+        const int k0 = 16 * ks + 2 * j;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const uint16_t* A = sm.A[h];
+            uint32_t* dst = h ? al : ah;
+            dst[0] = *reinterpret_cast<const uint32_t*>(A + g * kQStride + k0);
+            dst[1] = *reinterpret_cast<const uint32_t*>(A + (g + 8) * kQStride + k0);
+            dst[2] = *reinterpret_cast<const uint32_t*>(A + g * kQStride + k0 + 8);
+            dst[3] = *reinterpret_cast<const uint32_t*>(A + (g + 8) * kQStride + k0 + 8);
+        }
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+            const int n8 = 2 * warp + nt;  // core-matrix row group of the output columns
+            const int o0 = (n8 * (kD / 8) + 2 * ks) * 64 + g * 8 + 2 * j;
+            const uint32_t bh0 = *reinterpret_cast<const uint32_t*>(T[0] + o0);
+            const uint32_t bh1 = *reinterpret_cast<const uint32_t*>(T[0] + o0 + 64);
+            const uint32_t bl0 = *reinterpret_cast<const uint32_t*>(T[1] + o0);
+            const uint32_t bl1 = *reinterpret_cast<const uint32_t*>(T[1] + o0 + 64);
+            mma16816(acc[nt], ah, bh0, bh1);
+            mma16816(acc[nt], ah, bl0, bl1);
+            mma16816(acc[nt], al, bh0, bh1);
+        }
+    }
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+        const int c = 16 * warp + 8 * nt + 2 * j;
+        const float s0 = scalbnf(1.0f, static_cast<int>(sm.ex[g])) / tscale;
+        const float s1 = scalbnf(1.0f, static_cast<int>(sm.ex[g + 8])) / tscale;
+        out[g * kD + c] = acc[nt][0] * s0;
+        out[g * kD + c + 1] = acc[nt][1] * s0;
+        out[(g + 8) * kD + c] = acc[nt][2] * s1;
+        out[(g + 8) * kD + c + 1] = acc[nt][3] * s1;
+    }
 }
 
 template <int KB>
 __global__ void __launch_bounds__(kQThreads) qfrag_kernel(MmaArgs m) {
-    // one CTA per (sequence x kv head, row group): the 16 rows' q' and q'' in
-    // fp32 from tables staged in shared memory by one bulk copy; thread
-    // (i, half) runs 8 independent row chains for output coordinate i
-    extern __shared__ __align__(16) unsigned char qsm[];
+    // one CTA per (sequence x kv head, row group): q' = Q R^T and q'' = q' S^T
+    // for the 16 rows on the tensor cores, both operands split into fp16
+    // hi + lo (about 22 significant bits), tables staged by one bulk copy
+    extern __shared__ __align__(16) unsigned char qsm_raw[];
+    QSmem& sm = *reinterpret_cast<QSmem*>(qsm_raw);
     const DecodeArgs& a = m.a;
     const bool prod = a.kc.mode == TQ_MODE_PROD;
-    float* Rt = reinterpret_cast<float*>(qsm);   // [k][i] = R[i][k]
-    float* St = Rt + kD * kD;                    // prod
-    float* qs = St + (prod ? kD * kD : 0);       // [16][kD] query rows
-    float* q1 = qs + kRows * kD;                 // [16][kD] q'
-    float* q2 = q1 + kRows * kD;                 // [16][kD] q'' (prod)
-    uint64_t* bar = reinterpret_cast<uint64_t*>(q2 + kRows * kD);
     const int Hkv = a.pool.Hkv;
     const int bh = blockIdx.x;
     const int b = bh / Hkv, h = bh % Hkv;
     const int rg = blockIdx.y;
     const int RG = a.plan.row_groups;
     const int unit = bh * RG + rg;
-    const int tid = threadIdx.x;
-    const int i = tid & (kD - 1), half = tid >> 7;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
     if (tid == 0) {
-        mbar_init(bar, 1);
+        mbar_init(&sm.bar, 1);
         mbar_fence_init();
-        mbar_expect_tx(bar, (prod ? 2u : 1u) * kD * kD * 4u);
-        bulk_g2s(Rt, a.kc.Rt, kD * kD * 4, bar);
-        if (prod) bulk_g2s(St, a.kc.St, kD * kD * 4, bar);
+        mbar_expect_tx(&sm.bar, (prod ? 2u : 1u) * 2u * kD * kD * 2u);
+        bulk_g2s(sm.R, a.kc.Rtc, 2 * kD * kD * 2, &sm.bar);
+        if (prod) bulk_g2s(sm.S, a.kc.Stc, 2 * kD * kD * 2, &sm.bar);
     }
+    // query rows (fp32) into q2 as scratch, and each row's scale exponent
     for (int e = tid; e < kRows * kD; e += kQThreads) {
         const int rr = e / kD, k = e % kD;
         const int r = rg * kRows + rr;
         float v = 0.0f;
         if (r < a.plan.rows) {
-            const int g = r / a.Lq, l = r % a.Lq;
-            const int64_t src = ((static_cast<int64_t>(b) * a.Hq + h * a.G + g) * a.Lq + l) * kD + k;
+            const int gq = r / a.Lq, l = r % a.Lq;
+            const int64_t src = ((static_cast<int64_t>(b) * a.Hq + h * a.G + gq) * a.Lq + l) * kD + k;
             if (a.q_dtype == TQ_F32) v = static_cast<const float*>(a.q)[src];
             else if (a.q_dtype == TQ_BF16) v = __bfloat162float(static_cast<const __nv_bfloat16*>(a.q)[src]);
             else v = __half2float(static_cast<const __half*>(a.q)[src]);
         }
-        qs[e] = v;
-    }
-    const bool ok = mbar_wait(bar, 0);
-    if (__syncthreads_or(!ok)) {
-        if (tid == 0) atomicOr(a.err, TQ_DEVERR_TIMEOUT);
-        (void)mbar_wait(bar, 0);
-        return;
-    }
-    {
-        float acc[8];
-#pragma unroll
-        for (int r = 0; r < 8; ++r) acc[r] = 0.0f;
-#pragma unroll 4
-        for (int k = 0; k < kD; ++k) {
-            const float rt = Rt[k * kD + i];
-#pragma unroll
-            for (int r = 0; r < 8; ++r) acc[r] = fmaf(rt, qs[(8 * half + r) * kD + k], acc[r]);
-        }
-#pragma unroll
-        for (int r = 0; r < 8; ++r) q1[(8 * half + r) * kD + i] = acc[r];
+        sm.q2[rr][k] = v;
     }
     __syncthreads();
+    if (tid < kRows) {
+        float mx = 0.0f;
+        for (int k = 0; k < kD; ++k) mx = fmaxf(mx, fabsf(sm.q2[tid][k]));
+        sm.ex[tid] = mx > 0.0f ? static_cast<float>(ilogbf(mx)) : 0.0f;  // |q| * 2^-ex < 2
+    }
+    __syncthreads();
+    q_split_rows(sm, &sm.q2[0][0], tid);
+    const bool ok = mbar_wait(&sm.bar, 0);
+    if (__syncthreads_or(!ok)) {
+        if (tid == 0) atomicOr(a.err, TQ_DEVERR_TIMEOUT);
+        (void)mbar_wait(&sm.bar, 0);
+        return;
+    }
+    q_gemm(sm, sm.R, 16.0f, &sm.q1[0][0], warp, lane);  // the table holds 16 R
+    __syncthreads();
     if (prod) {
-        float acc[8];
-#pragma unroll
-        for (int r = 0; r < 8; ++r) acc[r] = 0.0f;
-#pragma unroll 4
-        for (int k = 0; k < kD; ++k) {
-            const float st = St[k * kD + i];
-#pragma unroll
-            for (int r = 0; r < 8; ++r) acc[r] = fmaf(st, q1[(8 * half + r) * kD + k], acc[r]);
-        }
-#pragma unroll
-        for (int r = 0; r < 8; ++r) q2[(8 * half + r) * kD + i] = acc[r];
+        // |q'| <= |q|_2 <= sqrt(128) * 2^(ex+1): scale q' by 2^-(ex+4)
+        if (tid < kRows) sm.ex[tid] += 4.0f;
+        __syncthreads();
+        q_split_rows(sm, &sm.q1[0][0], tid);
+        __syncthreads();
+        q_gemm(sm, sm.S, 1.0f, &sm.q2[0][0], warp, lane);
         __syncthreads();
     }
     // entry (row rr, which, ks, j, e): lane 4*(rr%8)+j, register 2e + (rr >= 8)
@@ -124,23 +175,23 @@ __global__ void __launch_bounds__(kQThreads) qfrag_kernel(MmaArgs m) {
     for (int e = tid; e < kRows * 128; e += kQThreads) {
         const int rr = e >> 7, x = e & 127;
         const int which = x >> 6, ks = (x >> 3) & 7, j = (x >> 1) & 3, ee = x & 1;
-        const int lane = 4 * (rr & 7) + j;
+        const int ln = 4 * (rr & 7) + j;
         const int reg = 2 * ee + (rr >= 8 ? 1 : 0);
         int pa, pb;
         const bool qjl = which && prod;
         mse_pair(qjl ? 1 : KB, 2 * ks + ee, pa, pb);
-        const float* q = (qjl ? q2 : q1) + rr * kD;
+        const float* q = qjl ? sm.q2[rr] : sm.q1[rr];
         const float sc = qjl ? s2 : s1;
         float va = q[32 * j + pa] * sc, vb = q[32 * j + pb] * sc;
         if (which && !qjl) {
             va -= __half2float(__float2half_rn(va));
             vb -= __half2float(__float2half_rn(vb));
         }
-        dst[((which * 8 + ks) * 32 + lane) * 4 + reg] = pack_half2(va, vb);
+        dst[((which * 8 + ks) * 32 + ln) * 4 + reg] = pack_half2(va, vb);
     }
     if (tid == 0) {
         m.cnt[unit] = 0u;
-        mbar_inval(bar);
+        mbar_inval(&sm.bar);
     }
 }
 
@@ -608,7 +659,7 @@ cudaError_t launch_mma(const MmaArgs& m, size_t smem, cudaStream_t s) {
     static std::atomic<uint64_t> qattr_set{0};
     if (!(qattr_set.load() & bit)) {
         cudaError_t e = cudaFuncSetAttribute(qfrag_kernel<KB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(qfrag_smem_bytes(true)));
+                                             static_cast<int>(sizeof(QSmem)));
         if (e != cudaSuccess) {
             (void)cudaGetLastError();
             return e;
@@ -616,7 +667,7 @@ cudaError_t launch_mma(const MmaArgs& m, size_t smem, cudaStream_t s) {
         qattr_set.fetch_or(bit);
     }
     const int RG = a.plan.row_groups;
-    qfrag_kernel<KB><<<dim3(a.batch * a.pool.Hkv, RG), kQThreads, qfrag_smem_bytes(KPROD), s>>>(m);
+    qfrag_kernel<KB><<<dim3(a.batch * a.pool.Hkv, RG), kQThreads, sizeof(QSmem), s>>>(m);
     g_launches.fetch_add(1, std::memory_order_relaxed);
     split_mma_kernel<KB, KPROD, VGROUP, VB>
         <<<dim3(a.plan.splits, a.pool.Hkv * RG, a.batch), kThreads, smem, s>>>(m);
