@@ -33,6 +33,13 @@ METRIC = "compressed-KV decode-attn HBM GB/s (% of peak) and steps/s @256k; enco
 UNIT = "GB/s"
 
 
+# DRAM bytes (read + write) ncu counted for one tq_decode_attention call of
+# this workload (split kernel 226.76 + 3.62 MB, query prep 0.18 MB); set to
+# None whenever those kernels change until they are captured again.
+DECODE_TRAFFIC_BYTES = 230.56e6
+DECODE_TRAFFIC_SOURCE = "profiles/decode_split_mma_long_256k_layer.md, profiles/decode_qfrag_long_256k_layer.md"
+
+
 def _peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -385,7 +392,8 @@ def run_gpu(args):
                        "model_tokens_per_s": N0 / (enc_ms * 1e-3),
                        "gb_s_in_out": (enc_tokens * (2 * 2 * D + rec_bytes)) / (enc_ms * 1e-3) / 1e9},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                         "frac": achieved / peak, "traffic": None, "peak_kind": peak_kind,
+                         "frac": achieved / peak, "traffic": DECODE_TRAFFIC_BYTES, "peak_kind": peak_kind,
+                         "traffic_source": DECODE_TRAFFIC_SOURCE,
                          "kernel": "tq_decode_attention (query prep + split + merge), per layer",
                          "avg_launch_ms": dec_ms, "algorithmic_bytes_per_launch": per_launch_bytes},
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,

@@ -33,11 +33,12 @@ namespace tq {
 namespace mmadec {
 
 constexpr int kD = 128;
-constexpr int kWarps = 8;
+constexpr int kWarps = 12;
 constexpr int kThreads = kWarps * 32;
-constexpr int kStages = 3;
+constexpr int kStages = 2;
 constexpr int kRows = 16;
 constexpr int kMaxTile = 64;
+constexpr int kQFragBytes = 2 * 8 * 32 * 16;  // query fragments of one unit
 constexpr unsigned kSpinLimit = 1u << 22;
 
 // ------------------------------------------------------------------ PTX helpers

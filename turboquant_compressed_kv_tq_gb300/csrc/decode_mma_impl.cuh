@@ -16,6 +16,7 @@ struct StageLayout {
     int off[7];             // stream offsets inside a stage (-1 = absent)
     int field[7];           // bytes per token of each stream
     int bar_off;            // byte offset of the mbarriers (past ring and merge areas)
+    int qs_off;             // byte offset of the query fragments (past the ring)
 };
 
 struct MmaArgs {
@@ -280,22 +281,14 @@ __global__ void __launch_bounds__(kThreads, 1) split_mma_kernel(MmaArgs m) {
     }
     __syncwarp();
 
-    // query fragments
-    uint32_t qa[8][4];
-    uint32_t qj[8][4];  // QJL query (prod keys) or low half of the split query (MSE keys)
+    // query fragments of this unit, shared by all warps: [2][8][32] uint4
+    const uint4* qsm = reinterpret_cast<const uint4*>(smem + st.qs_off);
     {
         const uint4* qf = m.qfrag + static_cast<int64_t>(unit) * 2 * 8 * 32;
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-            const uint4 v = qf[ks * 32 + lane];
-            qa[ks][0] = v.x; qa[ks][1] = v.y; qa[ks][2] = v.z; qa[ks][3] = v.w;
-        }
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-            const uint4 v = qf[(8 + ks) * 32 + lane];
-            qj[ks][0] = v.x; qj[ks][1] = v.y; qj[ks][2] = v.z; qj[ks][3] = v.w;
-        }
+        uint4* qd = reinterpret_cast<uint4*>(smem + st.qs_off);
+        for (int k = threadIdx.x; k < 2 * 8 * 32; k += kThreads) qd[k] = qf[k];
     }
+    __syncthreads();
     const auto ktab = mse_table<KB>(a.kc.c);
     typename MseTable<VGROUP ? 2 : VB>::type vtab{};
     if constexpr (!VGROUP) vtab = mse_table<VB>(a.vc.c);
@@ -392,13 +385,20 @@ __global__ void __launch_bounds__(kThreads, 1) split_mma_kernel(MmaArgs m) {
             }
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks) {
+                uint32_t qa[4], qj[4];
+                {
+                    const uint4 v = qsm[ks * 32 + lane];
+                    qa[0] = v.x; qa[1] = v.y; qa[2] = v.z; qa[3] = v.w;
+                    const uint4 w = qsm[(8 + ks) * 32 + lane];
+                    qj[0] = w.x; qj[1] = w.y; qj[2] = w.z; qj[3] = w.w;
+                }
 #pragma unroll
                 for (int nt = 0; nt < 2; ++nt) {
-                    mma16816(sc[nt], qa[ks], hk[nt][2 * ks], hk[nt][2 * ks + 1]);
+                    mma16816(sc[nt], qa, hk[nt][2 * ks], hk[nt][2 * ks + 1]);
                     if constexpr (KPROD)
-                        mma16816(sd[nt], qj[ks], dec1(sw[nt], 15 - ks, neg2[nt]), dec1(sw[nt], 7 - ks, neg2[nt]));
+                        mma16816(sd[nt], qj, dec1(sw[nt], 15 - ks, neg2[nt]), dec1(sw[nt], 7 - ks, neg2[nt]));
                     else
-                        mma16816(sd[nt], qj[ks], hk[nt][2 * ks], hk[nt][2 * ks + 1]);
+                        mma16816(sd[nt], qj, hk[nt][2 * ks], hk[nt][2 * ks + 1]);
                 }
             }
 #pragma unroll
@@ -548,7 +548,8 @@ __global__ void __launch_bounds__(kThreads, 1) split_mma_kernel(MmaArgs m) {
     const int tid = threadIdx.x;
     const int r = tid >> 4;
     const int dbase = (tid & 15) * 8;
-    {
+    const bool merger = tid < kRows * 16;  // 16 threads per row, 8 columns each
+    if (merger) {
         float M = -INFINITY;
         for (int w = 0; w < kWarps; ++w) M = fmaxf(M, cm[w * kRows + r]);
         float L = 0.0f, acc[8] = {};
@@ -579,7 +580,7 @@ __global__ void __launch_bounds__(kThreads, 1) split_mma_kernel(MmaArgs m) {
     if (s_ticket != static_cast<unsigned>(S - 1)) return;
     __threadfence();
     float* orot = cm;  // [16][kStride]
-    {
+    if (merger) {
         float M = -INFINITY;
         const float* mlu = m.ml + static_cast<int64_t>(unit) * S * kRows * 2;
         for (int s = 0; s < S; ++s) M = fmaxf(M, __ldcg(mlu + (s * kRows + r) * 2));
@@ -604,7 +605,7 @@ __global__ void __launch_bounds__(kThreads, 1) split_mma_kernel(MmaArgs m) {
     }
     __syncthreads();
     const int row = rg * kRows + r;
-    if (row < a.plan.rows) {
+    if (merger && row < a.plan.rows) {
         float res[8];
         if constexpr (!VGROUP) {
             for (int k = 0; k < 8; ++k) res[k] = 0.0f;

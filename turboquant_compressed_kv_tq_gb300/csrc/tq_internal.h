@@ -95,6 +95,7 @@ struct DecodePlan {
     int st_field[7];
     int st_bytes;
     int bar_off;      // shared-memory offset of the stage barriers
+    int qs_off;       // shared-memory offset of the query fragments
     size_t smem;      // dynamic shared memory of the split kernel
     size_t q_bytes;   // SIMT: q' and q'' buffers (each); tensor cores: query fragments
     size_t cnt_bytes; // tensor cores: per-unit arrival counters
