@@ -37,7 +37,8 @@ UNIT = "GB/s"
 # this workload (split kernel 226.76 + 3.62 MB, query prep 0.18 MB); set to
 # None whenever those kernels change until they are captured again.
 DECODE_TRAFFIC_BYTES = 230.56e6
-DECODE_TRAFFIC_SOURCE = "profiles/decode_split_mma_long_256k_layer.md, profiles/decode_qfrag_long_256k_layer.md"
+DECODE_TRAFFIC_SOURCE = ("ncu dram__bytes_read.sum + dram__bytes_write.sum of split_mma_kernel and qfrag_kernel, "
+                         "one layer of this workload: bench.py --layers 1 --steps 4 --warmup 3")
 
 
 def _peaks():
