@@ -319,10 +319,11 @@ __global__ void __launch_bounds__(kThreads, 1) split_mma_kernel(MmaArgs m) {
             for (int k = 0; k < 7; ++k)
                 if (st.off[k] >= 0) total += TT * st.field[k];
             mbar_expect_tx(bar, total);
+            const uint64_t pol = policy_evict_first();
             for (int k = 0; k < 7; ++k)
                 if (st.off[k] >= 0)
-                    bulk_g2s(dst + st.off[k], base + a.pool.off[k] + static_cast<int64_t>(slot0) * st.field[k],
-                             TT * st.field[k], bar);
+                    bulk_g2s_once(dst + st.off[k], base + a.pool.off[k] + static_cast<int64_t>(slot0) * st.field[k],
+                                  TT * st.field[k], bar, pol);
         }
     };
 
