@@ -41,13 +41,16 @@ DECODE_TRAFFIC_SOURCE = ("ncu dram__bytes_read.sum + dram__bytes_write.sum of sp
                          "one layer of this workload: bench.py --layers 1 --steps 4 --warmup 3")
 
 
-def _peaks():
+def _peaks(key: str = "hbm_gbs"):
+    """A measured peak of this GPU pool (HBM copy GB/s or bf16 TFLOP/s), else
+    the earlier single measurement the pool's notes give as a fallback."""
+    fallback = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
             p = json.load(f)
-        return float(p["hbm_gbs"]), "measured"
+        return float(p[key]), "measured"
     except Exception:
-        return 6800.0, "fallback"
+        return fallback[key], "fallback"
 
 
 # ------------------------------------------------------------------ clocks
@@ -224,6 +227,50 @@ def _workload_text(w):
 
 # ------------------------------------------------------------------ GPU arm
 
+def measure_prefill_attention(tq, wl, dev, reps: int = 3):
+    """Prefill attention of one layer with the long-context codecs: an 8192-token
+    chunk (64 query heads) attending to a 24,576-token compressed prefix and
+    causally to itself. Useful FLOPs: 2 x (QK^T + PV) over the causal key ranges."""
+    import torch
+    base = wl.long_256k()
+    C, P = 8192, 24576
+    w = dataclasses.replace(base, num_layers=1, seq_lens=(P + C,), q_len=C)
+    D, Hkv, Hq, BT = w.head_dim, w.num_kv_heads, w.num_q_heads, w.block_tokens
+    N = P + C
+    nblk = N // BT
+    kc = tq.Codec(D, w.key.bits, w.key.mode, w.key.seed)
+    vc = tq.Codec(D, w.value.bits, w.value.mode, w.value.seed)
+    cache = tq.CompressedKVCache(kc, vc, 1, nblk, BT, Hkv, dev)
+    starts = torch.arange(0, N, w.prefill_chunk, dtype=torch.int32, device=dev)
+    for c in range(N // w.prefill_chunk):
+        k = wl.kv_chunk(w, 0, 0, c * w.prefill_chunk, w.prefill_chunk, "k", dev).unsqueeze(0)
+        v = wl.kv_chunk(w, 0, 0, c * w.prefill_chunk, w.prefill_chunk, "v", dev).unsqueeze(0)
+        cache.append(0, k, v, starts[c:c + 1], None, nblk)
+    q = wl.queries(w, 0, 0, dev)
+    sl = torch.tensor([N], dtype=torch.int32, device=dev)
+    ws = torch.empty(cache.prefill_workspace_bytes(1, Hq, C), dtype=torch.uint8, device=dev)
+    out = torch.empty(1, Hq, C, D, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    cache.prefill_attention(0, q, sl, None, nblk, out, ws)
+    torch.cuda.synchronize(dev)
+    times = []
+    for _ in range(reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        cache.prefill_attention(0, q, sl, None, nblk, out, ws)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        times.append(e0.elapsed_time(e1))
+    assert tq.tq_device_error() == 0
+    ms = statistics.median(times)
+    keys = C * P + C * (C + 1) / 2            # visible keys summed over the chunk's positions
+    flops = 2.0 * 2.0 * Hq * keys * D
+    return {"workload": f"long_256k codecs, one layer: {C}-token chunk, {P}-token compressed prefix, "
+                        f"{Hq} query heads, GQA {Hq // Hkv}, causal", "ms": ms,
+            "tflops_useful": flops / (ms * 1e-3) / 1e12, "chunk_tokens_per_s": C / (ms * 1e-3),
+            "kernel": "qfrag_kernel + prefill_kernel (mma.sync)"}
+
+
 def run_gpu(args):
     import numpy as np
     import torch
@@ -370,6 +417,12 @@ def run_gpu(args):
 
     enc_tokens = N0 * L * Hkv
     result = None
+    pfa = None
+    if rank == 0 and not args.no_prefill_attention:
+        del steps_in, pin_in
+        pfa = measure_prefill_attention(tq, wl, dev)
+        peak_t, _ = _peaks("bf16_tflops")
+        pfa["frac_of_bf16_peak"] = pfa["tflops_useful"] / peak_t if peak_t else None
     if rank == 0:
         cpu = None
         if world == 1 and not args.no_cpu_baseline:
@@ -402,6 +455,8 @@ def run_gpu(args):
             "gpu_launches": launches,
             "clocks": clocks,
         }
+        if pfa:
+            result["prefill_attention"] = pfa
         if cpu:
             result["cpu_baseline"] = cpu
         print(json.dumps(result), flush=True)
@@ -418,6 +473,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-prefill-attention", action="store_true",
+                    help="skip the one-layer prefill-attention measurement")
     ap.add_argument("--layers", type=int, default=0,
                     help="run only the first L layers (profiling case; default: all 64)")
     args = ap.parse_args(argv)

@@ -278,6 +278,38 @@ tq_status tq_decode_attention(const tq_codec *key_codec, const tq_codec *value_c
                               int max_seq_len, float scale, float *out, void *workspace,
                               size_t workspace_bytes, tq_stream_t stream);
 
+/* ------------------------------------------------------------------ */
+/* Prefill attention                                                    */
+/* ------------------------------------------------------------------ */
+
+/* Workspace (device bytes) tq_prefill_attention needs for these sizes. */
+tq_status tq_prefill_workspace_bytes(const tq_cache_desc *cache, int batch, int num_q_heads,
+                                     int q_len, size_t *bytes);
+
+/*
+ * Prefill attention over layer `layer` of the compressed cache: the function
+ * of tq_decode_attention for a long query chunk ("omlx/turboquant_kv.py":
+ * BatchTurboQuantKVCache inherits prefill_attention from the cache it wraps,
+ * with the causal mask offset by the written end, make_mask). The q_len
+ * query positions are the newest of each sequence, already appended; query
+ * l attends to keys t <= seq_lens[b] - q_len + l, scores and values exactly
+ * as tq_decode_attention defines them. Each key/value tile is decoded once
+ * for 128 query rows (8 groups of 16) instead of once per 16, and no split-K
+ * is needed.
+ *   q, out, seq_lens, block_table, max_blocks, scale: as tq_decode_attention.
+ *   workspace device, >= tq_prefill_workspace_bytes(...), 256-byte aligned
+ *        (query fragments, 8 KB per 16 query rows of a KV head).
+ * head_dim 128; keys prod 3-bit with MSE 3/4-bit or group 4-bit values, or
+ * keys and values MSE 4-bit (TQ_ERR_UNSUPPORTED otherwise);
+ * (num_q_heads/num_kv_heads) * q_len / 16 <= 65535.
+ */
+tq_status tq_prefill_attention(const tq_codec *key_codec, const tq_codec *value_codec,
+                               const tq_cache_desc *cache, int layer, const void *q,
+                               tq_dtype q_dtype, int batch, int num_q_heads, int q_len,
+                               const int32_t *seq_lens, const int32_t *block_table, int max_blocks,
+                               float scale, float *out, void *workspace, size_t workspace_bytes,
+                               tq_stream_t stream);
+
 /*
  * Decode attention without a caller-provided workspace. (The pages have no
  * counterpart; this exists for callers of this library.)

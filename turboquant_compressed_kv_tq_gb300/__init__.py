@@ -20,6 +20,7 @@ __all__ = [
     "tq_codec_create", "tq_codec_create_group", "tq_codec_destroy", "tq_codec_info",
     "tq_codec_build_host", "tq_codec_export", "tq_cache_desc_init", "tq_encode_append",
     "tq_quantize", "tq_decode_workspace_bytes", "tq_decode_attention", "tq_decode_attention_noalloc",
+    "tq_prefill_workspace_bytes", "tq_prefill_attention",
     "tq_device_error",
     "tq_launch_count", "tq_abi_version", "Codec", "CompressedKVCache", "TQError",
     "TQ_MODE_MSE", "TQ_MODE_PROD", "TQ_MODE_GROUP", "TQ_F32", "TQ_BF16", "TQ_F16",
@@ -164,6 +165,24 @@ def tq_decode_attention(key_codec: int, value_codec: int, desc: tq_cache_desc, l
                                     ws_bytes, _stream(stream)), "tq_decode_attention")
 
 
+def tq_prefill_workspace_bytes(desc: tq_cache_desc, batch: int, num_q_heads: int, q_len: int) -> int:
+    out = ctypes.c_size_t()
+    check(lib().tq_prefill_workspace_bytes(ctypes.byref(desc), batch, num_q_heads, q_len, ctypes.byref(out)),
+          "tq_prefill_workspace_bytes")
+    return out.value
+
+
+def tq_prefill_attention(key_codec: int, value_codec: int, desc: tq_cache_desc, layer: int, q,
+                         seq_lens, block_table, max_blocks: int, out, workspace, scale: float = 0.0,
+                         stream=None) -> None:
+    batch, hq, lq, _ = q.shape
+    ws_bytes = workspace.numel() * workspace.element_size()
+    check(lib().tq_prefill_attention(key_codec, value_codec, ctypes.byref(desc), layer, _ptr(q),
+                                     _dtype_code(q), batch, hq, lq, _ptr(seq_lens), _ptr(block_table),
+                                     max_blocks, scale, _ptr(out), _ptr(workspace), ws_bytes,
+                                     _stream(stream)), "tq_prefill_attention")
+
+
 def tq_decode_attention_noalloc(key_codec: int, value_codec: int, desc: tq_cache_desc, layer: int, q,
                                 seq_lens, block_table, max_blocks: int, max_seq_len: int, out,
                                 scale: float = 0.0, stream=None) -> None:
@@ -241,6 +260,14 @@ class CompressedKVCache:
 
     def workspace_bytes(self, batch, num_q_heads, q_len, max_seq_len):
         return tq_decode_workspace_bytes(self.desc, batch, num_q_heads, q_len, max_seq_len)
+
+    def prefill_workspace_bytes(self, batch, num_q_heads, q_len):
+        return tq_prefill_workspace_bytes(self.desc, batch, num_q_heads, q_len)
+
+    def prefill_attention(self, layer, q, seq_lens, block_table, max_blocks, out, workspace, scale=0.0,
+                          stream=None):
+        tq_prefill_attention(self.key.handle, self.value.handle, self.desc, layer, q, seq_lens, block_table,
+                             max_blocks, out, workspace, scale, stream)
 
     def decode(self, layer, q, seq_lens, block_table, max_blocks, max_seq_len, out, workspace,
                scale=0.0, stream=None):

@@ -94,6 +94,9 @@ SIGNATURES = {
                                   _P, _I, _I, _F, _P, _P, _SZ, _P]),
     "tq_decode_attention_noalloc": (_ST, [_P, _P, ctypes.POINTER(tq_cache_desc), _I, _P, _I, _I, _I, _I,
                                           _P, _P, _I, _I, _F, _P, _P]),
+    "tq_prefill_workspace_bytes": (_ST, [ctypes.POINTER(tq_cache_desc), _I, _I, _I, ctypes.POINTER(_SZ)]),
+    "tq_prefill_attention": (_ST, [_P, _P, ctypes.POINTER(tq_cache_desc), _I, _P, _I, _I, _I, _I, _P,
+                                   _P, _I, _F, _P, _P, _SZ, _P]),
     "tq_device_error": (_ST, [ctypes.POINTER(ctypes.c_uint32)]),
 }
 

@@ -456,6 +456,79 @@ tq_status tq_decode_attention(const tq_codec* kc, const tq_codec* vc, const tq_c
     return launch_decode(a, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
 }
 
+namespace {
+
+// Plan of a prefill call: the decode plan's record layout and codec class, with
+// the query rows of the whole chunk; returns TQ_OK or the reason it cannot run.
+tq_status prefill_plan(const tq_cache_desc* cache, int batch, int num_q_heads, int q_len, DecodePlan* plan,
+                       size_t* ws) {
+    if (!cache || batch < 0 || q_len <= 0 || num_q_heads <= 0) return TQ_ERR_INVALID_ARG;
+    if (num_q_heads % cache->num_kv_heads != 0) return TQ_ERR_INVALID_ARG;
+    const int G = num_q_heads / cache->num_kv_heads;
+    const int64_t rows = static_cast<int64_t>(G) * q_len;
+    if ((rows + 15) / 16 > 65535) return TQ_ERR_UNSUPPORTED;
+    const DecodePlan p = make_decode_plan(cache, batch > 0 ? batch : 1, G, q_len, q_len, 1);
+    if (p.kind != 1 || !mmadec::prefill_supported(p.kb, p.kprod, p.vgroup, p.vb)) return TQ_ERR_UNSUPPORTED;
+    if (plan) *plan = p;
+    if (ws) *ws = (static_cast<size_t>(batch) * cache->num_kv_heads * p.row_groups * 2 * 8 * 32 * 16 + 255) / 256 * 256;
+    return TQ_OK;
+}
+
+}  // namespace
+
+tq_status tq_prefill_workspace_bytes(const tq_cache_desc* cache, int batch, int num_q_heads, int q_len,
+                                     size_t* bytes) {
+    if (!bytes) return TQ_ERR_INVALID_ARG;
+    return prefill_plan(cache, batch, num_q_heads, q_len, nullptr, bytes);
+}
+
+tq_status tq_prefill_attention(const tq_codec* kc, const tq_codec* vc, const tq_cache_desc* cache, int layer,
+                               const void* q, tq_dtype q_dtype, int batch, int num_q_heads, int q_len,
+                               const int32_t* seq_lens, const int32_t* block_table, int max_blocks, float scale,
+                               float* out, void* workspace, size_t workspace_bytes, tq_stream_t stream) {
+    tq_status st = check_codecs_vs_cache(kc, vc, cache);
+    if (st != TQ_OK) return st;
+    if (layer < 0 || layer >= cache->num_layers || batch < 0 || q_len <= 0 || max_blocks <= 0)
+        return TQ_ERR_INVALID_ARG;
+    if (q_dtype != TQ_F32 && q_dtype != TQ_BF16 && q_dtype != TQ_F16) return TQ_ERR_INVALID_ARG;
+    if (static_cast<int64_t>(q_len) > static_cast<int64_t>(max_blocks) * cache->block_tokens) return TQ_ERR_CAPACITY;
+    if (!block_table && static_cast<int64_t>(batch) * max_blocks > cache->num_blocks) return TQ_ERR_CAPACITY;
+    DecodePlan plan{};
+    size_t need = 0;
+    st = prefill_plan(cache, batch, num_q_heads, q_len, &plan, &need);
+    if (st != TQ_OK) return st;
+    if (batch == 0) return TQ_OK;
+    if (batch > 65535) return TQ_ERR_INVALID_ARG;
+    if (!q || !out || !seq_lens || !workspace) return TQ_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return TQ_ERR_INVALID_ARG;
+    if (!aligned16(out)) return TQ_ERR_INVALID_ARG;
+    if (workspace_bytes < need) return TQ_ERR_CAPACITY;
+    unsigned* err = nullptr;
+    if (device_state(&err, nullptr) != TQ_OK) return TQ_ERR_CUDA;
+    DecodeArgs a{};
+    a.kc = dev_view(kc);
+    a.vc = dev_view(vc);
+    a.pool = pool_view(cache, layer);
+    a.q = q;
+    a.q_dtype = q_dtype;
+    a.batch = batch;
+    a.Hq = num_q_heads;
+    a.Lq = q_len;
+    a.G = num_q_heads / cache->num_kv_heads;
+    a.seq_lens = seq_lens;
+    a.table = block_table;
+    a.max_blocks = max_blocks;
+    a.scale = scale == 0.0f ? 1.0f / std::sqrt(static_cast<float>(cache->head_dim)) : scale;
+    a.out = out;
+    a.ws = workspace;
+    a.plan = plan;
+    a.err = err;
+    return mmadec::launch_prefill(a, static_cast<const uint4*>(workspace), reinterpret_cast<cudaStream_t>(stream)) ==
+                   cudaSuccess
+               ? TQ_OK
+               : TQ_ERR_CUDA;
+}
+
 tq_status tq_device_error(uint32_t* flags) {
     unsigned* err = nullptr;
     if (device_state(&err, nullptr) != TQ_OK) return TQ_ERR_CUDA;

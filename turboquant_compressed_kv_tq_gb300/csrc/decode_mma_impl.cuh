@@ -191,7 +191,7 @@ __global__ void __launch_bounds__(kQThreads) qfrag_kernel(MmaArgs m) {
         dst[((which * 8 + ks) * 32 + ln) * 4 + reg] = pack_half2(va, vb);
     }
     if (tid == 0) {
-        m.cnt[unit] = 0u;
+        if (m.cnt) m.cnt[unit] = 0u;
         mbar_inval(&sm.bar);
     }
 }

@@ -133,6 +133,10 @@ bool encode_tc_supported(const EncodeAppendArgs& a, int is_v);
 cudaError_t launch_encode_tc(const EncodeAppendArgs& a, int is_v, cudaStream_t s);
 cudaError_t launch_quantize(const QuantizeArgs& a, cudaStream_t s);
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);
+namespace mmadec {
+bool prefill_supported(int kb, bool kprod, bool vgroup, int vb);
+cudaError_t launch_prefill(const DecodeArgs& a, const uint4* qfrag, cudaStream_t s);
+}  // namespace mmadec
 #endif
 
 extern std::atomic<uint64_t> g_launches;
