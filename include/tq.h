@@ -187,6 +187,27 @@ tq_status tq_cache_desc_init(tq_cache_desc *desc, const tq_codec *key_codec,
                              int block_tokens, int num_kv_heads, void *pool, size_t pool_bytes,
                              size_t *required_bytes);
 
+/*
+ * Copy whole blocks of compressed records, every layer, from cache `src` to
+ * cache `dst`: block src_blocks[i] of src becomes block dst_blocks[i] of dst.
+ * The batch operations of "omlx/turboquant_kv.py" (BatchTurboQuantKVCache.merge,
+ * extend, extract, filter) become, on a paged cache, block-table edits plus
+ * this copy: merge and extend copy the joining sequences' blocks into the
+ * batch's pool and append their table rows, extract copies one sequence's
+ * blocks into a cache of its own, filter keeps table rows and copies nothing.
+ * Ragged lengths need no padding (seq_lens are per sequence), so the pages'
+ * left/right-padding realignment (prepare, finalize) has no counterpart.
+ *   src_blocks, dst_blocks device int32 [n]; when src and dst share a pool,
+ *   the two sets must not overlap.
+ * Errors: TQ_ERR_CONFIG_MISMATCH unless both caches have the same head_dim,
+ * heads, block size, layer count and codec configuration (the mixed-config
+ * guard of BatchTurboQuantKVCache.merge); TQ_ERR_INVALID_ARG for bad
+ * pointers or n < 0. Ids outside [0, num_blocks) are skipped and flagged
+ * (TQ_DEVERR_BLOCK).
+ */
+tq_status tq_cache_copy_blocks(const tq_cache_desc *src, const tq_cache_desc *dst, const int32_t *src_blocks,
+                               const int32_t *dst_blocks, int n, tq_stream_t stream);
+
 /* ------------------------------------------------------------------ */
 /* Encode                                                               */
 /* ------------------------------------------------------------------ */

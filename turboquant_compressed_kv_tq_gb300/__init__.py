@@ -20,7 +20,7 @@ __all__ = [
     "tq_codec_create", "tq_codec_create_group", "tq_codec_destroy", "tq_codec_info",
     "tq_codec_build_host", "tq_codec_export", "tq_cache_desc_init", "tq_encode_append",
     "tq_quantize", "tq_decode_workspace_bytes", "tq_decode_attention", "tq_decode_attention_noalloc",
-    "tq_prefill_workspace_bytes", "tq_prefill_attention",
+    "tq_prefill_workspace_bytes", "tq_prefill_attention", "tq_cache_copy_blocks",
     "tq_device_error",
     "tq_launch_count", "tq_abi_version", "Codec", "CompressedKVCache", "TQError",
     "TQ_MODE_MSE", "TQ_MODE_PROD", "TQ_MODE_GROUP", "TQ_F32", "TQ_BF16", "TQ_F16",
@@ -165,6 +165,13 @@ def tq_decode_attention(key_codec: int, value_codec: int, desc: tq_cache_desc, l
                                     ws_bytes, _stream(stream)), "tq_decode_attention")
 
 
+def tq_cache_copy_blocks(src: tq_cache_desc, dst: tq_cache_desc, src_blocks, dst_blocks, stream=None) -> None:
+    n = src_blocks.numel()
+    assert dst_blocks.numel() == n
+    check(lib().tq_cache_copy_blocks(ctypes.byref(src), ctypes.byref(dst), _ptr(src_blocks), _ptr(dst_blocks), n,
+                                     _stream(stream)), "tq_cache_copy_blocks")
+
+
 def tq_prefill_workspace_bytes(desc: tq_cache_desc, batch: int, num_q_heads: int, q_len: int) -> int:
     out = ctypes.c_size_t()
     check(lib().tq_prefill_workspace_bytes(ctypes.byref(desc), batch, num_q_heads, q_len, ctypes.byref(out)),
@@ -260,6 +267,10 @@ class CompressedKVCache:
 
     def workspace_bytes(self, batch, num_q_heads, q_len, max_seq_len):
         return tq_decode_workspace_bytes(self.desc, batch, num_q_heads, q_len, max_seq_len)
+
+    def copy_blocks_from(self, src: "CompressedKVCache", src_blocks, dst_blocks, stream=None):
+        """Blocks src_blocks of `src` (every layer) become blocks dst_blocks of this cache."""
+        tq_cache_copy_blocks(src.desc, self.desc, src_blocks, dst_blocks, stream)
 
     def prefill_workspace_bytes(self, batch, num_q_heads, q_len):
         return tq_prefill_workspace_bytes(self.desc, batch, num_q_heads, q_len)

@@ -97,6 +97,7 @@ SIGNATURES = {
     "tq_prefill_workspace_bytes": (_ST, [ctypes.POINTER(tq_cache_desc), _I, _I, _I, ctypes.POINTER(_SZ)]),
     "tq_prefill_attention": (_ST, [_P, _P, ctypes.POINTER(tq_cache_desc), _I, _P, _I, _I, _I, _I, _P,
                                    _P, _I, _F, _P, _P, _SZ, _P]),
+    "tq_cache_copy_blocks": (_ST, [ctypes.POINTER(tq_cache_desc), ctypes.POINTER(tq_cache_desc), _P, _P, _I, _P]),
     "tq_device_error": (_ST, [ctypes.POINTER(ctypes.c_uint32)]),
 }
 

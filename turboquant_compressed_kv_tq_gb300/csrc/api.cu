@@ -335,6 +335,27 @@ tq_status tq_cache_desc_init(tq_cache_desc* d, const tq_codec* kc, const tq_code
     return TQ_OK;
 }
 
+tq_status tq_cache_copy_blocks(const tq_cache_desc* src, const tq_cache_desc* dst, const int32_t* src_blocks,
+                               const int32_t* dst_blocks, int n, tq_stream_t stream) {
+    if (!src || !dst || n < 0) return TQ_ERR_INVALID_ARG;
+    if (src->head_dim != dst->head_dim || src->num_kv_heads != dst->num_kv_heads ||
+        src->block_tokens != dst->block_tokens || src->num_layers != dst->num_layers ||
+        src->key_mode != dst->key_mode || src->key_bits != dst->key_bits || src->key_seed != dst->key_seed ||
+        src->value_mode != dst->value_mode || src->value_bits != dst->value_bits ||
+        src->value_group != dst->value_group || src->value_seed != dst->value_seed ||
+        src->subblock_bytes != dst->subblock_bytes)
+        return TQ_ERR_CONFIG_MISMATCH;
+    if (n == 0) return TQ_OK;
+    if (!src->pool || !dst->pool || !src_blocks || !dst_blocks) return TQ_ERR_INVALID_ARG;
+    if (n > 2147483647 / 2 || src->num_layers > 65535) return TQ_ERR_INVALID_ARG;
+    unsigned* err = nullptr;
+    if (device_state(&err, nullptr) != TQ_OK) return TQ_ERR_CUDA;
+    return launch_copy_blocks(src, dst, src_blocks, dst_blocks, n, err, reinterpret_cast<cudaStream_t>(stream)) ==
+                   cudaSuccess
+               ? TQ_OK
+               : TQ_ERR_CUDA;
+}
+
 tq_status tq_encode_append(const tq_codec* kc, const tq_codec* vc, const tq_cache_desc* cache, int layer,
                            const void* k, const void* v, tq_dtype dtype, int batch, int n_new,
                            const int32_t* seq_lens, const int32_t* block_table, int max_blocks,

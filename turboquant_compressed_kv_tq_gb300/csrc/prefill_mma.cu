@@ -106,7 +106,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_kernel(PrefillArgs P) {
     typename MseTable<VGROUP ? 2 : VB>::type vtab{};
     if constexpr (!VGROUP) vtab = mse_table<VB>(a.vc.c);
 
-    const uint64_t pol = policy_evict_first();
+    // records are shared by all query blocks of a KV head: default L2 policy
     auto issue = [&](int i) {
         const int t0 = i * TT;
         const int lb = t0 / BT;
@@ -123,8 +123,8 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_kernel(PrefillArgs P) {
         mbar_expect_tx(bar, total);
         for (int k = 0; k < 7; ++k)
             if (st.off[k] >= 0)
-                bulk_g2s_once(dst + st.off[k], base + a.pool.off[k] + static_cast<int64_t>(slot0) * st.field[k],
-                              TT * st.field[k], bar, pol);
+                bulk_g2s(dst + st.off[k], base + a.pool.off[k] + static_cast<int64_t>(slot0) * st.field[k],
+                         TT * st.field[k], bar);
     };
     if (tid == 0 && ntiles > 0) issue(0);
 

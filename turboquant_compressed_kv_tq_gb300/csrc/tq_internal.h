@@ -133,6 +133,8 @@ bool encode_tc_supported(const EncodeAppendArgs& a, int is_v);
 cudaError_t launch_encode_tc(const EncodeAppendArgs& a, int is_v, cudaStream_t s);
 cudaError_t launch_quantize(const QuantizeArgs& a, cudaStream_t s);
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);
+cudaError_t launch_copy_blocks(const tq_cache_desc* src, const tq_cache_desc* dst, const int32_t* src_ids,
+                               const int32_t* dst_ids, int n, unsigned* err, cudaStream_t s);
 namespace mmadec {
 bool prefill_supported(int kb, bool kprod, bool vgroup, int vb);
 cudaError_t launch_prefill(const DecodeArgs& a, const uint4* qfrag, cudaStream_t s);
