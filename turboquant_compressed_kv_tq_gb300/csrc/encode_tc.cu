@@ -29,7 +29,15 @@ namespace tq {
 namespace {
 
 constexpr int kTileRows = 128;  // tokens per tile = MMA M = TMEM lanes used
-constexpr int kThreads = 128;   // one thread per token of the tile
+
+// Threads per token: prod keys (one CTA per SM: their operand tables fill
+// shared memory) split each token's TMEM row between two threads; MSE codecs
+// run two CTAs per SM with one thread per token.
+template <bool PROD>
+struct Split {
+    static constexpr int kTPT = PROD ? 2 : 1;
+    static constexpr int kThreads = kTileRows * kTPT;
+};
 
 template <int D, bool PROD>
 struct TcLayout {
@@ -40,7 +48,7 @@ struct TcLayout {
     static constexpr int oA0 = oS + (PROD ? kTab : 0);   // inputs, then residual hi
     static constexpr int oA1 = oA0 + kTile;              // residual lo (prod)
     static constexpr int oMisc = oA1 + (PROD ? kTile : 0);
-    static constexpr int kBytes = oMisc + 256;
+    static constexpr int kBytes = oMisc + 2048;
     static constexpr uint32_t kLbo = 128;                // next 8 columns (K)
     static constexpr uint32_t kSbo = 16 * D;             // next 8 rows (M/N)
 };
@@ -98,20 +106,28 @@ __device__ __forceinline__ void store_words(uint32_t* dst, const uint32_t (&w)[N
 }
 
 template <int D, int KB, bool PROD>
-__global__ void __launch_bounds__(kThreads, 1) encode_tc_kernel(EncodeAppendArgs a, int is_v, int tiles_per_seq) {
+__global__ void __launch_bounds__(Split<PROD>::kThreads, 1)
+    encode_tc_kernel(EncodeAppendArgs a, int is_v, int tiles_per_seq) {
     using L = TcLayout<D, PROD>;
+    constexpr int TPT = Split<PROD>::kTPT;
     constexpr int NM = (1 << KB) - 1;   // midpoints
     constexpr int W = D * KB / 32;      // index words
     constexpr int WS = D / 32;          // sign words
+    constexpr int DH = D / TPT;         // columns per thread
+    constexpr int CH = DH / 32;         // 32-column chunks per thread
     extern __shared__ __align__(1024) unsigned char smem[];
     float* s_c = reinterpret_cast<float*>(smem + L::oMisc);
     float* s_m = s_c + 16;
     uint64_t* bar_tab = reinterpret_cast<uint64_t*>(smem + L::oMisc + 128);
     uint64_t* bar_mma = bar_tab + 1;
     uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bar_tab + 2);
+    float* s_n2 = reinterpret_cast<float*>(smem + L::oMisc + 256);    // [128] first-half norm sums
+    float* s_nrm = s_n2 + kTileRows;                                  // [128] norms
+    float* s_g2 = s_nrm + kTileRows;                                  // [128] second-half residual sums
 
     const CodecDev& cd = is_v ? a.vc : a.kc;
     const int tid = threadIdx.x, warp = tid >> 5;
+    const int row = tid & (kTileRows - 1), half = TPT == 2 ? (tid >> 7) : 0;
     const uint32_t sbase = tc::smem_addr(smem);
 
     if (warp == 0) {
@@ -134,7 +150,7 @@ __global__ void __launch_bounds__(kThreads, 1) encode_tc_kernel(EncodeAppendArgs
     __syncthreads();
     tc::tc_fence_after();
     const uint32_t tmem = *s_tmem;
-    const uint32_t tmem_row = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    const uint32_t tmem_row = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + DH * half;
     float mreg[NM];
 #pragma unroll
     for (int j = 0; j < NM; ++j) mreg[j] = s_m[j];
@@ -153,17 +169,17 @@ __global__ void __launch_bounds__(kThreads, 1) encode_tc_kernel(EncodeAppendArgs
     unsigned char* A0 = smem + L::oA0;
     unsigned char* A1 = smem + L::oA1;
 
-    // inputs of this thread's token in a tile, loaded one tile ahead
-    uint4 nraw[D / 8];
+    // this thread's columns of its token in a tile, loaded one tile ahead
+    uint4 nraw[DH / 8];
     auto load_row = [&](int64_t tl) {
         const int ts = static_cast<int>(tl % tiles_per_seq);
         const int bh = static_cast<int>(tl / tiles_per_seq);
-        const int t = ts * kTileRows + tid;
+        const int t = ts * kTileRows + row;
         const bool ok_row = tl < ntiles && t < a.n_new;
-        const int64_t row = (static_cast<int64_t>(bh / Hkv) * Hkv + bh % Hkv) * a.n_new + t;
-        const uint4* p = reinterpret_cast<const uint4*>(src + row * D * 2);
+        const int64_t r = (static_cast<int64_t>(bh / Hkv) * Hkv + bh % Hkv) * a.n_new + t;
+        const uint4* p = reinterpret_cast<const uint4*>(src + r * D * 2) + half * (DH / 8);
 #pragma unroll
-        for (int c8 = 0; c8 < D / 8; ++c8) nraw[c8] = ok_row ? __ldg(p + c8) : make_uint4(0, 0, 0, 0);
+        for (int c8 = 0; c8 < DH / 8; ++c8) nraw[c8] = ok_row ? __ldg(p + c8) : make_uint4(0, 0, 0, 0);
     };
     load_row(blockIdx.x);
 
@@ -171,31 +187,53 @@ __global__ void __launch_bounds__(kThreads, 1) encode_tc_kernel(EncodeAppendArgs
         const int ts = static_cast<int>(tile % tiles_per_seq);
         const int bh = static_cast<int>(tile / tiles_per_seq);
         const int h = bh % Hkv, b = bh / Hkv;
-        const int t = ts * kTileRows + tid;
+        const int t = ts * kTileRows + row;
         const bool valid = t < a.n_new;
 
-        // ---------------- this thread's token (loaded during the previous tile):
-        // norm in the sequential fma order, scaled fp16 operand row
-        uint4 raw[D / 8];
+        // ---------------- this thread's columns (loaded during the previous tile):
+        // the norm's sequential fma chain runs over the first half, then
+        // continues over the second half in the other thread of the token
+        uint4 raw[DH / 8];
 #pragma unroll
-        for (int c8 = 0; c8 < D / 8; ++c8) raw[c8] = nraw[c8];
+        for (int c8 = 0; c8 < DH / 8; ++c8) raw[c8] = nraw[c8];
         float n2 = 0.0f;
+        if (TPT == 1 || half == 0) {
 #pragma unroll
-        for (int c8 = 0; c8 < D / 8; ++c8)
+            for (int c8 = 0; c8 < DH / 8; ++c8)
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const float f = elem_f32(raw[c8], e, a.dtype);
-                n2 = __fmaf_rn(f, f, n2);
+                for (int e = 0; e < 8; ++e) {
+                    const float f = elem_f32(raw[c8], e, a.dtype);
+                    n2 = __fmaf_rn(f, f, n2);
+                }
+        }
+        float n;
+        if constexpr (TPT == 2) {
+            if (half == 0) s_n2[row] = n2;
+            __syncthreads();
+            if (half == 1) {
+                n2 = s_n2[row];
+#pragma unroll
+                for (int c8 = 0; c8 < DH / 8; ++c8)
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const float f = elem_f32(raw[c8], e, a.dtype);
+                        n2 = __fmaf_rn(f, f, n2);
+                    }
+                s_nrm[row] = __fsqrt_rn(n2);
             }
-        const float n = __fsqrt_rn(n2);
+            __syncthreads();
+            n = s_nrm[row];
+        } else {
+            n = __fsqrt_rn(n2);
+        }
         const int ex = n > 0.0f ? ilogbf(n) : 0;
         const float down = scalbnf(1.0f, -ex);
 #pragma unroll
-        for (int c8 = 0; c8 < D / 8; ++c8) {
+        for (int c8 = 0; c8 < DH / 8; ++c8) {
             float f[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e) f[e] = elem_f32(raw[c8], e, a.dtype) * down;
-            store8<D>(A0, nullptr, tid, 8 * c8, f);
+            store8<D>(A0, nullptr, row, DH * half + 8 * c8, f);
         }
         tc::fence_proxy_async_smem();
         tc::tc_fence_before();
@@ -247,7 +285,7 @@ __global__ void __launch_bounds__(kThreads, 1) encode_tc_kernel(EncodeAppendArgs
 
         float g2 = 0.0f;
 #pragma unroll 1
-        for (int ch = 0; ch < D / 32; ++ch) {
+        for (int ch = 0; ch < CH; ++ch) {
             float v[32];
             tc::tmem_ld32(tmem_row + 32 * ch, v);
             uint32_t cw[KB];
@@ -268,21 +306,22 @@ __global__ void __launch_bounds__(kThreads, 1) encode_tc_kernel(EncodeAppendArgs
                     v[i] = r * 256.0f;
                 }
             }
-            if (widx) store_words<KB>(widx + KB * ch, cw);
+            if (widx) store_words<KB>(widx + KB * (CH * half + ch), cw);
             if constexpr (PROD) {
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
                     float f[8];
 #pragma unroll
                     for (int e = 0; e < 8; ++e) f[e] = v[8 * q + e];
-                    store8<D>(A0, A1, tid, 32 * ch + 8 * q, f);
+                    store8<D>(A0, A1, row, DH * half + 32 * ch + 8 * q, f);
                 }
             }
         }
-        if (sub) reinterpret_cast<float*>(sub + o_norm)[slot] = n;
+        if (sub && half == 0) reinterpret_cast<float*>(sub + o_norm)[slot] = n;
 
         if constexpr (PROD) {
             // ---------------- GEMM 2: Z = r~ S^T in three fp16 parts
+            if (TPT == 2 && half == 1) s_g2[row] = g2;
             tc::fence_proxy_async_smem();
             tc::tc_fence_before();
             __syncthreads();
@@ -307,9 +346,9 @@ __global__ void __launch_bounds__(kThreads, 1) encode_tc_kernel(EncodeAppendArgs
             }
             phase ^= 1;
             tc::tc_fence_after();
-            uint32_t sw[WS];
+            uint32_t sw[CH];
 #pragma unroll
-            for (int ch = 0; ch < WS; ++ch) {
+            for (int ch = 0; ch < CH; ++ch) {
                 float v[32];
                 tc::tmem_ld32(tmem_row + 32 * ch, v);
                 uint32_t w = 0u;
@@ -318,8 +357,10 @@ __global__ void __launch_bounds__(kThreads, 1) encode_tc_kernel(EncodeAppendArgs
                 sw[ch] = w;
             }
             if (sub) {
-                store_words<WS>(reinterpret_cast<uint32_t*>(sub + a.pool.off[1]) + static_cast<int64_t>(slot) * WS, sw);
-                reinterpret_cast<float*>(sub + a.pool.off[3])[slot] = __fsqrt_rn(g2);
+                store_words<CH>(reinterpret_cast<uint32_t*>(sub + a.pool.off[1]) + static_cast<int64_t>(slot) * WS + CH * half,
+                                sw);
+                if (half == 0)
+                    reinterpret_cast<float*>(sub + a.pool.off[3])[slot] = __fsqrt_rn(TPT == 2 ? g2 + s_g2[row] : g2);
             }
         }
         // TMEM reads of this tile are complete before the next tile's MMAs
@@ -378,7 +419,8 @@ cudaError_t launch_tc(const EncodeAppendArgs& a, int is_v, cudaStream_t s) {
     int64_t grid = static_cast<int64_t>(sm_count()) * per_sm;
     if (grid <= 0) return cudaErrorInvalidDevice;
     if (grid > ntiles) grid = ntiles;
-    encode_tc_kernel<D, KB, PROD><<<static_cast<unsigned>(grid), kThreads, L::kBytes, s>>>(a, is_v, tiles_per_seq);
+    encode_tc_kernel<D, KB, PROD><<<static_cast<unsigned>(grid), Split<PROD>::kThreads, L::kBytes, s>>>(a, is_v,
+                                                                                                   tiles_per_seq);
     g_launches.fetch_add(1, std::memory_order_relaxed);
     return cudaGetLastError();
 }
