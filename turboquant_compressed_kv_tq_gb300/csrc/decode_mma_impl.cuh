@@ -2,6 +2,7 @@
 #pragma once
 
 #include "decode_mma.cuh"
+#include "tc_ptx.cuh"
 
 namespace tq {
 namespace mmadec {
@@ -153,6 +154,11 @@ __global__ void __launch_bounds__(kQThreads) qfrag_kernel(MmaArgs m) {
     __syncthreads();
     q_split_rows(sm, &sm.q2[0][0], tid);
     const bool ok = mbar_wait(&sm.bar, 0);
+    // the workspace is written below: the kernels before this one are done
+    // (the append before it waits for the decode before that); the split
+    // kernel may then start fetching records, which are all written by now
+    tc::grid_wait_prior();
+    tc::grid_release_dependents();
     if (__syncthreads_or(!ok)) {
         if (tid == 0) atomicOr(a.err, TQ_DEVERR_TIMEOUT);
         (void)mbar_wait(&sm.bar, 0);
@@ -281,14 +287,6 @@ __global__ void __launch_bounds__(kThreads, 1) split_mma_kernel(MmaArgs m) {
     }
     __syncwarp();
 
-    // query fragments of this unit, shared by all warps: [2][8][32] uint4
-    const uint4* qsm = reinterpret_cast<const uint4*>(smem + st.qs_off);
-    {
-        const uint4* qf = m.qfrag + static_cast<int64_t>(unit) * 2 * 8 * 32;
-        uint4* qd = reinterpret_cast<uint4*>(smem + st.qs_off);
-        for (int k = threadIdx.x; k < 2 * 8 * 32; k += kThreads) qd[k] = qf[k];
-    }
-    __syncthreads();
     const auto ktab = mse_table<KB>(a.kc.c);
     typename MseTable<VGROUP ? 2 : VB>::type vtab{};
     if constexpr (!VGROUP) vtab = mse_table<VB>(a.vc.c);
@@ -329,6 +327,16 @@ __global__ void __launch_bounds__(kThreads, 1) split_mma_kernel(MmaArgs m) {
 
     const int pre = my_n < kStages - 1 ? my_n : kStages - 1;
     for (int i = 0; i < pre; ++i) issue(i);
+    // query fragments of this unit, shared by all warps: [2][8][32] uint4
+    // (written by the query-prep kernel this one may overlap: wait for it)
+    const uint4* qsm = reinterpret_cast<const uint4*>(smem + st.qs_off);
+    tc::grid_wait_prior();
+    {
+        const uint4* qf = m.qfrag + static_cast<int64_t>(unit) * 2 * 8 * 32;
+        uint4* qd = reinterpret_cast<uint4*>(smem + st.qs_off);
+        for (int k = threadIdx.x; k < 2 * 8 * 32; k += kThreads) qd[k] = qf[k];
+    }
+    __syncthreads();
     int waited = 0;
     for (int i = 0; i < my_n; ++i) {
         if (i + kStages - 1 < my_n) {
@@ -506,6 +514,7 @@ __global__ void __launch_bounds__(kThreads, 1) split_mma_kernel(MmaArgs m) {
             for (int p = 0; p < 16; ++p) mma16816(o[p], pa, movmatrix_t(hA[p]), movmatrix_t(hB[p]));
         }
     }
+    tc::grid_release_dependents();  // the next kernel may start; it waits for this one before the workspace
     if (failed && lane == 0) atomicOr(a.err, TQ_DEVERR_TIMEOUT);
     // drain copies that were issued but never waited for (only after a timeout)
     if (failed) {
@@ -669,12 +678,14 @@ cudaError_t launch_mma(const MmaArgs& m, size_t smem, cudaStream_t s) {
         qattr_set.fetch_or(bit);
     }
     const int RG = a.plan.row_groups;
-    qfrag_kernel<KB><<<dim3(a.batch * a.pool.Hkv, RG), kQThreads, sizeof(QSmem), s>>>(m);
+    cudaError_t e = launch_overlapped(qfrag_kernel<KB>, dim3(a.batch * a.pool.Hkv, RG), dim3(kQThreads), sizeof(QSmem),
+                                      s, m);
     g_launches.fetch_add(1, std::memory_order_relaxed);
-    split_mma_kernel<KB, KPROD, VGROUP, VB>
-        <<<dim3(a.plan.splits, a.pool.Hkv * RG, a.batch), kThreads, smem, s>>>(m);
+    if (e != cudaSuccess) return e;
+    e = launch_overlapped(split_mma_kernel<KB, KPROD, VGROUP, VB>, dim3(a.plan.splits, a.pool.Hkv * RG, a.batch),
+                          dim3(kThreads), smem, s, m);
     g_launches.fetch_add(1, std::memory_order_relaxed);
-    return cudaGetLastError();
+    return e;
 }
 
 }  // namespace mmadec

@@ -222,6 +222,10 @@ __global__ void __launch_bounds__(D) encode_short_kernel(EncodeAppendArgs a) {
     unsigned char* codes = reinterpret_cast<unsigned char*>(bar + 1);  // [NV][D]
     const int i = threadIdx.x;
     const int n = a.n_new;
+    // the next kernel may start its prologue now; this grid completes only
+    // after the grid before it has (the wait at the end), so completion still
+    // orders everything earlier in the stream
+    tc::grid_release_dependents();
 
     if (i == 0) {
         tc::mbar_init(bar, 1);
@@ -244,6 +248,7 @@ __global__ void __launch_bounds__(D) encode_short_kernel(EncodeAppendArgs a) {
     if (__syncthreads_or(!ok)) {
         if (i == 0) atomicOr(a.err, TQ_DEVERR_TIMEOUT);
         (void)tc::mbar_wait(bar, 0);  // the copy may still land: bounded second wait
+        tc::grid_wait_prior();
         return;
     }
 
@@ -333,6 +338,7 @@ __global__ void __launch_bounds__(D) encode_short_kernel(EncodeAppendArgs a) {
     }
     __syncthreads();
     if (i == 0) tc::mbar_inval(bar);
+    tc::grid_wait_prior();
 }
 
 template <int D, int NV>
@@ -355,9 +361,9 @@ cudaError_t launch_short(const EncodeAppendArgs& a, bool values_rotated, cudaStr
         attr_set.fetch_or(bit);
     }
     const dim3 grid(a.pool.Hkv, a.batch, values_rotated ? 2 : 1);
-    encode_short_kernel<D, NV><<<grid, D, smem, s>>>(a);
+    const cudaError_t e = launch_overlapped(encode_short_kernel<D, NV>, grid, dim3(D), smem, s, a);
     g_launches.fetch_add(1, std::memory_order_relaxed);
-    return cudaGetLastError();
+    return e;
 }
 
 template <int D>

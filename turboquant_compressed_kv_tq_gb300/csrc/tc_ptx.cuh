@@ -150,5 +150,13 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// Programmatic dependent launch: wait until the grid this one depends on has
+// completed (its memory visible), or let the grids that depend on this one
+// start their prologues.
+__device__ __forceinline__ void grid_wait_prior() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+__device__ __forceinline__ void grid_release_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+}
+
 }  // namespace tc
 }  // namespace tq

@@ -127,6 +127,25 @@ struct DecodeArgs {
 DecodePlan make_decode_plan(const tq_cache_desc* d, int batch, int G, int Lq, int max_seq_len, int num_sms);
 
 #ifdef __CUDACC__
+// Launch with programmatic stream serialization: the kernel may start while
+// the previous kernel in the stream finishes; it must call griddepcontrol.wait
+// before it touches what that kernel (or anything before it) writes.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_overlapped(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                              Args... args) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 cudaError_t launch_encode_append(const EncodeAppendArgs& a, cudaStream_t s);
 cudaError_t launch_encode_block(const EncodeAppendArgs& a, int is_v, cudaStream_t s);
 bool encode_tc_supported(const EncodeAppendArgs& a, int is_v);
