@@ -18,7 +18,6 @@ checked here is:
 Expected values come from the oracle alone; the exact y and S r are recomputed
 here in fp64 from the oracle's fp32 tables.
 """
-import math
 
 import numpy as np
 import pytest
@@ -27,7 +26,7 @@ import torch
 import oracle as O
 import turboquant_compressed_kv_tq_gb300 as tq
 from turboquant_compressed_kv_tq_gb300 import workloads as wl
-from parity_util import GpuCase, compare_decode, oracle_decode, raw_kv, read_records, to_f32_np
+from parity_util import read_records, to_f32_np
 
 pytestmark = pytest.mark.gpu
 
@@ -179,22 +178,3 @@ def test_unknown_encode_policy_is_refused():
     with pytest.raises(tq.TQError) as e:
         cache.append(0, x, x, torch.zeros(1, dtype=torch.int32, device=DEV), None, 4)
     assert e.value.status == 1
-
-
-def test_decode_over_tensor_core_prefill():
-    # the bench's codecs and head layout, prefilled by the tensor-core encoder;
-    # the oracle decodes its own records (a rare tie-band code differs)
-    w = wl.long_256k()
-    import dataclasses
-    w = dataclasses.replace(w, seq_lens=(4099,), prefill_chunk=1024)
-    case = GpuCase(w, layers=[0], exact_encode=False)
-    case.prefill()
-    assert tq.tq_device_error() == 0
-    q = wl.queries(w, 0, 0, DEV)
-    out = to_f32_np(case.decode(0, q))
-    qn = to_f32_np(q).astype(np.float64)
-    K, V = raw_kv(w, 0, 0, case.seq_lens[0], DEV)
-    G = w.gqa
-    for h in range(w.num_kv_heads):
-        ref = oracle_decode(w, K[h], V[h], qn[0, h * G:(h + 1) * G])
-        compare_decode(out[0, h * G:(h + 1) * G], ref)

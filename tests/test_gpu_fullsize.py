@@ -1,13 +1,18 @@
 """Decode parity at the workloads' full sizes.
 
-The long-context case runs in the launch configuration the benchmark times
-(262,144 cached tokens, 256-token blocks, contiguous cache with no block
-table, tensor-core prefill in 8192-token chunks, a 2-token append through the
+The long-context case runs in the decode launch configuration the benchmark
+times (262,144 cached tokens, 256-token blocks, contiguous cache with no block
+table, prefill in 8192-token chunks, a 2-token append through the
 short-append kernel, then query length 2). The oracle cannot decode every
 output at these sizes in seconds, so each test compares sampled (sequence, KV
 head) outputs element by element against the oracle's decode of its own
 records, and checks the rest by properties that hold at any size (the device
 error word stays clear, every output is finite).
+
+The caches are written with the exact encode policy, so the GPU and the
+oracle decode identical records and the comparison measures the decode alone
+(the tensor-core prefill may differ from the oracle's codes inside the fp32
+tie band, which tests/test_gpu_encode_tc.py checks on its own).
 """
 import numpy as np
 import pytest
@@ -44,7 +49,7 @@ def test_long_context_full_size_bench_configuration():
     nblk = (cap + BT - 1) // BT
     kc = tq.Codec(D, w.key.bits, w.key.mode, w.key.seed)
     vc = tq.Codec(D, w.value.bits, w.value.mode, w.value.seed)
-    cache = tq.CompressedKVCache(kc, vc, 1, nblk, BT, Hkv, DEV)   # default policy, as the bench
+    cache = tq.CompressedKVCache(kc, vc, 1, nblk, BT, Hkv, DEV, exact_encode=True)
     starts = torch.arange(0, N0, C, dtype=torch.int32, device=DEV)
     for c in range(N0 // C):
         k = wl.kv_chunk(w, layer, 0, c * C, C, "k", DEV).unsqueeze(0)
@@ -74,7 +79,7 @@ def test_stack_32k_full_size_all_heads():
     # 32,768 tokens, 4-bit MSE keys and values, per-head scales, q_len 2
     w = wl.stack_32k()
     layer = 17
-    case = GpuCase(w, layers=[layer], exact_encode=False)
+    case = GpuCase(w, layers=[layer])
     case.prefill()
     assert tq.tq_device_error() == 0
     q = wl.queries(w, layer, 0, DEV)
@@ -93,7 +98,7 @@ def test_paged_batch_full_size_sampled_sequences():
     # batched decode step with q_len 1
     w = wl.paged_batch()
     layer = 3
-    case = GpuCase(w, layers=[layer], exact_encode=False)
+    case = GpuCase(w, layers=[layer])
     case.prefill()
     B = w.batch
     k = torch.stack([wl.kv_chunk(w, layer, b, w.seq_lens[b], 1, "k", DEV) for b in range(B)])
