@@ -268,7 +268,7 @@ def measure_prefill_attention(tq, wl, dev, reps: int = 3):
     return {"workload": f"long_256k codecs, one layer: {C}-token chunk, {P}-token compressed prefix, "
                         f"{Hq} query heads, GQA {Hq // Hkv}, causal", "ms": ms,
             "tflops_useful": flops / (ms * 1e-3) / 1e12, "chunk_tokens_per_s": C / (ms * 1e-3),
-            "kernel": "qfrag_kernel + prefill_kernel (mma.sync)"}
+            "kernel": "qfrag_kernel + prefill_tc_kernel (tcgen05, TMEM)"}
 
 
 def run_gpu(args):

@@ -1,0 +1,522 @@
+// Prefill attention over the compressed cache on the 5th-generation tensor
+// cores (tcgen05.mma, TMEM accumulators), head_dim 128.
+//
+// The function is the decode attention's for any query length: a chunk of
+// q_len positions, already appended, attends to its sequence's compressed
+// prefix and causally to itself (query l sees keys t <= N - q_len + l). One
+// CTA owns 128 query rows (8 groups of 16) of one KV head -- TMEM lane = row,
+// two threads per row (column halves of its scores and output) -- and walks
+// the key/value tiles its rows can see; each tile is fetched once (1-D bulk
+// copies, double-buffered) and decoded once for all 128 rows. Per 64-token
+// tile:
+//   decode   the CTA decodes the tile once into shared-memory operands in the
+//            canonical no-swizzle K-major layout: key levels c_k[idx] and
+//            +-rnorm signs (64 tokens x 128, in the query fragments' coordinate
+//            order), values row-major, then transposed 8x8 block by 8x8 block
+//            (ldmatrix.trans + stmatrix) into V^T (128 dims x 64 tokens);
+//   scores   S = Q' K^T (+ Q'' sigma^T) as tcgen05.mma M 128, N 64, K 16 into 64
+//            TMEM columns;
+//   softmax  each thread reads its half row of S (tcgen05.ld), scales by the
+//            key norms, masks, exchanges the row maximum with the other half,
+//            keeps a running row maximum that only moves when the tile maximum
+//            exceeds it by 8 (log2 units: weights stay <= 2^8 and the output
+//            accumulator is rescaled rarely), writes its half row of
+//            P' = p * value norm (fp16) as the K-major A operand;
+//   values   O += P' V as tcgen05.mma M 128, N 128, K 16 into 128 TMEM columns.
+// At the end the two threads of a row read its row of O, divide by the row
+// sum and apply the inverse value rotation from a shared-memory copy of R_v.
+// Query fragments come from the decode path's query-prep kernel (workspace).
+#include "decode_mma_impl.cuh"
+#include "tc_ptx.cuh"
+
+namespace tq {
+namespace mmadec {
+namespace {
+
+constexpr int kTRows = 128;       // query rows per CTA = MMA M = TMEM lanes
+constexpr int kTThreads = 256;    // two threads per row: column halves of its scores and output
+constexpr int kTTok = 64;         // tokens per tile
+constexpr int kVStride = kD + 8;  // halves per row of the row-major value scratch
+constexpr float kRescaleGap = 8.0f;
+
+struct TcPrefillArgs {
+    DecodeArgs a;
+    StageLayout st;               // record streams of one tile
+    const uint4* qfrag;           // [unit][2][8][32] uint4 (query-prep output)
+    int qa_off, qj_off;           // Q' and Q'' (or Q' remainder) operands: 128 x 128 fp16
+    int k_off, s_off;             // key levels and sign operands: 64 x 128 fp16
+    int vs_off;                   // value scratch [64][kVStride] fp16
+    int vt_off;                   // V^T operand: 128 x 64 fp16
+    int p_off;                    // P' operand: 128 x 64 fp16
+    int norm_off;                 // key and value norms [2][64] floats
+    int rv_off;                   // R_v [kD][kD] floats
+    int bar_off;                  // mbarriers: 2 tiles, mma, R_v; then the TMEM slot and key limit
+};
+
+// Byte offset of (row, k) in a K-major operand whose K extent is KX.
+template <int KX>
+__device__ __forceinline__ int kmaj(int row, int k) {
+    return ((row >> 3) * (KX / 8) + (k >> 3)) * 128 + (row & 7) * 16 + (k & 7) * 2;
+}
+
+template <int KB, bool KPROD, bool VGROUP, int VB>
+__global__ void __launch_bounds__(kTThreads, 1) prefill_tc_kernel(TcPrefillArgs P) {
+    extern __shared__ __align__(1024) unsigned char smem[];
+    const DecodeArgs& a = P.a;
+    const StageLayout& st = P.st;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int Hkv = a.pool.Hkv, RG = a.plan.row_groups, BT = a.pool.BT, TT = st.tt;
+    const int h = blockIdx.y, b = blockIdx.z;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + P.bar_off);   // [0,1] tiles, [2] mma, [3] R_v
+    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + 4);
+    int* s_lim = reinterpret_cast<int*>(s_tmem + 1);
+    float* s_x = reinterpret_cast<float*>(smem + P.norm_off + 2 * kTTok * 4);   // [2][128] half-row exchange
+    float* kn = reinterpret_cast<float*>(smem + P.norm_off);
+    float* vn = kn + kTTok;
+    float* Rv = reinterpret_cast<float*>(smem + P.rv_off);
+    const uint32_t sbase = tc::smem_addr(smem);
+
+    // this thread's row and column half
+    const int row = tid & (kTRows - 1), half = tid >> 7;
+    const int w8 = row >> 4;                        // row group slot of the CTA
+    const int rg = blockIdx.x + w8 * gridDim.x;
+    const int r = rg * kRows + (row & 15);
+    const bool row_ok = rg < RG && r < a.plan.rows;
+    const int N = a.seq_lens[b];
+    const bool bad = N < a.Lq || N > a.max_blocks * BT;
+    if (bad && tid == 0 && blockIdx.x == 0 && h == 0) atomicOr(a.err, TQ_DEVERR_SEQLEN);
+    const int lim = row_ok ? N - a.Lq + (r % a.Lq) : -1;
+
+    if (warp == 0) {
+        tc::tmem_alloc(s_tmem, 256);   // S: columns 0..63, O: columns 128..255
+        tc::tmem_relinquish();
+    }
+    if (tid == 0) {
+        *s_lim = -1;
+        for (int s = 0; s < 4; ++s) tc::mbar_init(&bars[s], 1);
+        tc::mbar_fence_init();
+        if constexpr (!VGROUP) {
+            tc::mbar_expect_tx(&bars[3], kD * kD * 4);
+            tc::bulk_g2s(Rv, a.vc.R, kD * kD * 4, &bars[3]);
+        }
+    }
+    // Q operands from the query fragments (8 units of 16 rows)
+    {
+        const uint32_t* qf = reinterpret_cast<const uint32_t*>(P.qfrag);
+        for (int e = tid; e < 8 * 2048; e += kTThreads) {
+            const int slot = e >> 11, x = e & 2047;
+            const int which = x >> 10, ks = (x >> 7) & 7, ln = (x >> 2) & 31, reg = x & 3;
+            const int rgs = blockIdx.x + slot * gridDim.x;
+            const uint32_t v = rgs < RG ? qf[static_cast<int64_t>((b * Hkv + h) * RG + rgs) * 2048 + x] : 0u;
+            const int row = slot * kRows + (ln >> 2) + 8 * (reg & 1);
+            const int k = 16 * ks + 2 * (ln & 3) + 8 * (reg >> 1);
+            *reinterpret_cast<uint32_t*>(smem + (which ? P.qj_off : P.qa_off) + kmaj<kD>(row, k)) = v;
+        }
+    }
+    tc::fence_proxy_async_smem();
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+    atomicMax(s_lim, lim);
+    const uint32_t tmem = *s_tmem;
+    const uint32_t t_row = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+    const uint32_t tS = t_row + 32 * half, tO = t_row + 128 + 64 * half;   // this thread's columns
+    __syncthreads();
+    const int kend = bad ? 0 : min(*s_lim + 1, N);
+    const int ntiles = kend > 0 ? (kend + TT - 1) / TT : 0;
+
+    const auto ktab = mse_table<KB>(a.kc.c);
+    typename MseTable<VGROUP ? 2 : VB>::type vtab{};
+    if constexpr (!VGROUP) vtab = mse_table<VB>(a.vc.c);
+
+    auto issue = [&](int i) {   // thread 0
+        const int t0 = i * TT;
+        const int lb = t0 / BT;
+        const int slot0 = t0 - lb * BT;
+        int64_t pb = a.table ? static_cast<int64_t>(a.table[static_cast<int64_t>(b) * a.max_blocks + lb])
+                             : static_cast<int64_t>(b) * a.max_blocks + lb;
+        if (pb < 0 || pb >= a.pool.num_blocks) pb = 0;
+        const char* base = a.pool.base + (pb * Hkv + h) * a.pool.sub_bytes;
+        unsigned char* dst = smem + static_cast<size_t>(i & 1) * st.bytes;
+        unsigned total = 0;
+        for (int k = 0; k < 7; ++k)
+            if (st.off[k] >= 0) total += TT * st.field[k];
+        tc::mbar_expect_tx(&bars[i & 1], total);
+        for (int k = 0; k < 7; ++k)
+            if (st.off[k] >= 0)
+                tc::bulk_g2s(dst + st.off[k], base + a.pool.off[k] + static_cast<int64_t>(slot0) * st.field[k],
+                             TT * st.field[k], &bars[i & 1]);
+    };
+    if (tid == 0 && ntiles > 0) issue(0);
+
+    constexpr uint32_t idS = tc::idesc_f16_f32(kTRows, kTTok);
+    constexpr uint32_t idO = tc::idesc_f16_f32(kTRows, kD);
+    float m = -INFINITY, l = 0.0f;
+    unsigned mphase = 0;
+    bool failed = false, o_started = false, mma_pending = false;
+    int waited = 0;
+
+    for (int i = 0; i < ntiles && !failed; ++i) {
+        if (tid == 0 && i + 1 < ntiles) issue(i + 1);   // its stage was consumed in iteration i - 1
+        bool ok = tc::mbar_wait(&bars[i & 1], (i >> 1) & 1);
+        if (__syncthreads_or(!ok)) {
+            failed = true;
+            break;
+        }
+        waited = i + 1;
+        const unsigned char* sp = smem + static_cast<size_t>(i & 1) * st.bytes;
+        const int t0 = i * TT;
+        int valid = min(TT, kend - t0);
+        {
+            const int lb = t0 / BT;
+            const int64_t pb = a.table ? static_cast<int64_t>(a.table[static_cast<int64_t>(b) * a.max_blocks + lb])
+                                       : static_cast<int64_t>(b) * a.max_blocks + lb;
+            if (pb < 0 || pb >= a.pool.num_blocks) {
+                if (tid == 0) atomicOr(a.err, TQ_DEVERR_BLOCK);
+                valid = 0;
+            }
+        }
+
+        // ---------------- decode the tile: (token, 32-coordinate quarter) units
+        __half* vs = reinterpret_cast<__half*>(smem + P.vs_off);
+        for (int e = tid; e < kTTok * 4; e += kTThreads) {
+            const int tok = e >> 2, qt = e & 3;
+            __half* vrow = vs + tok * kVStride;
+            if (tok < valid) {
+                const uint32_t* kidx = reinterpret_cast<const uint32_t*>(sp + st.off[0]);
+                uint32_t kw[KB], hk[16];
+                load_words<KB>(kidx + tok * (4 * KB) + qt * KB, kw);
+                mse_chunk<KB>(kw, ktab, hk);
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks) {
+                    *reinterpret_cast<uint32_t*>(smem + P.k_off + kmaj<kD>(tok, 16 * ks + 2 * qt)) = hk[2 * ks];
+                    *reinterpret_cast<uint32_t*>(smem + P.k_off + kmaj<kD>(tok, 16 * ks + 8 + 2 * qt)) = hk[2 * ks + 1];
+                }
+                if constexpr (KPROD) {
+                    const uint32_t sw = reinterpret_cast<const uint32_t*>(sp + st.off[1])[tok * 4 + qt];
+                    const uint32_t hg = h_bits(-reinterpret_cast<const float*>(sp + st.off[3])[tok]);
+                    const uint32_t neg2 = hg | (hg << 16);
+#pragma unroll
+                    for (int ks = 0; ks < 8; ++ks) {
+                        *reinterpret_cast<uint32_t*>(smem + P.s_off + kmaj<kD>(tok, 16 * ks + 2 * qt)) =
+                            dec1(sw, 15 - ks, neg2);
+                        *reinterpret_cast<uint32_t*>(smem + P.s_off + kmaj<kD>(tok, 16 * ks + 8 + 2 * qt)) =
+                            dec1(sw, 7 - ks, neg2);
+                    }
+                }
+                const uint32_t* vidx = reinterpret_cast<const uint32_t*>(sp + st.off[4]);
+                uint32_t vw[VB], hv[16];
+                load_words<VB>(vidx + tok * (4 * VB) + qt * VB, vw);
+                if constexpr (VGROUP) {
+                    const int ng = kD / a.vc.group;
+                    const int gi = (32 * qt) / a.vc.group;
+                    const float sc = __half2float(reinterpret_cast<const __half*>(sp + st.off[5])[tok * ng + gi]);
+                    const float mn = __half2float(reinterpret_cast<const __half*>(sp + st.off[6])[tok * ng + gi]);
+                    const float mul = sc * (VB == 4 ? 16.0f : 4.0f);
+                    GroupChunk<VB>::run(vw, pack_half2(mul, mul), pack_half2(mn, mn), hv);
+#pragma unroll
+                    for (int p = 0; p < 16; ++p) {
+                        int pa, pb;
+                        group_pair(VB, p, pa, pb);
+                        vrow[32 * qt + pa] = __ushort_as_half(static_cast<unsigned short>(hv[p] & 0xFFFFu));
+                        vrow[32 * qt + pb] = __ushort_as_half(static_cast<unsigned short>(hv[p] >> 16));
+                    }
+                } else {
+                    mse_chunk<VB>(vw, vtab, hv);
+#pragma unroll
+                    for (int p = 0; p < 16; ++p) {
+                        int pa, pb;
+                        mse_pair(VB, p, pa, pb);
+                        vrow[32 * qt + pa] = __ushort_as_half(static_cast<unsigned short>(hv[p] & 0xFFFFu));
+                        vrow[32 * qt + pb] = __ushort_as_half(static_cast<unsigned short>(hv[p] >> 16));
+                    }
+                }
+                if (qt == 0) {
+                    kn[tok] = reinterpret_cast<const float*>(sp + st.off[2])[tok];
+                    vn[tok] = VGROUP ? 1.0f : reinterpret_cast<const float*>(sp + st.off[5])[tok];
+                }
+            } else {
+                // masked tokens meet P' = 0: keep every operand finite
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks) {
+                    *reinterpret_cast<uint32_t*>(smem + P.k_off + kmaj<kD>(tok, 16 * ks + 2 * qt)) = 0u;
+                    *reinterpret_cast<uint32_t*>(smem + P.k_off + kmaj<kD>(tok, 16 * ks + 8 + 2 * qt)) = 0u;
+                    if constexpr (KPROD) {
+                        *reinterpret_cast<uint32_t*>(smem + P.s_off + kmaj<kD>(tok, 16 * ks + 2 * qt)) = 0u;
+                        *reinterpret_cast<uint32_t*>(smem + P.s_off + kmaj<kD>(tok, 16 * ks + 8 + 2 * qt)) = 0u;
+                    }
+                }
+#pragma unroll
+                for (int q = 0; q < 16; ++q) reinterpret_cast<uint32_t*>(vrow + 32 * qt)[q] = 0u;
+                if (qt == 0) {
+                    kn[tok] = 0.0f;
+                    vn[tok] = 0.0f;
+                }
+            }
+        }
+        __syncthreads();
+        // values to V^T: 8x8 blocks (token block tb, dim block db), four per instruction
+        for (int it = warp; it < (kD / 8) * (kTTok / 8) / 4; it += kTThreads / 32) {
+            const int mi = lane >> 3, rr = lane & 7;
+            const int blk = 4 * it + mi;
+            const int db = blk >> 3, tb = blk & 7;
+            uint32_t x0, x1, x2, x3;
+            tc::ldmatrix_x4_trans(x0, x1, x2, x3, vs + (8 * tb + rr) * kVStride + 8 * db);
+            tc::stmatrix_x4(smem + P.vt_off + ((8 * db) >> 3) * (kTTok / 8) * 128 + tb * 128 + rr * 16, x0, x1, x2, x3);
+        }
+        tc::fence_proxy_async_smem();
+        tc::tc_fence_before();
+        __syncthreads();
+
+        // ---------------- scores on the tensor cores
+        if (tid == 0) {
+            tc::tc_fence_after();
+#pragma unroll
+            for (int s = 0; s < kD / 16; ++s) {
+                const uint64_t bk = tc::smem_desc(sbase + P.k_off + 256 * s, 128, 2048);
+                tc::mma_f16(tS, tc::smem_desc(sbase + P.qa_off + 256 * s, 128, 2048), bk, idS, s > 0);
+                if constexpr (KPROD)
+                    tc::mma_f16(tS, tc::smem_desc(sbase + P.qj_off + 256 * s, 128, 2048),
+                                tc::smem_desc(sbase + P.s_off + 256 * s, 128, 2048), idS, 1);
+                else
+                    tc::mma_f16(tS, tc::smem_desc(sbase + P.qj_off + 256 * s, 128, 2048), bk, idS, 1);
+            }
+            tc::mma_commit(&bars[2]);
+        }
+        mma_pending = true;
+        ok = tc::mbar_wait(&bars[2], mphase);
+        if (__syncthreads_or(!ok)) {
+            failed = true;
+            break;
+        }
+        mma_pending = false;
+        mphase ^= 1;
+        tc::tc_fence_after();
+
+        // ---------------- softmax of this thread's half row (log2 units); the
+        // row maximum is exchanged with the other half through shared memory
+        constexpr int HC = kTTok / 2;
+        float sv[HC];
+        {
+            float v[32];
+            tc::tmem_ld32(tS, v);
+#pragma unroll
+            for (int c = 0; c < HC; ++c) sv[c] = v[c];
+        }
+        float mx = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < HC; ++c) {
+            const int tc_ = HC * half + c;
+            const bool in = tc_ < valid && t0 + tc_ <= lim;
+            sv[c] = in ? sv[c] * kn[tc_] : -INFINITY;
+            mx = fmaxf(mx, sv[c]);
+        }
+        s_x[half * kTRows + row] = mx;
+        __syncthreads();
+        mx = fmaxf(mx, s_x[(half ^ 1) * kTRows + row]);
+        // move the running maximum only when this tile exceeds it by the gap
+        // (both halves take the same decision from the same values)
+        const bool move = mx > m + kRescaleGap || (m == -INFINITY && mx != -INFINITY);
+        const float alpha = move ? (m == -INFINITY ? 0.0f : ex2(m - mx)) : 1.0f;
+        if (move) {
+            l *= alpha;
+            m = mx;
+        }
+        if (__any_sync(0xffffffffu, move) && o_started) {
+#pragma unroll 1
+            for (int c = 0; c < kD / 2; c += 32) {
+                float v[32];
+                tc::tmem_ld32(tO + c, v);
+#pragma unroll
+                for (int e = 0; e < 32; ++e) v[e] *= alpha;
+                tc::tmem_st32(tO + c, v);
+            }
+        }
+        // P' = fp16(p * value norm) into the A operand; the row sum adds the
+        // rounded weights divided back (a zero-norm value contributes p)
+#pragma unroll
+        for (int c8 = 0; c8 < HC / 8; ++c8) {
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int c = 8 * c8 + 2 * e;
+                const int tc_ = HC * half + c;
+                const float p0 = m == -INFINITY ? 0.0f : ex2(sv[c] - m);
+                const float p1 = m == -INFINITY ? 0.0f : ex2(sv[c + 1] - m);
+                const float v0 = vn[tc_], v1 = vn[tc_ + 1];
+                const bool z0 = !(v0 > 0.0f), z1 = !(v1 > 0.0f);
+                w[e] = pack_half2(z0 ? 0.0f : p0 * v0, z1 ? 0.0f : p1 * v1);
+                const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[e]));
+                l += (z0 ? p0 : f.x * __fdividef(1.0f, v0)) + (z1 ? p1 : f.y * __fdividef(1.0f, v1));
+            }
+            *reinterpret_cast<uint4*>(smem + P.p_off + kmaj<kTTok>(row, HC * half + 8 * c8)) =
+                make_uint4(w[0], w[1], w[2], w[3]);
+        }
+        tc::fence_proxy_async_smem();
+        tc::tc_fence_before();
+        __syncthreads();
+
+        // ---------------- O += P' V on the tensor cores
+        if (tid == 0) {
+            tc::tc_fence_after();
+#pragma unroll
+            for (int s = 0; s < kTTok / 16; ++s)
+                tc::mma_f16(tO, tc::smem_desc(sbase + P.p_off + 256 * s, 128, 1024),
+                            tc::smem_desc(sbase + P.vt_off + 256 * s, 128, 1024), idO, (o_started || s > 0) ? 1u : 0u);
+            tc::mma_commit(&bars[2]);
+        }
+        o_started = true;
+        mma_pending = true;
+        ok = tc::mbar_wait(&bars[2], mphase);   // the tile's operands are free again
+        if (__syncthreads_or(!ok)) {
+            failed = true;
+            break;
+        }
+        mma_pending = false;
+        mphase ^= 1;
+        tc::tc_fence_after();
+    }
+    if (failed) {
+        if (tid == 0) atomicOr(a.err, TQ_DEVERR_TIMEOUT);
+        const int issued = min(ntiles, waited + 2);
+        for (int i = waited; i < issued; ++i) (void)tc::mbar_wait(&bars[i & 1], (i >> 1) & 1);
+        if (mma_pending) (void)tc::mbar_wait(&bars[2], mphase);
+    }
+    bool rv_ok = true;
+    if constexpr (!VGROUP) rv_ok = tc::mbar_wait(&bars[3], 0);
+    if (__syncthreads_or(!rv_ok) && tid == 0) atomicOr(a.err, TQ_DEVERR_TIMEOUT);
+
+    // ---------------- output rows: O / l staged in shared memory (over the
+    // query operands, padded rows), then rotated back by R_v, each thread
+    // writing its half of the row's dimensions
+    s_x[half * kTRows + row] = l;
+    __syncthreads();
+    l += s_x[(half ^ 1) * kTRows + row];
+    float* orow = reinterpret_cast<float*>(smem + P.qa_off) + row * (kD + 1);
+    const float inv = (o_started && !failed && l > 0.0f) ? 1.0f / l : 0.0f;
+#pragma unroll 1
+    for (int c = 0; c < kD / 2; c += 32) {
+        float v[32];
+        tc::tmem_ld32(tO + c, v);
+#pragma unroll
+        for (int e = 0; e < 32; ++e) orow[64 * half + c + e] = (o_started && !failed) ? v[e] * inv : 0.0f;  // TMEM unwritten otherwise
+    }
+    __syncthreads();
+    if (row_ok) {
+        const int gq = r / a.Lq, lq = r % a.Lq;
+        float* dst = a.out + ((static_cast<int64_t>(b) * a.Hq + h * a.G + gq) * a.Lq + lq) * kD;
+#pragma unroll 1
+        for (int d0 = 64 * half; d0 < 64 * half + 64; d0 += 32) {
+            float acc[32];
+            if constexpr (VGROUP) {
+#pragma unroll
+                for (int e = 0; e < 32; ++e) acc[e] = orow[d0 + e];
+            } else {
+#pragma unroll
+                for (int e = 0; e < 32; ++e) acc[e] = 0.0f;
+#pragma unroll 2
+                for (int i2 = 0; i2 < kD; ++i2) {
+                    const float ov = orow[i2];
+                    const float4* rr = reinterpret_cast<const float4*>(Rv + i2 * kD + d0);
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) {
+                        const float4 r4 = rr[q];
+                        acc[4 * q] = fmaf(ov, r4.x, acc[4 * q]);
+                        acc[4 * q + 1] = fmaf(ov, r4.y, acc[4 * q + 1]);
+                        acc[4 * q + 2] = fmaf(ov, r4.z, acc[4 * q + 2]);
+                        acc[4 * q + 3] = fmaf(ov, r4.w, acc[4 * q + 3]);
+                    }
+                }
+            }
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+                *reinterpret_cast<float4*>(dst + d0 + 4 * q) =
+                    make_float4(acc[4 * q], acc[4 * q + 1], acc[4 * q + 2], acc[4 * q + 3]);
+        }
+    }
+    tc::tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc::tc_fence_after();
+        tc::tmem_dealloc(tmem, 256);
+    }
+    if (tid == 0)
+        for (int s = 0; s < 4; ++s) tc::mbar_inval(&bars[s]);
+}
+
+template <int KB, bool KPROD, bool VGROUP, int VB>
+cudaError_t launch_prefill_tc_t(const TcPrefillArgs& P, size_t smem, cudaStream_t s) {
+    static std::atomic<uint64_t> attr_set{0};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const uint64_t bit = 1ull << (dev & 63);
+    if (!(attr_set.load() & bit)) {
+        cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<KB, KPROD, VGROUP, VB>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(qfrag_kernel<KB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     static_cast<int>(sizeof(QSmem)));
+        if (e != cudaSuccess) {
+            (void)cudaGetLastError();
+            return e;
+        }
+        attr_set.fetch_or(bit);
+    }
+    const DecodeArgs& a = P.a;
+    const int RG = a.plan.row_groups;
+    MmaArgs m{};
+    m.a = a;
+    m.qfrag = P.qfrag;
+    m.cnt = nullptr;
+    qfrag_kernel<KB><<<dim3(a.batch * a.pool.Hkv, RG), kQThreads, sizeof(QSmem), s>>>(m);
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    const int gx = (RG + 7) / 8;
+    prefill_tc_kernel<KB, KPROD, VGROUP, VB><<<dim3(gx, a.pool.Hkv, a.batch), kTThreads, smem, s>>>(P);
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+// Codec combinations built for prefill attention.
+bool prefill_supported(int kb, bool kprod, bool vgroup, int vb) {
+    if (kprod && kb == 2 && !vgroup && (vb == 3 || vb == 4)) return true;
+    if (kprod && kb == 2 && vgroup && vb == 4) return true;
+    if (!kprod && kb == 4 && !vgroup && vb == 4) return true;
+    return false;
+}
+
+cudaError_t launch_prefill(const DecodeArgs& a, const uint4* qfrag, cudaStream_t s) {
+    const DecodePlan& p = a.plan;
+    TcPrefillArgs P{};
+    P.a = a;
+    P.qfrag = qfrag;
+    P.st.tt = p.tile;
+    P.st.bytes = p.st_bytes;
+    for (int k = 0; k < 7; ++k) {
+        P.st.off[k] = p.st_off[k];
+        P.st.field[k] = p.st_field[k];
+    }
+    int off = 2 * p.st_bytes;
+    off = (off + 1023) / 1024 * 1024;
+    P.qa_off = off; off += kTRows * kD * 2;
+    P.qj_off = off; off += kTRows * kD * 2;
+    P.k_off = off; off += kTTok * kD * 2;
+    P.s_off = off; off += p.kprod ? kTTok * kD * 2 : 0;   // sign operands (prod keys only)
+    P.vt_off = off; off += kD * kTTok * 2;
+    P.p_off = off; off += kTRows * kTTok * 2;
+    P.vs_off = off; off += kTTok * kVStride * 2;
+    P.norm_off = off; off += 2 * kTTok * 4 + 2 * kTRows * 4;   // norms, then the half-row exchange
+    P.rv_off = off; off += kD * kD * 4;
+    P.bar_off = off; off += 64;
+    const size_t smem = static_cast<size_t>(off);
+    if (smem > 232448) return cudaErrorInvalidValue;   // the largest dynamic shared memory a CTA can opt into
+    if (p.kprod && p.kb == 2 && !p.vgroup && p.vb == 3) return launch_prefill_tc_t<2, true, false, 3>(P, smem, s);
+    if (p.kprod && p.kb == 2 && !p.vgroup && p.vb == 4) return launch_prefill_tc_t<2, true, false, 4>(P, smem, s);
+    if (p.kprod && p.kb == 2 && p.vgroup && p.vb == 4) return launch_prefill_tc_t<2, true, true, 4>(P, smem, s);
+    if (!p.kprod && p.kb == 4 && !p.vgroup && p.vb == 4) return launch_prefill_tc_t<4, false, false, 4>(P, smem, s);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace mmadec
+}  // namespace tq
