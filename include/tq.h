@@ -112,6 +112,25 @@ typedef struct {
 tq_status tq_codec_create(int head_dim, int bits, tq_mode mode, uint64_t seed, tq_codec **out);
 
 /*
+ * Fractional bit widths, as the codec rebuild of "omlx/turboquant_kv.py"
+ * (_rebuild_codecs) reads them: a width b that is not an integer (further
+ * than 1e-6 from round(b)) gives keys floor(b) bits and values ceil(b) bits,
+ * so that the pair averages b over a token (b = 3.5: 3-bit keys, 4-bit
+ * values); an integer width (within 1e-6) gives both (int)b, truncated as the
+ * page converts it (2.9999995 -> 2). tq_bits_split is host arithmetic only
+ * (no CUDA device needed); widths whose key or value bits fall outside 1..4,
+ * and non-finite b, return TQ_ERR_UNSUPPORTED with both outputs 0;
+ * TQ_ERR_INVALID_ARG for NULL outputs.
+ * tq_codec_pair_for_bits builds the two MSE codecs of that rule with
+ * tq_codec_create: keys (head_dim, key bits, seed), values (head_dim, value
+ * bits, seed + 1). On any error neither codec is created and both outputs
+ * are NULL; on success the caller owns both (tq_codec_destroy).
+ */
+tq_status tq_bits_split(double bits, int *key_bits, int *value_bits);
+tq_status tq_codec_pair_for_bits(int head_dim, double bits, uint64_t seed, tq_codec **key_codec,
+                                 tq_codec **value_codec);
+
+/*
  * Group codec ("turboquant/validate_moe_phase2.py", quantize_values): per
  * group of group_size consecutive coordinates an fp16 scale
  * (max-min)/(2^bits-1) and an fp16 minimum; codes round((x-min)/scale)

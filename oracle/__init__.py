@@ -64,6 +64,7 @@ def _declare(L):
         "tqo_index_bits": (_I, [_I, _I]),
         "tqo_packed_words": (_I, [_I, _I]),
         "tqo_record_bytes": (_I, [_I, _I, _I, _I]),
+        "tqo_bits_split": (None, [_D, ctypes.POINTER(_I), ctypes.POINTER(_I)]),
         "tqo_pack": (None, [_P, _I, _I, _P]),
         "tqo_unpack": (None, [_P, _I, _I, _P]),
         "tqo_f32_to_f16": (ctypes.c_uint16, [ctypes.c_float]),
@@ -109,6 +110,12 @@ def packed_words(D: int, ib: int) -> int:
 
 def record_bytes(D: int, bits: int, mode: int, group: int = 0) -> int:
     return lib().tqo_record_bytes(D, bits, mode, group)
+
+
+def bits_split(bits: float) -> tuple:
+    kb, vb = ctypes.c_int(), ctypes.c_int()
+    lib().tqo_bits_split(float(bits), ctypes.byref(kb), ctypes.byref(vb))
+    return kb.value, vb.value
 
 
 def normals(seed: int, stream: int, n: int) -> np.ndarray:

@@ -257,6 +257,16 @@ int tqo_record_bytes(int D, int bits, int mode, int group) {
     return 4 * w + 4 * (D / group); /* fp16 scale + fp16 min per group */
 }
 
+/* Key and value widths of a possibly fractional width b, as the codec rebuild
+ * of "omlx/turboquant_kv.py" (_rebuild_codecs) computes them: b is
+ * fractional unless it lies within 1e-6 of round(b); a fractional b gives keys
+ * floor(b) and values ceil(b), any other b gives int(b) (truncation) to both. */
+void tqo_bits_split(double b, int *key_bits, int *value_bits) {
+    int fractional = fabs(b - nearbyint(b)) > 1e-6;
+    *key_bits = fractional ? (int)floor(b) : (int)b;
+    *value_bits = fractional ? (int)ceil(b) : (int)b;
+}
+
 int tqo_codec_tables(int D, int bits, int mode, uint64_t seed,
                      float *R, float *S, float *c, float *m) {
     if (mode == TQO_GROUP) return 0;

@@ -37,6 +37,8 @@ int tqo_codec_tables(int D, int bits, int mode, uint64_t seed,
 
 int tqo_index_bits(int bits, int mode);
 int tqo_packed_words(int D, int index_bits);
+/* Key and value widths of a possibly fractional bit width. */
+void tqo_bits_split(double b, int *key_bits, int *value_bits);
 /* Bytes of one token's record for a codec. */
 int tqo_record_bytes(int D, int bits, int mode, int group);
 

@@ -91,3 +91,24 @@ def test_cache_layout_matches_oracle_without_device(libtq):
     for (D, kb, km, vb, vm, g) in [(128, 3, 1, 3, 0, 0), (128, 3, 1, 4, 2, 64), (256, 3, 1, 2, 2, 32),
                                    (128, 4, 0, 4, 0, 0)]:
         assert O.record_bytes(D, kb, km, 0) + O.record_bytes(D, vb, vm, g) in (108, 128, 200, 136)
+
+
+def test_bits_split_matches_oracle(libtq):
+    # host-only arithmetic: the library's split of a fractional width against the oracle's
+    widths = [1.0, 1.5, 2.0, 2.25, 2.5, 2.75, 3.0, 3.5, 3.9, 4.0, 3.0000005, 2.9999995, 3.00001,
+              1.0000004, 3.999999, 2.0 + 1e-7]
+    for b in widths:
+        assert tq.tq_bits_split(b) == O.bits_split(b), b
+
+
+def test_bits_split_rejects_out_of_range(libtq):
+    kb, vb = ctypes.c_int(7), ctypes.c_int(7)
+    for b in (0.5, 0.9999995, 4.5, 5.0, -3.0, float("nan"), float("inf")):
+        st = libtq.tq_bits_split(b, ctypes.byref(kb), ctypes.byref(vb))
+        assert st == _lib.TQ_ERR_UNSUPPORTED, b
+        assert kb.value == 0 and vb.value == 0
+    assert libtq.tq_bits_split(3.5, None, ctypes.byref(vb)) == _lib.TQ_ERR_INVALID_ARG
+    kh, vh = ctypes.c_void_p(1), ctypes.c_void_p(1)
+    # rejected before any device work, and both outputs cleared
+    assert libtq.tq_codec_pair_for_bits(128, 4.5, 0, ctypes.byref(kh), ctypes.byref(vh)) == _lib.TQ_ERR_UNSUPPORTED
+    assert not kh.value and not vh.value

@@ -42,6 +42,20 @@ def test_device_codec_tables_bit_exact(D, bits, mode, seed):
     assert np.array_equal(mid.view(np.uint32), oc.m.view(np.uint32))
 
 
+@pytest.mark.parametrize("D,bits,seed,kb,vb", [(128, 3.5, 0, 3, 4), (128, 2.5, 7, 2, 3),
+                                                (64, 3.0, 3, 3, 3), (256, 1.5, 11, 1, 2)])
+def test_codec_pair_for_fractional_bits(D, bits, seed, kb, vb):
+    # keys: MSE floor(b) bits with the seed; values: MSE ceil(b) bits with seed + 1
+    kc, vc = tq.Codec.pair_for_bits(D, bits, seed)
+    for c, b, s in ((kc, kb, seed), (vc, vb, seed + 1)):
+        assert (c.info["head_dim"], c.info["bits"], c.info["mode"], c.info["seed"]) == (D, b, O.MSE, s)
+        R, _, cen, mid = c.export()
+        oc = O.Codec(D, b, O.MSE, s)
+        assert np.array_equal(R.view(np.uint32), oc.R.view(np.uint32))
+        assert np.array_equal(cen.view(np.uint32), oc.c.view(np.uint32))
+        assert np.array_equal(mid.view(np.uint32), oc.m.view(np.uint32))
+
+
 # ------------------------------------------------------------------ encode
 
 def _vectors(n, D, dtype, seed, group=None):

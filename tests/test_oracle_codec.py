@@ -155,3 +155,23 @@ def test_stored_levels_are_nearest_halves(oracle_lib, D, bits, mode):
     mid = (cd.c[:-1].astype(np.float64) + cd.c[1:].astype(np.float64)) / 2
     assert np.array_equal(cd.m.astype(np.float64), mid)
     assert np.array_equal(cd.c[::-1], -cd.c)
+
+
+def test_fractional_bits_split(oracle_lib):
+    # the codec rebuild of "omlx/turboquant_kv.py" (_rebuild_codecs): a width
+    # more than 1e-6 from an integer gives keys floor(b) and values ceil(b);
+    # otherwise both get int(b), which truncates
+    cases = {
+        3.5: (3, 4), 2.5: (2, 3), 1.5: (1, 2), 2.25: (2, 3), 3.75: (3, 4),
+        1.0: (1, 1), 2.0: (2, 2), 3.0: (3, 3), 4.0: (4, 4),
+        3.0000005: (3, 3),      # inside the tolerance above 3
+        2.9999995: (2, 2),      # inside the tolerance below 3: int() truncates
+        3.00001: (3, 4),        # outside the tolerance: fractional
+        2.99999: (2, 3),
+    }
+    for b, want in cases.items():
+        assert O.bits_split(b) == want, b
+    # a half-integer width averages exactly over one key and one value
+    for b in (1.5, 2.5, 3.5):
+        kb, vb = O.bits_split(b)
+        assert (kb + vb) / 2 == b

@@ -18,6 +18,7 @@ from ._lib import (TQ_BF16, TQ_DEVERR_BLOCK, TQ_DEVERR_CAPACITY, TQ_DEVERR_SEQLE
 
 __all__ = [
     "tq_codec_create", "tq_codec_create_group", "tq_codec_destroy", "tq_codec_info",
+    "tq_bits_split", "tq_codec_pair_for_bits",
     "tq_codec_build_host", "tq_codec_export", "tq_cache_desc_init", "tq_encode_append",
     "tq_quantize", "tq_decode_workspace_bytes", "tq_decode_attention", "tq_decode_attention_noalloc",
     "tq_prefill_workspace_bytes", "tq_prefill_attention", "tq_cache_copy_blocks",
@@ -79,6 +80,20 @@ def tq_codec_create_group(head_dim: int, bits: int, group_size: int) -> int:
     check(lib().tq_codec_create_group(head_dim, bits, group_size, ctypes.byref(h)),
           "tq_codec_create_group")
     return h.value
+
+
+def tq_bits_split(bits: float) -> tuple:
+    """(key bits, value bits) of a possibly fractional width: floor/ceil, or b/b."""
+    kb, vb = ctypes.c_int(), ctypes.c_int()
+    check(lib().tq_bits_split(float(bits), ctypes.byref(kb), ctypes.byref(vb)), "tq_bits_split")
+    return kb.value, vb.value
+
+
+def tq_codec_pair_for_bits(head_dim: int, bits: float, seed: int) -> tuple:
+    kh, vh = ctypes.c_void_p(), ctypes.c_void_p()
+    check(lib().tq_codec_pair_for_bits(head_dim, float(bits), seed, ctypes.byref(kh), ctypes.byref(vh)),
+          "tq_codec_pair_for_bits")
+    return kh.value, vh.value
 
 
 def tq_codec_destroy(handle: int) -> None:
@@ -215,12 +230,22 @@ def tq_device_error() -> int:
 class Codec:
     """Owns one codec handle."""
 
-    def __init__(self, head_dim: int, bits: int, mode: int, seed: int = 0, group: int = 0):
-        if mode == TQ_MODE_GROUP:
+    def __init__(self, head_dim: int, bits: int, mode: int, seed: int = 0, group: int = 0,
+                 _handle: int = 0):
+        if _handle:
+            self.handle = _handle
+        elif mode == TQ_MODE_GROUP:
             self.handle = tq_codec_create_group(head_dim, bits, group)
         else:
             self.handle = tq_codec_create(head_dim, bits, mode, seed)
         self.info = tq_codec_info(self.handle)
+
+    @classmethod
+    def pair_for_bits(cls, head_dim: int, bits: float, seed: int = 0) -> tuple:
+        """(key codec, value codec) for a possibly fractional bit width: MSE
+        codecs of floor(bits) and ceil(bits) bits, seeds seed and seed + 1."""
+        kh, vh = tq_codec_pair_for_bits(head_dim, bits, seed)
+        return cls(0, 0, 0, _handle=kh), cls(0, 0, 0, _handle=vh)
 
     def __del__(self):
         h = getattr(self, "handle", None)

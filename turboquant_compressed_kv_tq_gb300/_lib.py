@@ -79,6 +79,8 @@ SIGNATURES = {
     "tq_status_string": (ctypes.c_char_p, [_ST]),
     "tq_codec_create": (_ST, [_I, _I, _I, _U64, ctypes.POINTER(_P)]),
     "tq_codec_create_group": (_ST, [_I, _I, _I, ctypes.POINTER(_P)]),
+    "tq_bits_split": (_ST, [ctypes.c_double, ctypes.POINTER(_I), ctypes.POINTER(_I)]),
+    "tq_codec_pair_for_bits": (_ST, [_I, ctypes.c_double, _U64, ctypes.POINTER(_P), ctypes.POINTER(_P)]),
     "tq_codec_destroy": (None, [_P]),
     "tq_codec_info": (_ST, [_P, ctypes.POINTER(tq_codec_info_t)]),
     "tq_codec_build_host": (_ST, [_I, _I, _I, _U64, _P, _P, _P, _P]),

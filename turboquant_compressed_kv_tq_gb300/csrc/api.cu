@@ -206,6 +206,44 @@ tq_status tq_codec_create(int head_dim, int bits, tq_mode mode, uint64_t seed, t
     return TQ_OK;
 }
 
+tq_status tq_bits_split(double bits, int* key_bits, int* value_bits) {
+    if (!key_bits || !value_bits) return TQ_ERR_INVALID_ARG;
+    *key_bits = *value_bits = 0;
+    if (!(bits > -1e9 && bits < 1e9)) return TQ_ERR_UNSUPPORTED;  // NaN, infinities, absurd widths
+    int kb, vb;
+    if (std::fabs(bits - std::nearbyint(bits)) <= 1e-6) {
+        kb = vb = static_cast<int>(bits);  // an integer width converts by truncation, as printed
+    } else {
+        kb = static_cast<int>(std::floor(bits));
+        vb = static_cast<int>(std::ceil(bits));
+    }
+    if (kb < 1 || vb > 4) return TQ_ERR_UNSUPPORTED;
+    *key_bits = kb;
+    *value_bits = vb;
+    return TQ_OK;
+}
+
+tq_status tq_codec_pair_for_bits(int head_dim, double bits, uint64_t seed, tq_codec** key_codec,
+                                 tq_codec** value_codec) {
+    if (!key_codec || !value_codec) return TQ_ERR_INVALID_ARG;
+    *key_codec = *value_codec = nullptr;
+    int kb = 0, vb = 0;
+    tq_status st = tq_bits_split(bits, &kb, &vb);
+    if (st != TQ_OK) return st;
+    tq_codec* kc = nullptr;
+    tq_codec* vc = nullptr;
+    st = tq_codec_create(head_dim, kb, TQ_MODE_MSE, seed, &kc);
+    if (st == TQ_OK) st = tq_codec_create(head_dim, vb, TQ_MODE_MSE, seed + 1, &vc);
+    if (st != TQ_OK) {
+        tq_codec_destroy(kc);
+        tq_codec_destroy(vc);
+        return st;
+    }
+    *key_codec = kc;
+    *value_codec = vc;
+    return TQ_OK;
+}
+
 tq_status tq_codec_create_group(int head_dim, int bits, int group_size, tq_codec** out) {
     if (!out) return TQ_ERR_INVALID_ARG;
     *out = nullptr;
