@@ -9,11 +9,13 @@
 // the key/value tiles its rows can see; each tile is fetched once (1-D bulk
 // copies, double-buffered) and decoded once for all 128 rows. Per 64-token
 // tile:
-//   decode   the CTA decodes the tile once into shared-memory operands in the
-//            canonical no-swizzle K-major layout: key levels c_k[idx] and
-//            +-rnorm signs (64 tokens x 128, in the query fragments' coordinate
-//            order), values row-major, then transposed 8x8 block by 8x8 block
-//            (ldmatrix.trans + stmatrix) into V^T (128 dims x 64 tokens);
+//   decode   the CTA decodes the tile once (one token and 32-coordinate
+//            quarter per thread) into shared-memory operands in the canonical
+//            no-swizzle K-major layout: key levels c_k[idx] and +-rnorm signs
+//            (64 tokens x 128, decoder pair p of quarter q at position
+//            32q + 2p, the query operands permuted to match), values in the
+//            same pair order, then transposed 8x8 block by 8x8 block
+//            (ldmatrix.trans + stmatrix) into V^T (128 columns x 64 tokens);
 //   scores   S = Q' K^T (+ Q'' sigma^T) as tcgen05.mma M 128, N 64, K 16 into 64
 //            TMEM columns;
 //   softmax  each thread reads its half row of S (tcgen05.ld), scales by the
@@ -108,8 +110,9 @@ __global__ void __launch_bounds__(kTThreads, 1) prefill_tc_kernel(TcPrefillArgs 
             const int which = x >> 10, ks = (x >> 7) & 7, ln = (x >> 2) & 31, reg = x & 3;
             const int rgs = blockIdx.x + slot * gridDim.x;
             const uint32_t v = rgs < RG ? qf[static_cast<int64_t>((b * Hkv + h) * RG + rgs) * 2048 + x] : 0u;
+            // fragment (ks, lane, reg) holds pair 2ks + reg/2 of coordinate quarter lane % 4
             const int row = slot * kRows + (ln >> 2) + 8 * (reg & 1);
-            const int k = 16 * ks + 2 * (ln & 3) + 8 * (reg >> 1);
+            const int k = 32 * (ln & 3) + 4 * ks + 2 * (reg >> 1);
             *reinterpret_cast<uint32_t*>(smem + (which ? P.qj_off : P.qa_off) + kmaj<kD>(row, k)) = v;
         }
     }
@@ -177,32 +180,36 @@ __global__ void __launch_bounds__(kTThreads, 1) prefill_tc_kernel(TcPrefillArgs 
             }
         }
 
-        // ---------------- decode the tile: (token, 32-coordinate quarter) units
-        __half* vs = reinterpret_cast<__half*>(smem + P.vs_off);
-        for (int e = tid; e < kTTok * 4; e += kTThreads) {
-            const int tok = e >> 2, qt = e & 3;
-            __half* vrow = vs + tok * kVStride;
+        // ---------------- decode the tile: one (token, 32-coordinate quarter)
+        // unit per thread, lanes on consecutive tokens; pair p of quarter qt
+        // goes to operand position 32 qt + 2p, so each operand row is written
+        // as four 16-byte chunks (a store phase covers 8 tokens: no conflicts)
+        {
+            static_assert(kTTok * 4 == kTThreads, "one unit per thread");
+            const int tok = 32 * (warp & 1) + lane, qt = warp >> 1;
+            __half* vrow = reinterpret_cast<__half*>(smem + P.vs_off) + tok * kVStride + 32 * qt;
+            auto kchunk = [&](int off, int i) {
+                return reinterpret_cast<uint4*>(smem + off + kmaj<kD>(tok, 32 * qt + 8 * i));
+            };
             if (tok < valid) {
                 const uint32_t* kidx = reinterpret_cast<const uint32_t*>(sp + st.off[0]);
                 uint32_t kw[KB], hk[16];
                 load_words<KB>(kidx + tok * (4 * KB) + qt * KB, kw);
                 mse_chunk<KB>(kw, ktab, hk);
 #pragma unroll
-                for (int ks = 0; ks < 8; ++ks) {
-                    *reinterpret_cast<uint32_t*>(smem + P.k_off + kmaj<kD>(tok, 16 * ks + 2 * qt)) = hk[2 * ks];
-                    *reinterpret_cast<uint32_t*>(smem + P.k_off + kmaj<kD>(tok, 16 * ks + 8 + 2 * qt)) = hk[2 * ks + 1];
-                }
+                for (int i = 0; i < 4; ++i) *kchunk(P.k_off, i) = make_uint4(hk[4 * i], hk[4 * i + 1], hk[4 * i + 2], hk[4 * i + 3]);
                 if constexpr (KPROD) {
                     const uint32_t sw = reinterpret_cast<const uint32_t*>(sp + st.off[1])[tok * 4 + qt];
                     const uint32_t hg = h_bits(-reinterpret_cast<const float*>(sp + st.off[3])[tok]);
                     const uint32_t neg2 = hg | (hg << 16);
+                    uint32_t hs[16];
 #pragma unroll
                     for (int ks = 0; ks < 8; ++ks) {
-                        *reinterpret_cast<uint32_t*>(smem + P.s_off + kmaj<kD>(tok, 16 * ks + 2 * qt)) =
-                            dec1(sw, 15 - ks, neg2);
-                        *reinterpret_cast<uint32_t*>(smem + P.s_off + kmaj<kD>(tok, 16 * ks + 8 + 2 * qt)) =
-                            dec1(sw, 7 - ks, neg2);
+                        hs[2 * ks] = dec1(sw, 15 - ks, neg2);
+                        hs[2 * ks + 1] = dec1(sw, 7 - ks, neg2);
                     }
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) *kchunk(P.s_off, i) = make_uint4(hs[4 * i], hs[4 * i + 1], hs[4 * i + 2], hs[4 * i + 3]);
                 }
                 const uint32_t* vidx = reinterpret_cast<const uint32_t*>(sp + st.off[4]);
                 uint32_t vw[VB], hv[16];
@@ -214,40 +221,26 @@ __global__ void __launch_bounds__(kTThreads, 1) prefill_tc_kernel(TcPrefillArgs 
                     const float mn = __half2float(reinterpret_cast<const __half*>(sp + st.off[6])[tok * ng + gi]);
                     const float mul = sc * (VB == 4 ? 16.0f : 4.0f);
                     GroupChunk<VB>::run(vw, pack_half2(mul, mul), pack_half2(mn, mn), hv);
-#pragma unroll
-                    for (int p = 0; p < 16; ++p) {
-                        int pa, pb;
-                        group_pair(VB, p, pa, pb);
-                        vrow[32 * qt + pa] = __ushort_as_half(static_cast<unsigned short>(hv[p] & 0xFFFFu));
-                        vrow[32 * qt + pb] = __ushort_as_half(static_cast<unsigned short>(hv[p] >> 16));
-                    }
                 } else {
                     mse_chunk<VB>(vw, vtab, hv);
-#pragma unroll
-                    for (int p = 0; p < 16; ++p) {
-                        int pa, pb;
-                        mse_pair(VB, p, pa, pb);
-                        vrow[32 * qt + pa] = __ushort_as_half(static_cast<unsigned short>(hv[p] & 0xFFFFu));
-                        vrow[32 * qt + pb] = __ushort_as_half(static_cast<unsigned short>(hv[p] >> 16));
-                    }
                 }
+                // values in pair order; the epilogue maps columns back to coordinates
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    reinterpret_cast<uint4*>(vrow)[i] = make_uint4(hv[4 * i], hv[4 * i + 1], hv[4 * i + 2], hv[4 * i + 3]);
                 if (qt == 0) {
                     kn[tok] = reinterpret_cast<const float*>(sp + st.off[2])[tok];
                     vn[tok] = VGROUP ? 1.0f : reinterpret_cast<const float*>(sp + st.off[5])[tok];
                 }
             } else {
                 // masked tokens meet P' = 0: keep every operand finite
+                const uint4 z = make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
-                for (int ks = 0; ks < 8; ++ks) {
-                    *reinterpret_cast<uint32_t*>(smem + P.k_off + kmaj<kD>(tok, 16 * ks + 2 * qt)) = 0u;
-                    *reinterpret_cast<uint32_t*>(smem + P.k_off + kmaj<kD>(tok, 16 * ks + 8 + 2 * qt)) = 0u;
-                    if constexpr (KPROD) {
-                        *reinterpret_cast<uint32_t*>(smem + P.s_off + kmaj<kD>(tok, 16 * ks + 2 * qt)) = 0u;
-                        *reinterpret_cast<uint32_t*>(smem + P.s_off + kmaj<kD>(tok, 16 * ks + 8 + 2 * qt)) = 0u;
-                    }
+                for (int i = 0; i < 4; ++i) {
+                    *kchunk(P.k_off, i) = z;
+                    if constexpr (KPROD) *kchunk(P.s_off, i) = z;
+                    reinterpret_cast<uint4*>(vrow)[i] = z;
                 }
-#pragma unroll
-                for (int q = 0; q < 16; ++q) reinterpret_cast<uint32_t*>(vrow + 32 * qt)[q] = 0u;
                 if (qt == 0) {
                     kn[tok] = 0.0f;
                     vn[tok] = 0.0f;
@@ -256,6 +249,7 @@ __global__ void __launch_bounds__(kTThreads, 1) prefill_tc_kernel(TcPrefillArgs 
         }
         __syncthreads();
         // values to V^T: 8x8 blocks (token block tb, dim block db), four per instruction
+        const __half* vs = reinterpret_cast<const __half*>(smem + P.vs_off);
         for (int it = warp; it < (kD / 8) * (kTTok / 8) / 4; it += kTThreads / 32) {
             const int mi = lane >> 3, rr = lane & 7;
             const int blk = 4 * it + mi;
@@ -398,8 +392,15 @@ __global__ void __launch_bounds__(kTThreads, 1) prefill_tc_kernel(TcPrefillArgs 
     for (int c = 0; c < kD / 2; c += 32) {
         float v[32];
         tc::tmem_ld32(tO + c, v);
+        // column 32 qt + 2p + odd holds coordinate 32 qt + (odd ? b : a) of value pair p
+        const int qbase = 64 * half + c;
 #pragma unroll
-        for (int e = 0; e < 32; ++e) orow[64 * half + c + e] = (o_started && !failed) ? v[e] * inv : 0.0f;  // TMEM unwritten otherwise
+        for (int e = 0; e < 32; ++e) {
+            int pa, pb;
+            if constexpr (VGROUP) group_pair(VB, e >> 1, pa, pb);
+            else mse_pair(VB, e >> 1, pa, pb);
+            orow[qbase + ((e & 1) ? pb : pa)] = (o_started && !failed) ? v[e] * inv : 0.0f;  // TMEM unwritten otherwise
+        }
     }
     __syncthreads();
     if (row_ok) {
