@@ -5,12 +5,13 @@
 // q_len positions, already appended, attends to its sequence's compressed
 // prefix and causally to itself (query l sees keys t <= N - q_len + l). One
 // CTA owns 128 query rows (8 groups of 16) of one KV head -- TMEM lane = row,
-// two threads per row (column halves of its scores and output) -- and walks
+// four threads per row (column quarters of its scores and output) -- and walks
 // the key/value tiles its rows can see; each tile is fetched once (1-D bulk
 // copies, double-buffered) and decoded once for all 128 rows. Per 64-token
 // tile:
 //   decode   the CTA decodes the tile once (one token and 32-coordinate
-//            quarter per thread) into shared-memory operands in the canonical
+//            quarter per thread; half the threads take the keys and signs,
+//            half the values) into shared-memory operands in the canonical
 //            no-swizzle K-major layout: key levels c_k[idx] and +-rnorm signs
 //            (64 tokens x 128, decoder pair p of quarter q at position
 //            32q + 2p, the query operands permuted to match), values in the
@@ -18,16 +19,21 @@
 //            (ldmatrix.trans + stmatrix) into V^T (128 columns x 64 tokens);
 //   scores   S = Q' K^T (+ Q'' sigma^T) as tcgen05.mma M 128, N 64, K 16 into 64
 //            TMEM columns;
-//   softmax  each thread reads its half row of S (tcgen05.ld), scales by the
-//            key norms, masks, exchanges the row maximum with the other half,
+//   softmax  each thread reads its quarter row of S (tcgen05.ld), scales by
+//            the key norms, masks, exchanges the row maximum with the row's
+//            other threads,
 //            keeps a running row maximum that only moves when the tile maximum
 //            exceeds it by 8 (log2 units: weights stay <= 2^8 and the output
-//            accumulator is rescaled rarely), writes its half row of
+//            accumulator is rescaled rarely), writes its quarter row of
 //            P' = p * value norm (fp16) as the K-major A operand;
-//   values   O += P' V as tcgen05.mma M 128, N 128, K 16 into 128 TMEM columns.
-// At the end the two threads of a row read its row of O, divide by the row
+//   values   O += P' V as tcgen05.mma M 128, N 128, K 16 into 128 TMEM columns,
+//            running while the next tile is decoded (its V^T and P' are
+//            written only after this MMA has completed).
+// At the end the four threads of a row read its row of O, divide by the row
 // sum and apply the inverse value rotation from a shared-memory copy of R_v.
 // Query fragments come from the decode path's query-prep kernel (workspace).
+#include <climits>
+
 #include "decode_mma_impl.cuh"
 #include "tc_ptx.cuh"
 
@@ -36,7 +42,8 @@ namespace mmadec {
 namespace {
 
 constexpr int kTRows = 128;       // query rows per CTA = MMA M = TMEM lanes
-constexpr int kTThreads = 256;    // two threads per row: column halves of its scores and output
+constexpr int kTSplit = 4;        // threads per row: column quarters of its scores and output
+constexpr int kTThreads = kTRows * kTSplit;
 constexpr int kTTok = 64;         // tokens per tile
 constexpr int kVStride = kD + 8;  // halves per row of the row-major value scratch
 constexpr float kRescaleGap = 8.0f;
@@ -47,10 +54,10 @@ struct TcPrefillArgs {
     const uint4* qfrag;           // [unit][2][8][32] uint4 (query-prep output)
     int qa_off, qj_off;           // Q' and Q'' (or Q' remainder) operands: 128 x 128 fp16
     int k_off, s_off;             // key levels and sign operands: 64 x 128 fp16
-    int vs_off;                   // value scratch [64][kVStride] fp16
-    int vt_off;                   // V^T operand: 128 x 64 fp16
+    int vs_off;                   // value scratch [64][kVStride] fp16 (also the row-maximum exchange)
+    int vt_off;                   // V^T operand: 144 x 64 fp16 (value rows, a ones row, zero rows)
     int p_off;                    // P' operand: 128 x 64 fp16
-    int norm_off;                 // key and value norms [2][64] floats
+    int norm_off;                 // key norms, value weights [2][64] floats; 1/weight [2][64] fp16
     int rv_off;                   // R_v [kD][kD] floats
     int bar_off;                  // mbarriers: 2 tiles, mma, R_v; then the TMEM slot and key limit
 };
@@ -71,15 +78,18 @@ __global__ void __launch_bounds__(kTThreads, 1) prefill_tc_kernel(TcPrefillArgs 
     const int h = blockIdx.y, b = blockIdx.z;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + P.bar_off);   // [0,1] tiles, [2] mma, [3] R_v
     uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + 4);
-    int* s_lim = reinterpret_cast<int*>(s_tmem + 1);
-    float* s_x = reinterpret_cast<float*>(smem + P.norm_off + 2 * kTTok * 4);   // [2][128] half-row exchange
-    float* kn = reinterpret_cast<float*>(smem + P.norm_off);
-    float* vn = kn + kTTok;
+    int* s_lim = reinterpret_cast<int*>(s_tmem + 1);                    // largest and smallest row limit
+    float* kn = reinterpret_cast<float*>(smem + P.norm_off);           // key norms of the tile
+    float* vw = kn + kTTok;                                             // value weights: norm, or 1 for 0
+    __half* rhi = reinterpret_cast<__half*>(vw + kTTok);                // 1 / weight as fp16 hi + lo
+    __half* rlo = rhi + kTTok;
+    float* s_x = reinterpret_cast<float*>(smem + P.vs_off);            // [kTSplit][128] row exchange (over
+                                                                        // the value scratch, idle then)
     float* Rv = reinterpret_cast<float*>(smem + P.rv_off);
     const uint32_t sbase = tc::smem_addr(smem);
 
-    // this thread's row and column half
-    const int row = tid & (kTRows - 1), half = tid >> 7;
+    // this thread's row (its warp's TMEM lane quarter) and column quarter
+    const int row = 32 * (warp & 3) + lane, cq = warp >> 2;
     const int w8 = row >> 4;                        // row group slot of the CTA
     const int rg = blockIdx.x + w8 * gridDim.x;
     const int r = rg * kRows + (row & 15);
@@ -90,11 +100,12 @@ __global__ void __launch_bounds__(kTThreads, 1) prefill_tc_kernel(TcPrefillArgs 
     const int lim = row_ok ? N - a.Lq + (r % a.Lq) : -1;
 
     if (warp == 0) {
-        tc::tmem_alloc(s_tmem, 256);   // S: columns 0..63, O: columns 128..255
+        tc::tmem_alloc(s_tmem, 512);   // S: columns 0..63; O: 128..255; row sums: 256 + 257 (258..271 zero)
         tc::tmem_relinquish();
     }
     if (tid == 0) {
-        *s_lim = -1;
+        s_lim[0] = -1;
+        s_lim[1] = INT_MAX;
         for (int s = 0; s < 4; ++s) tc::mbar_init(&bars[s], 1);
         tc::mbar_fence_init();
         if constexpr (!VGROUP) {
@@ -116,16 +127,26 @@ __global__ void __launch_bounds__(kTThreads, 1) prefill_tc_kernel(TcPrefillArgs 
             *reinterpret_cast<uint32_t*>(smem + (which ? P.qj_off : P.qa_off) + kmaj<kD>(row, k)) = v;
         }
     }
+    // rows kD and kD+1 of the value operand hold 1 / weight (fp16 hi, lo) per
+    // token, so that their output columns accumulate the row sum of P' / weight;
+    // rows kD+2..kD+15 stay zero
+    for (int e = tid; e < 16 * (kTTok / 8); e += kTThreads) {
+        const int n = kD + (e >> 3), kc = e & 7;
+        *reinterpret_cast<uint4*>(smem + P.vt_off + kmaj<kTTok>(n, 8 * kc)) = make_uint4(0u, 0u, 0u, 0u);
+    }
     tc::fence_proxy_async_smem();
     tc::tc_fence_before();
     __syncthreads();
     tc::tc_fence_after();
-    atomicMax(s_lim, lim);
+    atomicMax(&s_lim[0], lim);
+    if (row_ok) atomicMin(&s_lim[1], lim);
     const uint32_t tmem = *s_tmem;
     const uint32_t t_row = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
-    const uint32_t tS = t_row + 32 * half, tO = t_row + 128 + 64 * half;   // this thread's columns
+    constexpr int HC = kTTok / kTSplit, OC = kD / kTSplit;   // score and output columns per thread
+    const uint32_t tS = t_row + HC * cq, tO = t_row + 128 + OC * cq, tL = t_row + 128 + kD;   // tL: row sums
     __syncthreads();
-    const int kend = bad ? 0 : min(*s_lim + 1, N);
+    const int kend = bad ? 0 : min(s_lim[0] + 1, N);
+    const int minlim = s_lim[1];   // tiles ending at or below it are visible to every valid row
     const int ntiles = kend > 0 ? (kend + TT - 1) / TT : 0;
 
     const auto ktab = mse_table<KB>(a.kc.c);
@@ -153,8 +174,8 @@ __global__ void __launch_bounds__(kTThreads, 1) prefill_tc_kernel(TcPrefillArgs 
     if (tid == 0 && ntiles > 0) issue(0);
 
     constexpr uint32_t idS = tc::idesc_f16_f32(kTRows, kTTok);
-    constexpr uint32_t idO = tc::idesc_f16_f32(kTRows, kD);
-    float m = -INFINITY, l = 0.0f;
+    constexpr uint32_t idO = tc::idesc_f16_f32(kTRows, kD + 16);
+    float m = -INFINITY;
     unsigned mphase = 0;
     bool failed = false, o_started = false, mma_pending = false;
     int waited = 0;
@@ -185,13 +206,15 @@ __global__ void __launch_bounds__(kTThreads, 1) prefill_tc_kernel(TcPrefillArgs 
         // goes to operand position 32 qt + 2p, so each operand row is written
         // as four 16-byte chunks (a store phase covers 8 tokens: no conflicts)
         {
-            static_assert(kTTok * 4 == kTThreads, "one unit per thread");
-            const int tok = 32 * (warp & 1) + lane, qt = warp >> 1;
+            static_assert(kTTok * 4 * 2 == kTThreads, "one key unit and one value unit per thread pair");
+            const bool vside = tid >= kTThreads / 2;   // first half: keys and signs; second: values
+            const int wd = warp & 7;
+            const int tok = 32 * (wd & 1) + lane, qt = wd >> 1;
             __half* vrow = reinterpret_cast<__half*>(smem + P.vs_off) + tok * kVStride + 32 * qt;
             auto kchunk = [&](int off, int i) {
                 return reinterpret_cast<uint4*>(smem + off + kmaj<kD>(tok, 32 * qt + 8 * i));
             };
-            if (tok < valid) {
+            if (tok < valid && !vside) {
                 const uint32_t* kidx = reinterpret_cast<const uint32_t*>(sp + st.off[0]);
                 uint32_t kw[KB], hk[16];
                 load_words<KB>(kidx + tok * (4 * KB) + qt * KB, kw);
@@ -211,43 +234,79 @@ __global__ void __launch_bounds__(kTThreads, 1) prefill_tc_kernel(TcPrefillArgs 
 #pragma unroll
                     for (int i = 0; i < 4; ++i) *kchunk(P.s_off, i) = make_uint4(hs[4 * i], hs[4 * i + 1], hs[4 * i + 2], hs[4 * i + 3]);
                 }
+                if (qt == 0) kn[tok] = reinterpret_cast<const float*>(sp + st.off[2])[tok];
+            } else if (tok < valid) {
                 const uint32_t* vidx = reinterpret_cast<const uint32_t*>(sp + st.off[4]);
-                uint32_t vw[VB], hv[16];
-                load_words<VB>(vidx + tok * (4 * VB) + qt * VB, vw);
+                uint32_t vwd[VB], hv[16];
+                load_words<VB>(vidx + tok * (4 * VB) + qt * VB, vwd);
                 if constexpr (VGROUP) {
                     const int ng = kD / a.vc.group;
                     const int gi = (32 * qt) / a.vc.group;
                     const float sc = __half2float(reinterpret_cast<const __half*>(sp + st.off[5])[tok * ng + gi]);
                     const float mn = __half2float(reinterpret_cast<const __half*>(sp + st.off[6])[tok * ng + gi]);
                     const float mul = sc * (VB == 4 ? 16.0f : 4.0f);
-                    GroupChunk<VB>::run(vw, pack_half2(mul, mul), pack_half2(mn, mn), hv);
+                    GroupChunk<VB>::run(vwd, pack_half2(mul, mul), pack_half2(mn, mn), hv);
                 } else {
-                    mse_chunk<VB>(vw, vtab, hv);
+                    mse_chunk<VB>(vwd, vtab, hv);
+                }
+                // P' carries the weight (the value norm; 1 for a zero vector, whose
+                // operand row is zero), and rows kD, kD+1 of V^T carry 1 / weight
+                float wt = 1.0f;
+                if constexpr (!VGROUP) {
+                    const float nv = reinterpret_cast<const float*>(sp + st.off[5])[tok];
+                    if (nv > 0.0f) {
+                        wt = nv;
+                    } else {
+#pragma unroll
+                        for (int p = 0; p < 16; ++p) hv[p] = 0u;
+                    }
+                }
+                if (qt == 0) {
+                    const float rw = 1.0f / wt;
+                    const __half h1 = __float2half_rn(rw);
+                    vw[tok] = wt;
+                    rhi[tok] = h1;
+                    rlo[tok] = __float2half_rn(rw - __half2float(h1));
                 }
                 // values in pair order; the epilogue maps columns back to coordinates
 #pragma unroll
                 for (int i = 0; i < 4; ++i)
                     reinterpret_cast<uint4*>(vrow)[i] = make_uint4(hv[4 * i], hv[4 * i + 1], hv[4 * i + 2], hv[4 * i + 3]);
-                if (qt == 0) {
-                    kn[tok] = reinterpret_cast<const float*>(sp + st.off[2])[tok];
-                    vn[tok] = VGROUP ? 1.0f : reinterpret_cast<const float*>(sp + st.off[5])[tok];
-                }
             } else {
                 // masked tokens meet P' = 0: keep every operand finite
                 const uint4 z = make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
-                    *kchunk(P.k_off, i) = z;
-                    if constexpr (KPROD) *kchunk(P.s_off, i) = z;
-                    reinterpret_cast<uint4*>(vrow)[i] = z;
+                    if (vside) {
+                        reinterpret_cast<uint4*>(vrow)[i] = z;
+                    } else {
+                        *kchunk(P.k_off, i) = z;
+                        if constexpr (KPROD) *kchunk(P.s_off, i) = z;
+                    }
                 }
                 if (qt == 0) {
-                    kn[tok] = 0.0f;
-                    vn[tok] = 0.0f;
+                    if (vside) {
+                        vw[tok] = 0.0f;
+                        rhi[tok] = rlo[tok] = __float2half_rn(0.0f);
+                    } else {
+                        kn[tok] = 0.0f;
+                    }
                 }
             }
         }
         __syncthreads();
+        // the previous tile's output MMA reads V^T and P': wait for it only now,
+        // so that it ran under this tile's decode
+        if (mma_pending) {
+            const bool done = tc::mbar_wait(&bars[2], mphase);
+            if (__syncthreads_or(!done)) {
+                failed = true;
+                break;
+            }
+            mma_pending = false;
+            mphase ^= 1;
+            tc::tc_fence_after();
+        }
         // values to V^T: 8x8 blocks (token block tb, dim block db), four per instruction
         const __half* vs = reinterpret_cast<const __half*>(smem + P.vs_off);
         for (int it = warp; it < (kD / 8) * (kTTok / 8) / 4; it += kTThreads / 32) {
@@ -256,7 +315,12 @@ __global__ void __launch_bounds__(kTThreads, 1) prefill_tc_kernel(TcPrefillArgs 
             const int db = blk >> 3, tb = blk & 7;
             uint32_t x0, x1, x2, x3;
             tc::ldmatrix_x4_trans(x0, x1, x2, x3, vs + (8 * tb + rr) * kVStride + 8 * db);
-            tc::stmatrix_x4(smem + P.vt_off + ((8 * db) >> 3) * (kTTok / 8) * 128 + tb * 128 + rr * 16, x0, x1, x2, x3);
+            tc::stmatrix_x4(smem + P.vt_off + kmaj<kTTok>(8 * db + rr, 8 * tb), x0, x1, x2, x3);
+        }
+        if (tid < 2 * (kTTok / 8)) {   // rows kD (hi) and kD+1 (lo), 8 tokens per chunk
+            const int n = tid >> 3, kc = tid & 7;
+            const uint4 v = reinterpret_cast<const uint4*>(n ? rlo : rhi)[kc];
+            *reinterpret_cast<uint4*>(smem + P.vt_off + kmaj<kTTok>(kD + n, 8 * kc)) = v;
         }
         tc::fence_proxy_async_smem();
         tc::tc_fence_before();
@@ -287,88 +351,117 @@ __global__ void __launch_bounds__(kTThreads, 1) prefill_tc_kernel(TcPrefillArgs 
         mphase ^= 1;
         tc::tc_fence_after();
 
-        // ---------------- softmax of this thread's half row (log2 units); the
-        // row maximum is exchanged with the other half through shared memory
-        constexpr int HC = kTTok / 2;
+        // ---------------- softmax of this thread's quarter row (log2 units); the
+        // row maximum is exchanged with the row's other threads through shared memory
         float sv[HC];
+        tc::tmem_ld16(tS, sv);
         {
-            float v[32];
-            tc::tmem_ld32(tS, v);
+            const float4* k4 = reinterpret_cast<const float4*>(kn + HC * cq);
 #pragma unroll
-            for (int c = 0; c < HC; ++c) sv[c] = v[c];
-        }
-        float mx = -INFINITY;
-#pragma unroll
-        for (int c = 0; c < HC; ++c) {
-            const int tc_ = HC * half + c;
-            const bool in = tc_ < valid && t0 + tc_ <= lim;
-            sv[c] = in ? sv[c] * kn[tc_] : -INFINITY;
-            mx = fmaxf(mx, sv[c]);
-        }
-        s_x[half * kTRows + row] = mx;
-        __syncthreads();
-        mx = fmaxf(mx, s_x[(half ^ 1) * kTRows + row]);
-        // move the running maximum only when this tile exceeds it by the gap
-        // (both halves take the same decision from the same values)
-        const bool move = mx > m + kRescaleGap || (m == -INFINITY && mx != -INFINITY);
-        const float alpha = move ? (m == -INFINITY ? 0.0f : ex2(m - mx)) : 1.0f;
-        if (move) {
-            l *= alpha;
-            m = mx;
-        }
-        if (__any_sync(0xffffffffu, move) && o_started) {
-#pragma unroll 1
-            for (int c = 0; c < kD / 2; c += 32) {
-                float v[32];
-                tc::tmem_ld32(tO + c, v);
-#pragma unroll
-                for (int e = 0; e < 32; ++e) v[e] *= alpha;
-                tc::tmem_st32(tO + c, v);
+            for (int q = 0; q < HC / 4; ++q) {
+                const float4 n4 = k4[q];
+                sv[4 * q] *= n4.x;
+                sv[4 * q + 1] *= n4.y;
+                sv[4 * q + 2] *= n4.z;
+                sv[4 * q + 3] *= n4.w;
             }
         }
-        // P' = fp16(p * value norm) into the A operand; the row sum adds the
-        // rounded weights divided back (a zero-norm value contributes p)
+        // a tile whose 64 operand columns are all valid tokens below every
+        // row's causal limit needs no mask (blocks shorter than 64 tokens
+        // leave zero columns, which the mask must keep out of the row sums)
+        const bool open = valid == kTTok && t0 + kTTok - 1 <= minlim;
+        if (!open) {
+#pragma unroll
+            for (int c = 0; c < HC; ++c) {
+                const int tc_ = HC * cq + c;
+                if (!(tc_ < valid && t0 + tc_ <= lim)) sv[c] = -INFINITY;
+            }
+        }
+        float mx = sv[0];
+#pragma unroll
+        for (int c = 1; c < HC; ++c) mx = fmaxf(mx, sv[c]);
+        s_x[cq * kTRows + row] = mx;
+        __syncthreads();
+#pragma unroll
+        for (int o = 1; o < kTSplit; ++o) mx = fmaxf(mx, s_x[((cq + o) & (kTSplit - 1)) * kTRows + row]);
+        // move the running maximum only when this tile exceeds it by the gap
+        // (the row's threads take the same decision from the same values)
+        const bool move = mx > m + kRescaleGap || (m == -INFINITY && mx != -INFINITY);
+        const float alpha = move ? (m == -INFINITY ? 0.0f : ex2(m - mx)) : 1.0f;
+        if (move) m = mx;
+        if (__any_sync(0xffffffffu, move) && o_started) {
+            float v[32];
+            tc::tmem_ld32(tO, v);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) v[e] *= alpha;
+            tc::tmem_st32(tO, v);
+            if (cq == 0) {   // the row-sum column
+                float w[16];
+                tc::tmem_ld16(tL, w);
+#pragma unroll
+                for (int e = 0; e < 16; ++e) w[e] *= alpha;
+                tc::tmem_st16(tL, w);
+            }
+        }
+        // P' = fp16(p * weight) into the A operand; the rows kD, kD+1 of V^T
+        // divide each rounded P' back by its weight for the row sum, so the
+        // rounding of P' cancels in O / l
+        float wv[HC];
+        {
+            const float4* w4 = reinterpret_cast<const float4*>(vw + HC * cq);
+#pragma unroll
+            for (int q = 0; q < HC / 4; ++q) {
+                const float4 n4 = w4[q];
+                wv[4 * q] = n4.x;
+                wv[4 * q + 1] = n4.y;
+                wv[4 * q + 2] = n4.z;
+                wv[4 * q + 3] = n4.w;
+            }
+        }
 #pragma unroll
         for (int c8 = 0; c8 < HC / 8; ++c8) {
             uint32_t w[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 const int c = 8 * c8 + 2 * e;
-                const int tc_ = HC * half + c;
-                const float p0 = m == -INFINITY ? 0.0f : ex2(sv[c] - m);
-                const float p1 = m == -INFINITY ? 0.0f : ex2(sv[c + 1] - m);
-                const float v0 = vn[tc_], v1 = vn[tc_ + 1];
-                const bool z0 = !(v0 > 0.0f), z1 = !(v1 > 0.0f);
-                w[e] = pack_half2(z0 ? 0.0f : p0 * v0, z1 ? 0.0f : p1 * v1);
-                const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[e]));
-                l += (z0 ? p0 : f.x * __fdividef(1.0f, v0)) + (z1 ? p1 : f.y * __fdividef(1.0f, v1));
+                float p0, p1;
+                if (open) {   // finite scores, so a finite maximum
+                    p0 = ex2(sv[c] - m);
+                    p1 = ex2(sv[c + 1] - m);
+                } else {
+                    p0 = m == -INFINITY ? 0.0f : ex2(sv[c] - m);
+                    p1 = m == -INFINITY ? 0.0f : ex2(sv[c + 1] - m);
+                }
+                w[e] = pack_half2(p0 * wv[c], p1 * wv[c + 1]);
             }
-            *reinterpret_cast<uint4*>(smem + P.p_off + kmaj<kTTok>(row, HC * half + 8 * c8)) =
+            *reinterpret_cast<uint4*>(smem + P.p_off + kmaj<kTTok>(row, HC * cq + 8 * c8)) =
                 make_uint4(w[0], w[1], w[2], w[3]);
         }
         tc::fence_proxy_async_smem();
         tc::tc_fence_before();
         __syncthreads();
 
-        // ---------------- O += P' V on the tensor cores
+        // ---------------- [O | row sum] += P' [V | 1/weight] on the tensor cores
         if (tid == 0) {
             tc::tc_fence_after();
 #pragma unroll
             for (int s = 0; s < kTTok / 16; ++s)
-                tc::mma_f16(tO, tc::smem_desc(sbase + P.p_off + 256 * s, 128, 1024),
+                tc::mma_f16(tmem + 128, tc::smem_desc(sbase + P.p_off + 256 * s, 128, 1024),
                             tc::smem_desc(sbase + P.vt_off + 256 * s, 128, 1024), idO, (o_started || s > 0) ? 1u : 0u);
             tc::mma_commit(&bars[2]);
         }
         o_started = true;
-        mma_pending = true;
-        ok = tc::mbar_wait(&bars[2], mphase);   // the tile's operands are free again
-        if (__syncthreads_or(!ok)) {
+        mma_pending = true;   // waited for before the next tile writes V^T and P'
+    }
+    if (!failed && mma_pending) {
+        const bool done = tc::mbar_wait(&bars[2], mphase);
+        if (__syncthreads_or(!done)) {
             failed = true;
-            break;
+        } else {
+            mma_pending = false;
+            mphase ^= 1;
+            tc::tc_fence_after();
         }
-        mma_pending = false;
-        mphase ^= 1;
-        tc::tc_fence_after();
     }
     if (failed) {
         if (tid == 0) atomicOr(a.err, TQ_DEVERR_TIMEOUT);
@@ -382,18 +475,21 @@ __global__ void __launch_bounds__(kTThreads, 1) prefill_tc_kernel(TcPrefillArgs 
 
     // ---------------- output rows: O / l staged in shared memory (over the
     // query operands, padded rows), then rotated back by R_v, each thread
-    // writing its half of the row's dimensions
-    s_x[half * kTRows + row] = l;
-    __syncthreads();
-    l += s_x[(half ^ 1) * kTRows + row];
+    // writing its quarter of the row's dimensions
+    float l = 0.0f;
+    if (o_started && !failed) {
+        float w[16];
+        tc::tmem_ld16(tL, w);
+        l = w[0] + w[1];
+    }
     float* orow = reinterpret_cast<float*>(smem + P.qa_off) + row * (kD + 1);
     const float inv = (o_started && !failed && l > 0.0f) ? 1.0f / l : 0.0f;
 #pragma unroll 1
-    for (int c = 0; c < kD / 2; c += 32) {
+    for (int c = 0; c < OC; c += 32) {
         float v[32];
         tc::tmem_ld32(tO + c, v);
         // column 32 qt + 2p + odd holds coordinate 32 qt + (odd ? b : a) of value pair p
-        const int qbase = 64 * half + c;
+        const int qbase = OC * cq + c;
 #pragma unroll
         for (int e = 0; e < 32; ++e) {
             int pa, pb;
@@ -407,7 +503,7 @@ __global__ void __launch_bounds__(kTThreads, 1) prefill_tc_kernel(TcPrefillArgs 
         const int gq = r / a.Lq, lq = r % a.Lq;
         float* dst = a.out + ((static_cast<int64_t>(b) * a.Hq + h * a.G + gq) * a.Lq + lq) * kD;
 #pragma unroll 1
-        for (int d0 = 64 * half; d0 < 64 * half + 64; d0 += 32) {
+        for (int d0 = OC * cq; d0 < OC * cq + OC; d0 += 32) {
             float acc[32];
             if constexpr (VGROUP) {
 #pragma unroll
@@ -439,7 +535,7 @@ __global__ void __launch_bounds__(kTThreads, 1) prefill_tc_kernel(TcPrefillArgs 
     __syncthreads();
     if (warp == 0) {
         tc::tc_fence_after();
-        tc::tmem_dealloc(tmem, 256);
+        tc::tmem_dealloc(tmem, 512);
     }
     if (tid == 0)
         for (int s = 0; s < 4; ++s) tc::mbar_inval(&bars[s]);
@@ -504,11 +600,11 @@ cudaError_t launch_prefill(const DecodeArgs& a, const uint4* qfrag, cudaStream_t
     P.qj_off = off; off += kTRows * kD * 2;
     P.k_off = off; off += kTTok * kD * 2;
     P.s_off = off; off += p.kprod ? kTTok * kD * 2 : 0;   // sign operands (prod keys only)
-    P.vt_off = off; off += kD * kTTok * 2;
+    P.vt_off = off; off += (kD + 16) * kTTok * 2;   // V^T plus a ones row and 15 zero rows
     P.p_off = off; off += kTRows * kTTok * 2;
     P.vs_off = off; off += kTTok * kVStride * 2;
-    P.norm_off = off; off += 2 * kTTok * 4 + 2 * kTRows * 4;   // norms, then the half-row exchange
-    P.rv_off = off; off += kD * kD * 4;
+    P.norm_off = off; off += 2 * kTTok * 4 + 2 * kTTok * 2;   // key norms, value weights, 1/weight hi, lo
+    P.rv_off = off; off += p.vgroup ? 0 : kD * kD * 4;        // group values are not rotated
     P.bar_off = off; off += 64;
     const size_t smem = static_cast<size_t>(off);
     if (smem > 232448) return cudaErrorInvalidValue;   // the largest dynamic shared memory a CTA can opt into
