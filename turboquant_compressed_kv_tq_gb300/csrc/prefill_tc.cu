@@ -43,23 +43,30 @@ namespace {
 
 constexpr int kTRows = 128;       // query rows per CTA = MMA M = TMEM lanes
 constexpr int kTSplit = 4;        // threads per row: column quarters of its scores and output
-constexpr int kTThreads = kTRows * kTSplit;
+constexpr int kTCompute = kTRows * kTSplit;   // the decode and softmax warps
+constexpr int kTThreads = kTCompute + 32;     // plus one warp that issues copies and MMAs
+constexpr int kCtlWarp = kTCompute / 32;
+constexpr int kBarCompute = 1;    // named barrier of the compute warps
 constexpr int kTTok = 64;         // tokens per tile
 constexpr int kVStride = kD + 8;  // halves per row of the row-major value scratch
 constexpr float kRescaleGap = 8.0f;
+constexpr int kStashBytes = 2 * kTTok * 4 + 2 * kTTok * 2;   // per-tile norms and weights
+// TMEM columns: output [O | row sums] (144), scores (64), P' (32 of fp16 pairs),
+// the query operands Q' and Q'' (64 each, fp16 pairs)
+constexpr uint32_t kColO = 0, kColS = 256, kColP = 320, kColQa = 384, kColQj = 448;
 
 struct TcPrefillArgs {
     DecodeArgs a;
     StageLayout st;               // record streams of one tile
     const uint4* qfrag;           // [unit][2][8][32] uint4 (query-prep output)
-    int qa_off, qj_off;           // Q' and Q'' (or Q' remainder) operands: 128 x 128 fp16
     int k_off, s_off;             // key levels and sign operands: 64 x 128 fp16
-    int vs_off;                   // value scratch [64][kVStride] fp16 (also the row-maximum exchange)
-    int vt_off;                   // V^T operand: 144 x 64 fp16 (value rows, a ones row, zero rows)
-    int p_off;                    // P' operand: 128 x 64 fp16
-    int norm_off;                 // key norms, value weights [2][64] floats; 1/weight [2][64] fp16
-    int rv_off;                   // R_v [kD][kD] floats
-    int bar_off;                  // mbarriers: 2 tiles, mma, R_v; then the TMEM slot and key limit
+    int vt_off;                   // V^T operand: 144 x 64 fp16 (value rows, 1/weight hi and lo, zero rows)
+    int vs_off;                   // value scratch [64][kVStride] fp16
+    int norm_off;                 // two stashes: key norms, value weights [2][64] floats; 1/weight [2][64] fp16
+    int sx_off;                   // row-maximum exchange [2][kTSplit][128] floats
+    int orow_off;                 // output staging [128][kD + 1] floats
+    int rv_off;                   // R_v [kD][kD] floats (MSE values only)
+    int bar_off;                  // mbarriers (7); then the TMEM slot and the row limits
 };
 
 // Byte offset of (row, k) in a K-major operand whose K extent is KX.
@@ -74,57 +81,47 @@ __global__ void __launch_bounds__(kTThreads, 1) prefill_tc_kernel(TcPrefillArgs 
     const DecodeArgs& a = P.a;
     const StageLayout& st = P.st;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const bool ctl = warp == kCtlWarp;
     const int Hkv = a.pool.Hkv, RG = a.plan.row_groups, BT = a.pool.BT, TT = st.tt;
     const int h = blockIdx.y, b = blockIdx.z;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + P.bar_off);   // [0,1] tiles, [2] mma, [3] R_v
-    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + 4);
+    // mbarriers: [0,1] tile records, [2] scores done, [3] R_v, [4] P' written by
+    // the 16 compute warps, [5] output MMA done, [6] operands written by the 16 compute warps
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + P.bar_off);
+    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + 7);
     int* s_lim = reinterpret_cast<int*>(s_tmem + 1);                    // largest and smallest row limit
-    float* kn = reinterpret_cast<float*>(smem + P.norm_off);           // key norms of the tile
-    float* vw = kn + kTTok;                                             // value weights: norm, or 1 for 0
-    __half* rhi = reinterpret_cast<__half*>(vw + kTTok);                // 1 / weight as fp16 hi + lo
-    __half* rlo = rhi + kTTok;
-    float* s_x = reinterpret_cast<float*>(smem + P.vs_off);            // [kTSplit][128] row exchange (over
-                                                                        // the value scratch, idle then)
     float* Rv = reinterpret_cast<float*>(smem + P.rv_off);
     const uint32_t sbase = tc::smem_addr(smem);
+    // per-tile values, double-buffered by tile parity (a warp may run one
+    // phase ahead of another): key norms, value weights, 1/weight as fp16 hi, lo
+    auto stash_kn = [&](int par) { return reinterpret_cast<float*>(smem + P.norm_off + par * kStashBytes); };
+    auto s_x = [&](int par) { return reinterpret_cast<float*>(smem + P.sx_off) + par * kTSplit * kTRows; };
 
-    // this thread's row (its warp's TMEM lane quarter) and column quarter
-    const int row = 32 * (warp & 3) + lane, cq = warp >> 2;
+    // a compute thread's row (its warp's TMEM lane quarter) and column quarter
+    const int row = 32 * (warp & 3) + lane, cq = (warp >> 2) & 3;
     const int w8 = row >> 4;                        // row group slot of the CTA
     const int rg = blockIdx.x + w8 * gridDim.x;
     const int r = rg * kRows + (row & 15);
-    const bool row_ok = rg < RG && r < a.plan.rows;
+    const bool row_ok = !ctl && rg < RG && r < a.plan.rows;
     const int N = a.seq_lens[b];
     const bool bad = N < a.Lq || N > a.max_blocks * BT;
     if (bad && tid == 0 && blockIdx.x == 0 && h == 0) atomicOr(a.err, TQ_DEVERR_SEQLEN);
     const int lim = row_ok ? N - a.Lq + (r % a.Lq) : -1;
 
     if (warp == 0) {
-        tc::tmem_alloc(s_tmem, 512);   // S: columns 0..63; O: 128..255; row sums: 256 + 257 (258..271 zero)
+        tc::tmem_alloc(s_tmem, 512);
         tc::tmem_relinquish();
     }
     if (tid == 0) {
         s_lim[0] = -1;
         s_lim[1] = INT_MAX;
         for (int s = 0; s < 4; ++s) tc::mbar_init(&bars[s], 1);
+        tc::mbar_init(&bars[4], kTCompute / 32);
+        tc::mbar_init(&bars[5], 1);
+        tc::mbar_init(&bars[6], kTCompute / 32);
         tc::mbar_fence_init();
         if constexpr (!VGROUP) {
             tc::mbar_expect_tx(&bars[3], kD * kD * 4);
             tc::bulk_g2s(Rv, a.vc.R, kD * kD * 4, &bars[3]);
-        }
-    }
-    // Q operands from the query fragments (8 units of 16 rows)
-    {
-        const uint32_t* qf = reinterpret_cast<const uint32_t*>(P.qfrag);
-        for (int e = tid; e < 8 * 2048; e += kTThreads) {
-            const int slot = e >> 11, x = e & 2047;
-            const int which = x >> 10, ks = (x >> 7) & 7, ln = (x >> 2) & 31, reg = x & 3;
-            const int rgs = blockIdx.x + slot * gridDim.x;
-            const uint32_t v = rgs < RG ? qf[static_cast<int64_t>((b * Hkv + h) * RG + rgs) * 2048 + x] : 0u;
-            // fragment (ks, lane, reg) holds pair 2ks + reg/2 of coordinate quarter lane % 4
-            const int row = slot * kRows + (ln >> 2) + 8 * (reg & 1);
-            const int k = 32 * (ln & 3) + 4 * ks + 2 * (reg >> 1);
-            *reinterpret_cast<uint32_t*>(smem + (which ? P.qj_off : P.qa_off) + kmaj<kD>(row, k)) = v;
         }
     }
     // rows kD and kD+1 of the value operand hold 1 / weight (fp16 hi, lo) per
@@ -138,358 +135,369 @@ __global__ void __launch_bounds__(kTThreads, 1) prefill_tc_kernel(TcPrefillArgs 
     tc::tc_fence_before();
     __syncthreads();
     tc::tc_fence_after();
-    atomicMax(&s_lim[0], lim);
-    if (row_ok) atomicMin(&s_lim[1], lim);
+    if (!ctl) {
+        atomicMax(&s_lim[0], lim);
+        if (row_ok) atomicMin(&s_lim[1], lim);
+    }
     const uint32_t tmem = *s_tmem;
     const uint32_t t_row = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
     constexpr int HC = kTTok / kTSplit, OC = kD / kTSplit;   // score and output columns per thread
-    const uint32_t tS = t_row + HC * cq, tO = t_row + 128 + OC * cq, tL = t_row + 128 + kD;   // tL: row sums
+    const uint32_t tS = t_row + kColS + HC * cq, tO = t_row + kColO + OC * cq, tL = t_row + kColO + kD;
+    // the query operands of this thread's row into TMEM: coordinate quarter cq
+    // (pairs p of the query fragments, column 16 cq + p) of Q' and of Q''
+    if (!ctl) {
+        const int rgs = blockIdx.x + w8 * gridDim.x;
+        const uint32_t* qf = reinterpret_cast<const uint32_t*>(P.qfrag) +
+                             static_cast<int64_t>((b * Hkv + h) * RG + rgs) * 2048;
+        const int ln = 4 * (row & 7) + cq, rbit = (row >> 3) & 1;
+        uint32_t qa[16], qj[16];
+#pragma unroll
+        for (int p = 0; p < 16; ++p) {
+            const int x = (p >> 1) * 128 + ln * 4 + rbit + 2 * (p & 1);   // fragment (ks, lane, reg)
+            qa[p] = rgs < RG ? qf[x] : 0u;
+            qj[p] = rgs < RG ? qf[1024 + x] : 0u;
+        }
+        tc::tmem_st16u(t_row + kColQa + 16 * cq, qa);
+        tc::tmem_st16u(t_row + kColQj + 16 * cq, qj);
+    }
+    tc::tc_fence_before();
     __syncthreads();
+    tc::tc_fence_after();
     const int kend = bad ? 0 : min(s_lim[0] + 1, N);
     const int minlim = s_lim[1];   // tiles ending at or below it are visible to every valid row
     const int ntiles = kend > 0 ? (kend + TT - 1) / TT : 0;
 
-    const auto ktab = mse_table<KB>(a.kc.c);
-    typename MseTable<VGROUP ? 2 : VB>::type vtab{};
-    if constexpr (!VGROUP) vtab = mse_table<VB>(a.vc.c);
-
-    auto issue = [&](int i) {   // thread 0
-        const int t0 = i * TT;
-        const int lb = t0 / BT;
-        const int slot0 = t0 - lb * BT;
-        int64_t pb = a.table ? static_cast<int64_t>(a.table[static_cast<int64_t>(b) * a.max_blocks + lb])
-                             : static_cast<int64_t>(b) * a.max_blocks + lb;
-        if (pb < 0 || pb >= a.pool.num_blocks) pb = 0;
-        const char* base = a.pool.base + (pb * Hkv + h) * a.pool.sub_bytes;
-        unsigned char* dst = smem + static_cast<size_t>(i & 1) * st.bytes;
-        unsigned total = 0;
-        for (int k = 0; k < 7; ++k)
-            if (st.off[k] >= 0) total += TT * st.field[k];
-        tc::mbar_expect_tx(&bars[i & 1], total);
-        for (int k = 0; k < 7; ++k)
-            if (st.off[k] >= 0)
-                tc::bulk_g2s(dst + st.off[k], base + a.pool.off[k] + static_cast<int64_t>(slot0) * st.field[k],
-                             TT * st.field[k], &bars[i & 1]);
-    };
-    if (tid == 0 && ntiles > 0) issue(0);
-
-    constexpr uint32_t idS = tc::idesc_f16_f32(kTRows, kTTok);
-    constexpr uint32_t idO = tc::idesc_f16_f32(kTRows, kD + 16);
-    float m = -INFINITY;
-    unsigned mphase = 0;
-    bool failed = false, o_started = false, mma_pending = false;
-    int waited = 0;
-
-    for (int i = 0; i < ntiles && !failed; ++i) {
-        if (tid == 0 && i + 1 < ntiles) issue(i + 1);   // its stage was consumed in iteration i - 1
-        bool ok = tc::mbar_wait(&bars[i & 1], (i >> 1) & 1);
-        if (__syncthreads_or(!ok)) {
-            failed = true;
-            break;
-        }
-        waited = i + 1;
-        const unsigned char* sp = smem + static_cast<size_t>(i & 1) * st.bytes;
-        const int t0 = i * TT;
-        int valid = min(TT, kend - t0);
-        {
-            const int lb = t0 / BT;
-            const int64_t pb = a.table ? static_cast<int64_t>(a.table[static_cast<int64_t>(b) * a.max_blocks + lb])
-                                       : static_cast<int64_t>(b) * a.max_blocks + lb;
-            if (pb < 0 || pb >= a.pool.num_blocks) {
-                if (tid == 0) atomicOr(a.err, TQ_DEVERR_BLOCK);
-                valid = 0;
-            }
-        }
-
-        // ---------------- decode the tile: one (token, 32-coordinate quarter)
-        // unit per thread, lanes on consecutive tokens; pair p of quarter qt
-        // goes to operand position 32 qt + 2p, so each operand row is written
-        // as four 16-byte chunks (a store phase covers 8 tokens: no conflicts)
-        {
-            static_assert(kTTok * 4 * 2 == kTThreads, "one key unit and one value unit per thread pair");
-            const bool vside = tid >= kTThreads / 2;   // first half: keys and signs; second: values
-            const int wd = warp & 7;
-            const int tok = 32 * (wd & 1) + lane, qt = wd >> 1;
-            __half* vrow = reinterpret_cast<__half*>(smem + P.vs_off) + tok * kVStride + 32 * qt;
-            auto kchunk = [&](int off, int i) {
-                return reinterpret_cast<uint4*>(smem + off + kmaj<kD>(tok, 32 * qt + 8 * i));
+    bool failed = false, o_started = false;
+    if (ctl) {
+        // ---------------- the control thread: record copies and MMAs
+        if (lane == 0) {
+            auto issue = [&](int i) {
+                const int t0 = i * TT;
+                const int lb = t0 / BT;
+                const int slot0 = t0 - lb * BT;
+                int64_t pb = a.table ? static_cast<int64_t>(a.table[static_cast<int64_t>(b) * a.max_blocks + lb])
+                                     : static_cast<int64_t>(b) * a.max_blocks + lb;
+                if (pb < 0 || pb >= a.pool.num_blocks) pb = 0;   // flagged and masked by the compute warps
+                const char* base = a.pool.base + (pb * Hkv + h) * a.pool.sub_bytes;
+                unsigned char* dst = smem + static_cast<size_t>(i & 1) * st.bytes;
+                unsigned total = 0;
+                for (int k = 0; k < 7; ++k)
+                    if (st.off[k] >= 0) total += TT * st.field[k];
+                tc::mbar_expect_tx(&bars[i & 1], total);
+                for (int k = 0; k < 7; ++k)
+                    if (st.off[k] >= 0)
+                        tc::bulk_g2s(dst + st.off[k],
+                                     base + a.pool.off[k] + static_cast<int64_t>(slot0) * st.field[k],
+                                     TT * st.field[k], &bars[i & 1]);
             };
-            if (tok < valid && !vside) {
-                const uint32_t* kidx = reinterpret_cast<const uint32_t*>(sp + st.off[0]);
-                uint32_t kw[KB], hk[16];
-                load_words<KB>(kidx + tok * (4 * KB) + qt * KB, kw);
-                mse_chunk<KB>(kw, ktab, hk);
+            constexpr uint32_t idS = tc::idesc_f16_f32(kTRows, kTTok);
+            constexpr uint32_t idO = tc::idesc_f16_f32(kTRows, kD + 16);
+            bool ok = true;
+            int issued = 0, s_commits = 0, o_commits = 0;
+            for (; issued < 2 && issued < ntiles; ++issued) issue(issued);
+            for (int j = 0; j < ntiles; ++j) {
+                ok = tc::mbar_wait(&bars[6], j & 1);   // tile j's operands are in shared memory
+                if (!ok) break;
+                tc::tc_fence_after();
 #pragma unroll
-                for (int i = 0; i < 4; ++i) *kchunk(P.k_off, i) = make_uint4(hk[4 * i], hk[4 * i + 1], hk[4 * i + 2], hk[4 * i + 3]);
-                if constexpr (KPROD) {
-                    const uint32_t sw = reinterpret_cast<const uint32_t*>(sp + st.off[1])[tok * 4 + qt];
-                    const uint32_t hg = h_bits(-reinterpret_cast<const float*>(sp + st.off[3])[tok]);
-                    const uint32_t neg2 = hg | (hg << 16);
-                    uint32_t hs[16];
-#pragma unroll
-                    for (int ks = 0; ks < 8; ++ks) {
-                        hs[2 * ks] = dec1(sw, 15 - ks, neg2);
-                        hs[2 * ks + 1] = dec1(sw, 7 - ks, neg2);
-                    }
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) *kchunk(P.s_off, i) = make_uint4(hs[4 * i], hs[4 * i + 1], hs[4 * i + 2], hs[4 * i + 3]);
+                for (int s = 0; s < kD / 16; ++s) {
+                    const uint64_t bk = tc::smem_desc(sbase + P.k_off + 256 * s, 128, 2048);
+                    tc::mma_f16_ta(tmem + kColS, tmem + kColQa + 8 * s, bk, idS, s > 0);
+                    if constexpr (KPROD)
+                        tc::mma_f16_ta(tmem + kColS, tmem + kColQj + 8 * s,
+                                       tc::smem_desc(sbase + P.s_off + 256 * s, 128, 2048), idS, 1);
+                    else
+                        tc::mma_f16_ta(tmem + kColS, tmem + kColQj + 8 * s, bk, idS, 1);
                 }
-                if (qt == 0) kn[tok] = reinterpret_cast<const float*>(sp + st.off[2])[tok];
-            } else if (tok < valid) {
-                const uint32_t* vidx = reinterpret_cast<const uint32_t*>(sp + st.off[4]);
-                uint32_t vwd[VB], hv[16];
-                load_words<VB>(vidx + tok * (4 * VB) + qt * VB, vwd);
-                if constexpr (VGROUP) {
-                    const int ng = kD / a.vc.group;
-                    const int gi = (32 * qt) / a.vc.group;
-                    const float sc = __half2float(reinterpret_cast<const __half*>(sp + st.off[5])[tok * ng + gi]);
-                    const float mn = __half2float(reinterpret_cast<const __half*>(sp + st.off[6])[tok * ng + gi]);
-                    const float mul = sc * (VB == 4 ? 16.0f : 4.0f);
-                    GroupChunk<VB>::run(vwd, pack_half2(mul, mul), pack_half2(mn, mn), hv);
+                tc::mma_commit(&bars[2]);
+                ++s_commits;
+                if (issued < ntiles) issue(issued++);   // tile j's stage has been decoded
+                ok = tc::mbar_wait(&bars[4], j & 1);   // P' (and the rescaled O) of tile j are in TMEM
+                if (!ok) break;
+                tc::tc_fence_after();
+#pragma unroll
+                for (int s = 0; s < kTTok / 16; ++s)
+                    tc::mma_f16_ta(tmem + kColO, tmem + kColP + 8 * s,
+                                   tc::smem_desc(sbase + P.vt_off + 256 * s, 128, 1024), idO, (j > 0 || s > 0) ? 1u : 0u);
+                tc::mma_commit(&bars[5]);
+                ++o_commits;
+            }
+            if (!ok) atomicOr(a.err, TQ_DEVERR_TIMEOUT);
+            // drain what is still in flight (after a timeout): the last copies and
+            // MMAs issued, whose phases are the most recent of their barriers
+            for (int t = issued > 2 ? issued - 2 : 0; t < issued; ++t) (void)tc::mbar_wait(&bars[t & 1], (t >> 1) & 1);
+            if (s_commits) (void)tc::mbar_wait(&bars[2], (s_commits - 1) & 1);
+            if (o_commits) (void)tc::mbar_wait(&bars[5], (o_commits - 1) & 1);
+        }
+        __syncwarp();
+    } else {
+        const auto ktab = mse_table<KB>(a.kc.c);
+        typename MseTable<VGROUP ? 2 : VB>::type vtab{};
+        if constexpr (!VGROUP) vtab = mse_table<VB>(a.vc.c);
+        float m = -INFINITY;
+
+        for (int i = 0; i < ntiles; ++i) {
+            const int par = i & 1;
+            const bool ring_ok = tc::mbar_wait(&bars[par], (i >> 1) & 1);
+            const unsigned char* sp = smem + static_cast<size_t>(par) * st.bytes;
+            const int t0 = i * TT;
+            int valid = min(TT, kend - t0);
+            {
+                const int lb = t0 / BT;
+                const int64_t pb = a.table ? static_cast<int64_t>(a.table[static_cast<int64_t>(b) * a.max_blocks + lb])
+                                           : static_cast<int64_t>(b) * a.max_blocks + lb;
+                if (pb < 0 || pb >= a.pool.num_blocks) {
+                    if (tid == 0) atomicOr(a.err, TQ_DEVERR_BLOCK);
+                    valid = 0;
+                }
+            }
+            float* kn = stash_kn(par);
+            float* vw = kn + kTTok;
+            __half* rhi = reinterpret_cast<__half*>(vw + kTTok);
+            __half* rlo = rhi + kTTok;
+
+            // ---------------- decode the tile: one (token, 32-coordinate quarter)
+            // unit per thread, lanes on consecutive tokens; pair p of quarter qt
+            // goes to operand position 32 qt + 2p, so each operand row is written
+            // as four 16-byte chunks (a store phase covers 8 tokens: no conflicts).
+            // The key and sign operands were last read by the previous tile's score
+            // MMA, which every thread has seen complete.
+            {
+                static_assert(kTTok * 4 * 2 == kTCompute, "one key unit and one value unit per thread pair");
+                const bool vside = tid >= kTCompute / 2;   // first half: keys and signs; second: values
+                const int wd = warp & 7;
+                const int tok = 32 * (wd & 1) + lane, qt = wd >> 1;
+                __half* vrow = reinterpret_cast<__half*>(smem + P.vs_off) + tok * kVStride + 32 * qt;
+                auto kchunk = [&](int off, int c) {
+                    return reinterpret_cast<uint4*>(smem + off + kmaj<kD>(tok, 32 * qt + 8 * c));
+                };
+                if (tok < valid && !vside) {
+                    const uint32_t* kidx = reinterpret_cast<const uint32_t*>(sp + st.off[0]);
+                    uint32_t kw[KB], hk[16];
+                    load_words<KB>(kidx + tok * (4 * KB) + qt * KB, kw);
+                    mse_chunk<KB>(kw, ktab, hk);
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) *kchunk(P.k_off, c) = make_uint4(hk[4 * c], hk[4 * c + 1], hk[4 * c + 2], hk[4 * c + 3]);
+                    if constexpr (KPROD) {
+                        const uint32_t sw = reinterpret_cast<const uint32_t*>(sp + st.off[1])[tok * 4 + qt];
+                        const uint32_t hg = h_bits(-reinterpret_cast<const float*>(sp + st.off[3])[tok]);
+                        const uint32_t neg2 = hg | (hg << 16);
+                        uint32_t hs[16];
+#pragma unroll
+                        for (int k2 = 0; k2 < 8; ++k2) {
+                            hs[2 * k2] = dec1(sw, 15 - k2, neg2);
+                            hs[2 * k2 + 1] = dec1(sw, 7 - k2, neg2);
+                        }
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) *kchunk(P.s_off, c) = make_uint4(hs[4 * c], hs[4 * c + 1], hs[4 * c + 2], hs[4 * c + 3]);
+                    }
+                    if (qt == 0) kn[tok] = reinterpret_cast<const float*>(sp + st.off[2])[tok];
+                } else if (tok < valid) {
+                    const uint32_t* vidx = reinterpret_cast<const uint32_t*>(sp + st.off[4]);
+                    uint32_t vwd[VB], hv[16];
+                    load_words<VB>(vidx + tok * (4 * VB) + qt * VB, vwd);
+                    if constexpr (VGROUP) {
+                        const int ng = kD / a.vc.group;
+                        const int gi = (32 * qt) / a.vc.group;
+                        const float sc = __half2float(reinterpret_cast<const __half*>(sp + st.off[5])[tok * ng + gi]);
+                        const float mn = __half2float(reinterpret_cast<const __half*>(sp + st.off[6])[tok * ng + gi]);
+                        const float mul = sc * (VB == 4 ? 16.0f : 4.0f);
+                        GroupChunk<VB>::run(vwd, pack_half2(mul, mul), pack_half2(mn, mn), hv);
+                    } else {
+                        mse_chunk<VB>(vwd, vtab, hv);
+                    }
+                    // P' carries the weight (the value norm; 1 for a zero vector, whose
+                    // operand row is zero), and rows kD, kD+1 of V^T carry 1 / weight
+                    float wt = 1.0f;
+                    if constexpr (!VGROUP) {
+                        const float nv = reinterpret_cast<const float*>(sp + st.off[5])[tok];
+                        if (nv > 0.0f) {
+                            wt = nv;
+                        } else {
+#pragma unroll
+                            for (int p = 0; p < 16; ++p) hv[p] = 0u;
+                        }
+                    }
+                    if (qt == 0) {
+                        const float rw = 1.0f / wt;
+                        const __half h1 = __float2half_rn(rw);
+                        vw[tok] = wt;
+                        rhi[tok] = h1;
+                        rlo[tok] = __float2half_rn(rw - __half2float(h1));
+                    }
+                    // values in pair order; the epilogue maps columns back to coordinates
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+                        reinterpret_cast<uint4*>(vrow)[c] = make_uint4(hv[4 * c], hv[4 * c + 1], hv[4 * c + 2], hv[4 * c + 3]);
                 } else {
-                    mse_chunk<VB>(vwd, vtab, hv);
-                }
-                // P' carries the weight (the value norm; 1 for a zero vector, whose
-                // operand row is zero), and rows kD, kD+1 of V^T carry 1 / weight
-                float wt = 1.0f;
-                if constexpr (!VGROUP) {
-                    const float nv = reinterpret_cast<const float*>(sp + st.off[5])[tok];
-                    if (nv > 0.0f) {
-                        wt = nv;
-                    } else {
+                    // masked tokens meet P' = 0: keep every operand finite
+                    const uint4 z = make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
-                        for (int p = 0; p < 16; ++p) hv[p] = 0u;
+                    for (int c = 0; c < 4; ++c) {
+                        if (vside) {
+                            reinterpret_cast<uint4*>(vrow)[c] = z;
+                        } else {
+                            *kchunk(P.k_off, c) = z;
+                            if constexpr (KPROD) *kchunk(P.s_off, c) = z;
+                        }
                     }
-                }
-                if (qt == 0) {
-                    const float rw = 1.0f / wt;
-                    const __half h1 = __float2half_rn(rw);
-                    vw[tok] = wt;
-                    rhi[tok] = h1;
-                    rlo[tok] = __float2half_rn(rw - __half2float(h1));
-                }
-                // values in pair order; the epilogue maps columns back to coordinates
-#pragma unroll
-                for (int i = 0; i < 4; ++i)
-                    reinterpret_cast<uint4*>(vrow)[i] = make_uint4(hv[4 * i], hv[4 * i + 1], hv[4 * i + 2], hv[4 * i + 3]);
-            } else {
-                // masked tokens meet P' = 0: keep every operand finite
-                const uint4 z = make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    if (vside) {
-                        reinterpret_cast<uint4*>(vrow)[i] = z;
-                    } else {
-                        *kchunk(P.k_off, i) = z;
-                        if constexpr (KPROD) *kchunk(P.s_off, i) = z;
-                    }
-                }
-                if (qt == 0) {
-                    if (vside) {
-                        vw[tok] = 0.0f;
-                        rhi[tok] = rlo[tok] = __float2half_rn(0.0f);
-                    } else {
-                        kn[tok] = 0.0f;
+                    if (qt == 0) {
+                        if (vside) {
+                            vw[tok] = 0.0f;
+                            rhi[tok] = rlo[tok] = __float2half_rn(0.0f);
+                        } else {
+                            kn[tok] = 0.0f;
+                        }
                     }
                 }
             }
-        }
-        __syncthreads();
-        // the previous tile's output MMA reads V^T and P': wait for it only now,
-        // so that it ran under this tile's decode
-        if (mma_pending) {
-            const bool done = tc::mbar_wait(&bars[2], mphase);
-            if (__syncthreads_or(!done)) {
+            // the previous tile's output MMA reads V^T and P': each thread waits for
+            // it only now, so that it ran under this tile's decode
+            bool o_ok = true;
+            if (i > 0) {
+                o_ok = tc::mbar_wait(&bars[5], (i - 1) & 1);
+                tc::tc_fence_after();
+            }
+            if (tc::bar_or(kBarCompute, kTCompute, !ring_ok || !o_ok)) {
                 failed = true;
                 break;
             }
-            mma_pending = false;
-            mphase ^= 1;
-            tc::tc_fence_after();
-        }
-        // values to V^T: 8x8 blocks (token block tb, dim block db), four per instruction
-        const __half* vs = reinterpret_cast<const __half*>(smem + P.vs_off);
-        for (int it = warp; it < (kD / 8) * (kTTok / 8) / 4; it += kTThreads / 32) {
-            const int mi = lane >> 3, rr = lane & 7;
-            const int blk = 4 * it + mi;
-            const int db = blk >> 3, tb = blk & 7;
-            uint32_t x0, x1, x2, x3;
-            tc::ldmatrix_x4_trans(x0, x1, x2, x3, vs + (8 * tb + rr) * kVStride + 8 * db);
-            tc::stmatrix_x4(smem + P.vt_off + kmaj<kTTok>(8 * db + rr, 8 * tb), x0, x1, x2, x3);
-        }
-        if (tid < 2 * (kTTok / 8)) {   // rows kD (hi) and kD+1 (lo), 8 tokens per chunk
-            const int n = tid >> 3, kc = tid & 7;
-            const uint4 v = reinterpret_cast<const uint4*>(n ? rlo : rhi)[kc];
-            *reinterpret_cast<uint4*>(smem + P.vt_off + kmaj<kTTok>(kD + n, 8 * kc)) = v;
-        }
-        tc::fence_proxy_async_smem();
-        tc::tc_fence_before();
-        __syncthreads();
+            // values to V^T: 8x8 blocks (token block tb, dim block db), four per instruction
+            const __half* vs = reinterpret_cast<const __half*>(smem + P.vs_off);
+            for (int it = warp; it < (kD / 8) * (kTTok / 8) / 4; it += kTCompute / 32) {
+                const int mi = lane >> 3, rr = lane & 7;
+                const int blk = 4 * it + mi;
+                const int db = blk >> 3, tb = blk & 7;
+                uint32_t x0, x1, x2, x3;
+                tc::ldmatrix_x4_trans(x0, x1, x2, x3, vs + (8 * tb + rr) * kVStride + 8 * db);
+                tc::stmatrix_x4(smem + P.vt_off + kmaj<kTTok>(8 * db + rr, 8 * tb), x0, x1, x2, x3);
+            }
+            if (tid < 2 * (kTTok / 8)) {   // rows kD (hi) and kD+1 (lo), 8 tokens per chunk
+                const int n = tid >> 3, kc = tid & 7;
+                const uint4 v = reinterpret_cast<const uint4*>(n ? rlo : rhi)[kc];
+                *reinterpret_cast<uint4*>(smem + P.vt_off + kmaj<kTTok>(kD + n, 8 * kc)) = v;
+            }
+            // hand the operands to the control thread
+            tc::fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&bars[6]);
 
-        // ---------------- scores on the tensor cores
-        if (tid == 0) {
+            // ---------------- softmax of this thread's quarter row (log2 units); the
+            // row maximum is exchanged with the row's other threads through shared memory
+            const bool s_ok = tc::mbar_wait(&bars[2], i & 1);
             tc::tc_fence_after();
+            float sv[HC];
+            tc::tmem_ld16(tS, sv);
+            {
+                const float4* k4 = reinterpret_cast<const float4*>(kn + HC * cq);
 #pragma unroll
-            for (int s = 0; s < kD / 16; ++s) {
-                const uint64_t bk = tc::smem_desc(sbase + P.k_off + 256 * s, 128, 2048);
-                tc::mma_f16(tS, tc::smem_desc(sbase + P.qa_off + 256 * s, 128, 2048), bk, idS, s > 0);
-                if constexpr (KPROD)
-                    tc::mma_f16(tS, tc::smem_desc(sbase + P.qj_off + 256 * s, 128, 2048),
-                                tc::smem_desc(sbase + P.s_off + 256 * s, 128, 2048), idS, 1);
-                else
-                    tc::mma_f16(tS, tc::smem_desc(sbase + P.qj_off + 256 * s, 128, 2048), bk, idS, 1);
+                for (int q = 0; q < HC / 4; ++q) {
+                    const float4 n4 = k4[q];
+                    sv[4 * q] *= n4.x;
+                    sv[4 * q + 1] *= n4.y;
+                    sv[4 * q + 2] *= n4.z;
+                    sv[4 * q + 3] *= n4.w;
+                }
             }
-            tc::mma_commit(&bars[2]);
-        }
-        mma_pending = true;
-        ok = tc::mbar_wait(&bars[2], mphase);
-        if (__syncthreads_or(!ok)) {
-            failed = true;
-            break;
-        }
-        mma_pending = false;
-        mphase ^= 1;
-        tc::tc_fence_after();
-
-        // ---------------- softmax of this thread's quarter row (log2 units); the
-        // row maximum is exchanged with the row's other threads through shared memory
-        float sv[HC];
-        tc::tmem_ld16(tS, sv);
-        {
-            const float4* k4 = reinterpret_cast<const float4*>(kn + HC * cq);
+            // a tile whose 64 operand columns are all valid tokens below every
+            // row's causal limit needs no mask (blocks shorter than 64 tokens
+            // leave zero columns, which the mask must keep out of the row sums)
+            const bool open = valid == kTTok && t0 + kTTok - 1 <= minlim;
+            if (!open) {
 #pragma unroll
-            for (int q = 0; q < HC / 4; ++q) {
-                const float4 n4 = k4[q];
-                sv[4 * q] *= n4.x;
-                sv[4 * q + 1] *= n4.y;
-                sv[4 * q + 2] *= n4.z;
-                sv[4 * q + 3] *= n4.w;
+                for (int c = 0; c < HC; ++c) {
+                    const int tc_ = HC * cq + c;
+                    if (!(tc_ < valid && t0 + tc_ <= lim)) sv[c] = -INFINITY;
+                }
             }
-        }
-        // a tile whose 64 operand columns are all valid tokens below every
-        // row's causal limit needs no mask (blocks shorter than 64 tokens
-        // leave zero columns, which the mask must keep out of the row sums)
-        const bool open = valid == kTTok && t0 + kTTok - 1 <= minlim;
-        if (!open) {
+            float mx = sv[0];
 #pragma unroll
-            for (int c = 0; c < HC; ++c) {
-                const int tc_ = HC * cq + c;
-                if (!(tc_ < valid && t0 + tc_ <= lim)) sv[c] = -INFINITY;
+            for (int c = 1; c < HC; ++c) mx = fmaxf(mx, sv[c]);
+            float* sx = s_x(par);
+            sx[cq * kTRows + row] = mx;
+            if (tc::bar_or(kBarCompute, kTCompute, !s_ok)) {
+                failed = true;
+                break;
             }
-        }
-        float mx = sv[0];
 #pragma unroll
-        for (int c = 1; c < HC; ++c) mx = fmaxf(mx, sv[c]);
-        s_x[cq * kTRows + row] = mx;
-        __syncthreads();
+            for (int o = 1; o < kTSplit; ++o) mx = fmaxf(mx, sx[((cq + o) & (kTSplit - 1)) * kTRows + row]);
+            // move the running maximum only when this tile exceeds it by the gap
+            // (the row's threads take the same decision from the same values)
+            const bool move = mx > m + kRescaleGap || (m == -INFINITY && mx != -INFINITY);
+            const float alpha = move ? (m == -INFINITY ? 0.0f : ex2(m - mx)) : 1.0f;
+            if (move) m = mx;
+            if (__any_sync(0xffffffffu, move) && o_started) {
+                float v[32];
+                tc::tmem_ld32(tO, v);
 #pragma unroll
-        for (int o = 1; o < kTSplit; ++o) mx = fmaxf(mx, s_x[((cq + o) & (kTSplit - 1)) * kTRows + row]);
-        // move the running maximum only when this tile exceeds it by the gap
-        // (the row's threads take the same decision from the same values)
-        const bool move = mx > m + kRescaleGap || (m == -INFINITY && mx != -INFINITY);
-        const float alpha = move ? (m == -INFINITY ? 0.0f : ex2(m - mx)) : 1.0f;
-        if (move) m = mx;
-        if (__any_sync(0xffffffffu, move) && o_started) {
-            float v[32];
-            tc::tmem_ld32(tO, v);
+                for (int e = 0; e < 32; ++e) v[e] *= alpha;
+                tc::tmem_st32(tO, v);
+                if (cq == 0) {   // the row-sum columns
+                    float w[16];
+                    tc::tmem_ld16(tL, w);
 #pragma unroll
-            for (int e = 0; e < 32; ++e) v[e] *= alpha;
-            tc::tmem_st32(tO, v);
-            if (cq == 0) {   // the row-sum column
-                float w[16];
-                tc::tmem_ld16(tL, w);
-#pragma unroll
-                for (int e = 0; e < 16; ++e) w[e] *= alpha;
-                tc::tmem_st16(tL, w);
+                    for (int e = 0; e < 16; ++e) w[e] *= alpha;
+                    tc::tmem_st16(tL, w);
+                }
             }
-        }
-        // P' = fp16(p * weight) into the A operand; the rows kD, kD+1 of V^T
-        // divide each rounded P' back by its weight for the row sum, so the
-        // rounding of P' cancels in O / l
-        float wv[HC];
-        {
+            // P' = fp16(p * weight) into TMEM (the A operand of the output MMA);
+            // the rows kD, kD+1 of V^T divide each rounded P' back by its weight
+            // for the row sum, so the rounding of P' cancels in O / l
             const float4* w4 = reinterpret_cast<const float4*>(vw + HC * cq);
+            uint32_t pw[HC / 2];
 #pragma unroll
             for (int q = 0; q < HC / 4; ++q) {
                 const float4 n4 = w4[q];
-                wv[4 * q] = n4.x;
-                wv[4 * q + 1] = n4.y;
-                wv[4 * q + 2] = n4.z;
-                wv[4 * q + 3] = n4.w;
-            }
-        }
-#pragma unroll
-        for (int c8 = 0; c8 < HC / 8; ++c8) {
-            uint32_t w[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int c = 8 * c8 + 2 * e;
-                float p0, p1;
+                const int c = 4 * q;
+                float p0, p1, p2, p3;
                 if (open) {   // finite scores, so a finite maximum
                     p0 = ex2(sv[c] - m);
                     p1 = ex2(sv[c + 1] - m);
+                    p2 = ex2(sv[c + 2] - m);
+                    p3 = ex2(sv[c + 3] - m);
                 } else {
                     p0 = m == -INFINITY ? 0.0f : ex2(sv[c] - m);
                     p1 = m == -INFINITY ? 0.0f : ex2(sv[c + 1] - m);
+                    p2 = m == -INFINITY ? 0.0f : ex2(sv[c + 2] - m);
+                    p3 = m == -INFINITY ? 0.0f : ex2(sv[c + 3] - m);
                 }
-                w[e] = pack_half2(p0 * wv[c], p1 * wv[c + 1]);
+                pw[2 * q] = pack_half2(p0 * n4.x, p1 * n4.y);
+                pw[2 * q + 1] = pack_half2(p2 * n4.z, p3 * n4.w);
             }
-            *reinterpret_cast<uint4*>(smem + P.p_off + kmaj<kTTok>(row, HC * cq + 8 * c8)) =
-                make_uint4(w[0], w[1], w[2], w[3]);
+            tc::tmem_st8u(t_row + kColP + (HC / 2) * cq, pw);
+            // hand P' and the rescaled O to the control thread
+            tc::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&bars[4]);
+            o_started = true;
         }
-        tc::fence_proxy_async_smem();
-        tc::tc_fence_before();
-        __syncthreads();
-
-        // ---------------- [O | row sum] += P' [V | 1/weight] on the tensor cores
-        if (tid == 0) {
+        if (!failed && o_started) {
+            const bool done = tc::mbar_wait(&bars[5], (ntiles - 1) & 1);
             tc::tc_fence_after();
-#pragma unroll
-            for (int s = 0; s < kTTok / 16; ++s)
-                tc::mma_f16(tmem + 128, tc::smem_desc(sbase + P.p_off + 256 * s, 128, 1024),
-                            tc::smem_desc(sbase + P.vt_off + 256 * s, 128, 1024), idO, (o_started || s > 0) ? 1u : 0u);
-            tc::mma_commit(&bars[2]);
+            if (tc::bar_or(kBarCompute, kTCompute, !done)) failed = true;
         }
-        o_started = true;
-        mma_pending = true;   // waited for before the next tile writes V^T and P'
+        if (failed && tid == 0) atomicOr(a.err, TQ_DEVERR_TIMEOUT);
     }
-    if (!failed && mma_pending) {
-        const bool done = tc::mbar_wait(&bars[2], mphase);
-        if (__syncthreads_or(!done)) {
-            failed = true;
-        } else {
-            mma_pending = false;
-            mphase ^= 1;
-            tc::tc_fence_after();
-        }
-    }
-    if (failed) {
-        if (tid == 0) atomicOr(a.err, TQ_DEVERR_TIMEOUT);
-        const int issued = min(ntiles, waited + 2);
-        for (int i = waited; i < issued; ++i) (void)tc::mbar_wait(&bars[i & 1], (i >> 1) & 1);
-        if (mma_pending) (void)tc::mbar_wait(&bars[2], mphase);
-    }
-    bool rv_ok = true;
-    if constexpr (!VGROUP) rv_ok = tc::mbar_wait(&bars[3], 0);
-    if (__syncthreads_or(!rv_ok) && tid == 0) atomicOr(a.err, TQ_DEVERR_TIMEOUT);
+    tc::tc_fence_before();
+    __syncthreads();   // the control thread has drained every copy and MMA
+    tc::tc_fence_after();
 
-    // ---------------- output rows: O / l staged in shared memory (over the
-    // query operands, padded rows), then rotated back by R_v, each thread
-    // writing its quarter of the row's dimensions
-    float l = 0.0f;
-    if (o_started && !failed) {
-        float w[16];
-        tc::tmem_ld16(tL, w);
-        l = w[0] + w[1];
-    }
-    float* orow = reinterpret_cast<float*>(smem + P.qa_off) + row * (kD + 1);
-    const float inv = (o_started && !failed && l > 0.0f) ? 1.0f / l : 0.0f;
-#pragma unroll 1
-    for (int c = 0; c < OC; c += 32) {
+    // ---------------- output rows: O / l staged in shared memory, then rotated
+    // back by R_v, each thread writing its quarter of the row's dimensions
+    failed = __syncthreads_or(failed);
+    float* orow = reinterpret_cast<float*>(smem + P.orow_off) + row * (kD + 1);
+    if (!ctl) {
+        float l = 0.0f;
+        if (o_started && !failed) {
+            float w[16];
+            tc::tmem_ld16(tL, w);
+            l = w[0] + w[1];
+        }
+        const float inv = (o_started && !failed && l > 0.0f) ? 1.0f / l : 0.0f;
         float v[32];
-        tc::tmem_ld32(tO + c, v);
+        tc::tmem_ld32(tO, v);
         // column 32 qt + 2p + odd holds coordinate 32 qt + (odd ? b : a) of value pair p
-        const int qbase = OC * cq + c;
+        const int qbase = OC * cq;
 #pragma unroll
         for (int e = 0; e < 32; ++e) {
             int pa, pb;
@@ -498,38 +506,38 @@ __global__ void __launch_bounds__(kTThreads, 1) prefill_tc_kernel(TcPrefillArgs 
             orow[qbase + ((e & 1) ? pb : pa)] = (o_started && !failed) ? v[e] * inv : 0.0f;  // TMEM unwritten otherwise
         }
     }
-    __syncthreads();
+    bool rv_ok = true;
+    if constexpr (!VGROUP) rv_ok = tc::mbar_wait(&bars[3], 0);
+    if (__syncthreads_or(!rv_ok) && tid == 0) atomicOr(a.err, TQ_DEVERR_TIMEOUT);
     if (row_ok) {
         const int gq = r / a.Lq, lq = r % a.Lq;
         float* dst = a.out + ((static_cast<int64_t>(b) * a.Hq + h * a.G + gq) * a.Lq + lq) * kD;
-#pragma unroll 1
-        for (int d0 = OC * cq; d0 < OC * cq + OC; d0 += 32) {
-            float acc[32];
-            if constexpr (VGROUP) {
+        const int d0 = OC * cq;
+        float acc[32];
+        if constexpr (VGROUP) {
 #pragma unroll
-                for (int e = 0; e < 32; ++e) acc[e] = orow[d0 + e];
-            } else {
+            for (int e = 0; e < 32; ++e) acc[e] = orow[d0 + e];
+        } else {
 #pragma unroll
-                for (int e = 0; e < 32; ++e) acc[e] = 0.0f;
+            for (int e = 0; e < 32; ++e) acc[e] = 0.0f;
 #pragma unroll 2
-                for (int i2 = 0; i2 < kD; ++i2) {
-                    const float ov = orow[i2];
-                    const float4* rr = reinterpret_cast<const float4*>(Rv + i2 * kD + d0);
+            for (int i2 = 0; i2 < kD; ++i2) {
+                const float ov = orow[i2];
+                const float4* rr = reinterpret_cast<const float4*>(Rv + i2 * kD + d0);
 #pragma unroll
-                    for (int q = 0; q < 8; ++q) {
-                        const float4 r4 = rr[q];
-                        acc[4 * q] = fmaf(ov, r4.x, acc[4 * q]);
-                        acc[4 * q + 1] = fmaf(ov, r4.y, acc[4 * q + 1]);
-                        acc[4 * q + 2] = fmaf(ov, r4.z, acc[4 * q + 2]);
-                        acc[4 * q + 3] = fmaf(ov, r4.w, acc[4 * q + 3]);
-                    }
+                for (int q = 0; q < 8; ++q) {
+                    const float4 r4 = rr[q];
+                    acc[4 * q] = fmaf(ov, r4.x, acc[4 * q]);
+                    acc[4 * q + 1] = fmaf(ov, r4.y, acc[4 * q + 1]);
+                    acc[4 * q + 2] = fmaf(ov, r4.z, acc[4 * q + 2]);
+                    acc[4 * q + 3] = fmaf(ov, r4.w, acc[4 * q + 3]);
                 }
             }
-#pragma unroll
-            for (int q = 0; q < 8; ++q)
-                *reinterpret_cast<float4*>(dst + d0 + 4 * q) =
-                    make_float4(acc[4 * q], acc[4 * q + 1], acc[4 * q + 2], acc[4 * q + 3]);
         }
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+            *reinterpret_cast<float4*>(dst + d0 + 4 * q) =
+                make_float4(acc[4 * q], acc[4 * q + 1], acc[4 * q + 2], acc[4 * q + 3]);
     }
     tc::tc_fence_before();
     __syncthreads();
@@ -538,7 +546,7 @@ __global__ void __launch_bounds__(kTThreads, 1) prefill_tc_kernel(TcPrefillArgs 
         tc::tmem_dealloc(tmem, 512);
     }
     if (tid == 0)
-        for (int s = 0; s < 4; ++s) tc::mbar_inval(&bars[s]);
+        for (int s = 0; s < 7; ++s) tc::mbar_inval(&bars[s]);
 }
 
 template <int KB, bool KPROD, bool VGROUP, int VB>
@@ -596,15 +604,15 @@ cudaError_t launch_prefill(const DecodeArgs& a, const uint4* qfrag, cudaStream_t
     }
     int off = 2 * p.st_bytes;
     off = (off + 1023) / 1024 * 1024;
-    P.qa_off = off; off += kTRows * kD * 2;
-    P.qj_off = off; off += kTRows * kD * 2;
     P.k_off = off; off += kTTok * kD * 2;
     P.s_off = off; off += p.kprod ? kTTok * kD * 2 : 0;   // sign operands (prod keys only)
-    P.vt_off = off; off += (kD + 16) * kTTok * 2;   // V^T plus a ones row and 15 zero rows
-    P.p_off = off; off += kTRows * kTTok * 2;
+    P.vt_off = off; off += (kD + 16) * kTTok * 2;           // V^T plus the 1/weight and zero rows
     P.vs_off = off; off += kTTok * kVStride * 2;
-    P.norm_off = off; off += 2 * kTTok * 4 + 2 * kTTok * 2;   // key norms, value weights, 1/weight hi, lo
-    P.rv_off = off; off += p.vgroup ? 0 : kD * kD * 4;        // group values are not rotated
+    P.norm_off = off; off += 2 * kStashBytes;
+    P.sx_off = off; off += 2 * kTSplit * kTRows * 4;
+    P.orow_off = off; off += kTRows * (kD + 1) * 4;
+    off = (off + 15) / 16 * 16;
+    P.rv_off = off; off += p.vgroup ? 0 : kD * kD * 4;       // group values are not rotated
     P.bar_off = off; off += 64;
     const size_t smem = static_cast<size_t>(off);
     if (smem > 232448) return cudaErrorInvalidValue;   // the largest dynamic shared memory a CTA can opt into
