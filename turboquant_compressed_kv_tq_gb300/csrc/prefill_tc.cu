@@ -51,20 +51,20 @@ constexpr int kTTok = 64;         // tokens per tile
 constexpr int kVStride = kD + 8;  // halves per row of the row-major value scratch
 constexpr float kRescaleGap = 8.0f;
 constexpr int kStashBytes = 2 * kTTok * 4 + 2 * kTTok * 2;   // per-tile norms and weights
-// TMEM columns: output [O | row sums] (144), scores (64), P' (32 of fp16 pairs),
-// the query operands Q' and Q'' (64 each, fp16 pairs)
-constexpr uint32_t kColO = 0, kColS = 256, kColP = 320, kColQa = 384, kColQj = 448;
+// TMEM columns: output [O | row sums] (144), scores of even and odd tiles (64
+// each), P' (32 of fp16 pairs), the query operands Q' and Q'' (64 each, fp16 pairs)
+constexpr uint32_t kColO = 0, kColS1 = 192, kColS0 = 256, kColP = 320, kColQa = 384, kColQj = 448;
 
 struct TcPrefillArgs {
     DecodeArgs a;
     StageLayout st;               // record streams of one tile
     const uint4* qfrag;           // [unit][2][8][32] uint4 (query-prep output)
-    int k_off, s_off;             // key levels and sign operands: 64 x 128 fp16
-    int vt_off;                   // V^T operand: 144 x 64 fp16 (value rows, 1/weight hi and lo, zero rows)
-    int vs_off;                   // value scratch [64][kVStride] fp16
-    int norm_off;                 // two stashes: key norms, value weights [2][64] floats; 1/weight [2][64] fp16
+    int k_off[2], s_off[2];       // key levels and sign operands of even / odd tiles: 64 x 128 fp16
+    int vt_off[2];                // V^T operands: 144 x 64 fp16 (value rows, 1/weight hi and lo, zero rows)
+    int vs_off[2];                // value scratch [64][kVStride] fp16
+    int norm_off;                 // three stashes: key norms, value weights [2][64] floats; 1/weight [2][64] fp16
     int sx_off;                   // row-maximum exchange [2][kTSplit][128] floats
-    int orow_off;                 // output staging [128][kD + 1] floats
+    int orow_off;                 // output staging [128][kD + 1] floats (over the operands, after the last tile)
     int rv_off;                   // R_v [kD][kD] floats (MSE values only)
     int bar_off;                  // mbarriers (7); then the TMEM slot and the row limits
 };
@@ -91,10 +91,11 @@ __global__ void __launch_bounds__(kTThreads, 1) prefill_tc_kernel(TcPrefillArgs 
     int* s_lim = reinterpret_cast<int*>(s_tmem + 1);                    // largest and smallest row limit
     float* Rv = reinterpret_cast<float*>(smem + P.rv_off);
     const uint32_t sbase = tc::smem_addr(smem);
-    // per-tile values, double-buffered by tile parity (a warp may run one
-    // phase ahead of another): key norms, value weights, 1/weight as fp16 hi, lo
-    auto stash_kn = [&](int par) { return reinterpret_cast<float*>(smem + P.norm_off + par * kStashBytes); };
-    auto s_x = [&](int par) { return reinterpret_cast<float*>(smem + P.sx_off) + par * kTSplit * kTRows; };
+    // per-tile values, three deep (tile t in stash t % 3: a warp may be a
+    // tile's decode ahead of another's softmax): key norms, value weights,
+    // 1/weight as fp16 hi, lo
+    auto stash_kn = [&](int t) { return reinterpret_cast<float*>(smem + P.norm_off + (t % 3) * kStashBytes); };
+    auto s_x = [&](int t) { return reinterpret_cast<float*>(smem + P.sx_off) + (t & 1) * kTSplit * kTRows; };
 
     // a compute thread's row (its warp's TMEM lane quarter) and column quarter
     const int row = 32 * (warp & 3) + lane, cq = (warp >> 2) & 3;
@@ -124,12 +125,12 @@ __global__ void __launch_bounds__(kTThreads, 1) prefill_tc_kernel(TcPrefillArgs 
             tc::bulk_g2s(Rv, a.vc.R, kD * kD * 4, &bars[3]);
         }
     }
-    // rows kD and kD+1 of the value operand hold 1 / weight (fp16 hi, lo) per
+    // rows kD and kD+1 of the value operands hold 1 / weight (fp16 hi, lo) per
     // token, so that their output columns accumulate the row sum of P' / weight;
     // rows kD+2..kD+15 stay zero
-    for (int e = tid; e < 16 * (kTTok / 8); e += kTThreads) {
-        const int n = kD + (e >> 3), kc = e & 7;
-        *reinterpret_cast<uint4*>(smem + P.vt_off + kmaj<kTTok>(n, 8 * kc)) = make_uint4(0u, 0u, 0u, 0u);
+    for (int e = tid; e < 2 * 16 * (kTTok / 8); e += kTThreads) {
+        const int bi = e >> 7, n = kD + ((e >> 3) & 15), kc = e & 7;
+        *reinterpret_cast<uint4*>(smem + P.vt_off[bi] + kmaj<kTTok>(n, 8 * kc)) = make_uint4(0u, 0u, 0u, 0u);
     }
     tc::fence_proxy_async_smem();
     tc::tc_fence_before();
@@ -142,7 +143,7 @@ __global__ void __launch_bounds__(kTThreads, 1) prefill_tc_kernel(TcPrefillArgs 
     const uint32_t tmem = *s_tmem;
     const uint32_t t_row = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
     constexpr int HC = kTTok / kTSplit, OC = kD / kTSplit;   // score and output columns per thread
-    const uint32_t tS = t_row + kColS + HC * cq, tO = t_row + kColO + OC * cq, tL = t_row + kColO + kD;
+    const uint32_t tO = t_row + kColO + OC * cq, tL = t_row + kColO + kD;
     // the query operands of this thread's row into TMEM: coordinate quarter cq
     // (pairs p of the query fragments, column 16 cq + p) of Q' and of Q''
     if (!ctl) {
@@ -169,7 +170,8 @@ __global__ void __launch_bounds__(kTThreads, 1) prefill_tc_kernel(TcPrefillArgs 
 
     bool failed = false, o_started = false;
     if (ctl) {
-        // ---------------- the control thread: record copies and MMAs
+        // ---------------- the control thread: record copies and MMAs. Tile j's
+        // scores go to TMEM columns S[j & 1] from the operand buffers j & 1
         if (lane == 0) {
             auto issue = [&](int i) {
                 const int t0 = i * TT;
@@ -196,18 +198,20 @@ __global__ void __launch_bounds__(kTThreads, 1) prefill_tc_kernel(TcPrefillArgs 
             int issued = 0, s_commits = 0, o_commits = 0;
             for (; issued < 2 && issued < ntiles; ++issued) issue(issued);
             for (int j = 0; j < ntiles; ++j) {
+                const int bj = j & 1;
                 ok = tc::mbar_wait(&bars[6], j & 1);   // tile j's operands are in shared memory
                 if (!ok) break;
                 tc::tc_fence_after();
+                const uint32_t dS = tmem + (bj ? kColS1 : kColS0);
 #pragma unroll
                 for (int s = 0; s < kD / 16; ++s) {
-                    const uint64_t bk = tc::smem_desc(sbase + P.k_off + 256 * s, 128, 2048);
-                    tc::mma_f16_ta(tmem + kColS, tmem + kColQa + 8 * s, bk, idS, s > 0);
+                    const uint64_t bk = tc::smem_desc(sbase + P.k_off[bj] + 256 * s, 128, 2048);
+                    tc::mma_f16_ta(dS, tmem + kColQa + 8 * s, bk, idS, s > 0);
                     if constexpr (KPROD)
-                        tc::mma_f16_ta(tmem + kColS, tmem + kColQj + 8 * s,
-                                       tc::smem_desc(sbase + P.s_off + 256 * s, 128, 2048), idS, 1);
+                        tc::mma_f16_ta(dS, tmem + kColQj + 8 * s,
+                                       tc::smem_desc(sbase + P.s_off[bj] + 256 * s, 128, 2048), idS, 1);
                     else
-                        tc::mma_f16_ta(tmem + kColS, tmem + kColQj + 8 * s, bk, idS, 1);
+                        tc::mma_f16_ta(dS, tmem + kColQj + 8 * s, bk, idS, 1);
                 }
                 tc::mma_commit(&bars[2]);
                 ++s_commits;
@@ -218,7 +222,8 @@ __global__ void __launch_bounds__(kTThreads, 1) prefill_tc_kernel(TcPrefillArgs 
 #pragma unroll
                 for (int s = 0; s < kTTok / 16; ++s)
                     tc::mma_f16_ta(tmem + kColO, tmem + kColP + 8 * s,
-                                   tc::smem_desc(sbase + P.vt_off + 256 * s, 128, 1024), idO, (j > 0 || s > 0) ? 1u : 0u);
+                                   tc::smem_desc(sbase + P.vt_off[bj] + 256 * s, 128, 1024), idO,
+                                   (j > 0 || s > 0) ? 1u : 0u);
                 tc::mma_commit(&bars[5]);
                 ++o_commits;
             }
@@ -236,12 +241,17 @@ __global__ void __launch_bounds__(kTThreads, 1) prefill_tc_kernel(TcPrefillArgs 
         if constexpr (!VGROUP) vtab = mse_table<VB>(a.vc.c);
         float m = -INFINITY;
 
-        for (int i = 0; i < ntiles; ++i) {
-            const int par = i & 1;
-            const bool ring_ok = tc::mbar_wait(&bars[par], (i >> 1) & 1);
-            const unsigned char* sp = smem + static_cast<size_t>(par) * st.bytes;
-            const int t0 = i * TT;
-            int valid = min(TT, kend - t0);
+        // ---------------- decode tile t into the operand buffers t & 1: one
+        // (token, 32-coordinate quarter) unit per thread, lanes on consecutive
+        // tokens; pair p of quarter qt goes to operand position 32 qt + 2p, so each
+        // operand row is written as four 16-byte chunks (no bank conflicts).
+        // Returns whether the tile's records arrived; `valid` = its valid tokens.
+        auto decode_tile = [&](int t, int& valid) -> bool {
+            const int bt = t & 1;
+            const bool ring_ok = tc::mbar_wait(&bars[bt], (t >> 1) & 1);
+            const unsigned char* sp = smem + static_cast<size_t>(bt) * st.bytes;
+            const int t0 = t * TT;
+            valid = min(TT, kend - t0);
             {
                 const int lb = t0 / BT;
                 const int64_t pb = a.table ? static_cast<int64_t>(a.table[static_cast<int64_t>(b) * a.max_blocks + lb])
@@ -251,143 +261,147 @@ __global__ void __launch_bounds__(kTThreads, 1) prefill_tc_kernel(TcPrefillArgs 
                     valid = 0;
                 }
             }
-            float* kn = stash_kn(par);
+            float* kn = stash_kn(t);
             float* vw = kn + kTTok;
             __half* rhi = reinterpret_cast<__half*>(vw + kTTok);
             __half* rlo = rhi + kTTok;
-
-            // ---------------- decode the tile: one (token, 32-coordinate quarter)
-            // unit per thread, lanes on consecutive tokens; pair p of quarter qt
-            // goes to operand position 32 qt + 2p, so each operand row is written
-            // as four 16-byte chunks (a store phase covers 8 tokens: no conflicts).
-            // The key and sign operands were last read by the previous tile's score
-            // MMA, which every thread has seen complete.
-            {
-                static_assert(kTTok * 4 * 2 == kTCompute, "one key unit and one value unit per thread pair");
-                const bool vside = tid >= kTCompute / 2;   // first half: keys and signs; second: values
-                const int wd = warp & 7;
-                const int tok = 32 * (wd & 1) + lane, qt = wd >> 1;
-                __half* vrow = reinterpret_cast<__half*>(smem + P.vs_off) + tok * kVStride + 32 * qt;
-                auto kchunk = [&](int off, int c) {
-                    return reinterpret_cast<uint4*>(smem + off + kmaj<kD>(tok, 32 * qt + 8 * c));
-                };
-                if (tok < valid && !vside) {
-                    const uint32_t* kidx = reinterpret_cast<const uint32_t*>(sp + st.off[0]);
-                    uint32_t kw[KB], hk[16];
-                    load_words<KB>(kidx + tok * (4 * KB) + qt * KB, kw);
-                    mse_chunk<KB>(kw, ktab, hk);
+            static_assert(kTTok * 4 * 2 == kTCompute, "one key unit and one value unit per thread pair");
+            const bool vside = tid >= kTCompute / 2;   // first half: keys and signs; second: values
+            const int wd = warp & 7;
+            const int tok = 32 * (wd & 1) + lane, qt = wd >> 1;
+            __half* vrow = reinterpret_cast<__half*>(smem + P.vs_off[bt]) + tok * kVStride + 32 * qt;
+            auto kchunk = [&](int off, int c) {
+                return reinterpret_cast<uint4*>(smem + off + kmaj<kD>(tok, 32 * qt + 8 * c));
+            };
+            if (tok < valid && !vside) {
+                const uint32_t* kidx = reinterpret_cast<const uint32_t*>(sp + st.off[0]);
+                uint32_t kw[KB], hk[16];
+                load_words<KB>(kidx + tok * (4 * KB) + qt * KB, kw);
+                mse_chunk<KB>(kw, ktab, hk);
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) *kchunk(P.k_off, c) = make_uint4(hk[4 * c], hk[4 * c + 1], hk[4 * c + 2], hk[4 * c + 3]);
-                    if constexpr (KPROD) {
-                        const uint32_t sw = reinterpret_cast<const uint32_t*>(sp + st.off[1])[tok * 4 + qt];
-                        const uint32_t hg = h_bits(-reinterpret_cast<const float*>(sp + st.off[3])[tok]);
-                        const uint32_t neg2 = hg | (hg << 16);
-                        uint32_t hs[16];
+                for (int c = 0; c < 4; ++c) *kchunk(P.k_off[bt], c) = make_uint4(hk[4 * c], hk[4 * c + 1], hk[4 * c + 2], hk[4 * c + 3]);
+                if constexpr (KPROD) {
+                    const uint32_t sw = reinterpret_cast<const uint32_t*>(sp + st.off[1])[tok * 4 + qt];
+                    const uint32_t hg = h_bits(-reinterpret_cast<const float*>(sp + st.off[3])[tok]);
+                    const uint32_t neg2 = hg | (hg << 16);
+                    uint32_t hs[16];
 #pragma unroll
-                        for (int k2 = 0; k2 < 8; ++k2) {
-                            hs[2 * k2] = dec1(sw, 15 - k2, neg2);
-                            hs[2 * k2 + 1] = dec1(sw, 7 - k2, neg2);
-                        }
-#pragma unroll
-                        for (int c = 0; c < 4; ++c) *kchunk(P.s_off, c) = make_uint4(hs[4 * c], hs[4 * c + 1], hs[4 * c + 2], hs[4 * c + 3]);
+                    for (int k2 = 0; k2 < 8; ++k2) {
+                        hs[2 * k2] = dec1(sw, 15 - k2, neg2);
+                        hs[2 * k2 + 1] = dec1(sw, 7 - k2, neg2);
                     }
-                    if (qt == 0) kn[tok] = reinterpret_cast<const float*>(sp + st.off[2])[tok];
-                } else if (tok < valid) {
-                    const uint32_t* vidx = reinterpret_cast<const uint32_t*>(sp + st.off[4]);
-                    uint32_t vwd[VB], hv[16];
-                    load_words<VB>(vidx + tok * (4 * VB) + qt * VB, vwd);
-                    if constexpr (VGROUP) {
-                        const int ng = kD / a.vc.group;
-                        const int gi = (32 * qt) / a.vc.group;
-                        const float sc = __half2float(reinterpret_cast<const __half*>(sp + st.off[5])[tok * ng + gi]);
-                        const float mn = __half2float(reinterpret_cast<const __half*>(sp + st.off[6])[tok * ng + gi]);
-                        const float mul = sc * (VB == 4 ? 16.0f : 4.0f);
-                        GroupChunk<VB>::run(vwd, pack_half2(mul, mul), pack_half2(mn, mn), hv);
-                    } else {
-                        mse_chunk<VB>(vwd, vtab, hv);
-                    }
-                    // P' carries the weight (the value norm; 1 for a zero vector, whose
-                    // operand row is zero), and rows kD, kD+1 of V^T carry 1 / weight
-                    float wt = 1.0f;
-                    if constexpr (!VGROUP) {
-                        const float nv = reinterpret_cast<const float*>(sp + st.off[5])[tok];
-                        if (nv > 0.0f) {
-                            wt = nv;
-                        } else {
 #pragma unroll
-                            for (int p = 0; p < 16; ++p) hv[p] = 0u;
-                        }
-                    }
-                    if (qt == 0) {
-                        const float rw = 1.0f / wt;
-                        const __half h1 = __float2half_rn(rw);
-                        vw[tok] = wt;
-                        rhi[tok] = h1;
-                        rlo[tok] = __float2half_rn(rw - __half2float(h1));
-                    }
-                    // values in pair order; the epilogue maps columns back to coordinates
-#pragma unroll
-                    for (int c = 0; c < 4; ++c)
-                        reinterpret_cast<uint4*>(vrow)[c] = make_uint4(hv[4 * c], hv[4 * c + 1], hv[4 * c + 2], hv[4 * c + 3]);
+                    for (int c = 0; c < 4; ++c) *kchunk(P.s_off[bt], c) = make_uint4(hs[4 * c], hs[4 * c + 1], hs[4 * c + 2], hs[4 * c + 3]);
+                }
+                if (qt == 0) kn[tok] = reinterpret_cast<const float*>(sp + st.off[2])[tok];
+            } else if (tok < valid) {
+                const uint32_t* vidx = reinterpret_cast<const uint32_t*>(sp + st.off[4]);
+                uint32_t vwd[VB], hv[16];
+                load_words<VB>(vidx + tok * (4 * VB) + qt * VB, vwd);
+                if constexpr (VGROUP) {
+                    const int ng = kD / a.vc.group;
+                    const int gi = (32 * qt) / a.vc.group;
+                    const float sc = __half2float(reinterpret_cast<const __half*>(sp + st.off[5])[tok * ng + gi]);
+                    const float mn = __half2float(reinterpret_cast<const __half*>(sp + st.off[6])[tok * ng + gi]);
+                    const float mul = sc * (VB == 4 ? 16.0f : 4.0f);
+                    GroupChunk<VB>::run(vwd, pack_half2(mul, mul), pack_half2(mn, mn), hv);
                 } else {
-                    // masked tokens meet P' = 0: keep every operand finite
-                    const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+                    mse_chunk<VB>(vwd, vtab, hv);
+                }
+                // P' carries the weight (the value norm; 1 for a zero vector, whose
+                // operand row is zero), and rows kD, kD+1 of V^T carry 1 / weight
+                float wt = 1.0f;
+                if constexpr (!VGROUP) {
+                    const float nv = reinterpret_cast<const float*>(sp + st.off[5])[tok];
+                    if (nv > 0.0f) {
+                        wt = nv;
+                    } else {
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        if (vside) {
-                            reinterpret_cast<uint4*>(vrow)[c] = z;
-                        } else {
-                            *kchunk(P.k_off, c) = z;
-                            if constexpr (KPROD) *kchunk(P.s_off, c) = z;
-                        }
+                        for (int p = 0; p < 16; ++p) hv[p] = 0u;
                     }
-                    if (qt == 0) {
-                        if (vside) {
-                            vw[tok] = 0.0f;
-                            rhi[tok] = rlo[tok] = __float2half_rn(0.0f);
-                        } else {
-                            kn[tok] = 0.0f;
-                        }
+                }
+                if (qt == 0) {
+                    const float rw = 1.0f / wt;
+                    const __half h1 = __float2half_rn(rw);
+                    vw[tok] = wt;
+                    rhi[tok] = h1;
+                    rlo[tok] = __float2half_rn(rw - __half2float(h1));
+                }
+                // values in pair order; the epilogue maps columns back to coordinates
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                    reinterpret_cast<uint4*>(vrow)[c] = make_uint4(hv[4 * c], hv[4 * c + 1], hv[4 * c + 2], hv[4 * c + 3]);
+            } else {
+                // masked tokens meet P' = 0: keep every operand finite
+                const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    if (vside) {
+                        reinterpret_cast<uint4*>(vrow)[c] = z;
+                    } else {
+                        *kchunk(P.k_off[bt], c) = z;
+                        if constexpr (KPROD) *kchunk(P.s_off[bt], c) = z;
+                    }
+                }
+                if (qt == 0) {
+                    if (vside) {
+                        vw[tok] = 0.0f;
+                        rhi[tok] = rlo[tok] = __float2half_rn(0.0f);
+                    } else {
+                        kn[tok] = 0.0f;
                     }
                 }
             }
-            // the previous tile's output MMA reads V^T and P': each thread waits for
-            // it only now, so that it ran under this tile's decode
-            bool o_ok = true;
-            if (i > 0) {
-                o_ok = tc::mbar_wait(&bars[5], (i - 1) & 1);
-                tc::tc_fence_after();
-            }
-            if (tc::bar_or(kBarCompute, kTCompute, !ring_ok || !o_ok)) {
-                failed = true;
-                break;
-            }
-            // values to V^T: 8x8 blocks (token block tb, dim block db), four per instruction
-            const __half* vs = reinterpret_cast<const __half*>(smem + P.vs_off);
+            return ring_ok;
+        };
+        // ---------------- tile t's values to V^T (8x8 blocks, four per
+        // instruction) and its 1/weight rows; then hand the operands to the
+        // control thread. Every warp's decode of tile t precedes this (barrier).
+        auto transpose_tile = [&](int t) {
+            const int bt = t & 1;
+            const __half* vs = reinterpret_cast<const __half*>(smem + P.vs_off[bt]);
             for (int it = warp; it < (kD / 8) * (kTTok / 8) / 4; it += kTCompute / 32) {
                 const int mi = lane >> 3, rr = lane & 7;
                 const int blk = 4 * it + mi;
                 const int db = blk >> 3, tb = blk & 7;
                 uint32_t x0, x1, x2, x3;
                 tc::ldmatrix_x4_trans(x0, x1, x2, x3, vs + (8 * tb + rr) * kVStride + 8 * db);
-                tc::stmatrix_x4(smem + P.vt_off + kmaj<kTTok>(8 * db + rr, 8 * tb), x0, x1, x2, x3);
+                tc::stmatrix_x4(smem + P.vt_off[bt] + kmaj<kTTok>(8 * db + rr, 8 * tb), x0, x1, x2, x3);
             }
             if (tid < 2 * (kTTok / 8)) {   // rows kD (hi) and kD+1 (lo), 8 tokens per chunk
+                const __half* rhi = reinterpret_cast<const __half*>(stash_kn(t) + 2 * kTTok);
                 const int n = tid >> 3, kc = tid & 7;
-                const uint4 v = reinterpret_cast<const uint4*>(n ? rlo : rhi)[kc];
-                *reinterpret_cast<uint4*>(smem + P.vt_off + kmaj<kTTok>(kD + n, 8 * kc)) = v;
+                const uint4 v = reinterpret_cast<const uint4*>(n ? rhi + kTTok : rhi)[kc];
+                *reinterpret_cast<uint4*>(smem + P.vt_off[bt] + kmaj<kTTok>(kD + n, 8 * kc)) = v;
             }
-            // hand the operands to the control thread
             tc::fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(&bars[6]);
+        };
+
+        // tile i's scores run on the tensor cores while tile i + 1 is decoded;
+        // its output MMA while tile i + 1 is transposed and tile i + 2 decoded
+        int valid_cur = 0;
+        bool late = false;   // a wait that failed after this tile's barrier
+        if (ntiles > 0) {
+            const bool ok0 = decode_tile(0, valid_cur);
+            if (tc::bar_or(kBarCompute, kTCompute, !ok0)) failed = true;
+            else transpose_tile(0);
+        }
+        for (int i = 0; i < ntiles && !failed; ++i) {
+            const bool more = i + 1 < ntiles;
+            int valid_next = 0;
+            const bool ring_ok = more ? decode_tile(i + 1, valid_next) : true;
 
             // ---------------- softmax of this thread's quarter row (log2 units); the
             // row maximum is exchanged with the row's other threads through shared memory
             const bool s_ok = tc::mbar_wait(&bars[2], i & 1);
             tc::tc_fence_after();
+            const float* kn = stash_kn(i);
+            const float* vw = kn + kTTok;
+            const int t0 = i * TT;
             float sv[HC];
-            tc::tmem_ld16(tS, sv);
+            tc::tmem_ld16(t_row + ((i & 1) ? kColS1 : kColS0) + HC * cq, sv);
             {
                 const float4* k4 = reinterpret_cast<const float4*>(kn + HC * cq);
 #pragma unroll
@@ -402,25 +416,31 @@ __global__ void __launch_bounds__(kTThreads, 1) prefill_tc_kernel(TcPrefillArgs 
             // a tile whose 64 operand columns are all valid tokens below every
             // row's causal limit needs no mask (blocks shorter than 64 tokens
             // leave zero columns, which the mask must keep out of the row sums)
-            const bool open = valid == kTTok && t0 + kTTok - 1 <= minlim;
+            const bool open = valid_cur == kTTok && t0 + kTTok - 1 <= minlim;
             if (!open) {
 #pragma unroll
                 for (int c = 0; c < HC; ++c) {
                     const int tc_ = HC * cq + c;
-                    if (!(tc_ < valid && t0 + tc_ <= lim)) sv[c] = -INFINITY;
+                    if (!(tc_ < valid_cur && t0 + tc_ <= lim)) sv[c] = -INFINITY;
                 }
             }
             float mx = sv[0];
 #pragma unroll
             for (int c = 1; c < HC; ++c) mx = fmaxf(mx, sv[c]);
-            float* sx = s_x(par);
+            float* sx = s_x(i);
             sx[cq * kTRows + row] = mx;
-            if (tc::bar_or(kBarCompute, kTCompute, !s_ok)) {
+            // every warp has decoded tile i + 1 and published its row maxima
+            if (tc::bar_or(kBarCompute, kTCompute, !s_ok || !ring_ok || late)) {
                 failed = true;
                 break;
             }
 #pragma unroll
             for (int o = 1; o < kTSplit; ++o) mx = fmaxf(mx, sx[((cq + o) & (kTSplit - 1)) * kTRows + row]);
+            // the previous tile's output MMA reads P' and the V^T buffers of tile i + 1
+            if (i > 0) {
+                late = !tc::mbar_wait(&bars[5], (i - 1) & 1);
+                tc::tc_fence_after();
+            }
             // move the running maximum only when this tile exceeds it by the gap
             // (the row's threads take the same decision from the same values)
             const bool move = mx > m + kRescaleGap || (m == -INFINITY && mx != -INFINITY);
@@ -470,11 +490,13 @@ __global__ void __launch_bounds__(kTThreads, 1) prefill_tc_kernel(TcPrefillArgs 
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(&bars[4]);
             o_started = true;
+            if (more) transpose_tile(i + 1);
+            valid_cur = valid_next;
         }
         if (!failed && o_started) {
             const bool done = tc::mbar_wait(&bars[5], (ntiles - 1) & 1);
             tc::tc_fence_after();
-            if (tc::bar_or(kBarCompute, kTCompute, !done)) failed = true;
+            if (tc::bar_or(kBarCompute, kTCompute, !done || late)) failed = true;
         }
         if (failed && tid == 0) atomicOr(a.err, TQ_DEVERR_TIMEOUT);
     }
@@ -482,8 +504,9 @@ __global__ void __launch_bounds__(kTThreads, 1) prefill_tc_kernel(TcPrefillArgs 
     __syncthreads();   // the control thread has drained every copy and MMA
     tc::tc_fence_after();
 
-    // ---------------- output rows: O / l staged in shared memory, then rotated
-    // back by R_v, each thread writing its quarter of the row's dimensions
+    // ---------------- output rows: O / l staged in shared memory (over the
+    // operand buffers, idle now), then rotated back by R_v, each thread writing
+    // its quarter of the row's dimensions
     failed = __syncthreads_or(failed);
     float* orow = reinterpret_cast<float*>(smem + P.orow_off) + row * (kD + 1);
     if (!ctl) {
@@ -604,16 +627,18 @@ cudaError_t launch_prefill(const DecodeArgs& a, const uint4* qfrag, cudaStream_t
     }
     int off = 2 * p.st_bytes;
     off = (off + 1023) / 1024 * 1024;
-    P.k_off = off; off += kTTok * kD * 2;
-    P.s_off = off; off += p.kprod ? kTTok * kD * 2 : 0;   // sign operands (prod keys only)
-    P.vt_off = off; off += (kD + 16) * kTTok * 2;           // V^T plus the 1/weight and zero rows
-    P.vs_off = off; off += kTTok * kVStride * 2;
-    P.norm_off = off; off += 2 * kStashBytes;
+    const int ops_begin = off;
+    for (int i = 0; i < 2; ++i) { P.k_off[i] = off; off += kTTok * kD * 2; }
+    for (int i = 0; i < 2; ++i) { P.s_off[i] = off; off += p.kprod ? kTTok * kD * 2 : 0; }   // prod keys only
+    for (int i = 0; i < 2; ++i) { P.vt_off[i] = off; off += (kD + 16) * kTTok * 2; }       // V^T, 1/weight and zero rows
+    const int ops_end = off;
+    for (int i = 0; i < 2; ++i) { P.vs_off[i] = off; off += kTTok * kVStride * 2; }
+    P.norm_off = off; off += 3 * kStashBytes;
     P.sx_off = off; off += 2 * kTSplit * kTRows * 4;
-    P.orow_off = off; off += kTRows * (kD + 1) * 4;
-    off = (off + 15) / 16 * 16;
     P.rv_off = off; off += p.vgroup ? 0 : kD * kD * 4;       // group values are not rotated
     P.bar_off = off; off += 64;
+    P.orow_off = ops_begin;                                  // after the last tile
+    if (ops_end - ops_begin < kTRows * (kD + 1) * 4) return cudaErrorInvalidValue;
     const size_t smem = static_cast<size_t>(off);
     if (smem > 232448) return cudaErrorInvalidValue;   // the largest dynamic shared memory a CTA can opt into
     if (p.kprod && p.kb == 2 && !p.vgroup && p.vb == 3) return launch_prefill_tc_t<2, true, false, 3>(P, smem, s);
