@@ -44,8 +44,8 @@ namespace {
 constexpr int kTRows = 128;       // query rows per CTA = MMA M = TMEM lanes
 constexpr int kTSplit = 4;        // threads per row: column quarters of its scores and output
 constexpr int kTCompute = kTRows * kTSplit;   // the decode and softmax warps
-constexpr int kTThreads = kTCompute + 32;     // plus one warp that issues copies and MMAs
-constexpr int kCtlWarp = kTCompute / 32;
+constexpr int kTThreads = kTCompute + 64;     // plus a warp that issues the MMAs and one for the copies
+constexpr int kCtlWarp = kTCompute / 32, kLoadWarp = kCtlWarp + 1;
 constexpr int kBarCompute = 1;    // named barrier of the compute warps
 constexpr int kTTok = 64;         // tokens per tile
 constexpr int kVStride = kD + 8;  // halves per row of the row-major value scratch
@@ -66,7 +66,7 @@ struct TcPrefillArgs {
     int sx_off;                   // row-maximum exchange [2][kTSplit][128] floats
     int orow_off;                 // output staging [128][kD + 1] floats (over the operands, after the last tile)
     int rv_off;                   // R_v [kD][kD] floats (MSE values only)
-    int bar_off;                  // mbarriers (7); then the TMEM slot and the row limits
+    int bar_off;                  // mbarriers (7); then the TMEM slot, the row limits and the consumed-tile count
 };
 
 // Byte offset of (row, k) in a K-major operand whose K extent is KX.
@@ -81,7 +81,7 @@ __global__ void __launch_bounds__(kTThreads, 1) prefill_tc_kernel(TcPrefillArgs 
     const DecodeArgs& a = P.a;
     const StageLayout& st = P.st;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const bool ctl = warp == kCtlWarp;
+    const bool ctl = warp == kCtlWarp, loader = warp == kLoadWarp;
     const int Hkv = a.pool.Hkv, RG = a.plan.row_groups, BT = a.pool.BT, TT = st.tt;
     const int h = blockIdx.y, b = blockIdx.z;
     // mbarriers: [0,1] tile records, [2] scores done, [3] R_v, [4] P' written by
@@ -89,6 +89,7 @@ __global__ void __launch_bounds__(kTThreads, 1) prefill_tc_kernel(TcPrefillArgs 
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + P.bar_off);
     uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + 7);
     int* s_lim = reinterpret_cast<int*>(s_tmem + 1);                    // largest and smallest row limit
+    int* s_consumed = s_lim + 2;   // tiles whose records every compute warp has decoded (control -> loader)
     float* Rv = reinterpret_cast<float*>(smem + P.rv_off);
     const uint32_t sbase = tc::smem_addr(smem);
     // per-tile values, three deep (tile t in stash t % 3: a warp may be a
@@ -102,7 +103,8 @@ __global__ void __launch_bounds__(kTThreads, 1) prefill_tc_kernel(TcPrefillArgs 
     const int w8 = row >> 4;                        // row group slot of the CTA
     const int rg = blockIdx.x + w8 * gridDim.x;
     const int r = rg * kRows + (row & 15);
-    const bool row_ok = !ctl && rg < RG && r < a.plan.rows;
+    const bool compute = warp < kCtlWarp;
+    const bool row_ok = compute && rg < RG && r < a.plan.rows;
     const int N = a.seq_lens[b];
     const bool bad = N < a.Lq || N > a.max_blocks * BT;
     if (bad && tid == 0 && blockIdx.x == 0 && h == 0) atomicOr(a.err, TQ_DEVERR_SEQLEN);
@@ -115,6 +117,7 @@ __global__ void __launch_bounds__(kTThreads, 1) prefill_tc_kernel(TcPrefillArgs 
     if (tid == 0) {
         s_lim[0] = -1;
         s_lim[1] = INT_MAX;
+        *s_consumed = 0;
         for (int s = 0; s < 4; ++s) tc::mbar_init(&bars[s], 1);
         tc::mbar_init(&bars[4], kTCompute / 32);
         tc::mbar_init(&bars[5], 1);
@@ -136,7 +139,7 @@ __global__ void __launch_bounds__(kTThreads, 1) prefill_tc_kernel(TcPrefillArgs 
     tc::tc_fence_before();
     __syncthreads();
     tc::tc_fence_after();
-    if (!ctl) {
+    if (compute) {
         atomicMax(&s_lim[0], lim);
         if (row_ok) atomicMin(&s_lim[1], lim);
     }
@@ -146,7 +149,7 @@ __global__ void __launch_bounds__(kTThreads, 1) prefill_tc_kernel(TcPrefillArgs 
     const uint32_t tO = t_row + kColO + OC * cq, tL = t_row + kColO + kD;
     // the query operands of this thread's row into TMEM: coordinate quarter cq
     // (pairs p of the query fragments, column 16 cq + p) of Q' and of Q''
-    if (!ctl) {
+    if (compute) {
         const int rgs = blockIdx.x + w8 * gridDim.x;
         const uint32_t* qf = reinterpret_cast<const uint32_t*>(P.qfrag) +
                              static_cast<int64_t>((b * Hkv + h) * RG + rgs) * 2048;
@@ -169,9 +172,9 @@ __global__ void __launch_bounds__(kTThreads, 1) prefill_tc_kernel(TcPrefillArgs 
     const int ntiles = kend > 0 ? (kend + TT - 1) / TT : 0;
 
     bool failed = false, o_started = false;
-    if (ctl) {
-        // ---------------- the control thread: record copies and MMAs. Tile j's
-        // scores go to TMEM columns S[j & 1] from the operand buffers j & 1
+    if (loader) {
+        // ---------------- the load thread: tile records into the two ring stages;
+        // tile j + 2 goes into tile j's stage once every compute warp has decoded it
         if (lane == 0) {
             auto issue = [&](int i) {
                 const int t0 = i * TT;
@@ -192,45 +195,73 @@ __global__ void __launch_bounds__(kTThreads, 1) prefill_tc_kernel(TcPrefillArgs 
                                      base + a.pool.off[k] + static_cast<int64_t>(slot0) * st.field[k],
                                      TT * st.field[k], &bars[i & 1]);
             };
+            int issued = 0;
+            bool ok = true;
+            for (; issued < 2 && issued < ntiles; ++issued) issue(issued);
+            while (issued < ntiles) {
+                unsigned it = 0;
+                while (tc::ld_acquire(s_consumed) < issued - 1 && ++it < tc::kSpinLimit) __nanosleep(32);
+                if (it >= tc::kSpinLimit) {
+                    ok = false;
+                    break;
+                }
+                issue(issued++);
+            }
+            if (!ok) atomicOr(a.err, TQ_DEVERR_TIMEOUT);
+            // drain the last copies (after a timeout elsewhere they may not have been waited for)
+            for (int t = issued > 2 ? issued - 2 : 0; t < issued; ++t) (void)tc::mbar_wait(&bars[t & 1], (t >> 1) & 1);
+        }
+        __syncwarp();
+    } else if (ctl) {
+        // ---------------- the control thread: the MMAs. Tile j's scores go to
+        // TMEM columns S[j & 1] from the operand buffers j & 1
+        if (lane == 0) {
             constexpr uint32_t idS = tc::idesc_f16_f32(kTRows, kTTok);
             constexpr uint32_t idO = tc::idesc_f16_f32(kTRows, kD + 16);
+            // descriptor words of the operand buffers; a 256-byte step of the start
+            // address adds 16 to the low word
+            auto lo_of = [&](int off, int lbo) {
+                return static_cast<uint32_t>(tc::smem_desc(sbase + off, lbo, 0) & 0xFFFFFFFFu);
+            };
+            const uint32_t hiK = static_cast<uint32_t>(tc::smem_desc(0, 0, 2048) >> 32);
+            const uint32_t hiV = static_cast<uint32_t>(tc::smem_desc(0, 0, 1024) >> 32);
+            const uint32_t loK0 = lo_of(P.k_off[0], 128), loK1 = lo_of(P.k_off[1], 128);
+            const uint32_t loS0 = KPROD ? lo_of(P.s_off[0], 128) : loK0;
+            const uint32_t loS1 = KPROD ? lo_of(P.s_off[1], 128) : loK1;
+            const uint32_t loV0 = lo_of(P.vt_off[0], 128), loV1 = lo_of(P.vt_off[1], 128);
             bool ok = true;
-            int issued = 0, s_commits = 0, o_commits = 0;
-            for (; issued < 2 && issued < ntiles; ++issued) issue(issued);
+            int s_commits = 0, o_commits = 0;
             for (int j = 0; j < ntiles; ++j) {
                 const int bj = j & 1;
                 ok = tc::mbar_wait(&bars[6], j & 1);   // tile j's operands are in shared memory
                 if (!ok) break;
+                tc::st_release(s_consumed, j + 1);    // and its records are free
                 tc::tc_fence_after();
                 const uint32_t dS = tmem + (bj ? kColS1 : kColS0);
+                const uint32_t k0 = bj ? loK1 : loK0, s0 = bj ? loS1 : loS0;
 #pragma unroll
                 for (int s = 0; s < kD / 16; ++s) {
-                    const uint64_t bk = tc::smem_desc(sbase + P.k_off[bj] + 256 * s, 128, 2048);
-                    tc::mma_f16_ta(dS, tmem + kColQa + 8 * s, bk, idS, s > 0);
-                    if constexpr (KPROD)
-                        tc::mma_f16_ta(dS, tmem + kColQj + 8 * s,
-                                       tc::smem_desc(sbase + P.s_off[bj] + 256 * s, 128, 2048), idS, 1);
-                    else
-                        tc::mma_f16_ta(dS, tmem + kColQj + 8 * s, bk, idS, 1);
+                    if (s == 0) tc::mma_f16_ta_w<false>(dS, tmem + kColQa, k0, hiK, idS);
+                    else tc::mma_f16_ta_w<true>(dS, tmem + kColQa + 8 * s, k0 + 16 * s, hiK, idS);
+                    tc::mma_f16_ta_w<true>(dS, tmem + kColQj + 8 * s, s0 + 16 * s, hiK, idS);
                 }
                 tc::mma_commit(&bars[2]);
                 ++s_commits;
-                if (issued < ntiles) issue(issued++);   // tile j's stage has been decoded
                 ok = tc::mbar_wait(&bars[4], j & 1);   // P' (and the rescaled O) of tile j are in TMEM
                 if (!ok) break;
                 tc::tc_fence_after();
+                const uint32_t v0 = bj ? loV1 : loV0;
+                if (j == 0) tc::mma_f16_ta_w<false>(tmem + kColO, tmem + kColP, v0, hiV, idO);
+                else tc::mma_f16_ta_w<true>(tmem + kColO, tmem + kColP, v0, hiV, idO);
 #pragma unroll
-                for (int s = 0; s < kTTok / 16; ++s)
-                    tc::mma_f16_ta(tmem + kColO, tmem + kColP + 8 * s,
-                                   tc::smem_desc(sbase + P.vt_off[bj] + 256 * s, 128, 1024), idO,
-                                   (j > 0 || s > 0) ? 1u : 0u);
+                for (int s = 1; s < kTTok / 16; ++s)
+                    tc::mma_f16_ta_w<true>(tmem + kColO, tmem + kColP + 8 * s, v0 + 16 * s, hiV, idO);
                 tc::mma_commit(&bars[5]);
                 ++o_commits;
             }
             if (!ok) atomicOr(a.err, TQ_DEVERR_TIMEOUT);
-            // drain what is still in flight (after a timeout): the last copies and
-            // MMAs issued, whose phases are the most recent of their barriers
-            for (int t = issued > 2 ? issued - 2 : 0; t < issued; ++t) (void)tc::mbar_wait(&bars[t & 1], (t >> 1) & 1);
+            // drain the last MMAs issued (after a timeout), whose phases are the
+            // most recent of their barriers
             if (s_commits) (void)tc::mbar_wait(&bars[2], (s_commits - 1) & 1);
             if (o_commits) (void)tc::mbar_wait(&bars[5], (o_commits - 1) & 1);
         }
@@ -509,7 +540,7 @@ __global__ void __launch_bounds__(kTThreads, 1) prefill_tc_kernel(TcPrefillArgs 
     // its quarter of the row's dimensions
     failed = __syncthreads_or(failed);
     float* orow = reinterpret_cast<float*>(smem + P.orow_off) + row * (kD + 1);
-    if (!ctl) {
+    if (compute) {
         float l = 0.0f;
         if (o_started && !failed) {
             float w[16];
@@ -636,7 +667,7 @@ cudaError_t launch_prefill(const DecodeArgs& a, const uint4* qfrag, cudaStream_t
     P.norm_off = off; off += 3 * kStashBytes;
     P.sx_off = off; off += 2 * kTSplit * kTRows * 4;
     P.rv_off = off; off += p.vgroup ? 0 : kD * kD * 4;       // group values are not rotated
-    P.bar_off = off; off += 64;
+    P.bar_off = off; off += 128;
     P.orow_off = ops_begin;                                  // after the last tile
     if (ops_end - ops_begin < kTRows * (kD + 1) * 4) return cudaErrorInvalidValue;
     const size_t smem = static_cast<size_t>(off);

@@ -140,6 +140,19 @@ __device__ __forceinline__ void mma_f16_ta(uint32_t d_tmem, uint32_t a_tmem, uin
         : "memory");
 }
 
+// The same with the B descriptor given as its low and high 32-bit words (a
+// caller stepping the start address adds to the low word only), accumulating
+// (acc = true) or overwriting D.
+template <bool kAcc>
+__device__ __forceinline__ void mma_f16_ta_w(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo, uint32_t b_hi,
+                                            uint32_t idesc) {
+    asm volatile(
+        "{\n .reg .b64 bd;\n mov.b64 bd, {%2, %3};\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], bd, %4, %5;\n}\n" ::"r"(d_tmem),
+        "r"(a_tmem), "r"(b_lo), "r"(b_hi), "r"(idesc), "n"(kAcc ? 1 : 0)
+        : "memory");
+}
+
 // Arrive once on `bar` when every tcgen05 operation this thread issued so far
 // has completed.
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
@@ -257,6 +270,17 @@ __device__ __forceinline__ void ldmatrix_x4_trans(uint32_t& r0, uint32_t& r1, ui
 // Programmatic dependent launch: wait until the grid this one depends on has
 // completed (its memory visible), or let the grids that depend on this one
 // start their prologues.
+// Release store / acquire load of a shared-memory word (CTA scope).
+__device__ __forceinline__ void st_release(int* p, int v) {
+    asm volatile("st.release.cta.shared::cta.u32 [%0], %1;\n" ::"r"(smem_addr(p)), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ int ld_acquire(const int* p) {
+    int v;
+    asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];\n" : "=r"(v) : "r"(smem_addr(p)) : "memory");
+    return v;
+}
+
 // Barrier `id` among `count` threads (whole warps) that also ORs `pred` over
 // them; the same memory ordering as __syncthreads among those threads.
 __device__ __forceinline__ bool bar_or(int id, int count, bool pred) {
