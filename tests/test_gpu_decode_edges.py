@@ -1,0 +1,138 @@
+"""Decode parity at the edges of the decode's tiling.
+
+Token counts around the 64-token tiles and 128-token blocks (only the query
+positions, a tile minus one, exactly one tile, one over) for every codec pair
+of the prefill kernels, 128- to 512-token blocks in a shuffled order, causal
+query lengths above one, more than 16 query rows (two row groups), a sequence
+long enough for many token splits, per-head scales, and inputs with zero,
+tiny and one-hot vectors (zero-norm values, zero keys). Every output row is
+compared with the oracle's decode of the same raw inputs (the max abs error
+and cosine bounds of the decode parity rule); the last case checks that two
+block sizes of one cache decode alike.
+"""
+import dataclasses
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+import turboquant_compressed_kv_tq_gb300 as tq
+from turboquant_compressed_kv_tq_gb300 import workloads as wl
+from parity_util import GpuCase, compare_decode, oracle_decode, raw_kv, to_f32_np
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib_built():
+    from turboquant_compressed_kv_tq_gb300 import build
+    build.build()
+    assert torch.cuda.is_available()
+
+
+def _workload(key, value, lens, Lq, Hkv, G, bt, shuffle=False, scales=None, seed=5):
+    kspec = wl._spec(key[0], key[1], 21)
+    vspec = wl._spec(value[0], value[1], 22, value[2] if len(value) > 2 else 0)
+    return wl.Workload("decode_tc", 1, len(lens), Hkv, Hkv * G, 128, tuple(lens), Lq, torch.bfloat16, 1.0,
+                       seed, kspec, vspec, block_tokens=bt, shuffle_blocks=shuffle, append_per_step=0,
+                       prefill_chunk=1024, head_scale_range=scales)
+
+
+def _check(w):
+    case = GpuCase(w, layers=[0])
+    case.prefill()
+    q = wl.queries(w, 0, 0, DEV)
+    out = to_f32_np(case.decode(0, q))
+    assert tq.tq_device_error() == 0
+    assert np.isfinite(out).all()
+    qn = to_f32_np(q).astype(np.float64)
+    G = w.gqa
+    for b in range(w.batch):
+        K, V = raw_kv(w, 0, b, w.seq_lens[b], DEV)
+        for h in range(w.num_kv_heads):
+            compare_decode(out[b, h * G:(h + 1) * G], oracle_decode(w, K[h], V[h], qn[b, h * G:(h + 1) * G]))
+
+
+@pytest.mark.parametrize("key,value", [(("prod", 3), ("mse", 3)), (("prod", 3), ("mse", 4)),
+                                       (("prod", 3), ("group", 4, 64)), (("mse", 4), ("mse", 4))])
+def test_tile_edges_every_codec_pair(key, value):
+    # one sequence per tile edge (the shortest holds just the
+    # two query positions), GQA 8
+    _check(_workload(key, value, (2, 127, 128, 129, 700), 2, 2, 8, 128))
+
+
+@pytest.mark.parametrize("bt", [128, 256, 512])
+def test_block_sizes_shuffled_pages(bt):
+    _check(_workload(("prod", 3), ("mse", 3), (300, 1000, 2049), 1, 2, 4, bt, shuffle=True))
+
+
+def test_two_row_groups_causal():
+    # G 8 x q_len 4 = 32 rows per KV head; the newest 4 tokens are causal
+    _check(_workload(("prod", 3), ("mse", 3), (513, 1280), 4, 2, 8, 256))
+
+
+def test_many_splits_long_sequence():
+    # one KV head: the plan spreads 40,000 tokens over many token splits
+    _check(_workload(("prod", 3), ("mse", 3), (40000,), 2, 1, 8, 256))
+
+
+def test_head_scales_mse4():
+    _check(_workload(("mse", 4), ("mse", 4), (5000,), 2, 2, 8, 256, scales=(0.5, 2.0)))
+
+
+def test_group_values_one_query_row_per_head():
+    _check(_workload(("prod", 3), ("group", 4, 64), (129, 3000), 1, 2, 1, 128, shuffle=True))
+
+
+@pytest.mark.parametrize("key,value", [(("prod", 3), ("mse", 3)), (("mse", 4), ("mse", 4))])
+def test_stress_vectors(key, value):
+    # keys and values with zero rows (zero norms), one-hot rows, constant rows
+    # and scales 2^-12 .. 2^12: the decode of those records against the oracle's
+    w = _workload(key, value, (900,), 2, 2, 4, 256)
+    D, Hkv, N = w.head_dim, w.num_kv_heads, w.seq_lens[0]
+    K = wl.encoder_stress(71, 1, Hkv, N, D, torch.bfloat16, DEV)
+    V = wl.encoder_stress(72, 1, Hkv, N, D, torch.bfloat16, DEV)
+    case = GpuCase(w, layers=[0])
+    zero = torch.zeros(1, dtype=torch.int32, device=DEV)
+    case.cache.append(0, K, V, zero, case.table_d, case.max_blocks)
+    torch.cuda.synchronize()
+    q = wl.queries(w, 0, 0, DEV)
+    out = to_f32_np(case.decode(0, q))
+    assert tq.tq_device_error() == 0
+    assert np.isfinite(out).all()
+    qn = to_f32_np(q).astype(np.float64)
+    Kn, Vn = to_f32_np(K[0]), to_f32_np(V[0])
+    G = w.gqa
+    for h in range(Hkv):
+        ref = oracle_decode(w, Kn[h], Vn[h], qn[0, h * G:(h + 1) * G]).reshape(-1, D)
+        got = out[0, h * G:(h + 1) * G].reshape(-1, D).astype(np.float64)
+        # value rows at 2^12 make outputs of that magnitude: compare relative to it
+        scale = max(1.0, float(np.abs(ref).max()))
+        assert np.abs(got - ref).max() / scale <= 2e-3
+        # 2^12-scaled keys concentrate a row's weight on one token, whose value
+        # may be a zero or 2^-100 vector: such rows are zero to fp32, and a
+        # cosine says nothing about them; every other row meets the bound
+        norm = np.linalg.norm(ref, axis=-1)
+        live = norm > 1e-3 * scale
+        assert live.sum() >= len(live) // 2
+        compare_decode(got[live] / scale, ref[live] / scale)
+
+
+def test_block_size_does_not_change_the_result():
+    # the same tokens cached in 128-token and in 64-token blocks decode alike
+    # (the token splits and block lookups differ)
+    w = _workload(("prod", 3), ("mse", 3), (1500,), 2, 2, 8, 128)
+    case = GpuCase(w, layers=[0])
+    case.prefill()
+    q = wl.queries(w, 0, 0, DEV)
+    out_tc = to_f32_np(case.decode(0, q))
+    w64 = dataclasses.replace(w, block_tokens=64)
+    case64 = GpuCase(w64, layers=[0])
+    case64.prefill()
+    out_mma = to_f32_np(case64.decode(0, q))
+    assert tq.tq_device_error() == 0
+    assert np.abs(out_tc - out_mma).max() <= 2e-3

@@ -91,3 +91,40 @@ def test_prefill_attention_unsupported_codecs():
     with pytest.raises(tq.TQError) as e:
         cache.prefill_workspace_bytes(1, 8, 32)
     assert e.value.status == 2
+
+
+def test_prefill_attention_stress_vectors():
+    # values with zero rows (zero norms), one-hot and constant rows and scales
+    # 2^-12 .. 2^12 (value norms up to ~5e4: P' = p * norm must stay inside
+    # fp16 while the running maximum lags by its gap); N(0, 1) keys (keys at
+    # 2^12 would make the softmax an argmax whose near-ties the fp16 query
+    # operand cannot resolve, whichever kernel computes it)
+    w = wl.Workload("prefill_stress", 1, 1, 2, 16, 128, (700,), 300, torch.bfloat16, 1.0, 3,
+                    wl._spec("prod", 3, 0), wl._spec("mse", 3, 1), block_tokens=64, append_per_step=0,
+                    prefill_chunk=512)
+    D, Hkv, N, Lq, G = 128, 2, 700, 300, 8
+    K = wl.kv_chunk(w, 0, 0, 0, N, "k", DEV).unsqueeze(0)
+    V = wl.encoder_stress(82, 1, Hkv, N, D, torch.bfloat16, DEV)
+    case = GpuCase(w, layers=[0])
+    zero = torch.zeros(1, dtype=torch.int32, device=DEV)
+    case.cache.append(0, K, V, zero, case.table_d, case.max_blocks)
+    q = wl.queries(w, 0, 0, DEV)
+    ws = torch.empty(case.cache.prefill_workspace_bytes(1, w.num_q_heads, Lq), dtype=torch.uint8, device=DEV)
+    out = torch.full((1, w.num_q_heads, Lq, D), float("nan"), dtype=torch.float32, device=DEV)
+    sl = torch.tensor([N], dtype=torch.int32, device=DEV)
+    case.cache.prefill_attention(0, q, sl, case.table_d, case.max_blocks, out, ws)
+    torch.cuda.synchronize()
+    assert tq.tq_device_error() == 0
+    out = to_f32_np(out)
+    assert np.isfinite(out).all()
+    qn = to_f32_np(q).astype(np.float64)
+    Kn, Vn = to_f32_np(K[0]), to_f32_np(V[0])
+    for h in range(Hkv):
+        ref = oracle_decode(w, Kn[h], Vn[h], qn[0, h * G:(h + 1) * G]).reshape(-1, D)
+        got = out[0, h * G:(h + 1) * G].reshape(-1, D).astype(np.float64)
+        scale = max(1.0, float(np.abs(ref).max()))
+        assert np.abs(got - ref).max() / scale <= 2e-3
+        # rows whose weight sits on a zero or 2^-100 value are zero to fp32
+        live = np.linalg.norm(ref, axis=-1) > 1e-3 * scale
+        assert live.sum() >= len(live) // 2
+        compare_decode(got[live] / scale, ref[live] / scale)

@@ -253,6 +253,77 @@ __device__ __forceinline__ void mse_chunk(const uint32_t* w, const typename MseT
     MseChunk<B>::run(w, t, h);
 }
 
+// The last CTA of a unit (by arrival ticket) merges the splits' partial
+// (max, sum, accumulator) rows, divides by the merged sum, applies the inverse
+// value rotation and writes the output rows; every CTA has written its own
+// partials before calling. `orot` is shared memory for 16 x (kD + 1) floats;
+// threads 0..255 merge (16 per row, 8 columns each).
+template <bool VGROUP>
+__device__ __forceinline__ void merge_unit(const MmaArgs& m, int unit, int split, int rg, int b, int h, float* orot,
+                                           int tid) {
+    const DecodeArgs& a = m.a;
+    constexpr int kStride = kD + 1;
+    const int S = a.plan.splits;
+    const int r = tid >> 4;
+    const int dbase = (tid & 15) * 8;
+    const bool merger = tid < kRows * 16;
+    __threadfence();
+    __syncthreads();
+    __shared__ unsigned s_ticket;
+    if (tid == 0) s_ticket = atomicAdd(m.cnt + unit, 1u);
+    __syncthreads();
+    if (s_ticket != static_cast<unsigned>(S - 1)) return;
+    __threadfence();
+    if (merger) {
+        float M = -INFINITY;
+        const float* mlu = m.ml + static_cast<int64_t>(unit) * S * kRows * 2;
+        for (int s = 0; s < S; ++s) M = fmaxf(M, __ldcg(mlu + (s * kRows + r) * 2));
+        float L = 0.0f, acc[8] = {};
+        if (M != -INFINITY) {
+            for (int s = 0; s < S; ++s) {
+                const float ms = __ldcg(mlu + (s * kRows + r) * 2);
+                if (ms == -INFINITY) continue;
+                const float wt = ex2(ms - M);
+                L = fmaf(wt, __ldcg(mlu + (s * kRows + r) * 2 + 1), L);
+                const float4* src = reinterpret_cast<const float4*>(
+                    m.part + ((static_cast<int64_t>(unit) * S + s) * kRows + r) * kD + dbase);
+                const float4 v0 = __ldcg(src), v1 = __ldcg(src + 1);
+                acc[0] = fmaf(wt, v0.x, acc[0]); acc[1] = fmaf(wt, v0.y, acc[1]);
+                acc[2] = fmaf(wt, v0.z, acc[2]); acc[3] = fmaf(wt, v0.w, acc[3]);
+                acc[4] = fmaf(wt, v1.x, acc[4]); acc[5] = fmaf(wt, v1.y, acc[5]);
+                acc[6] = fmaf(wt, v1.z, acc[6]); acc[7] = fmaf(wt, v1.w, acc[7]);
+            }
+        }
+        const float inv = L > 0.0f ? 1.0f / L : 0.0f;
+        for (int k = 0; k < 8; ++k) orot[r * kStride + dbase + k] = acc[k] * inv;
+    }
+    __syncthreads();
+    const int row = rg * kRows + r;
+    if (merger && row < a.plan.rows) {
+        float res[8];
+        if constexpr (!VGROUP) {
+            for (int k = 0; k < 8; ++k) res[k] = 0.0f;
+            const float* R = a.vc.R;
+            for (int i2 = 0; i2 < kD; ++i2) {
+                const float ov = orot[r * kStride + i2];
+                const float4 r0 = __ldg(reinterpret_cast<const float4*>(R + i2 * kD + dbase));
+                const float4 r1 = __ldg(reinterpret_cast<const float4*>(R + i2 * kD + dbase) + 1);
+                res[0] = fmaf(ov, r0.x, res[0]); res[1] = fmaf(ov, r0.y, res[1]);
+                res[2] = fmaf(ov, r0.z, res[2]); res[3] = fmaf(ov, r0.w, res[3]);
+                res[4] = fmaf(ov, r1.x, res[4]); res[5] = fmaf(ov, r1.y, res[5]);
+                res[6] = fmaf(ov, r1.z, res[6]); res[7] = fmaf(ov, r1.w, res[7]);
+            }
+        } else {
+            for (int k = 0; k < 8; ++k) res[k] = orot[r * kStride + dbase + k];
+        }
+        const int gq = row / a.Lq, l = row % a.Lq;
+        float* dst = a.out + ((static_cast<int64_t>(b) * a.Hq + h * a.G + gq) * a.Lq + l) * kD + dbase;
+        reinterpret_cast<float4*>(dst)[0] = make_float4(res[0], res[1], res[2], res[3]);
+        reinterpret_cast<float4*>(dst)[1] = make_float4(res[4], res[5], res[6], res[7]);
+    }
+    if (tid == 0) m.cnt[unit] = 0u;
+}
+
 template <int KB, bool KPROD, bool VGROUP, int VB>
 __global__ void __launch_bounds__(kThreads, 1) split_mma_kernel(MmaArgs m) {
     extern __shared__ __align__(128) unsigned char smem[];
@@ -581,63 +652,7 @@ __global__ void __launch_bounds__(kThreads, 1) split_mma_kernel(MmaArgs m) {
             mlp[1] = L;
         }
     }
-    // ---------------- the last CTA of this unit merges the splits
-    __threadfence();
-    __syncthreads();
-    __shared__ unsigned s_ticket;
-    if (tid == 0) s_ticket = atomicAdd(m.cnt + unit, 1u);
-    __syncthreads();
-    if (s_ticket != static_cast<unsigned>(S - 1)) return;
-    __threadfence();
-    float* orot = cm;  // [16][kStride]
-    if (merger) {
-        float M = -INFINITY;
-        const float* mlu = m.ml + static_cast<int64_t>(unit) * S * kRows * 2;
-        for (int s = 0; s < S; ++s) M = fmaxf(M, __ldcg(mlu + (s * kRows + r) * 2));
-        float L = 0.0f, acc[8] = {};
-        if (M != -INFINITY) {
-            for (int s = 0; s < S; ++s) {
-                const float ms = __ldcg(mlu + (s * kRows + r) * 2);
-                if (ms == -INFINITY) continue;
-                const float wt = ex2(ms - M);
-                L = fmaf(wt, __ldcg(mlu + (s * kRows + r) * 2 + 1), L);
-                const float4* src = reinterpret_cast<const float4*>(
-                    m.part + ((static_cast<int64_t>(unit) * S + s) * kRows + r) * kD + dbase);
-                const float4 v0 = __ldcg(src), v1 = __ldcg(src + 1);
-                acc[0] = fmaf(wt, v0.x, acc[0]); acc[1] = fmaf(wt, v0.y, acc[1]);
-                acc[2] = fmaf(wt, v0.z, acc[2]); acc[3] = fmaf(wt, v0.w, acc[3]);
-                acc[4] = fmaf(wt, v1.x, acc[4]); acc[5] = fmaf(wt, v1.y, acc[5]);
-                acc[6] = fmaf(wt, v1.z, acc[6]); acc[7] = fmaf(wt, v1.w, acc[7]);
-            }
-        }
-        const float inv = L > 0.0f ? 1.0f / L : 0.0f;
-        for (int k = 0; k < 8; ++k) orot[r * kStride + dbase + k] = acc[k] * inv;
-    }
-    __syncthreads();
-    const int row = rg * kRows + r;
-    if (merger && row < a.plan.rows) {
-        float res[8];
-        if constexpr (!VGROUP) {
-            for (int k = 0; k < 8; ++k) res[k] = 0.0f;
-            const float* R = a.vc.R;
-            for (int i2 = 0; i2 < kD; ++i2) {
-                const float ov = orot[r * kStride + i2];
-                const float4 r0 = __ldg(reinterpret_cast<const float4*>(R + i2 * kD + dbase));
-                const float4 r1 = __ldg(reinterpret_cast<const float4*>(R + i2 * kD + dbase) + 1);
-                res[0] = fmaf(ov, r0.x, res[0]); res[1] = fmaf(ov, r0.y, res[1]);
-                res[2] = fmaf(ov, r0.z, res[2]); res[3] = fmaf(ov, r0.w, res[3]);
-                res[4] = fmaf(ov, r1.x, res[4]); res[5] = fmaf(ov, r1.y, res[5]);
-                res[6] = fmaf(ov, r1.z, res[6]); res[7] = fmaf(ov, r1.w, res[7]);
-            }
-        } else {
-            for (int k = 0; k < 8; ++k) res[k] = orot[r * kStride + dbase + k];
-        }
-        const int gq = row / a.Lq, l = row % a.Lq;
-        float* dst = a.out + ((static_cast<int64_t>(b) * a.Hq + h * a.G + gq) * a.Lq + l) * kD + dbase;
-        reinterpret_cast<float4*>(dst)[0] = make_float4(res[0], res[1], res[2], res[3]);
-        reinterpret_cast<float4*>(dst)[1] = make_float4(res[4], res[5], res[6], res[7]);
-    }
-    if (tid == 0) m.cnt[unit] = 0u;
+    merge_unit<VGROUP>(m, unit, split, rg, b, h, cm, tid);
 }
 
 template <int KB, bool KPROD, bool VGROUP, int VB>

@@ -50,7 +50,9 @@ constexpr int kBarCompute = 1;    // named barrier of the compute warps
 constexpr int kTTok = 64;         // tokens per tile
 constexpr int kVStride = kD + 8;  // halves per row of the row-major value scratch
 constexpr float kRescaleGap = 8.0f;
-constexpr int kStashBytes = 2 * kTTok * 4 + 2 * kTTok * 2;   // per-tile norms and weights
+// per-tile stash: key norms, value weights [64] floats each, 1/weight hi and
+// lo [64] fp16 each, then whether a weight of each half tile exceeds 256 [2]
+constexpr int kStashBytes = 2 * kTTok * 4 + 2 * kTTok * 2 + 16;
 // TMEM columns: output [O | row sums] (144), scores of even and odd tiles (64
 // each), P' (32 of fp16 pairs), the query operands Q' and Q'' (64 each, fp16 pairs)
 constexpr uint32_t kColO = 0, kColS1 = 192, kColS0 = 256, kColP = 320, kColQa = 384, kColQj = 448;
@@ -304,6 +306,7 @@ __global__ void __launch_bounds__(kTThreads, 1) prefill_tc_kernel(TcPrefillArgs 
             auto kchunk = [&](int off, int c) {
                 return reinterpret_cast<uint4*>(smem + off + kmaj<kD>(tok, 32 * qt + 8 * c));
             };
+            float wt = 0.0f;   // the value thread's weight (0 for a masked token)
             if (tok < valid && !vside) {
                 const uint32_t* kidx = reinterpret_cast<const uint32_t*>(sp + st.off[0]);
                 uint32_t kw[KB], hk[16];
@@ -341,7 +344,7 @@ __global__ void __launch_bounds__(kTThreads, 1) prefill_tc_kernel(TcPrefillArgs 
                 }
                 // P' carries the weight (the value norm; 1 for a zero vector, whose
                 // operand row is zero), and rows kD, kD+1 of V^T carry 1 / weight
-                float wt = 1.0f;
+                wt = 1.0f;
                 if constexpr (!VGROUP) {
                     const float nv = reinterpret_cast<const float*>(sp + st.off[5])[tok];
                     if (nv > 0.0f) {
@@ -382,6 +385,10 @@ __global__ void __launch_bounds__(kTThreads, 1) prefill_tc_kernel(TcPrefillArgs 
                         kn[tok] = 0.0f;
                     }
                 }
+            }
+            if (vside && qt == 0) {   // whole warps: does a weight of these 32 tokens exceed 256?
+                const bool big = __any_sync(0xffffffffu, wt > 256.0f);
+                if (lane == 0) reinterpret_cast<int*>(rlo + kTTok)[wd & 1] = big;
             }
             return ring_ok;
         };
@@ -474,7 +481,16 @@ __global__ void __launch_bounds__(kTThreads, 1) prefill_tc_kernel(TcPrefillArgs 
             }
             // move the running maximum only when this tile exceeds it by the gap
             // (the row's threads take the same decision from the same values)
-            const bool move = mx > m + kRescaleGap || (m == -INFINITY && mx != -INFINITY);
+            // the gap is 8, or less when a value weight of the tile exceeds 256, so
+            // that P' = p * weight <= 2^15.8 stays inside fp16
+            const int* big = reinterpret_cast<const int*>(reinterpret_cast<const __half*>(vw + kTTok) + 2 * kTTok);
+            float gap = kRescaleGap;
+            if (big[0] | big[1]) {   // rare: the tile's largest weight
+                float wmax = 0.0f;
+                for (int t = 0; t < kTTok; ++t) wmax = fmaxf(wmax, vw[t]);
+                gap = fminf(kRescaleGap, 15.8f - __log2f(wmax));
+            }
+            const bool move = mx > m + gap || (m == -INFINITY && mx != -INFINITY);
             const float alpha = move ? (m == -INFINITY ? 0.0f : ex2(m - mx)) : 1.0f;
             if (move) m = mx;
             if (__any_sync(0xffffffffu, move) && o_started) {
