@@ -5,20 +5,27 @@
 // runs on the 5th-generation tensor cores: one persistent CTA per SM keeps the
 // codec's operand tables in shared memory and, per 128-token tile,
 //   GEMM 1  Y = X~ (R_hi + R_lo)^T      (tcgen05.mma kind::f16, fp32 in TMEM)
-//   epilogue: one thread per token reads its row of Y from TMEM, forms
-//            y = Y * 2^e / (16 n), the Lloyd-Max index #{midpoints < y}, packs
-//            the indices, and for prod keys the residual r = y - c[index],
+//   epilogue: y = Y * 2^e / (16 n), the Lloyd-Max index #{midpoints < y}, the
+//            packed indices, and for prod keys the residual r = y - c[index],
 //            its norm, and r~ = 256 r split into fp16 hi/lo operand tiles
 //   GEMM 2  Z = (r~_hi + r~_lo)(S_hi + S_lo)^T, minus the lo*lo term (prod)
 //   epilogue: sign bits (Z >= 0), residual norm and norm stored.
-// Operands: X~ = x * 2^-e (e = exponent of the norm) is exact in fp16 for bf16
-// or f16 inputs down to 2^-14 of the norm; 16 R and S are split into fp16
-// hi + lo (about 22 significant bits). Products are exact and sums are fp32,
-// so y and S r carry errors far below the fp32 dot-product bound of the
-// sequential specification: an index or sign can differ from it only where the
-// exact value lies within rounding distance of a decision threshold (a
-// midpoint, or 0). The norm keeps the specification's sequential fused
-// multiply-add order and is bit-exact.
+// The work is split across warps and pipelined over tiles:
+//   producer warps (4, one thread per token) load a token, compute its norm
+//            in the specification's sequential fused multiply-add order
+//            (bit-exact) and write X~ = x * 2^-e into the operand tile;
+//   MMA warp issues GEMM 1 of tile i + 1 while tile i's epilogue runs (two
+//            TMEM accumulators), then GEMM 2 of tile i;
+//   epilogue warps (8, two threads per token, column halves of its TMEM row)
+//            quantise, pack and store, and form the residual operands.
+// Hand-offs are mbarriers (per buffer: a producer arrives for a buffer's next
+// use only after the consumer of its previous use has signalled it free).
+// Operands: X~ is exact in fp16 for bf16 or f16 inputs down to 2^-14 of the
+// norm; 16 R and S are split into fp16 hi + lo (about 22 significant bits).
+// Products are exact and sums are fp32, so y and S r carry errors far below
+// the fp32 dot-product bound of the sequential specification: an index or
+// sign can differ from it only where the exact value lies within rounding
+// distance of a decision threshold (a midpoint, or 0).
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -28,15 +35,26 @@
 namespace tq {
 namespace {
 
-constexpr int kTileRows = 128;  // tokens per tile = MMA M = TMEM lanes used
+constexpr int kTileRows = 128;   // tokens per tile = MMA M = TMEM lanes used
+constexpr int kProdWarps = 4;    // warps 0..3: one thread per token
+constexpr int kEpiWarps = 8;     // warps 4..11: lane quarter warp % 4, column half (warp - 4) / 4
+constexpr int kMmaWarp = kProdWarps + kEpiWarps;
+constexpr int kEncThreads = 32 * (kMmaWarp + 1);
+constexpr int kEpiBar = 1;       // named barrier of the epilogue warps
 
-// Threads per token: prod keys (one CTA per SM: their operand tables fill
-// shared memory) split each token's TMEM row between two threads; MSE codecs
-// run two CTAs per SM with one thread per token.
-template <bool PROD>
-struct Split {
-    static constexpr int kTPT = PROD ? 2 : 1;
-    static constexpr int kThreads = kTileRows * kTPT;
+// mbarriers
+enum : int {
+    kBarTab = 0,        // codec tables copied
+    kBarAFull = 1,      // X~ tile written (4 producer warps)
+    kBarAEmpty = 2,     // GEMM 1 read it (commit)
+    kBarYFull = 3,      // [2] GEMM 1 done (commit)
+    kBarYEmpty = 5,     // [2] epilogue read the accumulator (8 epilogue warps)
+    kBarRFull = 7,      // residual tiles written (8 epilogue warps)
+    kBarREmpty = 8,     // GEMM 2 read them (commit)
+    kBarZFull = 9,      // GEMM 2 done (commit)
+    kBarZEmpty = 10,    // epilogue read Z (8 epilogue warps)
+    kBarNorm = 11,      // [3] a tile's norms written (4 producer warps)
+    kNumBars = 14
 };
 
 template <int D, bool PROD>
@@ -45,12 +63,18 @@ struct TcLayout {
     static constexpr int kTile = kTileRows * D * 2;      // one fp16 operand tile
     static constexpr int oR = 0;
     static constexpr int oS = oR + kTab;
-    static constexpr int oA0 = oS + (PROD ? kTab : 0);   // inputs, then residual hi
-    static constexpr int oA1 = oA0 + kTile;              // residual lo (prod)
-    static constexpr int oMisc = oA1 + (PROD ? kTile : 0);
-    static constexpr int kBytes = oMisc + 2048;
+    static constexpr int oA = oS + (PROD ? kTab : 0);    // X~
+    static constexpr int oRh = oA + kTile;               // residual hi (prod)
+    static constexpr int oRl = oRh + (PROD ? kTile : 0); // residual lo (prod)
+    static constexpr int oNorm = oRl + (PROD ? kTile : 0);   // [3][128] norms
+    static constexpr int oG2 = oNorm + 3 * kTileRows * 4;     // [2][128] residual sums of half 1
+    static constexpr int oCb = oG2 + 2 * kTileRows * 4;       // centroids [16], midpoints [16]
+    static constexpr int oBar = oCb + 128;
+    static constexpr int kBytes = oBar + 128;
     static constexpr uint32_t kLbo = 128;                // next 8 columns (K)
     static constexpr uint32_t kSbo = 16 * D;             // next 8 rows (M/N)
+    // TMEM: accumulators Y[2] (D columns each) and Z (prod)
+    static constexpr uint32_t kCols = PROD ? (D == 128 ? 512 : 256) : (D == 128 ? 256 : 128);
 };
 
 // Byte offset of element (row, k) of a [rows][D] fp16 operand tile in the
@@ -105,42 +129,78 @@ __device__ __forceinline__ void store_words(uint32_t* dst, const uint32_t (&w)[N
     }
 }
 
+// Lloyd-Max index #{j : y > m_j} over the 2^KB - 1 sorted midpoints, as a
+// binary search with register selects (KB compares instead of 2^KB - 1).
+template <int KB>
+__device__ __forceinline__ int lm_index(float y, const float (&m)[(1 << KB) - 1]) {
+    if constexpr (KB == 1) {
+        return y > m[0] ? 1 : 0;
+    } else if constexpr (KB == 2) {
+        const int b1 = y > m[1];
+        const int b0 = y > (b1 ? m[2] : m[0]);
+        return 2 * b1 + b0;
+    } else if constexpr (KB == 3) {
+        const int b2 = y > m[3];
+        const int b1 = y > (b2 ? m[5] : m[1]);
+        const float t0 = b2 ? (b1 ? m[6] : m[4]) : (b1 ? m[2] : m[0]);
+        const int b0 = y > t0;
+        return 4 * b2 + 2 * b1 + b0;
+    } else {
+        const int b3 = y > m[7];
+        const int b2 = y > (b3 ? m[11] : m[3]);
+        const float t1 = b3 ? (b2 ? m[13] : m[9]) : (b2 ? m[5] : m[1]);
+        const int b1 = y > t1;
+        const int hi = 4 * b3 + 2 * b2 + b1;   // which pair of midpoints is left: m[2 hi], m[2 hi + ...]
+        float t0 = m[0];
+#pragma unroll
+        for (int k = 1; k < 8; ++k) t0 = hi == k ? m[2 * k] : t0;
+        const int b0 = y > t0;
+        return 2 * hi + b0;
+    }
+}
+
 template <int D, int KB, bool PROD>
-__global__ void __launch_bounds__(Split<PROD>::kThreads, 1)
+__global__ void __launch_bounds__(kEncThreads, 1)
     encode_tc_kernel(EncodeAppendArgs a, int is_v, int tiles_per_seq) {
     using L = TcLayout<D, PROD>;
-    constexpr int TPT = Split<PROD>::kTPT;
     constexpr int NM = (1 << KB) - 1;   // midpoints
     constexpr int W = D * KB / 32;      // index words
     constexpr int WS = D / 32;          // sign words
-    constexpr int DH = D / TPT;         // columns per thread
-    constexpr int CH = DH / 32;         // 32-column chunks per thread
+    constexpr int DH = D / 2;           // columns per epilogue thread
+    constexpr int CH = DH / 32;         // 32-column chunks per epilogue thread
     extern __shared__ __align__(1024) unsigned char smem[];
-    float* s_c = reinterpret_cast<float*>(smem + L::oMisc);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::oBar);
+    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + kNumBars);
+    float* s_norm = reinterpret_cast<float*>(smem + L::oNorm);
+    float* s_g2 = reinterpret_cast<float*>(smem + L::oG2);
+    float* s_c = reinterpret_cast<float*>(smem + L::oCb);
     float* s_m = s_c + 16;
-    uint64_t* bar_tab = reinterpret_cast<uint64_t*>(smem + L::oMisc + 128);
-    uint64_t* bar_mma = bar_tab + 1;
-    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bar_tab + 2);
-    float* s_n2 = reinterpret_cast<float*>(smem + L::oMisc + 256);    // [128] first-half norm sums
-    float* s_nrm = s_n2 + kTileRows;                                  // [128] norms
-    float* s_g2 = s_nrm + kTileRows;                                  // [128] second-half residual sums
 
     const CodecDev& cd = is_v ? a.vc : a.kc;
-    const int tid = threadIdx.x, warp = tid >> 5;
-    const int row = tid & (kTileRows - 1), half = TPT == 2 ? (tid >> 7) : 0;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t sbase = tc::smem_addr(smem);
 
     if (warp == 0) {
-        tc::tmem_alloc(s_tmem, D);
+        tc::tmem_alloc(s_tmem, L::kCols);
         tc::tmem_relinquish();
     }
     if (tid == 0) {
-        tc::mbar_init(bar_tab, 1);
-        tc::mbar_init(bar_mma, 1);
+        tc::mbar_init(&bars[kBarTab], 1);
+        tc::mbar_init(&bars[kBarAFull], kProdWarps);
+        tc::mbar_init(&bars[kBarAEmpty], 1);
+        for (int i = 0; i < 2; ++i) {
+            tc::mbar_init(&bars[kBarYFull + i], 1);
+            tc::mbar_init(&bars[kBarYEmpty + i], kEpiWarps);
+        }
+        tc::mbar_init(&bars[kBarRFull], kEpiWarps);
+        tc::mbar_init(&bars[kBarREmpty], 1);
+        tc::mbar_init(&bars[kBarZFull], 1);
+        tc::mbar_init(&bars[kBarZEmpty], kEpiWarps);
+        for (int i = 0; i < 3; ++i) tc::mbar_init(&bars[kBarNorm + i], kProdWarps);
         tc::mbar_fence_init();
-        tc::mbar_expect_tx(bar_tab, (PROD ? 2 : 1) * L::kTab);
-        tc::bulk_g2s(smem + L::oR, cd.Rtc, L::kTab, bar_tab);
-        if constexpr (PROD) tc::bulk_g2s(smem + L::oS, cd.Stc, L::kTab, bar_tab);
+        tc::mbar_expect_tx(&bars[kBarTab], (PROD ? 2 : 1) * L::kTab);
+        tc::bulk_g2s(smem + L::oR, cd.Rtc, L::kTab, &bars[kBarTab]);
+        if constexpr (PROD) tc::bulk_g2s(smem + L::oS, cd.Stc, L::kTab, &bars[kBarTab]);
     }
     if (tid < 16) {
         s_c[tid] = tid <= NM ? cd.c[tid] : 0.0f;
@@ -150,239 +210,257 @@ __global__ void __launch_bounds__(Split<PROD>::kThreads, 1)
     __syncthreads();
     tc::tc_fence_after();
     const uint32_t tmem = *s_tmem;
-    const uint32_t tmem_row = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + DH * half;
-    float mreg[NM];
-#pragma unroll
-    for (int j = 0; j < NM; ++j) mreg[j] = s_m[j];
-
-    bool ok = tc::mbar_wait(bar_tab, 0);
-    const bool tables_failed = __syncthreads_or(!ok);
+    const bool tables_failed = __syncthreads_or(!tc::mbar_wait(&bars[kBarTab], 0));
 
     const int Hkv = a.pool.Hkv;
     const int64_t ntiles = static_cast<int64_t>(a.batch) * Hkv * tiles_per_seq;
-    const char* src = static_cast<const char*>(is_v ? a.v : a.k);
-    const int64_t o_idx = is_v ? a.pool.off[4] : a.pool.off[0];
-    const int64_t o_norm = is_v ? a.pool.off[5] : a.pool.off[2];
-    constexpr uint32_t idesc = tc::idesc_f16_f32(kTileRows, D);
-    unsigned phase = 0;
+    const int n_it = blockIdx.x < ntiles ? static_cast<int>((ntiles - 1 - blockIdx.x) / gridDim.x + 1) : 0;
+    auto tile_of = [&](int it) { return static_cast<int64_t>(blockIdx.x) + static_cast<int64_t>(it) * gridDim.x; };
     bool failed = tables_failed;
-    unsigned char* A0 = smem + L::oA0;
-    unsigned char* A1 = smem + L::oA1;
 
-    // this thread's columns of its token in a tile, loaded one tile ahead
-    uint4 nraw[DH / 8];
-    auto load_row = [&](int64_t tl) {
-        const int ts = static_cast<int>(tl % tiles_per_seq);
-        const int bh = static_cast<int>(tl / tiles_per_seq);
-        const int t = ts * kTileRows + row;
-        const bool ok_row = tl < ntiles && t < a.n_new;
-        const int64_t r = (static_cast<int64_t>(bh / Hkv) * Hkv + bh % Hkv) * a.n_new + t;
-        const uint4* p = reinterpret_cast<const uint4*>(src + r * D * 2) + half * (DH / 8);
+    if (warp < kProdWarps) {
+        // ---------------- producers: norm (sequential order) and X~ of one token
+        const char* src = static_cast<const char*>(is_v ? a.v : a.k);
+        const int row = tid;
+        for (int it = 0; it < n_it && !failed; ++it) {
+            const int64_t tile = tile_of(it);
+            const int ts = static_cast<int>(tile % tiles_per_seq);
+            const int bh = static_cast<int>(tile / tiles_per_seq);
+            const int t = ts * kTileRows + row;
+            const bool valid = t < a.n_new;
+            const uint4* p = reinterpret_cast<const uint4*>(src + (static_cast<int64_t>(bh) * a.n_new + t) * D * 2);
+            uint4 raw[D / 8];
 #pragma unroll
-        for (int c8 = 0; c8 < DH / 8; ++c8) nraw[c8] = ok_row ? __ldg(p + c8) : make_uint4(0, 0, 0, 0);
-    };
-    load_row(blockIdx.x);
-
-    for (int64_t tile = blockIdx.x; tile < ntiles && !failed; tile += gridDim.x) {
-        const int ts = static_cast<int>(tile % tiles_per_seq);
-        const int bh = static_cast<int>(tile / tiles_per_seq);
-        const int h = bh % Hkv, b = bh / Hkv;
-        const int t = ts * kTileRows + row;
-        const bool valid = t < a.n_new;
-
-        // ---------------- this thread's columns (loaded during the previous tile):
-        // the norm's sequential fma chain runs over the first half, then
-        // continues over the second half in the other thread of the token
-        uint4 raw[DH / 8];
+            for (int c8 = 0; c8 < D / 8; ++c8) raw[c8] = valid ? __ldg(p + c8) : make_uint4(0, 0, 0, 0);
+            float n2 = 0.0f;
 #pragma unroll
-        for (int c8 = 0; c8 < DH / 8; ++c8) raw[c8] = nraw[c8];
-        float n2 = 0.0f;
-        if (TPT == 1 || half == 0) {
-#pragma unroll
-            for (int c8 = 0; c8 < DH / 8; ++c8)
+            for (int c8 = 0; c8 < D / 8; ++c8)
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
                     const float f = elem_f32(raw[c8], e, a.dtype);
                     n2 = __fmaf_rn(f, f, n2);
                 }
-        }
-        float n;
-        if constexpr (TPT == 2) {
-            if (half == 0) s_n2[row] = n2;
-            __syncthreads();
-            if (half == 1) {
-                n2 = s_n2[row];
-#pragma unroll
-                for (int c8 = 0; c8 < DH / 8; ++c8)
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        const float f = elem_f32(raw[c8], e, a.dtype);
-                        n2 = __fmaf_rn(f, f, n2);
-                    }
-                s_nrm[row] = __fsqrt_rn(n2);
-            }
-            __syncthreads();
-            n = s_nrm[row];
-        } else {
-            n = __fsqrt_rn(n2);
-        }
-        const int ex = n > 0.0f ? ilogbf(n) : 0;
-        const float down = scalbnf(1.0f, -ex);
-#pragma unroll
-        for (int c8 = 0; c8 < DH / 8; ++c8) {
-            float f[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) f[e] = elem_f32(raw[c8], e, a.dtype) * down;
-            store8<D>(A0, nullptr, row, DH * half + 8 * c8, f);
-        }
-        tc::fence_proxy_async_smem();
-        tc::tc_fence_before();
-        __syncthreads();
-
-        // ---------------- GEMM 1: Y = X~ (16 R)^T in two fp16 parts
-        if (tid == 0) {
-            tc::tc_fence_after();
-#pragma unroll
-            for (int s = 0; s < D / 16; ++s) {
-                const uint64_t ad = tc::smem_desc(sbase + L::oA0 + 256 * s, L::kLbo, L::kSbo);
-                tc::mma_f16(tmem, ad, tc::smem_desc(sbase + L::oR + 256 * s, L::kLbo, L::kSbo), idesc, s > 0);
-                tc::mma_f16(tmem, ad, tc::smem_desc(sbase + L::oR + L::kTab / 2 + 256 * s, L::kLbo, L::kSbo),
-                            idesc, 1);
-            }
-            tc::mma_commit(bar_mma);
-        }
-        load_row(tile + gridDim.x);  // next tile's row, in flight during this tile
-        ok = tc::mbar_wait(bar_mma, phase);
-        if (__syncthreads_or(!ok)) {
-            failed = true;  // the commit of `phase` is still outstanding
-            break;
-        }
-        phase ^= 1;
-        tc::tc_fence_after();
-
-        // ---------------- epilogue 1: indices (and residual operands for prod),
-        // 32 columns at a time; their KB index words are stored directly
-        const float inv = n > 0.0f ? __fdiv_rn(scalbnf(1.0f, ex - 4), n) : 0.0f;
-
-        // destination of this token in the pool
-        char* sub = nullptr;
-        int slot = 0;
-        if (valid) {
-            const int pos = a.seq_lens[b] + t;
-            const int BT = a.pool.BT;
-            const int lb = pos / BT;
-            slot = pos - lb * BT;
-            if (pos < 0 || lb >= a.max_blocks) {
-                atomicOr(a.err, TQ_DEVERR_CAPACITY);
-            } else {
-                const int64_t pb = a.table ? static_cast<int64_t>(a.table[static_cast<int64_t>(b) * a.max_blocks + lb])
-                                           : static_cast<int64_t>(b) * a.max_blocks + lb;
-                if (pb < 0 || pb >= a.pool.num_blocks) atomicOr(a.err, TQ_DEVERR_BLOCK);
-                else sub = a.pool.base + (pb * Hkv + h) * a.pool.sub_bytes;
-            }
-        }
-        uint32_t* widx = sub ? reinterpret_cast<uint32_t*>(sub + o_idx) + static_cast<int64_t>(slot) * W : nullptr;
-
-        float g2 = 0.0f;
-#pragma unroll 1
-        for (int ch = 0; ch < CH; ++ch) {
-            float v[32];
-            tc::tmem_ld32(tmem_row + 32 * ch, v);
-            uint32_t cw[KB];
-#pragma unroll
-            for (int q = 0; q < KB; ++q) cw[q] = 0u;
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                const float y = v[i] * inv;
-                int code = 0;
-#pragma unroll
-                for (int j = 0; j < NM; ++j) code += y > mreg[j] ? 1 : 0;
-                const int bit = i * KB;
-                cw[bit >> 5] |= static_cast<uint32_t>(code) << (bit & 31);
-                if ((bit & 31) + KB > 32) cw[(bit >> 5) + 1] |= static_cast<uint32_t>(code) >> (32 - (bit & 31));
-                if constexpr (PROD) {
-                    const float r = __fsub_rn(y, s_c[code]);
-                    g2 = __fmaf_rn(r, r, g2);
-                    v[i] = r * 256.0f;
-                }
-            }
-            if (widx) store_words<KB>(widx + KB * (CH * half + ch), cw);
-            if constexpr (PROD) {
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    float f[8];
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) f[e] = v[8 * q + e];
-                    store8<D>(A0, A1, row, DH * half + 32 * ch + 8 * q, f);
-                }
-            }
-        }
-        if (sub && half == 0) reinterpret_cast<float*>(sub + o_norm)[slot] = n;
-
-        if constexpr (PROD) {
-            // ---------------- GEMM 2: Z = r~ S^T in three fp16 parts
-            if (TPT == 2 && half == 1) s_g2[row] = g2;
-            tc::fence_proxy_async_smem();
-            tc::tc_fence_before();
-            __syncthreads();
-            if (tid == 0) {
-                tc::tc_fence_after();
-#pragma unroll
-                for (int s = 0; s < D / 16; ++s) {
-                    const uint64_t ah = tc::smem_desc(sbase + L::oA0 + 256 * s, L::kLbo, L::kSbo);
-                    const uint64_t al = tc::smem_desc(sbase + L::oA1 + 256 * s, L::kLbo, L::kSbo);
-                    const uint64_t bh_ = tc::smem_desc(sbase + L::oS + 256 * s, L::kLbo, L::kSbo);
-                    const uint64_t bl = tc::smem_desc(sbase + L::oS + L::kTab / 2 + 256 * s, L::kLbo, L::kSbo);
-                    tc::mma_f16(tmem, ah, bh_, idesc, s > 0);
-                    tc::mma_f16(tmem, al, bh_, idesc, 1);
-                    tc::mma_f16(tmem, ah, bl, idesc, 1);
-                }
-                tc::mma_commit(bar_mma);
-            }
-            ok = tc::mbar_wait(bar_mma, phase);
-            if (__syncthreads_or(!ok)) {
+            const float n = __fsqrt_rn(n2);
+            const float down = scalbnf(1.0f, n > 0.0f ? -ilogbf(n) : 0);
+            // the operand tile and this stash slot are free once GEMM 1 of the
+            // previous tile has read the tile (which also means the epilogue of
+            // the tile three back, the slot's previous user, has finished)
+            if (!tc::mbar_wait(&bars[kBarAEmpty], (it & 1) ^ 1)) {
                 failed = true;
                 break;
             }
-            phase ^= 1;
-            tc::tc_fence_after();
-            uint32_t sw[CH];
+            s_norm[(it % 3) * kTileRows + row] = n;
 #pragma unroll
-            for (int ch = 0; ch < CH; ++ch) {
-                float v[32];
-                tc::tmem_ld32(tmem_row + 32 * ch, v);
-                uint32_t w = 0u;
+            for (int c8 = 0; c8 < D / 8; ++c8) {
+                float f[8];
 #pragma unroll
-                for (int i = 0; i < 32; ++i) w |= (v[i] >= 0.0f ? 1u : 0u) << i;
-                sw[ch] = w;
+                for (int e = 0; e < 8; ++e) f[e] = elem_f32(raw[c8], e, a.dtype) * down;
+                store8<D>(smem + L::oA, nullptr, row, 8 * c8, f);
             }
-            if (sub) {
-                store_words<CH>(reinterpret_cast<uint32_t*>(sub + a.pool.off[1]) + static_cast<int64_t>(slot) * WS + CH * half,
-                                sw);
-                if (half == 0)
-                    reinterpret_cast<float*>(sub + a.pool.off[3])[slot] = __fsqrt_rn(TPT == 2 ? g2 + s_g2[row] : g2);
+            tc::fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                tc::mbar_arrive(&bars[kBarAFull]);
+                tc::mbar_arrive(&bars[kBarNorm + it % 3]);
             }
         }
-        // TMEM reads of this tile are complete before the next tile's MMAs
-        tc::tc_fence_before();
+    } else if (warp == kMmaWarp) {
+        // ---------------- MMAs: GEMM 1 of tile it + 1 before GEMM 2 of tile it
+        if (lane == 0 && !failed) {
+            constexpr uint32_t idesc = tc::idesc_f16_f32(kTileRows, D);
+            auto lo_of = [&](int off) { return static_cast<uint32_t>(tc::smem_desc(sbase + off, L::kLbo, 0) & 0xFFFFFFFFu); };
+            const uint32_t hi = static_cast<uint32_t>(tc::smem_desc(0, 0, L::kSbo) >> 32);
+            const uint64_t hi64 = static_cast<uint64_t>(hi) << 32;
+            const uint32_t la = lo_of(L::oA), lrh = lo_of(L::oR), lrl = lo_of(L::oR + L::kTab / 2);
+            bool ok = true;
+            int g1 = 0, g2n = 0;
+            auto gemm1 = [&](int it) {
+                const int bb = it & 1;
+                ok = tc::mbar_wait(&bars[kBarAFull], it & 1) &&
+                     tc::mbar_wait(&bars[kBarYEmpty + bb], ((it >> 1) & 1) ^ 1);
+                if (!ok) return;
+                tc::tc_fence_after();
+                const uint32_t d = tmem + bb * D;
+#pragma unroll
+                for (int s = 0; s < D / 16; ++s) {
+                    tc::mma_f16(d, hi64 | (la + 16 * s), hi64 | (lrh + 16 * s), idesc, s > 0);
+                    tc::mma_f16(d, hi64 | (la + 16 * s), hi64 | (lrl + 16 * s), idesc, 1);
+                }
+                tc::mma_commit(&bars[kBarYFull + bb]);
+                tc::mma_commit(&bars[kBarAEmpty]);
+                ++g1;
+            };
+            if (n_it > 0) gemm1(0);
+            for (int it = 0; it < n_it && ok; ++it) {
+                if (it + 1 < n_it) gemm1(it + 1);
+                if (!ok) break;
+                if constexpr (PROD) {
+                    ok = tc::mbar_wait(&bars[kBarRFull], it & 1) && tc::mbar_wait(&bars[kBarZEmpty], (it & 1) ^ 1);
+                    if (!ok) break;
+                    tc::tc_fence_after();
+                    const uint32_t d = tmem + 2 * D;
+                    const uint32_t lh = lo_of(L::oRh), ll = lo_of(L::oRl);
+                    const uint32_t lsh = lo_of(L::oS), lsl = lo_of(L::oS + L::kTab / 2);
+#pragma unroll
+                    for (int s = 0; s < D / 16; ++s) {
+                        tc::mma_f16(d, hi64 | (lh + 16 * s), hi64 | (lsh + 16 * s), idesc, s > 0);
+                        tc::mma_f16(d, hi64 | (ll + 16 * s), hi64 | (lsh + 16 * s), idesc, 1);
+                        tc::mma_f16(d, hi64 | (lh + 16 * s), hi64 | (lsl + 16 * s), idesc, 1);
+                    }
+                    tc::mma_commit(&bars[kBarZFull]);
+                    tc::mma_commit(&bars[kBarREmpty]);
+                    ++g2n;
+                }
+            }
+            if (!ok) {
+                failed = true;
+                atomicOr(a.err, TQ_DEVERR_TIMEOUT);
+            }
+            // drain (after a timeout elsewhere): the last commits of each kind
+            if (g1) (void)tc::mbar_wait(&bars[kBarAEmpty], (g1 - 1) & 1);
+            if (g2n) (void)tc::mbar_wait(&bars[kBarREmpty], (g2n - 1) & 1);
+        }
+        __syncwarp();
+    } else {
+        // ---------------- epilogue: two threads per token (column halves)
+        const int ew = warp - kProdWarps;
+        const int lq = warp & 3, half = ew >> 2;
+        const int row = 32 * lq + lane;
+        const uint32_t t_lane = tmem + (static_cast<uint32_t>(32 * lq) << 16) + DH * half;
+        float mreg[NM];
+#pragma unroll
+        for (int j = 0; j < NM; ++j) mreg[j] = s_m[j];
+        float creg[4] = {s_c[0], s_c[1], s_c[2], s_c[3]};   // 2-bit codebooks: levels from registers
+        const int64_t o_idx = is_v ? a.pool.off[4] : a.pool.off[0];
+        const int64_t o_norm = is_v ? a.pool.off[5] : a.pool.off[2];
+        for (int it = 0; it < n_it && !failed; ++it) {
+            const int64_t tile = tile_of(it);
+            const int bb = it & 1;
+            const int ts = static_cast<int>(tile % tiles_per_seq);
+            const int bh = static_cast<int>(tile / tiles_per_seq);
+            const int h = bh % Hkv, b = bh / Hkv;
+            const int t = ts * kTileRows + row;
+            const bool valid = t < a.n_new;
+            bool ok = tc::mbar_wait(&bars[kBarYFull + bb], (it >> 1) & 1) &&
+                      tc::mbar_wait(&bars[kBarNorm + it % 3], (it / 3) & 1);
+            tc::tc_fence_after();
+            const float n = s_norm[(it % 3) * kTileRows + row];
+            const int ex = n > 0.0f ? ilogbf(n) : 0;
+            const float inv = n > 0.0f ? __fdiv_rn(scalbnf(1.0f, ex - 4), n) : 0.0f;
+
+            // destination of this token in the pool
+            char* sub = nullptr;
+            int slot = 0;
+            if (valid) {
+                const int pos = a.seq_lens[b] + t;
+                const int BT = a.pool.BT;
+                const int lb = pos / BT;
+                slot = pos - lb * BT;
+                if (pos < 0 || lb >= a.max_blocks) {
+                    atomicOr(a.err, TQ_DEVERR_CAPACITY);
+                } else {
+                    const int64_t pb = a.table ? static_cast<int64_t>(a.table[static_cast<int64_t>(b) * a.max_blocks + lb])
+                                               : static_cast<int64_t>(b) * a.max_blocks + lb;
+                    if (pb < 0 || pb >= a.pool.num_blocks) atomicOr(a.err, TQ_DEVERR_BLOCK);
+                    else sub = a.pool.base + (pb * Hkv + h) * a.pool.sub_bytes;
+                }
+            }
+            uint32_t* widx = sub ? reinterpret_cast<uint32_t*>(sub + o_idx) + static_cast<int64_t>(slot) * W : nullptr;
+            if constexpr (PROD) ok = ok && tc::mbar_wait(&bars[kBarREmpty], (it & 1) ^ 1);   // residual tiles free
+
+            // ---------------- epilogue 1: indices (and residual operands for prod)
+            float g2p[4] = {0.0f, 0.0f, 0.0f, 0.0f};   // residual sum of squares, four partial chains
+#pragma unroll 1
+            for (int ch = 0; ch < CH; ++ch) {
+                float v[32];
+                tc::tmem_ld32(t_lane + bb * D + 32 * ch, v);
+                uint32_t cw[KB];
+#pragma unroll
+                for (int q = 0; q < KB; ++q) cw[q] = 0u;
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const float y = v[i] * inv;
+                    const int code = lm_index<KB>(y, mreg);
+                    const int bit = i * KB;
+                    cw[bit >> 5] |= static_cast<uint32_t>(code) << (bit & 31);
+                    if ((bit & 31) + KB > 32) cw[(bit >> 5) + 1] |= static_cast<uint32_t>(code) >> (32 - (bit & 31));
+                    if constexpr (PROD) {
+                        float cc;
+                        if constexpr (KB <= 2) cc = (code & 2) ? ((code & 1) ? creg[3] : creg[2]) : ((code & 1) ? creg[1] : creg[0]);
+                        else cc = s_c[code];
+                        const float r = __fsub_rn(y, cc);
+                        g2p[i & 3] = __fmaf_rn(r, r, g2p[i & 3]);
+                        v[i] = r * 256.0f;
+                    }
+                }
+                if (widx) store_words<KB>(widx + KB * (CH * half + ch), cw);
+                if constexpr (PROD) {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        float f[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) f[e] = v[8 * q + e];
+                        store8<D>(smem + L::oRh, smem + L::oRl, row, DH * half + 32 * ch + 8 * q, f);
+                    }
+                }
+            }
+            // the accumulator may take the tile after next
+            tc::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&bars[kBarYEmpty + bb]);
+            if (sub && half == 0) reinterpret_cast<float*>(sub + o_norm)[slot] = n;
+
+            const float g2 = (g2p[0] + g2p[1]) + (g2p[2] + g2p[3]);
+            if constexpr (PROD) {
+                tc::fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(&bars[kBarRFull]);
+                if (half == 1) s_g2[bb * kTileRows + row] = g2;
+                // ---------------- epilogue 2: signs and the residual norm
+                ok = ok && tc::mbar_wait(&bars[kBarZFull], it & 1);
+                tc::tc_fence_after();
+                uint32_t sw[CH];
+#pragma unroll
+                for (int ch = 0; ch < CH; ++ch) {
+                    float v[32];
+                    tc::tmem_ld32(t_lane + 2 * D + 32 * ch, v);
+                    uint32_t w = 0u;
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) w |= (v[i] >= 0.0f ? 1u : 0u) << i;
+                    sw[ch] = w;
+                }
+                tc::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(&bars[kBarZEmpty]);
+                // the other half's residual sum (a uniform failure exit first)
+                if (tc::bar_or(kEpiBar, 32 * kEpiWarps, !ok)) {
+                    failed = true;
+                    break;
+                }
+                if (sub) {
+                    store_words<CH>(reinterpret_cast<uint32_t*>(sub + a.pool.off[1]) + static_cast<int64_t>(slot) * WS + CH * half,
+                                    sw);
+                    if (half == 0)
+                        reinterpret_cast<float*>(sub + a.pool.off[3])[slot] = __fsqrt_rn(g2 + s_g2[bb * kTileRows + row]);
+                }
+            } else {
+                if (tc::bar_or(kEpiBar, 32 * kEpiWarps, !ok)) {
+                    failed = true;
+                    break;
+                }
+            }
+        }
     }
 
-    if (failed) {
-        if (tid == 0) atomicOr(a.err, TQ_DEVERR_TIMEOUT);
-        // let the table copies and an MMA group already committed finish
-        // (bounded) before the shared and tensor memory go away
-        (void)tc::mbar_wait(bar_tab, 0);
-        if (!tables_failed) (void)tc::mbar_wait(bar_mma, phase);
-    }
+    if (__syncthreads_or(failed) && tid == 0) atomicOr(a.err, TQ_DEVERR_TIMEOUT);
+    tc::tc_fence_before();
     __syncthreads();
     if (warp == 0) {
         tc::tc_fence_after();
-        tc::tmem_dealloc(tmem, D);
+        tc::tmem_dealloc(tmem, L::kCols);
     }
-    if (tid == 0) {
-        tc::mbar_inval(bar_tab);
-        tc::mbar_inval(bar_mma);
-    }
+    if (tid == 0)
+        for (int i = 0; i < kNumBars; ++i) tc::mbar_inval(&bars[i]);
 }
 
 int sm_count() {
@@ -415,12 +493,10 @@ cudaError_t launch_tc(const EncodeAppendArgs& a, int is_v, cudaStream_t s) {
     }
     const int tiles_per_seq = (a.n_new + kTileRows - 1) / kTileRows;
     const int64_t ntiles = static_cast<int64_t>(a.batch) * a.pool.Hkv * tiles_per_seq;
-    const int per_sm = PROD ? 1 : 2;
-    int64_t grid = static_cast<int64_t>(sm_count()) * per_sm;
+    int64_t grid = static_cast<int64_t>(sm_count());
     if (grid <= 0) return cudaErrorInvalidDevice;
     if (grid > ntiles) grid = ntiles;
-    encode_tc_kernel<D, KB, PROD><<<static_cast<unsigned>(grid), Split<PROD>::kThreads, L::kBytes, s>>>(a, is_v,
-                                                                                                   tiles_per_seq);
+    encode_tc_kernel<D, KB, PROD><<<static_cast<unsigned>(grid), kEncThreads, L::kBytes, s>>>(a, is_v, tiles_per_seq);
     g_launches.fetch_add(1, std::memory_order_relaxed);
     return cudaGetLastError();
 }
