@@ -109,19 +109,17 @@ __device__ __forceinline__ void q_gemm(QSmem& sm, const uint16_t (*T)[kD * kD], 
 
 template <int KB>
 __global__ void __launch_bounds__(kQThreads) qfrag_kernel(MmaArgs m) {
-    // one CTA per (sequence x kv head, row group): q' = Q R^T and q'' = q' S^T
-    // for the 16 rows on the tensor cores, both operands split into fp16
-    // hi + lo (about 22 significant bits), tables staged by one bulk copy
+    // persistent CTAs over the units (sequence x kv head, row group): the
+    // tables are staged once per CTA by one bulk copy; per unit q' = Q R^T and
+    // q'' = q' S^T for the 16 rows on the tensor cores, both operands split
+    // into fp16 hi + lo (about 22 significant bits)
     extern __shared__ __align__(16) unsigned char qsm_raw[];
     QSmem& sm = *reinterpret_cast<QSmem*>(qsm_raw);
     const DecodeArgs& a = m.a;
     const bool prod = a.kc.mode == TQ_MODE_PROD;
     const int Hkv = a.pool.Hkv;
-    const int bh = blockIdx.x;
-    const int b = bh / Hkv, h = bh % Hkv;
-    const int rg = blockIdx.y;
     const int RG = a.plan.row_groups;
-    const int unit = bh * RG + rg;
+    const int units = a.batch * Hkv * RG;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
     if (tid == 0) {
@@ -131,75 +129,98 @@ __global__ void __launch_bounds__(kQThreads) qfrag_kernel(MmaArgs m) {
         bulk_g2s(sm.R, a.kc.Rtc, 2 * kD * kD * 2, &sm.bar);
         if (prod) bulk_g2s(sm.S, a.kc.Stc, 2 * kD * kD * 2, &sm.bar);
     }
-    // query rows (fp32) into q2 as scratch, and each row's scale exponent
-    for (int e = tid; e < kRows * kD; e += kQThreads) {
-        const int rr = e / kD, k = e % kD;
-        const int r = rg * kRows + rr;
-        float v = 0.0f;
-        if (r < a.plan.rows) {
-            const int gq = r / a.Lq, l = r % a.Lq;
-            const int64_t src = ((static_cast<int64_t>(b) * a.Hq + h * a.G + gq) * a.Lq + l) * kD + k;
-            if (a.q_dtype == TQ_F32) v = static_cast<const float*>(a.q)[src];
-            else if (a.q_dtype == TQ_BF16) v = __bfloat162float(static_cast<const __nv_bfloat16*>(a.q)[src]);
-            else v = __half2float(static_cast<const __half*>(a.q)[src]);
+    bool first = true;
+    for (int unit = blockIdx.x; unit < units; unit += gridDim.x) {
+        const int bh = unit / RG, rg = unit % RG;
+        const int b = bh / Hkv, h = bh % Hkv;
+        // query rows (fp32) into q2 as scratch, and each row's scale exponent
+        for (int e = tid; e < kRows * kD; e += kQThreads) {
+            const int rr = e / kD, k = e % kD;
+            const int r = rg * kRows + rr;
+            float v = 0.0f;
+            if (r < a.plan.rows) {
+                const int gq = r / a.Lq, l = r % a.Lq;
+                const int64_t src = ((static_cast<int64_t>(b) * a.Hq + h * a.G + gq) * a.Lq + l) * kD + k;
+                if (a.q_dtype == TQ_F32) v = static_cast<const float*>(a.q)[src];
+                else if (a.q_dtype == TQ_BF16) v = __bfloat162float(static_cast<const __nv_bfloat16*>(a.q)[src]);
+                else v = __half2float(static_cast<const __half*>(a.q)[src]);
+            }
+            sm.q2[rr][k] = v;
         }
-        sm.q2[rr][k] = v;
+        __syncthreads();
+        if (tid < kRows) {
+            float mx = 0.0f;
+            for (int k = 0; k < kD; ++k) mx = fmaxf(mx, fabsf(sm.q2[tid][k]));
+            sm.ex[tid] = mx > 0.0f ? static_cast<float>(ilogbf(mx)) : 0.0f;  // |q| * 2^-ex < 2
+        }
+        __syncthreads();
+        q_split_rows(sm, &sm.q2[0][0], tid);
+        if (first) {
+            first = false;
+            const bool ok = mbar_wait(&sm.bar, 0);
+            // the workspace is written below: the kernels before this one are done
+            // (the append before it waits for the decode before that); the split
+            // kernel may then start fetching records, which are all written by now
+            tc::grid_wait_prior();
+            tc::grid_release_dependents();
+            if (__syncthreads_or(!ok)) {
+                if (tid == 0) atomicOr(a.err, TQ_DEVERR_TIMEOUT);
+                (void)mbar_wait(&sm.bar, 0);
+                return;
+            }
+        }
+        q_gemm(sm, sm.R, 16.0f, &sm.q1[0][0], warp, lane);  // the table holds 16 R
+        __syncthreads();
+        if (prod) {
+            // |q'| <= |q|_2 <= sqrt(128) * 2^(ex+1): scale q' by 2^-(ex+4)
+            if (tid < kRows) sm.ex[tid] += 4.0f;
+            __syncthreads();
+            q_split_rows(sm, &sm.q1[0][0], tid);
+            __syncthreads();
+            q_gemm(sm, sm.S, 1.0f, &sm.q2[0][0], warp, lane);
+            __syncthreads();
+        }
+        // entry (row rr, which, ks, j, e): lane 4*(rr%8)+j, register 2e + (rr >= 8)
+        const float s1 = a.scale * kLog2e;
+        const float s2 = s1 * kSqrtHalfPi / static_cast<float>(kD);
+        uint32_t* dst = reinterpret_cast<uint32_t*>(const_cast<uint4*>(m.qfrag)) + static_cast<int64_t>(unit) * 2 * 8 * 32 * 4;
+        for (int e = tid; e < kRows * 128; e += kQThreads) {
+            const int rr = e >> 7, x = e & 127;
+            const int which = x >> 6, ks = (x >> 3) & 7, j = (x >> 1) & 3, ee = x & 1;
+            const int ln = 4 * (rr & 7) + j;
+            const int reg = 2 * ee + (rr >= 8 ? 1 : 0);
+            int pa, pb;
+            const bool qjl = which && prod;
+            mse_pair(qjl ? 1 : KB, 2 * ks + ee, pa, pb);
+            const float* q = qjl ? sm.q2[rr] : sm.q1[rr];
+            const float sc = qjl ? s2 : s1;
+            float va = q[32 * j + pa] * sc, vb = q[32 * j + pb] * sc;
+            if (which && !qjl) {
+                va -= __half2float(__float2half_rn(va));
+                vb -= __half2float(__float2half_rn(vb));
+            }
+            dst[((which * 8 + ks) * 32 + ln) * 4 + reg] = pack_half2(va, vb);
+        }
+        if (tid == 0 && m.cnt) m.cnt[unit] = 0u;
+        __syncthreads();   // q1 / q2 / A are rewritten by the next unit
     }
-    __syncthreads();
-    if (tid < kRows) {
-        float mx = 0.0f;
-        for (int k = 0; k < kD; ++k) mx = fmaxf(mx, fabsf(sm.q2[tid][k]));
-        sm.ex[tid] = mx > 0.0f ? static_cast<float>(ilogbf(mx)) : 0.0f;  // |q| * 2^-ex < 2
-    }
-    __syncthreads();
-    q_split_rows(sm, &sm.q2[0][0], tid);
-    const bool ok = mbar_wait(&sm.bar, 0);
-    // the workspace is written below: the kernels before this one are done
-    // (the append before it waits for the decode before that); the split
-    // kernel may then start fetching records, which are all written by now
-    tc::grid_wait_prior();
-    tc::grid_release_dependents();
-    if (__syncthreads_or(!ok)) {
-        if (tid == 0) atomicOr(a.err, TQ_DEVERR_TIMEOUT);
+    if (first && tid == 0) {   // no unit for this CTA: release the tables' copy
         (void)mbar_wait(&sm.bar, 0);
-        return;
     }
-    q_gemm(sm, sm.R, 16.0f, &sm.q1[0][0], warp, lane);  // the table holds 16 R
-    __syncthreads();
-    if (prod) {
-        // |q'| <= |q|_2 <= sqrt(128) * 2^(ex+1): scale q' by 2^-(ex+4)
-        if (tid < kRows) sm.ex[tid] += 4.0f;
-        __syncthreads();
-        q_split_rows(sm, &sm.q1[0][0], tid);
-        __syncthreads();
-        q_gemm(sm, sm.S, 1.0f, &sm.q2[0][0], warp, lane);
-        __syncthreads();
+    if (tid == 0) mbar_inval(&sm.bar);
+}
+
+// CTAs of the query-prep kernel: one per unit up to one per SM.
+inline int qfrag_grid(int units) {
+    static std::atomic<int> sms[64];
+    int dev = 0;
+    cudaGetDevice(&dev);
+    int n = sms[dev & 63].load();
+    if (n == 0) {
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 1;
+        sms[dev & 63].store(n);
     }
-    // entry (row rr, which, ks, j, e): lane 4*(rr%8)+j, register 2e + (rr >= 8)
-    const float s1 = a.scale * kLog2e;
-    const float s2 = s1 * kSqrtHalfPi / static_cast<float>(kD);
-    uint32_t* dst = reinterpret_cast<uint32_t*>(const_cast<uint4*>(m.qfrag)) + static_cast<int64_t>(unit) * 2 * 8 * 32 * 4;
-    for (int e = tid; e < kRows * 128; e += kQThreads) {
-        const int rr = e >> 7, x = e & 127;
-        const int which = x >> 6, ks = (x >> 3) & 7, j = (x >> 1) & 3, ee = x & 1;
-        const int ln = 4 * (rr & 7) + j;
-        const int reg = 2 * ee + (rr >= 8 ? 1 : 0);
-        int pa, pb;
-        const bool qjl = which && prod;
-        mse_pair(qjl ? 1 : KB, 2 * ks + ee, pa, pb);
-        const float* q = qjl ? sm.q2[rr] : sm.q1[rr];
-        const float sc = qjl ? s2 : s1;
-        float va = q[32 * j + pa] * sc, vb = q[32 * j + pb] * sc;
-        if (which && !qjl) {
-            va -= __half2float(__float2half_rn(va));
-            vb -= __half2float(__float2half_rn(vb));
-        }
-        dst[((which * 8 + ks) * 32 + ln) * 4 + reg] = pack_half2(va, vb);
-    }
-    if (tid == 0) {
-        if (m.cnt) m.cnt[unit] = 0u;
-        mbar_inval(&sm.bar);
-    }
+    return units < n ? units : n;
 }
 
 // ------------------------------------------------------------------ split kernel
@@ -693,8 +714,8 @@ cudaError_t launch_mma(const MmaArgs& m, size_t smem, cudaStream_t s) {
         qattr_set.fetch_or(bit);
     }
     const int RG = a.plan.row_groups;
-    cudaError_t e = launch_overlapped(qfrag_kernel<KB>, dim3(a.batch * a.pool.Hkv, RG), dim3(kQThreads), sizeof(QSmem),
-                                      s, m);
+    cudaError_t e = launch_overlapped(qfrag_kernel<KB>, dim3(qfrag_grid(a.batch * a.pool.Hkv * RG)), dim3(kQThreads),
+                                      sizeof(QSmem), s, m);
     g_launches.fetch_add(1, std::memory_order_relaxed);
     if (e != cudaSuccess) return e;
     e = launch_overlapped(split_mma_kernel<KB, KPROD, VGROUP, VB>, dim3(a.plan.splits, a.pool.Hkv * RG, a.batch),

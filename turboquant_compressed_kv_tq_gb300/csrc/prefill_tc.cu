@@ -643,7 +643,7 @@ cudaError_t launch_prefill_tc_t(const TcPrefillArgs& P, size_t smem, cudaStream_
     m.a = a;
     m.qfrag = P.qfrag;
     m.cnt = nullptr;
-    qfrag_kernel<KB><<<dim3(a.batch * a.pool.Hkv, RG), kQThreads, sizeof(QSmem), s>>>(m);
+    qfrag_kernel<KB><<<dim3(qfrag_grid(a.batch * a.pool.Hkv * RG)), kQThreads, sizeof(QSmem), s>>>(m);
     g_launches.fetch_add(1, std::memory_order_relaxed);
     const int gx = (RG + 7) / 8;
     prefill_tc_kernel<KB, KPROD, VGROUP, VB><<<dim3(gx, a.pool.Hkv, a.batch), kTThreads, smem, s>>>(P);
