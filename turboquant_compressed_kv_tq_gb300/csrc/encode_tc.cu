@@ -179,6 +179,10 @@ __global__ void __launch_bounds__(kEncThreads, 1)
     const CodecDev& cd = is_v ? a.vc : a.kc;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t sbase = tc::smem_addr(smem);
+    // the next kernel (the other tensor's encode, the next chunk's) shares no
+    // data with this one: it may take SMs as they free up at this launch's
+    // tail; this kernel completes only after its predecessor (wait at exit)
+    tc::grid_release_dependents();
 
     if (warp == 0) {
         tc::tmem_alloc(s_tmem, L::kCols);
@@ -461,6 +465,7 @@ __global__ void __launch_bounds__(kEncThreads, 1)
     }
     if (tid == 0)
         for (int i = 0; i < kNumBars; ++i) tc::mbar_inval(&bars[i]);
+    tc::grid_wait_prior();
 }
 
 int sm_count() {
@@ -496,9 +501,10 @@ cudaError_t launch_tc(const EncodeAppendArgs& a, int is_v, cudaStream_t s) {
     int64_t grid = static_cast<int64_t>(sm_count());
     if (grid <= 0) return cudaErrorInvalidDevice;
     if (grid > ntiles) grid = ntiles;
-    encode_tc_kernel<D, KB, PROD><<<static_cast<unsigned>(grid), kEncThreads, L::kBytes, s>>>(a, is_v, tiles_per_seq);
+    const cudaError_t e = launch_overlapped(encode_tc_kernel<D, KB, PROD>, dim3(static_cast<unsigned>(grid)),
+                                            dim3(kEncThreads), L::kBytes, s, a, is_v, tiles_per_seq);
     g_launches.fetch_add(1, std::memory_order_relaxed);
-    return cudaGetLastError();
+    return e;
 }
 
 template <int D>
