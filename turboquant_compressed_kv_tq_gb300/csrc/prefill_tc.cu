@@ -103,7 +103,10 @@ __global__ void __launch_bounds__(kTThreads, 1) prefill_tc_kernel(TcPrefillArgs 
     // a compute thread's row (its warp's TMEM lane quarter) and column quarter
     const int row = 32 * (warp & 3) + lane, cq = (warp >> 2) & 3;
     const int w8 = row >> 4;                        // row group slot of the CTA
-    const int rg = blockIdx.x + w8 * gridDim.x;
+    // row blocks in reverse launch order: the later query positions see more
+    // keys, so the longest CTAs start first and the last wave holds short ones
+    const int bx = gridDim.x - 1 - blockIdx.x;
+    const int rg = bx + w8 * gridDim.x;
     const int r = rg * kRows + (row & 15);
     const bool compute = warp < kCtlWarp;
     const bool row_ok = compute && rg < RG && r < a.plan.rows;
@@ -152,7 +155,7 @@ __global__ void __launch_bounds__(kTThreads, 1) prefill_tc_kernel(TcPrefillArgs 
     // the query operands of this thread's row into TMEM: coordinate quarter cq
     // (pairs p of the query fragments, column 16 cq + p) of Q' and of Q''
     if (compute) {
-        const int rgs = blockIdx.x + w8 * gridDim.x;
+        const int rgs = bx + w8 * gridDim.x;
         const uint32_t* qf = reinterpret_cast<const uint32_t*>(P.qfrag) +
                              static_cast<int64_t>((b * Hkv + h) * RG + rgs) * 2048;
         const int ln = 4 * (row & 7) + cq, rbit = (row >> 3) & 1;
