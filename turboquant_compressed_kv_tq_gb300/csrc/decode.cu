@@ -402,7 +402,12 @@ DecodePlan make_decode_plan(const tq_cache_desc* d, int batch, int G, int Lq, in
         p.st_bytes = (o + 127) / 128 * 128;
         const size_t ring = static_cast<size_t>(mmadec::kWarps) * mmadec::kStages * p.st_bytes;
         p.qs_off = static_cast<int>(ring);
-        const size_t ringq = ring + mmadec::kQFragBytes;
+        size_t ringq = ring + mmadec::kQFragBytes;
+        p.vt_off = -1;
+        if (!p.vgroup && p.vb == 3) {  // pair table of 3-bit value codes (aligned inside the region)
+            p.vt_off = static_cast<int>(ringq);
+            ringq += mmadec::kVPairRegion;
+        }
         const size_t combine = sizeof(float) * (2 * mmadec::kWarps * kRows + mmadec::kWarps * kRows * (D + 1));
         const size_t body = ((ringq > combine ? ringq : combine) + 127) / 128 * 128;
         p.bar_off = static_cast<int>(body);
@@ -431,6 +436,7 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s) {
         m.st.bytes = a.plan.st_bytes;
         m.st.bar_off = a.plan.bar_off;
         m.st.qs_off = a.plan.qs_off;
+        m.st.vt_off = a.plan.vt_off;
         for (int k = 0; k < 7; ++k) {
             m.st.off[k] = a.plan.st_off[k];
             m.st.field[k] = a.plan.st_field[k];

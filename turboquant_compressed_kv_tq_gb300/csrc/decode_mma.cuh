@@ -40,6 +40,10 @@ constexpr int kRows = 16;
 constexpr int kMaxTile = 64;
 constexpr int kQFragBytes = 2 * 8 * 32 * 16;  // query fragments of one unit
 constexpr unsigned kSpinLimit = 1u << 22;
+// Pair table of 3-bit value codes: 64 entries x 32 bank copies x 4 bytes,
+// placed at an 8 KB-aligned shared address inside a 16 KB region.
+constexpr int kVPairBytes = 64 * 32 * 4;
+constexpr int kVPairRegion = 2 * kVPairBytes;
 
 // ------------------------------------------------------------------ PTX helpers
 
@@ -137,6 +141,36 @@ __device__ __forceinline__ void bulk_g2s_once(void* dst, const void* src, unsign
         : "memory");
 }
 
+// ------------------------------------------------------------------ integer work on the FMA pipe
+//
+// The decoders are bound by the ALU pipe (logic, shifts, byte permutes, integer
+// adds). Left shifts and the shift-and-add steps of the bit spreading are
+// written as integer multiply-adds instead, which issue to the FMA pipe:
+// x << k is x * 2^k, and moving a masked field m of v up by k bits is
+// v + (2^k - 1) m. The multipliers sit in constant memory so that the compiler
+// keeps them as multiplies rather than folding them back into shifts and adds.
+// (Right shifts stay shifts: as the high word of a product they take two
+// issue cycles of the FMA pipe, measured slower than the shift.)
+struct DecConst {
+    uint32_t pow2[32];  // 2^k
+    uint32_t m3, m15, m11, m10001;
+};
+static __constant__ DecConst kDc = {
+    {1u << 0,  1u << 1,  1u << 2,  1u << 3,  1u << 4,  1u << 5,  1u << 6,  1u << 7,
+     1u << 8,  1u << 9,  1u << 10, 1u << 11, 1u << 12, 1u << 13, 1u << 14, 1u << 15,
+     1u << 16, 1u << 17, 1u << 18, 1u << 19, 1u << 20, 1u << 21, 1u << 22, 1u << 23,
+     1u << 24, 1u << 25, 1u << 26, 1u << 27, 1u << 28, 1u << 29, 1u << 30, 1u << 31},
+    3u, 15u, 0x11u, 0x10001u};
+
+__device__ __forceinline__ uint32_t mad_lo(uint32_t a, uint32_t b, uint32_t c) {
+    uint32_t d;
+    asm("mad.lo.u32 %0, %1, %2, %3;\n" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
+// x << k (k a compile-time constant after unrolling, 0..31).
+__device__ __forceinline__ uint32_t shl_f(uint32_t x, int k) { return k == 0 ? x : mad_lo(x, kDc.pow2[k], 0u); }
+
 // ------------------------------------------------------------------ codebooks in registers
 
 // Byte tables for __byte_perm lookups: for a 4-entry fp16 table T,
@@ -185,9 +219,10 @@ __device__ inline Tab8 make_tab8(const float* c) {
 
 // 2-bit codes, 16 per word: the codes s, s+4, s+8, s+12 of a word sit in the
 // bytes of (w >> 2s) & 0x03030303.
+// Selector nibbles (c, c + 4) per byte: x * 0x11 + 0x40404040.
 __device__ __forceinline__ void dec2_pair(uint32_t w, int s, const Tab4& t, uint32_t& h0, uint32_t& h1) {
     const uint32_t x = (w >> (2 * s)) & 0x03030303u;
-    const uint32_t sel = x * 0x11u + 0x40404040u;
+    const uint32_t sel = mad_lo(x, kDc.m11, 0x40404040u);
     h0 = prmt(t.lo, t.hi, sel);          // codes s, s+4
     h1 = prmt(t.lo, t.hi, sel >> 16);    // codes s+8, s+12
 }
@@ -196,9 +231,9 @@ __device__ __forceinline__ void dec2_pair(uint32_t w, int s, const Tab4& t, uint
 // value = +mu[k-8] for k >= 8 and -mu[7-k] below. Produces pairs (0,1),(2,3),
 // (4,5),(6,7).
 __device__ __forceinline__ void dec4_word(uint32_t w, const Tab8& mu, uint32_t (&h)[4]) {
-    const uint32_t f = (~(w >> 3)) & 0x11111111u;         // 1 where the code is negative
+    const uint32_t f = (~(w >> 3)) & 0x11111111u;     // 1 where the code is negative
     const uint32_t u = (w ^ (f * 7u)) & 0x77777777u;      // magnitude index per nibble
-    const uint32_t ws = w << 4;
+    const uint32_t ws = shl_f(w, 4);
     {
         const uint32_t lo4 = prmt(mu.lo0, mu.lo1, u);
         uint32_t hi4 = prmt(mu.hi0, mu.hi1, u);
@@ -208,7 +243,7 @@ __device__ __forceinline__ void dec4_word(uint32_t w, const Tab8& mu, uint32_t (
         h[1] = prmt(lo4, hi4, 0x7362);
     }
     {
-        const uint32_t u2 = u >> 16;
+        const uint32_t u2 = (u >> 16);
         const uint32_t lo4 = prmt(mu.lo0, mu.lo1, u2);
         uint32_t hi4 = prmt(mu.hi0, mu.hi1, u2);
         const uint32_t s4 = prmt(ws, w, 0xFBEA);   // codes 4..7
@@ -218,11 +253,12 @@ __device__ __forceinline__ void dec4_word(uint32_t w, const Tab8& mu, uint32_t (
     }
 }
 
-// 3-bit: 8 codes (24 bits) spread into nibbles, then an 8-entry lookup.
+// 3-bit: 8 codes (v < 2^24) spread into nibbles, then an 8-entry lookup.
+// Each spread step moves a masked field up by k bits as v + (2^k - 1)(v & m).
 __device__ __forceinline__ void dec3_group(uint32_t v, const Tab8& t, uint32_t (&h)[4]) {
-    uint32_t x = (v & 0x00000FFFu) | ((v << 4) & 0x0FFF0000u);
-    x = (x & 0x003F003Fu) | ((x << 2) & 0x3F003F00u);
-    x = (x & 0x07070707u) | ((x << 1) & 0x70707070u);
+    uint32_t x = mad_lo(v & 0x00FFF000u, kDc.m15, v);     // codes 4..7 up by 4
+    x = mad_lo(x & 0x0FC00FC0u, kDc.m3, x);                // codes 2, 3, 6, 7 up by 2
+    x = mad_lo(x & 0x38383838u, kDc.pow2[0], x);           // odd codes up by 1
     {
         const uint32_t lo4 = prmt(t.lo0, t.lo1, x);
         const uint32_t hi4 = prmt(t.hi0, t.hi1, x);
@@ -230,7 +266,7 @@ __device__ __forceinline__ void dec3_group(uint32_t v, const Tab8& t, uint32_t (
         h[1] = prmt(lo4, hi4, 0x7362);
     }
     {
-        const uint32_t x2 = x >> 16;
+        const uint32_t x2 = (x >> 16);
         const uint32_t lo4 = prmt(t.lo0, t.lo1, x2);
         const uint32_t hi4 = prmt(t.hi0, t.hi1, x2);
         h[2] = prmt(lo4, hi4, 0x5140);
@@ -241,8 +277,11 @@ __device__ __forceinline__ void dec3_group(uint32_t v, const Tab8& t, uint32_t (
 // One-bit codes / QJL signs: bit i of the word for coordinate i; pair (s, s+16)
 // and (s+8, s+24); `neg2` holds (-v, -v) so that a set bit yields +v.
 __device__ __forceinline__ uint32_t dec1(uint32_t w, int sh, uint32_t neg2) {
-    return ((w << sh) & 0x80008000u) ^ neg2;
+    return (shl_f(w, sh) & 0x80008000u) ^ neg2;
 }
+
+// (h, h) from the fp16 bits h.
+__device__ __forceinline__ uint32_t dup_half(uint32_t h) { return mad_lo(h, kDc.m10001, 0u); }
 
 // Decode a whole 32-coordinate chunk into 16 pairs (MSE codebooks).
 template <int B>
@@ -280,9 +319,10 @@ template <>
 struct MseChunk<3> {
     static constexpr int kWords = 3;
     __device__ __forceinline__ static void run(const uint32_t* w, const Tab8& t, uint32_t (&h)[16]) {
+        // the four 24-bit groups of the 96-bit chunk
         const uint32_t v0 = w[0] & 0xFFFFFFu;
-        const uint32_t v1 = __funnelshift_r(w[0], w[1], 24) & 0xFFFFFFu;
-        const uint32_t v2 = __funnelshift_r(w[1], w[2], 16) & 0xFFFFFFu;
+        const uint32_t v1 = mad_lo(w[1] & 0xFFFFu, kDc.pow2[8], (w[0] >> 24));
+        const uint32_t v2 = mad_lo(w[2] & 0xFFu, kDc.pow2[16], (w[1] >> 16));
         const uint32_t v3 = w[2] >> 8;
         uint32_t g[4];
         dec3_group(v0, t, g);
@@ -308,6 +348,32 @@ struct MseChunk<4> {
         }
     }
 };
+
+// 3-bit codes through a shared-memory table of code pairs, moving the lookups
+// from the ALU pipe (byte permutes) to the load pipe. Entry e holds the fp16
+// pair (c[e & 7], c[e >> 3]); the copy for lane L of entry e sits at byte
+// 128 e + 4 L of an 8 KB-aligned table, so the 32 lanes of a warp always read
+// 32 different banks. `lane_addr` is the table's shared address + 4 L. Field p
+// of the 96-bit chunk (codes 2p, 2p + 1, bits 6p..6p+5) is shifted to bit 7,
+// masked and or-ed onto the lane address: one shift, one logic op and one
+// load per pair, in the same pair order as MseChunk<3>.
+__device__ __forceinline__ uint32_t lds_u32(uint32_t addr) {
+    uint32_t v;
+    asm("ld.shared.u32 %0, [%1];\n" : "=r"(v) : "r"(addr));
+    return v;
+}
+
+__device__ __forceinline__ void pair3_chunk(const uint32_t* w, uint32_t lane_addr, uint32_t (&h)[16]) {
+#pragma unroll
+    for (int p = 0; p < 16; ++p) {
+        const int b = 6 * p, wi = b >> 5, off = b & 31;
+        uint32_t f;
+        if (off + 6 > 32) f = __funnelshift_r(w[wi], w[wi + 1], off - 7);
+        else if (off >= 7) f = w[wi] >> (off - 7);
+        else f = shl_f(w[wi], 7 - off);
+        h[p] = lds_u32((f & 0x1F80u) | lane_addr);
+    }
+}
 
 // Coordinates (within the 32-coordinate chunk) of pair p for an MSE decoder.
 __host__ __device__ inline void mse_pair(int bits, int p, int& a, int& b) {
@@ -354,7 +420,7 @@ struct GroupChunk<4> {
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const int sh = 6 - 4 * i;
-                const uint32_t x = sh >= 0 ? (w[wi] << sh) : (w[wi] >> (-sh));
+                const uint32_t x = sh >= 0 ? shl_f(w[wi], sh) : (w[wi] >> (-sh));
                 const uint32_t v = (x & 0x03C003C0u) | 0x3C003C00u;  // 1 + q/16 in each half
                 const __half2 f = __hsub2(*reinterpret_cast<const __half2*>(&v), __float2half2_rn(1.0f));
                 const __half2 r = __hfma2(f, m, c);
@@ -375,7 +441,7 @@ struct GroupChunk<2> {
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 const int sh = 8 - 2 * i;
-                const uint32_t x = sh >= 0 ? (w[wi] << sh) : (w[wi] >> (-sh));
+                const uint32_t x = sh >= 0 ? shl_f(w[wi], sh) : (w[wi] >> (-sh));
                 const uint32_t v = (x & 0x03000300u) | 0x3C003C00u;  // 1 + q/4 in each half
                 const __half2 f = __hsub2(*reinterpret_cast<const __half2*>(&v), __float2half2_rn(1.0f));
                 const __half2 r = __hfma2(f, m, c);

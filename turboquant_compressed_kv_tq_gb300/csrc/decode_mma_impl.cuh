@@ -8,6 +8,16 @@ namespace tq {
 namespace mmadec {
 
 constexpr float kLog2e = 1.4426950408889634f;
+// Running row maximum before any score: finite, so that ex2(score - max) and
+// ex2(old - new max) need no guard (a masked score is -inf and gives 0).
+constexpr float kNoMax = -3.402823466e38f;
+// Lagging row maximum: the reference maximum m of p = 2^(x - m) moves only
+// when a score passes it by more than kLag (log2 units), so p <= 2^kLag and
+// most 16-token steps skip the rescale of the accumulators. P' = fp16(p * value
+// norm) stays finite while norms are at most kLagNorm (2^8 * 2^7 < 65504);
+// a step holding a larger norm moves m to the exact maximum instead.
+constexpr float kLag = 8.0f;
+constexpr float kLagNorm = 128.0f;
 constexpr float kSqrtHalfPi = 1.2533141373155003f;  // sqrt(pi/2)
 
 // Per-launch layout of one shared-memory stage (TT tokens of every stream).
@@ -18,6 +28,7 @@ struct StageLayout {
     int field[7];           // bytes per token of each stream
     int bar_off;            // byte offset of the mbarriers (past ring and merge areas)
     int qs_off;             // byte offset of the query fragments (past the ring)
+    int vt_off;             // byte offset of the value pair table region (-1: none)
 };
 
 struct MmaArgs {
@@ -380,18 +391,32 @@ __global__ void __launch_bounds__(kThreads, 1) split_mma_kernel(MmaArgs m) {
     __syncwarp();
 
     const auto ktab = mse_table<KB>(a.kc.c);
+    // 3-bit MSE values decode through the shared pair table, others in registers
+    constexpr bool kPairTab = !VGROUP && VB == 3;
     typename MseTable<VGROUP ? 2 : VB>::type vtab{};
-    if constexpr (!VGROUP) vtab = mse_table<VB>(a.vc.c);
+    if constexpr (!VGROUP && !kPairTab) vtab = mse_table<VB>(a.vc.c);
+    uint32_t vt_lane = 0;
+    if constexpr (kPairTab) {
+        const uint32_t region = smem_u32(smem + st.vt_off);
+        const uint32_t base = (region + kVPairBytes - 1) & ~static_cast<uint32_t>(kVPairBytes - 1);
+        vt_lane = base + 4u * lane;
+        uint32_t* tab = reinterpret_cast<uint32_t*>(smem + st.vt_off + (base - region));
+        for (int i = threadIdx.x; i < 64 * 32; i += kThreads) {
+            const int e = i >> 5;
+            tab[i] = h_bits(__ldg(a.vc.c + (e & 7))) | (h_bits(__ldg(a.vc.c + (e >> 3))) << 16);
+        }
+    }
 
     // causal limits of this thread's two rows (padding rows see everything)
     const int r0 = rg * kRows + g, r1 = r0 + 8;
     const int lim0 = r0 < a.plan.rows ? N - a.Lq + (r0 % a.Lq) : N - 1;
     const int lim1 = r1 < a.plan.rows ? N - a.Lq + (r1 % a.Lq) : N - 1;
+    const int lim_all = N - a.Lq;  // every row sees the tokens up to here
 
     float o[16][4];
 #pragma unroll
     for (int p = 0; p < 16; ++p) o[p][0] = o[p][1] = o[p][2] = o[p][3] = 0.0f;
-    float mrow0 = -INFINITY, mrow1 = -INFINITY, lrow0 = 0.0f, lrow1 = 0.0f;
+    float mrow0 = kNoMax, mrow1 = kNoMax, lrow0 = 0.0f, lrow1 = 0.0f;
     bool failed = false;
 
     auto issue = [&](int i) {
@@ -480,8 +505,7 @@ __global__ void __launch_bounds__(kThreads, 1) split_mma_kernel(MmaArgs m) {
                 mse_chunk<KB>(kw, ktab, hk[nt]);
                 if constexpr (KPROD) {
                     sw[nt] = ksgn[tau * 4 + j];
-                    const uint32_t hg = h_bits(-krn[tau]);
-                    neg2[nt] = hg | (hg << 16);
+                        neg2[nt] = dup_half(h_bits(-krn[tau]));
                 }
             }
 #pragma unroll
@@ -529,6 +553,9 @@ __global__ void __launch_bounds__(kThreads, 1) split_mma_kernel(MmaArgs m) {
                     const uint32_t addB = pack_half2(mB, mB);
                     GroupChunk<VB>::run(wA, mulA, addA, hA);
                     GroupChunk<VB>::run(wB, mulB, addB, hB);
+                } else if constexpr (kPairTab) {
+                    pair3_chunk(wA, vt_lane, hA);
+                    pair3_chunk(wB, vt_lane, hB);
                 } else {
                     mse_chunk<VB>(wA, vtab, hA);
                     mse_chunk<VB>(wB, vtab, hB);
@@ -536,16 +563,31 @@ __global__ void __launch_bounds__(kThreads, 1) split_mma_kernel(MmaArgs m) {
             }
             // ---------------- scale, mask, online softmax (log2 domain)
             float x[2][4];
+            float2 nv[2] = {};
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt) {
-                const int tl = 16 * u + 8 * nt + 2 * j;
-                const float2 kn = *reinterpret_cast<const float2*>(knorm + tl);
-                const int pos = t0 + tl;
-                const bool v0 = tl < valid, v1 = tl + 1 < valid;
-                x[nt][0] = (v0 && pos <= lim0) ? sc[nt][0] * kn.x : -INFINITY;
-                x[nt][1] = (v1 && pos + 1 <= lim0) ? sc[nt][1] * kn.y : -INFINITY;
-                x[nt][2] = (v0 && pos <= lim1) ? sc[nt][2] * kn.x : -INFINITY;
-                x[nt][3] = (v1 && pos + 1 <= lim1) ? sc[nt][3] * kn.y : -INFINITY;
+                const float2 kn = *reinterpret_cast<const float2*>(knorm + 16 * u + 8 * nt + 2 * j);
+                if constexpr (!VGROUP) nv[nt] = *reinterpret_cast<const float2*>(vnorm + 16 * u + 8 * nt + 2 * j);
+                x[nt][0] = sc[nt][0] * kn.x;
+                x[nt][1] = sc[nt][1] * kn.y;
+                x[nt][2] = sc[nt][2] * kn.x;
+                x[nt][3] = sc[nt][3] * kn.y;
+            }
+            // masks only where the 16 tokens reach past the tile's end or a row's causal limit
+            // (past the end, the stage holds stale bytes: their value norms become 0)
+            if (16 * u + 16 > valid || t0 + 16 * u + 15 > lim_all) {
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt) {
+                    const int tl = 16 * u + 8 * nt + 2 * j;
+                    const int pos = t0 + tl;
+                    const bool v0 = tl < valid, v1 = tl + 1 < valid;
+                    if (!(v0 && pos <= lim0)) x[nt][0] = -INFINITY;
+                    if (!(v1 && pos + 1 <= lim0)) x[nt][1] = -INFINITY;
+                    if (!(v0 && pos <= lim1)) x[nt][2] = -INFINITY;
+                    if (!(v1 && pos + 1 <= lim1)) x[nt][3] = -INFINITY;
+                    if (!v0) nv[nt].x = 0.0f;
+                    if (!v1) nv[nt].y = 0.0f;
+                }
             }
             float mx0 = fmaxf(fmaxf(x[0][0], x[0][1]), fmaxf(x[1][0], x[1][1]));
             float mx1 = fmaxf(fmaxf(x[0][2], x[0][3]), fmaxf(x[1][2], x[1][3]));
@@ -553,10 +595,15 @@ __global__ void __launch_bounds__(kThreads, 1) split_mma_kernel(MmaArgs m) {
             mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
             mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
             mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-            const float mn0 = fmaxf(mrow0, mx0), mn1 = fmaxf(mrow1, mx1);
-            if (__any_sync(0xffffffffu, mn0 != mrow0 || mn1 != mrow1)) {
-                const float al0 = mn0 == -INFINITY ? 1.0f : ex2(mrow0 - mn0);
-                const float al1 = mn1 == -INFINITY ? 1.0f : ex2(mrow1 - mn1);
+            float lag = kLag;
+            if constexpr (!VGROUP) {
+                const bool big = fmaxf(fmaxf(nv[0].x, nv[0].y), fmaxf(nv[1].x, nv[1].y)) > kLagNorm;
+                if (__any_sync(0xffffffffu, big)) lag = 0.0f;
+            }
+            if (__any_sync(0xffffffffu, mx0 > mrow0 + lag || mx1 > mrow1 + lag)) {
+                const float mn0 = fmaxf(mrow0, mx0), mn1 = fmaxf(mrow1, mx1);
+                const float al0 = ex2(mrow0 - mn0);
+                const float al1 = ex2(mrow1 - mn1);
                 lrow0 *= al0;
                 lrow1 *= al1;
 #pragma unroll
@@ -570,30 +617,32 @@ __global__ void __launch_bounds__(kThreads, 1) split_mma_kernel(MmaArgs m) {
             float pr[2][4];
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt) {
-                pr[nt][0] = mrow0 == -INFINITY ? 0.0f : ex2(x[nt][0] - mrow0);
-                pr[nt][1] = mrow0 == -INFINITY ? 0.0f : ex2(x[nt][1] - mrow0);
-                pr[nt][2] = mrow1 == -INFINITY ? 0.0f : ex2(x[nt][2] - mrow1);
-                pr[nt][3] = mrow1 == -INFINITY ? 0.0f : ex2(x[nt][3] - mrow1);
+                pr[nt][0] = ex2(x[nt][0] - mrow0);
+                pr[nt][1] = ex2(x[nt][1] - mrow0);
+                pr[nt][2] = ex2(x[nt][2] - mrow1);
+                pr[nt][3] = ex2(x[nt][3] - mrow1);
             }
             // P' = fp16(p * value norm); the row sums add the weights actually
-            // multiplied (P' / norm), so the rounding of P' cancels in o = sum/L
-            // (a zero-norm value contributes its p directly).
+            // multiplied (P' / norm), so the rounding of P' cancels in o = sum/L.
+            // A zero-norm value contributes its p directly: with 1/norm taken as
+            // 0 there, 1 - norm * (1/norm) is 1 for it and within 2^-22 of 0
+            // otherwise.
             uint32_t pa[4];
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt) {
                 float w0 = pr[nt][0], w1 = pr[nt][1], w2 = pr[nt][2], w3 = pr[nt][3];
                 float r0 = 1.0f, r1 = 1.0f;
                 if constexpr (!VGROUP) {
-                    const float2 nv = *reinterpret_cast<const float2*>(vnorm + 16 * u + 8 * nt + 2 * j);
-                    const bool z0 = !(nv.x > 0.0f), z1 = !(nv.y > 0.0f);
-                    r0 = z0 ? 0.0f : __fdividef(1.0f, nv.x);
-                    r1 = z1 ? 0.0f : __fdividef(1.0f, nv.y);
-                    w0 = (w0 != 0.0f && !z0) ? w0 * nv.x : 0.0f;
-                    w1 = (w1 != 0.0f && !z1) ? w1 * nv.y : 0.0f;
-                    w2 = (w2 != 0.0f && !z0) ? w2 * nv.x : 0.0f;
-                    w3 = (w3 != 0.0f && !z1) ? w3 * nv.y : 0.0f;
-                    if (z0) { lrow0 += pr[nt][0]; lrow1 += pr[nt][2]; }
-                    if (z1) { lrow0 += pr[nt][1]; lrow1 += pr[nt][3]; }
+                    const float nx = nv[nt].x, ny = nv[nt].y;
+                    r0 = nx > 0.0f ? __fdividef(1.0f, nx) : 0.0f;
+                    r1 = ny > 0.0f ? __fdividef(1.0f, ny) : 0.0f;
+                    const float z0 = fmaf(-nx, r0, 1.0f), z1 = fmaf(-ny, r1, 1.0f);
+                    w0 *= nx;
+                    w1 *= ny;
+                    w2 *= nx;
+                    w3 *= ny;
+                    lrow0 = fmaf(z0, pr[nt][0], fmaf(z1, pr[nt][1], lrow0));
+                    lrow1 = fmaf(z0, pr[nt][2], fmaf(z1, pr[nt][3], lrow1));
                 }
                 pa[2 * nt] = pack_half2(w0, w1);
                 pa[2 * nt + 1] = pack_half2(w2, w3);
@@ -607,6 +656,8 @@ __global__ void __launch_bounds__(kThreads, 1) split_mma_kernel(MmaArgs m) {
         }
     }
     tc::grid_release_dependents();  // the next kernel may start; it waits for this one before the workspace
+    if (mrow0 == kNoMax) mrow0 = -INFINITY;  // no score seen by this thread's rows
+    if (mrow1 == kNoMax) mrow1 = -INFINITY;
     if (failed && lane == 0) atomicOr(a.err, TQ_DEVERR_TIMEOUT);
     // drain copies that were issued but never waited for (only after a timeout)
     if (failed) {
