@@ -419,27 +419,43 @@ __global__ void __launch_bounds__(kThreads, 1) split_mma_kernel(MmaArgs m) {
     float mrow0 = kNoMax, mrow1 = kNoMax, lrow0 = 0.0f, lrow1 = 0.0f;
     bool failed = false;
 
+    // Stage copies: lane k < 7 copies record stream k of the tile (one warp
+    // instruction for all streams), after lane 0 has posted the stage's bytes.
+    // Blocks hold a power-of-two token count, so block index and slot are a
+    // shift and a mask. bad_stage bit s marks a stage whose block-table entry
+    // was out of range (its copy reads block 0; the tile is flagged and skipped).
+    const int bt_shift = __ffs(BT) - 1;
+    unsigned stage_tx = 0;
+    int s_off = -1, s_field = 0;
+    int64_t s_src = 0;
+#pragma unroll
+    for (int k = 0; k < 7; ++k) {
+        if (st.off[k] >= 0) stage_tx += TT * st.field[k];
+        if (lane == k) {
+            s_off = st.off[k];
+            s_field = st.field[k];
+            s_src = a.pool.off[k];
+        }
+    }
+    const uint64_t pol = policy_evict_first();
+    uint32_t bad_stage = 0;
     auto issue = [&](int i) {
         const int t0 = t_begin + (warp + i * kWarps) * TT;
-        const int lb = t0 / BT;
-        const int slot0 = t0 - lb * BT;
+        const int lb = t0 >> bt_shift;
+        const int slot0 = t0 & (BT - 1);
         int64_t pb = a.table ? static_cast<int64_t>(a.table[static_cast<int64_t>(b) * a.max_blocks + lb])
                              : static_cast<int64_t>(b) * a.max_blocks + lb;
-        if (pb < 0 || pb >= a.pool.num_blocks) pb = 0;  // flagged and masked when computed
+        const int sidx = i % kStages;
+        const bool badb = pb < 0 || pb >= a.pool.num_blocks;
+        if (badb) pb = 0;
+        bad_stage = badb ? (bad_stage | (1u << sidx)) : (bad_stage & ~(1u << sidx));
         const char* base = a.pool.base + (pb * Hkv + h) * a.pool.sub_bytes;
-        unsigned char* dst = ring + static_cast<size_t>(i % kStages) * st.bytes;
-        uint64_t* bar = &bars[i % kStages];
-        if (lane == 0) {
-            unsigned total = 0;
-            for (int k = 0; k < 7; ++k)
-                if (st.off[k] >= 0) total += TT * st.field[k];
-            mbar_expect_tx(bar, total);
-            const uint64_t pol = policy_evict_first();
-            for (int k = 0; k < 7; ++k)
-                if (st.off[k] >= 0)
-                    bulk_g2s_once(dst + st.off[k], base + a.pool.off[k] + static_cast<int64_t>(slot0) * st.field[k],
-                                  TT * st.field[k], bar, pol);
-        }
+        unsigned char* dst = ring + static_cast<size_t>(sidx) * st.bytes;
+        uint64_t* bar = &bars[sidx];
+        if (lane == 0) mbar_expect_tx(bar, stage_tx);
+        __syncwarp();
+        if (s_off >= 0)
+            bulk_g2s_once(dst + s_off, base + s_src + static_cast<int64_t>(slot0) * s_field, TT * s_field, bar, pol);
     };
 
     const int pre = my_n < kStages - 1 ? my_n : kStages - 1;
@@ -477,14 +493,9 @@ __global__ void __launch_bounds__(kThreads, 1) split_mma_kernel(MmaArgs m) {
 
         const int t0 = t_begin + (warp + i * kWarps) * TT;
         int valid = min(TT, t_end - t0);
-        {
-            const int lb = t0 / BT;
-            const int64_t pb = a.table ? static_cast<int64_t>(a.table[static_cast<int64_t>(b) * a.max_blocks + lb])
-                                       : static_cast<int64_t>(b) * a.max_blocks + lb;
-            if (pb < 0 || pb >= a.pool.num_blocks) {
-                if (lane == 0) atomicOr(a.err, TQ_DEVERR_BLOCK);
-                valid = 0;
-            }
+        if ((bad_stage >> (i % kStages)) & 1u) {
+            if (lane == 0) atomicOr(a.err, TQ_DEVERR_BLOCK);
+            valid = 0;
         }
 
         for (int u = 0; u < TT / 16; ++u) {
