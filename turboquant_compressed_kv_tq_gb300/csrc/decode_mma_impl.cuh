@@ -14,8 +14,8 @@ constexpr float kNoMax = -3.402823466e38f;
 // Lagging row maximum: the reference maximum m of p = 2^(x - m) moves only
 // when a score passes it by more than kLag (log2 units), so p <= 2^kLag and
 // most 16-token steps skip the rescale of the accumulators. P' = fp16(p * value
-// norm) stays finite while norms are at most kLagNorm (2^8 * 2^7 < 65504);
-// a step holding a larger norm moves m to the exact maximum instead.
+// norm) stays finite while norms are at most kLagNorm (2^8 * 2^7 < 65504); in
+// a tile holding a larger norm, m follows the exact maximum instead.
 constexpr float kLag = 8.0f;
 constexpr float kLagNorm = 128.0f;
 constexpr float kSqrtHalfPi = 1.2533141373155003f;  // sqrt(pi/2)
@@ -498,6 +498,15 @@ __global__ void __launch_bounds__(kThreads, 1) split_mma_kernel(MmaArgs m) {
             valid = 0;
         }
 
+        // rescale threshold lag of this tile (0 if a value norm could overflow P')
+        float lag = kLag;
+        if constexpr (!VGROUP) {
+            float nmax = 0.0f;
+            if (2 * lane < valid) nmax = vnorm[2 * lane];
+            if (2 * lane + 1 < valid) nmax = fmaxf(nmax, vnorm[2 * lane + 1]);
+            if (__any_sync(0xffffffffu, nmax > kLagNorm)) lag = 0.0f;
+        }
+
         for (int u = 0; u < TT / 16; ++u) {
             if (16 * u >= valid) break;
             // ---------------- scores for 16 tokens (two n8 tiles)
@@ -600,18 +609,16 @@ __global__ void __launch_bounds__(kThreads, 1) split_mma_kernel(MmaArgs m) {
                     if (!v1) nv[nt].y = 0.0f;
                 }
             }
-            float mx0 = fmaxf(fmaxf(x[0][0], x[0][1]), fmaxf(x[1][0], x[1][1]));
-            float mx1 = fmaxf(fmaxf(x[0][2], x[0][3]), fmaxf(x[1][2], x[1][3]));
-            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-            float lag = kLag;
-            if constexpr (!VGROUP) {
-                const bool big = fmaxf(fmaxf(nv[0].x, nv[0].y), fmaxf(nv[1].x, nv[1].y)) > kLagNorm;
-                if (__any_sync(0xffffffffu, big)) lag = 0.0f;
-            }
-            if (__any_sync(0xffffffffu, mx0 > mrow0 + lag || mx1 > mrow1 + lag)) {
+            const float th0 = mrow0 + lag, th1 = mrow1 + lag;
+            if (__any_sync(0xffffffffu, x[0][0] > th0 || x[0][1] > th0 || x[1][0] > th0 || x[1][1] > th0 ||
+                                            x[0][2] > th1 || x[0][3] > th1 || x[1][2] > th1 || x[1][3] > th1)) {
+                // a score passed m + lag: move m to the exact row maxima
+                float mx0 = fmaxf(fmaxf(x[0][0], x[0][1]), fmaxf(x[1][0], x[1][1]));
+                float mx1 = fmaxf(fmaxf(x[0][2], x[0][3]), fmaxf(x[1][2], x[1][3]));
+                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
                 const float mn0 = fmaxf(mrow0, mx0), mn1 = fmaxf(mrow1, mx1);
                 const float al0 = ex2(mrow0 - mn0);
                 const float al1 = ex2(mrow1 - mn1);
@@ -635,9 +642,8 @@ __global__ void __launch_bounds__(kThreads, 1) split_mma_kernel(MmaArgs m) {
             }
             // P' = fp16(p * value norm); the row sums add the weights actually
             // multiplied (P' / norm), so the rounding of P' cancels in o = sum/L.
-            // A zero-norm value contributes its p directly: with 1/norm taken as
-            // 0 there, 1 - norm * (1/norm) is 1 for it and within 2^-22 of 0
-            // otherwise.
+            // A zero norm gives P' = 0 and a huge finite 1/norm (nothing added);
+            // its p enters the row sums in the rare branch below.
             uint32_t pa[4];
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt) {
@@ -645,15 +651,12 @@ __global__ void __launch_bounds__(kThreads, 1) split_mma_kernel(MmaArgs m) {
                 float r0 = 1.0f, r1 = 1.0f;
                 if constexpr (!VGROUP) {
                     const float nx = nv[nt].x, ny = nv[nt].y;
-                    r0 = nx > 0.0f ? __fdividef(1.0f, nx) : 0.0f;
-                    r1 = ny > 0.0f ? __fdividef(1.0f, ny) : 0.0f;
-                    const float z0 = fmaf(-nx, r0, 1.0f), z1 = fmaf(-ny, r1, 1.0f);
+                    r0 = rcp_approx(fmaxf(nx, 1e-30f));
+                    r1 = rcp_approx(fmaxf(ny, 1e-30f));
                     w0 *= nx;
                     w1 *= ny;
                     w2 *= nx;
                     w3 *= ny;
-                    lrow0 = fmaf(z0, pr[nt][0], fmaf(z1, pr[nt][1], lrow0));
-                    lrow1 = fmaf(z0, pr[nt][2], fmaf(z1, pr[nt][3], lrow1));
                 }
                 pa[2 * nt] = pack_half2(w0, w1);
                 pa[2 * nt + 1] = pack_half2(w2, w3);
@@ -661,6 +664,16 @@ __global__ void __launch_bounds__(kThreads, 1) split_mma_kernel(MmaArgs m) {
                 const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&pa[2 * nt + 1]));
                 lrow0 += f0.x * r0 + f0.y * r1;
                 lrow1 += f1.x * r0 + f1.y * r1;
+            }
+            if constexpr (!VGROUP) {
+                const bool zero = !(fminf(fminf(nv[0].x, nv[0].y), fminf(nv[1].x, nv[1].y)) > 0.0f);
+                if (__any_sync(0xffffffffu, zero)) {
+#pragma unroll
+                    for (int nt = 0; nt < 2; ++nt) {
+                        if (!(nv[nt].x > 0.0f)) { lrow0 += pr[nt][0]; lrow1 += pr[nt][2]; }
+                        if (!(nv[nt].y > 0.0f)) { lrow0 += pr[nt][1]; lrow1 += pr[nt][3]; }
+                    }
+                }
             }
 #pragma unroll
             for (int p = 0; p < 16; ++p) mma16816(o[p], pa, movmatrix_t(hA[p]), movmatrix_t(hB[p]));
