@@ -5,8 +5,10 @@ head_dim 128, keys 3-bit prod, values 3-bit MSE, 262,144 tokens prefilled by
 chunked encode (8192-token chunks), then decode steps that each append 2
 tokens per layer and attend with query length 2 over every layer.
 
-A step = for each of the 64 layers: tq_encode_append (2 tokens x 8 heads)
-followed by tq_decode_attention (q_len 2). `value` is the compressed bytes the
+A step = for each of the 64 layers: the append of 2 tokens x 8 heads and the
+decode attention (q_len 2), through tq_decode_step (the append runs inside the
+decode's query-prep launch; --step-api separate: tq_encode_append then
+tq_decode_attention). `value` is the compressed bytes the
 step's decode reads (valid tokens x heads x layers x record bytes) divided by
 the step time, summed over ranks. Inputs are resident in HBM before the timed
 region; the cache (14.5 GB) is far larger than L2, so no flush is needed.
@@ -342,9 +344,16 @@ def run_gpu(args):
     ws = torch.empty(cache.workspace_bytes(1, Hq, Lq, cap), dtype=torch.uint8, device=dev)
     out = torch.empty(L, 1, Hq, Lq, D, dtype=torch.float32, device=dev)
 
+    fused = args.step_api == "fused"
+
     def step(s, ev=None):
         k_new, v_new, q = steps_in[s]
         for layer in range(L):
+            if fused and ev is None:
+                # one call: the append runs inside the decode's query-prep launch
+                cache.decode_step(layer, k_new[layer], v_new[layer], q[layer], lens_pre[s:s + 1], None, nblk,
+                                  cap, out[layer], ws)
+                continue
             cache.append(layer, k_new[layer], v_new[layer], lens_pre[s:s + 1], None, nblk)
             if ev is not None:
                 ev[layer][0].record(stream)
@@ -406,8 +415,12 @@ def run_gpu(args):
         dv.copy_(hv, non_blocking=True)
         dq.copy_(hq, non_blocking=True)
         for layer in range(L):
-            cache.append(layer, dk[layer], dv[layer], lens_pre[s:s + 1], None, nblk)
-            cache.decode(layer, dq[layer], lens_post[s:s + 1], None, nblk, cap, out[layer], ws)
+            if fused:
+                cache.decode_step(layer, dk[layer], dv[layer], dq[layer], lens_pre[s:s + 1], None, nblk, cap,
+                                  out[layer], ws)
+            else:
+                cache.append(layer, dk[layer], dv[layer], lens_pre[s:s + 1], None, nblk)
+                cache.decode(layer, dq[layer], lens_post[s:s + 1], None, nblk, cap, out[layer], ws)
         out_host.copy_(out, non_blocking=True)
         torch.cuda.current_stream(dev).synchronize()
     e2e_s = (time.perf_counter() - t0) / args.steps
@@ -437,6 +450,7 @@ def run_gpu(args):
             "config": {"workload": _workload_text(w),
                        "bytes_per_step": bytes_per_step, "record_bytes_per_token_head": rec_bytes,
                        "l2": "inputs larger than L2: each step reads a 14.5 GB compressed cache",
+                       "step_api": ("tq_decode_step" if fused else "tq_encode_append + tq_decode_attention"),
                        "block_tokens": BT, "replicas": world},
             "steps_per_s": 1000.0 / step_ms_max,
             "hbm_frac_of_measured": value / world / peak,
@@ -473,6 +487,9 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--step-api", default="fused", choices=["fused", "separate"],
+                    help="decode step per layer: tq_decode_step (append fused into the decode's first launch) "
+                         "or tq_encode_append then tq_decode_attention")
     ap.add_argument("--no-prefill-attention", action="store_true",
                     help="skip the one-layer prefill-attention measurement")
     ap.add_argument("--layers", type=int, default=0,

@@ -318,6 +318,38 @@ tq_status tq_decode_attention(const tq_codec *key_codec, const tq_codec *value_c
                               int max_seq_len, float scale, float *out, void *workspace,
                               size_t workspace_bytes, tq_stream_t stream);
 
+/*
+ * One decode step of one layer: tq_encode_append of the step's n_new tokens
+ * followed by tq_decode_attention over the grown sequences
+ * ("lightning-mlx/plan.md", the minimum work list: an incremental append that
+ * quantizes only the new tokens, and attention over the compressed cache;
+ * running both from one call, with the append inside the decode's first
+ * launch, is this library's). Results are those of the two calls in sequence:
+ * the same cache bytes and the same outputs.
+ *   k_new, v_new device [batch][num_kv_heads][n_new][head_dim], kv_dtype
+ *        f32/bf16/f16; n_new >= 0 (0: a plain decode).
+ *   seq_lens device int32 [batch]: tokens in the cache BEFORE the step (not
+ *        modified); the new tokens go to positions seq_lens[b] ..
+ *        seq_lens[b] + n_new - 1 and sequence b then attends over
+ *        seq_lens[b] + n_new tokens, its q_len queries being the newest.
+ *   max_seq_len (host) bounds every seq_lens[b] + n_new; the workspace is
+ *        tq_decode_workspace_bytes(cache, batch, num_q_heads, q_len,
+ *        max_seq_len).
+ *   q, out, block_table, max_blocks, scale, workspace: as tq_decode_attention.
+ * With head_dim 128, rotated keys and values (MSE or prod), n_new <= 8 and the
+ * tensor-core decode, the append runs inside the query-prep launch (two
+ * launches per step instead of three); otherwise the two calls run in order.
+ * Errors: those of tq_encode_append and tq_decode_attention, checked before
+ * anything is launched.
+ */
+tq_status tq_decode_step(const tq_codec *key_codec, const tq_codec *value_codec,
+                         const tq_cache_desc *cache, int layer, const void *k_new,
+                         const void *v_new, tq_dtype kv_dtype, int n_new, const void *q,
+                         tq_dtype q_dtype, int batch, int num_q_heads, int q_len,
+                         const int32_t *seq_lens, const int32_t *block_table, int max_blocks,
+                         int max_seq_len, float scale, float *out, void *workspace,
+                         size_t workspace_bytes, tq_stream_t stream);
+
 /* ------------------------------------------------------------------ */
 /* Prefill attention                                                    */
 /* ------------------------------------------------------------------ */

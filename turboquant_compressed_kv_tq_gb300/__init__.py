@@ -21,6 +21,7 @@ __all__ = [
     "tq_bits_split", "tq_codec_pair_for_bits",
     "tq_codec_build_host", "tq_codec_export", "tq_cache_desc_init", "tq_encode_append",
     "tq_quantize", "tq_decode_workspace_bytes", "tq_decode_attention", "tq_decode_attention_noalloc",
+    "tq_decode_step",
     "tq_prefill_workspace_bytes", "tq_prefill_attention", "tq_cache_copy_blocks",
     "tq_device_error",
     "tq_launch_count", "tq_abi_version", "Codec", "CompressedKVCache", "TQError",
@@ -180,6 +181,20 @@ def tq_decode_attention(key_codec: int, value_codec: int, desc: tq_cache_desc, l
                                     ws_bytes, _stream(stream)), "tq_decode_attention")
 
 
+def tq_decode_step(key_codec: int, value_codec: int, desc: tq_cache_desc, layer: int, k_new, v_new, q,
+                   seq_lens, block_table, max_blocks: int, max_seq_len: int, out, workspace,
+                   scale: float = 0.0, stream=None) -> None:
+    """Append k_new / v_new [batch][kv heads][n_new][D] at seq_lens (the lengths before the step) and
+    decode q over the grown sequences, in one call (see include/tq.h)."""
+    batch, hq, lq, _ = q.shape
+    n_new = k_new.shape[2]
+    ws_bytes = workspace.numel() * workspace.element_size()
+    check(lib().tq_decode_step(key_codec, value_codec, ctypes.byref(desc), layer, _ptr(k_new), _ptr(v_new),
+                               _dtype_code(k_new), n_new, _ptr(q), _dtype_code(q), batch, hq, lq,
+                               _ptr(seq_lens), _ptr(block_table), max_blocks, max_seq_len, scale, _ptr(out),
+                               _ptr(workspace), ws_bytes, _stream(stream)), "tq_decode_step")
+
+
 def tq_cache_copy_blocks(src: tq_cache_desc, dst: tq_cache_desc, src_blocks, dst_blocks, stream=None) -> None:
     n = src_blocks.numel()
     assert dst_blocks.numel() == n
@@ -309,3 +324,9 @@ class CompressedKVCache:
                scale=0.0, stream=None):
         tq_decode_attention(self.key.handle, self.value.handle, self.desc, layer, q, seq_lens,
                             block_table, max_blocks, max_seq_len, out, workspace, scale, stream)
+
+    def decode_step(self, layer, k_new, v_new, q, seq_lens, block_table, max_blocks, max_seq_len, out,
+                    workspace, scale=0.0, stream=None):
+        """Append the step's tokens at seq_lens (lengths before the step) and decode, in one call."""
+        tq_decode_step(self.key.handle, self.value.handle, self.desc, layer, k_new, v_new, q, seq_lens,
+                       block_table, max_blocks, max_seq_len, out, workspace, scale, stream)

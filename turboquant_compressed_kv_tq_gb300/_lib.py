@@ -94,6 +94,8 @@ SIGNATURES = {
                                         ctypes.POINTER(_SZ)]),
     "tq_decode_attention": (_ST, [_P, _P, ctypes.POINTER(tq_cache_desc), _I, _P, _I, _I, _I, _I, _P,
                                   _P, _I, _I, _F, _P, _P, _SZ, _P]),
+    "tq_decode_step": (_ST, [_P, _P, ctypes.POINTER(tq_cache_desc), _I, _P, _P, _I, _I, _P, _I, _I, _I, _I,
+                             _P, _P, _I, _I, _F, _P, _P, _SZ, _P]),
     "tq_decode_attention_noalloc": (_ST, [_P, _P, ctypes.POINTER(tq_cache_desc), _I, _P, _I, _I, _I, _I,
                                           _P, _P, _I, _I, _F, _P, _P]),
     "tq_prefill_workspace_bytes": (_ST, [ctypes.POINTER(tq_cache_desc), _I, _I, _I, ctypes.POINTER(_SZ)]),

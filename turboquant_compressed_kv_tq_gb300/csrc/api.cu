@@ -394,10 +394,14 @@ tq_status tq_cache_copy_blocks(const tq_cache_desc* src, const tq_cache_desc* ds
                : TQ_ERR_CUDA;
 }
 
-tq_status tq_encode_append(const tq_codec* kc, const tq_codec* vc, const tq_cache_desc* cache, int layer,
-                           const void* k, const void* v, tq_dtype dtype, int batch, int n_new,
-                           const int32_t* seq_lens, const int32_t* block_table, int max_blocks,
-                           tq_stream_t stream) {
+namespace {
+
+// Checks of tq_encode_append and its launch arguments. *run = false when there
+// is nothing to append (batch or n_new zero) and the call is complete.
+tq_status append_args(const tq_codec* kc, const tq_codec* vc, const tq_cache_desc* cache, int layer, const void* k,
+                      const void* v, tq_dtype dtype, int batch, int n_new, const int32_t* seq_lens,
+                      const int32_t* block_table, int max_blocks, EncodeAppendArgs* out, bool* run) {
+    *run = false;
     tq_status st = check_codecs_vs_cache(kc, vc, cache);
     if (st != TQ_OK) return st;
     if (layer < 0 || layer >= cache->num_layers || batch < 0 || n_new < 0 || max_blocks <= 0)
@@ -411,7 +415,8 @@ tq_status tq_encode_append(const tq_codec* kc, const tq_codec* vc, const tq_cach
     if (batch > 32767) return TQ_ERR_INVALID_ARG;
     unsigned* err = nullptr;
     if (device_state(&err, nullptr) != TQ_OK) return TQ_ERR_CUDA;
-    EncodeAppendArgs a{};
+    EncodeAppendArgs& a = *out;
+    a = EncodeAppendArgs{};
     a.kc = dev_view(kc);
     a.vc = dev_view(vc);
     a.pool = pool_view(cache, layer);
@@ -425,6 +430,21 @@ tq_status tq_encode_append(const tq_codec* kc, const tq_codec* vc, const tq_cach
     a.max_blocks = max_blocks;
     a.exact = cache->encode_policy == TQ_ENCODE_EXACT;
     a.err = err;
+    *run = true;
+    return TQ_OK;
+}
+
+}  // namespace
+
+tq_status tq_encode_append(const tq_codec* kc, const tq_codec* vc, const tq_cache_desc* cache, int layer,
+                           const void* k, const void* v, tq_dtype dtype, int batch, int n_new,
+                           const int32_t* seq_lens, const int32_t* block_table, int max_blocks,
+                           tq_stream_t stream) {
+    EncodeAppendArgs a{};
+    bool run = false;
+    const tq_status st = append_args(kc, vc, cache, layer, k, v, dtype, batch, n_new, seq_lens, block_table,
+                                     max_blocks, &a, &run);
+    if (st != TQ_OK || !run) return st;
     return launch_encode_append(a, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
 }
 
@@ -462,11 +482,15 @@ tq_status tq_decode_workspace_bytes(const tq_cache_desc* cache, int batch, int n
     return TQ_OK;
 }
 
-tq_status tq_decode_attention(const tq_codec* kc, const tq_codec* vc, const tq_cache_desc* cache, int layer,
-                              const void* q, tq_dtype q_dtype, int batch, int num_q_heads, int q_len,
-                              const int32_t* seq_lens, const int32_t* block_table, int max_blocks,
-                              int max_seq_len, float scale, float* out, void* workspace,
-                              size_t workspace_bytes, tq_stream_t stream) {
+namespace {
+
+// Checks of tq_decode_attention and its launch arguments (*run = false: batch
+// zero, nothing to do).
+tq_status decode_args(const tq_codec* kc, const tq_codec* vc, const tq_cache_desc* cache, int layer, const void* q,
+                      tq_dtype q_dtype, int batch, int num_q_heads, int q_len, const int32_t* seq_lens,
+                      const int32_t* block_table, int max_blocks, int max_seq_len, float scale, float* out,
+                      void* workspace, size_t workspace_bytes, DecodeArgs* args, bool* run) {
+    *run = false;
     tq_status st = check_codecs_vs_cache(kc, vc, cache);
     if (st != TQ_OK) return st;
     if (layer < 0 || layer >= cache->num_layers || batch < 0 || q_len <= 0 || max_blocks <= 0)
@@ -489,7 +513,8 @@ tq_status tq_decode_attention(const tq_codec* kc, const tq_codec* vc, const tq_c
     if (device_state(&err, &sms) != TQ_OK) return TQ_ERR_CUDA;
     const DecodePlan plan = make_decode_plan(cache, batch, G, q_len, max_seq_len, sms);
     if (workspace_bytes < plan.total) return TQ_ERR_CAPACITY;
-    DecodeArgs a{};
+    DecodeArgs& a = *args;
+    a = DecodeArgs{};
     a.kc = dev_view(kc);
     a.vc = dev_view(vc);
     a.pool = pool_view(cache, layer);
@@ -512,7 +537,50 @@ tq_status tq_decode_attention(const tq_codec* kc, const tq_codec* vc, const tq_c
     a.ws = workspace;
     a.plan = plan;
     a.err = err;
+    *run = true;
+    return TQ_OK;
+}
+
+}  // namespace
+
+tq_status tq_decode_attention(const tq_codec* kc, const tq_codec* vc, const tq_cache_desc* cache, int layer,
+                              const void* q, tq_dtype q_dtype, int batch, int num_q_heads, int q_len,
+                              const int32_t* seq_lens, const int32_t* block_table, int max_blocks,
+                              int max_seq_len, float scale, float* out, void* workspace,
+                              size_t workspace_bytes, tq_stream_t stream) {
+    DecodeArgs a{};
+    bool run = false;
+    const tq_status st = decode_args(kc, vc, cache, layer, q, q_dtype, batch, num_q_heads, q_len, seq_lens,
+                                     block_table, max_blocks, max_seq_len, scale, out, workspace, workspace_bytes,
+                                     &a, &run);
+    if (st != TQ_OK || !run) return st;
     return launch_decode(a, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
+}
+
+tq_status tq_decode_step(const tq_codec* kc, const tq_codec* vc, const tq_cache_desc* cache, int layer,
+                         const void* k_new, const void* v_new, tq_dtype kv_dtype, int n_new, const void* q,
+                         tq_dtype q_dtype, int batch, int num_q_heads, int q_len, const int32_t* seq_lens,
+                         const int32_t* block_table, int max_blocks, int max_seq_len, float scale, float* out,
+                         void* workspace, size_t workspace_bytes, tq_stream_t stream) {
+    EncodeAppendArgs e{};
+    bool run_e = false;
+    tq_status st = append_args(kc, vc, cache, layer, k_new, v_new, kv_dtype, batch, n_new, seq_lens, block_table,
+                               max_blocks, &e, &run_e);
+    if (st != TQ_OK) return st;
+    DecodeArgs a{};
+    bool run_d = false;
+    st = decode_args(kc, vc, cache, layer, q, q_dtype, batch, num_q_heads, q_len, seq_lens, block_table, max_blocks,
+                     max_seq_len, scale, out, workspace, workspace_bytes, &a, &run_d);
+    if (st != TQ_OK || !run_d) return st;
+    a.len_add = run_e ? n_new : 0;
+    const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    // one launch for the append and the query prep where the tensor-core path
+    // and the short rotated encoder both apply; else the two calls in order
+    const bool fused = run_e && a.plan.kind == 1 && n_new <= 8 && cache->head_dim == 128 &&
+                       kc->mode != TQ_MODE_GROUP && vc->mode != TQ_MODE_GROUP;
+    if (fused) return launch_decode(a, s, &e) == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
+    if (run_e && launch_encode_append(e, s) != cudaSuccess) return TQ_ERR_CUDA;
+    return launch_decode(a, s) == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
 }
 
 namespace {

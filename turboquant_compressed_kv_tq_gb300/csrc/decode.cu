@@ -112,7 +112,7 @@ __global__ void __launch_bounds__(kThreads) split_kernel(DecodeArgs a) {
     const int BT = a.pool.BT;
     const float kappa = 1.2533141373155003f / static_cast<float>(D);  // sqrt(pi/2)/D
 
-    const int N = a.seq_lens[b];
+    const int N = a.seq_lens[b] + a.len_add;
     const int cap = a.max_blocks * BT;
     const bool bad = N < a.Lq || N > cap;
     if (bad && split == 0 && tid == 0 && rg == 0 && h == 0) atomicOr(a.err, TQ_DEVERR_SEQLEN);
@@ -331,9 +331,9 @@ struct MmaArgs;
 #include "decode_mma_impl.cuh"
 namespace tq {
 namespace mmadec {
-bool dispatch_a(int, bool, bool, int, const MmaArgs&, size_t, cudaStream_t, cudaError_t*);
-bool dispatch_b(int, bool, bool, int, const MmaArgs&, size_t, cudaStream_t, cudaError_t*);
-bool dispatch_c(int, bool, bool, int, const MmaArgs&, size_t, cudaStream_t, cudaError_t*);
+bool dispatch_a(int, bool, bool, int, const MmaArgs&, size_t, cudaStream_t, const EncodeAppendArgs*, cudaError_t*);
+bool dispatch_b(int, bool, bool, int, const MmaArgs&, size_t, cudaStream_t, const EncodeAppendArgs*, cudaError_t*);
+bool dispatch_c(int, bool, bool, int, const MmaArgs&, size_t, cudaStream_t, const EncodeAppendArgs*, cudaError_t*);
 }  // namespace mmadec
 
 namespace {
@@ -427,7 +427,7 @@ DecodePlan make_decode_plan(const tq_cache_desc* d, int batch, int G, int Lq, in
     return p;
 }
 
-cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s) {
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s, const EncodeAppendArgs* step) {
     if (a.batch == 0) return cudaSuccess;
     if (a.plan.kind == 1) {
         mmadec::MmaArgs m{};
@@ -448,9 +448,9 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s) {
         m.ml = reinterpret_cast<float*>(ws + a.plan.q_bytes + a.plan.cnt_bytes + a.plan.part_bytes);
         cudaError_t e = cudaErrorInvalidValue;
         const DecodePlan& p = a.plan;
-        if (mmadec::dispatch_a(p.kb, p.kprod, p.vgroup, p.vb, m, p.smem, s, &e)) return e;
-        if (mmadec::dispatch_b(p.kb, p.kprod, p.vgroup, p.vb, m, p.smem, s, &e)) return e;
-        if (mmadec::dispatch_c(p.kb, p.kprod, p.vgroup, p.vb, m, p.smem, s, &e)) return e;
+        if (mmadec::dispatch_a(p.kb, p.kprod, p.vgroup, p.vb, m, p.smem, s, step, &e)) return e;
+        if (mmadec::dispatch_b(p.kb, p.kprod, p.vgroup, p.vb, m, p.smem, s, step, &e)) return e;
+        if (mmadec::dispatch_c(p.kb, p.kprod, p.vgroup, p.vb, m, p.smem, s, step, &e)) return e;
         return cudaErrorInvalidValue;
     }
     switch (a.kc.D) {

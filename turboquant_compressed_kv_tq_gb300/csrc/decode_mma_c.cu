@@ -5,25 +5,25 @@ namespace tq {
 namespace mmadec {
 
 bool dispatch_c(int kb, bool prod, bool vgroup, int vb, const MmaArgs& m, size_t smem, cudaStream_t s,
-                cudaError_t* err) {
+                const EncodeAppendArgs* step, cudaError_t* err) {
     if (kb == 4 && prod == false && vgroup == false && vb == 2) {
-        *err = launch_mma<4, false, false, 2>(m, smem, s);
+        *err = launch_mma<4, false, false, 2>(m, smem, s, step);
         return true;
     }
     if (kb == 4 && prod == false && vgroup == false && vb == 3) {
-        *err = launch_mma<4, false, false, 3>(m, smem, s);
+        *err = launch_mma<4, false, false, 3>(m, smem, s, step);
         return true;
     }
     if (kb == 4 && prod == false && vgroup == false && vb == 4) {
-        *err = launch_mma<4, false, false, 4>(m, smem, s);
+        *err = launch_mma<4, false, false, 4>(m, smem, s, step);
         return true;
     }
     if (kb == 4 && prod == false && vgroup == true && vb == 2) {
-        *err = launch_mma<4, false, true, 2>(m, smem, s);
+        *err = launch_mma<4, false, true, 2>(m, smem, s, step);
         return true;
     }
     if (kb == 4 && prod == false && vgroup == true && vb == 4) {
-        *err = launch_mma<4, false, true, 4>(m, smem, s);
+        *err = launch_mma<4, false, true, 4>(m, smem, s, step);
         return true;
     }
     return false;

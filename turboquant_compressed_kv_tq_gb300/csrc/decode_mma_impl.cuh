@@ -118,13 +118,13 @@ __device__ __forceinline__ void q_gemm(QSmem& sm, const uint16_t (*T)[kD * kD], 
     }
 }
 
+// Persistent query prep over the units (sequence x kv head, row group): CTA
+// `cta` of `ncta` takes units cta, cta + ncta, ...; the tables are staged once
+// per CTA by one bulk copy; per unit q' = Q R^T and q'' = q' S^T for the 16
+// rows on the tensor cores, both operands split into fp16 hi + lo (about 22
+// significant bits). Runs in a block of kQThreads threads.
 template <int KB>
-__global__ void __launch_bounds__(kQThreads) qfrag_kernel(MmaArgs m) {
-    // persistent CTAs over the units (sequence x kv head, row group): the
-    // tables are staged once per CTA by one bulk copy; per unit q' = Q R^T and
-    // q'' = q' S^T for the 16 rows on the tensor cores, both operands split
-    // into fp16 hi + lo (about 22 significant bits)
-    extern __shared__ __align__(16) unsigned char qsm_raw[];
+__device__ __forceinline__ void qfrag_body(const MmaArgs& m, unsigned char* qsm_raw, int cta, int ncta) {
     QSmem& sm = *reinterpret_cast<QSmem*>(qsm_raw);
     const DecodeArgs& a = m.a;
     const bool prod = a.kc.mode == TQ_MODE_PROD;
@@ -141,7 +141,7 @@ __global__ void __launch_bounds__(kQThreads) qfrag_kernel(MmaArgs m) {
         if (prod) bulk_g2s(sm.S, a.kc.Stc, 2 * kD * kD * 2, &sm.bar);
     }
     bool first = true;
-    for (int unit = blockIdx.x; unit < units; unit += gridDim.x) {
+    for (int unit = cta; unit < units; unit += ncta) {
         const int bh = unit / RG, rg = unit % RG;
         const int b = bh / Hkv, h = bh % Hkv;
         // query rows (fp32) into q2 as scratch, and each row's scale exponent
@@ -219,6 +219,12 @@ __global__ void __launch_bounds__(kQThreads) qfrag_kernel(MmaArgs m) {
         (void)mbar_wait(&sm.bar, 0);
     }
     if (tid == 0) mbar_inval(&sm.bar);
+}
+
+template <int KB>
+__global__ void __launch_bounds__(kQThreads) qfrag_kernel(MmaArgs m) {
+    extern __shared__ __align__(16) unsigned char qsm_raw[];
+    qfrag_body<KB>(m, qsm_raw, blockIdx.x, gridDim.x);
 }
 
 // CTAs of the query-prep kernel: one per unit up to one per SM.
@@ -376,7 +382,7 @@ __global__ void __launch_bounds__(kThreads, 1) split_mma_kernel(MmaArgs m) {
     unsigned char* ring = smem + static_cast<size_t>(warp) * kStages * st.bytes;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + st.bar_off) + warp * kStages;
 
-    const int N = a.seq_lens[b];
+    const int N = a.seq_lens[b] + a.len_add;
     const bool bad = N < a.Lq || N > a.max_blocks * BT;
     if (bad && split == 0 && threadIdx.x == 0 && rg == 0 && h == 0) atomicOr(a.err, TQ_DEVERR_SEQLEN);
     const int t_begin = split * a.plan.chunk;
@@ -458,12 +464,18 @@ __global__ void __launch_bounds__(kThreads, 1) split_mma_kernel(MmaArgs m) {
             bulk_g2s_once(dst + s_off, base + s_src + static_cast<int64_t>(slot0) * s_field, TT * s_field, bar, pol);
     };
 
+    // First stages: fetched before waiting for the kernel this one may overlap,
+    // unless that kernel also appended this step's tokens (then the records it
+    // wrote are visible only after the wait).
     const int pre = my_n < kStages - 1 ? my_n : kStages - 1;
-    for (int i = 0; i < pre; ++i) issue(i);
+    if (a.len_add == 0)
+        for (int i = 0; i < pre; ++i) issue(i);
     // query fragments of this unit, shared by all warps: [2][8][32] uint4
     // (written by the query-prep kernel this one may overlap: wait for it)
     const uint4* qsm = reinterpret_cast<const uint4*>(smem + st.qs_off);
     tc::grid_wait_prior();
+    if (a.len_add != 0)
+        for (int i = 0; i < pre; ++i) issue(i);
     {
         const uint4* qf = m.qfrag + static_cast<int64_t>(unit) * 2 * 8 * 32;
         uint4* qd = reinterpret_cast<uint4*>(smem + st.qs_off);
@@ -751,8 +763,12 @@ __global__ void __launch_bounds__(kThreads, 1) split_mma_kernel(MmaArgs m) {
     merge_unit<VGROUP>(m, unit, split, rg, b, h, cm, tid);
 }
 
+// Query prep fused with the short encode of a decode step's new tokens
+// (decode_step.cu): one launch in place of the append and the query prep.
+cudaError_t launch_step_prep(int kb, const MmaArgs& m, const EncodeAppendArgs& e, cudaStream_t s);
+
 template <int KB, bool KPROD, bool VGROUP, int VB>
-cudaError_t launch_mma(const MmaArgs& m, size_t smem, cudaStream_t s) {
+cudaError_t launch_mma(const MmaArgs& m, size_t smem, cudaStream_t s, const EncodeAppendArgs* step) {
     const DecodeArgs& a = m.a;
     static std::atomic<uint64_t> attr_set{0};
     static std::atomic<int> max_dyn[64];
@@ -778,6 +794,16 @@ cudaError_t launch_mma(const MmaArgs& m, size_t smem, cudaStream_t s) {
         max_dyn[dev & 63].store(optin - static_cast<int>(fa.sharedSizeBytes));
     }
     if (static_cast<int>(smem) > max_dyn[dev & 63].load()) return cudaErrorInvalidValue;
+    const int RG = a.plan.row_groups;
+    cudaError_t e = cudaSuccess;
+    if (step) {
+        e = launch_step_prep(KB, m, *step, s);
+        if (e != cudaSuccess) return e;
+        e = launch_overlapped(split_mma_kernel<KB, KPROD, VGROUP, VB>, dim3(a.plan.splits, a.pool.Hkv * RG, a.batch),
+                              dim3(kThreads), smem, s, m);
+        g_launches.fetch_add(1, std::memory_order_relaxed);
+        return e;
+    }
     static std::atomic<uint64_t> qattr_set{0};
     if (!(qattr_set.load() & bit)) {
         cudaError_t e = cudaFuncSetAttribute(qfrag_kernel<KB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -788,9 +814,8 @@ cudaError_t launch_mma(const MmaArgs& m, size_t smem, cudaStream_t s) {
         }
         qattr_set.fetch_or(bit);
     }
-    const int RG = a.plan.row_groups;
-    cudaError_t e = launch_overlapped(qfrag_kernel<KB>, dim3(qfrag_grid(a.batch * a.pool.Hkv * RG)), dim3(kQThreads),
-                                      sizeof(QSmem), s, m);
+    e = launch_overlapped(qfrag_kernel<KB>, dim3(qfrag_grid(a.batch * a.pool.Hkv * RG)), dim3(kQThreads),
+                          sizeof(QSmem), s, m);
     g_launches.fetch_add(1, std::memory_order_relaxed);
     if (e != cudaSuccess) return e;
     e = launch_overlapped(split_mma_kernel<KB, KPROD, VGROUP, VB>, dim3(a.plan.splits, a.pool.Hkv * RG, a.batch),

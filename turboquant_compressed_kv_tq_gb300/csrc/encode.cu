@@ -17,6 +17,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include "encode_short.cuh"
 #include "tc_ptx.cuh"
 #include "tq_internal.h"
 
@@ -32,12 +33,6 @@ struct VecSmem {
     __half gscale[kMaxD / 8];
     __half gmin[kMaxD / 8];
 };
-
-__device__ __forceinline__ float load_elem(const void* p, int dtype, int64_t i) {
-    if (dtype == TQ_F32) return static_cast<const float*>(p)[i];
-    if (dtype == TQ_BF16) return __bfloat162float(static_cast<const __nv_bfloat16*>(p)[i]);
-    return __half2float(static_cast<const __half*>(p)[i]);
-}
 
 // Record destinations for one vector. Unused pointers are null.
 struct RecordOut {
@@ -201,159 +196,25 @@ __global__ void quantize_kernel(QuantizeArgs a) {
     encode_vector(cd, sm, o);
 }
 
-// Short appends (decode steps, n_new < 32) of rotated codecs, head_dim <= 128:
-// one CTA per (head, sequence, tensor) encodes all NV >= n_new vectors with one
-// thread per coordinate. The transposed rotation (and QJL matrix) is staged in
-// shared memory by one bulk copy, so the specification's sequential fma chains
-// (identical order, bit-exact with encode_vector) run at shared-memory latency,
-// NV independent chains per thread.
+// Short appends: the body lives in encode_short.cuh (shared with the fused
+// decode-step preparation kernel).
 template <int D, int NV>
 __global__ void __launch_bounds__(D) encode_short_kernel(EncodeAppendArgs a) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
-    const int h = blockIdx.x, bq = blockIdx.y, is_v = blockIdx.z;
-    const CodecDev& cd = is_v ? a.vc : a.kc;
-    const bool prod = cd.mode == TQ_MODE_PROD;
-    float* Rt = reinterpret_cast<float*>(smem_raw);        // [D][D]
-    float* St = Rt + D * D;                                 // [D][D] (prod)
-    float* xs = St + (prod ? D * D : 0);                    // [NV][D]
-    float* rs = xs + NV * D;                                // [NV][D] residuals (prod)
-    float* ns = rs + NV * D;                                // [NV] norms
-    uint64_t* bar = reinterpret_cast<uint64_t*>(ns + NV);  // 8-byte aligned (NV even)
-    unsigned char* codes = reinterpret_cast<unsigned char*>(bar + 1);  // [NV][D]
-    const int i = threadIdx.x;
-    const int n = a.n_new;
-    // the next kernel may start its prologue now; this grid completes only
-    // after the grid before it has (the wait at the end), so completion still
-    // orders everything earlier in the stream
-    tc::grid_release_dependents();
-
-    if (i == 0) {
-        tc::mbar_init(bar, 1);
-        tc::mbar_fence_init();
-        tc::mbar_expect_tx(bar, (prod ? 2u : 1u) * D * D * 4u);
-        tc::bulk_g2s(Rt, cd.Rt, D * D * 4, bar);
-        if (prod) tc::bulk_g2s(St, cd.St, D * D * 4, bar);
-    }
-    const void* src = is_v ? a.v : a.k;
-    const int64_t base = (static_cast<int64_t>(bq) * a.pool.Hkv + h) * n * D;
-#pragma unroll
-    for (int v = 0; v < NV; ++v) xs[v * D + i] = v < n ? load_elem(src, a.dtype, base + v * D + i) : 0.0f;
-    __syncthreads();
-    if (i < n) {
-        float n2 = 0.0f;
-        for (int k = 0; k < D; ++k) n2 = __fmaf_rn(xs[i * D + k], xs[i * D + k], n2);
-        ns[i] = __fsqrt_rn(n2);
-    }
-    const bool ok = tc::mbar_wait(bar, 0);
-    if (__syncthreads_or(!ok)) {
-        if (i == 0) atomicOr(a.err, TQ_DEVERR_TIMEOUT);
-        (void)tc::mbar_wait(bar, 0);  // the copy may still land: bounded second wait
-        tc::grid_wait_prior();
-        return;
-    }
-
-    // rotation: NV chains, each in ascending k
-    float acc[NV];
-#pragma unroll
-    for (int v = 0; v < NV; ++v) acc[v] = 0.0f;
-#pragma unroll 4
-    for (int k = 0; k < D; ++k) {
-        const float rt = Rt[k * D + i];
-#pragma unroll
-        for (int v = 0; v < NV; ++v) acc[v] = __fmaf_rn(rt, xs[v * D + k], acc[v]);
-    }
-    const int b = cd.ib;
-    const int nm = (1 << b) - 1;
-#pragma unroll
-    for (int v = 0; v < NV; ++v) {
-        const float nv = ns[v < n ? v : 0];
-        const float y = (nv > 0.0f) ? __fdiv_rn(acc[v], nv) : 0.0f;
-        int code = 0;
-        for (int j = 0; j < nm; ++j) code += (y > __ldg(cd.m + j)) ? 1 : 0;
-        codes[v * D + i] = static_cast<unsigned char>(code);
-        if (prod) rs[v * D + i] = __fsub_rn(y, __ldg(cd.c + code));
-    }
-    __syncthreads();
-
-    // destinations (per vector; out-of-range positions are flagged and skipped)
-    const int BT = a.pool.BT;
-    auto sub_of = [&](int v, int& slot) -> char* {
-        const int pos = a.seq_lens[bq] + v;
-        const int lb = pos / BT;
-        slot = pos - lb * BT;
-        if (pos < 0 || lb >= a.max_blocks) {
-            if (i == 0 && !is_v) atomicOr(a.err, TQ_DEVERR_CAPACITY);
-            return nullptr;
-        }
-        const int64_t pb = a.table ? static_cast<int64_t>(a.table[static_cast<int64_t>(bq) * a.max_blocks + lb])
-                                   : static_cast<int64_t>(bq) * a.max_blocks + lb;
-        if (pb < 0 || pb >= a.pool.num_blocks) {
-            if (i == 0 && !is_v) atomicOr(a.err, TQ_DEVERR_BLOCK);
-            return nullptr;
-        }
-        return a.pool.base + (pb * a.pool.Hkv + h) * a.pool.sub_bytes;
-    };
-    const int64_t o_idx = is_v ? a.pool.off[4] : a.pool.off[0];
-    const int64_t o_norm = is_v ? a.pool.off[5] : a.pool.off[2];
-
-    float z[NV];
-    if (prod) {
-#pragma unroll
-        for (int v = 0; v < NV; ++v) z[v] = 0.0f;
-#pragma unroll 4
-        for (int k = 0; k < D; ++k) {
-            const float st = St[k * D + i];
-#pragma unroll
-            for (int v = 0; v < NV; ++v) z[v] = __fmaf_rn(st, rs[v * D + k], z[v]);
-        }
-    }
-    // residual norms: thread v chains vector v (ascending k)
-    float g2 = 0.0f;
-    if (prod && i < n)
-        for (int k = 0; k < D; ++k) g2 = __fmaf_rn(rs[i * D + k], rs[i * D + k], g2);
-    const int W = cd.W;
-    for (int v = 0; v < n; ++v) {
-        int slot = 0;
-        char* sub = sub_of(v, slot);
-        if (prod) {
-            const unsigned bal = __ballot_sync(0xffffffffu, z[v] >= 0.0f);
-            if (sub && (i & 31) == 0) reinterpret_cast<uint32_t*>(sub + a.pool.off[1])[static_cast<int64_t>(slot) * cd.Ws + (i >> 5)] = bal;
-        }
-        if (!sub) continue;
-        if (i < W) {
-            const int bit0 = 32 * i;
-            const int first = bit0 / b;
-            int last = (bit0 + 31) / b;
-            if (last > D - 1) last = D - 1;
-            uint32_t word = 0;
-            for (int c = first; c <= last; ++c) {
-                const int sh = c * b - bit0;
-                const uint32_t cv = codes[v * D + c];
-                word |= (sh >= 0) ? (cv << sh) : (cv >> (-sh));
-            }
-            reinterpret_cast<uint32_t*>(sub + o_idx)[static_cast<int64_t>(slot) * W + i] = word;
-        }
-        if (i == D - 1) reinterpret_cast<float*>(sub + o_norm)[slot] = ns[v];
-        if (prod && i == v) reinterpret_cast<float*>(sub + a.pool.off[3])[slot] = __fsqrt_rn(g2);
-    }
-    __syncthreads();
-    if (i == 0) tc::mbar_inval(bar);
-    tc::grid_wait_prior();
+    encode_short_body<D, NV>(a, blockIdx.x, blockIdx.y, blockIdx.z, smem_raw);
 }
 
 template <int D, int NV>
 cudaError_t launch_short(const EncodeAppendArgs& a, bool values_rotated, cudaStream_t s) {
     const bool two = a.kc.mode == TQ_MODE_PROD || (values_rotated && a.vc.mode == TQ_MODE_PROD);
-    const size_t tab = static_cast<size_t>(D) * D * 4;
-    const size_t rest = static_cast<size_t>(2 * NV * D + NV) * 4 + 8 + static_cast<size_t>(NV) * D;
-    const size_t smem = (two ? 2 : 1) * tab + rest;  // the larger of the key and value layouts
+    const size_t smem = encode_short_smem<D, NV>(two);
     static std::atomic<uint64_t> attr_set{0};
     int dev = 0;
     cudaGetDevice(&dev);
     const uint64_t bit = 1ull << (dev & 63);
     if (!(attr_set.load() & bit)) {
         cudaError_t e = cudaFuncSetAttribute(encode_short_kernel<D, NV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(2 * tab + rest));
+                                             static_cast<int>(encode_short_smem<D, NV>(true)));
         if (e != cudaSuccess) {
             (void)cudaGetLastError();
             return e;

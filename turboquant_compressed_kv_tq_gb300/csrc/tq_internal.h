@@ -112,6 +112,7 @@ struct DecodeArgs {
     int q_dtype;
     int batch, Hq, Lq, G;
     const int32_t* seq_lens;
+    int len_add;   // tokens appended in the same step: sequence b attends seq_lens[b] + len_add
     const int32_t* table;
     int max_blocks;
     float scale;
@@ -152,7 +153,9 @@ cudaError_t launch_encode_block(const EncodeAppendArgs& a, int is_v, cudaStream_
 bool encode_tc_supported(const EncodeAppendArgs& a, int is_v);
 cudaError_t launch_encode_tc(const EncodeAppendArgs& a, int is_v, cudaStream_t s);
 cudaError_t launch_quantize(const QuantizeArgs& a, cudaStream_t s);
-cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);
+// `step` (tensor-core path only): the decode step's append, fused into the
+// query-prep launch; null for a plain decode.
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s, const EncodeAppendArgs* step = nullptr);
 cudaError_t launch_copy_blocks(const tq_cache_desc* src, const tq_cache_desc* dst, const int32_t* src_ids,
                                const int32_t* dst_ids, int n, unsigned* err, cudaStream_t s);
 namespace mmadec {
