@@ -179,6 +179,25 @@ __global__ void __launch_bounds__(kEncThreads, 1)
     const CodecDev& cd = is_v ? a.vc : a.kc;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t sbase = tc::smem_addr(smem);
+    const int Hkv = a.pool.Hkv;
+    const int64_t ntiles = static_cast<int64_t>(a.batch) * Hkv * tiles_per_seq;
+    const int n_it = blockIdx.x < ntiles ? static_cast<int>((ntiles - 1 - blockIdx.x) / gridDim.x + 1) : 0;
+    auto tile_of = [&](int it) { return static_cast<int64_t>(blockIdx.x) + static_cast<int64_t>(it) * gridDim.x; };
+    // The input rows of a tile are contiguous: thread 0 prefetches a tile's
+    // rows into L2 one tile ahead of the producers (the first at launch, while
+    // the prologue and the previous kernel's tail run).
+    const char* src = static_cast<const char*>(is_v ? a.v : a.k);
+    auto prefetch_tile = [&](int it) {
+        if (tid != 0 || it >= n_it) return;
+        const int64_t tile = tile_of(it);
+        const int ts = static_cast<int>(tile % tiles_per_seq);
+        const int bh = static_cast<int>(tile / tiles_per_seq);
+        const int t0 = ts * kTileRows;
+        const int rows = a.n_new - t0 < kTileRows ? a.n_new - t0 : kTileRows;
+        tc::bulk_prefetch_l2(src + (static_cast<int64_t>(bh) * a.n_new + t0) * D * 2,
+                             static_cast<unsigned>(rows) * D * 2);
+    };
+    prefetch_tile(0);
     // the next kernel (the other tensor's encode, the next chunk's) shares no
     // data with this one: it may take SMs as they free up at this launch's
     // tail; this kernel completes only after its predecessor (wait at exit)
@@ -216,17 +235,13 @@ __global__ void __launch_bounds__(kEncThreads, 1)
     const uint32_t tmem = *s_tmem;
     const bool tables_failed = __syncthreads_or(!tc::mbar_wait(&bars[kBarTab], 0));
 
-    const int Hkv = a.pool.Hkv;
-    const int64_t ntiles = static_cast<int64_t>(a.batch) * Hkv * tiles_per_seq;
-    const int n_it = blockIdx.x < ntiles ? static_cast<int>((ntiles - 1 - blockIdx.x) / gridDim.x + 1) : 0;
-    auto tile_of = [&](int it) { return static_cast<int64_t>(blockIdx.x) + static_cast<int64_t>(it) * gridDim.x; };
     bool failed = tables_failed;
 
     if (warp < kProdWarps) {
         // ---------------- producers: norm (sequential order) and X~ of one token
-        const char* src = static_cast<const char*>(is_v ? a.v : a.k);
         const int row = tid;
         for (int it = 0; it < n_it && !failed; ++it) {
+            prefetch_tile(it + 1);
             const int64_t tile = tile_of(it);
             const int ts = static_cast<int>(tile % tiles_per_seq);
             const int bh = static_cast<int>(tile / tiles_per_seq);

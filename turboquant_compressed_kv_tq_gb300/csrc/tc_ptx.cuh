@@ -60,6 +60,12 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, unsigned parity) {
 
 // 1-D bulk copy global -> shared, completion counted on `bar` (bytes and both
 // addresses multiples of 16).
+// Bulk prefetch of a contiguous global range into L2 (16-byte aligned start,
+// size a multiple of 16); no completion to wait for.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, unsigned bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;\n" ::"l"(src), "r"(bytes) : "memory");
+}
+
 __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, unsigned bytes, uint64_t* bar) {
     asm volatile(
         "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(
