@@ -289,7 +289,7 @@ def test_empty_batch_is_noop():
 
 
 KEYS = [("prod", 2), ("prod", 3), ("prod", 4), ("mse", 2), ("mse", 3), ("mse", 4)]
-VALUES = [("mse", 2), ("mse", 3), ("mse", 4), ("group", 2, 32), ("group", 4, 64), ("group", 4, 128)]
+VALUES = [("mse", 2), ("mse", 3), ("mse", 4), ("group", 2, 32), ("group", 4, 32), ("group", 4, 64), ("group", 4, 128)]
 
 
 @pytest.mark.parametrize("key", KEYS)

@@ -382,36 +382,51 @@ DecodePlan make_decode_plan(const tq_cache_desc* d, int batch, int G, int Lq, in
     const int64_t units = static_cast<int64_t>(batch) * Hkv * p.row_groups;
     if (mma_supported(d, p)) {
         p.kind = 1;
-        p.tile = d->block_tokens < mmadec::kMaxTile ? d->block_tokens : mmadec::kMaxTile;
-        choose_splits(p, units, num_sms, max_seq_len, p.tile, 16384);
-        int o = 0;
-        for (int k = 0; k < 7; ++k) {
-            const int64_t so = d->stream_offset[k];
-            int64_t next = d->subblock_bytes;
-            for (int k2 = k + 1; k2 < 7; ++k2)
-                if (d->stream_offset[k2] >= 0) { next = d->stream_offset[k2]; break; }
-            if (so < 0) {
-                p.st_off[k] = -1;
-                p.st_field[k] = 0;
-                continue;
+        // stage layout for a tile size; the tile halves (down to 16 tokens)
+        // while the split kernel's shared memory would exceed the budget
+        auto layout = [&](int tile) {
+            p.tile = tile;
+            int o = 0;
+            for (int k = 0; k < 7; ++k) {
+                const int64_t so = d->stream_offset[k];
+                int64_t next = d->subblock_bytes;
+                for (int k2 = k + 1; k2 < 7; ++k2)
+                    if (d->stream_offset[k2] >= 0) { next = d->stream_offset[k2]; break; }
+                if (so < 0) {
+                    p.st_off[k] = -1;
+                    p.st_field[k] = 0;
+                    continue;
+                }
+                p.st_field[k] = static_cast<int>((next - so) / d->block_tokens);
+                p.st_off[k] = o;
+                o += p.tile * p.st_field[k];
             }
-            p.st_field[k] = static_cast<int>((next - so) / d->block_tokens);
-            p.st_off[k] = o;
-            o += p.tile * p.st_field[k];
+            p.st_bytes = (o + 127) / 128 * 128;
+            const size_t ring = static_cast<size_t>(mmadec::kWarps) * mmadec::kStages * p.st_bytes;
+            p.qs_off = static_cast<int>(ring);
+            size_t ringq = ring + mmadec::kQFragBytes;
+            p.vt_off = -1;
+            if (!p.vgroup && p.vb == 3) {  // pair table of 3-bit value codes (aligned inside the region)
+                p.vt_off = static_cast<int>(ringq);
+                ringq += mmadec::kVPairRegion;
+            }
+            p.kt_off = -1;
+            if (mmadec::quad_keys(p.kb, p.kprod, p.vgroup)) {  // quad table of 2-bit key codes
+                p.kt_off = static_cast<int>(ringq);
+                ringq += mmadec::kKQuadBytes;
+            }
+            const size_t combine = sizeof(float) * (2 * mmadec::kWarps * kRows + mmadec::kWarps * kRows * (D + 1));
+            const size_t body = ((ringq > combine ? ringq : combine) + 127) / 128 * 128;
+            p.bar_off = static_cast<int>(body);
+            p.smem = body + sizeof(uint64_t) * mmadec::kWarps * mmadec::kStages;
+        };
+        int tile = d->block_tokens < mmadec::kMaxTile ? d->block_tokens : mmadec::kMaxTile;
+        layout(tile);
+        while (p.smem > mmadec::kSmemBudget && tile > 16) {
+            tile /= 2;
+            layout(tile);
         }
-        p.st_bytes = (o + 127) / 128 * 128;
-        const size_t ring = static_cast<size_t>(mmadec::kWarps) * mmadec::kStages * p.st_bytes;
-        p.qs_off = static_cast<int>(ring);
-        size_t ringq = ring + mmadec::kQFragBytes;
-        p.vt_off = -1;
-        if (!p.vgroup && p.vb == 3) {  // pair table of 3-bit value codes (aligned inside the region)
-            p.vt_off = static_cast<int>(ringq);
-            ringq += mmadec::kVPairRegion;
-        }
-        const size_t combine = sizeof(float) * (2 * mmadec::kWarps * kRows + mmadec::kWarps * kRows * (D + 1));
-        const size_t body = ((ringq > combine ? ringq : combine) + 127) / 128 * 128;
-        p.bar_off = static_cast<int>(body);
-        p.smem = body + sizeof(uint64_t) * mmadec::kWarps * mmadec::kStages;
+        choose_splits(p, units, num_sms, max_seq_len, p.tile, 16384);
         p.q_bytes = al256(static_cast<size_t>(units) * 2 * 8 * 32 * 16);
         p.cnt_bytes = al256(static_cast<size_t>(units) * sizeof(unsigned));
     } else {
@@ -437,6 +452,7 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s, const EncodeAppen
         m.st.bar_off = a.plan.bar_off;
         m.st.qs_off = a.plan.qs_off;
         m.st.vt_off = a.plan.vt_off;
+        m.st.kt_off = a.plan.kt_off;
         for (int k = 0; k < 7; ++k) {
             m.st.off[k] = a.plan.st_off[k];
             m.st.field[k] = a.plan.st_field[k];

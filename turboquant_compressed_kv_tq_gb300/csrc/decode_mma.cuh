@@ -38,12 +38,20 @@ constexpr int kThreads = kWarps * 32;
 constexpr int kStages = 2;
 constexpr int kRows = 16;
 constexpr int kMaxTile = 64;
+// Dynamic shared memory the split kernel may use: the 227 KB per-block opt-in
+// of the GPU less a margin for its static shared memory.
+constexpr size_t kSmemBudget = 227 * 1024 - 1024;
 constexpr int kQFragBytes = 2 * 8 * 32 * 16;  // query fragments of one unit
 constexpr unsigned kSpinLimit = 1u << 22;
 // Pair table of 3-bit value codes: 64 entries x 32 bank copies x 4 bytes,
 // placed at an 8 KB-aligned shared address inside a 16 KB region.
 constexpr int kVPairBytes = 64 * 32 * 4;
 constexpr int kVPairRegion = 2 * kVPairBytes;
+// Quad table of 2-bit key codes: 256 entries x 16 bank copies x 8 bytes. Used
+// for 2-bit key indices except with prod keys and group values, whose records
+// leave no room for it next to the 64-token stages.
+constexpr int kKQuadBytes = 256 * 16 * 8;
+__host__ __device__ constexpr bool quad_keys(int kb, bool kprod, bool vgroup) { return kb == 2 && !(kprod && vgroup); }
 
 // ------------------------------------------------------------------ PTX helpers
 
@@ -378,6 +386,32 @@ __device__ __forceinline__ void pair3_chunk(const uint32_t* w, uint32_t lane_add
         else if (off >= 7) f = w[wi] >> (off - 7);
         else f = shl_f(w[wi], 7 - off);
         h[p] = lds_u32((f & 0x1F80u) | lane_addr);
+    }
+}
+
+// 2-bit codes through a shared-memory table of code quads: entry e (one byte
+// of codes, four coordinates) holds the fp16 pairs (c[e & 3], c[(e >> 2) & 3])
+// and (c[(e >> 4) & 3], c[e >> 6]); the copy for lane L of entry e sits at byte
+// 128 e + 8 (L % 16), so each half-warp's 64-bit loads hit 16 different bank
+// pairs. `lane_addr` is the table's shared address + 8 (L % 16). Byte k of word
+// hw of the chunk gives pairs 8 hw + 2k and 8 hw + 2k + 1, i.e. coordinates in
+// natural order (pair p = coordinates 2p, 2p + 1).
+__device__ __forceinline__ uint2 lds_u64(uint32_t addr) {
+    uint2 v;
+    asm("ld.shared.v2.u32 {%0, %1}, [%2];\n" : "=r"(v.x), "=r"(v.y) : "r"(addr));
+    return v;
+}
+
+__device__ __forceinline__ void quad2_chunk(const uint32_t* w, uint32_t lane_addr, uint32_t (&h)[16]) {
+#pragma unroll
+    for (int hw = 0; hw < 2; ++hw) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const uint32_t f = k == 0 ? shl_f(w[hw], 7) : (w[hw] >> (8 * k - 7));
+            const uint2 v = lds_u64(mad_lo(f & 0x7F80u, kDc.pow2[0], lane_addr));
+            h[8 * hw + 2 * k] = v.x;
+            h[8 * hw + 2 * k + 1] = v.y;
+        }
     }
 }
 

@@ -29,6 +29,7 @@ struct StageLayout {
     int bar_off;            // byte offset of the mbarriers (past ring and merge areas)
     int qs_off;             // byte offset of the query fragments (past the ring)
     int vt_off;             // byte offset of the value pair table region (-1: none)
+    int kt_off;             // byte offset of the key quad table (-1: none)
 };
 
 struct MmaArgs {
@@ -123,7 +124,9 @@ __device__ __forceinline__ void q_gemm(QSmem& sm, const uint16_t (*T)[kD * kD], 
 // per CTA by one bulk copy; per unit q' = Q R^T and q'' = q' S^T for the 16
 // rows on the tensor cores, both operands split into fp16 hi + lo (about 22
 // significant bits). Runs in a block of kQThreads threads.
-template <int KB>
+// NAT: 2-bit key codes in natural pair order (the split kernel's quad-table
+// decoder) instead of the byte-permute decoder's order.
+template <int KB, bool NAT = false>
 __device__ __forceinline__ void qfrag_body(const MmaArgs& m, unsigned char* qsm_raw, int cta, int ncta) {
     QSmem& sm = *reinterpret_cast<QSmem*>(qsm_raw);
     const DecodeArgs& a = m.a;
@@ -202,7 +205,12 @@ __device__ __forceinline__ void qfrag_body(const MmaArgs& m, unsigned char* qsm_
             const int reg = 2 * ee + (rr >= 8 ? 1 : 0);
             int pa, pb;
             const bool qjl = which && prod;
-            mse_pair(qjl ? 1 : KB, 2 * ks + ee, pa, pb);
+            if (NAT && !qjl) {
+                pa = 2 * (2 * ks + ee);
+                pb = pa + 1;
+            } else {
+                mse_pair(qjl ? 1 : KB, 2 * ks + ee, pa, pb);
+            }
             const float* q = qjl ? sm.q2[rr] : sm.q1[rr];
             const float sc = qjl ? s2 : s1;
             float va = q[32 * j + pa] * sc, vb = q[32 * j + pb] * sc;
@@ -221,10 +229,10 @@ __device__ __forceinline__ void qfrag_body(const MmaArgs& m, unsigned char* qsm_
     if (tid == 0) mbar_inval(&sm.bar);
 }
 
-template <int KB>
+template <int KB, bool NAT = false>
 __global__ void __launch_bounds__(kQThreads) qfrag_kernel(MmaArgs m) {
     extern __shared__ __align__(16) unsigned char qsm_raw[];
-    qfrag_body<KB>(m, qsm_raw, blockIdx.x, gridDim.x);
+    qfrag_body<KB, NAT>(m, qsm_raw, blockIdx.x, gridDim.x);
 }
 
 // CTAs of the query-prep kernel: one per unit up to one per SM.
@@ -396,7 +404,21 @@ __global__ void __launch_bounds__(kThreads, 1) split_mma_kernel(MmaArgs m) {
     }
     __syncwarp();
 
-    const auto ktab = mse_table<KB>(a.kc.c);
+    // 2-bit keys decode through the shared quad table, others in registers
+    constexpr bool kQuadTab = quad_keys(KB, KPROD, VGROUP);
+    typename MseTable<KB>::type ktab{};
+    if constexpr (!kQuadTab) ktab = mse_table<KB>(a.kc.c);
+    uint32_t kt_lane = 0;
+    if constexpr (kQuadTab) {
+        kt_lane = smem_u32(smem + st.kt_off) + 8u * (lane & 15);
+        uint2* tab = reinterpret_cast<uint2*>(smem + st.kt_off);
+        for (int i = threadIdx.x; i < 256 * 16; i += kThreads) {
+            const int e = i >> 4;
+            const uint32_t c0 = h_bits(__ldg(a.kc.c + (e & 3))), c1 = h_bits(__ldg(a.kc.c + ((e >> 2) & 3)));
+            const uint32_t c2 = h_bits(__ldg(a.kc.c + ((e >> 4) & 3))), c3 = h_bits(__ldg(a.kc.c + (e >> 6)));
+            tab[i] = make_uint2(c0 | (c1 << 16), c2 | (c3 << 16));
+        }
+    }
     // 3-bit MSE values decode through the shared pair table, others in registers
     constexpr bool kPairTab = !VGROUP && VB == 3;
     typename MseTable<VGROUP ? 2 : VB>::type vtab{};
@@ -534,7 +556,8 @@ __global__ void __launch_bounds__(kThreads, 1) split_mma_kernel(MmaArgs m) {
                 const int tau = 16 * u + 8 * nt + g;
                 uint32_t kw[KB];
                 load_words<KB>(kidx + tau * (4 * KB) + j * KB, kw);
-                mse_chunk<KB>(kw, ktab, hk[nt]);
+                if constexpr (kQuadTab) quad2_chunk(kw, kt_lane, hk[nt]);
+                else mse_chunk<KB>(kw, ktab, hk[nt]);
                 if constexpr (KPROD) {
                     sw[nt] = ksgn[tau * 4 + j];
                         neg2[nt] = dup_half(h_bits(-krn[tau]));
@@ -765,7 +788,7 @@ __global__ void __launch_bounds__(kThreads, 1) split_mma_kernel(MmaArgs m) {
 
 // Query prep fused with the short encode of a decode step's new tokens
 // (decode_step.cu): one launch in place of the append and the query prep.
-cudaError_t launch_step_prep(int kb, const MmaArgs& m, const EncodeAppendArgs& e, cudaStream_t s);
+cudaError_t launch_step_prep(int kb, bool nat, const MmaArgs& m, const EncodeAppendArgs& e, cudaStream_t s);
 
 template <int KB, bool KPROD, bool VGROUP, int VB>
 cudaError_t launch_mma(const MmaArgs& m, size_t smem, cudaStream_t s, const EncodeAppendArgs* step) {
@@ -797,7 +820,7 @@ cudaError_t launch_mma(const MmaArgs& m, size_t smem, cudaStream_t s, const Enco
     const int RG = a.plan.row_groups;
     cudaError_t e = cudaSuccess;
     if (step) {
-        e = launch_step_prep(KB, m, *step, s);
+        e = launch_step_prep(KB, quad_keys(KB, KPROD, VGROUP), m, *step, s);
         if (e != cudaSuccess) return e;
         e = launch_overlapped(split_mma_kernel<KB, KPROD, VGROUP, VB>, dim3(a.plan.splits, a.pool.Hkv * RG, a.batch),
                               dim3(kThreads), smem, s, m);
@@ -806,7 +829,8 @@ cudaError_t launch_mma(const MmaArgs& m, size_t smem, cudaStream_t s, const Enco
     }
     static std::atomic<uint64_t> qattr_set{0};
     if (!(qattr_set.load() & bit)) {
-        cudaError_t e = cudaFuncSetAttribute(qfrag_kernel<KB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaError_t e = cudaFuncSetAttribute(qfrag_kernel<KB, quad_keys(KB, KPROD, VGROUP)>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              static_cast<int>(sizeof(QSmem)));
         if (e != cudaSuccess) {
             (void)cudaGetLastError();
@@ -814,7 +838,8 @@ cudaError_t launch_mma(const MmaArgs& m, size_t smem, cudaStream_t s, const Enco
         }
         qattr_set.fetch_or(bit);
     }
-    e = launch_overlapped(qfrag_kernel<KB>, dim3(qfrag_grid(a.batch * a.pool.Hkv * RG)), dim3(kQThreads),
+    e = launch_overlapped(qfrag_kernel<KB, quad_keys(KB, KPROD, VGROUP)>, dim3(qfrag_grid(a.batch * a.pool.Hkv * RG)),
+                          dim3(kQThreads),
                           sizeof(QSmem), s, m);
     g_launches.fetch_add(1, std::memory_order_relaxed);
     if (e != cudaSuccess) return e;

@@ -13,11 +13,11 @@
 namespace tq {
 namespace mmadec {
 
-template <int KB, int NV>
+template <int KB, int NV, bool NAT>
 __global__ void __launch_bounds__(kQThreads) step_prep_kernel(MmaArgs m, EncodeAppendArgs e, int nq) {
     extern __shared__ __align__(16) unsigned char smem[];
     if (static_cast<int>(blockIdx.x) < nq) {
-        qfrag_body<KB>(m, smem, blockIdx.x, nq);
+        qfrag_body<KB, NAT>(m, smem, blockIdx.x, nq);
         return;
     }
     const int u = blockIdx.x - nq;
@@ -30,7 +30,7 @@ __global__ void __launch_bounds__(kQThreads) step_prep_kernel(MmaArgs m, EncodeA
 
 namespace {
 
-template <int KB, int NV>
+template <int KB, int NV, bool NAT>
 cudaError_t launch_prep(const MmaArgs& m, const EncodeAppendArgs& e, cudaStream_t s) {
     const size_t enc = encode_short_smem<kD, NV>(true);
     const size_t smem = sizeof(QSmem) > enc ? sizeof(QSmem) : enc;
@@ -39,7 +39,7 @@ cudaError_t launch_prep(const MmaArgs& m, const EncodeAppendArgs& e, cudaStream_
     cudaGetDevice(&dev);
     const uint64_t bit = 1ull << (dev & 63);
     if (!(attr_set.load() & bit)) {
-        const cudaError_t r = cudaFuncSetAttribute(step_prep_kernel<KB, NV>,
+        const cudaError_t r = cudaFuncSetAttribute(step_prep_kernel<KB, NV, NAT>,
                                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                    static_cast<int>(smem));
         if (r != cudaSuccess) {
@@ -55,26 +55,28 @@ cudaError_t launch_prep(const MmaArgs& m, const EncodeAppendArgs& e, cudaStream_
     int nq = qfrag_grid(units + ne) - ne;
     if (nq > units) nq = units;
     if (nq < 1) nq = 1;
-    const cudaError_t r = launch_overlapped(step_prep_kernel<KB, NV>, dim3(nq + ne), dim3(kQThreads), smem, s, m, e, nq);
+    const cudaError_t r = launch_overlapped(step_prep_kernel<KB, NV, NAT>, dim3(nq + ne), dim3(kQThreads), smem, s, m, e, nq);
     g_launches.fetch_add(1, std::memory_order_relaxed);
     return r;
 }
 
-template <int KB>
+template <int KB, bool NAT>
 cudaError_t launch_prep_nv(const MmaArgs& m, const EncodeAppendArgs& e, cudaStream_t s) {
-    if (e.n_new <= 2) return launch_prep<KB, 2>(m, e, s);
-    if (e.n_new <= 8) return launch_prep<KB, 8>(m, e, s);
+    if (e.n_new <= 2) return launch_prep<KB, 2, NAT>(m, e, s);
+    if (e.n_new <= 8) return launch_prep<KB, 8, NAT>(m, e, s);
     return cudaErrorInvalidValue;
 }
 
 }  // namespace
 
-cudaError_t launch_step_prep(int kb, const MmaArgs& m, const EncodeAppendArgs& e, cudaStream_t s) {
+// nat: the query fragments in the natural pair order of the quad-table key
+// decoder (2-bit keys only).
+cudaError_t launch_step_prep(int kb, bool nat, const MmaArgs& m, const EncodeAppendArgs& e, cudaStream_t s) {
     switch (kb) {
-        case 1: return launch_prep_nv<1>(m, e, s);
-        case 2: return launch_prep_nv<2>(m, e, s);
-        case 3: return launch_prep_nv<3>(m, e, s);
-        case 4: return launch_prep_nv<4>(m, e, s);
+        case 1: return launch_prep_nv<1, false>(m, e, s);
+        case 2: return nat ? launch_prep_nv<2, true>(m, e, s) : launch_prep_nv<2, false>(m, e, s);
+        case 3: return launch_prep_nv<3, false>(m, e, s);
+        case 4: return launch_prep_nv<4, false>(m, e, s);
         default: return cudaErrorInvalidValue;
     }
 }

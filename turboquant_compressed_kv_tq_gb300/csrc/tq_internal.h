@@ -97,6 +97,7 @@ struct DecodePlan {
     int bar_off;      // shared-memory offset of the stage barriers
     int qs_off;       // shared-memory offset of the query fragments
     int vt_off;       // shared-memory offset of the 3-bit value pair table region (-1: unused)
+    int kt_off;       // shared-memory offset of the 2-bit key quad table (-1: unused)
     size_t smem;      // dynamic shared memory of the split kernel
     size_t q_bytes;   // SIMT: q' and q'' buffers (each); tensor cores: query fragments
     size_t cnt_bytes; // tensor cores: per-unit arrival counters
