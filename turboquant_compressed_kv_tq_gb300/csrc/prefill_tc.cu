@@ -443,15 +443,19 @@ __global__ void __launch_bounds__(kTThreads, 1) prefill_tc_kernel(TcPrefillArgs 
             const int t0 = i * TT;
             float sv[HC];
             tc::tmem_ld16(t_row + ((i & 1) ? kColS1 : kColS0) + HC * cq, sv);
+            // scores relative to the running maximum, y = s * norm - m, in one fused
+            // multiply-add (absolute, m taken as 0, while the row has no maximum yet)
+            const bool first = m == -INFINITY;
+            const float mneg = first ? 0.0f : -m;
             {
                 const float4* k4 = reinterpret_cast<const float4*>(kn + HC * cq);
 #pragma unroll
                 for (int q = 0; q < HC / 4; ++q) {
                     const float4 n4 = k4[q];
-                    sv[4 * q] *= n4.x;
-                    sv[4 * q + 1] *= n4.y;
-                    sv[4 * q + 2] *= n4.z;
-                    sv[4 * q + 3] *= n4.w;
+                    sv[4 * q] = fmaf(sv[4 * q], n4.x, mneg);
+                    sv[4 * q + 1] = fmaf(sv[4 * q + 1], n4.y, mneg);
+                    sv[4 * q + 2] = fmaf(sv[4 * q + 2], n4.z, mneg);
+                    sv[4 * q + 3] = fmaf(sv[4 * q + 3], n4.w, mneg);
                 }
             }
             // a tile whose 64 operand columns are all valid tokens below every
@@ -493,9 +497,12 @@ __global__ void __launch_bounds__(kTThreads, 1) prefill_tc_kernel(TcPrefillArgs 
                 for (int t = 0; t < kTTok; ++t) wmax = fmaxf(wmax, vw[t]);
                 gap = fminf(kRescaleGap, 15.8f - __log2f(wmax));
             }
-            const bool move = mx > m + gap || (m == -INFINITY && mx != -INFINITY);
-            const float alpha = move ? (m == -INFINITY ? 0.0f : ex2(m - mx)) : 1.0f;
-            if (move) m = mx;
+            // mx is the row's largest y: relative to m, or absolute for a first row
+            const bool move = first ? mx != -INFINITY : mx > gap;
+            const float alpha = move ? (first ? 0.0f : ex2(-mx)) : 1.0f;
+            // y - sub is the score relative to the new maximum
+            const float sub = move ? mx : 0.0f;
+            if (move) m = first ? mx : m + mx;
             if (__any_sync(0xffffffffu, move) && o_started) {
                 float v[32];
                 tc::tmem_ld32(tO, v);
@@ -514,22 +521,24 @@ __global__ void __launch_bounds__(kTThreads, 1) prefill_tc_kernel(TcPrefillArgs 
             // the rows kD, kD+1 of V^T divide each rounded P' back by its weight
             // for the row sum, so the rounding of P' cancels in O / l
             const float4* w4 = reinterpret_cast<const float4*>(vw + HC * cq);
+            const bool steady = __all_sync(0xffffffffu, !move && !first);
             uint32_t pw[HC / 2];
 #pragma unroll
             for (int q = 0; q < HC / 4; ++q) {
                 const float4 n4 = w4[q];
                 const int c = 4 * q;
                 float p0, p1, p2, p3;
-                if (open) {   // finite scores, so a finite maximum
-                    p0 = ex2(sv[c] - m);
-                    p1 = ex2(sv[c + 1] - m);
-                    p2 = ex2(sv[c + 2] - m);
-                    p3 = ex2(sv[c + 3] - m);
-                } else {
-                    p0 = m == -INFINITY ? 0.0f : ex2(sv[c] - m);
-                    p1 = m == -INFINITY ? 0.0f : ex2(sv[c + 1] - m);
-                    p2 = m == -INFINITY ? 0.0f : ex2(sv[c + 2] - m);
-                    p3 = m == -INFINITY ? 0.0f : ex2(sv[c + 3] - m);
+                if (steady) {   // no row of the warp moved its maximum or starts here
+                    p0 = ex2(sv[c]);
+                    p1 = ex2(sv[c + 1]);
+                    p2 = ex2(sv[c + 2]);
+                    p3 = ex2(sv[c + 3]);
+                } else {        // a row with no score yet keeps p = 0
+                    const bool none = m == -INFINITY;
+                    p0 = none ? 0.0f : ex2(sv[c] - sub);
+                    p1 = none ? 0.0f : ex2(sv[c + 1] - sub);
+                    p2 = none ? 0.0f : ex2(sv[c + 2] - sub);
+                    p3 = none ? 0.0f : ex2(sv[c + 3] - sub);
                 }
                 pw[2 * q] = pack_half2(p0 * n4.x, p1 * n4.y);
                 pw[2 * q + 1] = pack_half2(p2 * n4.z, p3 * n4.w);
