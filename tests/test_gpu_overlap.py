@@ -29,7 +29,7 @@ def _lib_built():
     assert torch.cuda.is_available()
 
 
-def _run_steps(w, layers, steps, sync_each):
+def _run_steps(w, layers, steps, sync_each, fused=False):
     D, Hkv, Hq, Lq, BT = w.head_dim, w.num_kv_heads, w.num_q_heads, w.q_len, w.block_tokens
     N0, A = w.seq_lens[0], w.append_per_step
     cap = N0 + A * steps
@@ -57,6 +57,10 @@ def _run_steps(w, layers, steps, sync_each):
     for s in range(steps):
         kn, vn, q = ins[s]
         for layer in range(layers):
+            if fused:   # tq_decode_step: the append inside the decode's first launch
+                cache.decode_step(layer, kn[layer], vn[layer], q[layer], pre[s:s + 1], None, nblk, cap,
+                                  outs[s, layer], ws)
+                continue
             cache.append(layer, kn[layer], vn[layer], pre[s:s + 1], None, nblk)
             if sync_each:
                 torch.cuda.synchronize()
@@ -83,3 +87,14 @@ def test_overlapped_steps_equal_serialised_steps():
         for h in (0, 3):
             ref = oracle_decode(w, K[h], V[h], qn[0, h * G:(h + 1) * G])
             compare_decode(fast[steps - 1, layer, 0, h * G:(h + 1) * G], ref)
+
+
+@pytest.mark.parametrize("layers,steps", [(4, 3), (1, 5)])
+def test_overlapped_fused_steps_equal_serialised_steps(layers, steps):
+    """The same steps through tq_decode_step, back to back: bit-identical to the
+    separate calls with a device synchronisation after each (one layer: each
+    step's append follows the previous step's decode of the same cache)."""
+    w = dataclasses.replace(wl.long_256k(), seq_lens=(20000,), prefill_chunk=4096)
+    fused, _ = _run_steps(w, layers, steps, sync_each=False, fused=True)
+    slow, _ = _run_steps(w, layers, steps, sync_each=True)
+    assert np.array_equal(fused.view(np.uint32), slow.view(np.uint32))
