@@ -6,19 +6,23 @@
 // (cp.async.bulk, completion on an mbarrier), and runs, 16 tokens at a time:
 //   scores  S = Q' K_hat^T (+ Q'' sigma^T for prod keys) on mma.sync
 //           m16n8k16 (fp16 operands, fp32 accumulate); the key operand is
-//           decoded from the packed indices straight into MMA fragments with
-//           byte-permute table lookups (no shared-memory round trip);
-//   softmax online, in log2 units (scale * log2(e) folded into the query);
+//           decoded from the packed indices straight into MMA fragments:
+//           2-bit indices through a shared table of code quads (one 64-bit
+//           load per four levels), other widths with byte-permute lookups in
+//           registers; QJL signs as +-gamma fp16 operands;
+//   softmax online, in log2 units (scale * log2(e) folded into the query),
+//           with a lagging row maximum;
 //   values  O += P' V_hat on mma.sync, P' = p * value norm, V_hat decoded per
-//           token into registers and transposed to the MMA operand layout with
-//           movmatrix.
+//           token into registers (3-bit indices through a shared table of
+//           code pairs) and transposed to the MMA operand layout with movmatrix.
 // Warps merge in shared memory; the CTA writes (max, sum, acc) partials and
 // the last CTA of each (sequence, head, row group) merges the splits, applies
 // the inverse value rotation and writes the output.
 //
-// Query fragments are prepared by a separate kernel in the coordinate order the
-// decoders produce (the contraction over head_dim is invariant under a common
-// permutation of both operands).
+// Query fragments are prepared by a separate kernel (or inside the fused
+// decode-step launch) in the coordinate order the decoders produce (the
+// contraction over head_dim is invariant under a common permutation of both
+// operands).
 #pragma once
 
 #include <cuda_bf16.h>
