@@ -65,7 +65,7 @@ def test_tile_edges_every_codec_pair(key, value):
     _check(_workload(key, value, (2, 127, 128, 129, 700), 2, 2, 8, 128))
 
 
-@pytest.mark.parametrize("bt", [128, 256, 512])
+@pytest.mark.parametrize("bt", [16, 32, 128, 256, 512])
 def test_block_sizes_shuffled_pages(bt):
     _check(_workload(("prod", 3), ("mse", 3), (300, 1000, 2049), 1, 2, 4, bt, shuffle=True))
 
@@ -88,7 +88,7 @@ def test_group_values_one_query_row_per_head():
     _check(_workload(("prod", 3), ("group", 4, 64), (129, 3000), 1, 2, 1, 128, shuffle=True))
 
 
-@pytest.mark.parametrize("key,value", [(("prod", 3), ("mse", 3)), (("mse", 4), ("mse", 4))])
+@pytest.mark.parametrize("key,value", [(("prod", 3), ("mse", 3)), (("mse", 4), ("mse", 4)), (("mse", 2), ("mse", 3))])
 def test_stress_vectors(key, value):
     # keys and values with zero rows (zero norms), one-hot rows, constant rows
     # and scales 2^-12 .. 2^12: the decode of those records against the oracle's

@@ -61,6 +61,8 @@ CASES = [
     pytest.param(("mse", 4), ("mse", 4), 128, (37, 100, 16, 3), 2, 2, 4, id="mse4-mse4-fused"),
     pytest.param(("prod", 2), ("mse", 2), 128, (70, 5), 1, 1, 8, id="prod2-mse2-fused-q1"),
     pytest.param(("prod", 4), ("mse", 4), 128, (0, 129, 64), 5, 5, 4, id="prod4-mse4-fused-nv8-empty-seq"),
+    pytest.param(("prod", 3), ("mse", 3), 128, (300, 17, 64), 8, 8, 8, id="prod3-mse3-fused-n8-64rows"),
+    pytest.param(("mse", 2), ("mse", 3), 128, (1000, 48), 2, 2, 8, id="mse2-mse3-fused-quad-pair"),
     # the two calls in order
     pytest.param(("prod", 3), ("group", 4, 64), 128, (37, 100, 16, 3), 2, 2, 4, id="group-values-unfused"),
     pytest.param(("prod", 3), ("mse", 3), 128, (37, 100), 12, 2, 4, id="n12-unfused"),
