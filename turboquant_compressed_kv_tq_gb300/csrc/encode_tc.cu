@@ -352,38 +352,45 @@ __global__ void __launch_bounds__(kEncThreads, 1)
         float creg[4] = {s_c[0], s_c[1], s_c[2], s_c[3]};   // 2-bit codebooks: levels from registers
         const int64_t o_idx = is_v ? a.pool.off[4] : a.pool.off[0];
         const int64_t o_norm = is_v ? a.pool.off[5] : a.pool.off[2];
-        for (int it = 0; it < n_it && !failed; ++it) {
+        // destination of this thread's token of tile it in the pool (null: out of
+        // range, flagged); computed one tile ahead, so that its loads (sequence
+        // length, block table) are in flight while the current tile is processed
+        auto dest_of = [&](int it, char*& sub, int& slot) {
             const int64_t tile = tile_of(it);
-            const int bb = it & 1;
             const int ts = static_cast<int>(tile % tiles_per_seq);
             const int bh = static_cast<int>(tile / tiles_per_seq);
             const int h = bh % Hkv, b = bh / Hkv;
             const int t = ts * kTileRows + row;
-            const bool valid = t < a.n_new;
+            sub = nullptr;
+            slot = 0;
+            if (t >= a.n_new) return;
+            const int pos = a.seq_lens[b] + t;
+            const int BT = a.pool.BT;
+            const int lb = pos / BT;
+            slot = pos - lb * BT;
+            if (pos < 0 || lb >= a.max_blocks) {
+                atomicOr(a.err, TQ_DEVERR_CAPACITY);
+                return;
+            }
+            const int64_t pb = a.table ? static_cast<int64_t>(a.table[static_cast<int64_t>(b) * a.max_blocks + lb])
+                                       : static_cast<int64_t>(b) * a.max_blocks + lb;
+            if (pb < 0 || pb >= a.pool.num_blocks) atomicOr(a.err, TQ_DEVERR_BLOCK);
+            else sub = a.pool.base + (pb * Hkv + h) * a.pool.sub_bytes;
+        };
+        char* sub_next = nullptr;
+        int slot_next = 0;
+        if (n_it > 0) dest_of(0, sub_next, slot_next);
+        for (int it = 0; it < n_it && !failed; ++it) {
+            const int bb = it & 1;
+            char* const sub = sub_next;
+            const int slot = slot_next;
             bool ok = tc::mbar_wait(&bars[kBarYFull + bb], (it >> 1) & 1) &&
                       tc::mbar_wait(&bars[kBarNorm + it % 3], (it / 3) & 1);
             tc::tc_fence_after();
+            if (it + 1 < n_it) dest_of(it + 1, sub_next, slot_next);
             const float n = s_norm[(it % 3) * kTileRows + row];
             const int ex = n > 0.0f ? ilogbf(n) : 0;
             const float inv = n > 0.0f ? __fdiv_rn(scalbnf(1.0f, ex - 4), n) : 0.0f;
-
-            // destination of this token in the pool
-            char* sub = nullptr;
-            int slot = 0;
-            if (valid) {
-                const int pos = a.seq_lens[b] + t;
-                const int BT = a.pool.BT;
-                const int lb = pos / BT;
-                slot = pos - lb * BT;
-                if (pos < 0 || lb >= a.max_blocks) {
-                    atomicOr(a.err, TQ_DEVERR_CAPACITY);
-                } else {
-                    const int64_t pb = a.table ? static_cast<int64_t>(a.table[static_cast<int64_t>(b) * a.max_blocks + lb])
-                                               : static_cast<int64_t>(b) * a.max_blocks + lb;
-                    if (pb < 0 || pb >= a.pool.num_blocks) atomicOr(a.err, TQ_DEVERR_BLOCK);
-                    else sub = a.pool.base + (pb * Hkv + h) * a.pool.sub_bytes;
-                }
-            }
             uint32_t* widx = sub ? reinterpret_cast<uint32_t*>(sub + o_idx) + static_cast<int64_t>(slot) * W : nullptr;
             if constexpr (PROD) ok = ok && tc::mbar_wait(&bars[kBarREmpty], (it & 1) ^ 1);   // residual tiles free
 
