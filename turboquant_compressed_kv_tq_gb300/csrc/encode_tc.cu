@@ -406,14 +406,23 @@ __global__ void __launch_bounds__(kEncThreads, 1)
 #pragma unroll
                 for (int i = 0; i < 32; ++i) {
                     const float y = v[i] * inv;
-                    const int code = lm_index<KB>(y, mreg);
+                    int code;
+                    float cc = 0.0f;   // the index's level (prod keys)
+                    if constexpr (PROD && KB == 2) {
+                        // the index and its level from the same two comparisons
+                        const bool p1 = y > mreg[1];
+                        const bool p0 = y > (p1 ? mreg[2] : mreg[0]);
+                        code = (p1 ? 2 : 0) + (p0 ? 1 : 0);
+                        cc = p1 ? (p0 ? creg[3] : creg[2]) : (p0 ? creg[1] : creg[0]);
+                    } else {
+                        code = lm_index<KB>(y, mreg);
+                    }
                     const int bit = i * KB;
-                    cw[bit >> 5] |= static_cast<uint32_t>(code) << (bit & 31);
+                    cw[bit >> 5] += static_cast<uint32_t>(code) << (bit & 31);   // disjoint bits: a shift-add
                     if ((bit & 31) + KB > 32) cw[(bit >> 5) + 1] |= static_cast<uint32_t>(code) >> (32 - (bit & 31));
                     if constexpr (PROD) {
-                        float cc;
-                        if constexpr (KB <= 2) cc = (code & 2) ? ((code & 1) ? creg[3] : creg[2]) : ((code & 1) ? creg[1] : creg[0]);
-                        else cc = s_c[code];
+                        if constexpr (KB == 1) cc = (code & 1) ? creg[1] : creg[0];
+                        else if constexpr (KB > 2) cc = s_c[code];
                         const float r = __fsub_rn(y, cc);
                         g2p[i & 3] = __fmaf_rn(r, r, g2p[i & 3]);
                         v[i] = r * 256.0f;
