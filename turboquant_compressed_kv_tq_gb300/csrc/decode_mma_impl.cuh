@@ -323,14 +323,17 @@ __device__ __forceinline__ void merge_unit(const MmaArgs& m, int unit, int split
     if (merger) {
         float M = -INFINITY;
         const float* mlu = m.ml + static_cast<int64_t>(unit) * S * kRows * 2;
+        // the splits' loads are independent: unrolled, so that they overlap
+#pragma unroll 4
         for (int s = 0; s < S; ++s) M = fmaxf(M, __ldcg(mlu + (s * kRows + r) * 2));
         float L = 0.0f, acc[8] = {};
         if (M != -INFINITY) {
+#pragma unroll 4
             for (int s = 0; s < S; ++s) {
-                const float ms = __ldcg(mlu + (s * kRows + r) * 2);
-                if (ms == -INFINITY) continue;
-                const float wt = ex2(ms - M);
-                L = fmaf(wt, __ldcg(mlu + (s * kRows + r) * 2 + 1), L);
+                const float2 ml = __ldcg(reinterpret_cast<const float2*>(mlu + (s * kRows + r) * 2));
+                // a split that saw no score has (-inf, 0) and a zero accumulator
+                const float wt = ml.x == -INFINITY ? 0.0f : ex2(ml.x - M);
+                L = fmaf(wt, ml.y, L);
                 const float4* src = reinterpret_cast<const float4*>(
                     m.part + ((static_cast<int64_t>(unit) * S + s) * kRows + r) * kD + dbase);
                 const float4 v0 = __ldcg(src), v1 = __ldcg(src + 1);
