@@ -490,17 +490,22 @@ __global__ void __launch_bounds__(kThreads, 1) split_mma_kernel(MmaArgs m) {
     };
 
     // First stages: fetched before waiting for the kernel this one may overlap,
-    // unless that kernel also appended this step's tokens (then the records it
-    // wrote are visible only after the wait).
+    // except a tile holding tokens that kernel appended in this step (positions
+    // from N - len_add on), which is visible only after the wait. Older records
+    // come from kernels complete before this one could start: the query-prep
+    // CTAs release it only after waiting for their own predecessor.
     const int pre = my_n < kStages - 1 ? my_n : kStages - 1;
-    if (a.len_add == 0)
-        for (int i = 0; i < pre; ++i) issue(i);
+    auto early = [&](int i) {
+        return a.len_add == 0 || t_begin + (warp + i * kWarps) * TT + TT <= N - a.len_add;
+    };
+    for (int i = 0; i < pre; ++i)
+        if (early(i)) issue(i);
     // query fragments of this unit, shared by all warps: [2][8][32] uint4
     // (written by the query-prep kernel this one may overlap: wait for it)
     const uint4* qsm = reinterpret_cast<const uint4*>(smem + st.qs_off);
     tc::grid_wait_prior();
-    if (a.len_add != 0)
-        for (int i = 0; i < pre; ++i) issue(i);
+    for (int i = 0; i < pre; ++i)
+        if (!early(i)) issue(i);
     {
         const uint4* qf = m.qfrag + static_cast<int64_t>(unit) * 2 * 8 * 32;
         uint4* qd = reinterpret_cast<uint4*>(smem + st.qs_off);
