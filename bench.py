@@ -36,9 +36,9 @@ UNIT = "GB/s"
 
 
 # DRAM bytes (read + write) ncu counted for one tq_decode_attention call of
-# this workload (split kernel 226.80 + 3.36 MB, query prep 0.19 MB); set to
+# this workload (split kernel 226.74 + 3.10 MB, query prep 0.19 MB); set to
 # None whenever those kernels change until they are captured again.
-DECODE_TRAFFIC_BYTES = 230.35e6
+DECODE_TRAFFIC_BYTES = 230.03e6
 DECODE_TRAFFIC_SOURCE = ("ncu dram__bytes_read.sum + dram__bytes_write.sum of split_mma_kernel and qfrag_kernel, "
                          "one layer of this workload: bench.py --layers 1 --steps 4 --warmup 3")
 
