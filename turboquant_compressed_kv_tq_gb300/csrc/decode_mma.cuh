@@ -375,6 +375,9 @@ struct MseChunk<4> {
 // of the 96-bit chunk (codes 2p, 2p + 1, bits 6p..6p+5) is shifted to bit 7,
 // masked and or-ed onto the lane address: one shift, one logic op and one
 // load per pair, in the same pair order as MseChunk<3>.
+// Plain shared loads of the lookup tables. The tables are written once before a
+// CTA barrier; every lookup address depends on record words loaded after that
+// barrier, so the loads (not volatile, free to be scheduled) cannot move above it.
 __device__ __forceinline__ uint32_t lds_u32(uint32_t addr) {
     uint32_t v;
     asm("ld.shared.u32 %0, [%1];\n" : "=r"(v) : "r"(addr));
