@@ -287,6 +287,28 @@ tq_status tq_quantize(const tq_codec *codec, const void *x, tq_dtype dtype, int6
 tq_status tq_decode_workspace_bytes(const tq_cache_desc *cache, int batch, int num_q_heads,
                                     int q_len, int max_seq_len, size_t *bytes);
 
+/* Launch shape tq_decode_attention would use (host arithmetic only; the pages
+ * have no counterpart: this exists so callers can inspect and size a decode). */
+typedef struct {
+    int tensor_cores;    /* 1: tensor-core split kernel (head_dim 128); 0: SIMT kernels   */
+    int row_groups;      /* 16-row groups per (sequence, KV head): ceil(G * q_len / 16)    */
+    int splits;          /* token splits per (sequence, KV head, row group)               */
+    int chunk_tokens;    /* tokens per split (a multiple of tile_tokens)                  */
+    int tile_tokens;     /* tokens per shared-memory stage (divides block_tokens)         */
+    size_t smem_bytes;   /* dynamic shared memory of the split kernel (tensor cores)     */
+    size_t workspace_bytes; /* as tq_decode_workspace_bytes for num_sms SMs              */
+} tq_decode_plan_info;
+
+/*
+ * The plan tq_decode_attention makes for these sizes on a GPU of num_sms SMs
+ * (the split count targets one CTA per SM). cache: the descriptor's layout
+ * fields (head_dim, modes, bits, group, block_tokens, num_kv_heads,
+ * subblock_bytes, stream_offset); no device is touched. Returns
+ * TQ_ERR_INVALID_ARG or TQ_ERR_UNSUPPORTED as tq_decode_workspace_bytes does.
+ */
+tq_status tq_decode_plan(const tq_cache_desc *cache, int batch, int num_q_heads, int q_len,
+                         int max_seq_len, int num_sms, tq_decode_plan_info *info);
+
 /*
  * Decode attention over layer `layer` of the compressed cache
  * ("lightning-mlx/plan.md": fused attention over Lloyd-Max codes;

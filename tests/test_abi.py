@@ -112,3 +112,68 @@ def test_bits_split_rejects_out_of_range(libtq):
     # rejected before any device work, and both outputs cleared
     assert libtq.tq_codec_pair_for_bits(128, 4.5, 0, ctypes.byref(kh), ctypes.byref(vh)) == _lib.TQ_ERR_UNSUPPORTED
     assert not kh.value and not vh.value
+
+
+# ------------------------------------------------------------------ decode planner (host arithmetic)
+
+_KEYS = [("prod", 2), ("prod", 3), ("prod", 4), ("mse", 2), ("mse", 3), ("mse", 4)]
+_VALUES = [("mse", 2, 0), ("mse", 3, 0), ("mse", 4, 0), ("group", 2, 32), ("group", 4, 32), ("group", 4, 64),
+           ("group", 4, 128)]
+_MODE = {"mse": 0, "prod": 1, "group": 2}
+# the split kernel's dynamic shared memory must fit the 227 KB per-block opt-in
+_SMEM_LIMIT = 227 * 1024
+
+
+def _desc_from_oracle(D, key, value, BT, Hkv):
+    """A cache descriptor whose layout fields come from the oracle's sub-block layout."""
+    kc = O.Codec(D, key[1], _MODE[key[0]], 0)
+    vc = O.Codec(D, value[1], _MODE[value[0]], 1, value[2])
+    sub, off = O.subblock_layout(kc, vc, BT)
+    d = _lib.tq_cache_desc()
+    d.block_tokens, d.num_kv_heads, d.head_dim = BT, Hkv, D
+    d.key_mode, d.key_bits = _MODE[key[0]], key[1]
+    d.value_mode, d.value_bits, d.value_group = _MODE[value[0]], value[1], value[2]
+    d.subblock_bytes = sub
+    for k in range(7):
+        d.stream_offset[k] = off[k]
+    return d
+
+
+def test_decode_plan_fits_shared_memory_for_every_codec_pair(libtq):
+    # every tensor-core codec pair and block size: the stages, query fragments
+    # and lookup tables fit; tiles divide blocks; the splits cover the sequence
+    for key in _KEYS:
+        for value in _VALUES:
+            for BT in (16, 64, 256, 4096):
+                d = _desc_from_oracle(128, key, value, BT, 8)
+                for (B, Hq, Lq, msl) in [(1, 64, 2, 262146), (32, 32, 1, 65536), (3, 8, 8, 700)]:
+                    p = tq.tq_decode_plan(d, B, Hq, Lq, msl, 152)
+                    assert p["tensor_cores"] == 1
+                    assert 0 < p["smem_bytes"] <= _SMEM_LIMIT - 1024, (key, value, BT, p)
+                    t = p["tile_tokens"]
+                    assert 16 <= t <= 64 and BT % t == 0, (key, value, BT, p)
+                    assert p["chunk_tokens"] % t == 0
+                    assert p["splits"] * p["chunk_tokens"] >= msl
+                    assert p["row_groups"] == (Hq // 8 * Lq + 15) // 16
+
+
+def test_decode_plan_of_the_bench_configuration(libtq):
+    # keys prod 3-bit, values MSE 3-bit, 256-token blocks, GQA 8 x q_len 2 at
+    # 256k on 152 SMs: 64-token tiles, 19 splits, 12 warps x 2 stages x 6912 B
+    # + 8 KB query fragments + 16 KB value pair region + 32 KB key quad table
+    d = _desc_from_oracle(128, ("prod", 3), ("mse", 3, 0), 256, 8)
+    p = tq.tq_decode_plan(d, 1, 64, 2, 262146, 152)
+    assert p["tile_tokens"] == 64 and p["splits"] == 19 and p["row_groups"] == 1
+    assert p["smem_bytes"] == 12 * 2 * 6912 + 8192 + 16384 + 32768 + 12 * 2 * 8
+    # a record pair too large for 64-token stages next to the tables: 32-token tiles
+    d = _desc_from_oracle(128, ("prod", 4), ("group", 4, 32), 256, 8)
+    assert tq.tq_decode_plan(d, 1, 64, 2, 4096, 152)["tile_tokens"] == 32
+
+
+def test_decode_plan_rejects_bad_sizes(libtq):
+    d = _desc_from_oracle(128, ("prod", 3), ("mse", 3, 0), 256, 8)
+    info = _lib.tq_decode_plan_info()
+    assert libtq.tq_decode_plan(ctypes.byref(d), 1, 64, 2, 1, 152, ctypes.byref(info)) == _lib.TQ_ERR_INVALID_ARG
+    assert libtq.tq_decode_plan(ctypes.byref(d), 1, 63, 2, 100, 152, ctypes.byref(info)) == _lib.TQ_ERR_INVALID_ARG
+    assert libtq.tq_decode_plan(ctypes.byref(d), 1, 64, 2, 100, 0, ctypes.byref(info)) == _lib.TQ_ERR_INVALID_ARG
+    assert libtq.tq_decode_plan(ctypes.byref(d), 1, 8 * 65, 1, 100, 152, ctypes.byref(info)) == _lib.TQ_ERR_UNSUPPORTED

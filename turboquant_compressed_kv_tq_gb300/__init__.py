@@ -12,6 +12,7 @@ from typing import Optional
 
 import numpy as np
 
+from . import _lib
 from ._lib import (TQ_BF16, TQ_DEVERR_BLOCK, TQ_DEVERR_CAPACITY, TQ_DEVERR_SEQLEN, TQ_ENCODE_AUTO,
                    TQ_ENCODE_EXACT, TQ_F16, TQ_F32, TQ_MODE_GROUP, TQ_MODE_MSE, TQ_MODE_PROD, TQ_OK, TQError, check,
                    lib, library_path, status_string, tq_cache_desc, tq_codec_info_t)
@@ -21,7 +22,7 @@ __all__ = [
     "tq_bits_split", "tq_codec_pair_for_bits",
     "tq_codec_build_host", "tq_codec_export", "tq_cache_desc_init", "tq_encode_append",
     "tq_quantize", "tq_decode_workspace_bytes", "tq_decode_attention", "tq_decode_attention_noalloc",
-    "tq_decode_step",
+    "tq_decode_step", "tq_decode_plan",
     "tq_prefill_workspace_bytes", "tq_prefill_attention", "tq_cache_copy_blocks",
     "tq_device_error",
     "tq_launch_count", "tq_abi_version", "Codec", "CompressedKVCache", "TQError",
@@ -179,6 +180,15 @@ def tq_decode_attention(key_codec: int, value_codec: int, desc: tq_cache_desc, l
                                     _dtype_code(q), batch, hq, lq, _ptr(seq_lens), _ptr(block_table),
                                     max_blocks, max_seq_len, scale, _ptr(out), _ptr(workspace),
                                     ws_bytes, _stream(stream)), "tq_decode_attention")
+
+
+def tq_decode_plan(desc: tq_cache_desc, batch: int, num_q_heads: int, q_len: int, max_seq_len: int,
+                   num_sms: int) -> dict:
+    """The launch shape tq_decode_attention would use (host arithmetic; see include/tq.h)."""
+    info = _lib.tq_decode_plan_info()
+    check(lib().tq_decode_plan(ctypes.byref(desc), batch, num_q_heads, q_len, max_seq_len, num_sms,
+                               ctypes.byref(info)), "tq_decode_plan")
+    return {f: getattr(info, f) for f, _ in info._fields_}
 
 
 def tq_decode_step(key_codec: int, value_codec: int, desc: tq_cache_desc, layer: int, k_new, v_new, q,

@@ -54,6 +54,12 @@ class tq_codec_info_t(ctypes.Structure):
                 ("device", ctypes.c_int)]
 
 
+class tq_decode_plan_info(ctypes.Structure):
+    _fields_ = [("tensor_cores", ctypes.c_int), ("row_groups", ctypes.c_int), ("splits", ctypes.c_int),
+                ("chunk_tokens", ctypes.c_int), ("tile_tokens", ctypes.c_int),
+                ("smem_bytes", ctypes.c_size_t), ("workspace_bytes", ctypes.c_size_t)]
+
+
 class tq_cache_desc(ctypes.Structure):
     _fields_ = [("pool", ctypes.c_void_p), ("layer_stride", ctypes.c_int64),
                 ("num_layers", ctypes.c_int), ("num_blocks", ctypes.c_int),
@@ -96,6 +102,8 @@ SIGNATURES = {
                                   _P, _I, _I, _F, _P, _P, _SZ, _P]),
     "tq_decode_step": (_ST, [_P, _P, ctypes.POINTER(tq_cache_desc), _I, _P, _P, _I, _I, _P, _I, _I, _I, _I,
                              _P, _P, _I, _I, _F, _P, _P, _SZ, _P]),
+    "tq_decode_plan": (_ST, [ctypes.POINTER(tq_cache_desc), _I, _I, _I, _I, _I,
+                             ctypes.POINTER(tq_decode_plan_info)]),
     "tq_decode_attention_noalloc": (_ST, [_P, _P, ctypes.POINTER(tq_cache_desc), _I, _P, _I, _I, _I, _I,
                                           _P, _P, _I, _I, _F, _P, _P]),
     "tq_prefill_workspace_bytes": (_ST, [ctypes.POINTER(tq_cache_desc), _I, _I, _I, ctypes.POINTER(_SZ)]),

@@ -470,6 +470,25 @@ tq_status tq_quantize(const tq_codec* c, const void* x, tq_dtype dtype, int64_t 
     return launch_quantize(a, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
 }
 
+tq_status tq_decode_plan(const tq_cache_desc* cache, int batch, int num_q_heads, int q_len, int max_seq_len,
+                         int num_sms, tq_decode_plan_info* info) {
+    if (!cache || !info || batch < 0 || q_len <= 0 || max_seq_len < q_len || num_sms <= 0) return TQ_ERR_INVALID_ARG;
+    if (num_q_heads <= 0 || cache->num_kv_heads <= 0 || num_q_heads % cache->num_kv_heads != 0)
+        return TQ_ERR_INVALID_ARG;
+    if (cache->block_tokens < 16 || (cache->block_tokens & (cache->block_tokens - 1)) != 0) return TQ_ERR_INVALID_ARG;
+    const int G = num_q_heads / cache->num_kv_heads;
+    if (G * q_len > 64) return TQ_ERR_UNSUPPORTED;
+    const DecodePlan p = make_decode_plan(cache, batch, G, q_len, max_seq_len, num_sms);
+    info->tensor_cores = p.kind == 1 ? 1 : 0;
+    info->row_groups = p.row_groups;
+    info->splits = p.splits;
+    info->chunk_tokens = p.chunk;
+    info->tile_tokens = p.tile;
+    info->smem_bytes = p.kind == 1 ? p.smem : 0;
+    info->workspace_bytes = p.total;
+    return TQ_OK;
+}
+
 tq_status tq_decode_workspace_bytes(const tq_cache_desc* cache, int batch, int num_q_heads, int q_len,
                                     int max_seq_len, size_t* bytes) {
     if (!cache || !bytes || batch < 0 || q_len <= 0 || max_seq_len < q_len) return TQ_ERR_INVALID_ARG;
