@@ -177,3 +177,12 @@ def test_decode_plan_rejects_bad_sizes(libtq):
     assert libtq.tq_decode_plan(ctypes.byref(d), 1, 63, 2, 100, 152, ctypes.byref(info)) == _lib.TQ_ERR_INVALID_ARG
     assert libtq.tq_decode_plan(ctypes.byref(d), 1, 64, 2, 100, 0, ctypes.byref(info)) == _lib.TQ_ERR_INVALID_ARG
     assert libtq.tq_decode_plan(ctypes.byref(d), 1, 8 * 65, 1, 100, 152, ctypes.byref(info)) == _lib.TQ_ERR_UNSUPPORTED
+
+
+def test_decode_plan_simt_shapes(libtq):
+    # head_dim 64 and 256 take the SIMT kernels: no tensor-core shared memory
+    for D, key, value in [(256, ("prod", 3), ("group", 2, 32)), (64, ("mse", 2), ("mse", 2, 0))]:
+        d = _desc_from_oracle(D, key, value, 64, 2)
+        p = tq.tq_decode_plan(d, 2, 16, 1, 8192, 152)
+        assert p["tensor_cores"] == 0 and p["smem_bytes"] == 0
+        assert p["splits"] * p["chunk_tokens"] >= 8192 and p["workspace_bytes"] > 0
