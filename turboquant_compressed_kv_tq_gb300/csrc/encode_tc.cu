@@ -349,7 +349,9 @@ __global__ void __launch_bounds__(kEncThreads, 1)
         float mreg[NM];
 #pragma unroll
         for (int j = 0; j < NM; ++j) mreg[j] = s_m[j];
-        float creg[4] = {s_c[0], s_c[1], s_c[2], s_c[3]};   // 2-bit codebooks: levels from registers
+        // 2-bit codebooks: levels from registers, as -256 c (the residual is
+        // formed directly as r~ = 256 y - 256 c, see below)
+        const float creg[4] = {-256.0f * s_c[0], -256.0f * s_c[1], -256.0f * s_c[2], -256.0f * s_c[3]};
         const int64_t o_idx = is_v ? a.pool.off[4] : a.pool.off[0];
         const int64_t o_norm = is_v ? a.pool.off[5] : a.pool.off[2];
         // destination of this thread's token of tile it in the pool (null: out of
@@ -395,7 +397,7 @@ __global__ void __launch_bounds__(kEncThreads, 1)
             if constexpr (PROD) ok = ok && tc::mbar_wait(&bars[kBarREmpty], (it & 1) ^ 1);   // residual tiles free
 
             // ---------------- epilogue 1: indices (and residual operands for prod)
-            float g2p[4] = {0.0f, 0.0f, 0.0f, 0.0f};   // residual sum of squares, four partial chains
+            float g2p[4] = {0.0f, 0.0f, 0.0f, 0.0f};   // 2^16 x the residual sum of squares, four chains
 #pragma unroll 1
             for (int ch = 0; ch < CH; ++ch) {
                 float v[32];
@@ -407,7 +409,7 @@ __global__ void __launch_bounds__(kEncThreads, 1)
                 for (int i = 0; i < 32; ++i) {
                     const float y = v[i] * inv;
                     int code;
-                    float cc = 0.0f;   // the index's level (prod keys)
+                    float cc = 0.0f;   // -256 x the index's level (prod keys)
                     if constexpr (PROD && KB == 2) {
                         // the index and its level from the same two comparisons
                         const bool p1 = y > mreg[1];
@@ -422,10 +424,14 @@ __global__ void __launch_bounds__(kEncThreads, 1)
                     if ((bit & 31) + KB > 32) cw[(bit >> 5) + 1] |= static_cast<uint32_t>(code) >> (32 - (bit & 31));
                     if constexpr (PROD) {
                         if constexpr (KB == 1) cc = (code & 1) ? creg[1] : creg[0];
-                        else if constexpr (KB > 2) cc = s_c[code];
-                        const float r = __fsub_rn(y, cc);
-                        g2p[i & 3] = __fmaf_rn(r, r, g2p[i & 3]);
-                        v[i] = r * 256.0f;
+                        else if constexpr (KB > 2) cc = -256.0f * s_c[code];
+                        // r~ = 256 (y - c) in one rounding: scaling by a power of two
+                        // commutes with rounding (y - c is 0 or a normal number), so
+                        // r~ is bit for bit 256 x fp32(y - c); the sums of r~^2 are
+                        // then exactly 2^16 x the sums of r^2
+                        const float rs = __fmaf_rn(y, 256.0f, cc);
+                        g2p[i & 3] = __fmaf_rn(rs, rs, g2p[i & 3]);
+                        v[i] = rs;
                     }
                 }
                 if (widx) store_words<KB>(widx + KB * (CH * half + ch), cw);
@@ -476,7 +482,8 @@ __global__ void __launch_bounds__(kEncThreads, 1)
                     store_words<CH>(reinterpret_cast<uint32_t*>(sub + a.pool.off[1]) + static_cast<int64_t>(slot) * WS + CH * half,
                                     sw);
                     if (half == 0)
-                        reinterpret_cast<float*>(sub + a.pool.off[3])[slot] = __fsqrt_rn(g2 + s_g2[bb * kTileRows + row]);
+                        reinterpret_cast<float*>(sub + a.pool.off[3])[slot] =
+                            __fsqrt_rn(g2 + s_g2[bb * kTileRows + row]) * 0.00390625f;   // sqrt(2^16 x) / 256, exact
                 }
             } else {
                 if (tc::bar_or(kEpiBar, 32 * kEpiWarps, !ok)) {
