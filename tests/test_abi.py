@@ -186,3 +186,15 @@ def test_decode_plan_simt_shapes(libtq):
         p = tq.tq_decode_plan(d, 2, 16, 1, 8192, 152)
         assert p["tensor_cores"] == 0 and p["smem_bytes"] == 0
         assert p["splits"] * p["chunk_tokens"] >= 8192 and p["workspace_bytes"] > 0
+
+
+def test_decode_plan_split_rule(libtq):
+    # splits: enough CTAs to cover the SMs, each split a multiple of the tile
+    # and at most 16384 tokens (so that many short units still balance)
+    d = _desc_from_oracle(128, ("prod", 3), ("mse", 3, 0), 256, 8)
+    one = tq.tq_decode_plan(d, 1, 64, 2, 262146, 152)        # 8 units -> 19 splits of 13,824 tokens
+    assert one["splits"] == 19 and one["chunk_tokens"] == 13824
+    many = tq.tq_decode_plan(d, 32, 32, 1, 65536, 152)       # 256 units >= 152 SMs: split by length only
+    assert many["splits"] == 4 and many["chunk_tokens"] == 16384
+    short = tq.tq_decode_plan(d, 1, 64, 2, 100, 152)         # a short sequence: one 64-token tile per split
+    assert short["chunk_tokens"] == 64 and short["splits"] == 2
