@@ -48,9 +48,9 @@ enum : int {
     kBarAFull = 1,      // X~ tile written (4 producer warps)
     kBarAEmpty = 2,     // GEMM 1 read it (commit)
     kBarYFull = 3,      // [2] GEMM 1 done (commit)
-    kBarYEmpty = 5,     // [2] epilogue read the accumulator (8 epilogue warps)
-    kBarRFull = 7,      // residual tiles written (8 epilogue warps)
-    kBarREmpty = 8,     // GEMM 2 read them (commit)
+    kBarYEmpty = 5,     // [2] accumulator free again: the epilogue read it (8 warps), or
+                        //     for prod keys GEMM 2 read the residual stored over it (commit)
+    kBarRFull = 7,      // [2] prod keys: the residual stored over accumulator b (8 epilogue warps)
     kBarZFull = 9,      // GEMM 2 done (commit)
     kBarZEmpty = 10,    // epilogue read Z (8 epilogue warps)
     kBarNorm = 11,      // [3] a tile's norms written (4 producer warps)
@@ -64,11 +64,9 @@ struct TcLayout {
     static constexpr int oR = 0;
     static constexpr int oS = oR + kTab;
     static constexpr int oA = oS + (PROD ? kTab : 0);    // X~
-    static constexpr int oRh = oA + kTile;               // residual hi (prod)
-    static constexpr int oRl = oRh + (PROD ? kTile : 0); // residual lo (prod)
-    static constexpr int oNorm = oRl + (PROD ? kTile : 0);   // [3][128] norms
-    static constexpr int oG2 = oNorm + 3 * kTileRows * 4;     // [2][128] residual sums of half 1
-    static constexpr int oCb = oG2 + 2 * kTileRows * 4;       // centroids [16], midpoints [16]
+    static constexpr int oNorm = oA + kTile;                  // [3][128] norms
+    static constexpr int oG2 = oNorm + 3 * kTileRows * 4;     // [3][128] residual sums of half 1 (prod)
+    static constexpr int oCb = oG2 + 3 * kTileRows * 4;       // centroids [16], midpoints [16]
     static constexpr int oBar = oCb + 128;
     static constexpr int kBytes = oBar + 128;
     static constexpr uint32_t kLbo = 128;                // next 8 columns (K)
@@ -213,10 +211,9 @@ __global__ void __launch_bounds__(kEncThreads, 1)
         tc::mbar_init(&bars[kBarAEmpty], 1);
         for (int i = 0; i < 2; ++i) {
             tc::mbar_init(&bars[kBarYFull + i], 1);
-            tc::mbar_init(&bars[kBarYEmpty + i], kEpiWarps);
+            tc::mbar_init(&bars[kBarYEmpty + i], PROD ? 1 : kEpiWarps);
+            tc::mbar_init(&bars[kBarRFull + i], kEpiWarps);
         }
-        tc::mbar_init(&bars[kBarRFull], kEpiWarps);
-        tc::mbar_init(&bars[kBarREmpty], 1);
         tc::mbar_init(&bars[kBarZFull], 1);
         tc::mbar_init(&bars[kBarZEmpty], kEpiWarps);
         for (int i = 0; i < 3; ++i) tc::mbar_init(&bars[kBarNorm + i], kProdWarps);
@@ -314,20 +311,26 @@ __global__ void __launch_bounds__(kEncThreads, 1)
                 if (it + 1 < n_it) gemm1(it + 1);
                 if (!ok) break;
                 if constexpr (PROD) {
-                    ok = tc::mbar_wait(&bars[kBarRFull], it & 1) && tc::mbar_wait(&bars[kBarZEmpty], (it & 1) ^ 1);
+                    // GEMM 2 of tile it: its A operand, the residual r~ as fp16 hi / lo
+                    // pairs, lies over accumulator bb: 32-coordinate chunk q in
+                    // columns 32 q .. 32 q + 15 (hi) and 32 q + 16 .. 32 q + 31 (lo)
+                    const int bb = it & 1;
+                    ok = tc::mbar_wait(&bars[kBarRFull + bb], (it >> 1) & 1) &&
+                         tc::mbar_wait(&bars[kBarZEmpty], (it & 1) ^ 1);
                     if (!ok) break;
                     tc::tc_fence_after();
                     const uint32_t d = tmem + 2 * D;
-                    const uint32_t lh = lo_of(L::oRh), ll = lo_of(L::oRl);
+                    const uint32_t yb = tmem + bb * D;
                     const uint32_t lsh = lo_of(L::oS), lsl = lo_of(L::oS + L::kTab / 2);
 #pragma unroll
                     for (int s = 0; s < D / 16; ++s) {
-                        tc::mma_f16(d, hi64 | (lh + 16 * s), hi64 | (lsh + 16 * s), idesc, s > 0);
-                        tc::mma_f16(d, hi64 | (ll + 16 * s), hi64 | (lsh + 16 * s), idesc, 1);
-                        tc::mma_f16(d, hi64 | (lh + 16 * s), hi64 | (lsl + 16 * s), idesc, 1);
+                        const uint32_t ah = yb + 32 * (s >> 1) + 8 * (s & 1), al = ah + 16;
+                        tc::mma_f16_ta(d, ah, hi64 | (lsh + 16 * s), idesc, s > 0);
+                        tc::mma_f16_ta(d, al, hi64 | (lsh + 16 * s), idesc, 1);
+                        tc::mma_f16_ta(d, ah, hi64 | (lsl + 16 * s), idesc, 1);
                     }
                     tc::mma_commit(&bars[kBarZFull]);
-                    tc::mma_commit(&bars[kBarREmpty]);
+                    tc::mma_commit(&bars[kBarYEmpty + bb]);   // the accumulator takes tile it + 2
                     ++g2n;
                 }
             }
@@ -337,7 +340,7 @@ __global__ void __launch_bounds__(kEncThreads, 1)
             }
             // drain (after a timeout elsewhere): the last commits of each kind
             if (g1) (void)tc::mbar_wait(&bars[kBarAEmpty], (g1 - 1) & 1);
-            if (g2n) (void)tc::mbar_wait(&bars[kBarREmpty], (g2n - 1) & 1);
+            if (g2n) (void)tc::mbar_wait(&bars[kBarZFull], (g2n - 1) & 1);
         }
         __syncwarp();
     } else {
@@ -379,29 +382,26 @@ __global__ void __launch_bounds__(kEncThreads, 1)
             if (pb < 0 || pb >= a.pool.num_blocks) atomicOr(a.err, TQ_DEVERR_BLOCK);
             else sub = a.pool.base + (pb * Hkv + h) * a.pool.sub_bytes;
         };
-        char* sub_next = nullptr;
-        int slot_next = 0;
-        if (n_it > 0) dest_of(0, sub_next, slot_next);
-        for (int it = 0; it < n_it && !failed; ++it) {
-            const int bb = it & 1;
-            char* const sub = sub_next;
-            const int slot = slot_next;
-            bool ok = tc::mbar_wait(&bars[kBarYFull + bb], (it >> 1) & 1) &&
-                      tc::mbar_wait(&bars[kBarNorm + it % 3], (it / 3) & 1);
+        // Index pass of tile j: Lloyd-Max indices packed and stored, the norm
+        // stored; for prod keys also the residual r~ = 256 (y - c), stored as fp16
+        // hi / lo pairs over the 32-column accumulator chunk the thread has just
+        // read (the A operand of GEMM 2), and this half's residual sum.
+        auto index_pass = [&](int j, char*& sub, int& slot, float& g2) -> bool {
+            const int bj = j & 1;
+            const bool okw = tc::mbar_wait(&bars[kBarYFull + bj], (j >> 1) & 1) &&
+                             tc::mbar_wait(&bars[kBarNorm + j % 3], (j / 3) & 1);
             tc::tc_fence_after();
-            if (it + 1 < n_it) dest_of(it + 1, sub_next, slot_next);
-            const float n = s_norm[(it % 3) * kTileRows + row];
+            dest_of(j, sub, slot);
+            const float n = s_norm[(j % 3) * kTileRows + row];
             const int ex = n > 0.0f ? ilogbf(n) : 0;
             const float inv = n > 0.0f ? __fdiv_rn(scalbnf(1.0f, ex - 4), n) : 0.0f;
             uint32_t* widx = sub ? reinterpret_cast<uint32_t*>(sub + o_idx) + static_cast<int64_t>(slot) * W : nullptr;
-            if constexpr (PROD) ok = ok && tc::mbar_wait(&bars[kBarREmpty], (it & 1) ^ 1);   // residual tiles free
-
-            // ---------------- epilogue 1: indices (and residual operands for prod)
             float g2p[4] = {0.0f, 0.0f, 0.0f, 0.0f};   // 2^16 x the residual sum of squares, four chains
 #pragma unroll 1
             for (int ch = 0; ch < CH; ++ch) {
                 float v[32];
-                tc::tmem_ld32(t_lane + bb * D + 32 * ch, v);
+                const uint32_t tcol = t_lane + bj * D + 32 * ch;
+                tc::tmem_ld32(tcol, v);
                 uint32_t cw[KB];
 #pragma unroll
                 for (int q = 0; q < KB; ++q) cw[q] = 0u;
@@ -436,29 +436,34 @@ __global__ void __launch_bounds__(kEncThreads, 1)
                 }
                 if (widx) store_words<KB>(widx + KB * (CH * half + ch), cw);
                 if constexpr (PROD) {
+                    uint32_t hi[16], lo[16];
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        float f[8];
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) f[e] = v[8 * q + e];
-                        store8<D>(smem + L::oRh, smem + L::oRl, row, DH * half + 32 * ch + 8 * q, f);
+                    for (int p = 0; p < 16; ++p) {
+                        hi[p] = half2_bits(v[2 * p], v[2 * p + 1]);
+                        const float2 back = __half22float2(*reinterpret_cast<const __half2*>(&hi[p]));
+                        lo[p] = half2_bits(v[2 * p] - back.x, v[2 * p + 1] - back.y);
                     }
+                    tc::tmem_st16u(tcol, hi);
+                    tc::tmem_st16u(tcol + 16, lo);
                 }
             }
-            // the accumulator may take the tile after next
+            if (sub && half == 0) reinterpret_cast<float*>(sub + o_norm)[slot] = n;
+            g2 = (g2p[0] + g2p[1]) + (g2p[2] + g2p[3]);
             tc::tc_fence_before();
             __syncwarp();
-            if (lane == 0) tc::mbar_arrive(&bars[kBarYEmpty + bb]);
-            if (sub && half == 0) reinterpret_cast<float*>(sub + o_norm)[slot] = n;
-
-            const float g2 = (g2p[0] + g2p[1]) + (g2p[2] + g2p[3]);
             if constexpr (PROD) {
-                tc::fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) tc::mbar_arrive(&bars[kBarRFull]);
-                if (half == 1) s_g2[bb * kTileRows + row] = g2;
-                // ---------------- epilogue 2: signs and the residual norm
-                ok = ok && tc::mbar_wait(&bars[kBarZFull], it & 1);
+                if (half == 1) s_g2[(j % 3) * kTileRows + row] = g2;
+                if (lane == 0) tc::mbar_arrive(&bars[kBarRFull + bj]);   // GEMM 2 may read the residual
+            } else {
+                if (lane == 0) tc::mbar_arrive(&bars[kBarYEmpty + bj]);  // the accumulator may take the tile after next
+            }
+            return okw;
+        };
+        if constexpr (PROD) {
+            // Sign pass of tile j: the signs of S r and the residual norm (the
+            // other half's residual sum from shared memory, after the barrier).
+            auto sign_pass = [&](int j, char* sub, int slot, float g2, bool ok) -> bool {
+                ok = ok && tc::mbar_wait(&bars[kBarZFull], j & 1);
                 tc::tc_fence_after();
                 uint32_t sw[CH];
 #pragma unroll
@@ -473,19 +478,41 @@ __global__ void __launch_bounds__(kEncThreads, 1)
                 tc::tc_fence_before();
                 __syncwarp();
                 if (lane == 0) tc::mbar_arrive(&bars[kBarZEmpty]);
-                // the other half's residual sum (a uniform failure exit first)
-                if (tc::bar_or(kEpiBar, 32 * kEpiWarps, !ok)) {
-                    failed = true;
-                    break;
-                }
+                if (tc::bar_or(kEpiBar, 32 * kEpiWarps, !ok)) return false;   // uniform failure exit
                 if (sub) {
-                    store_words<CH>(reinterpret_cast<uint32_t*>(sub + a.pool.off[1]) + static_cast<int64_t>(slot) * WS + CH * half,
+                    store_words<CH>(reinterpret_cast<uint32_t*>(sub + a.pool.off[1]) + static_cast<int64_t>(slot) * WS +
+                                        CH * half,
                                     sw);
                     if (half == 0)
                         reinterpret_cast<float*>(sub + a.pool.off[3])[slot] =
-                            __fsqrt_rn(g2 + s_g2[bb * kTileRows + row]) * 0.00390625f;   // sqrt(2^16 x) / 256, exact
+                            __fsqrt_rn(g2 + s_g2[(j % 3) * kTileRows + row]) * 0.00390625f;   // sqrt(2^16 x) / 256, exact
                 }
-            } else {
+                return true;
+            };
+            // the index pass runs one tile ahead: GEMM 2 of tile it overlaps the
+            // index pass of tile it + 1 (the residual of tile it + 1 lies over the
+            // other accumulator; the residual sums rotate through three slots)
+            char* sub_c = nullptr;
+            char* sub_n = nullptr;
+            int slot_c = 0, slot_n = 0;
+            float g2_c = 0.0f, g2_n = 0.0f;
+            bool ok = n_it > 0 ? index_pass(0, sub_c, slot_c, g2_c) : true;
+            for (int it = 0; it < n_it && !failed; ++it) {
+                if (it + 1 < n_it) ok = index_pass(it + 1, sub_n, slot_n, g2_n) && ok;
+                if (!sign_pass(it, sub_c, slot_c, g2_c, ok)) {
+                    failed = true;
+                    break;
+                }
+                sub_c = sub_n;
+                slot_c = slot_n;
+                g2_c = g2_n;
+            }
+        } else {
+            for (int it = 0; it < n_it && !failed; ++it) {
+                char* sub = nullptr;
+                int slot = 0;
+                float g2 = 0.0f;
+                const bool ok = index_pass(it, sub, slot, g2);
                 if (tc::bar_or(kEpiBar, 32 * kEpiWarps, !ok)) {
                     failed = true;
                     break;
