@@ -26,23 +26,32 @@ _lib = None
 MSE, PROD, GROUP = 0, 1, 2
 
 
+def compile_source(src: str, out: str) -> str:
+    """Compile one oracle source file into the shared library ``out`` (no FMA
+    contraction, OpenMP); the include directory is this package's."""
+    tmp = out + f".tmp{os.getpid()}"
+    subprocess.check_call(["gcc", "-O2", "-fPIC", "-shared", "-std=c11", "-ffp-contract=off",
+                           "-fopenmp", "-Wall", "-I", _HERE, src, "-o", tmp, "-lm"])
+    os.replace(tmp, out)
+    return out
+
+
 def build(force: bool = False) -> str:
     """Compile the oracle with gcc (no FMA contraction, OpenMP)."""
     os.makedirs(_BUILD, exist_ok=True)
     if force or not os.path.exists(_SO) or os.path.getmtime(_SO) < max(
             os.path.getmtime(_SRC), os.path.getmtime(os.path.join(_HERE, "tq_oracle.h"))):
-        tmp = _SO + f".tmp{os.getpid()}"
-        subprocess.check_call(["gcc", "-O2", "-fPIC", "-shared", "-std=c11", "-ffp-contract=off",
-                               "-fopenmp", "-Wall", _SRC, "-o", tmp, "-lm"])
-        os.replace(tmp, _SO)
+        compile_source(_SRC, _SO)
     return _SO
 
 
 def lib():
+    """The loaded oracle. ``TQO_LIBRARY`` names another compiled copy of it to
+    load instead (the planted-mistake tests point it at a mutant)."""
     global _lib
     with _lock:
         if _lib is None:
-            _lib = _declare(ctypes.CDLL(build()))
+            _lib = _declare(ctypes.CDLL(os.environ.get("TQO_LIBRARY") or build()))
     return _lib
 
 
