@@ -20,7 +20,7 @@ def _brute(q, K, V, scale, Lq):
     return out
 
 
-@pytest.mark.parametrize("Lq", [1, 2, 3])
+@pytest.mark.parametrize("Lq", [1, 2, 3, 9])
 def test_attention_equals_brute_force(oracle_lib, Lq):
     rng = np.random.default_rng(Lq)
     G, N, D = 3, 9, 16
@@ -29,6 +29,9 @@ def test_attention_equals_brute_force(oracle_lib, Lq):
     V = rng.standard_normal((N, D))
     got = O.attention_f64(q, K, V, 0.3, Lq)
     assert np.abs(got - _brute(q, K, V, 0.3, Lq)).max() < 1e-13
+    if Lq == N:
+        # a chunk that is the whole sequence: its first query sees one token
+        assert np.array_equal(got[:, 0], np.broadcast_to(V[0], (G, D)))
 
 
 def test_attention_single_token_is_value(oracle_lib):
@@ -46,6 +49,8 @@ CASES = [
     (128, (O.PROD, 3), (O.MSE, 3, 0), 8, 2, 50),
     (256, (O.PROD, 3), (O.GROUP, 2, 32), 8, 1, 40),
     (128, (O.PROD, 3), (O.GROUP, 4, 64), 4, 1, 45),
+    # a prefill chunk that is the whole sequence (every query causal)
+    (128, (O.PROD, 3), (O.MSE, 3, 0), 2, 24, 24),
 ]
 
 
