@@ -198,3 +198,55 @@ def test_decode_plan_split_rule(libtq):
     assert many["splits"] == 4 and many["chunk_tokens"] == 16384
     short = tq.tq_decode_plan(d, 1, 64, 2, 100, 152)         # a short sequence: one 64-token tile per split
     assert short["chunk_tokens"] == 64 and short["splits"] == 2
+
+
+# ------------------------------------------------------------------ host-side argument checks
+
+def _zero_args(fn):
+    """One argument per ctypes argtype: NULL pointers, zero numbers."""
+    args = []
+    for t in fn.argtypes:
+        if t in (ctypes.c_float, ctypes.c_double):
+            args.append(0.0)
+        elif t in (ctypes.c_int, ctypes.c_int64, ctypes.c_uint64, ctypes.c_size_t, ctypes.c_uint32):
+            args.append(0)
+        else:
+            args.append(None)
+    return args
+
+
+@pytest.mark.parametrize("name", ["tq_encode_append", "tq_decode_attention", "tq_decode_step",
+                                  "tq_decode_attention_noalloc", "tq_prefill_attention"])
+def test_compute_calls_reject_missing_codecs_before_device_work(libtq, name):
+    # a NULL codec is refused on the host, before any CUDA call (none is
+    # possible here), with the header's status
+    fn = getattr(libtq, name)
+    d = _desc_from_oracle(128, ("prod", 3), ("mse", 3, 0), 256, 8)
+    d.num_layers = 1
+    args = _zero_args(fn)
+    args[2] = ctypes.byref(d)
+    args[3] = 0                       # layer
+    assert fn(*args) == _lib.TQ_ERR_INVALID_ARG
+
+
+def test_copy_blocks_mixed_configuration_guard_without_device(libtq):
+    # the batch operations refuse caches of different configurations (the
+    # pages raise on mixing them); the check is host arithmetic
+    def desc(key=("prod", 3), value=("mse", 3, 0), BT=16, Hkv=2, D=128):
+        d = _desc_from_oracle(D, key, value, BT, Hkv)
+        d.num_layers = 2
+        return d
+    a = desc()
+    f = libtq.tq_cache_copy_blocks
+    assert f(ctypes.byref(a), ctypes.byref(desc()), None, None, 0, None) == _lib.TQ_OK   # nothing to copy
+    for other in (desc(key=("prod", 4)), desc(key=("mse", 3)), desc(value=("mse", 4, 0)),
+                  desc(value=("group", 4, 64)), desc(BT=32), desc(Hkv=4)):
+        assert f(ctypes.byref(a), ctypes.byref(other), None, None, 0, None) == _lib.TQ_ERR_CONFIG_MISMATCH
+    b = desc()
+    b.num_layers = 3
+    assert f(ctypes.byref(a), ctypes.byref(b), None, None, 0, None) == _lib.TQ_ERR_CONFIG_MISMATCH
+    b = desc()
+    b.key_seed = 5
+    assert f(ctypes.byref(a), ctypes.byref(b), None, None, 0, None) == _lib.TQ_ERR_CONFIG_MISMATCH
+    assert f(None, ctypes.byref(a), None, None, 0, None) == _lib.TQ_ERR_INVALID_ARG
+    assert f(ctypes.byref(a), ctypes.byref(desc()), None, None, -1, None) == _lib.TQ_ERR_INVALID_ARG
