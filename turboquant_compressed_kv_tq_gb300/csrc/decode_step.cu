@@ -13,6 +13,9 @@
 namespace tq {
 namespace mmadec {
 
+// the encoder body needs one thread per coordinate
+static_assert(kQThreads >= kD, "the preparation block must cover head_dim threads");
+
 template <int KB, int NV, bool NAT>
 __global__ void __launch_bounds__(kQThreads) step_prep_kernel(MmaArgs m, EncodeAppendArgs e, int nq) {
     extern __shared__ __align__(16) unsigned char smem[];
