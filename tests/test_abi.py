@@ -250,3 +250,28 @@ def test_copy_blocks_mixed_configuration_guard_without_device(libtq):
     assert f(ctypes.byref(a), ctypes.byref(b), None, None, 0, None) == _lib.TQ_ERR_CONFIG_MISMATCH
     assert f(None, ctypes.byref(a), None, None, 0, None) == _lib.TQ_ERR_INVALID_ARG
     assert f(ctypes.byref(a), ctypes.byref(desc()), None, None, -1, None) == _lib.TQ_ERR_INVALID_ARG
+
+
+def test_decode_plan_invariants_on_random_shapes(libtq):
+    # seeded sweep: every plan covers the sequence with non-empty splits of
+    # whole tiles, at most 16384 tokens each, inside the shared-memory budget
+    rng = np.random.default_rng(11)
+    for _ in range(300):
+        key = _KEYS[rng.integers(len(_KEYS))]
+        value = _VALUES[rng.integers(len(_VALUES))]
+        BT = int(rng.choice([16, 32, 64, 128, 256, 1024]))
+        Hkv = int(rng.choice([1, 2, 4, 8]))
+        G = int(rng.choice([1, 2, 4, 8]))
+        Lq = int(rng.integers(1, 65 // G + 1))
+        B = int(rng.integers(1, 65))
+        msl = int(rng.integers(Lq, 300001))
+        sms = int(rng.choice([1, 20, 76, 148, 152]))
+        d = _desc_from_oracle(128, key, value, BT, Hkv)
+        p = tq.tq_decode_plan(d, B, Hkv * G, Lq, msl, sms)
+        t, c, s = p["tile_tokens"], p["chunk_tokens"], p["splits"]
+        case = (key, value, BT, Hkv, G, Lq, B, msl, sms, p)
+        assert p["tensor_cores"] == 1 and BT % t == 0 and 16 <= t <= 64, case
+        assert c % t == 0 and c <= max(16384, t), case
+        assert s * c >= msl and (s - 1) * c < msl, case
+        assert 0 < p["smem_bytes"] <= _SMEM_LIMIT - 1024, case
+        assert p["row_groups"] == (G * Lq + 15) // 16 and p["workspace_bytes"] > 0, case
