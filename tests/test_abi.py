@@ -275,3 +275,29 @@ def test_decode_plan_invariants_on_random_shapes(libtq):
         assert s * c >= msl and (s - 1) * c < msl, case
         assert 0 < p["smem_bytes"] <= _SMEM_LIMIT - 1024, case
         assert p["row_groups"] == (G * Lq + 15) // 16 and p["workspace_bytes"] > 0, case
+
+
+def test_prefill_workspace_follows_the_supported_codec_rule(libtq):
+    # host arithmetic: the header's codec set for prefill attention (head_dim
+    # 128; prod 3-bit keys with MSE 3/4-bit or group 4-bit values, or MSE
+    # 4-bit keys and values) sizes a workspace; anything else is refused
+    supported = {(("prod", 3), ("mse", 3, 0)), (("prod", 3), ("mse", 4, 0)), (("prod", 3), ("group", 4, 32)),
+                 (("prod", 3), ("group", 4, 64)), (("prod", 3), ("group", 4, 128)), (("mse", 4), ("mse", 4, 0))}
+    f = libtq.tq_prefill_workspace_bytes
+    n = ctypes.c_size_t(0)
+    for key in _KEYS:
+        for value in _VALUES:
+            d = _desc_from_oracle(128, key, value, 64, 8)
+            st = f(ctypes.byref(d), 2, 64, 8192, ctypes.byref(n))
+            if (key, value) in supported:
+                # one 16-row fragment set per (sequence, KV head, row group), 256-byte rounded
+                rows = (8 * 8192 + 15) // 16
+                assert st == _lib.TQ_OK and n.value == (2 * 8 * rows * 2 * 8 * 32 * 16 + 255) // 256 * 256
+            else:
+                assert st == _lib.TQ_ERR_UNSUPPORTED, (key, value)
+    d = _desc_from_oracle(256, ("prod", 3), ("group", 2, 32), 64, 2)
+    assert f(ctypes.byref(d), 1, 16, 128, ctypes.byref(n)) == _lib.TQ_ERR_UNSUPPORTED
+    d = _desc_from_oracle(128, ("prod", 3), ("mse", 3, 0), 64, 8)
+    assert f(ctypes.byref(d), 1, 64, 0, ctypes.byref(n)) == _lib.TQ_ERR_INVALID_ARG
+    assert f(ctypes.byref(d), 1, 60, 16, ctypes.byref(n)) == _lib.TQ_ERR_INVALID_ARG
+    assert f(ctypes.byref(d), 1, 64, 16, None) == _lib.TQ_ERR_INVALID_ARG
