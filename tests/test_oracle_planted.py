@@ -66,6 +66,17 @@ MUTANTS = [
     # rotated decode: the output rotated by R_v instead of back by R_v^T
     ("value_rotation_not_inverted", "s += acc[i] * (double)vR[(size_t)i * D + d];",
      "s += acc[i] * (double)vR[(size_t)d * D + i];", 1),
+    # fractional widths: the keys take the upper width
+    ("fractional_split_swapped", "fractional ? (int)floor(b)", "fractional ? (int)ceil(b)", 1),
+    # group: codes rounded down instead of to nearest
+    ("group_rounds_down", "float r = rintf((xv[gi * g + k] - mf) / sf);",
+     "float r = floorf((xv[gi * g + k] - mf) / sf);", 1),
+    # group: the minimum dropped when dequantising
+    ("group_dequant_min_dropped", "out[v * D + d] = (double)codes[d] * s + m0;",
+     "out[v * D + d] = (double)codes[d] * s;", 1),
+    # rotated decode: the group minimum dropped from the value sum
+    ("group_decode_min_dropped", "acc[d] += p * ((double)codes[d] * sc + m0);",
+     "acc[d] += p * ((double)codes[d] * sc);", 1),
     # pool writer: the block table ignored
     ("block_table_ignored",
      "int64_t p = table ? table[(int64_t)seq * max_blocks + lb] : (int64_t)seq * max_blocks + lb;",
