@@ -38,6 +38,10 @@ MUTANTS = [
     ("centroid_moment_sign", "double mom = Ge[j + 1] - Ge[j];", "double mom = Ge[j] - Ge[j + 1];", 1),
     # Lloyd-Max: thresholds at the left centroid instead of the midpoint
     ("threshold_not_midpoint", "m[j] = 0.5 * (c[j] + c[j + 1]);", "m[j] = c[j];", 1),
+    # Lloyd-Max: iterations stopped at a step of 1e-3
+    ("lloyd_stops_early", "if (delta <= 1e-17) break;", "if (delta <= 1e-3) break;", 1),
+    # Lloyd-Max: the cell-mass recurrence loses its factor 2
+    ("mass_recurrence", "I = (t * p + 2.0 * a * I) / (2.0 * a + 1.0);", "I = (t * p + a * I) / (2.0 * a + 1.0);", 1),
     # packing: codes that straddle two words lose their high bits
     ("pack_straddle_dropped", "if ((p & 31) + b > 32) words[(p >> 5) + 1] |= (uint32_t)(v >> 32);", "", 1),
     # binary16: truncation instead of round to nearest even
@@ -48,6 +52,8 @@ MUTANTS = [
     # encode: y = R^T x instead of R x
     ("rotation_transposed_in_encode", "t = fmaf(R[(size_t)i * D + k], x[k], t);",
      "t = fmaf(R[(size_t)k * D + i], x[k], t);", 1),
+    # prod: residual y + c instead of y - c
+    ("residual_sign", "r[i] = y[i] - c[codes[i]];", "r[i] = y[i] + c[codes[i]];", 1),
     # prod: sign bit set for negative projections
     ("qjl_sign_flipped", "if (z >= 0.0f) sw[j >> 5]", "if (z < 0.0f) sw[j >> 5]", 1),
     # prod: QJL constant sqrt(2/pi)/D instead of sqrt(pi/2)/D, everywhere
