@@ -1,8 +1,11 @@
-"""Static checks of the tree: the product never reaches the oracle, and every
-committed ncu command leaves the GPU clocks alone."""
+"""Checks of the tree: the product never reaches the oracle and has no
+fallback when its library is missing, and every committed ncu command leaves
+the GPU clocks alone."""
 import ast
 import os
 import re
+import subprocess
+import sys
 
 from conftest import ROOT
 
@@ -50,3 +53,16 @@ def test_profile_commands_leave_clocks_alone():
         for line in joined.splitlines():
             if re.search(r"(^|\s)ncu\s+-", line) and "-i " not in line:
                 assert "--clock-control none" in line, (f, line)
+
+
+def test_missing_library_fails_loudly():
+    # without libtq.so every call raises: there is no fallback path
+    code = ("import turboquant_compressed_kv_tq_gb300 as tq\n"
+            "from turboquant_compressed_kv_tq_gb300 import _lib, build\n"
+            "build.LIB = '/nonexistent/libtq.so'\n"
+            "try:\n"
+            "    tq.tq_abi_version()\n"
+            "except RuntimeError as e:\n"
+            "    print('raised', 'not built' in str(e))\n")
+    r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0 and r.stdout.strip() == "raised True", (r.stdout, r.stderr)
