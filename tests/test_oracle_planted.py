@@ -62,6 +62,10 @@ MUTANTS = [
     ("group_min_from_max", "mh = tqo_f32_to_f16(lo);", "mh = tqo_f32_to_f16(hi);", 1),
     # dequantisers: the vector norm dropped
     ("dequant_norm_dropped", "out[v * D + d] = (double)norm[v] * s;", "out[v * D + d] = s;", 2),
+    # attention: the score scale applied twice
+    ("score_scale_squared", "s[t] = a * scale;", "s[t] = a * scale * scale;", 1),
+    # rotated decode: the key norm dropped from the score
+    ("key_norm_dropped_in_decode", "double s = scale * (double)knorm[t] * a;", "double s = scale * a;", 1),
     # attention: the causal window one token short, everywhere
     ("causal_off_by_one", "const int64_t nv = N - Lq + l + 1;", "const int64_t nv = N - Lq + l;", 2),
     # rotated decode: q'' = S^T q' instead of S q'
