@@ -72,12 +72,16 @@ def _vectors(n, D, dtype, seed, group=None):
 CODECS = [(1, 2), (1, 3), (1, 4), (1, 5), (0, 1), (0, 2), (0, 3), (0, 4)]
 
 
-@pytest.mark.parametrize("D", [64, 128, 256])
-@pytest.mark.parametrize("mode,bits", CODECS)
-@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16, torch.float16])
+# every head_dim and codec in bf16; the f32 and f16 inputs on one shape
+QUANT_CASES = [pytest.param(D, m, b, torch.bfloat16, id=f"bf16-d{D}-mode{m}-b{b}")
+               for D in (64, 128, 256) for m, b in CODECS] + \
+              [pytest.param(128, m, b, dt, id=f"{name}-d128-mode{m}-b{b}")
+               for dt, name in ((torch.float32, "f32"), (torch.float16, "f16"))
+               for m, b in CODECS if b in (3, 4)]
+
+
+@pytest.mark.parametrize("D,mode,bits,dtype", QUANT_CASES)
 def test_quantize_bit_exact(D, mode, bits, dtype):
-    if dtype != torch.bfloat16 and (D != 128 or bits not in (3, 4)):
-        pytest.skip("dtype sweep on one shape")
     n = 3000 if D <= 128 else 1500
     x = _vectors(n, D, dtype, D * 100 + bits * 10 + mode)
     if dtype == torch.float16:
