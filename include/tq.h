@@ -413,15 +413,24 @@ tq_status tq_prefill_attention(const tq_codec *key_codec, const tq_codec *value_
  * not allocate once running (an allocation can block on the device or fail
  * under memory pressure mid-request). Arguments and results are those of
  * tq_decode_attention; the scratch it needs lives instead in a fixed device
- * array of TQ_NOALLOC_SCRATCH_BYTES that every GPU loading this library keeps
- * until the process exits. Nothing is allocated by this call.
- *   - Returns TQ_ERR_CAPACITY when tq_decode_workspace_bytes() for these sizes
- *     exceeds TQ_NOALLOC_SCRATCH_BYTES (use tq_decode_attention instead).
- *   - The first call on a device looks up the array's device address (with
- *     that device current); make that first call before any stream capture.
+ * array of TQ_NOALLOC_SCRATCH_BYTES that every GPU where this library is set
+ * up keeps until the process exits. Nothing is allocated by this call.
+ *   - The array is reserved, and its device address looked up, when the
+ *     library is first set up on a device: by the first tq_codec_create,
+ *     tq_codec_create_group or tq_codec_pair_for_bits with that device
+ *     current. On a device never set up, this call fails as
+ *     tq_decode_attention does with no workspace (TQ_ERR_INVALID_ARG).
+ *   - Returns the statuses of tq_decode_attention for the same arguments,
+ *     checked in the same order, with TQ_ERR_CAPACITY (nothing launched)
+ *     when tq_decode_workspace_bytes() for these sizes exceeds
+ *     TQ_NOALLOC_SCRATCH_BYTES (use tq_decode_attention instead).
  *   - All calls on a device share the one array, which keeps the last call's
  *     contents: calls that overlap on the GPU (other streams, or other host
  *     threads) race and corrupt each other's results. Serialise them.
+ *   - The cached address belongs to the device's primary context: resetting
+ *     the device (cudaDeviceReset) while this library is loaded is not
+ *     supported, by this call or by any other (the per-device error word's
+ *     address is cached the same way).
  */
 #define TQ_NOALLOC_SCRATCH_BYTES (16u << 20)
 tq_status tq_decode_attention_noalloc(const tq_codec *key_codec, const tq_codec *value_codec,

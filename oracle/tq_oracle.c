@@ -37,8 +37,8 @@
  *       code = clamp(rint((x - min)/scale)), values are not rotated;
  *  [R7] decode: contiguous GQA grouping, query l of Lq sees keys
  *       t <= N - Lq + l;
- *  [R10] stored codebook: the half-precision values nearest to the Lloyd-Max
- *       levels, thresholds at the exact midpoints of adjacent stored levels.
+ *  [R10] stored codebook: the fp32 roundings of the fp64 Lloyd-Max levels and
+ *       of the fp64 midpoints between adjacent levels.
  */
 #include "tq_oracle.h"
 
@@ -233,18 +233,6 @@ int tqo_lloyd_max(int D, int b, double *c, double *m) {
     return it;
 }
 
-/* Nearest binary16 value of x (ties to even), computed in double: in the
- * normal range the grid spacing is 2^(floor(log2|x|) - 10), below 2^-14 it is
- * 2^-24; values past the largest finite half are not needed here. */
-static double round_to_half_grid(double x) {
-    if (x == 0.0) return x;
-    int e;
-    (void)frexp(x, &e); /* |x| = f * 2^e, f in [0.5, 1) */
-    int q = e - 11;     /* exponent of the spacing: floor(log2|x|) - 10 */
-    if (q < -24) q = -24;
-    return ldexp(rint(ldexp(x, -q)), q);
-}
-
 int tqo_index_bits(int bits, int mode) { return mode == TQO_PROD ? bits - 1 : bits; }
 
 int tqo_packed_words(int D, int ib) { return (D * ib + 31) / 32; }
@@ -283,12 +271,10 @@ int tqo_codec_tables(int D, int bits, int mode, uint64_t seed,
     int L = 1 << ib;
     double c64[256], m64[255];
     tqo_lloyd_max(D, ib, c64, m64);
-    /* [R10] the stored levels are the half-precision numbers nearest to the
-     * fp64 levels, so that a half-precision operand holds them exactly; the
-     * decision thresholds are the exact midpoints of adjacent stored levels. */
-    (void)m64;
-    for (int j = 0; j < L; ++j) c[j] = (float)round_to_half_grid(c64[j]);
-    for (int j = 0; j + 1 < L; ++j) m[j] = (float)(0.5 * ((double)c[j] + (double)c[j + 1]));
+    /* The stored levels and decision thresholds are the fp32 numbers nearest
+     * to the fp64 Lloyd-Max levels and to the fp64 midpoints between them. */
+    for (int j = 0; j < L; ++j) c[j] = (float)c64[j];
+    for (int j = 0; j + 1 < L; ++j) m[j] = (float)m64[j];
     return 0;
 }
 

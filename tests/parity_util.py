@@ -154,3 +154,40 @@ def read_records(layer_pool: np.ndarray, kc: O.Codec, vc: O.Codec, Hkv: int, BT:
     else:
         vrec["norm"] = out["v_norm"][:, 0]
     return krec, vrec
+
+
+def read_records_blocks(layer_pool: np.ndarray, kc: O.Codec, vc: O.Codec, Hkv: int, BT: int, table,
+                        max_blocks: int, seq: int, h: int, n: int):
+    """Records of tokens [0, n) of (seq, head h), gathered a whole block at a
+    time (the same layout as ``read_records``; fast enough for full-size
+    sequences)."""
+    sub, off = O.subblock_layout(kc, vc, BT)
+    Wk, Wv, Ws = kc.W, vc.W, kc.D // 32
+    ng = vc.D // vc.group if vc.mode == O.GROUP else 0
+    fields = [(0, Wk, np.uint32, "k_idx"), (2, 1, np.float32, "k_norm"), (4, Wv, np.uint32, "v_idx")]
+    if kc.mode == O.PROD:
+        fields += [(1, Ws, np.uint32, "k_sgn"), (3, 1, np.float32, "k_rnorm")]
+    if vc.mode == O.GROUP:
+        fields += [(5, ng, np.uint16, "v_scale"), (6, ng, np.uint16, "v_min")]
+    else:
+        fields += [(5, 1, np.float32, "v_norm")]
+    parts = {name: [] for *_, name in fields}
+    nblk = (n + BT - 1) // BT
+    for lb in range(nblk):
+        pb = int(table[seq, lb]) if table is not None else seq * max_blocks + lb
+        base = (pb * Hkv + h) * sub
+        take = min(BT, n - lb * BT)
+        for k, count, dt, name in fields:
+            size = np.dtype(dt).itemsize * count
+            a = base + off[k]
+            parts[name].append(layer_pool[a:a + BT * size].view(dt).reshape(BT, count)[:take])
+    out = {name: np.concatenate(v) for name, v in parts.items()}
+    krec = {"idx": out["k_idx"], "norm": out["k_norm"][:, 0]}
+    if kc.mode == O.PROD:
+        krec["sgn"], krec["rnorm"] = out["k_sgn"], out["k_rnorm"][:, 0]
+    vrec = {"idx": out["v_idx"]}
+    if vc.mode == O.GROUP:
+        vrec["scale"], vrec["min"] = out["v_scale"], out["v_min"]
+    else:
+        vrec["norm"] = out["v_norm"][:, 0]
+    return krec, vrec

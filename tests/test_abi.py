@@ -179,6 +179,17 @@ def test_decode_plan_rejects_bad_sizes(libtq):
     assert libtq.tq_decode_plan(ctypes.byref(d), 1, 8 * 65, 1, 100, 152, ctypes.byref(info)) == _lib.TQ_ERR_UNSUPPORTED
 
 
+def test_workspace_query_rejects_a_descriptor_without_heads(libtq):
+    # checked on the host before any division by the head count or device call
+    d = _desc_from_oracle(128, ("prod", 3), ("mse", 3, 0), 256, 8)
+    d.num_kv_heads = 0
+    n = ctypes.c_size_t(0)
+    assert libtq.tq_decode_workspace_bytes(ctypes.byref(d), 1, 64, 2, 100, ctypes.byref(n)) == _lib.TQ_ERR_INVALID_ARG
+    d.num_kv_heads = 8
+    d.block_tokens = 24
+    assert libtq.tq_decode_workspace_bytes(ctypes.byref(d), 1, 64, 2, 100, ctypes.byref(n)) == _lib.TQ_ERR_INVALID_ARG
+
+
 def test_decode_plan_simt_shapes(libtq):
     # head_dim 64 and 256 take the SIMT kernels: no tensor-core shared memory
     for D, key, value in [(256, ("prod", 3), ("group", 2, 32)), (64, ("mse", 2), ("mse", 2, 0))]:

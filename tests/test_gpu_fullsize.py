@@ -9,10 +9,13 @@ head) outputs element by element against the oracle's decode of its own
 records, and checks the rest by properties that hold at any size (the device
 error word stays clear, every output is finite).
 
-The caches are written with the exact encode policy, so the GPU and the
+Most caches are written with the exact encode policy, so the GPU and the
 oracle decode identical records and the comparison measures the decode alone
 (the tensor-core prefill may differ from the oracle's codes inside the fp32
-tie band, which tests/test_gpu_encode_tc.py checks on its own).
+tie band, which tests/test_gpu_encode_tc.py checks on its own). The benchmark
+itself prefills with the tensor-core encoder: its test reads the records the
+GPU wrote back to the host and holds the GPU decode of them to the decode
+tolerance against the oracle's decode of the same records.
 """
 import numpy as np
 import pytest
@@ -20,7 +23,8 @@ import torch
 
 import turboquant_compressed_kv_tq_gb300 as tq
 from turboquant_compressed_kv_tq_gb300 import workloads as wl
-from parity_util import GpuCase, compare_decode, oracle_decode, to_f32_np
+import oracle as O
+from parity_util import GpuCase, compare_decode, oracle_codec, oracle_decode, read_records_blocks, to_f32_np
 
 pytestmark = pytest.mark.gpu
 
@@ -41,15 +45,17 @@ def _head_kv(w, layer, seq, n, h):
     return to_f32_np(k), to_f32_np(v)
 
 
-def test_long_context_full_size_bench_configuration():
+def _long_context_cache(layer, exact_encode):
+    """One layer of the 256k workload, prefilled in 8192-token chunks and
+    grown by one 2-token append, as the benchmark builds it."""
     w = wl.long_256k()
-    layer, D, Hkv, Hq, Lq, BT = 37, w.head_dim, w.num_kv_heads, w.num_q_heads, w.q_len, w.block_tokens
+    D, Hkv, Hq, Lq, BT = w.head_dim, w.num_kv_heads, w.num_q_heads, w.q_len, w.block_tokens
     N0, A, C = w.seq_lens[0], w.append_per_step, w.prefill_chunk
     cap = N0 + A
     nblk = (cap + BT - 1) // BT
     kc = tq.Codec(D, w.key.bits, w.key.mode, w.key.seed)
     vc = tq.Codec(D, w.value.bits, w.value.mode, w.value.seed)
-    cache = tq.CompressedKVCache(kc, vc, 1, nblk, BT, Hkv, DEV, exact_encode=True)
+    cache = tq.CompressedKVCache(kc, vc, 1, nblk, BT, Hkv, DEV, exact_encode=exact_encode)
     starts = torch.arange(0, N0, C, dtype=torch.int32, device=DEV)
     for c in range(N0 // C):
         k = wl.kv_chunk(w, layer, 0, c * C, C, "k", DEV).unsqueeze(0)
@@ -67,11 +73,32 @@ def test_long_context_full_size_bench_configuration():
     assert tq.tq_device_error() == 0
     out = to_f32_np(out)
     assert np.isfinite(out).all()
-    qn = to_f32_np(q).astype(np.float64)
+    return w, cache, nblk, cap, to_f32_np(q).astype(np.float64), out
+
+
+def test_long_context_full_size_bench_configuration():
+    layer = 37
+    w, cache, nblk, cap, qn, out = _long_context_cache(layer, exact_encode=True)
     G = w.gqa
     for h in (0, 5):
         K, V = _head_kv(w, layer, 0, cap, h)
         ref = oracle_decode(w, K, V, qn[0, h * G:(h + 1) * G])
+        compare_decode(out[0, h * G:(h + 1) * G], ref)
+
+
+def test_long_context_tensor_core_prefill_decode_tolerance():
+    # the benchmark's own composition: prefill on the tensor-core encoder
+    # (the default policy), then decode; the oracle decodes the records the
+    # GPU wrote, so every difference left is the decode's
+    layer = 11
+    w, cache, nblk, cap, qn, out = _long_context_cache(layer, exact_encode=False)
+    assert cache.desc.encode_policy == tq.TQ_ENCODE_AUTO
+    kc, vc = oracle_codec(w.key, w.head_dim), oracle_codec(w.value, w.head_dim)
+    pool = cache.pool.cpu().numpy()
+    G = w.gqa
+    for h in (0, 3, 6):
+        krec, vrec = read_records_blocks(pool, kc, vc, w.num_kv_heads, w.block_tokens, None, nblk, 0, h, cap)
+        ref = O.decode_rotated(qn[0, h * G:(h + 1) * G], kc, krec, vc, vrec, 1 / np.sqrt(w.head_dim), w.q_len)
         compare_decode(out[0, h * G:(h + 1) * G], ref)
 
 

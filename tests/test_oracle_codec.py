@@ -145,16 +145,31 @@ def test_codec_determinism_and_seed_separation(oracle_lib):
     assert a.ib == 2 and np.array_equal(a.c, mse2.c) and np.array_equal(a.R, mse2.R)
 
 
-@pytest.mark.parametrize("D,bits,mode", [(128, 3, O.PROD), (128, 4, O.MSE), (256, 3, O.MSE), (64, 1, O.MSE)])
-def test_stored_levels_are_nearest_halves(oracle_lib, D, bits, mode):
-    # the stored codebook is the IEEE half rounding of the fp64 Lloyd-Max levels
-    # and the thresholds are the exact midpoints of adjacent stored levels
+@pytest.mark.parametrize("D,bits,mode", [(128, 3, O.PROD), (128, 4, O.MSE), (256, 3, O.MSE), (64, 1, O.MSE),
+                                         (128, 2, O.MSE), (256, 5, O.PROD)])
+def test_stored_fp32_levels_meet_lloyd_max_conditions(oracle_lib, D, bits, mode):
+    # The codec's stored fp32 tables, checked directly against the Lloyd-Max
+    # conditions by independent adaptive quadrature: each stored level is the
+    # centroid of the cell that the stored thresholds bound, and each stored
+    # threshold is the midpoint of its two stored levels, both to fp32
+    # precision (a few units in the last place).
     cd = O.Codec(D, bits, mode, 1)
-    c64, _, _ = O.lloyd_max(D, cd.ib)
-    assert np.array_equal(cd.c.astype(np.float64), c64.astype(np.float16).astype(np.float64))
-    mid = (cd.c[:-1].astype(np.float64) + cd.c[1:].astype(np.float64)) / 2
-    assert np.array_equal(cd.m.astype(np.float64), mid)
+    c = cd.c.astype(np.float64)
+    m = cd.m.astype(np.float64)
+    ulp = lambda x: np.spacing(np.float32(abs(x))).astype(np.float64)
+    f = _density(D)
+    edges = np.concatenate([[-1.0], m, [1.0]])
+    for j in range(len(c)):
+        lo, hi = edges[j], edges[j + 1]
+        num = integrate.quad(lambda t: t * f(t), lo, hi, epsabs=0, epsrel=1e-13, limit=200)[0]
+        den = integrate.quad(f, lo, hi, epsabs=0, epsrel=1e-13, limit=200)[0]
+        assert abs(num / den - c[j]) <= 2 * ulp(c[j]), (j, num / den, c[j])
+    for j in range(len(m)):
+        assert abs((c[j] + c[j + 1]) / 2 - m[j]) <= ulp(m[j]) + 1e-300, (j, m[j])
     assert np.array_equal(cd.c[::-1], -cd.c)
+    # levels are not rounded to a coarser grid: at least one level needs more
+    # than the 11 significant bits of a half-precision number
+    assert not np.array_equal(c, c.astype(np.float16).astype(np.float64))
 
 
 def test_fractional_bits_split(oracle_lib):

@@ -30,6 +30,9 @@ tq_status device_state(unsigned** err, int* num_sms) {
     if (!g_err_ptr[dev]) {
         void* p = nullptr;
         if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return TQ_ERR_CUDA;
+        // the allocation-free decode's fixed scratch array is reserved here, when
+        // the library is first set up on the device, not by that entry point
+        if (noalloc_reserve() != TQ_OK) return TQ_ERR_CUDA;
         int sms = 0;
         if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return TQ_ERR_CUDA;
         g_err_ptr[dev] = static_cast<unsigned*>(p);
@@ -61,6 +64,7 @@ void free_codec(tq_codec* c) {
     cudaFree(c->d_St);
     cudaFree(c->d_c);
     cudaFree(c->d_m);
+    cudaFree(c->d_cq);
     cudaFree(c->d_Rtc);
     cudaFree(c->d_Stc);
     if (prev >= 0) cudaSetDevice(prev);
@@ -90,6 +94,8 @@ CodecDev dev_view(const tq_codec* c) {
     d.St = c->d_St;
     d.c = c->d_c;
     d.m = c->d_m;
+    d.cq = c->d_cq;
+    d.cq_scale = c->host.op_scale;
     d.Rtc = c->d_Rtc;
     d.Stc = c->d_Stc;
     d.D = c->head_dim;
@@ -187,6 +193,7 @@ tq_status tq_codec_create(int head_dim, int bits, tq_mode mode, uint64_t seed, t
     if (st == TQ_OK && mode == TQ_MODE_PROD) st = upload(&c->d_St, transpose(c->host.qjl, head_dim));
     if (st == TQ_OK) st = upload(&c->d_c, c->host.centroids);
     if (st == TQ_OK) st = upload(&c->d_m, c->host.midpoints);
+    if (st == TQ_OK) st = upload(&c->d_cq, c->host.op_levels);
     if (st == TQ_OK && head_dim <= 128) {
         // tensor-core operands for the chunked-prefill encoder: 16 R and S, fp16 hi + lo
         std::vector<uint16_t> op;
@@ -492,7 +499,9 @@ tq_status tq_decode_plan(const tq_cache_desc* cache, int batch, int num_q_heads,
 tq_status tq_decode_workspace_bytes(const tq_cache_desc* cache, int batch, int num_q_heads, int q_len,
                                     int max_seq_len, size_t* bytes) {
     if (!cache || !bytes || batch < 0 || q_len <= 0 || max_seq_len < q_len) return TQ_ERR_INVALID_ARG;
-    if (num_q_heads <= 0 || num_q_heads % cache->num_kv_heads != 0) return TQ_ERR_INVALID_ARG;
+    if (num_q_heads <= 0 || cache->num_kv_heads <= 0 || num_q_heads % cache->num_kv_heads != 0)
+        return TQ_ERR_INVALID_ARG;
+    if (cache->block_tokens < 16 || (cache->block_tokens & (cache->block_tokens - 1)) != 0) return TQ_ERR_INVALID_ARG;
     const int G = num_q_heads / cache->num_kv_heads;
     if (G * q_len > 64) return TQ_ERR_UNSUPPORTED;
     int sms = 0;

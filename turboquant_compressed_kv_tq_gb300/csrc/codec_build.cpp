@@ -10,8 +10,8 @@
 //   rotation: Householder QR of the Gaussian matrix (row-major fill), every
 //            sum in ascending index order without fused multiply-add, then
 //            the columns signed so that R's diagonal is positive;
-//   codebook: Lloyd iteration on (1-t^2)^((D-3)/2) over [-1, 1], levels
-//            stored as the nearest half-precision numbers.
+//   codebook: Lloyd iteration on (1-t^2)^((D-3)/2) over [-1, 1]; levels and
+//            midpoints stored as the nearest fp32 numbers.
 // This file must be compiled without floating-point contraction.
 #include "tq_internal.h"
 
@@ -239,20 +239,62 @@ void build_tc_operand(const std::vector<float>& M, int D, double scale, std::vec
         }
 }
 
+// Scale of the half-precision operand levels: the alpha in [1, 2) (on a grid
+// of 2^-21) minimising the largest relative error of rounding alpha * |c_j|
+// to fp16 over the distinct magnitudes; ties keep the smaller alpha. The
+// decode multiplies fp16 levels with fp16 query or weight operands on the
+// tensor cores; a well-chosen common scale leaves one or two magnitudes
+// (1- and 2-bit codebooks) almost exact and cuts the error of the larger
+// codebooks several-fold compared with rounding the levels themselves.
+static double operand_scale(const std::vector<float>& levels) {
+    std::vector<double> mags;
+    for (float v : levels)
+        if (v > 0.0f) mags.push_back(static_cast<double>(v));
+    if (mags.empty()) return 1.0;
+    double best_err = INFINITY, best = 1.0;
+    constexpr int kSteps = 1 << 21;
+    for (int i = 0; i < kSteps; ++i) {
+        const double a = 1.0 + std::ldexp(static_cast<double>(i), -21);
+        double worst = 0.0;
+        for (double m : mags) {
+            const double v = a * m;
+            const double e = std::fabs(nearest_half(v) - v) / v;
+            if (e > worst) {
+                worst = e;
+                if (worst >= best_err) break;
+            }
+        }
+        if (worst < best_err) {
+            best_err = worst;
+            best = a;
+        }
+    }
+    return best;
+}
+
 void build_codec_tables(int D, int index_bits, bool with_qjl, uint64_t seed, HostTables& out) {
     static std::mutex mu;
-    static std::map<std::pair<int, int>, std::pair<std::vector<double>, std::vector<double>>> cache;
+    struct Levels {
+        std::vector<double> c, m;
+        double scale;
+    };
+    static std::map<std::pair<int, int>, Levels> cache;
     std::vector<double> c, m;
+    double scale = 1.0;
     {
         std::lock_guard<std::mutex> lk(mu);
         auto key = std::make_pair(D, index_bits);
         auto it = cache.find(key);
         if (it == cache.end()) {
             lloyd_max_levels(D, index_bits, c, m);
-            cache[key] = {c, m};
+            std::vector<float> cf(c.size());
+            for (size_t i = 0; i < c.size(); ++i) cf[i] = static_cast<float>(c[i]);
+            scale = operand_scale(cf);
+            cache[key] = {c, m, scale};
         } else {
-            c = it->second.first;
-            m = it->second.second;
+            c = it->second.c;
+            m = it->second.m;
+            scale = it->second.scale;
         }
     }
     const std::vector<double> R = haar_rotation(D, seed);
@@ -264,15 +306,16 @@ void build_codec_tables(int D, int index_bits, bool with_qjl, uint64_t seed, Hos
         out.qjl.resize(S.size());
         for (size_t i = 0; i < S.size(); ++i) out.qjl[i] = static_cast<float>(S[i]);
     }
-    // Stored levels: the nearest half-precision numbers to the fp64 levels
-    // (exact fp16 operands for the tensor-core decode); thresholds: exact
-    // midpoints of adjacent stored levels.
+    // Stored levels and thresholds: the fp32 numbers nearest to the fp64
+    // levels and to the fp64 midpoints between adjacent levels.
     out.centroids.resize(c.size());
-    for (size_t i = 0; i < c.size(); ++i) out.centroids[i] = static_cast<float>(nearest_half(c[i]));
+    for (size_t i = 0; i < c.size(); ++i) out.centroids[i] = static_cast<float>(c[i]);
     out.midpoints.resize(m.size());
-    for (size_t i = 0; i < m.size(); ++i)
-        out.midpoints[i] = static_cast<float>((static_cast<double>(out.centroids[i]) +
-                                               static_cast<double>(out.centroids[i + 1])) * 0.5);
+    for (size_t i = 0; i < m.size(); ++i) out.midpoints[i] = static_cast<float>(m[i]);
+    out.op_scale = static_cast<float>(scale);
+    out.op_levels.resize(c.size());
+    for (size_t i = 0; i < c.size(); ++i)
+        out.op_levels[i] = static_cast<float>(nearest_half(scale * static_cast<double>(out.centroids[i])));
 }
 
 }  // namespace tq

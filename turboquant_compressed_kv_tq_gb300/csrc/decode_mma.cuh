@@ -9,7 +9,11 @@
 //           decoded from the packed indices straight into MMA fragments:
 //           2-bit indices through a shared table of code quads (one 64-bit
 //           load per four levels), other widths with byte-permute lookups in
-//           registers; QJL signs as +-gamma fp16 operands;
+//           registers; QJL signs as exact +-1 operands, their products
+//           weighted by the residual norm in fp32; codebook operands are the
+//           fp16 numbers nearest to op_scale * level (a per-codebook scale
+//           that keeps the rounding error small), op_scale divided out in the
+//           query (keys) and in the merge (values);
 //   softmax online, in log2 units (scale * log2(e) folded into the query),
 //           with a lagging row maximum;
 //   values  O += P' V_hat on mma.sync, P' = p * value norm, V_hat decoded per

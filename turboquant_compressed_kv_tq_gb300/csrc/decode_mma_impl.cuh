@@ -195,8 +195,10 @@ __device__ __forceinline__ void qfrag_body(const MmaArgs& m, unsigned char* qsm_
             __syncthreads();
         }
         // entry (row rr, which, ks, j, e): lane 4*(rr%8)+j, register 2e + (rr >= 8)
-        const float s1 = a.scale * kLog2e;
-        const float s2 = s1 * kSqrtHalfPi / static_cast<float>(kD);
+        // the key codebook operand is fp16(op_scale * level): the q' operand
+        // carries 1 / op_scale so that their product is q' * level
+        const float s1 = a.scale * kLog2e / a.kc.cq_scale;
+        const float s2 = a.scale * kLog2e * kSqrtHalfPi / static_cast<float>(kD);
         uint32_t* dst = reinterpret_cast<uint32_t*>(const_cast<uint4*>(m.qfrag)) + static_cast<int64_t>(unit) * 2 * 8 * 32 * 4;
         for (int e = tid; e < kRows * 128; e += kQThreads) {
             const int rr = e >> 7, x = e & 127;
@@ -343,7 +345,9 @@ __device__ __forceinline__ void merge_unit(const MmaArgs& m, int unit, int split
                 acc[6] = fmaf(wt, v1.z, acc[6]); acc[7] = fmaf(wt, v1.w, acc[7]);
             }
         }
-        const float inv = L > 0.0f ? 1.0f / L : 0.0f;
+        // MSE values were multiplied as fp16(op_scale * level): divide op_scale out
+        const float vs = VGROUP ? 1.0f : a.vc.cq_scale;
+        const float inv = L > 0.0f ? 1.0f / (L * vs) : 0.0f;
         for (int k = 0; k < 8; ++k) orot[r * kStride + dbase + k] = acc[k] * inv;
     }
     __syncthreads();
@@ -410,22 +414,22 @@ __global__ void __launch_bounds__(kThreads, 1) split_mma_kernel(MmaArgs m) {
     // 2-bit keys decode through the shared quad table, others in registers
     constexpr bool kQuadTab = quad_keys(KB, KPROD, VGROUP);
     typename MseTable<KB>::type ktab{};
-    if constexpr (!kQuadTab) ktab = mse_table<KB>(a.kc.c);
+    if constexpr (!kQuadTab) ktab = mse_table<KB>(a.kc.cq);
     uint32_t kt_lane = 0;
     if constexpr (kQuadTab) {
         kt_lane = smem_u32(smem + st.kt_off) + 8u * (lane & 15);
         uint2* tab = reinterpret_cast<uint2*>(smem + st.kt_off);
         for (int i = threadIdx.x; i < 256 * 16; i += kThreads) {
             const int e = i >> 4;
-            const uint32_t c0 = h_bits(__ldg(a.kc.c + (e & 3))), c1 = h_bits(__ldg(a.kc.c + ((e >> 2) & 3)));
-            const uint32_t c2 = h_bits(__ldg(a.kc.c + ((e >> 4) & 3))), c3 = h_bits(__ldg(a.kc.c + (e >> 6)));
+            const uint32_t c0 = h_bits(__ldg(a.kc.cq + (e & 3))), c1 = h_bits(__ldg(a.kc.cq + ((e >> 2) & 3)));
+            const uint32_t c2 = h_bits(__ldg(a.kc.cq + ((e >> 4) & 3))), c3 = h_bits(__ldg(a.kc.cq + (e >> 6)));
             tab[i] = make_uint2(c0 | (c1 << 16), c2 | (c3 << 16));
         }
     }
     // 3-bit MSE values decode through the shared pair table, others in registers
     constexpr bool kPairTab = !VGROUP && VB == 3;
     typename MseTable<VGROUP ? 2 : VB>::type vtab{};
-    if constexpr (!VGROUP && !kPairTab) vtab = mse_table<VB>(a.vc.c);
+    if constexpr (!VGROUP && !kPairTab) vtab = mse_table<VB>(a.vc.cq);
     uint32_t vt_lane = 0;
     if constexpr (kPairTab) {
         const uint32_t region = smem_u32(smem + st.vt_off);
@@ -434,7 +438,7 @@ __global__ void __launch_bounds__(kThreads, 1) split_mma_kernel(MmaArgs m) {
         uint32_t* tab = reinterpret_cast<uint32_t*>(smem + st.vt_off + (base - region));
         for (int i = threadIdx.x; i < 64 * 32; i += kThreads) {
             const int e = i >> 5;
-            tab[i] = h_bits(__ldg(a.vc.c + (e & 7))) | (h_bits(__ldg(a.vc.c + (e >> 3))) << 16);
+            tab[i] = h_bits(__ldg(a.vc.cq + (e & 7))) | (h_bits(__ldg(a.vc.cq + (e >> 3))) << 16);
         }
     }
 
@@ -556,7 +560,10 @@ __global__ void __launch_bounds__(kThreads, 1) split_mma_kernel(MmaArgs m) {
             // QJL part or low half of the split query) keep four MMAs in flight
             float sc[2][4], sd[2][4];
             uint32_t hk[2][16];
-            uint32_t sw[2], neg2[2];
+            uint32_t sw[2];
+            // QJL signs as exact +-1 operands; the residual norm multiplies the
+            // sign products in fp32 below
+            constexpr uint32_t neg2 = 0xBC00BC00u;  // (-1, -1): a set bit gives +1
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt) {
                 sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.0f;
@@ -566,10 +573,7 @@ __global__ void __launch_bounds__(kThreads, 1) split_mma_kernel(MmaArgs m) {
                 load_words<KB>(kidx + tau * (4 * KB) + j * KB, kw);
                 if constexpr (kQuadTab) quad2_chunk(kw, kt_lane, hk[nt]);
                 else mse_chunk<KB>(kw, ktab, hk[nt]);
-                if constexpr (KPROD) {
-                    sw[nt] = ksgn[tau * 4 + j];
-                        neg2[nt] = dup_half(h_bits(-krn[tau]));
-                }
+                if constexpr (KPROD) sw[nt] = ksgn[tau * 4 + j];
             }
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks) {
@@ -584,15 +588,25 @@ __global__ void __launch_bounds__(kThreads, 1) split_mma_kernel(MmaArgs m) {
                 for (int nt = 0; nt < 2; ++nt) {
                     mma16816(sc[nt], qa, hk[nt][2 * ks], hk[nt][2 * ks + 1]);
                     if constexpr (KPROD)
-                        mma16816(sd[nt], qj, dec1(sw[nt], 15 - ks, neg2[nt]), dec1(sw[nt], 7 - ks, neg2[nt]));
+                        mma16816(sd[nt], qj, dec1(sw[nt], 15 - ks, neg2), dec1(sw[nt], 7 - ks, neg2));
                     else
                         mma16816(sd[nt], qj, hk[nt][2 * ks], hk[nt][2 * ks + 1]);
                 }
             }
 #pragma unroll
-            for (int nt = 0; nt < 2; ++nt)
+            for (int nt = 0; nt < 2; ++nt) {
+                if constexpr (KPROD) {
+                    // codebook part + residual norm x QJL part, per token column
+                    const float2 gm = *reinterpret_cast<const float2*>(krn + 16 * u + 8 * nt + 2 * j);
+                    sc[nt][0] = fmaf(gm.x, sd[nt][0], sc[nt][0]);
+                    sc[nt][1] = fmaf(gm.y, sd[nt][1], sc[nt][1]);
+                    sc[nt][2] = fmaf(gm.x, sd[nt][2], sc[nt][2]);
+                    sc[nt][3] = fmaf(gm.y, sd[nt][3], sc[nt][3]);
+                } else {
 #pragma unroll
-                for (int e = 0; e < 4; ++e) sc[nt][e] += sd[nt][e];
+                    for (int e = 0; e < 4; ++e) sc[nt][e] += sd[nt][e];
+                }
+            }
             // ---------------- values of the same 16 tokens: decoded while the score MMAs
             // are in flight (independent of the scores)
             uint32_t hA[16], hB[16];

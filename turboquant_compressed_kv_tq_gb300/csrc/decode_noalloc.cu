@@ -9,7 +9,10 @@
 // the scratch workspace that tq_decode_attention takes. This entry point runs
 // the same decode with its scratch in a fixed, file-scope device array instead:
 // every GPU that loads the library reserves kScratchBytes for it until the
-// process exits, and no call here allocates.
+// process exits, and no call here allocates. The array is reserved when the
+// library is first set up on a device (the first codec created there): CUDA
+// loads a module's device arrays lazily, so the set-up looks up the array's
+// address then, and this entry point only reuses it.
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -48,6 +51,13 @@ tq_status scratch_address(void** out) {
 
 }  // namespace
 
+namespace tq {
+tq_status noalloc_reserve() {
+    void* p = nullptr;
+    return scratch_address(&p);
+}
+}  // namespace tq
+
 extern "C" {
 
 tq_status tq_decode_attention_noalloc(const tq_codec* key_codec, const tq_codec* value_codec,
@@ -55,19 +65,26 @@ tq_status tq_decode_attention_noalloc(const tq_codec* key_codec, const tq_codec*
                                       int batch, int num_q_heads, int q_len, const int32_t* seq_lens,
                                       const int32_t* block_table, int max_blocks, int max_seq_len, float scale,
                                       float* out, tq_stream_t stream) {
-    size_t need = 0;
-    const tq_status st = tq_decode_workspace_bytes(cache, batch, num_q_heads, q_len, max_seq_len, &need);
-    if (st != TQ_OK) return st;
-    if (need > kScratchBytes) return TQ_ERR_CAPACITY;
+    // The array's address was looked up when the library was set up on this
+    // device; a device never set up (no codec created there) has none, and
+    // the call then fails as the regular entry point does without a workspace.
     void* scratch = nullptr;
-    const tq_status sa = scratch_address(&scratch);
-    if (sa != TQ_OK) return sa;
-    // The decode kernels write every partial they read and the query-prep
-    // kernel zeroes the arrival counters at the start of each call, so the
-    // previous call's contents of the array need no clearing here.
+    int dev = -1;
+    if (cudaGetDevice(&dev) == cudaSuccess && dev >= 0 && dev < kMaxDevices) {
+        std::lock_guard<std::mutex> lk(g_scratch_mu);
+        scratch = g_scratch_ptr[dev];
+    } else {
+        (void)cudaGetLastError();  // no device: the checks below refuse the call
+    }
+    // The regular entry point checks every argument first, in its own order,
+    // and returns TQ_ERR_CAPACITY without launching anything when the decode
+    // needs more scratch than the array holds. The decode kernels write every
+    // partial they read and the query-prep kernel zeroes the arrival counters
+    // at the start of each call, so the previous call's contents of the array
+    // need no clearing here.
     return tq_decode_attention(key_codec, value_codec, cache, layer, q, q_dtype, batch, num_q_heads, q_len,
                                seq_lens, block_table, max_blocks, max_seq_len, scale, out, scratch,
-                               kScratchBytes, stream);
+                               scratch ? kScratchBytes : 0, stream);
 }
 
 }  // extern "C"

@@ -272,9 +272,9 @@ __global__ void __launch_bounds__(kTThreads, 1) prefill_tc_kernel(TcPrefillArgs 
         }
         __syncwarp();
     } else {
-        const auto ktab = mse_table<KB>(a.kc.c);
+        const auto ktab = mse_table<KB>(a.kc.cq);
         typename MseTable<VGROUP ? 2 : VB>::type vtab{};
-        if constexpr (!VGROUP) vtab = mse_table<VB>(a.vc.c);
+        if constexpr (!VGROUP) vtab = mse_table<VB>(a.vc.cq);
         float m = -INFINITY;
 
         // ---------------- decode tile t into the operand buffers t & 1: one
@@ -575,7 +575,9 @@ __global__ void __launch_bounds__(kTThreads, 1) prefill_tc_kernel(TcPrefillArgs 
             tc::tmem_ld16(tL, w);
             l = w[0] + w[1];
         }
-        const float inv = (o_started && !failed && l > 0.0f) ? 1.0f / l : 0.0f;
+        // MSE values were multiplied as fp16(op_scale * level): divide op_scale out
+        const float vs = VGROUP ? 1.0f : a.vc.cq_scale;
+        const float inv = (o_started && !failed && l > 0.0f) ? 1.0f / (l * vs) : 0.0f;
         float v[32];
         tc::tmem_ld32(tO, v);
         // column 32 qt + 2p + odd holds coordinate 32 qt + (odd ? b : a) of value pair p

@@ -18,6 +18,13 @@ struct HostTables {
     std::vector<float> qjl;        // D x D row-major (prod only)
     std::vector<float> centroids;  // 2^index_bits, ascending, antisymmetric
     std::vector<float> midpoints;  // 2^index_bits - 1
+    // Half-precision operand levels of the tensor-core kernels: op_levels[j]
+    // is the fp16 number nearest to op_scale * centroids[j] (stored as fp32,
+    // exactly), with op_scale in [1, 2) chosen so that the largest relative
+    // rounding error over the levels is as small as a search finds; kernels
+    // divide op_scale out again in fp32.
+    std::vector<float> op_levels;
+    float op_scale = 1.0f;
 };
 
 // Deterministic codec tables from (D, index bits, seed) (host, fp64 -> fp32).
@@ -35,6 +42,8 @@ struct CodecDev {
     const float* St;   // [D][D] transposed QJL matrix (prod) or nullptr
     const float* c;    // centroids
     const float* m;    // midpoints
+    const float* cq;   // fp16-exact operand levels op_scale * c (see HostTables)
+    float cq_scale;    // op_scale
     const uint16_t* Rtc;  // tensor-core operand of 16 R (hi, lo), or nullptr
     const uint16_t* Stc;  // tensor-core operand of S (hi, lo) (prod), or nullptr
     int D;
@@ -167,6 +176,11 @@ cudaError_t launch_prefill(const DecodeArgs& a, const uint4* qfrag, cudaStream_t
 
 extern std::atomic<uint64_t> g_launches;
 
+// Looks up, once per device with that device current, the device address of
+// the fixed scratch array of tq_decode_attention_noalloc; loading the array's
+// module is what reserves its memory on the device.
+tq_status noalloc_reserve();
+
 }  // namespace tq
 
 // Opaque codec handle behind the C ABI.
@@ -187,6 +201,7 @@ struct tq_codec {
     float* d_St = nullptr;
     float* d_c = nullptr;
     float* d_m = nullptr;
+    float* d_cq = nullptr;
     uint16_t* d_Rtc = nullptr;
     uint16_t* d_Stc = nullptr;
 };
