@@ -227,6 +227,92 @@ tq_status tq_cache_desc_init(tq_cache_desc *desc, const tq_codec *key_codec,
 tq_status tq_cache_copy_blocks(const tq_cache_desc *src, const tq_cache_desc *dst, const int32_t *src_blocks,
                                const int32_t *dst_blocks, int n, tq_stream_t stream);
 
+/*
+ * A batch of sequences in a paged cache: the state that
+ * "omlx/turboquant_kv.py" (BatchTurboQuantKVCache) keeps per batch, on the
+ * paged layout. Row b of the block table lists the physical blocks of
+ * sequence b in token order (-1 = no block); seq_lens[b] counts its cached
+ * tokens, which occupy its first ceil(seq_lens[b] / block_tokens) blocks.
+ * Entries past those may hold blocks reserved for later appends.
+ */
+typedef struct {
+    const tq_cache_desc *cache; /* pool and layout holding the batch's blocks     */
+    int32_t *block_table;       /* device [capacity][max_blocks]                   */
+    int32_t *seq_lens;          /* device [capacity]                               */
+    int batch;                  /* sequences in use: rows 0 .. batch-1             */
+    int capacity;               /* rows that block_table and seq_lens hold         */
+    int max_blocks;             /* entries per block-table row                     */
+} tq_batch;
+
+/*
+ * The batch operations of "omlx/turboquant_kv.py" (BatchTurboQuantKVCache
+ * .filter, .extend, .merge, .extract) on the paged layout. Each checks the
+ * mixed-configuration guard of .merge on the host (TQ_ERR_CONFIG_MISMATCH
+ * unless every cache involved has the same head_dim, KV heads, block size,
+ * layer count and key/value codec configuration), then rewrites block-table
+ * rows and sequence lengths on the device and, where a sequence moves to
+ * another pool, copies its blocks (every layer). Ragged lengths need no
+ * padding, so the pages' left-padding realignment (prepare, finalize, the
+ * padding arithmetic of extend and extract) has no counterpart here.
+ *
+ * Blocks taken in a destination pool come from the caller's free list:
+ * free_blocks (device int32 [n_free]) is consumed in order from index
+ * *n_used (device int32, read and advanced by the call; zero it before a
+ * first call). A sequence whose blocks do not fit gets -1 entries and sets
+ * TQ_DEVERR_CAPACITY; a source block id outside its pool is skipped and
+ * sets TQ_DEVERR_BLOCK; a length beyond its row's blocks sets
+ * TQ_DEVERR_SEQLEN (tq_device_error). Where source and destination share a
+ * pool (the same pool pointer), rows keep their block ids and nothing is
+ * copied: the blocks change owner.
+ * Table and length arrays of the two sides must not overlap; all calls are
+ * asynchronous on the stream and update the host fields batch as stated.
+ */
+
+/*
+ * filter (BatchTurboQuantKVCache.filter): out rows 0..n_keep-1 become rows
+ * keep[0..n_keep-1] (host int32, distinct, each in [0, batch->batch)) of
+ * `batch`, whole rows with their reserved entries; out->batch = n_keep.
+ * `out` describes the same pool. Every block id (>= 0) of the rows not kept
+ * is written to freed (device int32, room for (batch->batch - n_keep) *
+ * max_blocks ids) in row then entry order, and *n_freed (device int32) is set
+ * to their count. Nothing is copied.
+ * Errors: TQ_ERR_INVALID_ARG for bad pointers, sizes, repeated or
+ * out-of-range keep entries, or out->capacity < n_keep;
+ * TQ_ERR_CONFIG_MISMATCH if out->cache is not the same pool and layout.
+ */
+tq_status tq_batch_filter(const tq_batch *batch, const int32_t *keep, int n_keep, tq_batch *out, int32_t *freed,
+                          int32_t *n_freed, tq_stream_t stream);
+
+/*
+ * extend (BatchTurboQuantKVCache.extend): the sequences of `src` become rows
+ * dst->batch .. dst->batch + src->batch - 1 of `dst`, in order; each keeps
+ * its length, and its blocks are copied into blocks taken from the free list
+ * of dst's pool (entries past its last token's block become -1), unless both
+ * batches share a pool. dst->batch grows by src->batch.
+ * Errors: TQ_ERR_CAPACITY if dst->capacity is too small; TQ_ERR_INVALID_ARG
+ * for bad pointers or sizes; the mixed-configuration guard.
+ */
+tq_status tq_batch_extend(tq_batch *dst, const tq_batch *src, const int32_t *free_blocks, int n_free,
+                          int32_t *n_used, tq_stream_t stream);
+
+/*
+ * merge (BatchTurboQuantKVCache.merge): tq_batch_extend of dst by srcs[0],
+ * srcs[1], ... in order (each src usually one sequence in a cache of its
+ * own). The guard covers every source before anything is launched.
+ */
+tq_status tq_batch_merge(tq_batch *dst, const tq_batch *srcs, int n_srcs, const int32_t *free_blocks, int n_free,
+                         int32_t *n_used, tq_stream_t stream);
+
+/*
+ * extract (BatchTurboQuantKVCache.extract): sequence idx (host, in
+ * [0, src->batch)) of `src` becomes the only sequence of `dst` (row 0,
+ * dst->batch = 1), its blocks copied into blocks from dst's free list unless
+ * the two share a pool.
+ * Errors: as tq_batch_extend; TQ_ERR_INVALID_ARG for idx out of range.
+ */
+tq_status tq_batch_extract(const tq_batch *src, int idx, tq_batch *dst, const int32_t *free_blocks, int n_free,
+                           int32_t *n_used, tq_stream_t stream);
+
 /* ------------------------------------------------------------------ */
 /* Encode                                                               */
 /* ------------------------------------------------------------------ */
@@ -371,6 +457,58 @@ tq_status tq_decode_step(const tq_codec *key_codec, const tq_codec *value_codec,
                          const int32_t *seq_lens, const int32_t *block_table, int max_blocks,
                          int max_seq_len, float scale, float *out, void *workspace,
                          size_t workspace_bytes, tq_stream_t stream);
+
+/* ------------------------------------------------------------------ */
+/* Sequence-sharded decode                                              */
+/* ------------------------------------------------------------------ */
+
+/*
+ * Decode attention over one shard of each sequence's tokens, when a KV cache
+ * is split by sequence position across GPUs ("turboquant/validate_moe_phase2.py",
+ * TEST 3: with tensor parallelism each GPU holds a shard of the KV cache).
+ * Each shard yields, per query row, the unnormalised softmax state of its
+ * keys; tq_decode_merge combines the shards' states. Scores and values are
+ * those of tq_decode_attention.
+ *   seq_lens   device int32 [batch]: tokens of this shard (0 allowed).
+ *   causal_end device int32 [batch] or NULL: the end of the queries' causal
+ *              window in this shard's local token indices, i.e. the global
+ *              sequence length minus the global index of the shard's first
+ *              token; query l (of q_len) sees local keys t <= causal_end -
+ *              q_len + l. NULL means the shard's own length (the queries are
+ *              its newest tokens).
+ *   part_ml    device float [batch][num_q_heads][q_len][2] (8-byte aligned):
+ *              m (a reference maximum of the scores, natural-log units) and
+ *              l = sum_t exp(s_t - m) over the visible keys; a row with no
+ *              visible key gets m = -inf, l = 0.
+ *   part_acc   device float [batch][num_q_heads][q_len][head_dim] (16-byte
+ *              aligned): sum_t exp(s_t - m) v_t, with v_t in the rotated
+ *              domain for MSE values (n c[index], before the inverse
+ *              rotation) and dequantised for group values.
+ *   m is any reference value the kernels keep (the state is defined up to it:
+ *   m + ln l and acc / l are unique).
+ *   max_seq_len >= 1 bounds every seq_lens[b]; workspace as
+ *   tq_decode_workspace_bytes(cache, batch, num_q_heads, q_len, max_seq_len).
+ * Other arguments and errors as tq_decode_attention.
+ */
+tq_status tq_decode_partials(const tq_codec *key_codec, const tq_codec *value_codec,
+                             const tq_cache_desc *cache, int layer, const void *q, tq_dtype q_dtype,
+                             int batch, int num_q_heads, int q_len, const int32_t *seq_lens,
+                             const int32_t *causal_end, const int32_t *block_table, int max_blocks,
+                             int max_seq_len, float scale, float *part_ml, float *part_acc,
+                             void *workspace, size_t workspace_bytes, tq_stream_t stream);
+
+/*
+ * Log-sum-exp merge of num_parts shards' states of `rows` query rows:
+ * parts_ml [num_parts][rows][2] and parts_acc [num_parts][rows][head_dim]
+ * (device, in the layout tq_decode_partials writes, one part after another;
+ * rows = batch * num_q_heads * q_len). out [rows][head_dim] (device fp32) =
+ * (sum_p e^(m_p - M) acc_p) / (sum_p e^(m_p - M) l_p), M = max_p m_p, then
+ * `@ R_v` for MSE values (value_codec's rotation; "lightning-mlx/plan.md",
+ * the inverse rotation `rotated @ Q`); rows no part sees are 0. The parts
+ * may come from different GPUs (gathered by the caller).
+ */
+tq_status tq_decode_merge(const tq_codec *value_codec, int num_parts, const float *parts_ml,
+                          const float *parts_acc, int64_t rows, float *out, tq_stream_t stream);
 
 /* ------------------------------------------------------------------ */
 /* Prefill attention                                                    */

@@ -87,6 +87,9 @@ def _declare(L):
         "tqo_attention_f64": (None, [_I, _I64, _I, _I, _P, _P, _P, _D, _P]),
         "tqo_decode_rotated": (None, [_I, _I64, _I, _I, _P, _I, _I, _P, _P, _P, _P, _P, _P, _P,
                                       _I, _I, _I, _P, _P, _P, _P, _P, _P, _D, _P]),
+        "tqo_decode_partial": (None, [_I, _I64, _I64, _I, _I, _P, _I, _I, _P, _P, _P, _P, _P, _P, _P,
+                                      _I, _I, _I, _P, _P, _P, _P, _P, _D, _P, _P, _P]),
+        "tqo_merge_partials": (None, [_I, _I, _I64, _P, _P, _P, _I, _P, _P]),
         "tqo_subblock_layout": (_I64, [_I, _I, _I, _I, _I, _I, _I, _P]),
         "tqo_pool_write": (None, [_P, _I, _I, _I, _P, _I, _I, _I, _I64, _I64, _I, _I, _I, _I, _I,
                                   _P, _P, _P, _P, _P, _P, _P, _P]),
@@ -264,6 +267,35 @@ def decode_rotated(q: np.ndarray, kc: Codec, krec: dict, vc: Codec, vrec: dict,
         _p(krec["norm"]), _p(krec.get("rnorm")), _p(kc.R), _p(kc.S), _p(kc.c),
         vc.mode, vc.bits, vc.group, _p(vrec["idx"]), _p(vrec.get("norm")),
         _p(vrec.get("scale")), _p(vrec.get("min")), _p(vc.R), _p(vc.c), scale, _p(out))
+    return out
+
+
+def decode_partial(q: np.ndarray, kc: Codec, krec: dict, vc: Codec, vrec: dict, scale: float, Lq: int,
+                   causal_end: int = None):
+    """Unnormalised softmax state of a shard of keys. q: [G, Lq, D]; returns
+    (m [G*Lq], l [G*Lq], acc [G*Lq, D]) in fp64; causal_end defaults to the
+    shard's own length (the queries are its newest tokens)."""
+    q = _c(q, np.float64)
+    G, _, D = q.shape
+    N = krec["idx"].shape[0]
+    E = N if causal_end is None else int(causal_end)
+    m = np.empty(G * Lq, np.float64)
+    l = np.empty(G * Lq, np.float64)
+    acc = np.empty((G * Lq, D), np.float64)
+    lib().tqo_decode_partial(
+        D, N, E, G, Lq, _p(q), kc.mode, kc.bits, _p(krec["idx"]), _p(krec.get("sgn")),
+        _p(krec["norm"]), _p(krec.get("rnorm")), _p(kc.R), _p(kc.S), _p(kc.c),
+        vc.mode, vc.bits, vc.group, _p(vrec["idx"]), _p(vrec.get("norm")),
+        _p(vrec.get("scale")), _p(vrec.get("min")), _p(vc.c), scale, _p(m), _p(l), _p(acc))
+    return m, l, acc
+
+
+def merge_partials(vc: Codec, m: np.ndarray, l: np.ndarray, acc: np.ndarray) -> np.ndarray:
+    """Log-sum-exp merge of P parts: m, l [P, rows], acc [P, rows, D] -> [rows, D]."""
+    m, l, acc = _c(m, np.float64), _c(l, np.float64), _c(acc, np.float64)
+    P, rows, D = acc.shape
+    out = np.empty((rows, D), np.float64)
+    lib().tqo_merge_partials(D, P, rows, _p(m), _p(l), _p(acc), vc.mode, _p(vc.R), _p(out))
     return out
 
 

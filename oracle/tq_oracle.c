@@ -635,6 +635,123 @@ void tqo_decode_rotated(int D, int64_t N, int G, int Lq, const double *q,
 }
 
 /* ------------------------------------------------------------------ */
+/* Sequence-sharded decode. A shard holds tokens [offset, offset + N) of  */
+/* each sequence; its rows keep the unnormalised softmax state over them: */
+/*   m = max_t s_t, l = sum_t exp(s_t - m), acc = sum_t exp(s_t - m) v_t  */
+/* with v_t the value in the rotated domain (MSE) or the dequantised      */
+/* value (group). A key at local index t is visible to query l of Lq when */
+/* t <= E - Lq + l, where E = (global sequence length) - offset is the    */
+/* shard's causal end. Parts merge by the log-sum-exp rule:               */
+/*   M = max_p m_p, L = sum_p exp(m_p - M) l_p,                           */
+/*   acc = sum_p exp(m_p - M) acc_p, out = (acc / L) (@ R_v for MSE).     */
+/* A part with no visible key has m = -inf, l = 0, acc = 0 and adds       */
+/* nothing. The plain decode is the merge of one part with E = N.         */
+/* ------------------------------------------------------------------ */
+void tqo_decode_partial(int D, int64_t N, int64_t E, int G, int Lq, const double *q,
+                        int kmode, int kbits, const uint32_t *kidx, const uint32_t *ksgn,
+                        const float *knorm, const float *krn, const float *kR,
+                        const float *kS, const float *kc,
+                        int vmode, int vbits, int vgroup, const uint32_t *vidx,
+                        const float *vnorm, const uint16_t *vscale, const uint16_t *vmin,
+                        const float *vc, double scale, double *m_out, double *l_out,
+                        double *acc_out) {
+    const int kb = tqo_index_bits(kbits, kmode);
+    const int Wk = tqo_packed_words(D, kb);
+    const int Ws = D / 32;
+    const int Wv = tqo_packed_words(D, vbits);
+    const double kappa = sqrt(M_PI / 2.0) / (double)D;
+    const int ng = (vmode == TQO_GROUP) ? D / vgroup : 0;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int r = 0; r < G * Lq; ++r) {
+        const int l = r % Lq;
+        int64_t nv = E - Lq + l + 1; /* visible local keys t < nv */
+        if (nv > N) nv = N;
+        const double *qr = q + (size_t)r * D;
+        double *acc = acc_out + (size_t)r * D;
+        double q1[512], q2[512];
+        uint8_t codes[512];
+        for (int i = 0; i < D; ++i) {
+            double s = 0.0;
+            for (int k = 0; k < D; ++k) s += (double)kR[(size_t)i * D + k] * qr[k];
+            q1[i] = s;
+        }
+        if (kmode == TQO_PROD) {
+            for (int j = 0; j < D; ++j) {
+                double s = 0.0;
+                for (int i = 0; i < D; ++i) s += (double)kS[(size_t)j * D + i] * q1[i];
+                q2[j] = s;
+            }
+        }
+        for (int d = 0; d < D; ++d) acc[d] = 0.0;
+        double mx = -INFINITY, den = 0.0;
+        for (int64_t t = 0; t < nv; ++t) {
+            tqo_unpack(kidx + t * Wk, D, kb, codes);
+            double a = 0.0;
+            for (int i = 0; i < D; ++i) a += q1[i] * (double)kc[codes[i]];
+            if (kmode == TQO_PROD) {
+                double z = 0.0;
+                const uint32_t *sw = ksgn + t * Ws;
+                for (int j = 0; j < D; ++j)
+                    z += ((sw[j >> 5] >> (j & 31)) & 1u) ? q2[j] : -q2[j];
+                a += kappa * (double)krn[t] * z;
+            }
+            double s = scale * (double)knorm[t] * a;
+            double mnew = s > mx ? s : mx;
+            double corr = exp(mx - mnew);
+            double p = exp(s - mnew);
+            den = den * corr + p;
+            for (int d = 0; d < D; ++d) acc[d] *= corr;
+            mx = mnew;
+            tqo_unpack(vidx + t * Wv, D, vbits, codes);
+            if (vmode == TQO_MSE) {
+                double w = p * (double)vnorm[t];
+                for (int d = 0; d < D; ++d) acc[d] += w * (double)vc[codes[d]];
+            } else {
+                for (int d = 0; d < D; ++d) {
+                    double sc = tqo_f16_to_f32(vscale[t * ng + d / vgroup]);
+                    double m0 = tqo_f16_to_f32(vmin[t * ng + d / vgroup]);
+                    acc[d] += p * ((double)codes[d] * sc + m0);
+                }
+            }
+        }
+        m_out[r] = mx;
+        l_out[r] = den;
+    }
+}
+
+void tqo_merge_partials(int D, int P, int64_t rows, const double *m, const double *l,
+                        const double *acc, int vmode, const float *vR, double *out) {
+    for (int64_t r = 0; r < rows; ++r) {
+        double M = -INFINITY;
+        for (int p = 0; p < P; ++p)
+            if (m[(size_t)p * rows + r] > M) M = m[(size_t)p * rows + r];
+        double L = 0.0, a[512];
+        for (int d = 0; d < D; ++d) a[d] = 0.0;
+        if (M != -INFINITY) {
+            for (int p = 0; p < P; ++p) {
+                const double mp = m[(size_t)p * rows + r];
+                if (mp == -INFINITY) continue;
+                const double w = exp(mp - M);
+                L += w * l[(size_t)p * rows + r];
+                const double *ap = acc + ((size_t)p * rows + r) * D;
+                for (int d = 0; d < D; ++d) a[d] += w * ap[d];
+            }
+        }
+        double *o = out + (size_t)r * D;
+        for (int d = 0; d < D; ++d) {
+            if (!(L > 0.0)) { o[d] = 0.0; continue; }
+            if (vmode == TQO_MSE) {
+                double s = 0.0;
+                for (int i = 0; i < D; ++i) s += a[i] * (double)vR[(size_t)i * D + d];
+                o[d] = s / L;
+            } else {
+                o[d] = a[d] / L;
+            }
+        }
+    }
+}
+
+/* ------------------------------------------------------------------ */
 /* Paged pool layout. A layer pool is an array of blocks; block p holds  */
 /* BT tokens of every kv head; the (p, h) sub-block starts at byte       */
 /* (p*Hkv + h) * BT * record_bytes and stores its streams one after      */

@@ -86,6 +86,22 @@ void tqo_decode_rotated(int D, int64_t N, int G, int Lq, const double *q,
                         const float *vnorm, const uint16_t *vscale, const uint16_t *vmin,
                         const float *vR, const float *vc, double scale, double *out);
 
+/* Sequence-sharded decode: the unnormalised softmax state (m, l, acc) of
+ * each row over a shard of N local keys whose causal end is E (a local key t
+ * is visible to query l when t <= E - Lq + l); acc in the rotated domain
+ * (MSE values) or the value domain (group). Then the log-sum-exp merge of P
+ * parts, each [rows] (m, l) and [rows][D] acc, into out [rows][D]. */
+void tqo_decode_partial(int D, int64_t N, int64_t E, int G, int Lq, const double *q,
+                        int kmode, int kbits, const uint32_t *kidx, const uint32_t *ksgn,
+                        const float *knorm, const float *krn, const float *kR,
+                        const float *kS, const float *kc,
+                        int vmode, int vbits, int vgroup, const uint32_t *vidx,
+                        const float *vnorm, const uint16_t *vscale, const uint16_t *vmin,
+                        const float *vc, double scale, double *m_out, double *l_out,
+                        double *acc_out);
+void tqo_merge_partials(int D, int P, int64_t rows, const double *m, const double *l,
+                        const double *acc, int vmode, const float *vR, double *out);
+
 /* Paged-pool layout: byte offset of each stream inside one (block, head)
  * sub-block of BT tokens, in the stream order of the layout; returns the
  * sub-block size. off[] receives up to 4 key streams then up to 3 value

@@ -128,3 +128,79 @@ def test_subblock_layout_and_pool_write(oracle_lib):
     # head 0 and unused blocks untouched
     assert not pool[(7 * Hkv) * sub:(7 * Hkv + 1) * sub].any()
     assert not pool[0:(2 * Hkv) * sub].any()
+
+
+# ------------------------------------------------------------------ sequence-sharded decode
+
+def _slice_rec(rec, a, b):
+    return {k: v[a:b] for k, v in rec.items()}
+
+
+@pytest.mark.parametrize("case", CASES[:5])
+def test_partial_state_equals_dequantised_brute_force(oracle_lib, case):
+    # (m, l, acc) of a shard computed independently: scores from the
+    # dequantised keys, values in the rotated domain (MSE) or as dequantised
+    # (group)
+    D, ks, vs, G, Lq, N = case
+    kc, vc, K, V, q = _setup(*case)
+    kr, vr = kc.encode(K), vc.encode(V)
+    scale = 1 / math.sqrt(D)
+    a, b = N // 3, N - 5
+    E = N - a                                  # the shard's causal end: the global end, locally
+    m, l, acc = O.decode_partial(q, kc, _slice_rec(kr, a, b), vc, _slice_rec(vr, a, b), scale, Lq, E)
+    Kh, Vh = kc.dequant(kr)[a:b], vc.dequant(vr)[a:b]
+    # V_hat = (n c_hat) @ R_v: the rotated-domain value is V_hat R_v^-1 (the
+    # fp32 table is orthogonal only to ~1e-7, so its transpose is not exact)
+    Vr = Vh @ np.linalg.inv(vc.R.astype(np.float64)) if vc.mode == O.MSE else Vh
+    for g in range(G):
+        for lq in range(Lq):
+            r = g * Lq + lq
+            nv = min(b - a, E - Lq + lq + 1)
+            s = scale * (Kh[:nv] @ q[g, lq])
+            mm = s.max()
+            p = np.exp(s - mm)
+            assert abs(m[r] - mm) <= 1e-12 * max(1.0, abs(mm))
+            assert abs(l[r] - p.sum()) <= 1e-11 * p.sum()
+            assert np.abs(acc[r] - p @ Vr[:nv]).max() <= 1e-10 * max(1.0, np.abs(acc[r]).max())
+
+
+@pytest.mark.parametrize("case", CASES)
+def test_merged_shards_equal_the_unsharded_decode(oracle_lib, case):
+    D, ks, vs, G, Lq, N = case
+    kc, vc, K, V, q = _setup(*case)
+    kr, vr = kc.encode(K), vc.encode(V)
+    scale = 1 / math.sqrt(D)
+    ref = O.decode_rotated(q, kc, kr, vc, vr, scale, Lq).reshape(G * Lq, D)
+    # one part with its own end is the plain decode
+    m, l, acc = O.decode_partial(q, kc, kr, vc, vr, scale, Lq)
+    one = O.merge_partials(vc, m[None], l[None], acc[None])
+    assert np.abs(one - ref).max() <= 1e-12 * max(1.0, np.abs(ref).max())
+    # three shards, the last one shorter than the query chunk when Lq is large
+    cuts = [0, N // 2, N - 1, N] if Lq > 2 else [0, 7, N // 2, N]
+    parts = [O.decode_partial(q, kc, _slice_rec(kr, a, b), vc, _slice_rec(vr, a, b), scale, Lq, N - a)
+             for a, b in zip(cuts[:-1], cuts[1:])]
+    m = np.stack([p[0] for p in parts])
+    l = np.stack([p[1] for p in parts])
+    acc = np.stack([p[2] for p in parts])
+    got = O.merge_partials(vc, m, l, acc)
+    assert np.abs(got - ref).max() <= 1e-11 * max(1.0, np.abs(ref).max())
+    # the order of the parts does not matter
+    rev = O.merge_partials(vc, m[::-1], l[::-1], acc[::-1])
+    assert np.abs(rev - ref).max() <= 1e-11 * max(1.0, np.abs(ref).max())
+
+
+def test_shard_with_no_visible_key_is_neutral(oracle_lib):
+    D, ks, vs, G, Lq, N = CASES[5]           # a whole-sequence chunk: query 0 sees token 0 only
+    kc, vc, K, V, q = _setup(*CASES[5])
+    kr, vr = kc.encode(K), vc.encode(V)
+    m, l, acc = O.decode_partial(q, kc, _slice_rec(kr, 1, N), vc, _slice_rec(vr, 1, N), 0.1, Lq, N - 1)
+    # rows of query 0 see no key of the shard [1, N)
+    rows0 = [g * Lq for g in range(G)]
+    assert np.all(m[rows0] == -np.inf) and np.all(l[rows0] == 0) and not acc[rows0].any()
+    m0, l0, a0 = O.decode_partial(q, kc, _slice_rec(kr, 0, 1), vc, _slice_rec(vr, 0, 1), 0.1, Lq, N)
+    both = O.merge_partials(vc, np.stack([m, m0]), np.stack([l, l0]), np.stack([acc, a0]))
+    ref = O.decode_rotated(q, kc, kr, vc, vr, 0.1, Lq).reshape(G * Lq, D)
+    assert np.abs(both - ref).max() <= 1e-11 * max(1.0, np.abs(ref).max())
+    # an all-empty merge gives zeros rather than NaN
+    empty = O.merge_partials(vc, np.full((2, G * Lq), -np.inf), np.zeros((2, G * Lq)), np.zeros((2, G * Lq, D)))
+    assert not empty.any()

@@ -57,7 +57,7 @@ MUTANTS = [
     # prod: sign bit set for negative projections
     ("qjl_sign_flipped", "if (z >= 0.0f) sw[j >> 5]", "if (z < 0.0f) sw[j >> 5]", 1),
     # prod: QJL constant sqrt(2/pi)/D instead of sqrt(pi/2)/D, everywhere
-    ("qjl_constant", "sqrt(M_PI / 2.0) / (double)D", "sqrt(2.0 / M_PI) / (double)D", 2),
+    ("qjl_constant", "sqrt(M_PI / 2.0) / (double)D", "sqrt(2.0 / M_PI) / (double)D", 3),
     # group: the fp16 minimum taken from the group maximum
     ("group_min_from_max", "mh = tqo_f32_to_f16(lo);", "mh = tqo_f32_to_f16(hi);", 1),
     # dequantisers: the vector norm dropped
@@ -65,14 +65,14 @@ MUTANTS = [
     # attention: the score scale applied twice
     ("score_scale_squared", "s[t] = a * scale;", "s[t] = a * scale * scale;", 1),
     # rotated decode: the key norm dropped from the score
-    ("key_norm_dropped_in_decode", "double s = scale * (double)knorm[t] * a;", "double s = scale * a;", 1),
+    ("key_norm_dropped_in_decode", "double s = scale * (double)knorm[t] * a;", "double s = scale * a;", 2),
     # attention: the causal window one token short, everywhere
     ("causal_off_by_one", "const int64_t nv = N - Lq + l + 1;", "const int64_t nv = N - Lq + l;", 2),
     # rotated decode: q'' = S^T q' instead of S q'
     ("qjl_matrix_transposed_in_decode", "s += (double)kS[(size_t)j * D + i] * q1[i];",
-     "s += (double)kS[(size_t)i * D + j] * q1[i];", 1),
+     "s += (double)kS[(size_t)i * D + j] * q1[i];", 2),
     # rotated decode: the residual norm dropped from the QJL term
-    ("residual_norm_dropped_in_decode", "a += kappa * (double)krn[t] * z;", "a += kappa * z;", 1),
+    ("residual_norm_dropped_in_decode", "a += kappa * (double)krn[t] * z;", "a += kappa * z;", 2),
     # rotated decode: the output rotated by R_v instead of back by R_v^T
     ("value_rotation_not_inverted", "s += acc[i] * (double)vR[(size_t)i * D + d];",
      "s += acc[i] * (double)vR[(size_t)d * D + i];", 1),
@@ -86,7 +86,14 @@ MUTANTS = [
      "out[v * D + d] = (double)codes[d] * s;", 1),
     # rotated decode: the group minimum dropped from the value sum
     ("group_decode_min_dropped", "acc[d] += p * ((double)codes[d] * sc + m0);",
-     "acc[d] += p * ((double)codes[d] * sc);", 1),
+     "acc[d] += p * ((double)codes[d] * sc);", 2),
+    # sharded decode: a shard's causal window one token short
+    ("shard_causal_end_off_by_one", "int64_t nv = E - Lq + l + 1; /* visible local keys t < nv */",
+     "int64_t nv = E - Lq + l; /* visible local keys t < nv */", 1),
+    # shard merge: parts weighted by e^(M - m_p) instead of e^(m_p - M)
+    ("merge_weight_inverted", "const double w = exp(mp - M);", "const double w = exp(M - mp);", 1),
+    # shard merge: the parts' sums added without their weights
+    ("merge_sum_unweighted", "L += w * l[(size_t)p * rows + r];", "L += l[(size_t)p * rows + r];", 1),
     # pool writer: the block table ignored
     ("block_table_ignored",
      "int64_t p = table ? table[(int64_t)seq * max_blocks + lb] : (int64_t)seq * max_blocks + lb;",

@@ -15,7 +15,7 @@ import numpy as np
 from . import _lib
 from ._lib import (TQ_BF16, TQ_DEVERR_BLOCK, TQ_DEVERR_CAPACITY, TQ_DEVERR_SEQLEN, TQ_ENCODE_AUTO,
                    TQ_ENCODE_EXACT, TQ_F16, TQ_F32, TQ_MODE_GROUP, TQ_MODE_MSE, TQ_MODE_PROD, TQ_OK, TQError, check,
-                   lib, library_path, status_string, tq_cache_desc, tq_codec_info_t)
+                   lib, library_path, status_string, tq_batch, tq_cache_desc, tq_codec_info_t)
 
 __all__ = [
     "tq_codec_create", "tq_codec_create_group", "tq_codec_destroy", "tq_codec_info",
@@ -24,6 +24,8 @@ __all__ = [
     "tq_quantize", "tq_decode_workspace_bytes", "tq_decode_attention", "tq_decode_attention_noalloc",
     "tq_decode_step", "tq_decode_plan",
     "tq_prefill_workspace_bytes", "tq_prefill_attention", "tq_cache_copy_blocks",
+    "tq_decode_partials", "tq_decode_merge",
+    "tq_batch_filter", "tq_batch_extend", "tq_batch_merge", "tq_batch_extract", "Batch",
     "tq_device_error",
     "tq_launch_count", "tq_abi_version", "Codec", "CompressedKVCache", "TQError",
     "TQ_MODE_MSE", "TQ_MODE_PROD", "TQ_MODE_GROUP", "TQ_F32", "TQ_BF16", "TQ_F16",
@@ -242,6 +244,93 @@ def tq_decode_attention_noalloc(key_codec: int, value_codec: int, desc: tq_cache
                                             _stream(stream)), "tq_decode_attention_noalloc")
 
 
+def tq_decode_partials(key_codec: int, value_codec: int, desc: tq_cache_desc, layer: int, q, seq_lens,
+                       causal_end, block_table, max_blocks: int, max_seq_len: int, part_ml, part_acc, workspace,
+                       scale: float = 0.0, stream=None) -> None:
+    """Unnormalised softmax state of this shard of every sequence (see include/tq.h)."""
+    batch, hq, lq, _ = q.shape
+    ws_bytes = workspace.numel() * workspace.element_size()
+    check(lib().tq_decode_partials(key_codec, value_codec, ctypes.byref(desc), layer, _ptr(q), _dtype_code(q),
+                                   batch, hq, lq, _ptr(seq_lens), _ptr(causal_end), _ptr(block_table), max_blocks,
+                                   max_seq_len, scale, _ptr(part_ml), _ptr(part_acc), _ptr(workspace), ws_bytes,
+                                   _stream(stream)), "tq_decode_partials")
+
+
+def tq_decode_merge(value_codec: int, parts_ml, parts_acc, out, stream=None) -> None:
+    """Log-sum-exp merge of shards' states: parts_ml [P, ..., 2], parts_acc [P, ..., D] -> out [..., D]."""
+    P = parts_ml.shape[0]
+    rows = parts_ml[0].numel() // 2
+    check(lib().tq_decode_merge(value_codec, P, _ptr(parts_ml), _ptr(parts_acc), rows, _ptr(out),
+                                _stream(stream)), "tq_decode_merge")
+
+
+class Batch:
+    """A batch of sequences in a paged cache: device block table [capacity][max_blocks]
+    (-1 = no block) and sequence lengths [capacity], rows 0..batch-1 in use."""
+
+    def __init__(self, cache: "CompressedKVCache", capacity: int, max_blocks: int, table=None, lens=None,
+                 batch: int = 0):
+        torch = _torch()
+        dev = cache.pool.device
+        self.cache = cache
+        self.table = table if table is not None else torch.full((capacity, max_blocks), -1, dtype=torch.int32,
+                                                                 device=dev)
+        self.lens = lens if lens is not None else torch.zeros(capacity, dtype=torch.int32, device=dev)
+        self.batch = batch
+        assert self.table.shape == (capacity, max_blocks) and self.lens.shape == (capacity,)
+
+    @property
+    def capacity(self) -> int:
+        return self.table.shape[0]
+
+    @property
+    def max_blocks(self) -> int:
+        return self.table.shape[1]
+
+    def view(self) -> tq_batch:
+        return tq_batch(ctypes.pointer(self.cache.desc), _ptr(self.table), _ptr(self.lens), self.batch,
+                        self.capacity, self.max_blocks)
+
+
+def tq_batch_filter(batch: Batch, keep, out: Batch, freed, n_freed, stream=None) -> None:
+    """Rows `keep` (host list) of `batch` become rows 0.. of `out` (same pool); the block ids of the
+    other rows go to `freed` (device int32) and their count to n_freed (device int32 [1])."""
+    keep_arr = (ctypes.c_int32 * max(1, len(keep)))(*[int(i) for i in keep])
+    src, dst = batch.view(), out.view()
+    check(lib().tq_batch_filter(ctypes.byref(src), keep_arr, len(keep), ctypes.byref(dst), _ptr(freed),
+                                _ptr(n_freed), _stream(stream)), "tq_batch_filter")
+    out.batch = dst.batch
+
+
+def tq_batch_extend(dst: Batch, src: Batch, free_blocks=None, n_used=None, stream=None) -> None:
+    """Append the sequences of `src` to `dst`, copying their blocks into dst's free blocks
+    (free_blocks device int32, consumed from n_used[0]) unless both share a pool."""
+    d, s_ = dst.view(), src.view()
+    n_free = 0 if free_blocks is None else free_blocks.numel()
+    check(lib().tq_batch_extend(ctypes.byref(d), ctypes.byref(s_), _ptr(free_blocks), n_free, _ptr(n_used),
+                                _stream(stream)), "tq_batch_extend")
+    dst.batch = d.batch
+
+
+def tq_batch_merge(dst: Batch, srcs, free_blocks=None, n_used=None, stream=None) -> None:
+    """tq_batch_extend of `dst` by each of `srcs` in order (one guard over all of them first)."""
+    d = dst.view()
+    arr = (tq_batch * max(1, len(srcs)))(*[b.view() for b in srcs])
+    n_free = 0 if free_blocks is None else free_blocks.numel()
+    check(lib().tq_batch_merge(ctypes.byref(d), arr, len(srcs), _ptr(free_blocks), n_free, _ptr(n_used),
+                               _stream(stream)), "tq_batch_merge")
+    dst.batch = d.batch
+
+
+def tq_batch_extract(src: Batch, idx: int, dst: Batch, free_blocks=None, n_used=None, stream=None) -> None:
+    """Sequence idx of `src` becomes the only sequence of `dst`."""
+    s_, d = src.view(), dst.view()
+    n_free = 0 if free_blocks is None else free_blocks.numel()
+    check(lib().tq_batch_extract(ctypes.byref(s_), idx, ctypes.byref(d), _ptr(free_blocks), n_free,
+                                 _ptr(n_used), _stream(stream)), "tq_batch_extract")
+    dst.batch = d.batch
+
+
 def tq_device_error() -> int:
     flags = ctypes.c_uint32()
     st = lib().tq_device_error(ctypes.byref(flags))
@@ -334,6 +423,12 @@ class CompressedKVCache:
                scale=0.0, stream=None):
         tq_decode_attention(self.key.handle, self.value.handle, self.desc, layer, q, seq_lens,
                             block_table, max_blocks, max_seq_len, out, workspace, scale, stream)
+
+    def decode_partials(self, layer, q, seq_lens, causal_end, block_table, max_blocks, max_seq_len, part_ml,
+                        part_acc, workspace, scale=0.0, stream=None):
+        """This cache holds one shard of each sequence: its unnormalised softmax state."""
+        tq_decode_partials(self.key.handle, self.value.handle, self.desc, layer, q, seq_lens, causal_end,
+                           block_table, max_blocks, max_seq_len, part_ml, part_acc, workspace, scale, stream)
 
     def decode_step(self, layer, k_new, v_new, q, seq_lens, block_table, max_blocks, max_seq_len, out,
                     workspace, scale=0.0, stream=None):

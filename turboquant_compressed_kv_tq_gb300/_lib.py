@@ -71,6 +71,12 @@ class tq_cache_desc(ctypes.Structure):
                 ("stream_offset", ctypes.c_int64 * 7), ("encode_policy", ctypes.c_int)]
 
 
+class tq_batch(ctypes.Structure):
+    _fields_ = [("cache", ctypes.POINTER(tq_cache_desc)), ("block_table", ctypes.c_void_p),
+                ("seq_lens", ctypes.c_void_p), ("batch", ctypes.c_int), ("capacity", ctypes.c_int),
+                ("max_blocks", ctypes.c_int)]
+
+
 _P = ctypes.c_void_p
 _I = ctypes.c_int
 _I64 = ctypes.c_int64
@@ -110,6 +116,13 @@ SIGNATURES = {
     "tq_prefill_attention": (_ST, [_P, _P, ctypes.POINTER(tq_cache_desc), _I, _P, _I, _I, _I, _I, _P,
                                    _P, _I, _F, _P, _P, _SZ, _P]),
     "tq_cache_copy_blocks": (_ST, [ctypes.POINTER(tq_cache_desc), ctypes.POINTER(tq_cache_desc), _P, _P, _I, _P]),
+    "tq_decode_partials": (_ST, [_P, _P, ctypes.POINTER(tq_cache_desc), _I, _P, _I, _I, _I, _I, _P, _P, _P, _I,
+                                 _I, _F, _P, _P, _P, _SZ, _P]),
+    "tq_decode_merge": (_ST, [_P, _I, _P, _P, _I64, _P, _P]),
+    "tq_batch_filter": (_ST, [ctypes.POINTER(tq_batch), _P, _I, ctypes.POINTER(tq_batch), _P, _P, _P]),
+    "tq_batch_extend": (_ST, [ctypes.POINTER(tq_batch), ctypes.POINTER(tq_batch), _P, _I, _P, _P]),
+    "tq_batch_merge": (_ST, [ctypes.POINTER(tq_batch), ctypes.POINTER(tq_batch), _I, _P, _I, _P, _P]),
+    "tq_batch_extract": (_ST, [ctypes.POINTER(tq_batch), _I, ctypes.POINTER(tq_batch), _P, _I, _P, _P]),
     "tq_device_error": (_ST, [ctypes.POINTER(ctypes.c_uint32)]),
 }
 

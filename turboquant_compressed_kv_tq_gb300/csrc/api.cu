@@ -137,6 +137,63 @@ PoolDev pool_view(const tq_cache_desc* d, int layer) {
     return p;
 }
 
+// The mixed-configuration guard of BatchTurboQuantKVCache.merge ("omlx/
+// turboquant_kv.py"): caches share blocks only under one layout and codec
+// configuration.
+bool same_config(const tq_cache_desc* a, const tq_cache_desc* b) {
+    return a->head_dim == b->head_dim && a->num_kv_heads == b->num_kv_heads && a->block_tokens == b->block_tokens &&
+           a->num_layers == b->num_layers && a->key_mode == b->key_mode && a->key_bits == b->key_bits &&
+           a->key_seed == b->key_seed && a->value_mode == b->value_mode && a->value_bits == b->value_bits &&
+           a->value_group == b->value_group && a->value_seed == b->value_seed &&
+           a->subblock_bytes == b->subblock_bytes;
+}
+
+bool same_pool(const tq_cache_desc* a, const tq_cache_desc* b) {
+    return a->pool == b->pool && a->layer_stride == b->layer_stride && a->num_blocks == b->num_blocks;
+}
+
+bool ranges_overlap(const void* a, size_t na, const void* b, size_t nb) {
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return x < y + nb && y < x + na;
+}
+
+// Host checks common to the batch operations: a usable view of a batch.
+tq_status check_batch(const tq_batch* t) {
+    if (!t || !t->cache || !t->block_table || !t->seq_lens) return TQ_ERR_INVALID_ARG;
+    const tq_cache_desc* c = t->cache;
+    if (!c->pool || c->num_blocks <= 0 || c->num_kv_heads <= 0 || c->num_layers <= 0 || c->num_layers > 65535 ||
+        c->block_tokens < 16 || (c->block_tokens & (c->block_tokens - 1)) != 0 || c->subblock_bytes <= 0 ||
+        c->subblock_bytes % 16 != 0)
+        return TQ_ERR_INVALID_ARG;
+    if (t->batch < 0 || t->capacity < t->batch || t->max_blocks <= 0) return TQ_ERR_INVALID_ARG;
+    if (static_cast<int64_t>(t->max_blocks) * c->block_tokens > 2147483647) return TQ_ERR_INVALID_ARG;
+    return TQ_OK;
+}
+
+bool batch_arrays_overlap(const tq_batch* a, const tq_batch* b) {
+    const size_t ta = static_cast<size_t>(a->capacity) * a->max_blocks * 4, tb = static_cast<size_t>(b->capacity) * b->max_blocks * 4;
+    const size_t la = static_cast<size_t>(a->capacity) * 4, lb = static_cast<size_t>(b->capacity) * 4;
+    return ranges_overlap(a->block_table, ta, b->block_table, tb) || ranges_overlap(a->seq_lens, la, b->seq_lens, lb) ||
+           ranges_overlap(a->block_table, ta, b->seq_lens, lb) || ranges_overlap(a->seq_lens, la, b->block_table, tb);
+}
+
+// Rows [0, n) of src (from row src_row0) appended to dst at dst_row0, in
+// chunks; blocks copied from the free list unless the two share a pool.
+tq_status append_rows(const tq_batch* src, int src_row0, int n, tq_batch* dst, int dst_row0,
+                      const int32_t* free_blocks, int n_free, int32_t* n_used, cudaStream_t s) {
+    const bool copy = !same_pool(src->cache, dst->cache);
+    if (copy && (!n_used || (n_free > 0 && !free_blocks) || n_free < 0)) return TQ_ERR_INVALID_ARG;
+    unsigned* err = nullptr;
+    if (device_state(&err, nullptr) != TQ_OK) return TQ_ERR_CUDA;
+    for (int c = 0; c < n; c += kBatchRowChunk) {
+        const int m = n - c < kBatchRowChunk ? n - c : kBatchRowChunk;
+        if (launch_batch_rows(src, dst, m, nullptr, src_row0 + c, dst_row0 + c, copy, free_blocks, n_free, n_used,
+                              0, nullptr, nullptr, nullptr, false, err, s) != cudaSuccess)
+            return TQ_ERR_CUDA;
+    }
+    return TQ_OK;
+}
+
 }  // namespace
 }  // namespace tq
 
@@ -380,16 +437,93 @@ tq_status tq_cache_desc_init(tq_cache_desc* d, const tq_codec* kc, const tq_code
     return TQ_OK;
 }
 
+tq_status tq_batch_filter(const tq_batch* batch, const int32_t* keep, int n_keep, tq_batch* out, int32_t* freed,
+                          int32_t* n_freed, tq_stream_t stream) {
+    tq_status st = check_batch(batch);
+    if (st == TQ_OK) st = check_batch(out);
+    if (st != TQ_OK) return st;
+    if (!same_config(batch->cache, out->cache) || !same_pool(batch->cache, out->cache)) return TQ_ERR_CONFIG_MISMATCH;
+    if (n_keep < 0 || n_keep > batch->batch || (n_keep > 0 && !keep) || out->capacity < n_keep || !n_freed ||
+        out->max_blocks != batch->max_blocks || batch_arrays_overlap(batch, out))
+        return TQ_ERR_INVALID_ARG;
+    const int n_drop = batch->batch - n_keep;
+    if (n_drop > 0 && !freed) return TQ_ERR_INVALID_ARG;
+    std::vector<char> kept(static_cast<size_t>(batch->batch), 0);
+    for (int i = 0; i < n_keep; ++i) {
+        if (keep[i] < 0 || keep[i] >= batch->batch || kept[keep[i]]) return TQ_ERR_INVALID_ARG;
+        kept[keep[i]] = 1;
+    }
+    std::vector<int> drop;
+    for (int r = 0; r < batch->batch; ++r)
+        if (!kept[r]) drop.push_back(r);
+    unsigned* err = nullptr;
+    if (device_state(&err, nullptr) != TQ_OK) return TQ_ERR_CUDA;
+    const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const int rounds = std::max(1, (std::max(n_keep, n_drop) + kBatchRowChunk - 1) / kBatchRowChunk);
+    for (int c = 0; c < rounds; ++c) {
+        const int r0 = c * kBatchRowChunk;
+        const int m = std::max(0, std::min(kBatchRowChunk, n_keep - r0));
+        const int md = std::max(0, std::min(kBatchRowChunk, n_drop - r0));
+        if (launch_batch_rows(batch, out, m, m ? keep + r0 : nullptr, 0, r0, false, nullptr, 0, nullptr, md,
+                              md ? drop.data() + r0 : nullptr, freed, n_freed, c == 0, err, s) != cudaSuccess)
+            return TQ_ERR_CUDA;
+    }
+    out->batch = n_keep;
+    return TQ_OK;
+}
+
+tq_status tq_batch_extend(tq_batch* dst, const tq_batch* src, const int32_t* free_blocks, int n_free,
+                          int32_t* n_used, tq_stream_t stream) {
+    tq_status st = check_batch(dst);
+    if (st == TQ_OK) st = check_batch(src);
+    if (st != TQ_OK) return st;
+    if (!same_config(src->cache, dst->cache)) return TQ_ERR_CONFIG_MISMATCH;
+    if (batch_arrays_overlap(src, dst)) return TQ_ERR_INVALID_ARG;
+    if (static_cast<int64_t>(dst->batch) + src->batch > dst->capacity) return TQ_ERR_CAPACITY;
+    st = append_rows(src, 0, src->batch, dst, dst->batch, free_blocks, n_free, n_used,
+                     reinterpret_cast<cudaStream_t>(stream));
+    if (st == TQ_OK) dst->batch += src->batch;
+    return st;
+}
+
+tq_status tq_batch_merge(tq_batch* dst, const tq_batch* srcs, int n_srcs, const int32_t* free_blocks, int n_free,
+                         int32_t* n_used, tq_stream_t stream) {
+    tq_status st = check_batch(dst);
+    if (st != TQ_OK) return st;
+    if (n_srcs < 0 || (n_srcs > 0 && !srcs)) return TQ_ERR_INVALID_ARG;
+    int64_t rows = dst->batch;
+    for (int i = 0; i < n_srcs; ++i) {
+        st = check_batch(&srcs[i]);
+        if (st != TQ_OK) return st;
+        if (!same_config(srcs[i].cache, dst->cache)) return TQ_ERR_CONFIG_MISMATCH;
+        if (batch_arrays_overlap(&srcs[i], dst)) return TQ_ERR_INVALID_ARG;
+        rows += srcs[i].batch;
+    }
+    if (rows > dst->capacity) return TQ_ERR_CAPACITY;
+    for (int i = 0; i < n_srcs; ++i) {
+        st = tq_batch_extend(dst, &srcs[i], free_blocks, n_free, n_used, stream);
+        if (st != TQ_OK) return st;
+    }
+    return TQ_OK;
+}
+
+tq_status tq_batch_extract(const tq_batch* src, int idx, tq_batch* dst, const int32_t* free_blocks, int n_free,
+                           int32_t* n_used, tq_stream_t stream) {
+    tq_status st = check_batch(src);
+    if (st == TQ_OK) st = check_batch(dst);
+    if (st != TQ_OK) return st;
+    if (!same_config(src->cache, dst->cache)) return TQ_ERR_CONFIG_MISMATCH;
+    if (idx < 0 || idx >= src->batch || batch_arrays_overlap(src, dst)) return TQ_ERR_INVALID_ARG;
+    if (dst->capacity < 1) return TQ_ERR_CAPACITY;
+    st = append_rows(src, idx, 1, dst, 0, free_blocks, n_free, n_used, reinterpret_cast<cudaStream_t>(stream));
+    if (st == TQ_OK) dst->batch = 1;
+    return st;
+}
+
 tq_status tq_cache_copy_blocks(const tq_cache_desc* src, const tq_cache_desc* dst, const int32_t* src_blocks,
                                const int32_t* dst_blocks, int n, tq_stream_t stream) {
     if (!src || !dst || n < 0) return TQ_ERR_INVALID_ARG;
-    if (src->head_dim != dst->head_dim || src->num_kv_heads != dst->num_kv_heads ||
-        src->block_tokens != dst->block_tokens || src->num_layers != dst->num_layers ||
-        src->key_mode != dst->key_mode || src->key_bits != dst->key_bits || src->key_seed != dst->key_seed ||
-        src->value_mode != dst->value_mode || src->value_bits != dst->value_bits ||
-        src->value_group != dst->value_group || src->value_seed != dst->value_seed ||
-        src->subblock_bytes != dst->subblock_bytes)
-        return TQ_ERR_CONFIG_MISMATCH;
+    if (!same_config(src, dst)) return TQ_ERR_CONFIG_MISMATCH;
     if (n == 0) return TQ_OK;
     if (!src->pool || !dst->pool || !src_blocks || !dst_blocks) return TQ_ERR_INVALID_ARG;
     if (n > 2147483647 / 2 || src->num_layers > 65535) return TQ_ERR_INVALID_ARG;
@@ -517,7 +651,9 @@ namespace {
 tq_status decode_args(const tq_codec* kc, const tq_codec* vc, const tq_cache_desc* cache, int layer, const void* q,
                       tq_dtype q_dtype, int batch, int num_q_heads, int q_len, const int32_t* seq_lens,
                       const int32_t* block_table, int max_blocks, int max_seq_len, float scale, float* out,
-                      void* workspace, size_t workspace_bytes, DecodeArgs* args, bool* run) {
+                      void* workspace, size_t workspace_bytes, DecodeArgs* args, bool* run,
+                      const int32_t* causal_end = nullptr, float* part_ml = nullptr, float* part_acc = nullptr) {
+    const bool shard = part_acc != nullptr;
     *run = false;
     tq_status st = check_codecs_vs_cache(kc, vc, cache);
     if (st != TQ_OK) return st;
@@ -525,7 +661,7 @@ tq_status decode_args(const tq_codec* kc, const tq_codec* vc, const tq_cache_des
         return TQ_ERR_INVALID_ARG;
     if (q_dtype != TQ_F32 && q_dtype != TQ_BF16 && q_dtype != TQ_F16) return TQ_ERR_INVALID_ARG;
     if (num_q_heads <= 0 || num_q_heads % cache->num_kv_heads != 0) return TQ_ERR_INVALID_ARG;
-    if (max_seq_len < q_len) return TQ_ERR_INVALID_ARG;
+    if (max_seq_len < (shard ? 1 : q_len)) return TQ_ERR_INVALID_ARG;
     if (static_cast<int64_t>(max_seq_len) > static_cast<int64_t>(max_blocks) * cache->block_tokens)
         return TQ_ERR_CAPACITY;
     if (!block_table && static_cast<int64_t>(batch) * max_blocks > cache->num_blocks) return TQ_ERR_CAPACITY;
@@ -533,9 +669,11 @@ tq_status decode_args(const tq_codec* kc, const tq_codec* vc, const tq_cache_des
     if (G * q_len > 64) return TQ_ERR_UNSUPPORTED;
     if (batch == 0) return TQ_OK;
     if (batch > 65535) return TQ_ERR_INVALID_ARG;
-    if (!q || !out || !seq_lens || !workspace) return TQ_ERR_INVALID_ARG;
+    if (!q || !seq_lens || !workspace) return TQ_ERR_INVALID_ARG;
+    if (shard ? (!part_ml || !aligned16(part_acc) || (reinterpret_cast<uintptr_t>(part_ml) & 7u) != 0) : !out)
+        return TQ_ERR_INVALID_ARG;
     if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return TQ_ERR_INVALID_ARG;
-    if (!aligned16(out)) return TQ_ERR_INVALID_ARG;
+    if (!shard && !aligned16(out)) return TQ_ERR_INVALID_ARG;
     unsigned* err = nullptr;
     int sms = 0;
     if (device_state(&err, &sms) != TQ_OK) return TQ_ERR_CUDA;
@@ -557,6 +695,9 @@ tq_status decode_args(const tq_codec* kc, const tq_codec* vc, const tq_cache_des
     a.max_blocks = max_blocks;
     a.scale = scale == 0.0f ? 1.0f / std::sqrt(static_cast<float>(cache->head_dim)) : scale;
     a.out = out;
+    a.causal_end = causal_end;
+    a.part_ml = part_ml;
+    a.part_acc = part_acc;
     char* ws = static_cast<char*>(workspace);
     a.qrot = reinterpret_cast<float*>(ws);
     a.qjl = reinterpret_cast<float*>(ws + plan.q_bytes);
@@ -583,6 +724,36 @@ tq_status tq_decode_attention(const tq_codec* kc, const tq_codec* vc, const tq_c
                                      &a, &run);
     if (st != TQ_OK || !run) return st;
     return launch_decode(a, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
+}
+
+tq_status tq_decode_partials(const tq_codec* kc, const tq_codec* vc, const tq_cache_desc* cache, int layer,
+                             const void* q, tq_dtype q_dtype, int batch, int num_q_heads, int q_len,
+                             const int32_t* seq_lens, const int32_t* causal_end, const int32_t* block_table,
+                             int max_blocks, int max_seq_len, float scale, float* part_ml, float* part_acc,
+                             void* workspace, size_t workspace_bytes, tq_stream_t stream) {
+    if (!part_acc) return TQ_ERR_INVALID_ARG;
+    DecodeArgs a{};
+    bool run = false;
+    const tq_status st = decode_args(kc, vc, cache, layer, q, q_dtype, batch, num_q_heads, q_len, seq_lens,
+                                     block_table, max_blocks, max_seq_len, scale, nullptr, workspace,
+                                     workspace_bytes, &a, &run, causal_end, part_ml, part_acc);
+    if (st != TQ_OK || !run) return st;
+    return launch_decode(a, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
+}
+
+tq_status tq_decode_merge(const tq_codec* value_codec, int num_parts, const float* parts_ml, const float* parts_acc,
+                          int64_t rows, float* out, tq_stream_t stream) {
+    if (!value_codec || num_parts < 0 || rows < 0) return TQ_ERR_INVALID_ARG;
+    if (rows == 0) return TQ_OK;
+    if (num_parts == 0 || !parts_ml || !parts_acc || !out) return TQ_ERR_INVALID_ARG;
+    if (rows > 2147483647) return TQ_ERR_INVALID_ARG;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return TQ_ERR_CUDA;
+    if (dev != value_codec->device) return TQ_ERR_INVALID_ARG;
+    return launch_shard_merge(dev_view(value_codec), num_parts, parts_ml, parts_acc, rows, out,
+                              reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? TQ_OK
+               : TQ_ERR_CUDA;
 }
 
 tq_status tq_decode_step(const tq_codec* kc, const tq_codec* vc, const tq_cache_desc* cache, int layer,

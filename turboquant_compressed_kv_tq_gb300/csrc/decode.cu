@@ -114,7 +114,9 @@ __global__ void __launch_bounds__(kThreads) split_kernel(DecodeArgs a) {
 
     const int N = a.seq_lens[b] + a.len_add;
     const int cap = a.max_blocks * BT;
-    const bool bad = N < a.Lq || N > cap;
+    // causal window end (local token index): the sequence's end, or a shard's
+    const int vis = a.causal_end ? a.causal_end[b] : N;
+    const bool bad = N < (a.causal_end ? 0 : a.Lq) || N > cap;
     if (bad && split == 0 && tid == 0 && rg == 0 && h == 0) atomicOr(a.err, TQ_DEVERR_SEQLEN);
     const int t_begin = split * a.plan.chunk;
     int t_end = t_begin + a.plan.chunk;
@@ -186,7 +188,7 @@ __global__ void __launch_bounds__(kThreads) split_kernel(DecodeArgs a) {
                 if (t < nt && r < rows && pb_ok) {
                     const int l = r % a.Lq;
                     const int pos = tile + t;
-                    if (pos <= N - a.Lq + l) {
+                    if (pos <= vis - a.Lq + l) {
                         float dot = 0.0f;
                         for (int i = 0; i < D; ++i) dot = fmaf(sm.qr[rr][i], sm.kh[t][i], dot);
                         if (a.kc.mode == TQ_MODE_PROD) {
@@ -282,6 +284,17 @@ __global__ void merge_kernel(DecodeArgs a) {
                 o = fmaf(w, a.part[((base + s) * kRows + rr) * D + i], o);
             }
         }
+        const int g = r / a.Lq, l = r % a.Lq;
+        const int64_t orow = (static_cast<int64_t>(b) * a.Hq + h * a.G + g) * a.Lq + l;
+        if (a.part_acc) {
+            // a shard's state: max (natural-log units), sum, rotated-domain accumulator
+            if (i == 0) {
+                a.part_ml[2 * orow] = M;
+                a.part_ml[2 * orow + 1] = L;
+            }
+            a.part_acc[orow * D + i] = o;
+            continue;
+        }
         orot[i] = L > 0.0f ? o / L : 0.0f;
         __syncthreads();
         float res = orot[i];
@@ -289,10 +302,40 @@ __global__ void merge_kernel(DecodeArgs a) {
             res = 0.0f;
             for (int k = 0; k < D; ++k) res = fmaf(orot[k], __ldg(a.vc.R + k * D + i), res);
         }
-        const int g = r / a.Lq, l = r % a.Lq;
-        a.out[((static_cast<int64_t>(b) * a.Hq + h * a.G + g) * a.Lq + l) * D + i] = res;
+        a.out[orow * D + i] = res;
         __syncthreads();
     }
+}
+
+// Log-sum-exp merge of the partial states of P sequence shards, row r of
+// part p at ml[(p * rows + r) * 2] (max, sum) and acc[(p * rows + r) * D]:
+// M = max_p m_p, L = sum_p e^(m_p - M) l_p, o = sum_p e^(m_p - M) acc_p / L,
+// rotated back by R_v for MSE values. One CTA of D threads per row.
+__global__ void shard_merge_kernel(CodecDev vc, int P, const float* ml, const float* acc, int64_t rows, float* out) {
+    __shared__ float orot[256];
+    const int D = vc.D;
+    const int64_t r = blockIdx.x;
+    const int i = threadIdx.x;
+    float M = -INFINITY;
+    for (int p = 0; p < P; ++p) M = fmaxf(M, ml[(p * rows + r) * 2]);
+    float L = 0.0f, o = 0.0f;
+    if (M != -INFINITY) {
+        for (int p = 0; p < P; ++p) {
+            const float mp = ml[(p * rows + r) * 2];
+            if (mp == -INFINITY) continue;
+            const float w = expf(mp - M);
+            L = fmaf(w, ml[(p * rows + r) * 2 + 1], L);
+            o = fmaf(w, acc[(p * rows + r) * D + i], o);
+        }
+    }
+    orot[i] = L > 0.0f ? o / L : 0.0f;
+    __syncthreads();
+    float res = orot[i];
+    if (vc.mode != TQ_MODE_GROUP) {
+        res = 0.0f;
+        for (int k = 0; k < D; ++k) res = fmaf(orot[k], __ldg(vc.R + k * D + i), res);
+    }
+    out[r * D + i] = res;
 }
 
 template <int D>
@@ -475,6 +518,13 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s, const EncodeAppen
         case 256: return launch_decode_d<256>(a, s);
         default: return cudaErrorInvalidValue;
     }
+}
+
+cudaError_t launch_shard_merge(const CodecDev& vc, int parts, const float* ml, const float* acc, int64_t rows,
+                               float* out, cudaStream_t s) {
+    shard_merge_kernel<<<static_cast<unsigned>(rows), vc.D, 0, s>>>(vc, parts, ml, acc, rows, out);
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    return cudaGetLastError();
 }
 
 }  // namespace tq

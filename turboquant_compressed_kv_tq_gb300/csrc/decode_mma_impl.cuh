@@ -347,12 +347,29 @@ __device__ __forceinline__ void merge_unit(const MmaArgs& m, int unit, int split
         }
         // MSE values were multiplied as fp16(op_scale * level): divide op_scale out
         const float vs = VGROUP ? 1.0f : a.vc.cq_scale;
-        const float inv = L > 0.0f ? 1.0f / (L * vs) : 0.0f;
-        for (int k = 0; k < 8; ++k) orot[r * kStride + dbase + k] = acc[k] * inv;
+        const int row = rg * kRows + r;
+        if (a.part_acc) {
+            // a shard's state: max in natural-log units, sum, accumulator
+            if (row < a.plan.rows) {
+                const int gq = row / a.Lq, l = row % a.Lq;
+                const int64_t o = (static_cast<int64_t>(b) * a.Hq + h * a.G + gq) * a.Lq + l;
+                if ((tid & 15) == 0) {
+                    a.part_ml[2 * o] = M == -INFINITY ? -INFINITY : M * 0.6931471805599453f;
+                    a.part_ml[2 * o + 1] = L;
+                }
+                const float iv = 1.0f / vs;
+                float4* dst = reinterpret_cast<float4*>(a.part_acc + o * kD + dbase);
+                dst[0] = make_float4(acc[0] * iv, acc[1] * iv, acc[2] * iv, acc[3] * iv);
+                dst[1] = make_float4(acc[4] * iv, acc[5] * iv, acc[6] * iv, acc[7] * iv);
+            }
+        } else {
+            const float inv = L > 0.0f ? 1.0f / (L * vs) : 0.0f;
+            for (int k = 0; k < 8; ++k) orot[r * kStride + dbase + k] = acc[k] * inv;
+        }
     }
     __syncthreads();
     const int row = rg * kRows + r;
-    if (merger && row < a.plan.rows) {
+    if (merger && row < a.plan.rows && !a.part_acc) {
         float res[8];
         if constexpr (!VGROUP) {
             for (int k = 0; k < 8; ++k) res[k] = 0.0f;
@@ -398,7 +415,9 @@ __global__ void __launch_bounds__(kThreads, 1) split_mma_kernel(MmaArgs m) {
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + st.bar_off) + warp * kStages;
 
     const int N = a.seq_lens[b] + a.len_add;
-    const bool bad = N < a.Lq || N > a.max_blocks * BT;
+    // causal window end (local token index): the sequence's end, or a shard's
+    const int vis = a.causal_end ? a.causal_end[b] : N;
+    const bool bad = N < (a.causal_end ? 0 : a.Lq) || N > a.max_blocks * BT;
     if (bad && split == 0 && threadIdx.x == 0 && rg == 0 && h == 0) atomicOr(a.err, TQ_DEVERR_SEQLEN);
     const int t_begin = split * a.plan.chunk;
     const int t_end = min(t_begin + a.plan.chunk, bad ? 0 : N);
@@ -444,9 +463,9 @@ __global__ void __launch_bounds__(kThreads, 1) split_mma_kernel(MmaArgs m) {
 
     // causal limits of this thread's two rows (padding rows see everything)
     const int r0 = rg * kRows + g, r1 = r0 + 8;
-    const int lim0 = r0 < a.plan.rows ? N - a.Lq + (r0 % a.Lq) : N - 1;
-    const int lim1 = r1 < a.plan.rows ? N - a.Lq + (r1 % a.Lq) : N - 1;
-    const int lim_all = N - a.Lq;  // every row sees the tokens up to here
+    const int lim0 = r0 < a.plan.rows ? vis - a.Lq + (r0 % a.Lq) : N - 1;
+    const int lim1 = r1 < a.plan.rows ? vis - a.Lq + (r1 % a.Lq) : N - 1;
+    const int lim_all = vis - a.Lq;  // every row sees the tokens up to here
 
     float o[16][4];
 #pragma unroll

@@ -127,6 +127,14 @@ struct DecodeArgs {
     int max_blocks;
     float scale;
     float* out;
+    // Sequence shards (tq_decode_partials): causal_end[b] (device, or null:
+    // the sequence's own length) is where the queries' causal window ends in
+    // the shard's local token indices; with part_ml / part_acc set, the final
+    // merge writes each row's unnormalised softmax state (max in natural-log
+    // units, sum, accumulator in the rotated domain) there instead of out.
+    const int32_t* causal_end;
+    float* part_ml;    // [B][Hq][Lq][2]
+    float* part_acc;   // [B][Hq][Lq][D]
     float* qrot;   // [B][Hkv][RG*16][D]
     float* qjl;    // [B][Hkv][RG*16][D]
     float* part;   // [B][Hkv][RG][splits][16][D]
@@ -166,8 +174,21 @@ cudaError_t launch_quantize(const QuantizeArgs& a, cudaStream_t s);
 // `step` (tensor-core path only): the decode step's append, fused into the
 // query-prep launch; null for a plain decode.
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s, const EncodeAppendArgs* step = nullptr);
+// Log-sum-exp merge of sequence shards' partial states, then 1 / sum and
+// the inverse value rotation (MSE values): decode.cu.
+cudaError_t launch_shard_merge(const CodecDev& vc, int parts, const float* ml, const float* acc, int64_t rows,
+                               float* out, cudaStream_t s);
 cudaError_t launch_copy_blocks(const tq_cache_desc* src, const tq_cache_desc* dst, const int32_t* src_ids,
                                const int32_t* dst_ids, int n, unsigned* err, cudaStream_t s);
+// Block-table rows of a batch operation (cache_ops.cu): n output rows from
+// src rows `rows` (host list, <= 256) or src_row0.., written at dst_row0..;
+// copy: blocks moved into ids from the free list; n_drop rows (host list)
+// whose block ids go to `freed`.
+cudaError_t launch_batch_rows(const tq_batch* src, tq_batch* dst, int n, const int* rows, int src_row0, int dst_row0,
+                              bool copy, const int32_t* free_blocks, int n_free, int32_t* n_used, int n_drop,
+                              const int* drop, int32_t* freed, int32_t* n_freed, bool reset_freed, unsigned* err,
+                              cudaStream_t s);
+constexpr int kBatchRowChunk = 256;
 namespace mmadec {
 bool prefill_supported(int kb, bool kprod, bool vgroup, int vb);
 cudaError_t launch_prefill(const DecodeArgs& a, const uint4* qfrag, cudaStream_t s);
