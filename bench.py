@@ -1,19 +1,26 @@
-"""Benchmark: TurboQuant compressed-KV decode attention at 256k context.
+"""Benchmark: TurboQuant compressed-KV decode attention.
 
-Workload (one replica per GPU): 64 layers, 8 KV heads, 64 query heads,
-head_dim 128, keys 3-bit prod, values 3-bit MSE, 262,144 tokens prefilled by
-chunked encode (8192-token chunks), then decode steps that each append 2
-tokens per layer and attend with query length 2 over every layer.
+Default workload, long_256k (one replica per GPU): 64 layers, 8 KV heads, 64
+query heads, head_dim 128, keys 3-bit prod, values 3-bit MSE, 262,144 tokens
+prefilled by chunked encode (8192-token chunks), then decode steps that each
+append 2 tokens per layer and attend with query length 2 over every layer.
+Other workloads of the same family (--workload): stack_32k (64 layers,
+32,768 tokens, 4-bit MSE keys and values, q_len 2, no append), paged_batch
+(32 ragged sequences in 16-token blocks handed out in a shuffled order, one
+token appended per sequence per step, q_len 1), layer_d256 (one head_dim-256
+layer, 8192 tokens, group values) and tiny (one layer, 512 tokens).
 
-A step = for each of the 64 layers: the append of 2 tokens x 8 heads and the
-decode attention (q_len 2), through tq_decode_step (the append runs inside the
-decode's query-prep launch; --step-api separate: tq_encode_append then
-tq_decode_attention). `value` is the compressed bytes the
-step's decode reads (valid tokens x heads x layers x record bytes) divided by
-the step time, summed over ranks. Inputs are resident in HBM before the timed
-region; the cache (14.5 GB) is far larger than L2, so no flush is needed.
+A step = for each layer: the append of the step's tokens and the decode
+attention, through tq_decode_step (the append runs inside the decode's
+query-prep launch; --step-api separate: tq_encode_append then
+tq_decode_attention), or tq_decode_attention alone for workloads without an
+append. `value` is the compressed bytes the step's decode reads (valid tokens
+x heads x layers x record bytes, summed over the sequences) divided by the
+step time, summed over ranks. Inputs are resident in HBM before the timed
+region; caches larger than L2 need no flush, smaller ones are flushed by a
+write of 512 MB between timed steps (outside the timed events).
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference] [--workload NAME]
 """
 from __future__ import annotations
 
@@ -35,12 +42,40 @@ METRIC = "compressed-KV decode-attn HBM GB/s (% of peak) and steps/s @256k; enco
 UNIT = "GB/s"
 
 
-# DRAM bytes (read + write) ncu counted for one tq_decode_attention call of
-# this workload (split kernel 226.74 + 3.10 MB, query prep 0.19 MB); set to
-# None whenever those kernels change until they are captured again.
-DECODE_TRAFFIC_BYTES = 230.03e6
-DECODE_TRAFFIC_SOURCE = ("ncu dram__bytes_read.sum + dram__bytes_write.sum of split_mma_kernel and qfrag_kernel, "
-                         "one layer of this workload: bench.py --layers 1 --steps 4 --warmup 3")
+# DRAM traffic of the dominant decode kernel as an ncu capture measured it,
+# valid only for the kernel sources it was measured on (profiles/
+# decode_traffic_<workload>.txt: the sources' sha256, the bytes per launch and
+# the capture command); otherwise the roofline's traffic is null.
+TRAFFIC_SOURCES = ["decode_mma.cuh", "decode_mma_impl.cuh", "decode_mma_a.cu", "decode_mma_b.cu",
+                   "decode_mma_c.cu", "decode_step.cu", "decode.cu", "tc_ptx.cuh", "tq_internal.h"]
+
+
+def decode_sources_sha256() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "turboquant_compressed_kv_tq_gb300", "csrc")
+    for name in TRAFFIC_SOURCES:
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()
+
+
+def measured_traffic(workload: str):
+    """(bytes per launch, source line) from the committed capture record when
+    it was taken on the current kernel sources, else (None, reason)."""
+    path = os.path.join(ROOT, "profiles", f"decode_traffic_{workload}.txt")
+    try:
+        rec = {}
+        with open(path) as f:
+            for line in f:
+                if ":" in line and not line.startswith("#"):
+                    k, v = line.split(":", 1)
+                    rec[k.strip()] = v.strip()
+        if rec.get("sources_sha256") != decode_sources_sha256():
+            return None, "ncu capture taken on other kernel sources"
+        return float(rec["dram_bytes_per_launch"]), rec.get("command", path)
+    except (OSError, KeyError, ValueError):
+        return None, "no ncu capture of these kernel sources"
 
 
 def _peaks(key: str = "hbm_gbs"):
@@ -152,23 +187,24 @@ def aggregate(bytes_per_step: float, step_ms_local: float, world: int, device=No
 # ------------------------------------------------------------------ oracle baseline
 
 class OracleSample:
-    """Oracle records of a bounded sample of the bench workload: layer 0,
-    `kv_heads` KV heads at the full prefill length (encoded once, by the
-    oracle, from the same device-generated inputs the GPU arm encodes)."""
+    """Oracle records of a bounded sample of a workload: layer 0, sequence 0,
+    `kv_heads` KV heads at the sequence's full prefill length (encoded once, by
+    the oracle, from the same device-generated inputs the GPU arm encodes)."""
 
     def __init__(self, w, kv_heads=1, device="cuda"):
         import oracle as O
         from turboquant_compressed_kv_tq_gb300 import workloads as wl
         O.build()
-        self.O, self.w, self.kv_heads = O, w, kv_heads
+        self.O, self.w = O, w
+        self.kv_heads = min(kv_heads, w.num_kv_heads)
         D, N = w.head_dim, w.seq_lens[0]
-        self.kc = O.Codec(D, w.key.bits, w.key.mode, w.key.seed)
-        self.vc = O.Codec(D, w.value.bits, w.value.mode, w.value.seed)
-        K = wl.kv_chunk(w, 0, 0, 0, N, "k", device)[:kv_heads].float().cpu().numpy()
-        V = wl.kv_chunk(w, 0, 0, 0, N, "v", device)[:kv_heads].float().cpu().numpy()
+        self.kc = O.Codec(D, w.key.bits, w.key.mode, w.key.seed, w.key.group_size)
+        self.vc = O.Codec(D, w.value.bits, w.value.mode, w.value.seed, w.value.group_size)
+        K = wl.kv_chunk(w, 0, 0, 0, N, "k", device)[:self.kv_heads].float().cpu().numpy()
+        V = wl.kv_chunk(w, 0, 0, 0, N, "v", device)[:self.kv_heads].float().cpu().numpy()
         self.q = wl.queries(w, 0, 0, device)[0].double().cpu().numpy()
-        self.recs = [(self.kc.encode(K[h]), self.vc.encode(V[h])) for h in range(kv_heads)]
-        self.nbytes = kv_heads * N * (self.kc.record_bytes + self.vc.record_bytes)
+        self.recs = [(self.kc.encode(K[h]), self.vc.encode(V[h])) for h in range(self.kv_heads)]
+        self.nbytes = self.kv_heads * N * (self.kc.record_bytes + self.vc.record_bytes)
 
     def decode_seconds(self):
         """Wall time of the oracle's rotated-domain decode of the sample."""
@@ -181,8 +217,8 @@ class OracleSample:
 
     def describe(self):
         w = self.w
-        return (f"oracle rotated-domain decode (fp64, OpenMP over query rows), layer 0, "
-                f"{self.kv_heads} KV head(s) x {w.gqa * w.q_len} query rows, N={w.seq_lens[0]}, "
+        return (f"oracle rotated-domain decode (fp64, OpenMP over query rows) of {w.name}: layer 0, "
+                f"sequence 0, {self.kv_heads} KV head(s) x {w.gqa * w.q_len} query rows, N={w.seq_lens[0]}, "
                 f"{self.nbytes / 1e6:.1f} MB of compressed records per sample")
 
 
@@ -195,13 +231,22 @@ def cpu_baseline(w, kv_heads=2, device="cuda", repeats=3):
     return smp.nbytes / t / 1e9, smp.O.num_threads(), smp.describe(), sum(times)
 
 
+def _workload(args):
+    from turboquant_compressed_kv_tq_gb300 import workloads as wl
+    w = wl.WORKLOADS[args.workload]()
+    if args.layers:
+        # fewer layers of the same workload: a small case for profiler captures,
+        # never a headline number (the layer count is in config.workload)
+        w = dataclasses.replace(w, num_layers=args.layers)
+    return w
+
+
 def run_reference(args):
     rank, world, local = dist_env()
     if rank != 0:
         return 0
     import torch
-    from turboquant_compressed_kv_tq_gb300 import workloads as wl
-    w = wl.long_256k()
+    w = _workload(args)
     dev = "cuda" if torch.cuda.is_available() else "cpu"
     smp = OracleSample(w, 1, dev)
     for _ in range(args.warmup):
@@ -220,11 +265,20 @@ def run_reference(args):
     return 0
 
 
+def _codec_text(c):
+    name = {0: "MSE", 1: "prod", 2: "group"}[c.mode]
+    return f"{c.bits}-bit {name}" + (f" (group {c.group_size})" if c.mode == 2 else "")
+
+
 def _workload_text(w):
-    return (f"{w.name}: {w.num_layers} layers, {w.num_kv_heads} KV heads, {w.num_q_heads} query "
-            f"heads, head_dim {w.head_dim}, batch {w.batch}, N={w.seq_lens[0]} prefilled in "
-            f"{w.prefill_chunk}-token chunks then +{w.append_per_step} tokens per step, q_len "
-            f"{w.q_len}; keys {w.key.bits}-bit prod, values {w.value.bits}-bit MSE; bf16 inputs N(0,1)")
+    lens = w.seq_lens
+    n = f"N={lens[0]}" if len(lens) == 1 else f"N in [{min(lens)}, {max(lens)}] (sum {sum(lens)})"
+    return (f"{w.name}: {w.num_layers} layers, batch {w.batch}, {w.num_kv_heads} KV heads, {w.num_q_heads} "
+            f"query heads, head_dim {w.head_dim}, {n} prefilled in {w.prefill_chunk}-token chunks"
+            f"{f' then +{w.append_per_step} token(s) per sequence per step' if w.append_per_step else ''}, "
+            f"q_len {w.q_len}, {w.block_tokens}-token blocks{' (shuffled)' if w.shuffle_blocks else ''}; "
+            f"keys {_codec_text(w.key)}, values {_codec_text(w.value)}; {str(w.dtype).split('.')[-1]} inputs "
+            f"N(0, {w.std}^2){' x per-head scale U' + str(w.head_scale_range) if w.head_scale_range else ''}")
 
 
 # ------------------------------------------------------------------ GPU arm
@@ -274,7 +328,6 @@ def measure_prefill_attention(tq, wl, dev, reps: int = 3):
 
 
 def run_gpu(args):
-    import numpy as np
     import torch
 
     rank, world, local = dist_env()
@@ -291,136 +344,174 @@ def run_gpu(args):
     import turboquant_compressed_kv_tq_gb300 as tq
     from turboquant_compressed_kv_tq_gb300 import workloads as wl
 
-    w = wl.long_256k()
-    if args.layers:
-        # fewer layers of the same workload: a small case for profiler captures,
-        # never a headline number (the layer count is in config.workload)
-        w = dataclasses.replace(w, num_layers=args.layers)
-    L, Hkv, Hq, D, Lq = w.num_layers, w.num_kv_heads, w.num_q_heads, w.head_dim, w.q_len
-    N0 = w.seq_lens[0]
+    w = _workload(args)
+    L, B, Hkv, Hq, D, Lq = w.num_layers, w.batch, w.num_kv_heads, w.num_q_heads, w.head_dim, w.q_len
     A = w.append_per_step
+    lens0 = list(w.seq_lens)
     total_steps = args.warmup + args.steps
-    cap = N0 + A * total_steps
+    caps = [n + A * total_steps for n in lens0]
+    cap = max(caps)
     BT = w.block_tokens
-    nblk = (cap + BT - 1) // BT
-    kc = tq.Codec(D, w.key.bits, w.key.mode, w.key.seed)
-    vc = tq.Codec(D, w.value.bits, w.value.mode, w.value.seed)
+    paged = w.shuffle_blocks or B > 1
+    if paged:
+        table_h, nblk = wl.block_table(w, caps)
+        max_blocks = table_h.shape[1]
+        table = table_h.to(dev)
+    else:
+        max_blocks = nblk = (cap + BT - 1) // BT
+        table = None
+    kc = tq.Codec(D, w.key.bits, w.key.mode, w.key.seed, w.key.group_size)
+    vc = tq.Codec(D, w.value.bits, w.value.mode, w.value.seed, w.value.group_size)
     cache = tq.CompressedKVCache(kc, vc, L, nblk, BT, Hkv, dev)
     rec_bytes = kc.record_bytes + vc.record_bytes
 
     stream = torch.cuda.current_stream(dev)
-    # ---------------- prefill: chunked encode of every layer (timed per layer)
-    zero = torch.zeros(1, dtype=torch.int32, device=dev)
+    # ---------------- prefill: chunked encode of every layer and sequence (timed)
     enc_ms = 0.0
     chunk = w.prefill_chunk
-    nchunks = (N0 + chunk - 1) // chunk
-    starts = torch.arange(0, N0, chunk, dtype=torch.int32, device=dev)
     for layer in range(L):
-        ks = [wl.kv_chunk(w, layer, rank, c * chunk, min(chunk, N0 - c * chunk), "k", dev).unsqueeze(0)
-              for c in range(nchunks)]
-        vs = [wl.kv_chunk(w, layer, rank, c * chunk, min(chunk, N0 - c * chunk), "v", dev).unsqueeze(0)
-              for c in range(nchunks)]
+        jobs = []
+        for b in range(B):
+            for c0 in range(0, lens0[b], chunk):
+                n = min(chunk, lens0[b] - c0)
+                jobs.append((b, c0,
+                             wl.kv_chunk(w, layer, b + rank * B, c0, n, "k", dev).unsqueeze(0),
+                             wl.kv_chunk(w, layer, b + rank * B, c0, n, "v", dev).unsqueeze(0),
+                             torch.tensor([c0], dtype=torch.int32, device=dev)))
         torch.cuda.synchronize(dev)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        for c in range(nchunks):
-            cache.append(layer, ks[c], vs[c], starts[c:c + 1], None, nblk)
+        for b, c0, k, v, start in jobs:
+            cache.append(layer, k, v, start, table[b:b + 1] if paged else None, max_blocks)
         e1.record(stream)
         torch.cuda.synchronize(dev)
         enc_ms += e0.elapsed_time(e1)
-        del ks, vs
+        del jobs
     assert tq.tq_device_error() == 0
 
     # ---------------- decode-step inputs, resident on the device
     steps_in = []
     for s in range(total_steps):
-        k_new = torch.stack([wl.kv_chunk(w, layer, rank, N0 + A * s, A, "k", dev) for layer in range(L)])
-        v_new = torch.stack([wl.kv_chunk(w, layer, rank, N0 + A * s, A, "v", dev) for layer in range(L)])
-        q = torch.stack([wl.queries(w, layer, s, dev)[0] for layer in range(L)])
-        steps_in.append((k_new.unsqueeze(1).contiguous(), v_new.unsqueeze(1).contiguous(),
-                         q.unsqueeze(1).contiguous()))
-    lens_pre = torch.tensor([N0 + A * s for s in range(total_steps)], dtype=torch.int32, device=dev)
-    lens_post = lens_pre + A
-    ws = torch.empty(cache.workspace_bytes(1, Hq, Lq, cap), dtype=torch.uint8, device=dev)
-    out = torch.empty(L, 1, Hq, Lq, D, dtype=torch.float32, device=dev)
+        q = torch.stack([wl.queries(w, layer, s, dev) for layer in range(L)])      # [L, B, Hq, Lq, D]
+        if A:
+            k_new = torch.stack([torch.stack([wl.kv_chunk(w, layer, b + rank * B, lens0[b] + A * s, A, "k", dev)
+                                              for b in range(B)]) for layer in range(L)])
+            v_new = torch.stack([torch.stack([wl.kv_chunk(w, layer, b + rank * B, lens0[b] + A * s, A, "v", dev)
+                                              for b in range(B)]) for layer in range(L)])
+            steps_in.append((k_new.contiguous(), v_new.contiguous(), q.contiguous()))
+        else:
+            steps_in.append((None, None, q.contiguous()))
+    lens_pre = [torch.tensor([n + A * s for n in lens0], dtype=torch.int32, device=dev) for s in range(total_steps)]
+    lens_post = [t + A for t in lens_pre]
+    ws = torch.empty(cache.workspace_bytes(B, Hq, Lq, cap), dtype=torch.uint8, device=dev)
+    out = torch.empty(L, B, Hq, Lq, D, dtype=torch.float32, device=dev)
+    # caches that fit in L2 (129 MB) with room to spare are flushed before each step
+    l2_resident = sum(lens0) * Hkv * rec_bytes * L < 64e6
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev) if l2_resident else None
 
     fused = args.step_api == "fused"
 
-    def step(s, ev=None):
-        k_new, v_new, q = steps_in[s]
+    def step(s, inputs=None):
+        k_new, v_new, q = inputs if inputs is not None else steps_in[s]
         for layer in range(L):
-            if fused and ev is None:
+            if A and fused:
                 # one call: the append runs inside the decode's query-prep launch
-                cache.decode_step(layer, k_new[layer], v_new[layer], q[layer], lens_pre[s:s + 1], None, nblk,
+                cache.decode_step(layer, k_new[layer], v_new[layer], q[layer], lens_pre[s], table, max_blocks,
                                   cap, out[layer], ws)
                 continue
-            cache.append(layer, k_new[layer], v_new[layer], lens_pre[s:s + 1], None, nblk)
-            if ev is not None:
-                ev[layer][0].record(stream)
-            cache.decode(layer, q[layer], lens_post[s:s + 1], None, nblk, cap, out[layer], ws)
-            if ev is not None:
-                ev[layer][1].record(stream)
+            if A:
+                cache.append(layer, k_new[layer], v_new[layer], lens_pre[s], table, max_blocks)
+            cache.decode(layer, q[layer], lens_post[s], table, max_blocks, cap, out[layer], ws)
 
     for s in range(args.warmup):
         step(s)
     torch.cuda.synchronize(dev)
+    # small workloads are launch-bound on the host: each timed step of an
+    # L2-resident cache is replayed from a CUDA graph of its launches
+    graphs = None
+    if l2_resident:
+        try:
+            graphs, graph_launches = [], 0
+            for s in range(args.warmup, total_steps):
+                gph = torch.cuda.CUDAGraph()
+                n0 = tq.tq_launch_count()
+                with torch.cuda.graph(gph):
+                    step(s)
+                graph_launches += tq.tq_launch_count() - n0   # kernels each replay launches
+                graphs.append(gph)
+            torch.cuda.synchronize(dev)
+        except Exception as exc:   # capture refused: time the eager calls instead
+            print(f"CUDA graph capture unavailable ({exc}); timing eager launches", file=sys.stderr)
+            graphs = None
     # ---------------- timed region
     n_launch0 = tq.tq_launch_count()
     barrier(world)
     torch.cuda.synchronize(dev)
-    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps if l2_resident else 1)]
     with ClockSampler(local) as clk:
-        t_start.record(stream)
-        for s in range(args.warmup, total_steps):
-            step(s)
-        t_end.record(stream)
+        if l2_resident:
+            # caches that fit in L2: each step timed alone after a flush write
+            for i, s in enumerate(range(args.warmup, total_steps)):
+                flush.fill_(i & 255)
+                evs[i][0].record(stream)
+                if graphs is not None:
+                    graphs[i].replay()
+                else:
+                    step(s)
+                evs[i][1].record(stream)
+        else:
+            evs[0][0].record(stream)
+            for s in range(args.warmup, total_steps):
+                step(s)
+            evs[0][1].record(stream)
         torch.cuda.synchronize(dev)
     barrier(world)
-    launches = tq.tq_launch_count() - n_launch0
-    step_ms = t_start.elapsed_time(t_end) / args.steps
+    launches = tq.tq_launch_count() - n_launch0   # this library's kernels only (the flush is torch's)
+    if graphs is not None:
+        launches += graph_launches   # replays launch the captured kernels again
+    step_ms = sum(a.elapsed_time(b) for a, b in evs) / args.steps
     # bytes the decode of step s reads: valid tokens x heads x layers x record bytes
-    dec_bytes = [L * Hkv * (N0 + A * s + A) * rec_bytes for s in range(args.warmup, total_steps)]
+    dec_bytes = [L * Hkv * sum(n + A * s + A for n in lens0) * rec_bytes for s in range(args.warmup, total_steps)]
     bytes_per_step = sum(dec_bytes) / args.steps
     value, step_ms_max = aggregate(bytes_per_step, step_ms, world, dev)
 
-    # ---------------- roofline pass: per-launch decode timing on the launching stream
-    evs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-            for _ in range(L)] for _ in range(args.steps)]
-    torch.cuda.synchronize(dev)
-    for i, s in enumerate(range(args.warmup, total_steps)):
-        step(s, evs[i])
-    torch.cuda.synchronize(dev)
-    durs = [a.elapsed_time(b) for row in evs for a, b in row]
-    dec_ms = sum(durs) / len(durs)
+    # ---------------- roofline: the decode of one layer is the dominant launch;
+    # inside a step a layer's preparation kernel overlaps the previous layer's
+    # decode, so the decode's in-step duration per launch is the step time
+    # over the layers (CUDA events on the launching stream, timed region above)
     per_launch_bytes = bytes_per_step / L
+    launch_ms = step_ms / L
     peak, peak_kind = _peaks()
-    achieved = per_launch_bytes / (dec_ms * 1e-3) / 1e9
+    achieved = per_launch_bytes / (launch_ms * 1e-3) / 1e9
+    traffic, traffic_src = measured_traffic(w.name)
+    # the decode call timed alone between events (which serialise it with its
+    # neighbours), for reference
+    e_iso = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(L)]
+    s_last = total_steps - 1
+    torch.cuda.synchronize(dev)
+    for layer in range(L):
+        e_iso[layer][0].record(stream)
+        cache.decode(layer, steps_in[s_last][2][layer], lens_post[s_last], table, max_blocks, cap, out[layer], ws)
+        e_iso[layer][1].record(stream)
+    torch.cuda.synchronize(dev)
+    iso_ms = sum(a.elapsed_time(b) for a, b in e_iso) / L
 
     # ---------------- end to end through the API with host buffers
-    pin_in = []
-    for s in range(args.warmup, total_steps):
-        pin_in.append(tuple(t.cpu().pin_memory() for t in steps_in[s]))
+    pin_in = [tuple(None if t is None else t.cpu().pin_memory() for t in steps_in[s])
+              for s in range(args.warmup, total_steps)]
     out_host = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
-    dk = torch.empty_like(steps_in[0][0])
-    dv = torch.empty_like(steps_in[0][1])
-    dq = torch.empty_like(steps_in[0][2])
-    h2d = sum(t.numel() * t.element_size() for t in pin_in[0])
+    dev_in = tuple(None if t is None else torch.empty_like(t) for t in steps_in[0])
+    h2d = sum(t.numel() * t.element_size() for t in pin_in[0] if t is not None)
     d2h = out_host.numel() * out_host.element_size()
     torch.cuda.synchronize(dev)
     barrier(world)
     t0 = time.perf_counter()
     for i, s in enumerate(range(args.warmup, total_steps)):
-        hk, hv, hq = pin_in[i]
-        dk.copy_(hk, non_blocking=True)
-        dv.copy_(hv, non_blocking=True)
-        dq.copy_(hq, non_blocking=True)
-        for layer in range(L):
-            if fused:
-                cache.decode_step(layer, dk[layer], dv[layer], dq[layer], lens_pre[s:s + 1], None, nblk, cap,
-                                  out[layer], ws)
-            else:
-                cache.append(layer, dk[layer], dv[layer], lens_pre[s:s + 1], None, nblk)
-                cache.decode(layer, dq[layer], lens_post[s:s + 1], None, nblk, cap, out[layer], ws)
+        for d, h in zip(dev_in, pin_in[i]):
+            if d is not None:
+                d.copy_(h, non_blocking=True)
+        step(s, dev_in)
         out_host.copy_(out, non_blocking=True)
         torch.cuda.current_stream(dev).synchronize()
     e2e_s = (time.perf_counter() - t0) / args.steps
@@ -428,10 +519,9 @@ def run_gpu(args):
     e2e_value = world * bytes_per_step / e2e_s / 1e9
     assert tq.tq_device_error() == 0
 
-    enc_tokens = N0 * L * Hkv
-    result = None
+    enc_tokens = sum(lens0) * L * Hkv
     pfa = None
-    if rank == 0 and not args.no_prefill_attention:
+    if rank == 0 and not args.no_prefill_attention and w.name == "long_256k" and not args.layers:
         del steps_in, pin_in
         pfa = measure_prefill_attention(tq, wl, dev)
         peak_t, _ = _peaks("bf16_tflops")
@@ -443,27 +533,35 @@ def run_gpu(args):
             cpu = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample,
                    "seconds": round(secs, 2)}
         clocks = clk.summary()
+        dominant = ("split_mma_kernel (tensor-core split-K decode)" if D == 128
+                    else "split_kernel + merge_kernel (SIMT decode)")
         result = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": step_ms_max, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f16+f32", "data": "synthetic",
             "config": {"workload": _workload_text(w),
                        "bytes_per_step": bytes_per_step, "record_bytes_per_token_head": rec_bytes,
-                       "l2": "inputs larger than L2: each step reads a 14.5 GB compressed cache",
-                       "step_api": ("tq_decode_step" if fused else "tq_encode_append + tq_decode_attention"),
-                       "block_tokens": BT, "replicas": world},
+                       "l2": ("caches fit in L2: a 512 MB write flushes L2 before each timed step"
+                              + ("; each step replayed from a CUDA graph" if graphs is not None else "")
+                              if l2_resident else
+                              f"inputs larger than L2: each step reads {bytes_per_step / 1e9:.2f} GB of records"),
+                       "step_api": ("tq_decode_step" if (fused and A) else
+                                    "tq_encode_append + tq_decode_attention" if A else "tq_decode_attention"),
+                       "block_tokens": BT, "block_table": "shuffled" if w.shuffle_blocks else
+                       ("identity" if paged else "none (contiguous)"), "replicas": world},
             "steps_per_s": 1000.0 / step_ms_max,
+            "us_per_step": 1000.0 * step_ms_max,
             "hbm_frac_of_measured": value / world / peak,
             "encode": {"prefill_s": enc_ms / 1e3,
                        "mtok_s": enc_tokens / (enc_ms * 1e-3) / 1e6,
                        "unit": "M token-head-layers/s",
-                       "model_tokens_per_s": N0 / (enc_ms * 1e-3),
+                       "model_tokens_per_s": sum(lens0) / (enc_ms * 1e-3),
                        "gb_s_in_out": (enc_tokens * (2 * 2 * D + rec_bytes)) / (enc_ms * 1e-3) / 1e9},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                         "frac": achieved / peak, "traffic": DECODE_TRAFFIC_BYTES, "peak_kind": peak_kind,
-                         "traffic_source": DECODE_TRAFFIC_SOURCE,
-                         "kernel": "tq_decode_attention (query prep + split + merge), per layer",
-                         "avg_launch_ms": dec_ms, "algorithmic_bytes_per_launch": per_launch_bytes},
+                         "frac": achieved / peak, "traffic": traffic, "peak_kind": peak_kind,
+                         "traffic_source": traffic_src, "kernel": dominant + ", one layer per launch",
+                         "avg_launch_ms": launch_ms, "launch_timing": "in-step: step time / layers",
+                         "isolated_call_ms": iso_ms, "algorithmic_bytes_per_launch": per_launch_bytes},
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": e2e_s * 1e3},
             "gpu_launches": launches,
@@ -483,9 +581,12 @@ def run_gpu(args):
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=256)  # the workload's 256 decode steps
+    ap.add_argument("--steps", type=int, default=0,
+                    help="timed steps (default: the workload's own: 256 decode steps for long_256k, else 20)")
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--workload", default="long_256k",
+                    choices=["long_256k", "stack_32k", "paged_batch", "layer_d256", "tiny"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--step-api", default="fused", choices=["fused", "separate"],
                     help="decode step per layer: tq_decode_step (append fused into the decode's first launch) "
@@ -493,8 +594,10 @@ def main(argv=None):
     ap.add_argument("--no-prefill-attention", action="store_true",
                     help="skip the one-layer prefill-attention measurement")
     ap.add_argument("--layers", type=int, default=0,
-                    help="run only the first L layers (profiling case; default: all 64)")
+                    help="run only the first L layers (profiling case; default: all of the workload's)")
     args = ap.parse_args(argv)
+    if args.steps <= 0:
+        args.steps = 256 if args.workload == "long_256k" else 20
     if args.warmup < 3 and args.impl != "reference":
         args.warmup = 3
     if args.impl == "reference":

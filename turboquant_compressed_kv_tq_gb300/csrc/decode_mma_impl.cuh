@@ -1,6 +1,8 @@
 // Kernel templates of the tensor-core decode path (see decode_mma.cuh).
 #pragma once
 
+#include <type_traits>
+
 #include "decode_mma.cuh"
 #include "tc_ptx.cuh"
 
@@ -251,6 +253,45 @@ inline int qfrag_grid(int units) {
 }
 
 // ------------------------------------------------------------------ split kernel
+
+// Key operands of k-steps 2 q2 and 2 q2 + 1 (four half2: (b0, b1) of each)
+// from one token's index words, in the pair order the query fragments use.
+template <int KB, bool QUAD, typename Tab>
+__device__ __forceinline__ void key_ks2(const uint32_t (&w)[KB], const Tab& t, uint32_t lane_addr, int q2,
+                                        uint32_t (&h)[4]) {
+    if constexpr (QUAD) {
+        // 2-bit codes, natural pair order: byte k of word hw is k-step 4 hw + k
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int ks = 2 * q2 + e, hw = ks >> 2, k = ks & 3;
+            const uint32_t f = k == 0 ? shl_f(w[hw], 7) : (w[hw] >> (8 * k - 7));
+            const uint2 v = lds_u64(mad_lo(f & 0x7F80u, kDc.pow2[0], lane_addr));
+            h[2 * e] = v.x;
+            h[2 * e + 1] = v.y;
+        }
+    } else if constexpr (KB == 1) {
+        const uint32_t neg2 = t.lo;
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int ks = 2 * q2 + e;
+            h[2 * e] = dec1(w[0], 15 - ks, neg2);
+            h[2 * e + 1] = dec1(w[0], 7 - ks, neg2);
+        }
+    } else if constexpr (KB == 2) {
+        // k-step 2 s + hw from word hw, code group s
+        dec2_pair(w[0], q2, t, h[0], h[1]);
+        dec2_pair(w[1], q2, t, h[2], h[3]);
+    } else if constexpr (KB == 3) {
+        uint32_t v;
+        if (q2 == 0) v = w[0] & 0xFFFFFFu;
+        else if (q2 == 1) v = mad_lo(w[1] & 0xFFFFu, kDc.pow2[8], (w[0] >> 24));
+        else if (q2 == 2) v = mad_lo(w[2] & 0xFFu, kDc.pow2[16], (w[1] >> 16));
+        else v = w[2] >> 8;
+        dec3_group(v, t, h);
+    } else {
+        dec4_word(w[q2], t, h);
+    }
+}
 
 template <int NW>
 __device__ __forceinline__ void load_words(const uint32_t* p, uint32_t (&w)[NW]) {
@@ -572,65 +613,58 @@ __global__ void __launch_bounds__(kThreads, 1) split_mma_kernel(MmaArgs m) {
             if (__any_sync(0xffffffffu, nmax > kLagNorm)) lag = 0.0f;
         }
 
-        for (int u = 0; u < TT / 16; ++u) {
-            if (16 * u >= valid) break;
-            // ---------------- scores for 16 tokens (two n8 tiles)
-            // two n8 tiles x two independent accumulator chains (codebook part;
-            // QJL part or low half of the split query) keep four MMAs in flight
-            float sc[2][4], sd[2][4];
-            uint32_t hk[2][16];
-            uint32_t sw[2];
+        // One step = NT n8 tiles of tokens (8 NT tokens): the score MMAs run as
+        // 2 NT independent accumulator chains of eight k-steps each (a chain's
+        // MMAs wait on one another), so wider steps keep more MMAs in flight.
+        auto step = [&](auto ntc, const int base) {
+            constexpr int NT = decltype(ntc)::value;
             // QJL signs as exact +-1 operands; the residual norm multiplies the
             // sign products in fp32 below
-            constexpr uint32_t neg2 = 0xBC00BC00u;  // (-1, -1): a set bit gives +1
+            [[maybe_unused]] constexpr uint32_t neg2 = 0xBC00BC00u;  // (-1, -1): a set bit gives +1
+            // ---------------- scores: S = Q' K^T (+ Q'' sigma^T), key operands
+            // decoded two k-steps at a time
+            float sc[NT][4], sd[NT][4];
+            uint32_t kw[NT][KB];
+            uint32_t sw[NT];
 #pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
+            for (int nt = 0; nt < NT; ++nt) {
                 sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.0f;
                 sd[nt][0] = sd[nt][1] = sd[nt][2] = sd[nt][3] = 0.0f;
-                const int tau = 16 * u + 8 * nt + g;
-                uint32_t kw[KB];
-                load_words<KB>(kidx + tau * (4 * KB) + j * KB, kw);
-                if constexpr (kQuadTab) quad2_chunk(kw, kt_lane, hk[nt]);
-                else mse_chunk<KB>(kw, ktab, hk[nt]);
+                const int tau = base + 8 * nt + g;
+                load_words<KB>(kidx + tau * (4 * KB) + j * KB, kw[nt]);
                 if constexpr (KPROD) sw[nt] = ksgn[tau * 4 + j];
+                else sw[nt] = 0u;
             }
 #pragma unroll
-            for (int ks = 0; ks < 8; ++ks) {
-                uint32_t qa[4], qj[4];
-                {
-                    const uint4 v = qsm[ks * 32 + lane];
-                    qa[0] = v.x; qa[1] = v.y; qa[2] = v.z; qa[3] = v.w;
-                    const uint4 w = qsm[(8 + ks) * 32 + lane];
-                    qj[0] = w.x; qj[1] = w.y; qj[2] = w.z; qj[3] = w.w;
-                }
+            for (int q2 = 0; q2 < 4; ++q2) {
+                uint32_t hk[NT][4];
 #pragma unroll
-                for (int nt = 0; nt < 2; ++nt) {
-                    mma16816(sc[nt], qa, hk[nt][2 * ks], hk[nt][2 * ks + 1]);
-                    if constexpr (KPROD)
-                        mma16816(sd[nt], qj, dec1(sw[nt], 15 - ks, neg2), dec1(sw[nt], 7 - ks, neg2));
-                    else
-                        mma16816(sd[nt], qj, hk[nt][2 * ks], hk[nt][2 * ks + 1]);
-                }
-            }
+                for (int nt = 0; nt < NT; ++nt) key_ks2<KB, kQuadTab>(kw[nt], ktab, kt_lane, q2, hk[nt]);
 #pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
-                if constexpr (KPROD) {
-                    // codebook part + residual norm x QJL part, per token column
-                    const float2 gm = *reinterpret_cast<const float2*>(krn + 16 * u + 8 * nt + 2 * j);
-                    sc[nt][0] = fmaf(gm.x, sd[nt][0], sc[nt][0]);
-                    sc[nt][1] = fmaf(gm.y, sd[nt][1], sc[nt][1]);
-                    sc[nt][2] = fmaf(gm.x, sd[nt][2], sc[nt][2]);
-                    sc[nt][3] = fmaf(gm.y, sd[nt][3], sc[nt][3]);
-                } else {
+                for (int e = 0; e < 2; ++e) {
+                    const int ks = 2 * q2 + e;
+                    uint32_t qa[4], qj[4];
+                    {
+                        const uint4 v = qsm[ks * 32 + lane];
+                        qa[0] = v.x; qa[1] = v.y; qa[2] = v.z; qa[3] = v.w;
+                        const uint4 w = qsm[(8 + ks) * 32 + lane];
+                        qj[0] = w.x; qj[1] = w.y; qj[2] = w.z; qj[3] = w.w;
+                    }
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) sc[nt][e] += sd[nt][e];
+                    for (int nt = 0; nt < NT; ++nt) {
+                        mma16816(sc[nt], qa, hk[nt][2 * e], hk[nt][2 * e + 1]);
+                        if constexpr (KPROD)
+                            mma16816(sd[nt], qj, dec1(sw[nt], 15 - ks, neg2), dec1(sw[nt], 7 - ks, neg2));
+                        else
+                            mma16816(sd[nt], qj, hk[nt][2 * e], hk[nt][2 * e + 1]);
+                    }
                 }
             }
-            // ---------------- values of the same 16 tokens: decoded while the score MMAs
-            // are in flight (independent of the scores)
+            // ---------------- values of the first 16 tokens: decoded while the
+            // score MMAs are in flight (independent of the scores)
             uint32_t hA[16], hB[16];
-            {
-                const int tA = 16 * u + g, tB = tA + 8;
+            auto decode_values = [&](int kg) {
+                const int tA = base + 16 * kg + g, tB = tA + 8;
                 uint32_t wA[VB], wB[VB];
                 load_words<VB>(vidx + tA * (4 * VB) + j * VB, wA);
                 load_words<VB>(vidx + tB * (4 * VB) + j * VB, wB);
@@ -643,12 +677,8 @@ __global__ void __launch_bounds__(kThreads, 1) split_mma_kernel(MmaArgs m) {
                     const float mA = okA ? __half2float(vmn[tA * ng + gi]) : 0.0f;
                     const float sB = okB ? __half2float(vsc[tB * ng + gi]) : 0.0f;
                     const float mB = okB ? __half2float(vmn[tB * ng + gi]) : 0.0f;
-                    const uint32_t mulA = pack_half2(sA * mulf, sA * mulf);
-                    const uint32_t addA = pack_half2(mA, mA);
-                    const uint32_t mulB = pack_half2(sB * mulf, sB * mulf);
-                    const uint32_t addB = pack_half2(mB, mB);
-                    GroupChunk<VB>::run(wA, mulA, addA, hA);
-                    GroupChunk<VB>::run(wB, mulB, addB, hB);
+                    GroupChunk<VB>::run(wA, pack_half2(sA * mulf, sA * mulf), pack_half2(mA, mA), hA);
+                    GroupChunk<VB>::run(wB, pack_half2(sB * mulf, sB * mulf), pack_half2(mB, mB), hB);
                 } else if constexpr (kPairTab) {
                     pair3_chunk(wA, vt_lane, hA);
                     pair3_chunk(wB, vt_lane, hB);
@@ -656,41 +686,64 @@ __global__ void __launch_bounds__(kThreads, 1) split_mma_kernel(MmaArgs m) {
                     mse_chunk<VB>(wA, vtab, hA);
                     mse_chunk<VB>(wB, vtab, hB);
                 }
+            };
+            decode_values(0);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                if constexpr (KPROD) {
+                    // codebook part + residual norm x QJL part, per token column
+                    const float2 gm = *reinterpret_cast<const float2*>(krn + base + 8 * nt + 2 * j);
+                    sc[nt][0] = fmaf(gm.x, sd[nt][0], sc[nt][0]);
+                    sc[nt][1] = fmaf(gm.y, sd[nt][1], sc[nt][1]);
+                    sc[nt][2] = fmaf(gm.x, sd[nt][2], sc[nt][2]);
+                    sc[nt][3] = fmaf(gm.y, sd[nt][3], sc[nt][3]);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) sc[nt][e] += sd[nt][e];
+                }
             }
             // ---------------- scale, mask, online softmax (log2 domain)
-            float x[2][4];
-            float2 nv[2] = {};
+            float2 nv[NT];
 #pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
-                const float2 kn = *reinterpret_cast<const float2*>(knorm + 16 * u + 8 * nt + 2 * j);
-                if constexpr (!VGROUP) nv[nt] = *reinterpret_cast<const float2*>(vnorm + 16 * u + 8 * nt + 2 * j);
-                x[nt][0] = sc[nt][0] * kn.x;
-                x[nt][1] = sc[nt][1] * kn.y;
-                x[nt][2] = sc[nt][2] * kn.x;
-                x[nt][3] = sc[nt][3] * kn.y;
+            for (int nt = 0; nt < NT; ++nt) {
+                const float2 kn = *reinterpret_cast<const float2*>(knorm + base + 8 * nt + 2 * j);
+                if constexpr (!VGROUP) nv[nt] = *reinterpret_cast<const float2*>(vnorm + base + 8 * nt + 2 * j);
+                else nv[nt] = make_float2(0.0f, 0.0f);
+                sc[nt][0] *= kn.x;
+                sc[nt][1] *= kn.y;
+                sc[nt][2] *= kn.x;
+                sc[nt][3] *= kn.y;
             }
-            // masks only where the 16 tokens reach past the tile's end or a row's causal limit
-            // (past the end, the stage holds stale bytes: their value norms become 0)
-            if (16 * u + 16 > valid || t0 + 16 * u + 15 > lim_all) {
+            // masks only where the step reaches past the tile's end or a row's
+            // causal limit (past the end, the stage holds stale bytes: their
+            // value norms become 0)
+            if (base + 8 * NT > valid || t0 + base + 8 * NT - 1 > lim_all) {
 #pragma unroll
-                for (int nt = 0; nt < 2; ++nt) {
-                    const int tl = 16 * u + 8 * nt + 2 * j;
+                for (int nt = 0; nt < NT; ++nt) {
+                    const int tl = base + 8 * nt + 2 * j;
                     const int pos = t0 + tl;
                     const bool v0 = tl < valid, v1 = tl + 1 < valid;
-                    if (!(v0 && pos <= lim0)) x[nt][0] = -INFINITY;
-                    if (!(v1 && pos + 1 <= lim0)) x[nt][1] = -INFINITY;
-                    if (!(v0 && pos <= lim1)) x[nt][2] = -INFINITY;
-                    if (!(v1 && pos + 1 <= lim1)) x[nt][3] = -INFINITY;
+                    if (!(v0 && pos <= lim0)) sc[nt][0] = -INFINITY;
+                    if (!(v1 && pos + 1 <= lim0)) sc[nt][1] = -INFINITY;
+                    if (!(v0 && pos <= lim1)) sc[nt][2] = -INFINITY;
+                    if (!(v1 && pos + 1 <= lim1)) sc[nt][3] = -INFINITY;
                     if (!v0) nv[nt].x = 0.0f;
                     if (!v1) nv[nt].y = 0.0f;
                 }
             }
             const float th0 = mrow0 + lag, th1 = mrow1 + lag;
-            if (__any_sync(0xffffffffu, x[0][0] > th0 || x[0][1] > th0 || x[1][0] > th0 || x[1][1] > th0 ||
-                                            x[0][2] > th1 || x[0][3] > th1 || x[1][2] > th1 || x[1][3] > th1)) {
+            bool over = false;
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+                over |= sc[nt][0] > th0 || sc[nt][1] > th0 || sc[nt][2] > th1 || sc[nt][3] > th1;
+            if (__any_sync(0xffffffffu, over)) {
                 // a score passed m + lag: move m to the exact row maxima
-                float mx0 = fmaxf(fmaxf(x[0][0], x[0][1]), fmaxf(x[1][0], x[1][1]));
-                float mx1 = fmaxf(fmaxf(x[0][2], x[0][3]), fmaxf(x[1][2], x[1][3]));
+                float mx0 = fmaxf(sc[0][0], sc[0][1]), mx1 = fmaxf(sc[0][2], sc[0][3]);
+#pragma unroll
+                for (int nt = 1; nt < NT; ++nt) {
+                    mx0 = fmaxf(mx0, fmaxf(sc[nt][0], sc[nt][1]));
+                    mx1 = fmaxf(mx1, fmaxf(sc[nt][2], sc[nt][3]));
+                }
                 mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
                 mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
                 mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
@@ -708,51 +761,63 @@ __global__ void __launch_bounds__(kThreads, 1) split_mma_kernel(MmaArgs m) {
                 mrow0 = mn0;
                 mrow1 = mn1;
             }
-            float pr[2][4];
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
-                pr[nt][0] = ex2(x[nt][0] - mrow0);
-                pr[nt][1] = ex2(x[nt][1] - mrow0);
-                pr[nt][2] = ex2(x[nt][2] - mrow1);
-                pr[nt][3] = ex2(x[nt][3] - mrow1);
-            }
             // P' = fp16(p * value norm); the row sums add the weights actually
             // multiplied (P' / norm), so the rounding of P' cancels in o = sum/L.
             // A zero norm gives P' = 0 and a huge finite 1/norm (nothing added);
             // its p enters the row sums in the rare branch below.
-            uint32_t pa[4];
+            uint32_t pa[NT][2];
+            [[maybe_unused]] bool zero = false;
 #pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
-                float w0 = pr[nt][0], w1 = pr[nt][1], w2 = pr[nt][2], w3 = pr[nt][3];
+            for (int nt = 0; nt < NT; ++nt) {
+                float w0 = ex2(sc[nt][0] - mrow0), w1 = ex2(sc[nt][1] - mrow0);
+                float w2 = ex2(sc[nt][2] - mrow1), w3 = ex2(sc[nt][3] - mrow1);
                 float r0 = 1.0f, r1 = 1.0f;
                 if constexpr (!VGROUP) {
                     const float nx = nv[nt].x, ny = nv[nt].y;
+                    zero |= !(fminf(nx, ny) > 0.0f);
                     r0 = rcp_approx(fmaxf(nx, 1e-30f));
                     r1 = rcp_approx(fmaxf(ny, 1e-30f));
+                    sc[nt][0] = w0;  // keep p for the zero-norm branch
+                    sc[nt][1] = w1;
+                    sc[nt][2] = w2;
+                    sc[nt][3] = w3;
                     w0 *= nx;
                     w1 *= ny;
                     w2 *= nx;
                     w3 *= ny;
                 }
-                pa[2 * nt] = pack_half2(w0, w1);
-                pa[2 * nt + 1] = pack_half2(w2, w3);
-                const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&pa[2 * nt]));
-                const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&pa[2 * nt + 1]));
+                pa[nt][0] = pack_half2(w0, w1);
+                pa[nt][1] = pack_half2(w2, w3);
+                const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&pa[nt][0]));
+                const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&pa[nt][1]));
                 lrow0 += f0.x * r0 + f0.y * r1;
                 lrow1 += f1.x * r0 + f1.y * r1;
             }
             if constexpr (!VGROUP) {
-                const bool zero = !(fminf(fminf(nv[0].x, nv[0].y), fminf(nv[1].x, nv[1].y)) > 0.0f);
                 if (__any_sync(0xffffffffu, zero)) {
 #pragma unroll
-                    for (int nt = 0; nt < 2; ++nt) {
-                        if (!(nv[nt].x > 0.0f)) { lrow0 += pr[nt][0]; lrow1 += pr[nt][2]; }
-                        if (!(nv[nt].y > 0.0f)) { lrow0 += pr[nt][1]; lrow1 += pr[nt][3]; }
+                    for (int nt = 0; nt < NT; ++nt) {
+                        if (!(nv[nt].x > 0.0f)) { lrow0 += sc[nt][0]; lrow1 += sc[nt][2]; }
+                        if (!(nv[nt].y > 0.0f)) { lrow0 += sc[nt][1]; lrow1 += sc[nt][3]; }
                     }
                 }
             }
+            // ---------------- O += P' V, 16 tokens per k-group
 #pragma unroll
-            for (int p = 0; p < 16; ++p) mma16816(o[p], pa, movmatrix_t(hA[p]), movmatrix_t(hB[p]));
+            for (int kg = 0; kg < NT / 2; ++kg) {
+                if (kg > 0) decode_values(kg);
+                const uint32_t pk[4] = {pa[2 * kg][0], pa[2 * kg][1], pa[2 * kg + 1][0], pa[2 * kg + 1][1]};
+#pragma unroll
+                for (int p = 0; p < 16; ++p) mma16816(o[p], pk, movmatrix_t(hA[p]), movmatrix_t(hB[p]));
+            }
+        };
+        if (TT >= 32) {
+            for (int u = 0; u < TT / 32; ++u) {
+                if (32 * u >= valid) break;
+                step(std::integral_constant<int, 4>{}, 32 * u);
+            }
+        } else if (valid > 0) {
+            step(std::integral_constant<int, 2>{}, 0);
         }
     }
     tc::grid_release_dependents();  // the next kernel may start; it waits for this one before the workspace
