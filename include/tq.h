@@ -511,6 +511,62 @@ tq_status tq_decode_merge(const tq_codec *value_codec, int num_parts, const floa
                           const float *parts_acc, int64_t rows, float *out, tq_stream_t stream);
 
 /* ------------------------------------------------------------------ */
+/* Split (low/high) states                                              */
+/* ------------------------------------------------------------------ */
+
+/*
+ * Split states ("omlx/turboquant_kv.py": TurboQuantSplitState(low, high),
+ * carried through the batch operations by _filter_state and
+ * _concat_state_batch): each key and value vector of head_dim D is stored as
+ * two TurboQuant states, the low coordinates [0, DL) under one codec pair and
+ * the high coordinates [DL, D) under another, each with its own norm,
+ * rotation, Lloyd-Max codebook and bit width (for example more bits on the
+ * high channels, the outlier channels of a mixed width). The two halves live
+ * in two caches of the same layout shape (layers, blocks, block size, KV
+ * heads) addressed by one block table and one set of lengths; each cache is
+ * an ordinary cache of its half's head_dim (batch operations apply to both).
+ */
+typedef struct {
+    const tq_codec *key_low, *value_low;    /* head_dim DL                         */
+    const tq_codec *key_high, *value_high;  /* head_dim DH                         */
+    const tq_cache_desc *low, *high;        /* caches of the two halves            */
+} tq_split_state;
+
+/*
+ * Append n_new tokens per sequence to both halves: tq_encode_append of the
+ * low halves k_low, v_low [batch][num_kv_heads][n_new][DL] into `low` and of
+ * k_high, v_high [batch][num_kv_heads][n_new][DH] into `high` (device,
+ * contiguous, one dtype). Errors: those of tq_encode_append;
+ * TQ_ERR_CONFIG_MISMATCH if the two caches differ in layers, blocks, block
+ * size or KV heads.
+ */
+tq_status tq_encode_append_split(const tq_split_state *state, int layer, const void *k_low, const void *v_low,
+                                 const void *k_high, const void *v_high, tq_dtype dtype, int batch, int n_new,
+                                 const int32_t *seq_lens, const int32_t *block_table, int max_blocks,
+                                 tq_stream_t stream);
+
+/* Workspace (device bytes) of tq_decode_attention_split for these sizes. */
+tq_status tq_decode_workspace_bytes_split(const tq_split_state *state, int batch, int num_q_heads, int q_len,
+                                          int max_seq_len, size_t *bytes);
+
+/*
+ * Decode attention over split states: score_t = scale * (<q_low, k_hat_low_t>
+ * + <q_high, k_hat_high_t>), each half scored in its own rotated domain as
+ * tq_decode_attention scores a whole vector, softmax over the visible keys
+ * (the causal rule of tq_decode_attention), out = [o_low | o_high] with each
+ * half's value sum rotated back by its own value rotation (group halves are
+ * not rotated).
+ *   q    device [batch][num_q_heads][q_len][D], D = DL + DH; scale 0 means
+ *        1/sqrt(D). out device [batch][num_q_heads][q_len][D] fp32.
+ * DL, DH in {64, 128}; (num_q_heads/num_kv_heads) * q_len <= 64. Other
+ * arguments and errors as tq_decode_attention.
+ */
+tq_status tq_decode_attention_split(const tq_split_state *state, int layer, const void *q, tq_dtype q_dtype,
+                                    int batch, int num_q_heads, int q_len, const int32_t *seq_lens,
+                                    const int32_t *block_table, int max_blocks, int max_seq_len, float scale,
+                                    float *out, void *workspace, size_t workspace_bytes, tq_stream_t stream);
+
+/* ------------------------------------------------------------------ */
 /* Prefill attention                                                    */
 /* ------------------------------------------------------------------ */
 

@@ -299,6 +299,18 @@ def merge_partials(vc: Codec, m: np.ndarray, l: np.ndarray, acc: np.ndarray) -> 
     return out
 
 
+def decode_split(q: np.ndarray, low: tuple, high: tuple, scale: float, Lq: int) -> np.ndarray:
+    """Decode over split states by the plain definition: each half's records
+    dequantised by its own codec, the halves concatenated into whole vectors
+    [k_low | k_high], [v_low | v_high], then plain softmax attention (fp64).
+    low / high: (key codec, key records, value codec, value records); q [G, Lq, D]."""
+    kcl, krl, vcl, vrl = low
+    kch, krh, vch, vrh = high
+    K = np.concatenate([kcl.dequant(krl), kch.dequant(krh)], axis=1)
+    V = np.concatenate([vcl.dequant(vrl), vch.dequant(vrh)], axis=1)
+    return attention_f64(q, K, V, scale, Lq)
+
+
 def subblock_layout(kc: Codec, vc: Codec, BT: int):
     off = np.empty(7, np.int64)
     sub = lib().tqo_subblock_layout(kc.D, kc.mode, kc.bits, vc.mode, vc.bits, vc.group, BT,

@@ -15,7 +15,7 @@ import numpy as np
 from . import _lib
 from ._lib import (TQ_BF16, TQ_DEVERR_BLOCK, TQ_DEVERR_CAPACITY, TQ_DEVERR_SEQLEN, TQ_ENCODE_AUTO,
                    TQ_ENCODE_EXACT, TQ_F16, TQ_F32, TQ_MODE_GROUP, TQ_MODE_MSE, TQ_MODE_PROD, TQ_OK, TQError, check,
-                   lib, library_path, status_string, tq_batch, tq_cache_desc, tq_codec_info_t)
+                   lib, library_path, status_string, tq_batch, tq_cache_desc, tq_codec_info_t, tq_split_state)
 
 __all__ = [
     "tq_codec_create", "tq_codec_create_group", "tq_codec_destroy", "tq_codec_info",
@@ -25,6 +25,7 @@ __all__ = [
     "tq_decode_step", "tq_decode_plan",
     "tq_prefill_workspace_bytes", "tq_prefill_attention", "tq_cache_copy_blocks",
     "tq_decode_partials", "tq_decode_merge",
+    "tq_encode_append_split", "tq_decode_workspace_bytes_split", "tq_decode_attention_split", "SplitCache",
     "tq_batch_filter", "tq_batch_extend", "tq_batch_merge", "tq_batch_extract", "Batch",
     "tq_device_error",
     "tq_launch_count", "tq_abi_version", "Codec", "CompressedKVCache", "TQError",
@@ -262,6 +263,65 @@ def tq_decode_merge(value_codec: int, parts_ml, parts_acc, out, stream=None) -> 
     rows = parts_ml[0].numel() // 2
     check(lib().tq_decode_merge(value_codec, P, _ptr(parts_ml), _ptr(parts_acc), rows, _ptr(out),
                                 _stream(stream)), "tq_decode_merge")
+
+
+class SplitCache:
+    """Split (low/high) states: the low coordinates [0, DL) of every key and value
+    in one cache, the high coordinates [DL, D) in another, each under its own
+    codec pair; both caches share one block layout."""
+
+    def __init__(self, key_low: "Codec", value_low: "Codec", key_high: "Codec", value_high: "Codec",
+                 num_layers: int, num_blocks: int, block_tokens: int, num_kv_heads: int, device="cuda",
+                 exact_encode: bool = False):
+        self.low = CompressedKVCache(key_low, value_low, num_layers, num_blocks, block_tokens, num_kv_heads,
+                                     device, exact_encode)
+        self.high = CompressedKVCache(key_high, value_high, num_layers, num_blocks, block_tokens, num_kv_heads,
+                                      device, exact_encode)
+        self.low_dim = key_low.info["head_dim"]
+        self.head_dim = self.low_dim + key_high.info["head_dim"]
+
+    def state(self) -> tq_split_state:
+        return tq_split_state(self.low.key.handle, self.low.value.handle, self.high.key.handle,
+                              self.high.value.handle, ctypes.pointer(self.low.desc), ctypes.pointer(self.high.desc))
+
+    def append(self, layer, k_low, v_low, k_high, v_high, seq_lens, block_table=None, max_blocks=0, stream=None):
+        tq_encode_append_split(self, layer, k_low, v_low, k_high, v_high, seq_lens, block_table, max_blocks, stream)
+
+    def workspace_bytes(self, batch, num_q_heads, q_len, max_seq_len):
+        return tq_decode_workspace_bytes_split(self, batch, num_q_heads, q_len, max_seq_len)
+
+    def decode(self, layer, q, seq_lens, block_table, max_blocks, max_seq_len, out, workspace, scale=0.0,
+               stream=None):
+        tq_decode_attention_split(self, layer, q, seq_lens, block_table, max_blocks, max_seq_len, out, workspace,
+                                  scale, stream)
+
+
+def tq_encode_append_split(sc: SplitCache, layer: int, k_low, v_low, k_high, v_high, seq_lens, block_table=None,
+                           max_blocks: int = 0, stream=None) -> None:
+    batch, _, n_new, _ = k_low.shape
+    st = sc.state()
+    check(lib().tq_encode_append_split(ctypes.byref(st), layer, _ptr(k_low), _ptr(v_low), _ptr(k_high),
+                                       _ptr(v_high), _dtype_code(k_low), batch, n_new, _ptr(seq_lens),
+                                       _ptr(block_table), max_blocks, _stream(stream)), "tq_encode_append_split")
+
+
+def tq_decode_workspace_bytes_split(sc: SplitCache, batch: int, num_q_heads: int, q_len: int, max_seq_len: int) -> int:
+    out = ctypes.c_size_t()
+    st = sc.state()
+    check(lib().tq_decode_workspace_bytes_split(ctypes.byref(st), batch, num_q_heads, q_len, max_seq_len,
+                                                ctypes.byref(out)), "tq_decode_workspace_bytes_split")
+    return out.value
+
+
+def tq_decode_attention_split(sc: SplitCache, layer: int, q, seq_lens, block_table, max_blocks: int,
+                              max_seq_len: int, out, workspace, scale: float = 0.0, stream=None) -> None:
+    batch, hq, lq, _ = q.shape
+    st = sc.state()
+    ws_bytes = workspace.numel() * workspace.element_size()
+    check(lib().tq_decode_attention_split(ctypes.byref(st), layer, _ptr(q), _dtype_code(q), batch, hq, lq,
+                                          _ptr(seq_lens), _ptr(block_table), max_blocks, max_seq_len, scale,
+                                          _ptr(out), _ptr(workspace), ws_bytes, _stream(stream)),
+          "tq_decode_attention_split")
 
 
 class Batch:

@@ -77,6 +77,12 @@ class tq_batch(ctypes.Structure):
                 ("max_blocks", ctypes.c_int)]
 
 
+class tq_split_state(ctypes.Structure):
+    _fields_ = [("key_low", ctypes.c_void_p), ("value_low", ctypes.c_void_p), ("key_high", ctypes.c_void_p),
+                ("value_high", ctypes.c_void_p), ("low", ctypes.POINTER(tq_cache_desc)),
+                ("high", ctypes.POINTER(tq_cache_desc))]
+
+
 _P = ctypes.c_void_p
 _I = ctypes.c_int
 _I64 = ctypes.c_int64
@@ -119,6 +125,12 @@ SIGNATURES = {
     "tq_decode_partials": (_ST, [_P, _P, ctypes.POINTER(tq_cache_desc), _I, _P, _I, _I, _I, _I, _P, _P, _P, _I,
                                  _I, _F, _P, _P, _P, _SZ, _P]),
     "tq_decode_merge": (_ST, [_P, _I, _P, _P, _I64, _P, _P]),
+    "tq_encode_append_split": (_ST, [ctypes.POINTER(tq_split_state), _I, _P, _P, _P, _P, _I, _I, _I, _P, _P, _I,
+                                     _P]),
+    "tq_decode_workspace_bytes_split": (_ST, [ctypes.POINTER(tq_split_state), _I, _I, _I, _I,
+                                              ctypes.POINTER(_SZ)]),
+    "tq_decode_attention_split": (_ST, [ctypes.POINTER(tq_split_state), _I, _P, _I, _I, _I, _I, _P, _P, _I, _I, _F,
+                                        _P, _P, _SZ, _P]),
     "tq_batch_filter": (_ST, [ctypes.POINTER(tq_batch), _P, _I, ctypes.POINTER(tq_batch), _P, _P, _P]),
     "tq_batch_extend": (_ST, [ctypes.POINTER(tq_batch), ctypes.POINTER(tq_batch), _P, _I, _P, _P]),
     "tq_batch_merge": (_ST, [ctypes.POINTER(tq_batch), ctypes.POINTER(tq_batch), _I, _P, _I, _P, _P]),

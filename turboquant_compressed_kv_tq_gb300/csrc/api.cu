@@ -756,6 +756,120 @@ tq_status tq_decode_merge(const tq_codec* value_codec, int num_parts, const floa
                : TQ_ERR_CUDA;
 }
 
+namespace {
+
+// The two halves of a split state: codecs matching their caches, and caches
+// of one layout shape (addressed by one block table).
+tq_status check_split(const tq_split_state* st) {
+    if (!st || !st->low || !st->high) return TQ_ERR_INVALID_ARG;
+    tq_status e = check_codecs_vs_cache(st->key_low, st->value_low, st->low);
+    if (e == TQ_OK) e = check_codecs_vs_cache(st->key_high, st->value_high, st->high);
+    if (e != TQ_OK) return e;
+    const tq_cache_desc *a = st->low, *b = st->high;
+    if (a->num_layers != b->num_layers || a->num_blocks != b->num_blocks || a->block_tokens != b->block_tokens ||
+        a->num_kv_heads != b->num_kv_heads)
+        return TQ_ERR_CONFIG_MISMATCH;
+    const int dl = a->head_dim, dh = b->head_dim;
+    if ((dl != 64 && dl != 128) || (dh != 64 && dh != 128)) return TQ_ERR_UNSUPPORTED;
+    return TQ_OK;
+}
+
+}  // namespace
+
+tq_status tq_encode_append_split(const tq_split_state* st, int layer, const void* k_low, const void* v_low,
+                                 const void* k_high, const void* v_high, tq_dtype dtype, int batch, int n_new,
+                                 const int32_t* seq_lens, const int32_t* block_table, int max_blocks,
+                                 tq_stream_t stream) {
+    tq_status e = check_split(st);
+    if (e != TQ_OK) return e;
+    // both halves are checked before either is launched
+    EncodeAppendArgs lo{}, hi{};
+    bool run_lo = false, run_hi = false;
+    e = append_args(st->key_low, st->value_low, st->low, layer, k_low, v_low, dtype, batch, n_new, seq_lens,
+                    block_table, max_blocks, &lo, &run_lo);
+    if (e == TQ_OK)
+        e = append_args(st->key_high, st->value_high, st->high, layer, k_high, v_high, dtype, batch, n_new,
+                        seq_lens, block_table, max_blocks, &hi, &run_hi);
+    if (e != TQ_OK) return e;
+    const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (run_lo && launch_encode_append(lo, s) != cudaSuccess) return TQ_ERR_CUDA;
+    if (run_hi && launch_encode_append(hi, s) != cudaSuccess) return TQ_ERR_CUDA;
+    return TQ_OK;
+}
+
+namespace {
+
+tq_status split_args(const tq_split_state* st, int batch, int num_q_heads, int q_len, int max_seq_len,
+                     SplitStateArgs* a) {
+    tq_status e = check_split(st);
+    if (e != TQ_OK) return e;
+    const tq_cache_desc* c = st->low;
+    if (batch < 0 || q_len <= 0 || max_seq_len < q_len || num_q_heads <= 0 || num_q_heads % c->num_kv_heads != 0)
+        return TQ_ERR_INVALID_ARG;
+    const int G = num_q_heads / c->num_kv_heads;
+    if (G * q_len > 64) return TQ_ERR_UNSUPPORTED;
+    unsigned* err = nullptr;
+    int sms = 0;
+    if (device_state(&err, &sms) != TQ_OK) return TQ_ERR_CUDA;
+    *a = SplitStateArgs{};
+    a->klo = dev_view(st->key_low);
+    a->vlo = dev_view(st->value_low);
+    a->khi = dev_view(st->key_high);
+    a->vhi = dev_view(st->value_high);
+    a->batch = batch;
+    a->Hq = num_q_heads;
+    a->Lq = q_len;
+    a->G = G;
+    a->Hkv = c->num_kv_heads;
+    a->err = err;
+    split_state_plan(*a, max_seq_len, sms);
+    return TQ_OK;
+}
+
+}  // namespace
+
+tq_status tq_decode_workspace_bytes_split(const tq_split_state* st, int batch, int num_q_heads, int q_len,
+                                          int max_seq_len, size_t* bytes) {
+    if (!bytes) return TQ_ERR_INVALID_ARG;
+    SplitStateArgs a{};
+    const tq_status e = split_args(st, batch, num_q_heads, q_len, max_seq_len, &a);
+    if (e != TQ_OK) return e;
+    *bytes = split_state_workspace(a, st->low->head_dim + st->high->head_dim);
+    return TQ_OK;
+}
+
+tq_status tq_decode_attention_split(const tq_split_state* st, int layer, const void* q, tq_dtype q_dtype,
+                                    int batch, int num_q_heads, int q_len, const int32_t* seq_lens,
+                                    const int32_t* block_table, int max_blocks, int max_seq_len, float scale,
+                                    float* out, void* workspace, size_t workspace_bytes, tq_stream_t stream) {
+    SplitStateArgs a{};
+    tq_status e = split_args(st, batch, num_q_heads, q_len, max_seq_len, &a);
+    if (e != TQ_OK) return e;
+    const tq_cache_desc* c = st->low;
+    if (layer < 0 || layer >= c->num_layers || max_blocks <= 0) return TQ_ERR_INVALID_ARG;
+    if (q_dtype != TQ_F32 && q_dtype != TQ_BF16 && q_dtype != TQ_F16) return TQ_ERR_INVALID_ARG;
+    if (static_cast<int64_t>(max_seq_len) > static_cast<int64_t>(max_blocks) * c->block_tokens)
+        return TQ_ERR_CAPACITY;
+    if (!block_table && static_cast<int64_t>(batch) * max_blocks > c->num_blocks) return TQ_ERR_CAPACITY;
+    if (batch == 0) return TQ_OK;
+    if (batch > 65535) return TQ_ERR_INVALID_ARG;
+    if (!q || !out || !seq_lens || !workspace) return TQ_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return TQ_ERR_INVALID_ARG;
+    const int D = c->head_dim + st->high->head_dim;
+    if (workspace_bytes < split_state_workspace(a, D)) return TQ_ERR_CAPACITY;
+    a.plo = pool_view(st->low, layer);
+    a.phi = pool_view(st->high, layer);
+    a.q = q;
+    a.q_dtype = q_dtype;
+    a.seq_lens = seq_lens;
+    a.table = block_table;
+    a.max_blocks = max_blocks;
+    a.scale = scale == 0.0f ? 1.0f / std::sqrt(static_cast<float>(D)) : scale;
+    a.out = out;
+    split_state_bind_workspace(a, workspace, D);
+    return launch_split_state(a, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
+}
+
 tq_status tq_decode_step(const tq_codec* kc, const tq_codec* vc, const tq_cache_desc* cache, int layer,
                          const void* k_new, const void* v_new, tq_dtype kv_dtype, int n_new, const void* q,
                          tq_dtype q_dtype, int batch, int num_q_heads, int q_len, const int32_t* seq_lens,

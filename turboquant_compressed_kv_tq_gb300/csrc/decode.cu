@@ -26,6 +26,7 @@ namespace tq {
 namespace {
 
 constexpr int kTile = 32;   // tokens per tile
+constexpr int kSimtMinChunk = 256;   // fewest tokens per split of the SIMT decode
 constexpr int kRows = 16;   // query rows per CTA (one row group)
 constexpr int kThreads = 128;
 
@@ -44,11 +45,13 @@ __device__ __forceinline__ unsigned extract_code(const uint32_t* words, int i, i
     return v & ((1u << b) - 1u);
 }
 
-// q' = R q and q'' = S q' for the 16 rows of one (sequence, kv head, row group).
+// q' = R q and q'' = S q' for the 16 rows of one (sequence, kv head, row
+// group): one pass over each matrix for all 16 rows (a matrix element is
+// loaded once and used for every row).
 template <int D>
 __global__ void qprep_kernel(DecodeArgs a) {
-    __shared__ float qs[D];
-    __shared__ float q1[D];
+    __shared__ float qs[kRows][D];
+    __shared__ float q1[kRows][D];
     const int Hkv = a.pool.Hkv;
     const int bh = blockIdx.x;
     const int b = bh / Hkv, h = bh % Hkv;
@@ -57,29 +60,37 @@ __global__ void qprep_kernel(DecodeArgs a) {
     const int i = threadIdx.x;
     for (int rr = 0; rr < kRows; ++rr) {
         const int r = rg * kRows + rr;
+        float v = 0.0f;
+        if (r < a.plan.rows) {
+            const int g = r / a.Lq, l = r % a.Lq;
+            v = load_q(a.q, a.q_dtype, ((static_cast<int64_t>(b) * a.Hq + h * a.G + g) * a.Lq + l) * D + i);
+        }
+        qs[rr][i] = v;
+    }
+    __syncthreads();
+    float t[kRows] = {};
+    for (int k = 0; k < D; ++k) {
+        const float rk = __ldg(a.kc.Rt + k * D + i);
+#pragma unroll
+        for (int rr = 0; rr < kRows; ++rr) t[rr] = fmaf(rk, qs[rr][k], t[rr]);
+    }
+    float z[kRows] = {};
+    if (a.kc.mode == TQ_MODE_PROD) {
+#pragma unroll
+        for (int rr = 0; rr < kRows; ++rr) q1[rr][i] = t[rr];
+        __syncthreads();
+        for (int k = 0; k < D; ++k) {
+            const float sk = __ldg(a.kc.St + k * D + i);
+#pragma unroll
+            for (int rr = 0; rr < kRows; ++rr) z[rr] = fmaf(sk, q1[rr][k], z[rr]);
+        }
+    }
+#pragma unroll
+    for (int rr = 0; rr < kRows; ++rr) {
+        const bool live = rg * kRows + rr < a.plan.rows;
         const int64_t o = ((static_cast<int64_t>(bh) * RG + rg) * kRows + rr) * D + i;
-        if (r >= a.plan.rows) {
-            a.qrot[o] = 0.0f;
-            a.qjl[o] = 0.0f;
-            continue;
-        }
-        const int g = r / a.Lq, l = r % a.Lq;
-        const int hq = h * a.G + g;
-        qs[i] = load_q(a.q, a.q_dtype, ((static_cast<int64_t>(b) * a.Hq + hq) * a.Lq + l) * D + i);
-        __syncthreads();
-        float t = 0.0f;
-        for (int k = 0; k < D; ++k) t = fmaf(__ldg(a.kc.Rt + k * D + i), qs[k], t);
-        q1[i] = t;
-        a.qrot[o] = t;
-        __syncthreads();
-        if (a.kc.mode == TQ_MODE_PROD) {
-            float z = 0.0f;
-            for (int k = 0; k < D; ++k) z = fmaf(__ldg(a.kc.St + k * D + i), q1[k], z);
-            a.qjl[o] = z;
-        } else {
-            a.qjl[o] = 0.0f;
-        }
-        __syncthreads();
+        a.qrot[o] = live ? t[rr] : 0.0f;
+        a.qjl[o] = live ? z[rr] : 0.0f;
     }
 }
 
@@ -89,7 +100,7 @@ struct SplitSmem {
     float qj[kRows][D];
     float kh[kTile][D + 1];
     float vh[kTile][D + 1];
-    uint32_t sg[kTile][D / 32];
+    uint32_t sg[kTile][D / 32 + 1];   // padded: the lanes of a warp read different banks
     float kn[kTile], kr[kTile], vn[kTile];
     float sc[kRows][kTile + 1];
     float m[kRows], l[kRows], alpha[kRows];
@@ -193,9 +204,13 @@ __global__ void __launch_bounds__(kThreads) split_kernel(DecodeArgs a) {
                         for (int i = 0; i < D; ++i) dot = fmaf(sm.qr[rr][i], sm.kh[t][i], dot);
                         if (a.kc.mode == TQ_MODE_PROD) {
                             float sd = 0.0f;
-                            for (int i = 0; i < D; ++i) {
-                                const float qv = sm.qj[rr][i];
-                                sd += ((sm.sg[t][i >> 5] >> (i & 31)) & 1u) ? qv : -qv;
+                            for (int w = 0; w < D / 32; ++w) {
+                                const uint32_t word = sm.sg[t][w];
+#pragma unroll 8
+                                for (int k = 0; k < 32; ++k) {
+                                    const float qv = sm.qj[rr][32 * w + k];
+                                    sd += ((word >> k) & 1u) ? qv : -qv;
+                                }
                             }
                             dot = fmaf(kappa * sm.kr[t], sd, dot);
                         }
@@ -233,10 +248,12 @@ __global__ void __launch_bounds__(kThreads) split_kernel(DecodeArgs a) {
             const int d = tid + j * kThreads;
             if (d < D) {
 #pragma unroll
-                for (int r = 0; r < kRows; ++r) {
-                    float v = acc[r][j] * sm.alpha[r];
-                    for (int t = 0; t < nt; ++t) v = fmaf(sm.sc[r][t], sm.vh[t][d], v);
-                    acc[r][j] = v;
+                for (int r = 0; r < kRows; ++r) acc[r][j] *= sm.alpha[r];
+                // one value load per token, used for all 16 rows
+                for (int t = 0; t < nt; ++t) {
+                    const float vv = sm.vh[t][d];
+#pragma unroll
+                    for (int r = 0; r < kRows; ++r) acc[r][j] = fmaf(sm.sc[r][t], vv, acc[r][j]);
                 }
             }
         }
@@ -257,10 +274,11 @@ __global__ void __launch_bounds__(kThreads) split_kernel(DecodeArgs a) {
     }
 }
 
-// Merge the splits of one (sequence, kv head, row group) and rotate back.
+// Merge the splits of one (sequence, kv head, row group) and rotate back:
+// first every row's merged accumulator, then one pass over R_v for all rows.
 template <int D>
 __global__ void merge_kernel(DecodeArgs a) {
-    __shared__ float orot[D];
+    __shared__ float orot[kRows][D];
     const int Hkv = a.pool.Hkv;
     const int bh = blockIdx.x;
     const int b = bh / Hkv, h = bh % Hkv;
@@ -268,10 +286,8 @@ __global__ void merge_kernel(DecodeArgs a) {
     const int RG = a.plan.row_groups;
     const int S = a.plan.splits;
     const int i = threadIdx.x;
+    const int64_t base = (static_cast<int64_t>(bh) * RG + rg) * S;
     for (int rr = 0; rr < kRows; ++rr) {
-        const int r = rg * kRows + rr;
-        if (r >= a.plan.rows) break;
-        const int64_t base = (static_cast<int64_t>(bh) * RG + rg) * S;
         float M = -INFINITY;
         for (int s = 0; s < S; ++s) M = fmaxf(M, a.ml[((base + s) * kRows + rr) * 2]);
         float L = 0.0f, o = 0.0f;
@@ -284,26 +300,42 @@ __global__ void merge_kernel(DecodeArgs a) {
                 o = fmaf(w, a.part[((base + s) * kRows + rr) * D + i], o);
             }
         }
-        const int g = r / a.Lq, l = r % a.Lq;
-        const int64_t orow = (static_cast<int64_t>(b) * a.Hq + h * a.G + g) * a.Lq + l;
+        const int r = rg * kRows + rr;
         if (a.part_acc) {
             // a shard's state: max (natural-log units), sum, rotated-domain accumulator
-            if (i == 0) {
-                a.part_ml[2 * orow] = M;
-                a.part_ml[2 * orow + 1] = L;
+            if (r < a.plan.rows) {
+                const int g = r / a.Lq, l = r % a.Lq;
+                const int64_t orow = (static_cast<int64_t>(b) * a.Hq + h * a.G + g) * a.Lq + l;
+                if (i == 0) {
+                    a.part_ml[2 * orow] = M;
+                    a.part_ml[2 * orow + 1] = L;
+                }
+                a.part_acc[orow * D + i] = o;
             }
-            a.part_acc[orow * D + i] = o;
             continue;
         }
-        orot[i] = L > 0.0f ? o / L : 0.0f;
-        __syncthreads();
-        float res = orot[i];
-        if (a.vc.mode != TQ_MODE_GROUP) {
-            res = 0.0f;
-            for (int k = 0; k < D; ++k) res = fmaf(orot[k], __ldg(a.vc.R + k * D + i), res);
+        orot[rr][i] = L > 0.0f ? o / L : 0.0f;
+    }
+    if (a.part_acc) return;
+    __syncthreads();
+    float res[kRows];
+#pragma unroll
+    for (int rr = 0; rr < kRows; ++rr) res[rr] = orot[rr][i];
+    if (a.vc.mode != TQ_MODE_GROUP) {
+#pragma unroll
+        for (int rr = 0; rr < kRows; ++rr) res[rr] = 0.0f;
+        for (int k = 0; k < D; ++k) {
+            const float rk = __ldg(a.vc.R + k * D + i);
+#pragma unroll
+            for (int rr = 0; rr < kRows; ++rr) res[rr] = fmaf(orot[rr][k], rk, res[rr]);
         }
-        a.out[orow * D + i] = res;
-        __syncthreads();
+    }
+#pragma unroll
+    for (int rr = 0; rr < kRows; ++rr) {
+        const int r = rg * kRows + rr;
+        if (r >= a.plan.rows) break;
+        const int g = r / a.Lq, l = r % a.Lq;
+        a.out[((static_cast<int64_t>(b) * a.Hq + h * a.G + g) * a.Lq + l) * D + i] = res[rr];
     }
 }
 
@@ -385,8 +417,9 @@ size_t al256(size_t x) { return (x + 255) / 256 * 256; }
 
 // Token splits: enough CTAs to cover the GPU, split length a multiple of the
 // tile, and at most `max_chunk` tokens so that many short units still balance.
-void choose_splits(DecodePlan& p, int64_t units, int64_t target_ctas, int max_seq_len, int tile, int max_chunk) {
-    const int64_t max_splits = (max_seq_len + tile - 1) / tile;
+void choose_splits(DecodePlan& p, int64_t units, int64_t target_ctas, int max_seq_len, int tile, int max_chunk,
+                   int min_chunk = 0) {
+    const int64_t max_splits = (max_seq_len + (min_chunk > tile ? min_chunk : tile) - 1) / (min_chunk > tile ? min_chunk : tile);
     int64_t splits = (target_ctas + units - 1) / units;
     if (splits > max_splits) splits = max_splits;
     if (splits < 1) splits = 1;
@@ -475,7 +508,10 @@ DecodePlan make_decode_plan(const tq_cache_desc* d, int batch, int G, int Lq, in
     } else {
         p.kind = 0;
         p.tile = kTile;
-        choose_splits(p, units, static_cast<int64_t>(num_sms) * 4, max_seq_len, kTile, 1 << 30);
+        // at least kSimtMinChunk tokens per split: the merge reads every
+        // split's partials once per output row, so many short splits cost
+        // more in the merge than they gain in the split kernel
+        choose_splits(p, units, static_cast<int64_t>(num_sms) * 4, max_seq_len, kTile, 1 << 30, kSimtMinChunk);
         p.q_bytes = al256(static_cast<size_t>(units) * kRows * D * sizeof(float));
         p.cnt_bytes = 0;
     }

@@ -144,6 +144,30 @@ struct DecodeArgs {
     unsigned* err;
 };
 
+// Decode over split (low/high) states (decode_split.cu): two codec pairs and
+// two pools holding the low coordinates [0, DL) and the high [DL, D).
+struct SplitStateArgs {
+    CodecDev klo, vlo, khi, vhi;
+    PoolDev plo, phi;
+    const void* q;
+    int q_dtype;
+    int batch, Hq, Lq, G, Hkv;
+    const int32_t* seq_lens;
+    const int32_t* table;
+    int max_blocks;
+    float scale;
+    float* out;
+    float* qrot;   // [B][Hkv][RG*16][D]
+    float* qjl;
+    float* part;   // [B][Hkv][RG][splits][16][D]
+    float* ml;
+    int rows, row_groups, splits, chunk;
+    unsigned* err;
+};
+void split_state_plan(SplitStateArgs& a, int max_seq_len, int num_sms);
+size_t split_state_workspace(const SplitStateArgs& a, int D);
+void split_state_bind_workspace(SplitStateArgs& a, void* ws, int D);
+
 DecodePlan make_decode_plan(const tq_cache_desc* d, int batch, int G, int Lq, int max_seq_len, int num_sms);
 
 #ifdef __CUDACC__
@@ -178,6 +202,7 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s, const EncodeAppen
 // the inverse value rotation (MSE values): decode.cu.
 cudaError_t launch_shard_merge(const CodecDev& vc, int parts, const float* ml, const float* acc, int64_t rows,
                                float* out, cudaStream_t s);
+cudaError_t launch_split_state(const SplitStateArgs& a, cudaStream_t s);
 cudaError_t launch_copy_blocks(const tq_cache_desc* src, const tq_cache_desc* dst, const int32_t* src_ids,
                                const int32_t* dst_ids, int n, unsigned* err, cudaStream_t s);
 // Block-table rows of a batch operation (cache_ops.cu): n output rows from
