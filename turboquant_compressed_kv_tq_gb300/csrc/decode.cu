@@ -496,7 +496,10 @@ DecodePlan make_decode_plan(const tq_cache_desc* d, int batch, int G, int Lq, in
             p.bar_off = static_cast<int>(body);
             p.smem = body + sizeof(uint64_t) * mmadec::kWarps * mmadec::kStages;
         };
-        int tile = d->block_tokens < mmadec::kMaxTile ? d->block_tokens : mmadec::kMaxTile;
+        // 64-token tiles; a tile gathers up to four shorter blocks (one copy per
+        // block and record stream)
+        int tile = mmadec::kMaxTile;
+        if (d->block_tokens < 16) tile = d->block_tokens;
         layout(tile);
         while (p.smem > mmadec::kSmemBudget && tile > 16) {
             tile /= 2;

@@ -520,14 +520,21 @@ __global__ void __launch_bounds__(kThreads, 1) split_mma_kernel(MmaArgs m) {
     // shift and a mask. bad_stage bit s marks a stage whose block-table entry
     // was out of range (its copy reads block 0; the tile is flagged and skipped).
     const int bt_shift = __ffs(BT) - 1;
-    unsigned stage_tx = 0;
+    // A tile of TT tokens spans TT / BT blocks when blocks are shorter than
+    // the tile (up to four: 7 streams x 4 blocks fit the warp's lanes), one
+    // block otherwise. Lane k copies record stream k % 7 of block k / 7 of the
+    // tile into that stream's run of the stage (blocks one after another).
+    const int tile_blocks = TT > BT ? TT / BT : 1;
+    const int blk_tokens = TT > BT ? BT : TT;   // tokens a lane's copy carries
+    const int my_stream = lane % 7, my_blk = lane / 7;
+    unsigned blk_tx = 0;                         // bytes of one block's part of a stage
     int s_off = -1, s_field = 0;
     int64_t s_src = 0;
 #pragma unroll
     for (int k = 0; k < 7; ++k) {
-        if (st.off[k] >= 0) stage_tx += TT * st.field[k];
-        if (lane == k) {
-            s_off = st.off[k];
+        if (st.off[k] >= 0) blk_tx += blk_tokens * st.field[k];
+        if (my_stream == k && my_blk < tile_blocks && st.off[k] >= 0) {
+            s_off = st.off[k] + my_blk * blk_tokens * st.field[k];
             s_field = st.field[k];
             s_src = a.pool.off[k];
         }
@@ -536,21 +543,31 @@ __global__ void __launch_bounds__(kThreads, 1) split_mma_kernel(MmaArgs m) {
     uint32_t bad_stage = 0;
     auto issue = [&](int i) {
         const int t0 = t_begin + (warp + i * kWarps) * TT;
-        const int lb = t0 >> bt_shift;
+        const int lb = (t0 >> bt_shift) + my_blk;
         const int slot0 = t0 & (BT - 1);
-        int64_t pb = a.table ? static_cast<int64_t>(a.table[static_cast<int64_t>(b) * a.max_blocks + lb])
-                             : static_cast<int64_t>(b) * a.max_blocks + lb;
+        // blocks of the tile that hold tokens of this split (a partial last tile
+        // may end before the tile's last block, whose table entry is not read)
+        const int live = min(tile_blocks, (t_end - t0 + blk_tokens - 1) / blk_tokens);
+        const bool mine = s_off >= 0 && my_blk < live;
+        int64_t pb = 0;
+        bool badb = false;
+        if (mine) {
+            pb = a.table ? static_cast<int64_t>(a.table[static_cast<int64_t>(b) * a.max_blocks + lb])
+                         : static_cast<int64_t>(b) * a.max_blocks + lb;
+            badb = pb < 0 || pb >= a.pool.num_blocks;
+            if (badb) pb = 0;
+        }
         const int sidx = i % kStages;
-        const bool badb = pb < 0 || pb >= a.pool.num_blocks;
-        if (badb) pb = 0;
-        bad_stage = badb ? (bad_stage | (1u << sidx)) : (bad_stage & ~(1u << sidx));
+        const bool bad_any = __any_sync(0xffffffffu, badb);
+        bad_stage = bad_any ? (bad_stage | (1u << sidx)) : (bad_stage & ~(1u << sidx));
         const char* base = a.pool.base + (pb * Hkv + h) * a.pool.sub_bytes;
         unsigned char* dst = ring + static_cast<size_t>(sidx) * st.bytes;
         uint64_t* bar = &bars[sidx];
-        if (lane == 0) mbar_expect_tx(bar, stage_tx);
+        if (lane == 0) mbar_expect_tx(bar, blk_tx * live);
         __syncwarp();
-        if (s_off >= 0)
-            bulk_g2s_once(dst + s_off, base + s_src + static_cast<int64_t>(slot0) * s_field, TT * s_field, bar, pol);
+        if (mine)
+            bulk_g2s_once(dst + s_off, base + s_src + static_cast<int64_t>(slot0) * s_field, blk_tokens * s_field,
+                          bar, pol);
     };
 
     // First stages: fetched before waiting for the kernel this one may overlap,

@@ -680,13 +680,19 @@ cudaError_t launch_prefill(const DecodeArgs& a, const uint4* qfrag, cudaStream_t
     TcPrefillArgs P{};
     P.a = a;
     P.qfrag = qfrag;
-    P.st.tt = p.tile;
-    P.st.bytes = p.st_bytes;
+    // a stage holds one tile of one block: the decode plan's tile, or the
+    // block when blocks are shorter (the decode gathers several short blocks
+    // into one stage; this kernel copies one block per stage)
+    const int TT = p.tile > a.pool.BT ? a.pool.BT : p.tile;
+    P.st.tt = TT;
+    int so = 0;
     for (int k = 0; k < 7; ++k) {
-        P.st.off[k] = p.st_off[k];
         P.st.field[k] = p.st_field[k];
+        P.st.off[k] = p.st_off[k] >= 0 ? so : -1;
+        if (p.st_off[k] >= 0) so += TT * p.st_field[k];
     }
-    int off = 2 * p.st_bytes;
+    P.st.bytes = (so + 127) / 128 * 128;
+    int off = 2 * P.st.bytes;
     off = (off + 1023) / 1024 * 1024;
     const int ops_begin = off;
     for (int i = 0; i < 2; ++i) { P.k_off[i] = off; off += kTTok * kD * 2; }
