@@ -491,7 +491,7 @@ DecodePlan make_decode_plan(const tq_cache_desc* d, int batch, int G, int Lq, in
                 p.kt_off = static_cast<int>(ringq);
                 ringq += mmadec::kKQuadBytes;
             }
-            const size_t combine = sizeof(float) * (2 * mmadec::kWarps * kRows + mmadec::kWarps * kRows * (D + 1));
+            const size_t combine = mmadec::kWarpMergeBytes;
             const size_t body = ((ringq > combine ? ringq : combine) + 127) / 128 * 128;
             p.bar_off = static_cast<int>(body);
             p.smem = body + sizeof(uint64_t) * mmadec::kWarps * mmadec::kStages;
@@ -506,6 +506,19 @@ DecodePlan make_decode_plan(const tq_cache_desc* d, int batch, int G, int Lq, in
             layout(tile);
         }
         choose_splits(p, units, num_sms, max_seq_len, p.tile, 16384);
+        // the last CTA of a unit stages up to merge_splits split accumulators
+        // and R_v below the barriers: grow the launch's shared memory for them
+        // while the budget allows (the main loop is done by then)
+        const size_t bars = sizeof(uint64_t) * mmadec::kWarps * mmadec::kStages;
+        int nc = p.splits;
+        while (nc > 1 && (static_cast<size_t>(mmadec::merge_bytes(nc)) + 127) / 128 * 128 + bars > mmadec::kSmemBudget)
+            --nc;
+        p.merge_splits = nc;
+        const size_t need = (static_cast<size_t>(mmadec::merge_bytes(nc)) + 127) / 128 * 128;
+        if (need > static_cast<size_t>(p.bar_off)) {
+            p.bar_off = static_cast<int>(need);
+            p.smem = need + bars;
+        }
         p.q_bytes = al256(static_cast<size_t>(units) * 2 * 8 * 32 * 16);
         p.cnt_bytes = al256(static_cast<size_t>(units) * sizeof(unsigned));
     } else {
@@ -535,6 +548,7 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s, const EncodeAppen
         m.st.qs_off = a.plan.qs_off;
         m.st.vt_off = a.plan.vt_off;
         m.st.kt_off = a.plan.kt_off;
+        m.st.merge_splits = a.plan.merge_splits;
         for (int k = 0; k < 7; ++k) {
             m.st.off[k] = a.plan.st_off[k];
             m.st.field[k] = a.plan.st_field[k];

@@ -32,6 +32,7 @@ struct StageLayout {
     int qs_off;             // byte offset of the query fragments (past the ring)
     int vt_off;             // byte offset of the value pair table region (-1: none)
     int kt_off;             // byte offset of the key quad table (-1: none)
+    int merge_splits;       // splits the final merge stages in shared memory at once
 };
 
 struct MmaArgs {
@@ -344,95 +345,203 @@ __device__ __forceinline__ void mse_chunk(const uint32_t* w, const typename MseT
 
 // The last CTA of a unit (by arrival ticket) merges the splits' partial
 // (max, sum, accumulator) rows, divides by the merged sum, applies the inverse
-// value rotation and writes the output rows; every CTA has written its own
-// partials before calling. `orot` is shared memory for 16 x (kD + 1) floats;
-// threads 0..255 merge (16 per row, 8 columns each).
+// value rotation and writes the output rows (or, for a shard's state, the
+// merged (max, sum, accumulator) without the rotation); every CTA has written
+// its own partials before calling. The merging CTA stages R_v and the splits'
+// accumulators in shared memory with bulk copies (merge_splits of them at a
+// time) and spreads the merge and the rotation over all its threads: the
+// merge runs while the other CTAs of the grid have already finished, so its
+// latency is the launch's tail.
 template <bool VGROUP>
-__device__ __forceinline__ void merge_unit(const MmaArgs& m, int unit, int split, int rg, int b, int h, float* orot,
+__device__ __forceinline__ void merge_unit(const MmaArgs& m, int unit, int rg, int b, int h, unsigned char* smem,
                                            int tid) {
     const DecodeArgs& a = m.a;
-    constexpr int kStride = kD + 1;
     const int S = a.plan.splits;
-    const int r = tid >> 4;
-    const int dbase = (tid & 15) * 8;
-    const bool merger = tid < kRows * 16;
     __threadfence();
+    tc::fence_proxy_async_smem();  // this thread's shared-memory accesses before the bulk copies below
     __syncthreads();
     __shared__ unsigned s_ticket;
     if (tid == 0) s_ticket = atomicAdd(m.cnt + unit, 1u);
     __syncthreads();
     if (s_ticket != static_cast<unsigned>(S - 1)) return;
     __threadfence();
-    if (merger) {
-        float M = -INFINITY;
-        const float* mlu = m.ml + static_cast<int64_t>(unit) * S * kRows * 2;
-        // the splits' loads are independent: unrolled, so that they overlap
-#pragma unroll 4
-        for (int s = 0; s < S; ++s) M = fmaxf(M, __ldcg(mlu + (s * kRows + r) * 2));
-        float L = 0.0f, acc[8] = {};
-        if (M != -INFINITY) {
-#pragma unroll 4
-            for (int s = 0; s < S; ++s) {
-                const float2 ml = __ldcg(reinterpret_cast<const float2*>(mlu + (s * kRows + r) * 2));
-                // a split that saw no score has (-inf, 0) and a zero accumulator
-                const float wt = ml.x == -INFINITY ? 0.0f : ex2(ml.x - M);
-                L = fmaf(wt, ml.y, L);
-                const float4* src = reinterpret_cast<const float4*>(
-                    m.part + ((static_cast<int64_t>(unit) * S + s) * kRows + r) * kD + dbase);
-                const float4 v0 = __ldcg(src), v1 = __ldcg(src + 1);
-                acc[0] = fmaf(wt, v0.x, acc[0]); acc[1] = fmaf(wt, v0.y, acc[1]);
-                acc[2] = fmaf(wt, v0.z, acc[2]); acc[3] = fmaf(wt, v0.w, acc[3]);
-                acc[4] = fmaf(wt, v1.x, acc[4]); acc[5] = fmaf(wt, v1.y, acc[5]);
-                acc[6] = fmaf(wt, v1.z, acc[6]); acc[7] = fmaf(wt, v1.w, acc[7]);
-            }
-        }
-        // MSE values were multiplied as fp16(op_scale * level): divide op_scale out
-        const float vs = VGROUP ? 1.0f : a.vc.cq_scale;
-        const int row = rg * kRows + r;
-        if (a.part_acc) {
-            // a shard's state: max in natural-log units, sum, accumulator
-            if (row < a.plan.rows) {
-                const int gq = row / a.Lq, l = row % a.Lq;
-                const int64_t o = (static_cast<int64_t>(b) * a.Hq + h * a.G + gq) * a.Lq + l;
-                if ((tid & 15) == 0) {
-                    a.part_ml[2 * o] = M == -INFINITY ? -INFINITY : M * 0.6931471805599453f;
-                    a.part_ml[2 * o + 1] = L;
-                }
-                const float iv = 1.0f / vs;
-                float4* dst = reinterpret_cast<float4*>(a.part_acc + o * kD + dbase);
-                dst[0] = make_float4(acc[0] * iv, acc[1] * iv, acc[2] * iv, acc[3] * iv);
-                dst[1] = make_float4(acc[4] * iv, acc[5] * iv, acc[6] * iv, acc[7] * iv);
-            }
-        } else {
-            const float inv = L > 0.0f ? 1.0f / (L * vs) : 0.0f;
-            for (int k = 0; k < 8; ++k) orot[r * kStride + dbase + k] = acc[k] * inv;
+    const bool rotate = !VGROUP && !a.part_acc;
+    // barrier 0: R_v, 1: the partials
+    uint64_t* rbar = reinterpret_cast<uint64_t*>(smem + m.st.bar_off);
+    uint64_t* bar = rbar + 1;
+    const int NC = m.st.merge_splits;
+    float* sp = reinterpret_cast<float*>(smem);
+    const float* sR = reinterpret_cast<const float*>(smem + merge_r_off(NC));
+    float* sw = sp + NC * kRows * kD;   // [NC][16] weights 2^(m - M)
+    float* swl = sw + NC * kRows;       // [NC][16] weight x sum
+    float* red = swl + NC * kRows;      // [24][16] row maxima of the thread groups
+    float* ssum = red + kThreads;       // [16] merged sums
+    const float* mlu = m.ml + static_cast<int64_t>(unit) * S * kRows * 2;
+    const float* pu = m.part + static_cast<int64_t>(unit) * S * kRows * kD;
+    if (tid == 0) {
+        mbar_init(bar, 1);
+        if (rotate) mbar_init(rbar, 1);
+        mbar_fence_init();
+        tc::fence_proxy_async_global();  // the other CTAs' partials, acquired through the ticket
+        const int n0 = S < NC ? S : NC;
+        mbar_expect_tx(bar, n0 * kMergePartBytes);
+        bulk_g2s(sp, pu, n0 * kMergePartBytes, bar);
+        if (rotate) {
+            mbar_expect_tx(rbar, kMergeRBytes);
+            bulk_g2s(const_cast<float*>(sR), a.vc.R, kMergeRBytes, rbar);
         }
     }
+    // row maximum: thread t takes row t % 16 of splits t / 16, t / 16 + 24, ...
+    constexpr int kGroups = kThreads / kRows;
+    const int rr = tid % kRows;
+    float mx = -INFINITY;
+    for (int s = tid / kRows; s < S; s += kGroups) mx = fmaxf(mx, __ldcg(mlu + (s * kRows + rr) * 2));
+    red[tid] = mx;  // = red[(tid / 16) * 16 + rr]
     __syncthreads();
-    const int row = rg * kRows + r;
-    if (merger && row < a.plan.rows && !a.part_acc) {
-        float res[8];
-        if constexpr (!VGROUP) {
-            for (int k = 0; k < 8; ++k) res[k] = 0.0f;
-            const float* R = a.vc.R;
-            for (int i2 = 0; i2 < kD; ++i2) {
-                const float ov = orot[r * kStride + i2];
-                const float4 r0 = __ldg(reinterpret_cast<const float4*>(R + i2 * kD + dbase));
-                const float4 r1 = __ldg(reinterpret_cast<const float4*>(R + i2 * kD + dbase) + 1);
-                res[0] = fmaf(ov, r0.x, res[0]); res[1] = fmaf(ov, r0.y, res[1]);
-                res[2] = fmaf(ov, r0.z, res[2]); res[3] = fmaf(ov, r0.w, res[3]);
-                res[4] = fmaf(ov, r1.x, res[4]); res[5] = fmaf(ov, r1.y, res[5]);
-                res[6] = fmaf(ov, r1.z, res[6]); res[7] = fmaf(ov, r1.w, res[7]);
-            }
-        } else {
-            for (int k = 0; k < 8; ++k) res[k] = orot[r * kStride + dbase + k];
+    float M = -INFINITY;
+#pragma unroll
+    for (int g2 = 0; g2 < kGroups; ++g2) M = fmaxf(M, red[g2 * kRows + rr]);
+    // float4 slots of the 16 x D output: slot sl = row * (D / 4) + column / 4;
+    // the first 256 threads take slots tid and tid + 256
+    constexpr int kSlots = kRows * kD / 4;
+    constexpr int kSlotThreads = kSlots / 2;
+    const bool slotter = tid < kSlotThreads;
+    const int sl0 = tid, sl1 = tid + kSlotThreads;
+    const int r0 = sl0 / (kD / 4), r1 = sl1 / (kD / 4);
+    float4 acc0 = make_float4(0.0f, 0.0f, 0.0f, 0.0f), acc1 = acc0;
+    float L = 0.0f;  // merged sum of row tid (threads tid < 16)
+    unsigned phase = 0;
+    for (int c0 = 0; c0 < S; c0 += NC) {
+        const int n = S - c0 < NC ? S - c0 : NC;
+        // weights of this chunk's splits (a split that saw no score has (-inf, 0)
+        // and a zero accumulator); entry i covers row i % 16 = tid % 16
+        for (int i = tid; i < n * kRows; i += kThreads) {
+            const float2 ml = __ldcg(reinterpret_cast<const float2*>(mlu + ((c0 + i / kRows) * kRows + rr) * 2));
+            const float w = ml.x == -INFINITY ? 0.0f : ex2(ml.x - M);
+            sw[i] = w;
+            swl[i] = w * ml.y;
         }
-        const int gq = row / a.Lq, l = row % a.Lq;
-        float* dst = a.out + ((static_cast<int64_t>(b) * a.Hq + h * a.G + gq) * a.Lq + l) * kD + dbase;
-        reinterpret_cast<float4*>(dst)[0] = make_float4(res[0], res[1], res[2], res[3]);
-        reinterpret_cast<float4*>(dst)[1] = make_float4(res[4], res[5], res[6], res[7]);
+        __syncthreads();
+        if (!mbar_wait(bar, phase)) {
+            if (tid == 0) atomicOr(a.err, TQ_DEVERR_TIMEOUT);
+            (void)mbar_wait(bar, phase);
+        }
+        phase ^= 1u;
+        if (tid < kRows)
+            for (int s = 0; s < n; ++s) L += swl[s * kRows + tid];
+        if (slotter) {
+            const float4* sp4 = reinterpret_cast<const float4*>(sp);
+            for (int s = 0; s < n; ++s) {
+                const float w0 = sw[s * kRows + r0], w1 = sw[s * kRows + r1];
+                const float4 v0 = sp4[s * kSlots + sl0], v1 = sp4[s * kSlots + sl1];
+                acc0.x = fmaf(w0, v0.x, acc0.x); acc0.y = fmaf(w0, v0.y, acc0.y);
+                acc0.z = fmaf(w0, v0.z, acc0.z); acc0.w = fmaf(w0, v0.w, acc0.w);
+                acc1.x = fmaf(w1, v1.x, acc1.x); acc1.y = fmaf(w1, v1.y, acc1.y);
+                acc1.z = fmaf(w1, v1.z, acc1.z); acc1.w = fmaf(w1, v1.w, acc1.w);
+            }
+        }
+        tc::fence_proxy_async_smem();
+        __syncthreads();  // the chunk's buffers are rewritten below
+        if (c0 + NC < S && tid == 0) {
+            const int n1 = S - c0 - NC < NC ? S - c0 - NC : NC;
+            mbar_expect_tx(bar, n1 * kMergePartBytes);
+            bulk_g2s(sp, pu + static_cast<int64_t>(c0 + NC) * kRows * kD, n1 * kMergePartBytes, bar);
+        }
     }
-    if (tid == 0) m.cnt[unit] = 0u;
+    // MSE values were multiplied as fp16(op_scale * level): divide op_scale out
+    const float vs = VGROUP ? 1.0f : a.vc.cq_scale;
+    if (a.part_acc) {
+        // a shard's state: max in natural-log units, sum, accumulator
+        const float iv = 1.0f / vs;
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int sl = e ? sl1 : sl0;
+            const int row = rg * kRows + (e ? r1 : r0);
+            const float4 v = e ? acc1 : acc0;
+            if (slotter && row < a.plan.rows) {
+                const int gq = row / a.Lq, l = row % a.Lq;
+                const int64_t oo = (static_cast<int64_t>(b) * a.Hq + h * a.G + gq) * a.Lq + l;
+                reinterpret_cast<float4*>(a.part_acc + oo * kD)[sl % (kD / 4)] =
+                    make_float4(v.x * iv, v.y * iv, v.z * iv, v.w * iv);
+            }
+        }
+        const int row = rg * kRows + tid;
+        if (tid < kRows && row < a.plan.rows) {
+            const int gq = row / a.Lq, l = row % a.Lq;
+            const int64_t oo = (static_cast<int64_t>(b) * a.Hq + h * a.G + gq) * a.Lq + l;
+            a.part_ml[2 * oo] = M == -INFINITY ? -INFINITY : M * 0.6931471805599453f;
+            a.part_ml[2 * oo + 1] = L;
+        }
+    } else {
+        if (tid < kRows) ssum[tid] = L > 0.0f ? 1.0f / (L * vs) : 0.0f;
+        __syncthreads();
+        // normalised rows (rotated domain), row stride kOS floats: over the
+        // first chunk's buffer (and the dead weights after it when one split)
+        constexpr int kOS = kD + 4;
+        float* orot = sp;
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int sl = e ? sl1 : sl0, r = e ? r1 : r0;
+            const float iv = ssum[r];
+            const float4 v = e ? acc1 : acc0;
+            const float4 x = make_float4(v.x * iv, v.y * iv, v.z * iv, v.w * iv);
+            const int row = rg * kRows + r;
+            if (slotter && !rotate && row < a.plan.rows) {
+                const int gq = row / a.Lq, l = row % a.Lq;
+                reinterpret_cast<float4*>(a.out + ((static_cast<int64_t>(b) * a.Hq + h * a.G + gq) * a.Lq + l) *
+                                                      kD)[sl % (kD / 4)] = x;
+            }
+            if (slotter && rotate) reinterpret_cast<float4*>(orot + r * kOS)[sl % (kD / 4)] = x;
+        }
+        if (rotate) {
+            if (!mbar_wait(rbar, 0)) {
+                if (tid == 0) atomicOr(a.err, TQ_DEVERR_TIMEOUT);
+                (void)mbar_wait(rbar, 0);
+            }
+            __syncthreads();
+            // out = orot R_v: warp w < 8 takes columns 16 w .. 16 w + 15; lane
+            // (rb, cb) rows rb + 4 k (k < 4) at columns 16 w + 2 cb, + 1
+            const int warp = tid >> 5, lane = tid & 31;
+            if (warp < kD / 16) {
+                const int rb = lane >> 3, cb = lane & 7;
+                const int col = 16 * warp + 2 * cb;
+                float2 res[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) res[k] = make_float2(0.0f, 0.0f);
+                const float4* o4 = reinterpret_cast<const float4*>(orot);
+#pragma unroll 2
+                for (int i4 = 0; i4 < kD / 4; ++i4) {
+                    float4 ov[4];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) ov[k] = o4[(rb + 4 * k) * (kOS / 4) + i4];
+#pragma unroll
+                    for (int ii = 0; ii < 4; ++ii) {
+                        const float2 rv = *reinterpret_cast<const float2*>(sR + (4 * i4 + ii) * kD + col);
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            const float x = ii == 0 ? ov[k].x : ii == 1 ? ov[k].y : ii == 2 ? ov[k].z : ov[k].w;
+                            res[k].x = fmaf(x, rv.x, res[k].x);
+                            res[k].y = fmaf(x, rv.y, res[k].y);
+                        }
+                    }
+                }
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int row = rg * kRows + rb + 4 * k;
+                    if (row < a.plan.rows) {
+                        const int gq = row / a.Lq, l = row % a.Lq;
+                        *reinterpret_cast<float2*>(
+                            a.out + ((static_cast<int64_t>(b) * a.Hq + h * a.G + gq) * a.Lq + l) * kD + col) = res[k];
+                    }
+                }
+            }
+        }
+    }
+    if (tid == 0) {
+        m.cnt[unit] = 0u;
+        mbar_inval(bar);
+        if (rotate) mbar_inval(rbar);
+    }
 }
 
 template <int KB, bool KPROD, bool VGROUP, int VB>
@@ -857,7 +966,7 @@ __global__ void __launch_bounds__(kThreads, 1) split_mma_kernel(MmaArgs m) {
     lrow1 += __shfl_xor_sync(0xffffffffu, lrow1, 1);
     lrow1 += __shfl_xor_sync(0xffffffffu, lrow1, 2);
     __syncthreads();
-    constexpr int kStride = kD + 1;
+    constexpr int kStride = kCoStride;  // column d at d + d / 32
     float* cm = reinterpret_cast<float*>(smem);
     float* cl = cm + kWarps * kRows;
     float* co = cl + kWarps * kRows;
@@ -872,7 +981,7 @@ __global__ void __launch_bounds__(kThreads, 1) split_mma_kernel(MmaArgs m) {
         int pa_, pb_;
         if constexpr (VGROUP) group_pair(VB, p, pa_, pb_);
         else mse_pair(VB, p, pa_, pb_);
-        const int d0 = 32 * j + pa_, d1 = 32 * j + pb_;
+        const int d0 = 33 * j + pa_, d1 = 33 * j + pb_;
         co[(warp * kRows + g) * kStride + d0] = o[p][0];
         co[(warp * kRows + g) * kStride + d1] = o[p][1];
         co[(warp * kRows + g + 8) * kStride + d0] = o[p][2];
@@ -894,7 +1003,8 @@ __global__ void __launch_bounds__(kThreads, 1) split_mma_kernel(MmaArgs m) {
                 if (mw == -INFINITY) continue;
                 const float wt = ex2(mw - M);
                 L = fmaf(wt, cl[w * kRows + r], L);
-                for (int k = 0; k < 8; ++k) acc[k] = fmaf(wt, co[(w * kRows + r) * kStride + dbase + k], acc[k]);
+                for (int k = 0; k < 8; ++k)
+                    acc[k] = fmaf(wt, co[(w * kRows + r) * kStride + dbase + dbase / 32 + k], acc[k]);
             }
         }
         float* dst = m.part + ((static_cast<int64_t>(unit) * S + split) * kRows + r) * kD + dbase;
@@ -906,7 +1016,7 @@ __global__ void __launch_bounds__(kThreads, 1) split_mma_kernel(MmaArgs m) {
             mlp[1] = L;
         }
     }
-    merge_unit<VGROUP>(m, unit, split, rg, b, h, cm, tid);
+    merge_unit<VGROUP>(m, unit, rg, b, h, smem, tid);
 }
 
 // Query prep fused with the short encode of a decode step's new tokens

@@ -80,6 +80,12 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
 }
 
+// Order this thread's generic-proxy view of global memory (writes of other
+// CTAs it has acquired) before its later async-proxy reads (bulk copies).
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;\n" ::: "memory");
+}
+
 // ------------------------------------------------------------------ tensor memory
 
 // Allocate `ncols` (power of two >= 32) TMEM columns; the whole warp executes
