@@ -506,21 +506,7 @@ DecodePlan make_decode_plan(const tq_cache_desc* d, int batch, int G, int Lq, in
             layout(tile);
         }
         choose_splits(p, units, num_sms, max_seq_len, p.tile, 16384);
-        // the last CTA of a unit stages up to merge_splits split accumulators
-        // and R_v below the barriers: grow the launch's shared memory for them
-        // while the budget allows (the main loop is done by then)
-        const size_t bars = sizeof(uint64_t) * mmadec::kWarps * mmadec::kStages;
-        int nc = p.splits;
-        while (nc > 1 && (static_cast<size_t>(mmadec::merge_bytes(nc)) + 127) / 128 * 128 + bars > mmadec::kSmemBudget)
-            --nc;
-        p.merge_splits = nc;
-        const size_t need = (static_cast<size_t>(mmadec::merge_bytes(nc)) + 127) / 128 * 128;
-        if (need > static_cast<size_t>(p.bar_off)) {
-            p.bar_off = static_cast<int>(need);
-            p.smem = need + bars;
-        }
         p.q_bytes = al256(static_cast<size_t>(units) * 2 * 8 * 32 * 16);
-        p.cnt_bytes = al256(static_cast<size_t>(units) * sizeof(unsigned));
     } else {
         p.kind = 0;
         p.tile = kTile;
@@ -529,11 +515,10 @@ DecodePlan make_decode_plan(const tq_cache_desc* d, int batch, int G, int Lq, in
         // more in the merge than they gain in the split kernel
         choose_splits(p, units, static_cast<int64_t>(num_sms) * 4, max_seq_len, kTile, 1 << 30, kSimtMinChunk);
         p.q_bytes = al256(static_cast<size_t>(units) * kRows * D * sizeof(float));
-        p.cnt_bytes = 0;
     }
     p.part_bytes = al256(static_cast<size_t>(units) * p.splits * kRows * D * sizeof(float));
     p.ml_bytes = al256(static_cast<size_t>(units) * p.splits * kRows * 2 * sizeof(float));
-    p.total = (p.kind ? p.q_bytes + p.cnt_bytes : 2 * p.q_bytes) + p.part_bytes + p.ml_bytes;
+    p.total = (p.kind ? p.q_bytes : 2 * p.q_bytes) + p.part_bytes + p.ml_bytes;
     return p;
 }
 
@@ -548,16 +533,14 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s, const EncodeAppen
         m.st.qs_off = a.plan.qs_off;
         m.st.vt_off = a.plan.vt_off;
         m.st.kt_off = a.plan.kt_off;
-        m.st.merge_splits = a.plan.merge_splits;
         for (int k = 0; k < 7; ++k) {
             m.st.off[k] = a.plan.st_off[k];
             m.st.field[k] = a.plan.st_field[k];
         }
         char* ws = static_cast<char*>(a.ws);
         m.qfrag = reinterpret_cast<const uint4*>(ws);
-        m.cnt = reinterpret_cast<unsigned*>(ws + a.plan.q_bytes);
-        m.part = reinterpret_cast<float*>(ws + a.plan.q_bytes + a.plan.cnt_bytes);
-        m.ml = reinterpret_cast<float*>(ws + a.plan.q_bytes + a.plan.cnt_bytes + a.plan.part_bytes);
+        m.part = reinterpret_cast<float*>(ws + a.plan.q_bytes);
+        m.ml = reinterpret_cast<float*>(ws + a.plan.q_bytes + a.plan.part_bytes);
         cudaError_t e = cudaErrorInvalidValue;
         const DecodePlan& p = a.plan;
         if (mmadec::dispatch_a(p.kb, p.kprod, p.vgroup, p.vb, m, p.smem, s, step, &e)) return e;

@@ -50,30 +50,11 @@ constexpr int kMaxTile = 64;
 // of the GPU less a margin for its static shared memory.
 constexpr size_t kSmemBudget = 227 * 1024 - 1024;
 constexpr int kQFragBytes = 2 * 8 * 32 * 16;  // query fragments of one unit
-// End of the split kernel. The warps merge their (max, sum, accumulator) rows
+// End of the split kernel: the warps merge their (max, sum, accumulator) rows
 // in shared memory from offset 0 (rows of kCoStride floats, a column d at
 // d + d / 32 so that the fragment layout stores without bank conflicts).
-// Then the unit's last CTA merges the splits, shared memory from offset 0: a
-// chunk of split accumulators (16 x D fp32 each) with their per-row weights and
-// weighted sums, the row maxima of the 24 thread groups and the rows' sums;
-// R_v (fp32, D x D) past both areas. Both are staged by bulk copies (the ring
-// and the tables are free by then).
 constexpr int kCoStride = kD + 4;
 constexpr int kWarpMergeBytes = (2 * kWarps * kRows + kWarps * kRows * kCoStride) * 4;
-constexpr int kMergeRBytes = kD * kD * 4;
-constexpr int kMergePartBytes = kRows * kD * 4;
-constexpr int kMergePerSplit = kMergePartBytes + 2 * kRows * 4;
-__host__ __device__ constexpr int merge_r_off(int splits) {
-    return ((splits * kMergePerSplit + kThreads * 4 + kRows * 4 > kWarpMergeBytes
-                 ? splits * kMergePerSplit + kThreads * 4 + kRows * 4
-                 : kWarpMergeBytes) + 127) / 128 * 128;
-}
-__host__ __device__ constexpr int merge_bytes(int splits) { return merge_r_off(splits) + kMergeRBytes; }
-static_assert(kThreads % kRows == 0 && kThreads % kD == 0, "merge thread mapping");
-// the normalised rows (16 x (D + 4) floats) overwrite the first staged partial and,
-// with one split, the dead weights and row maxima after it (not the sums)
-static_assert(kRows * (kD + 4) * 4 <= kMergePerSplit + kThreads * 4, "merge row buffer");
-static_assert(kThreads >= kRows * kD / 8 && kD % 16 == 0, "merge slots");
 constexpr unsigned kSpinLimit = 1u << 22;
 // Pair table of 3-bit value codes: 64 entries x 32 bank copies x 4 bytes,
 // placed at an 8 KB-aligned shared address inside a 16 KB region.

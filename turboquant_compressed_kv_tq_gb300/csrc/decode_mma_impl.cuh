@@ -32,14 +32,12 @@ struct StageLayout {
     int qs_off;             // byte offset of the query fragments (past the ring)
     int vt_off;             // byte offset of the value pair table region (-1: none)
     int kt_off;             // byte offset of the key quad table (-1: none)
-    int merge_splits;       // splits the final merge stages in shared memory at once
 };
 
 struct MmaArgs {
     DecodeArgs a;
     StageLayout st;
     const uint4* qfrag;     // [unit][2][8][32] uint4
-    unsigned* cnt;          // [unit]
     float* part;            // [unit][splits][16][128]
     float* ml;              // [unit][splits][16][2]
 };
@@ -225,7 +223,6 @@ __device__ __forceinline__ void qfrag_body(const MmaArgs& m, unsigned char* qsm_
             }
             dst[((which * 8 + ks) * 32 + ln) * 4 + reg] = pack_half2(va, vb);
         }
-        if (tid == 0 && m.cnt) m.cnt[unit] = 0u;
         __syncthreads();   // q1 / q2 / A are rewritten by the next unit
     }
     if (first && tid == 0) {   // no unit for this CTA: release the tables' copy
@@ -343,205 +340,117 @@ __device__ __forceinline__ void mse_chunk(const uint32_t* w, const typename MseT
     MseChunk<B>::run(w, t, h);
 }
 
-// The last CTA of a unit (by arrival ticket) merges the splits' partial
-// (max, sum, accumulator) rows, divides by the merged sum, applies the inverse
-// value rotation and writes the output rows (or, for a shard's state, the
-// merged (max, sum, accumulator) without the rotation); every CTA has written
-// its own partials before calling. The merging CTA stages R_v and the splits'
-// accumulators in shared memory with bulk copies (merge_splits of them at a
-// time) and spreads the merge and the rotation over all its threads: the
-// merge runs while the other CTAs of the grid have already finished, so its
-// latency is the launch's tail.
+// Merge of a unit's split partials, one CTA per (unit, row), launched after
+// the split kernel with programmatic dependent launch: R_v is staged in shared
+// memory before the CTA waits for the split kernel; then the CTA takes the
+// row's maximum over the splits, weights each split's (sum, accumulator) by
+// 2^(m - max), divides by the merged sum and applies the inverse value
+// rotation (or, for a shard's state, writes the merged (max, sum,
+// accumulator) without the rotation). Thread d owns output column d.
+constexpr int kMThreads = kD;
+
 template <bool VGROUP>
-__device__ __forceinline__ void merge_unit(const MmaArgs& m, int unit, int rg, int b, int h, unsigned char* smem,
-                                           int tid) {
+__global__ void __launch_bounds__(kMThreads) merge_rows_kernel(MmaArgs m) {
+    extern __shared__ __align__(128) unsigned char smem[];
     const DecodeArgs& a = m.a;
-    const int S = a.plan.splits;
-    __threadfence();
-    tc::fence_proxy_async_smem();  // this thread's shared-memory accesses before the bulk copies below
-    __syncthreads();
-    __shared__ unsigned s_ticket;
-    if (tid == 0) s_ticket = atomicAdd(m.cnt + unit, 1u);
-    __syncthreads();
-    if (s_ticket != static_cast<unsigned>(S - 1)) return;
-    __threadfence();
+    tc::grid_release_dependents();  // the next kernel waits for this grid before the workspace
+    const int unit = blockIdx.x, r = blockIdx.y;
+    const int RG = a.plan.row_groups;
+    const int rg = unit % RG, bh = unit / RG;
+    const int b = bh / a.pool.Hkv, h = bh % a.pool.Hkv;
+    const int row = rg * kRows + r;
+    if (row >= a.plan.rows) return;  // padding row of the last group
+    const int d = threadIdx.x, lane = d & 31, wid = d >> 5;
     const bool rotate = !VGROUP && !a.part_acc;
-    // barrier 0: R_v, 1: the partials
-    uint64_t* rbar = reinterpret_cast<uint64_t*>(smem + m.st.bar_off);
-    uint64_t* bar = rbar + 1;
-    const int NC = m.st.merge_splits;
-    float* sp = reinterpret_cast<float*>(smem);
-    const float* sR = reinterpret_cast<const float*>(smem + merge_r_off(NC));
-    float* sw = sp + NC * kRows * kD;   // [NC][16] weights 2^(m - M)
-    float* swl = sw + NC * kRows;       // [NC][16] weight x sum
-    float* red = swl + NC * kRows;      // [24][16] row maxima of the thread groups
-    float* ssum = red + kThreads;       // [16] merged sums
-    const float* mlu = m.ml + static_cast<int64_t>(unit) * S * kRows * 2;
-    const float* pu = m.part + static_cast<int64_t>(unit) * S * kRows * kD;
-    if (tid == 0) {
-        mbar_init(bar, 1);
-        if (rotate) mbar_init(rbar, 1);
+    float* sR = reinterpret_cast<float*>(smem);      // [D][D], rotation only
+    float* so = sR + (rotate ? kD * kD : 0);         // [D] the merged row
+    float* sw = so + kD;                             // [kMThreads] weights of a chunk of splits
+    float* sred = sw + kMThreads;                    // [4] per-warp maxima / sums
+    __shared__ uint64_t bar;
+    if (rotate && d == 0) {
+        mbar_init(&bar, 1);
         mbar_fence_init();
-        tc::fence_proxy_async_global();  // the other CTAs' partials, acquired through the ticket
-        const int n0 = S < NC ? S : NC;
-        mbar_expect_tx(bar, n0 * kMergePartBytes);
-        bulk_g2s(sp, pu, n0 * kMergePartBytes, bar);
-        if (rotate) {
-            mbar_expect_tx(rbar, kMergeRBytes);
-            bulk_g2s(const_cast<float*>(sR), a.vc.R, kMergeRBytes, rbar);
-        }
+        mbar_expect_tx(&bar, kD * kD * 4);
+        bulk_g2s(sR, a.vc.R, kD * kD * 4, &bar);
     }
-    // row maximum: thread t takes row t % 16 of splits t / 16, t / 16 + 24, ...
-    constexpr int kGroups = kThreads / kRows;
-    const int rr = tid % kRows;
+    tc::grid_wait_prior();  // the split kernel's partials
+    const int S = a.plan.splits;
+    const float* mlr = m.ml + (static_cast<int64_t>(unit) * S * kRows + r) * 2;     // split s at + s * 32
+    const float* pr = m.part + (static_cast<int64_t>(unit) * S * kRows + r) * kD + d;  // split s at + s * 16 D
+    // the row's maximum over the splits
     float mx = -INFINITY;
-    for (int s = tid / kRows; s < S; s += kGroups) mx = fmaxf(mx, __ldcg(mlu + (s * kRows + rr) * 2));
-    red[tid] = mx;  // = red[(tid / 16) * 16 + rr]
-    __syncthreads();
-    float M = -INFINITY;
+    for (int s = d; s < S; s += kMThreads) mx = fmaxf(mx, __ldcg(mlr + s * kRows * 2));
 #pragma unroll
-    for (int g2 = 0; g2 < kGroups; ++g2) M = fmaxf(M, red[g2 * kRows + rr]);
-    // float4 slots of the 16 x D output: slot sl = row * (D / 4) + column / 4;
-    // the first 256 threads take slots tid and tid + 256
-    constexpr int kSlots = kRows * kD / 4;
-    constexpr int kSlotThreads = kSlots / 2;
-    const bool slotter = tid < kSlotThreads;
-    const int sl0 = tid, sl1 = tid + kSlotThreads;
-    const int r0 = sl0 / (kD / 4), r1 = sl1 / (kD / 4);
-    float4 acc0 = make_float4(0.0f, 0.0f, 0.0f, 0.0f), acc1 = acc0;
-    float L = 0.0f;  // merged sum of row tid (threads tid < 16)
-    unsigned phase = 0;
-    for (int c0 = 0; c0 < S; c0 += NC) {
-        const int n = S - c0 < NC ? S - c0 : NC;
-        // weights of this chunk's splits (a split that saw no score has (-inf, 0)
-        // and a zero accumulator); entry i covers row i % 16 = tid % 16
-        for (int i = tid; i < n * kRows; i += kThreads) {
-            const float2 ml = __ldcg(reinterpret_cast<const float2*>(mlu + ((c0 + i / kRows) * kRows + rr) * 2));
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    if (lane == 0) sred[wid] = mx;
+    __syncthreads();
+    const float M = fmaxf(fmaxf(sred[0], sred[1]), fmaxf(sred[2], sred[3]));
+    __syncthreads();
+    float acc = 0.0f, lsum = 0.0f;
+    for (int s0 = 0; s0 < S; s0 += kMThreads) {
+        const int n = S - s0 < kMThreads ? S - s0 : kMThreads;
+        // weights of this chunk (a split that saw no score has (-inf, 0) and a
+        // zero accumulator); thread d's share of the merged sum
+        if (d < n) {
+            const float2 ml = __ldcg(reinterpret_cast<const float2*>(mlr + (s0 + d) * kRows * 2));
             const float w = ml.x == -INFINITY ? 0.0f : ex2(ml.x - M);
-            sw[i] = w;
-            swl[i] = w * ml.y;
+            sw[d] = w;
+            lsum = fmaf(w, ml.y, lsum);
         }
         __syncthreads();
-        if (!mbar_wait(bar, phase)) {
-            if (tid == 0) atomicOr(a.err, TQ_DEVERR_TIMEOUT);
-            (void)mbar_wait(bar, phase);
-        }
-        phase ^= 1u;
-        if (tid < kRows)
-            for (int s = 0; s < n; ++s) L += swl[s * kRows + tid];
-        if (slotter) {
-            const float4* sp4 = reinterpret_cast<const float4*>(sp);
-            for (int s = 0; s < n; ++s) {
-                const float w0 = sw[s * kRows + r0], w1 = sw[s * kRows + r1];
-                const float4 v0 = sp4[s * kSlots + sl0], v1 = sp4[s * kSlots + sl1];
-                acc0.x = fmaf(w0, v0.x, acc0.x); acc0.y = fmaf(w0, v0.y, acc0.y);
-                acc0.z = fmaf(w0, v0.z, acc0.z); acc0.w = fmaf(w0, v0.w, acc0.w);
-                acc1.x = fmaf(w1, v1.x, acc1.x); acc1.y = fmaf(w1, v1.y, acc1.y);
-                acc1.z = fmaf(w1, v1.z, acc1.z); acc1.w = fmaf(w1, v1.w, acc1.w);
-            }
-        }
-        tc::fence_proxy_async_smem();
-        __syncthreads();  // the chunk's buffers are rewritten below
-        if (c0 + NC < S && tid == 0) {
-            const int n1 = S - c0 - NC < NC ? S - c0 - NC : NC;
-            mbar_expect_tx(bar, n1 * kMergePartBytes);
-            bulk_g2s(sp, pu + static_cast<int64_t>(c0 + NC) * kRows * kD, n1 * kMergePartBytes, bar);
-        }
+        // the split loads are independent: unrolled so that they overlap
+#pragma unroll 8
+        for (int s = 0; s < n; ++s) acc = fmaf(sw[s], __ldcg(pr + static_cast<int64_t>(s0 + s) * kRows * kD), acc);
+        __syncthreads();
     }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, o);
+    if (lane == 0) sred[wid] = lsum;
+    __syncthreads();
+    const float L = (sred[0] + sred[1]) + (sred[2] + sred[3]);
     // MSE values were multiplied as fp16(op_scale * level): divide op_scale out
     const float vs = VGROUP ? 1.0f : a.vc.cq_scale;
+    const int gq = row / a.Lq, l = row % a.Lq;
+    const int64_t oo = (static_cast<int64_t>(b) * a.Hq + h * a.G + gq) * a.Lq + l;
     if (a.part_acc) {
         // a shard's state: max in natural-log units, sum, accumulator
-        const float iv = 1.0f / vs;
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-            const int sl = e ? sl1 : sl0;
-            const int row = rg * kRows + (e ? r1 : r0);
-            const float4 v = e ? acc1 : acc0;
-            if (slotter && row < a.plan.rows) {
-                const int gq = row / a.Lq, l = row % a.Lq;
-                const int64_t oo = (static_cast<int64_t>(b) * a.Hq + h * a.G + gq) * a.Lq + l;
-                reinterpret_cast<float4*>(a.part_acc + oo * kD)[sl % (kD / 4)] =
-                    make_float4(v.x * iv, v.y * iv, v.z * iv, v.w * iv);
-            }
-        }
-        const int row = rg * kRows + tid;
-        if (tid < kRows && row < a.plan.rows) {
-            const int gq = row / a.Lq, l = row % a.Lq;
-            const int64_t oo = (static_cast<int64_t>(b) * a.Hq + h * a.G + gq) * a.Lq + l;
+        a.part_acc[oo * kD + d] = acc * (1.0f / vs);
+        if (d == 0) {
             a.part_ml[2 * oo] = M == -INFINITY ? -INFINITY : M * 0.6931471805599453f;
             a.part_ml[2 * oo + 1] = L;
         }
-    } else {
-        if (tid < kRows) ssum[tid] = L > 0.0f ? 1.0f / (L * vs) : 0.0f;
-        __syncthreads();
-        // normalised rows (rotated domain), row stride kOS floats: over the
-        // first chunk's buffer (and the dead weights after it when one split)
-        constexpr int kOS = kD + 4;
-        float* orot = sp;
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-            const int sl = e ? sl1 : sl0, r = e ? r1 : r0;
-            const float iv = ssum[r];
-            const float4 v = e ? acc1 : acc0;
-            const float4 x = make_float4(v.x * iv, v.y * iv, v.z * iv, v.w * iv);
-            const int row = rg * kRows + r;
-            if (slotter && !rotate && row < a.plan.rows) {
-                const int gq = row / a.Lq, l = row % a.Lq;
-                reinterpret_cast<float4*>(a.out + ((static_cast<int64_t>(b) * a.Hq + h * a.G + gq) * a.Lq + l) *
-                                                      kD)[sl % (kD / 4)] = x;
-            }
-            if (slotter && rotate) reinterpret_cast<float4*>(orot + r * kOS)[sl % (kD / 4)] = x;
-        }
-        if (rotate) {
-            if (!mbar_wait(rbar, 0)) {
-                if (tid == 0) atomicOr(a.err, TQ_DEVERR_TIMEOUT);
-                (void)mbar_wait(rbar, 0);
-            }
-            __syncthreads();
-            // out = orot R_v: warp w < 8 takes columns 16 w .. 16 w + 15; lane
-            // (rb, cb) rows rb + 4 k (k < 4) at columns 16 w + 2 cb, + 1
-            const int warp = tid >> 5, lane = tid & 31;
-            if (warp < kD / 16) {
-                const int rb = lane >> 3, cb = lane & 7;
-                const int col = 16 * warp + 2 * cb;
-                float2 res[4];
-#pragma unroll
-                for (int k = 0; k < 4; ++k) res[k] = make_float2(0.0f, 0.0f);
-                const float4* o4 = reinterpret_cast<const float4*>(orot);
-#pragma unroll 2
-                for (int i4 = 0; i4 < kD / 4; ++i4) {
-                    float4 ov[4];
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) ov[k] = o4[(rb + 4 * k) * (kOS / 4) + i4];
-#pragma unroll
-                    for (int ii = 0; ii < 4; ++ii) {
-                        const float2 rv = *reinterpret_cast<const float2*>(sR + (4 * i4 + ii) * kD + col);
-#pragma unroll
-                        for (int k = 0; k < 4; ++k) {
-                            const float x = ii == 0 ? ov[k].x : ii == 1 ? ov[k].y : ii == 2 ? ov[k].z : ov[k].w;
-                            res[k].x = fmaf(x, rv.x, res[k].x);
-                            res[k].y = fmaf(x, rv.y, res[k].y);
-                        }
-                    }
-                }
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const int row = rg * kRows + rb + 4 * k;
-                    if (row < a.plan.rows) {
-                        const int gq = row / a.Lq, l = row % a.Lq;
-                        *reinterpret_cast<float2*>(
-                            a.out + ((static_cast<int64_t>(b) * a.Hq + h * a.G + gq) * a.Lq + l) * kD + col) = res[k];
-                    }
-                }
-            }
-        }
+        return;
     }
-    if (tid == 0) {
-        m.cnt[unit] = 0u;
-        mbar_inval(bar);
-        if (rotate) mbar_inval(rbar);
+    const float x = L > 0.0f ? acc * (1.0f / (L * vs)) : 0.0f;
+    if (!rotate) {
+        a.out[oo * kD + d] = x;
+        return;
     }
+    so[d] = x;
+    __syncthreads();
+    if (!mbar_wait(&bar, 0)) {
+        if (d == 0) atomicOr(a.err, TQ_DEVERR_TIMEOUT);
+        (void)mbar_wait(&bar, 0);
+    }
+    // out[d] = sum_i row[i] R_v[i][d]: R_v's row i is one contiguous load, the
+    // merged row's values are broadcasts (four at a time)
+    float y0 = 0.0f, y1 = 0.0f;
+    const float4* so4 = reinterpret_cast<const float4*>(so);
+#pragma unroll 4
+    for (int i4 = 0; i4 < kD / 4; ++i4) {
+        const float4 v = so4[i4];
+        y0 = fmaf(v.x, sR[(4 * i4) * kD + d], y0);
+        y1 = fmaf(v.y, sR[(4 * i4 + 1) * kD + d], y1);
+        y0 = fmaf(v.z, sR[(4 * i4 + 2) * kD + d], y0);
+        y1 = fmaf(v.w, sR[(4 * i4 + 3) * kD + d], y1);
+    }
+    a.out[oo * kD + d] = y0 + y1;
+    if (d == 0) mbar_inval(&bar);
+}
+
+// Dynamic shared memory of merge_rows_kernel.
+inline size_t merge_rows_smem(bool rotate) {
+    return (rotate ? static_cast<size_t>(kD) * kD * 4 : 0) + (kD + 2 * kMThreads) * 4;
 }
 
 template <int KB, bool KPROD, bool VGROUP, int VB>
@@ -819,10 +728,10 @@ __global__ void __launch_bounds__(kThreads, 1) split_mma_kernel(MmaArgs m) {
                 if constexpr (KPROD) {
                     // codebook part + residual norm x QJL part, per token column
                     const float2 gm = *reinterpret_cast<const float2*>(krn + base + 8 * nt + 2 * j);
-                    sc[nt][0] = fmaf(gm.x, sd[nt][0], sc[nt][0]);
-                    sc[nt][1] = fmaf(gm.y, sd[nt][1], sc[nt][1]);
-                    sc[nt][2] = fmaf(gm.x, sd[nt][2], sc[nt][2]);
-                    sc[nt][3] = fmaf(gm.y, sd[nt][3], sc[nt][3]);
+                    // (two tokens' columns per packed fp32 pair operation)
+                    const float2 lo = __ffma2_rn(gm, make_float2(sd[nt][0], sd[nt][1]), make_float2(sc[nt][0], sc[nt][1]));
+                    const float2 hi = __ffma2_rn(gm, make_float2(sd[nt][2], sd[nt][3]), make_float2(sc[nt][2], sc[nt][3]));
+                    sc[nt][0] = lo.x; sc[nt][1] = lo.y; sc[nt][2] = hi.x; sc[nt][3] = hi.y;
                 } else {
 #pragma unroll
                     for (int e = 0; e < 4; ++e) sc[nt][e] += sd[nt][e];
@@ -835,10 +744,9 @@ __global__ void __launch_bounds__(kThreads, 1) split_mma_kernel(MmaArgs m) {
                 const float2 kn = *reinterpret_cast<const float2*>(knorm + base + 8 * nt + 2 * j);
                 if constexpr (!VGROUP) nv[nt] = *reinterpret_cast<const float2*>(vnorm + base + 8 * nt + 2 * j);
                 else nv[nt] = make_float2(0.0f, 0.0f);
-                sc[nt][0] *= kn.x;
-                sc[nt][1] *= kn.y;
-                sc[nt][2] *= kn.x;
-                sc[nt][3] *= kn.y;
+                const float2 lo = __fmul2_rn(make_float2(sc[nt][0], sc[nt][1]), kn);
+                const float2 hi = __fmul2_rn(make_float2(sc[nt][2], sc[nt][3]), kn);
+                sc[nt][0] = lo.x; sc[nt][1] = lo.y; sc[nt][2] = hi.x; sc[nt][3] = hi.y;
             }
             // masks only where the step reaches past the tile's end or a row's
             // causal limit (past the end, the stage holds stale bytes: their
@@ -893,32 +801,36 @@ __global__ void __launch_bounds__(kThreads, 1) split_mma_kernel(MmaArgs m) {
             // its p enters the row sums in the rare branch below.
             uint32_t pa[NT][2];
             [[maybe_unused]] bool zero = false;
+            const float2 nm0 = make_float2(-mrow0, -mrow0), nm1 = make_float2(-mrow1, -mrow1);
+            float2 lsum = make_float2(0.0f, 0.0f);  // this step's (row g, row g + 8) sums
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
-                float w0 = ex2(sc[nt][0] - mrow0), w1 = ex2(sc[nt][1] - mrow0);
-                float w2 = ex2(sc[nt][2] - mrow1), w3 = ex2(sc[nt][3] - mrow1);
+                const float2 x0 = __fadd2_rn(make_float2(sc[nt][0], sc[nt][1]), nm0);
+                const float2 x1 = __fadd2_rn(make_float2(sc[nt][2], sc[nt][3]), nm1);
+                float2 w01 = make_float2(ex2(x0.x), ex2(x0.y));
+                float2 w23 = make_float2(ex2(x1.x), ex2(x1.y));
                 float r0 = 1.0f, r1 = 1.0f;
                 if constexpr (!VGROUP) {
                     const float nx = nv[nt].x, ny = nv[nt].y;
                     zero |= !(fminf(nx, ny) > 0.0f);
                     r0 = rcp_approx(fmaxf(nx, 1e-30f));
                     r1 = rcp_approx(fmaxf(ny, 1e-30f));
-                    sc[nt][0] = w0;  // keep p for the zero-norm branch
-                    sc[nt][1] = w1;
-                    sc[nt][2] = w2;
-                    sc[nt][3] = w3;
-                    w0 *= nx;
-                    w1 *= ny;
-                    w2 *= nx;
-                    w3 *= ny;
+                    sc[nt][0] = w01.x;  // keep p for the zero-norm branch
+                    sc[nt][1] = w01.y;
+                    sc[nt][2] = w23.x;
+                    sc[nt][3] = w23.y;
+                    w01 = __fmul2_rn(w01, nv[nt]);
+                    w23 = __fmul2_rn(w23, nv[nt]);
                 }
-                pa[nt][0] = pack_half2(w0, w1);
-                pa[nt][1] = pack_half2(w2, w3);
+                pa[nt][0] = pack_half2(w01.x, w01.y);
+                pa[nt][1] = pack_half2(w23.x, w23.y);
                 const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&pa[nt][0]));
                 const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&pa[nt][1]));
-                lrow0 += f0.x * r0 + f0.y * r1;
-                lrow1 += f1.x * r0 + f1.y * r1;
+                lsum = __ffma2_rn(make_float2(f0.x, f1.x), make_float2(r0, r0), lsum);
+                lsum = __ffma2_rn(make_float2(f0.y, f1.y), make_float2(r1, r1), lsum);
             }
+            lrow0 += lsum.x;
+            lrow1 += lsum.y;
             if constexpr (!VGROUP) {
                 if (__any_sync(0xffffffffu, zero)) {
 #pragma unroll
@@ -1016,12 +928,36 @@ __global__ void __launch_bounds__(kThreads, 1) split_mma_kernel(MmaArgs m) {
             mlp[1] = L;
         }
     }
-    merge_unit<VGROUP>(m, unit, rg, b, h, smem, tid);
 }
 
 // Query prep fused with the short encode of a decode step's new tokens
 // (decode_step.cu): one launch in place of the append and the query prep.
 cudaError_t launch_step_prep(int kb, bool nat, const MmaArgs& m, const EncodeAppendArgs& e, cudaStream_t s);
+
+// The merge kernel after a split kernel: one CTA per (unit, row).
+template <bool VGROUP>
+cudaError_t launch_merge(const MmaArgs& m, cudaStream_t s) {
+    const DecodeArgs& a = m.a;
+    const bool rotate = !VGROUP && !a.part_acc;
+    const size_t smem = merge_rows_smem(rotate);
+    static std::atomic<uint64_t> attr_set{0};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const uint64_t bit = 1ull << (dev & 63);
+    if (!(attr_set.load() & bit)) {
+        const cudaError_t e = cudaFuncSetAttribute(merge_rows_kernel<VGROUP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                   static_cast<int>(merge_rows_smem(true)));
+        if (e != cudaSuccess) {
+            (void)cudaGetLastError();
+            return e;
+        }
+        attr_set.fetch_or(bit);
+    }
+    const int units = a.batch * a.pool.Hkv * a.plan.row_groups;
+    const cudaError_t e = launch_overlapped(merge_rows_kernel<VGROUP>, dim3(units, kRows), dim3(kMThreads), smem, s, m);
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    return e;
+}
 
 template <int KB, bool KPROD, bool VGROUP, int VB>
 cudaError_t launch_mma(const MmaArgs& m, size_t smem, cudaStream_t s, const EncodeAppendArgs* step) {
@@ -1058,7 +994,8 @@ cudaError_t launch_mma(const MmaArgs& m, size_t smem, cudaStream_t s, const Enco
         e = launch_overlapped(split_mma_kernel<KB, KPROD, VGROUP, VB>, dim3(a.plan.splits, a.pool.Hkv * RG, a.batch),
                               dim3(kThreads), smem, s, m);
         g_launches.fetch_add(1, std::memory_order_relaxed);
-        return e;
+        if (e != cudaSuccess) return e;
+        return launch_merge<VGROUP>(m, s);
     }
     static std::atomic<uint64_t> qattr_set{0};
     if (!(qattr_set.load() & bit)) {
@@ -1079,7 +1016,8 @@ cudaError_t launch_mma(const MmaArgs& m, size_t smem, cudaStream_t s, const Enco
     e = launch_overlapped(split_mma_kernel<KB, KPROD, VGROUP, VB>, dim3(a.plan.splits, a.pool.Hkv * RG, a.batch),
                           dim3(kThreads), smem, s, m);
     g_launches.fetch_add(1, std::memory_order_relaxed);
-    return e;
+    if (e != cudaSuccess) return e;
+    return launch_merge<VGROUP>(m, s);
 }
 
 }  // namespace mmadec

@@ -656,7 +656,6 @@ cudaError_t launch_prefill_tc_t(const TcPrefillArgs& P, size_t smem, cudaStream_
     MmaArgs m{};
     m.a = a;
     m.qfrag = P.qfrag;
-    m.cnt = nullptr;
     qfrag_kernel<KB><<<dim3(qfrag_grid(a.batch * a.pool.Hkv * RG)), kQThreads, sizeof(QSmem), s>>>(m);
     g_launches.fetch_add(1, std::memory_order_relaxed);
     const int gx = (RG + 7) / 8;

@@ -107,10 +107,8 @@ struct DecodePlan {
     int qs_off;       // shared-memory offset of the query fragments
     int vt_off;       // shared-memory offset of the 3-bit value pair table region (-1: unused)
     int kt_off;       // shared-memory offset of the 2-bit key quad table (-1: unused)
-    int merge_splits; // splits the last CTA of a unit stages in shared memory at once
     size_t smem;      // dynamic shared memory of the split kernel
     size_t q_bytes;   // SIMT: q' and q'' buffers (each); tensor cores: query fragments
-    size_t cnt_bytes; // tensor cores: per-unit arrival counters
     size_t part_bytes;// partial accumulators
     size_t ml_bytes;  // partial (max, sum)
     size_t total;
