@@ -171,16 +171,12 @@ __device__ __forceinline__ void qfrag_body(const MmaArgs& m, unsigned char* qsm_
         __syncthreads();
         q_split_rows(sm, &sm.q2[0][0], tid);
         if (first) {
-            first = false;
             const bool ok = mbar_wait(&sm.bar, 0);
-            // the workspace is written below: the kernels before this one are done
-            // (the append before it waits for the decode before that); the split
-            // kernel may then start fetching records, which are all written by now
-            tc::grid_wait_prior();
-            tc::grid_release_dependents();
             if (__syncthreads_or(!ok)) {
                 if (tid == 0) atomicOr(a.err, TQ_DEVERR_TIMEOUT);
                 (void)mbar_wait(&sm.bar, 0);
+                tc::grid_wait_prior();
+                tc::grid_release_dependents();
                 return;
             }
         }
@@ -194,6 +190,16 @@ __device__ __forceinline__ void qfrag_body(const MmaArgs& m, unsigned char* qsm_
             __syncthreads();
             q_gemm(sm, sm.S, 1.0f, &sm.q2[0][0], warp, lane);
             __syncthreads();
+        }
+        if (first) {
+            first = false;
+            // the workspace is written below: wait until the kernels before this
+            // one are done (the queries and tables it has read so far are no
+            // kernel's output in this chain; the append before it waits for the
+            // decode before that); the split kernel may then start fetching
+            // records, which are all written by now
+            tc::grid_wait_prior();
+            tc::grid_release_dependents();
         }
         // entry (row rr, which, ks, j, e): lane 4*(rr%8)+j, register 2e + (rr >= 8)
         // the key codebook operand is fp16(op_scale * level): the q' operand
@@ -377,32 +383,54 @@ __global__ void __launch_bounds__(kMThreads) merge_rows_kernel(MmaArgs m) {
     const int S = a.plan.splits;
     const float* mlr = m.ml + (static_cast<int64_t>(unit) * S * kRows + r) * 2;     // split s at + s * 32
     const float* pr = m.part + (static_cast<int64_t>(unit) * S * kRows + r) * kD + d;  // split s at + s * 16 D
+    // every load of the first kMPre splits issued at once (one L2 round trip):
+    // thread d's column of each split's accumulator, and the (max, sum) of
+    // split d
+    constexpr int kMPre = 32;
+    float pv[kMPre];
+#pragma unroll
+    for (int s = 0; s < kMPre; ++s) pv[s] = s < S ? __ldcg(pr + static_cast<int64_t>(s) * kRows * kD) : 0.0f;
+    float2 myml = make_float2(-INFINITY, 0.0f);
+    if (d < S) myml = __ldcg(reinterpret_cast<const float2*>(mlr + d * kRows * 2));
     // the row's maximum over the splits
-    float mx = -INFINITY;
-    for (int s = d; s < S; s += kMThreads) mx = fmaxf(mx, __ldcg(mlr + s * kRows * 2));
+    float mx = myml.x;
+    for (int s = d + kMThreads; s < S; s += kMThreads) mx = fmaxf(mx, __ldcg(mlr + s * kRows * 2));
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
     if (lane == 0) sred[wid] = mx;
     __syncthreads();
     const float M = fmaxf(fmaxf(sred[0], sred[1]), fmaxf(sred[2], sred[3]));
+    // weights 2^(m - M) of the first kMThreads splits (a split that saw no
+    // score has (-inf, 0) and a zero accumulator); thread d's share of the sum
+    float lsum = 0.0f;
+    if (d < S) {
+        const float w = myml.x == -INFINITY ? 0.0f : ex2(myml.x - M);
+        sw[d] = w;
+        lsum = w * myml.y;
+    }
     __syncthreads();
-    float acc = 0.0f, lsum = 0.0f;
+    float acc = 0.0f;
+#pragma unroll
+    for (int s = 0; s < kMPre; ++s)
+        if (s < S) acc = fmaf(sw[s], pv[s], acc);
+    // splits past the first kMPre (long sequences over few units)
     for (int s0 = 0; s0 < S; s0 += kMThreads) {
         const int n = S - s0 < kMThreads ? S - s0 : kMThreads;
-        // weights of this chunk (a split that saw no score has (-inf, 0) and a
-        // zero accumulator); thread d's share of the merged sum
-        if (d < n) {
-            const float2 ml = __ldcg(reinterpret_cast<const float2*>(mlr + (s0 + d) * kRows * 2));
-            const float w = ml.x == -INFINITY ? 0.0f : ex2(ml.x - M);
-            sw[d] = w;
-            lsum = fmaf(w, ml.y, lsum);
+        if (s0 > 0) {
+            __syncthreads();
+            if (d < n) {
+                const float2 ml = __ldcg(reinterpret_cast<const float2*>(mlr + (s0 + d) * kRows * 2));
+                const float w = ml.x == -INFINITY ? 0.0f : ex2(ml.x - M);
+                sw[d] = w;
+                lsum = fmaf(w, ml.y, lsum);
+            }
+            __syncthreads();
         }
-        __syncthreads();
-        // the split loads are independent: unrolled so that they overlap
 #pragma unroll 8
-        for (int s = 0; s < n; ++s) acc = fmaf(sw[s], __ldcg(pr + static_cast<int64_t>(s0 + s) * kRows * kD), acc);
-        __syncthreads();
+        for (int s = s0 > 0 ? 0 : kMPre; s < n; ++s)
+            acc = fmaf(sw[s], __ldcg(pr + static_cast<int64_t>(s0 + s) * kRows * kD), acc);
     }
+    __syncthreads();
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, o);
     if (lane == 0) sred[wid] = lsum;
