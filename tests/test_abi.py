@@ -163,10 +163,11 @@ def test_decode_plan_of_the_bench_configuration(libtq):
     # keys prod 3-bit, values MSE 3-bit, 256-token blocks, GQA 8 x q_len 2 at
     # 256k on 152 SMs: 64-token tiles, 19 splits, 12 warps x 2 stages x 6912 B
     # + 8 KB query fragments + 16 KB value pair region + 32 KB key quad table
+    # + 24 stage barriers and the tables' barrier
     d = _desc_from_oracle(128, ("prod", 3), ("mse", 3, 0), 256, 8)
     p = tq.tq_decode_plan(d, 1, 64, 2, 262146, 152)
     assert p["tile_tokens"] == 64 and p["splits"] == 19 and p["row_groups"] == 1
-    assert p["smem_bytes"] == 12 * 2 * 6912 + 8192 + 16384 + 32768 + 12 * 2 * 8
+    assert p["smem_bytes"] == 12 * 2 * 6912 + 8192 + 16384 + 32768 + (12 * 2 + 1) * 8
     # a record pair too large for 64-token stages next to the tables: 32-token tiles
     d = _desc_from_oracle(128, ("prod", 4), ("group", 4, 32), 256, 8)
     assert tq.tq_decode_plan(d, 1, 64, 2, 4096, 152)["tile_tokens"] == 32

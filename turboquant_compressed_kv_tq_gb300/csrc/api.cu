@@ -67,6 +67,8 @@ void free_codec(tq_codec* c) {
     cudaFree(c->d_cq);
     cudaFree(c->d_Rtc);
     cudaFree(c->d_Stc);
+    cudaFree(c->d_quad);
+    cudaFree(c->d_pair);
     if (prev >= 0) cudaSetDevice(prev);
     delete c;
 }
@@ -78,6 +80,39 @@ tq_status upload(T** dst, const std::vector<T>& src) {
     if (cudaMemcpy(*dst, src.data(), src.size() * sizeof(T), cudaMemcpyHostToDevice) != cudaSuccess)
         return TQ_ERR_CUDA;
     return TQ_OK;
+}
+
+// fp16 bits of a float that is exactly an fp16 value (the operand levels are)
+uint32_t half_bits_exact(float f) {
+    uint32_t u;
+    std::memcpy(&u, &f, 4);
+    const uint32_t sign = (u >> 16) & 0x8000u;
+    const int e = static_cast<int>((u >> 23) & 0xFFu) - 127;
+    const uint32_t mant = u & 0x7FFFFFu;
+    if ((u & 0x7FFFFFFFu) == 0) return sign;
+    if (e >= -14) return sign | (static_cast<uint32_t>(e + 15) << 10) | (mant >> 13);
+    return sign | ((mant | 0x800000u) >> (-e - 1));  // subnormal half: value 2^-24 x m
+}
+
+// Decode lookup tables of an MSE codebook in the split kernel's shared-memory
+// layout (bank copies included): code quads for 2 index bits, code pairs for 3.
+std::vector<uint32_t> quad_table(const std::vector<float>& cq) {
+    std::vector<uint32_t> t(256 * 16 * 2);
+    for (int i = 0; i < 256 * 16; ++i) {
+        const int e = i >> 4;
+        t[2 * i] = half_bits_exact(cq[e & 3]) | (half_bits_exact(cq[(e >> 2) & 3]) << 16);
+        t[2 * i + 1] = half_bits_exact(cq[(e >> 4) & 3]) | (half_bits_exact(cq[e >> 6]) << 16);
+    }
+    return t;
+}
+
+std::vector<uint32_t> pair_table(const std::vector<float>& cq) {
+    std::vector<uint32_t> t(64 * 32);
+    for (int i = 0; i < 64 * 32; ++i) {
+        const int e = i >> 5;
+        t[i] = half_bits_exact(cq[e & 7]) | (half_bits_exact(cq[e >> 3]) << 16);
+    }
+    return t;
 }
 
 std::vector<float> transpose(const std::vector<float>& a, int D) {
@@ -98,6 +133,8 @@ CodecDev dev_view(const tq_codec* c) {
     d.cq_scale = c->host.op_scale;
     d.Rtc = c->d_Rtc;
     d.Stc = c->d_Stc;
+    d.quad = c->d_quad;
+    d.pair = c->d_pair;
     d.D = c->head_dim;
     d.mode = c->mode;
     d.bits = c->bits;
@@ -251,6 +288,8 @@ tq_status tq_codec_create(int head_dim, int bits, tq_mode mode, uint64_t seed, t
     if (st == TQ_OK) st = upload(&c->d_c, c->host.centroids);
     if (st == TQ_OK) st = upload(&c->d_m, c->host.midpoints);
     if (st == TQ_OK) st = upload(&c->d_cq, c->host.op_levels);
+    if (st == TQ_OK && c->index_bits == 2) st = upload(&c->d_quad, quad_table(c->host.op_levels));
+    if (st == TQ_OK && c->index_bits == 3) st = upload(&c->d_pair, pair_table(c->host.op_levels));
     if (st == TQ_OK && head_dim <= 128) {
         // tensor-core operands for the chunked-prefill encoder: 16 R and S, fp16 hi + lo
         std::vector<uint16_t> op;

@@ -494,7 +494,7 @@ DecodePlan make_decode_plan(const tq_cache_desc* d, int batch, int G, int Lq, in
             const size_t combine = mmadec::kWarpMergeBytes;
             const size_t body = ((ringq > combine ? ringq : combine) + 127) / 128 * 128;
             p.bar_off = static_cast<int>(body);
-            p.smem = body + sizeof(uint64_t) * mmadec::kWarps * mmadec::kStages;
+            p.smem = body + sizeof(uint64_t) * (mmadec::kWarps * mmadec::kStages + 1);  // + the tables' barrier
         };
         // 64-token tiles; a tile gathers up to four shorter blocks (one copy per
         // block and record stream)

@@ -517,34 +517,53 @@ __global__ void __launch_bounds__(kThreads, 1) split_mma_kernel(MmaArgs m) {
     }
     __syncwarp();
 
+    // Barrier of the lookup tables (bulk-copied from the codec's prebuilt copy
+    // at once) and the query fragments (copied after the wait below): two
+    // arrivals, one per copy group.
+    uint64_t* tbar = reinterpret_cast<uint64_t*>(smem + st.bar_off) + kWarps * kStages;
     // 2-bit keys decode through the shared quad table, others in registers
     constexpr bool kQuadTab = quad_keys(KB, KPROD, VGROUP);
+    // 3-bit MSE values decode through the shared pair table, others in registers
+    constexpr bool kPairTab = !VGROUP && VB == 3;
+    uint32_t pair_off = 0;  // the pair table's offset: 8 KB-aligned shared address inside its region
+    if constexpr (kPairTab) {
+        const uint32_t region = smem_u32(smem + st.vt_off);
+        pair_off = st.vt_off + (((region + kVPairBytes - 1) & ~static_cast<uint32_t>(kVPairBytes - 1)) - region);
+    }
+    const bool quad_copy = kQuadTab && a.kc.quad, pair_copy = kPairTab && a.vc.pair;
+    if (threadIdx.x == 0) {
+        mbar_init(tbar, 2);
+        mbar_fence_init();
+        mbar_expect_tx(tbar, (quad_copy ? kKQuadBytes : 0) + (pair_copy ? kVPairBytes : 0));
+        if (quad_copy) bulk_g2s(smem + st.kt_off, a.kc.quad, kKQuadBytes, tbar);
+        if (pair_copy) bulk_g2s(smem + pair_off, a.vc.pair, kVPairBytes, tbar);
+    }
     typename MseTable<KB>::type ktab{};
     if constexpr (!kQuadTab) ktab = mse_table<KB>(a.kc.cq);
     uint32_t kt_lane = 0;
     if constexpr (kQuadTab) {
         kt_lane = smem_u32(smem + st.kt_off) + 8u * (lane & 15);
-        uint2* tab = reinterpret_cast<uint2*>(smem + st.kt_off);
-        for (int i = threadIdx.x; i < 256 * 16; i += kThreads) {
-            const int e = i >> 4;
-            const uint32_t c0 = h_bits(__ldg(a.kc.cq + (e & 3))), c1 = h_bits(__ldg(a.kc.cq + ((e >> 2) & 3)));
-            const uint32_t c2 = h_bits(__ldg(a.kc.cq + ((e >> 4) & 3))), c3 = h_bits(__ldg(a.kc.cq + (e >> 6)));
-            tab[i] = make_uint2(c0 | (c1 << 16), c2 | (c3 << 16));
+        if (!quad_copy) {  // a codec without the prebuilt table: build it here
+            uint2* tab = reinterpret_cast<uint2*>(smem + st.kt_off);
+            for (int i = threadIdx.x; i < 256 * 16; i += kThreads) {
+                const int e = i >> 4;
+                const uint32_t c0 = h_bits(__ldg(a.kc.cq + (e & 3))), c1 = h_bits(__ldg(a.kc.cq + ((e >> 2) & 3)));
+                const uint32_t c2 = h_bits(__ldg(a.kc.cq + ((e >> 4) & 3))), c3 = h_bits(__ldg(a.kc.cq + (e >> 6)));
+                tab[i] = make_uint2(c0 | (c1 << 16), c2 | (c3 << 16));
+            }
         }
     }
-    // 3-bit MSE values decode through the shared pair table, others in registers
-    constexpr bool kPairTab = !VGROUP && VB == 3;
     typename MseTable<VGROUP ? 2 : VB>::type vtab{};
     if constexpr (!VGROUP && !kPairTab) vtab = mse_table<VB>(a.vc.cq);
     uint32_t vt_lane = 0;
     if constexpr (kPairTab) {
-        const uint32_t region = smem_u32(smem + st.vt_off);
-        const uint32_t base = (region + kVPairBytes - 1) & ~static_cast<uint32_t>(kVPairBytes - 1);
-        vt_lane = base + 4u * lane;
-        uint32_t* tab = reinterpret_cast<uint32_t*>(smem + st.vt_off + (base - region));
-        for (int i = threadIdx.x; i < 64 * 32; i += kThreads) {
-            const int e = i >> 5;
-            tab[i] = h_bits(__ldg(a.vc.cq + (e & 7))) | (h_bits(__ldg(a.vc.cq + (e >> 3))) << 16);
+        vt_lane = smem_u32(smem + pair_off) + 4u * lane;
+        if (!pair_copy) {
+            uint32_t* tab = reinterpret_cast<uint32_t*>(smem + pair_off);
+            for (int i = threadIdx.x; i < 64 * 32; i += kThreads) {
+                const int e = i >> 5;
+                tab[i] = h_bits(__ldg(a.vc.cq + (e & 7))) | (h_bits(__ldg(a.vc.cq + (e >> 3))) << 16);
+            }
         }
     }
 
@@ -633,12 +652,16 @@ __global__ void __launch_bounds__(kThreads, 1) split_mma_kernel(MmaArgs m) {
     tc::grid_wait_prior();
     for (int i = 0; i < pre; ++i)
         if (!early(i)) issue(i);
-    {
-        const uint4* qf = m.qfrag + static_cast<int64_t>(unit) * 2 * 8 * 32;
-        uint4* qd = reinterpret_cast<uint4*>(smem + st.qs_off);
-        for (int k = threadIdx.x; k < 2 * 8 * 32; k += kThreads) qd[k] = qf[k];
+    if (threadIdx.x == 0) {
+        tc::fence_proxy_async_global();
+        mbar_expect_tx(tbar, kQFragBytes);
+        bulk_g2s(smem + st.qs_off, m.qfrag + static_cast<int64_t>(unit) * 2 * 8 * 32, kQFragBytes, tbar);
     }
-    __syncthreads();
+    __syncthreads();  // the barrier's initialisation and any tables built here
+    if (!mbar_wait(tbar, 0)) {
+        if (threadIdx.x == 0) atomicOr(a.err, TQ_DEVERR_TIMEOUT);
+        (void)mbar_wait(tbar, 0);  // no copy may still be in flight below
+    }
     int waited = 0;
     for (int i = 0; i < my_n; ++i) {
         if (i + kStages - 1 < my_n) {
@@ -899,6 +922,7 @@ __global__ void __launch_bounds__(kThreads, 1) split_mma_kernel(MmaArgs m) {
     __syncwarp();
     if (lane == 0)
         for (int s = 0; s < kStages; ++s) mbar_inval(&bars[s]);
+    if (threadIdx.x == 0) mbar_inval(tbar);
 
     // ---------------- merge the warps of this CTA
     lrow0 += __shfl_xor_sync(0xffffffffu, lrow0, 1);

@@ -46,6 +46,13 @@ struct CodecDev {
     float cq_scale;    // op_scale
     const uint16_t* Rtc;  // tensor-core operand of 16 R (hi, lo), or nullptr
     const uint16_t* Stc;  // tensor-core operand of S (hi, lo) (prod), or nullptr
+    // decode lookup tables in their shared-memory layout (copied as they are),
+    // or nullptr: 2-bit code quads, entry e (a byte of four codes) at
+    // 128 e + 8 c for bank copy c < 16, fp16 pairs (cq[e & 3], cq[(e >> 2) & 3]),
+    // (cq[(e >> 4) & 3], cq[e >> 6]); 3-bit code pairs, entry e (six bits) at
+    // 128 e + 4 c for bank copy c < 32, fp16 pair (cq[e & 7], cq[e >> 3])
+    const uint32_t* quad;
+    const uint32_t* pair;
     int D;
     int mode;          // tq_mode
     int bits;          // total bits
@@ -249,4 +256,6 @@ struct tq_codec {
     float* d_cq = nullptr;
     uint16_t* d_Rtc = nullptr;
     uint16_t* d_Stc = nullptr;
+    uint32_t* d_quad = nullptr;  // decode lookup table of 2-bit code quads (index bits 2)
+    uint32_t* d_pair = nullptr;  // decode lookup table of 3-bit code pairs (index bits 3)
 };
