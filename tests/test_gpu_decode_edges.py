@@ -4,7 +4,7 @@ Token counts around the 64-token tiles and 128-token blocks (only the query
 positions, a tile minus one, exactly one tile, one over) for every codec pair
 of the prefill kernels, 128- to 512-token blocks in a shuffled order, causal
 query lengths above one, more than 16 query rows (two row groups), a sequence
-long enough for many token splits, per-head scales, and inputs with zero,
+long enough for many token splits (past one merge chunk), per-head scales, and inputs with zero,
 tiny and one-hot vectors (zero-norm values, zero keys). Every output row is
 compared with the oracle's decode of the same raw inputs (the max abs error
 and cosine bounds of the decode parity rule); the last case checks that two
@@ -78,6 +78,24 @@ def test_two_row_groups_causal():
 def test_many_splits_long_sequence():
     # one KV head: the plan spreads 40,000 tokens over many token splits
     _check(_workload(("prod", 3), ("mse", 3), (40000,), 2, 1, 8, 256))
+
+
+def test_splits_beyond_one_merge_chunk():
+    # one KV head at 150,000 tokens: more than 128 token splits, so the merge
+    # goes past the 32 splits whose loads it issues at once and past its first
+    # chunk of 128 split weights
+    w = _workload(("prod", 3), ("mse", 3), (150000,), 2, 1, 8, 256)
+    case = GpuCase(w, layers=[0])
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    plan = tq.tq_decode_plan(case.cache.desc, 1, w.num_q_heads, w.q_len, w.seq_lens[0], sms)
+    assert plan["splits"] > 128, plan
+    case.prefill()
+    q = wl.queries(w, 0, 0, DEV)
+    out = to_f32_np(case.decode(0, q))
+    assert tq.tq_device_error() == 0
+    qn = to_f32_np(q).astype(np.float64)
+    K, V = raw_kv(w, 0, 0, w.seq_lens[0], DEV)
+    compare_decode(out[0], oracle_decode(w, K[0], V[0], qn[0]))
 
 
 def test_head_scales_mse4():

@@ -44,6 +44,7 @@ CASES = [
     (128, ("mse", 4), ("mse", 4), 2, 8, 2, 700, (0, 699, 700)),             # last shard shorter than q_len
     (128, ("prod", 3), ("group", 4, 64), 2, 4, 1, 900, (0, 0, 450, 900)),   # an empty shard
     (256, ("prod", 3), ("group", 2, 32), 2, 8, 1, 1000, (0, 600, 1000)),    # head_dim 256 (SIMT kernels)
+    (128, ("prod", 3), ("mse", 3), 1, 8, 2, 160000, (0, 10000, 160000)),    # one head: a shard of > 128 splits
 ]
 
 
