@@ -65,6 +65,17 @@ constexpr int kVPairRegion = 2 * kVPairBytes;
 // leave no room for it next to the 64-token stages.
 constexpr int kKQuadBytes = 256 * 16 * 8;
 __host__ __device__ constexpr bool quad_keys(int kb, bool kprod, bool vgroup) { return kb == 2 && !(kprod && vgroup); }
+// QJL sign operands through a shared table of sign nibbles (16 entries x 16
+// bank copies x 8 bytes), placed in the slack of the value pair table's
+// region: prod keys with 3-bit MSE values.
+constexpr int kQNibBytes = 16 * 16 * 8;
+__host__ __device__ constexpr bool nibble_qjl(bool kprod, bool vgroup, int vb) { return kprod && !vgroup && vb == 3; }
+// Coordinate order of the query fragments: bit 0 natural pair order of the
+// codebook part (quad-table keys), bit 1 natural pair order of the QJL part
+// (nibble-table signs); otherwise the byte-permute decoders' orders.
+__host__ __device__ constexpr int frag_order(int kb, bool kprod, bool vgroup, int vb) {
+    return (quad_keys(kb, kprod, vgroup) ? 1 : 0) | (nibble_qjl(kprod, vgroup, vb) ? 2 : 0);
+}
 
 // ------------------------------------------------------------------ PTX helpers
 

@@ -125,9 +125,10 @@ __device__ __forceinline__ void q_gemm(QSmem& sm, const uint16_t (*T)[kD * kD], 
 // per CTA by one bulk copy; per unit q' = Q R^T and q'' = q' S^T for the 16
 // rows on the tensor cores, both operands split into fp16 hi + lo (about 22
 // significant bits). Runs in a block of kQThreads threads.
-// NAT: 2-bit key codes in natural pair order (the split kernel's quad-table
-// decoder) instead of the byte-permute decoder's order.
-template <int KB, bool NAT = false>
+// ORD (frag_order): bit 0 puts the codebook part in natural pair order (the
+// split kernel's quad-table key decoder), bit 1 the QJL part (its nibble-table
+// sign decoder); otherwise the byte-permute decoders' orders.
+template <int KB, int ORD = 0>
 __device__ __forceinline__ void qfrag_body(const MmaArgs& m, unsigned char* qsm_raw, int cta, int ncta) {
     QSmem& sm = *reinterpret_cast<QSmem*>(qsm_raw);
     const DecodeArgs& a = m.a;
@@ -214,7 +215,7 @@ __device__ __forceinline__ void qfrag_body(const MmaArgs& m, unsigned char* qsm_
             const int reg = 2 * ee + (rr >= 8 ? 1 : 0);
             int pa, pb;
             const bool qjl = which && prod;
-            if (NAT && !qjl) {
+            if (qjl ? (ORD & 2) != 0 : (ORD & 1) != 0) {
                 pa = 2 * (2 * ks + ee);
                 pb = pa + 1;
             } else {
@@ -237,10 +238,10 @@ __device__ __forceinline__ void qfrag_body(const MmaArgs& m, unsigned char* qsm_
     if (tid == 0) mbar_inval(&sm.bar);
 }
 
-template <int KB, bool NAT = false>
+template <int KB, int ORD = 0>
 __global__ void __launch_bounds__(kQThreads) qfrag_kernel(MmaArgs m) {
     extern __shared__ __align__(16) unsigned char qsm_raw[];
-    qfrag_body<KB, NAT>(m, qsm_raw, blockIdx.x, gridDim.x);
+    qfrag_body<KB, ORD>(m, qsm_raw, blockIdx.x, gridDim.x);
 }
 
 // CTAs of the query-prep kernel: one per unit up to one per SM.
@@ -553,6 +554,25 @@ __global__ void __launch_bounds__(kThreads, 1) split_mma_kernel(MmaArgs m) {
             }
         }
     }
+    // QJL signs of prod keys with 3-bit values: a table of sign nibbles in the
+    // slack of the pair table's region (a 2 KB-aligned 2 KB block: the larger
+    // slack, before or after the 8 KB-aligned pair table, holds one); entry e
+    // (four sign bits, a set bit is +1) copy c at 128 e + 8 c: the fp16 pairs
+    // (s0, s1), (s2, s3)
+    constexpr bool kNibQ = nibble_qjl(KPROD, VGROUP, VB);
+    uint32_t qn_lane = 0;
+    if constexpr (kNibQ) {
+        const uint32_t region = smem_u32(smem + st.vt_off);
+        const uint32_t pair_at = smem_u32(smem + pair_off);
+        const uint32_t nib = pair_at - region >= 4096u ? (region + 2047u) & ~2047u : pair_at + kVPairBytes;
+        qn_lane = nib + 8u * (lane & 15);
+        uint2* tab = reinterpret_cast<uint2*>(smem + st.vt_off + (nib - region));
+        for (int i = threadIdx.x; i < 16 * 16; i += kThreads) {
+            const int e = i >> 4;
+            auto pm = [&](int bit) { return (e >> bit) & 1 ? 0x3C00u : 0xBC00u; };
+            tab[i] = make_uint2(pm(0) | (pm(1) << 16), pm(2) | (pm(3) << 16));
+        }
+    }
     typename MseTable<VGROUP ? 2 : VB>::type vtab{};
     if constexpr (!VGROUP && !kPairTab) vtab = mse_table<VB>(a.vc.cq);
     uint32_t vt_lane = 0;
@@ -739,7 +759,13 @@ __global__ void __launch_bounds__(kThreads, 1) split_mma_kernel(MmaArgs m) {
 #pragma unroll
                     for (int nt = 0; nt < NT; ++nt) {
                         mma16816(sc[nt], qa, hk[nt][2 * e], hk[nt][2 * e + 1]);
-                        if constexpr (KPROD)
+                        if constexpr (KPROD && kNibQ) {
+                            // sign nibble ks of the lane's word at bits 7..10: a table address
+                            const uint32_t x = ks == 0 ? shl_f(sw[nt], 7)
+                                               : ks == 1 ? shl_f(sw[nt], 3) : (sw[nt] >> (4 * ks - 7));
+                            const uint2 sv = lds_u64((x & 0x780u) | qn_lane);
+                            mma16816(sd[nt], qj, sv.x, sv.y);
+                        } else if constexpr (KPROD)
                             mma16816(sd[nt], qj, dec1(sw[nt], 15 - ks, neg2), dec1(sw[nt], 7 - ks, neg2));
                         else
                             mma16816(sd[nt], qj, hk[nt][2 * e], hk[nt][2 * e + 1]);
@@ -984,7 +1010,7 @@ __global__ void __launch_bounds__(kThreads, 1) split_mma_kernel(MmaArgs m) {
 
 // Query prep fused with the short encode of a decode step's new tokens
 // (decode_step.cu): one launch in place of the append and the query prep.
-cudaError_t launch_step_prep(int kb, bool nat, const MmaArgs& m, const EncodeAppendArgs& e, cudaStream_t s);
+cudaError_t launch_step_prep(int kb, int ord, const MmaArgs& m, const EncodeAppendArgs& e, cudaStream_t s);
 
 // The merge kernel after a split kernel: one CTA per (unit, row).
 template <bool VGROUP>
@@ -1041,7 +1067,7 @@ cudaError_t launch_mma(const MmaArgs& m, size_t smem, cudaStream_t s, const Enco
     const int RG = a.plan.row_groups;
     cudaError_t e = cudaSuccess;
     if (step) {
-        e = launch_step_prep(KB, quad_keys(KB, KPROD, VGROUP), m, *step, s);
+        e = launch_step_prep(KB, frag_order(KB, KPROD, VGROUP, VB), m, *step, s);
         if (e != cudaSuccess) return e;
         e = launch_overlapped(split_mma_kernel<KB, KPROD, VGROUP, VB>, dim3(a.plan.splits, a.pool.Hkv * RG, a.batch),
                               dim3(kThreads), smem, s, m);
@@ -1051,7 +1077,7 @@ cudaError_t launch_mma(const MmaArgs& m, size_t smem, cudaStream_t s, const Enco
     }
     static std::atomic<uint64_t> qattr_set{0};
     if (!(qattr_set.load() & bit)) {
-        cudaError_t e = cudaFuncSetAttribute(qfrag_kernel<KB, quad_keys(KB, KPROD, VGROUP)>,
+        cudaError_t e = cudaFuncSetAttribute(qfrag_kernel<KB, frag_order(KB, KPROD, VGROUP, VB)>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              static_cast<int>(sizeof(QSmem)));
         if (e != cudaSuccess) {
@@ -1060,7 +1086,7 @@ cudaError_t launch_mma(const MmaArgs& m, size_t smem, cudaStream_t s, const Enco
         }
         qattr_set.fetch_or(bit);
     }
-    e = launch_overlapped(qfrag_kernel<KB, quad_keys(KB, KPROD, VGROUP)>, dim3(qfrag_grid(a.batch * a.pool.Hkv * RG)),
+    e = launch_overlapped(qfrag_kernel<KB, frag_order(KB, KPROD, VGROUP, VB)>, dim3(qfrag_grid(a.batch * a.pool.Hkv * RG)),
                           dim3(kQThreads),
                           sizeof(QSmem), s, m);
     g_launches.fetch_add(1, std::memory_order_relaxed);

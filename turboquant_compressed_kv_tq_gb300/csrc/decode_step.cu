@@ -16,11 +16,11 @@ namespace mmadec {
 // the encoder body needs one thread per coordinate
 static_assert(kQThreads >= kD, "the preparation block must cover head_dim threads");
 
-template <int KB, int NV, bool NAT>
+template <int KB, int NV, int ORD>
 __global__ void __launch_bounds__(kQThreads) step_prep_kernel(MmaArgs m, EncodeAppendArgs e, int nq) {
     extern __shared__ __align__(16) unsigned char smem[];
     if (static_cast<int>(blockIdx.x) < nq) {
-        qfrag_body<KB, NAT>(m, smem, blockIdx.x, nq);
+        qfrag_body<KB, ORD>(m, smem, blockIdx.x, nq);
         return;
     }
     const int u = blockIdx.x - nq;
@@ -33,7 +33,7 @@ __global__ void __launch_bounds__(kQThreads) step_prep_kernel(MmaArgs m, EncodeA
 
 namespace {
 
-template <int KB, int NV, bool NAT>
+template <int KB, int NV, int ORD>
 cudaError_t launch_prep(const MmaArgs& m, const EncodeAppendArgs& e, cudaStream_t s) {
     const size_t enc = encode_short_smem<kD, NV>(true);
     const size_t smem = sizeof(QSmem) > enc ? sizeof(QSmem) : enc;
@@ -42,7 +42,7 @@ cudaError_t launch_prep(const MmaArgs& m, const EncodeAppendArgs& e, cudaStream_
     cudaGetDevice(&dev);
     const uint64_t bit = 1ull << (dev & 63);
     if (!(attr_set.load() & bit)) {
-        const cudaError_t r = cudaFuncSetAttribute(step_prep_kernel<KB, NV, NAT>,
+        const cudaError_t r = cudaFuncSetAttribute(step_prep_kernel<KB, NV, ORD>,
                                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                    static_cast<int>(smem));
         if (r != cudaSuccess) {
@@ -58,28 +58,31 @@ cudaError_t launch_prep(const MmaArgs& m, const EncodeAppendArgs& e, cudaStream_
     int nq = qfrag_grid(units + ne) - ne;
     if (nq > units) nq = units;
     if (nq < 1) nq = 1;
-    const cudaError_t r = launch_overlapped(step_prep_kernel<KB, NV, NAT>, dim3(nq + ne), dim3(kQThreads), smem, s, m, e, nq);
+    const cudaError_t r = launch_overlapped(step_prep_kernel<KB, NV, ORD>, dim3(nq + ne), dim3(kQThreads), smem, s, m, e, nq);
     g_launches.fetch_add(1, std::memory_order_relaxed);
     return r;
 }
 
-template <int KB, bool NAT>
+template <int KB, int ORD>
 cudaError_t launch_prep_nv(const MmaArgs& m, const EncodeAppendArgs& e, cudaStream_t s) {
-    if (e.n_new <= 2) return launch_prep<KB, 2, NAT>(m, e, s);
-    if (e.n_new <= 8) return launch_prep<KB, 8, NAT>(m, e, s);
+    if (e.n_new <= 2) return launch_prep<KB, 2, ORD>(m, e, s);
+    if (e.n_new <= 8) return launch_prep<KB, 8, ORD>(m, e, s);
     return cudaErrorInvalidValue;
 }
 
 }  // namespace
 
-// nat: the query fragments in the natural pair order of the quad-table key
-// decoder (2-bit keys only).
-cudaError_t launch_step_prep(int kb, bool nat, const MmaArgs& m, const EncodeAppendArgs& e, cudaStream_t s) {
-    switch (kb) {
-        case 1: return launch_prep_nv<1, false>(m, e, s);
-        case 2: return nat ? launch_prep_nv<2, true>(m, e, s) : launch_prep_nv<2, false>(m, e, s);
-        case 3: return launch_prep_nv<3, false>(m, e, s);
-        case 4: return launch_prep_nv<4, false>(m, e, s);
+// ord: the query fragments' coordinate order (frag_order).
+cudaError_t launch_step_prep(int kb, int ord, const MmaArgs& m, const EncodeAppendArgs& e, cudaStream_t s) {
+    switch (kb * 4 + ord) {
+        case 1 * 4 + 0: return launch_prep_nv<1, 0>(m, e, s);
+        case 1 * 4 + 2: return launch_prep_nv<1, 2>(m, e, s);
+        case 2 * 4 + 0: return launch_prep_nv<2, 0>(m, e, s);
+        case 2 * 4 + 1: return launch_prep_nv<2, 1>(m, e, s);
+        case 2 * 4 + 3: return launch_prep_nv<2, 3>(m, e, s);
+        case 3 * 4 + 0: return launch_prep_nv<3, 0>(m, e, s);
+        case 3 * 4 + 2: return launch_prep_nv<3, 2>(m, e, s);
+        case 4 * 4 + 0: return launch_prep_nv<4, 0>(m, e, s);
         default: return cudaErrorInvalidValue;
     }
 }
