@@ -262,6 +262,10 @@ cudaError_t launch_encode_append(const EncodeAppendArgs& a, cudaStream_t s) {
     constexpr int kTensorFrom = 64;
     const bool aligned = (reinterpret_cast<uintptr_t>(a.k) % 16 == 0) && (reinterpret_cast<uintptr_t>(a.v) % 16 == 0);
     const bool tc_ok = !a.exact && a.n_new >= kTensorFrom && aligned;
+    if (tc_ok && encode_tc_supported(a, 0) && encode_tc_supported(a, 1)) {
+        cudaError_t pe = cudaSuccess;
+        if (launch_encode_tc_pair(a, s, &pe)) return pe;   // keys and values in one launch
+    }
     cudaError_t e = (tc_ok && encode_tc_supported(a, 0)) ? launch_encode_tc(a, 0, s) : launch_encode_block(a, 0, s);
     if (e != cudaSuccess) return e;
     if (a.vc.mode == TQ_MODE_GROUP) {

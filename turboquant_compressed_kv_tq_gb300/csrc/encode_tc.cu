@@ -157,18 +157,21 @@ __device__ __forceinline__ int lm_index(float y, const float (&m)[(1 << KB) - 1]
     }
 }
 
+// One tensor's tiles t0, t0 + stride, ... (n_it of them) through the pipeline
+// below, with the shared memory laid out by TcLayout<D, PROD> and the TMEM
+// columns from tmem; returns whether a wait ran out. Every thread of the CTA
+// calls it; its barriers are initialised here and invalidated at the end, so
+// that a CTA can run one phase per tensor.
 template <int D, int KB, bool PROD>
-__global__ void __launch_bounds__(kEncThreads, 1)
-    encode_tc_kernel(EncodeAppendArgs a, int is_v, int tiles_per_seq) {
+__device__ __forceinline__ bool tc_phase(const EncodeAppendArgs& a, int is_v, int tiles_per_seq, int64_t t0,
+                                         int64_t stride, int n_it, unsigned char* smem, uint32_t tmem) {
     using L = TcLayout<D, PROD>;
     constexpr int NM = (1 << KB) - 1;   // midpoints
     constexpr int W = D * KB / 32;      // index words
     constexpr int WS = D / 32;          // sign words
     constexpr int DH = D / 2;           // columns per epilogue thread
     constexpr int CH = DH / 32;         // 32-column chunks per epilogue thread
-    extern __shared__ __align__(1024) unsigned char smem[];
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::oBar);
-    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + kNumBars);
     float* s_norm = reinterpret_cast<float*>(smem + L::oNorm);
     float* s_g2 = reinterpret_cast<float*>(smem + L::oG2);
     float* s_c = reinterpret_cast<float*>(smem + L::oCb);
@@ -178,9 +181,7 @@ __global__ void __launch_bounds__(kEncThreads, 1)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t sbase = tc::smem_addr(smem);
     const int Hkv = a.pool.Hkv;
-    const int64_t ntiles = static_cast<int64_t>(a.batch) * Hkv * tiles_per_seq;
-    const int n_it = blockIdx.x < ntiles ? static_cast<int>((ntiles - 1 - blockIdx.x) / gridDim.x + 1) : 0;
-    auto tile_of = [&](int it) { return static_cast<int64_t>(blockIdx.x) + static_cast<int64_t>(it) * gridDim.x; };
+    auto tile_of = [&](int it) { return t0 + static_cast<int64_t>(it) * stride; };
     // The input rows of a tile are contiguous: thread 0 prefetches a tile's
     // rows into L2 one tile ahead of the producers (the first at launch, while
     // the prologue and the previous kernel's tail run).
@@ -196,15 +197,6 @@ __global__ void __launch_bounds__(kEncThreads, 1)
                              static_cast<unsigned>(rows) * D * 2);
     };
     prefetch_tile(0);
-    // the next kernel (the other tensor's encode, the next chunk's) shares no
-    // data with this one: it may take SMs as they free up at this launch's
-    // tail; this kernel completes only after its predecessor (wait at exit)
-    tc::grid_release_dependents();
-
-    if (warp == 0) {
-        tc::tmem_alloc(s_tmem, L::kCols);
-        tc::tmem_relinquish();
-    }
     if (tid == 0) {
         tc::mbar_init(&bars[kBarTab], 1);
         tc::mbar_init(&bars[kBarAFull], kProdWarps);
@@ -229,7 +221,6 @@ __global__ void __launch_bounds__(kEncThreads, 1)
     tc::tc_fence_before();
     __syncthreads();
     tc::tc_fence_after();
-    const uint32_t tmem = *s_tmem;
     const bool tables_failed = __syncthreads_or(!tc::mbar_wait(&bars[kBarTab], 0));
 
     bool failed = tables_failed;
@@ -521,16 +512,79 @@ __global__ void __launch_bounds__(kEncThreads, 1)
         }
     }
 
-    if (__syncthreads_or(failed) && tid == 0) atomicOr(a.err, TQ_DEVERR_TIMEOUT);
+    failed = __syncthreads_or(failed);
+    if (failed && tid == 0) atomicOr(a.err, TQ_DEVERR_TIMEOUT);
     tc::tc_fence_before();
     __syncthreads();
-    if (warp == 0) {
-        tc::tc_fence_after();
-        tc::tmem_dealloc(tmem, L::kCols);
-    }
+    tc::tc_fence_after();
     if (tid == 0)
         for (int i = 0; i < kNumBars; ++i) tc::mbar_inval(&bars[i]);
+    __syncthreads();  // the next phase may reuse this shared memory and these TMEM columns
+    return failed;
+}
+
+// The CTA's TMEM columns for its phases (the widest layout's), allocated by
+// warp 0; the next kernel may take SMs as they free up at this launch's tail
+// (it shares no data with this one); this kernel completes only after its
+// predecessor (the wait at exit).
+template <int COLS>
+__device__ __forceinline__ uint32_t tc_begin(uint32_t* slot) {
+    tc::grid_release_dependents();
+    if (threadIdx.x < 32) {
+        tc::tmem_alloc(slot, COLS);
+        tc::tmem_relinquish();
+    }
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+    return *slot;
+}
+
+template <int COLS>
+__device__ __forceinline__ void tc_end(uint32_t tmem) {
+    if (threadIdx.x < 32) {
+        tc::tc_fence_after();
+        tc::tmem_dealloc(tmem, COLS);
+    }
     tc::grid_wait_prior();
+}
+
+// One tensor (keys: is_v = 0, values: is_v = 1), persistent CTAs over its tiles.
+template <int D, int KB, bool PROD>
+__global__ void __launch_bounds__(kEncThreads, 1)
+    encode_tc_kernel(EncodeAppendArgs a, int is_v, int tiles_per_seq) {
+    using L = TcLayout<D, PROD>;
+    extern __shared__ __align__(1024) unsigned char smem[];
+    __shared__ uint32_t s_tmem;
+    const uint32_t tmem = tc_begin<L::kCols>(&s_tmem);
+    const int64_t ntiles = static_cast<int64_t>(a.batch) * a.pool.Hkv * tiles_per_seq;
+    const int n_it = blockIdx.x < ntiles ? static_cast<int>((ntiles - 1 - blockIdx.x) / gridDim.x + 1) : 0;
+    (void)tc_phase<D, KB, PROD>(a, is_v, tiles_per_seq, blockIdx.x, gridDim.x, n_it, smem, tmem);
+    tc_end<L::kCols>(tmem);
+}
+
+// Keys and values of one append in one launch: CTA c takes the tiles c, c + G,
+// ... of the keys' tiles followed by the values' (G CTAs), so every CTA runs
+// about twice the tiles of a one-tensor launch and pays one prologue and one
+// tail for both: its key phase, then its value phase in the same shared
+// memory (the layouts of the two codecs) and TMEM columns.
+template <int D, int KBK, bool PRODK, int KBV, bool PRODV>
+__global__ void __launch_bounds__(kEncThreads, 1)
+    encode_tc_pair_kernel(EncodeAppendArgs a, int tiles_per_seq) {
+    using LK = TcLayout<D, PRODK>;
+    using LV = TcLayout<D, PRODV>;
+    constexpr int kCols = LK::kCols > LV::kCols ? LK::kCols : LV::kCols;
+    extern __shared__ __align__(1024) unsigned char smem[];
+    __shared__ uint32_t s_tmem;
+    const uint32_t tmem = tc_begin<kCols>(&s_tmem);
+    const int64_t nt = static_cast<int64_t>(a.batch) * a.pool.Hkv * tiles_per_seq;   // per tensor
+    const int64_t c = blockIdx.x, G = gridDim.x;
+    const int nk = c < nt ? static_cast<int>((nt - 1 - c) / G + 1) : 0;
+    const int64_t u = c + static_cast<int64_t>(nk) * G;   // the CTA's first index past the keys
+    const int nv = u < 2 * nt ? static_cast<int>((2 * nt - 1 - u) / G + 1) : 0;
+    bool failed = tc_phase<D, KBK, PRODK>(a, 0, tiles_per_seq, c, G, nk, smem, tmem);
+    if (!failed) (void)tc_phase<D, KBV, PRODV>(a, 1, tiles_per_seq, u - nt, G, nv, smem, tmem);
+    tc_end<kCols>(tmem);
 }
 
 int sm_count() {
@@ -572,6 +626,35 @@ cudaError_t launch_tc(const EncodeAppendArgs& a, int is_v, cudaStream_t s) {
     return e;
 }
 
+template <int D, int KBK, bool PRODK, int KBV, bool PRODV>
+cudaError_t launch_tc_pair(const EncodeAppendArgs& a, cudaStream_t s) {
+    constexpr size_t kBytes = TcLayout<D, PRODK>::kBytes > TcLayout<D, PRODV>::kBytes ? TcLayout<D, PRODK>::kBytes
+                                                                                       : TcLayout<D, PRODV>::kBytes;
+    static std::atomic<uint64_t> attr_set{0};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const uint64_t bit = 1ull << (dev & 63);
+    if (!(attr_set.load() & bit)) {
+        cudaError_t e = cudaFuncSetAttribute(encode_tc_pair_kernel<D, KBK, PRODK, KBV, PRODV>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kBytes));
+        if (e != cudaSuccess) {
+            (void)cudaGetLastError();
+            return e;
+        }
+        attr_set.fetch_or(bit);
+    }
+    const int tiles_per_seq = (a.n_new + kTileRows - 1) / kTileRows;
+    const int64_t ntiles = 2 * static_cast<int64_t>(a.batch) * a.pool.Hkv * tiles_per_seq;
+    int64_t grid = static_cast<int64_t>(sm_count());
+    if (grid <= 0) return cudaErrorInvalidDevice;
+    if (grid > ntiles) grid = ntiles;
+    const cudaError_t e = launch_overlapped(encode_tc_pair_kernel<D, KBK, PRODK, KBV, PRODV>,
+                                            dim3(static_cast<unsigned>(grid)), dim3(kEncThreads), kBytes, s, a,
+                                            tiles_per_seq);
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    return e;
+}
+
 template <int D>
 cudaError_t dispatch_kb(const EncodeAppendArgs& a, int is_v, const CodecDev& cd, cudaStream_t s) {
     const bool prod = cd.mode == TQ_MODE_PROD;
@@ -592,6 +675,19 @@ bool encode_tc_supported(const EncodeAppendArgs& a, int is_v) {
     if (cd.D != 64 && cd.D != 128) return false;
     if (!cd.Rtc || (cd.mode == TQ_MODE_PROD && !cd.Stc)) return false;
     return a.dtype == TQ_BF16 || a.dtype == TQ_F16;
+}
+
+// Keys and values in one tensor-core launch, for the codec pairs built as
+// one kernel (head_dim 128: prod keys of 3 bits with 3- or 4-bit MSE values,
+// 4-bit MSE keys and values); false for the others (two launches instead).
+bool launch_encode_tc_pair(const EncodeAppendArgs& a, cudaStream_t s, cudaError_t* err) {
+    if (a.kc.D != 128 || a.vc.D != 128) return false;
+    const bool kp = a.kc.mode == TQ_MODE_PROD, vp = a.vc.mode == TQ_MODE_PROD;
+    if (kp && a.kc.ib == 2 && !vp && a.vc.ib == 3) *err = launch_tc_pair<128, 2, true, 3, false>(a, s);
+    else if (kp && a.kc.ib == 2 && !vp && a.vc.ib == 4) *err = launch_tc_pair<128, 2, true, 4, false>(a, s);
+    else if (!kp && a.kc.ib == 4 && !vp && a.vc.ib == 4) *err = launch_tc_pair<128, 4, false, 4, false>(a, s);
+    else return false;
+    return true;
 }
 
 // Tensor-core encode of one tensor (keys: is_v = 0, values: is_v = 1).

@@ -200,6 +200,7 @@ cudaError_t launch_encode_append(const EncodeAppendArgs& a, cudaStream_t s);
 cudaError_t launch_encode_block(const EncodeAppendArgs& a, int is_v, cudaStream_t s);
 bool encode_tc_supported(const EncodeAppendArgs& a, int is_v);
 cudaError_t launch_encode_tc(const EncodeAppendArgs& a, int is_v, cudaStream_t s);
+bool launch_encode_tc_pair(const EncodeAppendArgs& a, cudaStream_t s, cudaError_t* err);
 cudaError_t launch_quantize(const QuantizeArgs& a, cudaStream_t s);
 // `step` (tensor-core path only): the decode step's append, fused into the
 // query-prep launch; null for a plain decode.
