@@ -563,14 +563,15 @@ __global__ void __launch_bounds__(kEncThreads, 1)
     tc_end<L::kCols>(tmem);
 }
 
-// Keys and values of one append in one launch: CTA c takes the tiles c, c + G,
-// ... of the keys' tiles followed by the values' (G CTAs), so every CTA runs
-// about twice the tiles of a one-tensor launch and pays one prologue and one
-// tail for both: its key phase, then its value phase in the same shared
-// memory (the layouts of the two codecs) and TMEM columns.
+// Keys and values of one append in one launch: the first GK CTAs run the
+// keys' tiles (CTA c takes c, c + GK, ...), the others the values' tiles, both
+// tensors side by side on disjoint SMs. GK splits the grid by the tensors'
+// relative tile cost (a prod tile, with its QJL GEMM and sign pass, costs about
+// 1.2 MSE tiles), so that both halves finish together; each CTA runs one
+// phase, with no switch of tables or barriers inside a CTA.
 template <int D, int KBK, bool PRODK, int KBV, bool PRODV>
 __global__ void __launch_bounds__(kEncThreads, 1)
-    encode_tc_pair_kernel(EncodeAppendArgs a, int tiles_per_seq) {
+    encode_tc_pair_kernel(EncodeAppendArgs a, int tiles_per_seq, int gk) {
     using LK = TcLayout<D, PRODK>;
     using LV = TcLayout<D, PRODV>;
     constexpr int kCols = LK::kCols > LV::kCols ? LK::kCols : LV::kCols;
@@ -578,12 +579,15 @@ __global__ void __launch_bounds__(kEncThreads, 1)
     __shared__ uint32_t s_tmem;
     const uint32_t tmem = tc_begin<kCols>(&s_tmem);
     const int64_t nt = static_cast<int64_t>(a.batch) * a.pool.Hkv * tiles_per_seq;   // per tensor
-    const int64_t c = blockIdx.x, G = gridDim.x;
-    const int nk = c < nt ? static_cast<int>((nt - 1 - c) / G + 1) : 0;
-    const int64_t u = c + static_cast<int64_t>(nk) * G;   // the CTA's first index past the keys
-    const int nv = u < 2 * nt ? static_cast<int>((2 * nt - 1 - u) / G + 1) : 0;
-    bool failed = tc_phase<D, KBK, PRODK>(a, 0, tiles_per_seq, c, G, nk, smem, tmem);
-    if (!failed) (void)tc_phase<D, KBV, PRODV>(a, 1, tiles_per_seq, u - nt, G, nv, smem, tmem);
+    const int64_t c = blockIdx.x;
+    if (c < gk) {
+        const int n = c < nt ? static_cast<int>((nt - 1 - c) / gk + 1) : 0;
+        (void)tc_phase<D, KBK, PRODK>(a, 0, tiles_per_seq, c, gk, n, smem, tmem);
+    } else {
+        const int64_t cv = c - gk, gv = gridDim.x - gk;
+        const int n = cv < nt ? static_cast<int>((nt - 1 - cv) / gv + 1) : 0;
+        (void)tc_phase<D, KBV, PRODV>(a, 1, tiles_per_seq, cv, gv, n, smem, tmem);
+    }
     tc_end<kCols>(tmem);
 }
 
@@ -644,13 +648,21 @@ cudaError_t launch_tc_pair(const EncodeAppendArgs& a, cudaStream_t s) {
         attr_set.fetch_or(bit);
     }
     const int tiles_per_seq = (a.n_new + kTileRows - 1) / kTileRows;
-    const int64_t ntiles = 2 * static_cast<int64_t>(a.batch) * a.pool.Hkv * tiles_per_seq;
+    const int64_t nt = static_cast<int64_t>(a.batch) * a.pool.Hkv * tiles_per_seq;   // per tensor
     int64_t grid = static_cast<int64_t>(sm_count());
     if (grid <= 0) return cudaErrorInvalidDevice;
-    if (grid > ntiles) grid = ntiles;
+    if (grid > 2 * nt) grid = 2 * nt;
+    if (grid < 2) grid = 2;
+    // CTAs for the keys: the grid split by the tiles' relative cost
+    constexpr double wk = PRODK ? 1.2 : 1.0, wv = PRODV ? 1.2 : 1.0;
+    int64_t gk = static_cast<int64_t>(static_cast<double>(grid) * wk / (wk + wv) + 0.5);
+    if (gk > nt) gk = nt;
+    if (grid - gk > nt) gk = grid - nt;
+    if (gk < 1) gk = 1;
+    if (gk > grid - 1) gk = grid - 1;
     const cudaError_t e = launch_overlapped(encode_tc_pair_kernel<D, KBK, PRODK, KBV, PRODV>,
                                             dim3(static_cast<unsigned>(grid)), dim3(kEncThreads), kBytes, s, a,
-                                            tiles_per_seq);
+                                            tiles_per_seq, static_cast<int>(gk));
     g_launches.fetch_add(1, std::memory_order_relaxed);
     return e;
 }
