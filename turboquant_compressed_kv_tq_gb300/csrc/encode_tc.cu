@@ -26,6 +26,8 @@
 // the fp32 dot-product bound of the sequential specification: an index or
 // sign can differ from it only where the exact value lies within rounding
 // distance of a decision threshold (a midpoint, or 0).
+#include <algorithm>
+
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -653,13 +655,20 @@ cudaError_t launch_tc_pair(const EncodeAppendArgs& a, cudaStream_t s) {
     if (grid <= 0) return cudaErrorInvalidDevice;
     if (grid > 2 * nt) grid = 2 * nt;
     if (grid < 2) grid = 2;
-    // CTAs for the keys: the grid split by the tiles' relative cost
+    // CTAs for the keys: the split that minimises the later of the two halves'
+    // ends, each half's time its most tiles per CTA x its tiles' relative cost
+    // (a prod tile costs about 1.2 MSE tiles)
     constexpr double wk = PRODK ? 1.2 : 1.0, wv = PRODV ? 1.2 : 1.0;
-    int64_t gk = static_cast<int64_t>(static_cast<double>(grid) * wk / (wk + wv) + 0.5);
-    if (gk > nt) gk = nt;
-    if (grid - gk > nt) gk = grid - nt;
-    if (gk < 1) gk = 1;
-    if (gk > grid - 1) gk = grid - 1;
+    int64_t gk = 1;
+    double best = 1e300;
+    for (int64_t g = 1; g < grid; ++g) {
+        const double t = std::max(static_cast<double>((nt + g - 1) / g) * wk,
+                                  static_cast<double>((nt + grid - g - 1) / (grid - g)) * wv);
+        if (t < best) {
+            best = t;
+            gk = g;
+        }
+    }
     const cudaError_t e = launch_overlapped(encode_tc_pair_kernel<D, KBK, PRODK, KBV, PRODV>,
                                             dim3(static_cast<unsigned>(grid)), dim3(kEncThreads), kBytes, s, a,
                                             tiles_per_seq, static_cast<int>(gk));
