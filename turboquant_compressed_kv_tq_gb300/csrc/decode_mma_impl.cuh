@@ -355,6 +355,7 @@ __device__ __forceinline__ void mse_chunk(const uint32_t* w, const typename MseT
 // rotation (or, for a shard's state, writes the merged (max, sum,
 // accumulator) without the rotation). Thread d owns output column d.
 constexpr int kMThreads = kD;
+static_assert(kMThreads == 4 * 32, "the merge's reductions take four warps");
 
 template <bool VGROUP>
 __global__ void __launch_bounds__(kMThreads) merge_rows_kernel(MmaArgs m) {
