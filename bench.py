@@ -533,8 +533,11 @@ def run_gpu(args):
             cpu = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample,
                    "seconds": round(secs, 2)}
         clocks = clk.summary()
-        dominant = ("split_mma_kernel (tensor-core split-K decode)" if D == 128
-                    else "split_kernel + merge_kernel (SIMT decode)")
+        plan = tq.tq_decode_plan(cache.desc, B, Hq, Lq, cap,
+                                 torch.cuda.get_device_properties(dev).multi_processor_count)
+        dominant = ("split_mma_kernel (tensor-core split-K decode" +
+                    (")" if D == 128 else f", head_dim {D}: two 128-column value halves per unit)")
+                    if plan["tensor_cores"] else "split_kernel + merge_kernel (SIMT decode)")
         result = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": step_ms_max, "higher_is_better": True,

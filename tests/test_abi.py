@@ -194,12 +194,35 @@ def test_workspace_query_rejects_a_descriptor_without_heads(libtq):
 
 
 def test_decode_plan_simt_shapes(libtq):
-    # head_dim 64 and 256 take the SIMT kernels: no tensor-core shared memory
-    for D, key, value in [(256, ("prod", 3), ("group", 2, 32)), (64, ("mse", 2), ("mse", 2, 0))]:
+    # head_dim 64, and 256 with codec pairs the tensor-core kernels are not
+    # built for, take the SIMT kernels: no tensor-core shared memory
+    for D, key, value in [(256, ("prod", 2), ("group", 4, 64)), (64, ("mse", 2), ("mse", 2, 0))]:
         d = _desc_from_oracle(D, key, value, 64, 2)
         p = tq.tq_decode_plan(d, 2, 16, 1, 8192, 152)
         assert p["tensor_cores"] == 0 and p["smem_bytes"] == 0
         assert p["splits"] * p["chunk_tokens"] >= 8192 and p["workspace_bytes"] > 0
+
+
+@pytest.mark.parametrize("value", [("group", 2, 32), ("mse", 3, 1)])
+def test_decode_plan_head_dim_256_tensor_cores(libtq, value):
+    # prod 3-bit keys with group 2-bit or MSE 3-bit values at head_dim 256:
+    # two CTAs (128-column value halves) per (unit, split), so 2 sequences x
+    # 2 KV heads x 1 row group = 4 units x 2 halves = 8 CTAs per split; 19
+    # splits cover 152 SMs; 200 or 204 record bytes per token need 32-token
+    # tiles (64-token stages would not fit)
+    d = _desc_from_oracle(256, ("prod", 3), value, 64, 2)
+    p = tq.tq_decode_plan(d, 2, 16, 1, 8192, 152)
+    assert p["tensor_cores"] == 1 and p["tile_tokens"] == 32
+    assert p["splits"] == 19 and p["chunk_tokens"] == 448
+    assert 0 < p["smem_bytes"] <= 227 * 1024 - 1024
+    # fp32 q' and q'' rows (two arrays), partials for both halves, (max, sum)
+    # rows for both halves
+    units = 4
+    q = units * 16 * 256 * 4
+    part = units * 19 * 16 * 256 * 4
+    ml = units * 2 * 19 * 16 * 2 * 4
+    r = lambda x: (x + 255) // 256 * 256
+    assert p["workspace_bytes"] == 2 * r(q) + r(part) + r(ml)
 
 
 def test_decode_plan_split_rule(libtq):

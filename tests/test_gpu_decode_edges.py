@@ -4,7 +4,8 @@ Token counts around the 64-token tiles and 128-token blocks (only the query
 positions, a tile minus one, exactly one tile, one over) for every codec pair
 of the prefill kernels, 128- to 512-token blocks in a shuffled order, causal
 query lengths above one, more than 16 query rows (two row groups), a sequence
-long enough for many token splits (past one merge chunk), per-head scales, and inputs with zero,
+long enough for many token splits (past one merge chunk), head_dim 256 on the
+tensor-core path (two 128-column value halves per unit), per-head scales, and inputs with zero,
 tiny and one-hot vectors (zero-norm values, zero keys). Every output row is
 compared with the oracle's decode of the same raw inputs (the max abs error
 and cosine bounds of the decode parity rule); the last case checks that two
@@ -34,10 +35,10 @@ def _lib_built():
     assert torch.cuda.is_available()
 
 
-def _workload(key, value, lens, Lq, Hkv, G, bt, shuffle=False, scales=None, seed=5):
+def _workload(key, value, lens, Lq, Hkv, G, bt, shuffle=False, scales=None, seed=5, D=128):
     kspec = wl._spec(key[0], key[1], 21)
     vspec = wl._spec(value[0], value[1], 22, value[2] if len(value) > 2 else 0)
-    return wl.Workload("decode_tc", 1, len(lens), Hkv, Hkv * G, 128, tuple(lens), Lq, torch.bfloat16, 1.0,
+    return wl.Workload("decode_tc", 1, len(lens), Hkv, Hkv * G, D, tuple(lens), Lq, torch.bfloat16, 1.0,
                        seed, kspec, vspec, block_tokens=bt, shuffle_blocks=shuffle, append_per_step=0,
                        prefill_chunk=1024, head_scale_range=scales)
 
@@ -96,6 +97,36 @@ def test_splits_beyond_one_merge_chunk():
     qn = to_f32_np(q).astype(np.float64)
     K, V = raw_kv(w, 0, 0, w.seq_lens[0], DEV)
     compare_decode(out[0], oracle_decode(w, K[0], V[0], qn[0]))
+
+
+def _plan(w):
+    case = GpuCase(w, layers=[0])
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    return case, tq.tq_decode_plan(case.cache.desc, w.batch, w.num_q_heads, w.q_len, max(w.seq_lens), sms)
+
+
+@pytest.mark.parametrize("value", [("group", 2, 32), ("mse", 3), ("group", 2, 64)])
+def test_head_dim_256_tile_edges(value):
+    # 32-token tiles at head_dim 256: sequences around one tile, 64-token
+    # blocks, q_len 2 x GQA 8
+    w = _workload(("prod", 3), value, (2, 31, 32, 33, 700), 2, 2, 8, 64, D=256)
+    _, plan = _plan(w)
+    assert plan["tensor_cores"] == 1, plan
+    _check(w)
+
+
+def test_head_dim_256_two_row_groups_shuffled():
+    # 32 rows per KV head (two row groups), 16-token blocks in a shuffled order
+    w = _workload(("prod", 3), ("mse", 3), (513, 1280), 4, 2, 8, 16, shuffle=True, D=256)
+    _check(w)
+
+
+def test_head_dim_256_many_splits():
+    # one KV head: more splits than the merge loads at once
+    w = _workload(("prod", 3), ("group", 2, 32), (20000,), 1, 1, 8, 256, D=256)
+    _, plan = _plan(w)
+    assert plan["tensor_cores"] == 1 and plan["splits"] > 32, plan
+    _check(w)
 
 
 def test_head_scales_mse4():

@@ -67,6 +67,8 @@ CASES = [
     pytest.param(("prod", 3), ("group", 4, 64), 128, (37, 100, 16, 3), 2, 2, 4, id="group-values-unfused"),
     pytest.param(("prod", 3), ("mse", 3), 128, (37, 100), 12, 2, 4, id="n12-unfused"),
     pytest.param(("prod", 3), ("mse", 3), 64, (37, 100), 2, 2, 4, id="d64-unfused"),
+    pytest.param(("prod", 3), ("group", 2, 32), 256, (37, 100, 5), 2, 2, 8, id="d256-group2-unfused"),
+    pytest.param(("prod", 3), ("mse", 3), 256, (70, 300), 1, 1, 8, id="d256-mse3-unfused"),
 ]
 
 

@@ -209,6 +209,13 @@ def test_decode_layer_d256(n):
     _check_decode(wl.layer_d256(n), [0])
 
 
+@pytest.mark.parametrize("n", [1000, 4097])
+def test_decode_layer_d256_mse_values(n):
+    # the same layer with 3-bit MSE values (rotated back in the merge)
+    w = dataclasses.replace(wl.layer_d256(4096), value=wl._spec("mse", 3, 1), seq_lens=(n,))
+    _check_decode(w, [0])
+
+
 def test_decode_stack_shape_reduced():
     w = dataclasses.replace(wl.stack_32k(), seq_lens=(3001,))
     _check_decode(w, [0, 63])

@@ -43,7 +43,9 @@ CASES = [
     (128, ("prod", 3), ("mse", 3), 2, 8, 2, 5003, (0, 1700, 3333, 5003)),   # the long-context codecs
     (128, ("mse", 4), ("mse", 4), 2, 8, 2, 700, (0, 699, 700)),             # last shard shorter than q_len
     (128, ("prod", 3), ("group", 4, 64), 2, 4, 1, 900, (0, 0, 450, 900)),   # an empty shard
-    (256, ("prod", 3), ("group", 2, 32), 2, 8, 1, 1000, (0, 600, 1000)),    # head_dim 256 (SIMT kernels)
+    (256, ("prod", 3), ("group", 2, 32), 2, 8, 1, 1000, (0, 600, 1000)),    # head_dim 256, group values
+    (256, ("prod", 3), ("mse", 3), 2, 8, 2, 3000, (0, 1000, 3000)),         # head_dim 256, MSE values
+    (256, ("prod", 2), ("group", 4, 64), 1, 4, 1, 800, (0, 400, 800)),      # head_dim 256 on the SIMT kernels
     (128, ("prod", 3), ("mse", 3), 1, 8, 2, 160000, (0, 10000, 160000)),    # one head: a shard of > 128 splits
 ]
 

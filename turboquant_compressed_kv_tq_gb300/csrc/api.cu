@@ -62,6 +62,7 @@ void free_codec(tq_codec* c) {
     cudaFree(c->d_R);
     cudaFree(c->d_Rt);
     cudaFree(c->d_St);
+    cudaFree(c->d_SRt);
     cudaFree(c->d_c);
     cudaFree(c->d_m);
     cudaFree(c->d_cq);
@@ -122,11 +123,29 @@ std::vector<float> transpose(const std::vector<float>& a, int D) {
     return t;
 }
 
+// Transposed product (S R)^T of two D x D row-major matrices, accumulated in
+// fp64 over ascending k and rounded once to fp32: entry [k][i] = sum_j S[i][j] R[j][k].
+std::vector<float> product_transposed(const std::vector<float>& S, const std::vector<float>& R, int D) {
+    std::vector<float> t(S.size());
+    std::vector<double> row(D);
+    for (int i = 0; i < D; ++i) {
+        for (int k = 0; k < D; ++k) row[k] = 0.0;
+        for (int j = 0; j < D; ++j) {
+            const double sij = S[static_cast<size_t>(i) * D + j];
+            const float* rj = R.data() + static_cast<size_t>(j) * D;
+            for (int k = 0; k < D; ++k) row[k] += sij * rj[k];
+        }
+        for (int k = 0; k < D; ++k) t[static_cast<size_t>(k) * D + i] = static_cast<float>(row[k]);
+    }
+    return t;
+}
+
 CodecDev dev_view(const tq_codec* c) {
     CodecDev d{};
     d.R = c->d_R;
     d.Rt = c->d_Rt;
     d.St = c->d_St;
+    d.SRt = c->d_SRt;
     d.c = c->d_c;
     d.m = c->d_m;
     d.cq = c->d_cq;
@@ -285,6 +304,9 @@ tq_status tq_codec_create(int head_dim, int bits, tq_mode mode, uint64_t seed, t
     tq_status st = upload(&c->d_R, c->host.rotation);
     if (st == TQ_OK) st = upload(&c->d_Rt, transpose(c->host.rotation, head_dim));
     if (st == TQ_OK && mode == TQ_MODE_PROD) st = upload(&c->d_St, transpose(c->host.qjl, head_dim));
+    // q'' = (S R) q in one pass with q' = R q: the query prep of the wide tensor-core decode
+    if (st == TQ_OK && mode == TQ_MODE_PROD && head_dim > 128)
+        st = upload(&c->d_SRt, product_transposed(c->host.qjl, c->host.rotation, head_dim));
     if (st == TQ_OK) st = upload(&c->d_c, c->host.centroids);
     if (st == TQ_OK) st = upload(&c->d_m, c->host.midpoints);
     if (st == TQ_OK) st = upload(&c->d_cq, c->host.op_levels);

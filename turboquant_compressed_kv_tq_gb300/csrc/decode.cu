@@ -409,6 +409,8 @@ namespace mmadec {
 bool dispatch_a(int, bool, bool, int, const MmaArgs&, size_t, cudaStream_t, const EncodeAppendArgs*, cudaError_t*);
 bool dispatch_b(int, bool, bool, int, const MmaArgs&, size_t, cudaStream_t, const EncodeAppendArgs*, cudaError_t*);
 bool dispatch_c(int, bool, bool, int, const MmaArgs&, size_t, cudaStream_t, const EncodeAppendArgs*, cudaError_t*);
+bool wide_supported(int D, int kb, bool prod, bool vgroup, int vb);
+bool dispatch_d(int D, int kb, bool prod, bool vgroup, int vb, const MmaArgs&, size_t, cudaStream_t, cudaError_t*);
 }  // namespace mmadec
 
 namespace {
@@ -433,7 +435,7 @@ void choose_splits(DecodePlan& p, int64_t units, int64_t target_ctas, int max_se
 }
 
 bool mma_supported(const tq_cache_desc* d, DecodePlan& p) {
-    if (d->head_dim != mmadec::kD) return false;
+    if (d->head_dim != mmadec::kD && d->head_dim != 2 * mmadec::kD) return false;
     p.kprod = d->key_mode == TQ_MODE_PROD;
     p.kb = p.kprod ? d->key_bits - 1 : d->key_bits;
     if (p.kprod ? (p.kb < 1 || p.kb > 3) : (p.kb < 2 || p.kb > 4)) return false;
@@ -444,7 +446,8 @@ bool mma_supported(const tq_cache_desc* d, DecodePlan& p) {
     } else if (p.vb < 2 || p.vb > 4) {
         return false;
     }
-    return true;
+    // head_dim 256: the instantiated codec pairs only
+    return d->head_dim == mmadec::kD || mmadec::wide_supported(d->head_dim, p.kb, p.kprod, p.vgroup, p.vb);
 }
 
 }  // namespace
@@ -458,6 +461,7 @@ DecodePlan make_decode_plan(const tq_cache_desc* d, int batch, int G, int Lq, in
     const int64_t units = static_cast<int64_t>(batch) * Hkv * p.row_groups;
     if (mma_supported(d, p)) {
         p.kind = 1;
+        const int NH = D / mmadec::kD;  // 128-column value halves: CTAs per (unit, split)
         // stage layout for a tile size; the tile halves (down to 16 tokens)
         // while the split kernel's shared memory would exceed the budget
         auto layout = [&](int tile) {
@@ -480,7 +484,7 @@ DecodePlan make_decode_plan(const tq_cache_desc* d, int batch, int G, int Lq, in
             p.st_bytes = (o + 127) / 128 * 128;
             const size_t ring = static_cast<size_t>(mmadec::kWarps) * mmadec::kStages * p.st_bytes;
             p.qs_off = static_cast<int>(ring);
-            size_t ringq = ring + mmadec::kQFragBytes;
+            size_t ringq = ring + static_cast<size_t>(mmadec::kQFragBytes) * NH;
             p.vt_off = -1;
             if (!p.vgroup && p.vb == 3) {  // pair table of 3-bit value codes (aligned inside the region)
                 p.vt_off = static_cast<int>(ringq);
@@ -505,8 +509,11 @@ DecodePlan make_decode_plan(const tq_cache_desc* d, int batch, int G, int Lq, in
             tile /= 2;
             layout(tile);
         }
-        choose_splits(p, units, num_sms, max_seq_len, p.tile, 16384);
-        p.q_bytes = al256(static_cast<size_t>(units) * 2 * 8 * 32 * 16);
+        choose_splits(p, units * NH, num_sms, max_seq_len, p.tile, 16384);
+        // head_dim 128: the units' query fragments; above it the fp32 q' and
+        // q'' rows of the SIMT query prep (two arrays of q_bytes)
+        p.q_bytes = NH == 1 ? al256(static_cast<size_t>(units) * 2 * 8 * 32 * 16)
+                            : al256(static_cast<size_t>(units) * kRows * D * sizeof(float));
     } else {
         p.kind = 0;
         p.tile = kTile;
@@ -517,8 +524,10 @@ DecodePlan make_decode_plan(const tq_cache_desc* d, int batch, int G, int Lq, in
         p.q_bytes = al256(static_cast<size_t>(units) * kRows * D * sizeof(float));
     }
     p.part_bytes = al256(static_cast<size_t>(units) * p.splits * kRows * D * sizeof(float));
-    p.ml_bytes = al256(static_cast<size_t>(units) * p.splits * kRows * 2 * sizeof(float));
-    p.total = (p.kind ? p.q_bytes : 2 * p.q_bytes) + p.part_bytes + p.ml_bytes;
+    // (max, sum) rows: one set per value half of the tensor-core path
+    const int ml_sets = p.kind == 1 ? D / mmadec::kD : 1;
+    p.ml_bytes = al256(static_cast<size_t>(units) * ml_sets * p.splits * kRows * 2 * sizeof(float));
+    p.total = (p.kind == 1 && D == mmadec::kD ? p.q_bytes : 2 * p.q_bytes) + p.part_bytes + p.ml_bytes;
     return p;
 }
 
@@ -538,11 +547,19 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s, const EncodeAppen
             m.st.field[k] = a.plan.st_field[k];
         }
         char* ws = static_cast<char*>(a.ws);
+        cudaError_t e = cudaErrorInvalidValue;
+        const DecodePlan& p = a.plan;
+        if (a.kc.D != mmadec::kD) {
+            // fp32 query rows at a.qrot / a.qjl, partials after both
+            m.part = a.part;
+            m.ml = a.ml;
+            if (step) return cudaErrorInvalidValue;  // the step's append runs before
+            if (mmadec::dispatch_d(a.kc.D, p.kb, p.kprod, p.vgroup, p.vb, m, p.smem, s, &e)) return e;
+            return cudaErrorInvalidValue;
+        }
         m.qfrag = reinterpret_cast<const uint4*>(ws);
         m.part = reinterpret_cast<float*>(ws + a.plan.q_bytes);
         m.ml = reinterpret_cast<float*>(ws + a.plan.q_bytes + a.plan.part_bytes);
-        cudaError_t e = cudaErrorInvalidValue;
-        const DecodePlan& p = a.plan;
         if (mmadec::dispatch_a(p.kb, p.kprod, p.vgroup, p.vb, m, p.smem, s, step, &e)) return e;
         if (mmadec::dispatch_b(p.kb, p.kprod, p.vgroup, p.vb, m, p.smem, s, step, &e)) return e;
         if (mmadec::dispatch_c(p.kb, p.kprod, p.vgroup, p.vb, m, p.smem, s, step, &e)) return e;

@@ -349,17 +349,20 @@ __device__ __forceinline__ void mse_chunk(const uint32_t* w, const typename MseT
 
 // Merge of a unit's split partials, one CTA per (unit, row), launched after
 // the split kernel with programmatic dependent launch: R_v is staged in shared
-// memory before the CTA waits for the split kernel; then the CTA takes the
-// row's maximum over the splits, weights each split's (sum, accumulator) by
-// 2^(m - max), divides by the merged sum and applies the inverse value
-// rotation (or, for a shard's state, writes the merged (max, sum,
-// accumulator) without the rotation). Thread d owns output column d.
-constexpr int kMThreads = kD;
-static_assert(kMThreads == 4 * 32, "the merge's reductions take four warps");
+// memory before the CTA waits for the split kernel (head_dim 128; at 256 the
+// rotation reads R_v's rows from L2); then the CTA takes the row's maximum
+// over the splits, weights each split's (sum, accumulator) by 2^(m - max),
+// divides by the merged sum and applies the inverse value rotation (or, for a
+// shard's state, writes the merged (max, sum, accumulator) without the
+// rotation). Thread d owns output column d; at head_dim 256 the split
+// kernel's two 128-column halves are separate partial rows (the same max and
+// sum in both).
+constexpr int kMThreads = kD;   // threads per merge CTA at head_dim 128
 
-template <bool VGROUP>
-__global__ void __launch_bounds__(kMThreads) merge_rows_kernel(MmaArgs m) {
+template <bool VGROUP, int D = kD>
+__global__ void __launch_bounds__(D) merge_rows_kernel(MmaArgs m) {
     extern __shared__ __align__(128) unsigned char smem[];
+    constexpr int NH = D / kD, kW = D / 32;
     const DecodeArgs& a = m.a;
     tc::grid_release_dependents();  // the next kernel waits for this grid before the workspace
     const int unit = blockIdx.x, r = blockIdx.y;
@@ -369,13 +372,15 @@ __global__ void __launch_bounds__(kMThreads) merge_rows_kernel(MmaArgs m) {
     const int row = rg * kRows + r;
     if (row >= a.plan.rows) return;  // padding row of the last group
     const int d = threadIdx.x, lane = d & 31, wid = d >> 5;
+    const int h2 = d / kD, cc = d % kD;
     const bool rotate = !VGROUP && !a.part_acc;
-    float* sR = reinterpret_cast<float*>(smem);      // [D][D], rotation only
-    float* so = sR + (rotate ? kD * kD : 0);         // [D] the merged row
-    float* sw = so + kD;                             // [kMThreads] weights of a chunk of splits
-    float* sred = sw + kMThreads;                    // [4] per-warp maxima / sums
+    const bool stage_r = rotate && D == kD;
+    float* sR = reinterpret_cast<float*>(smem);      // [D][D], staged rotation only
+    float* so = sR + (stage_r ? kD * kD : 0);        // [D] the merged row
+    float* sw = so + D;                              // [D] weights of a chunk of splits
+    float* sred = sw + D;                            // [kW] per-warp maxima / sums
     __shared__ uint64_t bar;
-    if (rotate && d == 0) {
+    if (stage_r && d == 0) {
         mbar_init(&bar, 1);
         mbar_fence_init();
         mbar_expect_tx(&bar, kD * kD * 4);
@@ -383,8 +388,9 @@ __global__ void __launch_bounds__(kMThreads) merge_rows_kernel(MmaArgs m) {
     }
     tc::grid_wait_prior();  // the split kernel's partials
     const int S = a.plan.splits;
-    const float* mlr = m.ml + (static_cast<int64_t>(unit) * S * kRows + r) * 2;     // split s at + s * 32
-    const float* pr = m.part + (static_cast<int64_t>(unit) * S * kRows + r) * kD + d;  // split s at + s * 16 D
+    // (max, sum) rows of the unit's first half; accumulator column cc of half h2
+    const float* mlr = m.ml + (static_cast<int64_t>(unit) * NH * S * kRows + r) * 2;     // split s at + s * 32
+    const float* pr = m.part + ((static_cast<int64_t>(unit) * NH + h2) * S * kRows + r) * kD + cc;  // + s * 16 x 128
     // every load of the first kMPre splits issued at once (one L2 round trip):
     // thread d's column of each split's accumulator, and the (max, sum) of
     // split d
@@ -396,14 +402,16 @@ __global__ void __launch_bounds__(kMThreads) merge_rows_kernel(MmaArgs m) {
     if (d < S) myml = __ldcg(reinterpret_cast<const float2*>(mlr + d * kRows * 2));
     // the row's maximum over the splits
     float mx = myml.x;
-    for (int s = d + kMThreads; s < S; s += kMThreads) mx = fmaxf(mx, __ldcg(mlr + s * kRows * 2));
+    for (int s = d + D; s < S; s += D) mx = fmaxf(mx, __ldcg(mlr + s * kRows * 2));
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
     if (lane == 0) sred[wid] = mx;
     __syncthreads();
-    const float M = fmaxf(fmaxf(sred[0], sred[1]), fmaxf(sred[2], sred[3]));
-    // weights 2^(m - M) of the first kMThreads splits (a split that saw no
-    // score has (-inf, 0) and a zero accumulator); thread d's share of the sum
+    float M = sred[0];
+#pragma unroll
+    for (int w = 1; w < kW; ++w) M = fmaxf(M, sred[w]);
+    // weights 2^(m - M) of the first D splits (a split that saw no score has
+    // (-inf, 0) and a zero accumulator); thread d's share of the sum
     float lsum = 0.0f;
     if (d < S) {
         const float w = myml.x == -INFINITY ? 0.0f : ex2(myml.x - M);
@@ -416,8 +424,8 @@ __global__ void __launch_bounds__(kMThreads) merge_rows_kernel(MmaArgs m) {
     for (int s = 0; s < kMPre; ++s)
         if (s < S) acc = fmaf(sw[s], pv[s], acc);
     // splits past the first kMPre (long sequences over few units)
-    for (int s0 = 0; s0 < S; s0 += kMThreads) {
-        const int n = S - s0 < kMThreads ? S - s0 : kMThreads;
+    for (int s0 = 0; s0 < S; s0 += D) {
+        const int n = S - s0 < D ? S - s0 : D;
         if (s0 > 0) {
             __syncthreads();
             if (d < n) {
@@ -437,14 +445,16 @@ __global__ void __launch_bounds__(kMThreads) merge_rows_kernel(MmaArgs m) {
     for (int o = 16; o > 0; o >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, o);
     if (lane == 0) sred[wid] = lsum;
     __syncthreads();
-    const float L = (sred[0] + sred[1]) + (sred[2] + sred[3]);
+    float L = sred[0];
+#pragma unroll
+    for (int w = 1; w < kW; ++w) L += sred[w];
     // MSE values were multiplied as fp16(op_scale * level): divide op_scale out
     const float vs = VGROUP ? 1.0f : a.vc.cq_scale;
     const int gq = row / a.Lq, l = row % a.Lq;
     const int64_t oo = (static_cast<int64_t>(b) * a.Hq + h * a.G + gq) * a.Lq + l;
     if (a.part_acc) {
         // a shard's state: max in natural-log units, sum, accumulator
-        a.part_acc[oo * kD + d] = acc * (1.0f / vs);
+        a.part_acc[oo * D + d] = acc * (1.0f / vs);
         if (d == 0) {
             a.part_ml[2 * oo] = M == -INFINITY ? -INFINITY : M * 0.6931471805599453f;
             a.part_ml[2 * oo + 1] = L;
@@ -453,37 +463,85 @@ __global__ void __launch_bounds__(kMThreads) merge_rows_kernel(MmaArgs m) {
     }
     const float x = L > 0.0f ? acc * (1.0f / (L * vs)) : 0.0f;
     if (!rotate) {
-        a.out[oo * kD + d] = x;
+        a.out[oo * D + d] = x;
         return;
     }
     so[d] = x;
     __syncthreads();
-    if (!mbar_wait(&bar, 0)) {
-        if (d == 0) atomicOr(a.err, TQ_DEVERR_TIMEOUT);
-        (void)mbar_wait(&bar, 0);
-    }
     // out[d] = sum_i row[i] R_v[i][d]: R_v's row i is one contiguous load, the
     // merged row's values are broadcasts (four at a time)
     float y0 = 0.0f, y1 = 0.0f;
     const float4* so4 = reinterpret_cast<const float4*>(so);
+    if (stage_r) {
+        if (!mbar_wait(&bar, 0)) {
+            if (d == 0) atomicOr(a.err, TQ_DEVERR_TIMEOUT);
+            (void)mbar_wait(&bar, 0);
+        }
 #pragma unroll 4
-    for (int i4 = 0; i4 < kD / 4; ++i4) {
-        const float4 v = so4[i4];
-        y0 = fmaf(v.x, sR[(4 * i4) * kD + d], y0);
-        y1 = fmaf(v.y, sR[(4 * i4 + 1) * kD + d], y1);
-        y0 = fmaf(v.z, sR[(4 * i4 + 2) * kD + d], y0);
-        y1 = fmaf(v.w, sR[(4 * i4 + 3) * kD + d], y1);
+        for (int i4 = 0; i4 < D / 4; ++i4) {
+            const float4 v = so4[i4];
+            y0 = fmaf(v.x, sR[(4 * i4) * D + d], y0);
+            y1 = fmaf(v.y, sR[(4 * i4 + 1) * D + d], y1);
+            y0 = fmaf(v.z, sR[(4 * i4 + 2) * D + d], y0);
+            y1 = fmaf(v.w, sR[(4 * i4 + 3) * D + d], y1);
+        }
+    } else {
+        const float* R = a.vc.R;
+#pragma unroll 8
+        for (int i4 = 0; i4 < D / 4; ++i4) {
+            const float4 v = so4[i4];
+            y0 = fmaf(v.x, __ldg(R + (4 * i4) * D + d), y0);
+            y1 = fmaf(v.y, __ldg(R + (4 * i4 + 1) * D + d), y1);
+            y0 = fmaf(v.z, __ldg(R + (4 * i4 + 2) * D + d), y0);
+            y1 = fmaf(v.w, __ldg(R + (4 * i4 + 3) * D + d), y1);
+        }
     }
-    a.out[oo * kD + d] = y0 + y1;
-    if (d == 0) mbar_inval(&bar);
+    a.out[oo * D + d] = y0 + y1;
+    if (stage_r && d == 0) mbar_inval(&bar);
 }
 
 // Dynamic shared memory of merge_rows_kernel.
+template <int D = kD>
 inline size_t merge_rows_smem(bool rotate) {
-    return (rotate ? static_cast<size_t>(kD) * kD * 4 : 0) + (kD + 2 * kMThreads) * 4;
+    return (rotate && D == kD ? static_cast<size_t>(kD) * kD * 4 : 0) + (2 * D + D / 32) * 4;
 }
 
-template <int KB, bool KPROD, bool VGROUP, int VB>
+// Query fragments of one unit (16 rows) from its fp32 q' and q'' rows, in the
+// layout and coordinate order qfrag_body writes for head_dim 128, over D / 16
+// k-steps: entry (which, k-step 8 c + ks, lane 4 (row % 8) + j, register
+// 2 e + (row >= 8)) holds the pair (pa, pb) of the lane's chunk j D / 128 + c.
+// Slot 1 holds q'' for prod keys and fp16(q') 's rounding remainder otherwise.
+template <int KB, int ORD, int D>
+__device__ __forceinline__ void frag_from_rows(uint32_t* dst, const float* q1, const float* q2, bool prod, float s1,
+                                               float s2, int tid, int nthreads) {
+    constexpr int KS = D / 16, NC = D / kD;
+    constexpr int kPerRow = 2 * KS * 4 * 2;
+    for (int e = tid; e < kRows * kPerRow; e += nthreads) {
+        const int rr = e / kPerRow, x = e % kPerRow;
+        const int which = x / (KS * 8), ksg = (x / 8) % KS, j = (x >> 1) & 3, ee = x & 1;
+        const int c = ksg / 8, ks = ksg % 8;
+        const int ln = 4 * (rr & 7) + j;
+        const int reg = 2 * ee + (rr >= 8 ? 1 : 0);
+        const bool qjl = which && prod;
+        int pa, pb;
+        if (qjl ? (ORD & 2) != 0 : (ORD & 1) != 0) {
+            pa = 2 * (2 * ks + ee);
+            pb = pa + 1;
+        } else {
+            mse_pair(qjl ? 1 : KB, 2 * ks + ee, pa, pb);
+        }
+        const float* q = (qjl ? q2 : q1) + rr * D + 32 * (j * NC + c);
+        const float sc = qjl ? s2 : s1;
+        float va = q[pa] * sc, vb = q[pb] * sc;
+        if (which && !qjl) {
+            va -= __half2float(__float2half_rn(va));
+            vb -= __half2float(__float2half_rn(vb));
+        }
+        dst[((which * KS + ksg) * 32 + ln) * 4 + reg] = pack_half2(va, vb);
+    }
+}
+
+template <int KB, bool KPROD, bool VGROUP, int VB, int D = kD>
 __global__ void __launch_bounds__(kThreads, 1) split_mma_kernel(MmaArgs m) {
     extern __shared__ __align__(128) unsigned char smem[];
     const DecodeArgs& a = m.a;
@@ -492,11 +550,18 @@ __global__ void __launch_bounds__(kThreads, 1) split_mma_kernel(MmaArgs m) {
     const int g = lane >> 2, j = lane & 3;
     const int Hkv = a.pool.Hkv;
     const int RG = a.plan.row_groups;
+    // head_dim D = 128 NH: each CTA takes one 128-column half h2 of the values
+    // (the output accumulator of a warp is 16 x 128); every lane decodes NC
+    // 32-coordinate chunks of each key (scores need all D coordinates)
+    static_assert(D % kD == 0, "head_dim a multiple of 128");
+    constexpr int NH = D / kD, NC = D / kD;
     const int split = blockIdx.x;
-    const int h = blockIdx.y % Hkv;
-    const int rg = blockIdx.y / Hkv;
+    const int h2 = blockIdx.y % NH;
+    const int h = (blockIdx.y / NH) % Hkv;
+    const int rg = blockIdx.y / NH / Hkv;
     const int b = blockIdx.z;
     const int unit = (b * Hkv + h) * RG + rg;
+    const int punit = unit * NH + h2;  // the half's partial rows
     const int BT = a.pool.BT;
     const int TT = st.tt;
 
@@ -673,12 +738,21 @@ __global__ void __launch_bounds__(kThreads, 1) split_mma_kernel(MmaArgs m) {
     tc::grid_wait_prior();
     for (int i = 0; i < pre; ++i)
         if (!early(i)) issue(i);
-    if (threadIdx.x == 0) {
-        tc::fence_proxy_async_global();
-        mbar_expect_tx(tbar, kQFragBytes);
-        bulk_g2s(smem + st.qs_off, m.qfrag + static_cast<int64_t>(unit) * 2 * 8 * 32, kQFragBytes, tbar);
+    if constexpr (D == kD) {
+        if (threadIdx.x == 0) {
+            tc::fence_proxy_async_global();
+            mbar_expect_tx(tbar, kQFragBytes);
+            bulk_g2s(smem + st.qs_off, m.qfrag + static_cast<int64_t>(unit) * 2 * 8 * 32, kQFragBytes, tbar);
+        }
+    } else {
+        // from the unit's fp32 q' and q'' rows (the query prep of this head_dim)
+        frag_from_rows<KB, frag_order(KB, KPROD, VGROUP, VB), D>(
+            reinterpret_cast<uint32_t*>(smem + st.qs_off), a.qrot + static_cast<int64_t>(unit) * kRows * D,
+            a.qjl + static_cast<int64_t>(unit) * kRows * D, KPROD, a.scale * kLog2e / a.kc.cq_scale,
+            a.scale * kLog2e * kSqrtHalfPi / static_cast<float>(D), threadIdx.x, kThreads);
+        if (threadIdx.x == 0) mbar_expect_tx(tbar, 0);
     }
-    __syncthreads();  // the barrier's initialisation and any tables built here
+    __syncthreads();  // the barrier's initialisation and any tables and fragments built here
     if (!mbar_wait(tbar, 0)) {
         if (threadIdx.x == 0) atomicOr(a.err, TQ_DEVERR_TIMEOUT);
         (void)mbar_wait(tbar, 0);  // no copy may still be in flight below
@@ -737,9 +811,15 @@ __global__ void __launch_bounds__(kThreads, 1) split_mma_kernel(MmaArgs m) {
             for (int nt = 0; nt < NT; ++nt) {
                 sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.0f;
                 sd[nt][0] = sd[nt][1] = sd[nt][2] = sd[nt][3] = 0.0f;
+            }
+            // the lane's 32-coordinate chunk j NC + c of each key, k-steps 8 c .. 8 c + 7
+#pragma unroll
+            for (int c = 0; c < NC; ++c) {
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
                 const int tau = base + 8 * nt + g;
-                load_words<KB>(kidx + tau * (4 * KB) + j * KB, kw[nt]);
-                if constexpr (KPROD) sw[nt] = ksgn[tau * 4 + j];
+                load_words<KB>(kidx + tau * (D / 32 * KB) + (j * NC + c) * KB, kw[nt]);
+                if constexpr (KPROD) sw[nt] = ksgn[tau * (D / 32) + j * NC + c];
                 else sw[nt] = 0u;
             }
 #pragma unroll
@@ -752,9 +832,9 @@ __global__ void __launch_bounds__(kThreads, 1) split_mma_kernel(MmaArgs m) {
                     const int ks = 2 * q2 + e;
                     uint32_t qa[4], qj[4];
                     {
-                        const uint4 v = qsm[ks * 32 + lane];
+                        const uint4 v = qsm[(8 * c + ks) * 32 + lane];
                         qa[0] = v.x; qa[1] = v.y; qa[2] = v.z; qa[3] = v.w;
-                        const uint4 w = qsm[(8 + ks) * 32 + lane];
+                        const uint4 w = qsm[(D / 16 + 8 * c + ks) * 32 + lane];
                         qj[0] = w.x; qj[1] = w.y; qj[2] = w.z; qj[3] = w.w;
                     }
 #pragma unroll
@@ -773,17 +853,19 @@ __global__ void __launch_bounds__(kThreads, 1) split_mma_kernel(MmaArgs m) {
                     }
                 }
             }
+            }
             // ---------------- values of the first 16 tokens: decoded while the
             // score MMAs are in flight (independent of the scores)
             uint32_t hA[16], hB[16];
             auto decode_values = [&](int kg) {
                 const int tA = base + 16 * kg + g, tB = tA + 8;
                 uint32_t wA[VB], wB[VB];
-                load_words<VB>(vidx + tA * (4 * VB) + j * VB, wA);
-                load_words<VB>(vidx + tB * (4 * VB) + j * VB, wB);
+                // the lane's 32-coordinate chunk 4 h2 + j of the CTA's value half
+                load_words<VB>(vidx + tA * (D / 32 * VB) + (4 * h2 + j) * VB, wA);
+                load_words<VB>(vidx + tB * (D / 32 * VB) + (4 * h2 + j) * VB, wB);
                 if constexpr (VGROUP) {
-                    const int ng = kD / a.vc.group;
-                    const int gi = (32 * j) / a.vc.group;
+                    const int ng = D / a.vc.group;
+                    const int gi = (32 * (4 * h2 + j)) / a.vc.group;
                     const float mulf = VB == 4 ? 16.0f : 4.0f;
                     const bool okA = tA < valid, okB = tB < valid;
                     const float sA = okA ? __half2float(vsc[tA * ng + gi]) : 0.0f;
@@ -998,11 +1080,11 @@ __global__ void __launch_bounds__(kThreads, 1) split_mma_kernel(MmaArgs m) {
                     acc[k] = fmaf(wt, co[(w * kRows + r) * kStride + dbase + dbase / 32 + k], acc[k]);
             }
         }
-        float* dst = m.part + ((static_cast<int64_t>(unit) * S + split) * kRows + r) * kD + dbase;
+        float* dst = m.part + ((static_cast<int64_t>(punit) * S + split) * kRows + r) * kD + dbase;
         reinterpret_cast<float4*>(dst)[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
         reinterpret_cast<float4*>(dst)[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
         if ((tid & 15) == 0) {
-            float* mlp = m.ml + ((static_cast<int64_t>(unit) * S + split) * kRows + r) * 2;
+            float* mlp = m.ml + ((static_cast<int64_t>(punit) * S + split) * kRows + r) * 2;
             mlp[0] = M;
             mlp[1] = L;
         }
@@ -1014,18 +1096,19 @@ __global__ void __launch_bounds__(kThreads, 1) split_mma_kernel(MmaArgs m) {
 cudaError_t launch_step_prep(int kb, int ord, const MmaArgs& m, const EncodeAppendArgs& e, cudaStream_t s);
 
 // The merge kernel after a split kernel: one CTA per (unit, row).
-template <bool VGROUP>
+template <bool VGROUP, int D = kD>
 cudaError_t launch_merge(const MmaArgs& m, cudaStream_t s) {
     const DecodeArgs& a = m.a;
     const bool rotate = !VGROUP && !a.part_acc;
-    const size_t smem = merge_rows_smem(rotate);
+    const size_t smem = merge_rows_smem<D>(rotate);
     static std::atomic<uint64_t> attr_set{0};
     int dev = 0;
     cudaGetDevice(&dev);
     const uint64_t bit = 1ull << (dev & 63);
     if (!(attr_set.load() & bit)) {
-        const cudaError_t e = cudaFuncSetAttribute(merge_rows_kernel<VGROUP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                   static_cast<int>(merge_rows_smem(true)));
+        const cudaError_t e = cudaFuncSetAttribute(merge_rows_kernel<VGROUP, D>,
+                                                   cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                   static_cast<int>(merge_rows_smem<D>(true)));
         if (e != cudaSuccess) {
             (void)cudaGetLastError();
             return e;
@@ -1033,9 +1116,152 @@ cudaError_t launch_merge(const MmaArgs& m, cudaStream_t s) {
         attr_set.fetch_or(bit);
     }
     const int units = a.batch * a.pool.Hkv * a.plan.row_groups;
-    const cudaError_t e = launch_overlapped(merge_rows_kernel<VGROUP>, dim3(units, kRows), dim3(kMThreads), smem, s, m);
+    const cudaError_t e = launch_overlapped(merge_rows_kernel<VGROUP, D>, dim3(units, kRows), dim3(D), smem, s, m);
     g_launches.fetch_add(1, std::memory_order_relaxed);
     return e;
+}
+
+// Opt-in of a split kernel to the largest dynamic shared memory the device
+// allows next to its static shared memory (once per device); the result is
+// that limit, or -1 with the error in *err.
+template <typename K>
+int split_smem_limit(K kernel, std::atomic<uint64_t>& attr_set, std::atomic<int>* max_dyn, cudaError_t* err) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const uint64_t bit = 1ull << (dev & 63);
+    if (!(attr_set.load() & bit)) {
+        int optin = 0;
+        cudaFuncAttributes fa{};
+        cudaError_t e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+        if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, kernel);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     optin - static_cast<int>(fa.sharedSizeBytes));
+        if (e != cudaSuccess) {
+            (void)cudaGetLastError();  // do not leave the error for the next launch
+            *err = e;
+            return -1;
+        }
+        attr_set.fetch_or(bit);
+        max_dyn[dev & 63].store(optin - static_cast<int>(fa.sharedSizeBytes));
+    }
+    return max_dyn[dev & 63].load();
+}
+
+// Query prep of head dims above 128: q' = R_k q and, for prod keys,
+// q'' = (S_k R_k) q (S_k q' up to rounding: the product is a codec table), in
+// fp32 into [unit][16][D]. CTA (unit, 32-column slice, matrix): the slice of
+// the transposed matrix (D rows of 128 B, one bulk copy each) and the unit's 16
+// query rows (contiguous in q) are staged in shared memory at once; lane c
+// owns column c of the slice, warp w rows 2 w and 2 w + 1, and each output is
+// one fp32 chain of fused multiply-adds over ascending k.
+constexpr int kQRThreads = 256;
+
+template <int D>
+__global__ void __launch_bounds__(kQRThreads) qrows_kernel(DecodeArgs a) {
+    static_assert(D % 32 == 0 && D <= kQRThreads, "one bulk copy per matrix row and thread");
+    extern __shared__ __align__(128) float qr_smem[];
+    float* ms = qr_smem;        // [D][32] the matrix slice
+    float* qs = ms + D * 32;    // [16][D] query rows
+    __shared__ uint64_t bar;
+    const int unit = blockIdx.x, c0 = 32 * blockIdx.y;
+    const bool qjl = blockIdx.z != 0;
+    const float* M = qjl ? a.kc.SRt : a.kc.Rt;
+    const int tid = threadIdx.x;
+    if (tid == 0) {
+        mbar_init(&bar, 1);
+        mbar_fence_init();
+        mbar_expect_tx(&bar, D * 32 * 4);
+    }
+    __syncthreads();
+    if (tid < D) bulk_g2s(ms + tid * 32, M + static_cast<int64_t>(tid) * D + c0, 32 * 4, &bar);
+    const int RG = a.plan.row_groups;
+    const int rg = unit % RG, bh = unit / RG;
+    const int b = bh / a.pool.Hkv, h = bh % a.pool.Hkv;
+    // row r of the group: query head h G + r / Lq, position r % Lq, at
+    // (b Hq + h G) Lq + r rows into q
+    const int64_t q0 = (static_cast<int64_t>(b) * a.Hq + h * a.G) * a.Lq + rg * kRows;
+    const int nrows = min(kRows, a.plan.rows - rg * kRows);
+#pragma unroll 4
+    for (int e = tid; e < kRows * D; e += kQRThreads) {
+        const int rr = e / D;
+        float v = 0.0f;
+        if (rr < nrows) {
+            const int64_t src = q0 * D + e;
+            if (a.q_dtype == TQ_F32) v = static_cast<const float*>(a.q)[src];
+            else if (a.q_dtype == TQ_BF16) v = __bfloat162float(static_cast<const __nv_bfloat16*>(a.q)[src]);
+            else v = __half2float(static_cast<const __half*>(a.q)[src]);
+        }
+        qs[e] = v;
+    }
+    __syncthreads();
+    if (!mbar_wait(&bar, 0)) {
+        if (tid == 0) atomicOr(a.err, TQ_DEVERR_TIMEOUT);
+        (void)mbar_wait(&bar, 0);  // no copy may still be in flight below
+    }
+    const int lane = tid & 31, w = tid >> 5;
+    const float4* x0 = reinterpret_cast<const float4*>(qs + (2 * w) * D);
+    const float4* x1 = reinterpret_cast<const float4*>(qs + (2 * w + 1) * D);
+    float y0 = 0.0f, y1 = 0.0f;
+#pragma unroll 4
+    for (int k4 = 0; k4 < D / 4; ++k4) {
+        const float4 u = x0[k4], v = x1[k4];
+        const float m0 = ms[(4 * k4) * 32 + lane], m1 = ms[(4 * k4 + 1) * 32 + lane];
+        const float m2 = ms[(4 * k4 + 2) * 32 + lane], m3 = ms[(4 * k4 + 3) * 32 + lane];
+        y0 = fmaf(m0, u.x, y0);
+        y1 = fmaf(m0, v.x, y1);
+        y0 = fmaf(m1, u.y, y0);
+        y1 = fmaf(m1, v.y, y1);
+        y0 = fmaf(m2, u.z, y0);
+        y1 = fmaf(m2, v.z, y1);
+        y0 = fmaf(m3, u.w, y0);
+        y1 = fmaf(m3, v.w, y1);
+    }
+    float* out = (qjl ? a.qjl : a.qrot) + static_cast<int64_t>(unit) * kRows * D + c0 + lane;
+    out[(2 * w) * D] = y0;       // padding rows: zero queries give zeros
+    out[(2 * w + 1) * D] = y1;
+    if (tid == 0) mbar_inval(&bar);
+}
+
+template <int D>
+constexpr size_t qrows_smem() { return static_cast<size_t>(D) * 32 * 4 + static_cast<size_t>(kRows) * D * 4; }
+
+// Head dims above 128 (two 128-column value halves per unit): the query
+// prep writes the fp32 q' and q'' rows, the split kernel builds its fragments
+// from them, then the merge.
+template <int KB, bool KPROD, bool VGROUP, int VB, int D>
+cudaError_t launch_mma_wide(const MmaArgs& m, size_t smem, cudaStream_t s) {
+    static_assert(D > kD && D % kD == 0, "a multiple of 128 above it");
+    const DecodeArgs& a = m.a;
+    static std::atomic<uint64_t> attr_set{0}, qr_set{0};
+    static std::atomic<int> max_dyn[64];
+    cudaError_t e = cudaSuccess;
+    const int lim = split_smem_limit(split_mma_kernel<KB, KPROD, VGROUP, VB, D>, attr_set, max_dyn, &e);
+    if (lim < 0) return e;
+    if (static_cast<int>(smem) > lim) return cudaErrorInvalidValue;
+    if (KPROD && !a.kc.SRt) return cudaErrorInvalidValue;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const uint64_t bit = 1ull << (dev & 63);
+    if (!(qr_set.load() & bit)) {
+        e = cudaFuncSetAttribute(qrows_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(qrows_smem<D>()));
+        if (e != cudaSuccess) {
+            (void)cudaGetLastError();
+            return e;
+        }
+        qr_set.fetch_or(bit);
+    }
+    const int units = a.batch * a.pool.Hkv * a.plan.row_groups;
+    qrows_kernel<D><<<dim3(units, D / 32, KPROD ? 2 : 1), kQRThreads, qrows_smem<D>(), s>>>(a);
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    e = launch_overlapped(split_mma_kernel<KB, KPROD, VGROUP, VB, D>,
+                          dim3(a.plan.splits, a.pool.Hkv * a.plan.row_groups * (D / kD), a.batch), dim3(kThreads),
+                          smem, s, m);
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    if (e != cudaSuccess) return e;
+    return launch_merge<VGROUP, D>(m, s);
 }
 
 template <int KB, bool KPROD, bool VGROUP, int VB>

@@ -40,6 +40,7 @@ struct CodecDev {
     const float* R;    // [D][D] row-major
     const float* Rt;   // [D][D] transposed rotation (Rt[k*D+i] = R[i][k])
     const float* St;   // [D][D] transposed QJL matrix (prod) or nullptr
+    const float* SRt;  // [D][D] transposed product S R (prod, head_dim above 128) or nullptr
     const float* c;    // centroids
     const float* m;    // midpoints
     const float* cq;   // fp16-exact operand levels op_scale * c (see HostTables)
@@ -99,7 +100,7 @@ struct QuantizeArgs {
 
 // Decode plan shared by workspace sizing and the launch.
 struct DecodePlan {
-    int kind;         // 0: SIMT kernels (any shape), 1: tensor-core kernels (head_dim 128)
+    int kind;         // 0: SIMT kernels (any shape), 1: tensor-core kernels (head_dim 128, some 256)
     int rows;         // G * Lq
     int row_groups;   // ceil(rows / 16)
     int splits;       // token splits per (sequence, kv head, row group)
@@ -115,7 +116,7 @@ struct DecodePlan {
     int vt_off;       // shared-memory offset of the 3-bit value pair table region (-1: unused)
     int kt_off;       // shared-memory offset of the 2-bit key quad table (-1: unused)
     size_t smem;      // dynamic shared memory of the split kernel
-    size_t q_bytes;   // SIMT: q' and q'' buffers (each); tensor cores: query fragments
+    size_t q_bytes;   // SIMT and head_dim 256: q' and q'' buffers (each); tensor cores at 128: query fragments
     size_t part_bytes;// partial accumulators
     size_t ml_bytes;  // partial (max, sum)
     size_t total;
@@ -252,6 +253,7 @@ struct tq_codec {
     float* d_R = nullptr;
     float* d_Rt = nullptr;
     float* d_St = nullptr;
+    float* d_SRt = nullptr;  // transposed S R (prod codecs with head_dim above 128)
     float* d_c = nullptr;
     float* d_m = nullptr;
     float* d_cq = nullptr;
