@@ -78,10 +78,10 @@ tq_status tq_decode_attention_noalloc(const tq_codec* key_codec, const tq_codec*
     }
     // The regular entry point checks every argument first, in its own order,
     // and returns TQ_ERR_CAPACITY without launching anything when the decode
-    // needs more scratch than the array holds. The decode kernels write every
-    // partial they read and the query-prep kernel zeroes the arrival counters
-    // at the start of each call, so the previous call's contents of the array
-    // need no clearing here.
+    // needs more scratch than the array holds. Every decode kernel writes each
+    // scratch value (query rows or fragments, split partials) before any
+    // kernel of the same call reads it, so the previous call's contents of the
+    // array need no clearing here.
     return tq_decode_attention(key_codec, value_codec, cache, layer, q, q_dtype, batch, num_q_heads, q_len,
                                seq_lens, block_table, max_blocks, max_seq_len, scale, out, scratch,
                                scratch ? kScratchBytes : 0, stream);
