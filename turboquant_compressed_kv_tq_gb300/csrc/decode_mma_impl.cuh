@@ -354,15 +354,20 @@ __device__ __forceinline__ void mse_chunk(const uint32_t* w, const typename MseT
 // over the splits, weights each split's (sum, accumulator) by 2^(m - max),
 // divides by the merged sum and applies the inverse value rotation (or, for a
 // shard's state, writes the merged (max, sum, accumulator) without the
-// rotation). Thread d owns output column d; at head_dim 256 the split
+// rotation). Thread d < D owns output column d; at head_dim 256 the split
 // kernel's two 128-column halves are separate partial rows (the same max and
-// sum in both).
-constexpr int kMThreads = kD;   // threads per merge CTA at head_dim 128
+// sum in both), and with MSE values the CTA has 4 D threads: quarter k of
+// them sums rows [D k / 4, D (k + 1) / 4) of the rotation (four L2 loads of
+// R_v in flight per column instead of one), the quarters' sums added in a
+// fixed order.
+template <bool VGROUP, int D>
+__host__ __device__ constexpr int merge_threads() { return D == kD || VGROUP ? D : 4 * D; }
 
 template <bool VGROUP, int D = kD>
-__global__ void __launch_bounds__(D) merge_rows_kernel(MmaArgs m) {
+__global__ void __launch_bounds__(merge_threads<VGROUP, D>()) merge_rows_kernel(MmaArgs m) {
     extern __shared__ __align__(128) unsigned char smem[];
     constexpr int NH = D / kD, kW = D / 32;
+    constexpr int kQ = merge_threads<VGROUP, D>() / D;   // rotation quarters (1: no split of the rotation)
     const DecodeArgs& a = m.a;
     tc::grid_release_dependents();  // the next kernel waits for this grid before the workspace
     const int unit = blockIdx.x, r = blockIdx.y;
@@ -371,7 +376,8 @@ __global__ void __launch_bounds__(D) merge_rows_kernel(MmaArgs m) {
     const int b = bh / a.pool.Hkv, h = bh % a.pool.Hkv;
     const int row = rg * kRows + r;
     if (row >= a.plan.rows) return;  // padding row of the last group
-    const int d = threadIdx.x, lane = d & 31, wid = d >> 5;
+    const int d = threadIdx.x % D, quarter = threadIdx.x / D, lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    const bool col = quarter == 0;   // the threads of the split merge (one per column)
     const int h2 = d / kD, cc = d % kD;
     const bool rotate = !VGROUP && !a.part_acc;
     const bool stage_r = rotate && D == kD;
@@ -379,8 +385,9 @@ __global__ void __launch_bounds__(D) merge_rows_kernel(MmaArgs m) {
     float* so = sR + (stage_r ? kD * kD : 0);        // [D] the merged row
     float* sw = so + D;                              // [D] weights of a chunk of splits
     float* sred = sw + D;                            // [kW] per-warp maxima / sums
+    float* sq = sred + kW;                           // [kQ][D] the rotation quarters' sums
     __shared__ uint64_t bar;
-    if (stage_r && d == 0) {
+    if (stage_r && threadIdx.x == 0) {
         mbar_init(&bar, 1);
         mbar_fence_init();
         mbar_expect_tx(&bar, kD * kD * 4);
@@ -397,15 +404,16 @@ __global__ void __launch_bounds__(D) merge_rows_kernel(MmaArgs m) {
     constexpr int kMPre = 32;
     float pv[kMPre];
 #pragma unroll
-    for (int s = 0; s < kMPre; ++s) pv[s] = s < S ? __ldcg(pr + static_cast<int64_t>(s) * kRows * kD) : 0.0f;
+    for (int s = 0; s < kMPre; ++s) pv[s] = col && s < S ? __ldcg(pr + static_cast<int64_t>(s) * kRows * kD) : 0.0f;
     float2 myml = make_float2(-INFINITY, 0.0f);
-    if (d < S) myml = __ldcg(reinterpret_cast<const float2*>(mlr + d * kRows * 2));
+    if (col && d < S) myml = __ldcg(reinterpret_cast<const float2*>(mlr + d * kRows * 2));
     // the row's maximum over the splits
     float mx = myml.x;
-    for (int s = d + D; s < S; s += D) mx = fmaxf(mx, __ldcg(mlr + s * kRows * 2));
+    if (col)
+        for (int s = d + D; s < S; s += D) mx = fmaxf(mx, __ldcg(mlr + s * kRows * 2));
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    if (lane == 0) sred[wid] = mx;
+    if (col && lane == 0) sred[wid] = mx;
     __syncthreads();
     float M = sred[0];
 #pragma unroll
@@ -413,7 +421,7 @@ __global__ void __launch_bounds__(D) merge_rows_kernel(MmaArgs m) {
     // weights 2^(m - M) of the first D splits (a split that saw no score has
     // (-inf, 0) and a zero accumulator); thread d's share of the sum
     float lsum = 0.0f;
-    if (d < S) {
+    if (col && d < S) {
         const float w = myml.x == -INFINITY ? 0.0f : ex2(myml.x - M);
         sw[d] = w;
         lsum = w * myml.y;
@@ -428,7 +436,7 @@ __global__ void __launch_bounds__(D) merge_rows_kernel(MmaArgs m) {
         const int n = S - s0 < D ? S - s0 : D;
         if (s0 > 0) {
             __syncthreads();
-            if (d < n) {
+            if (col && d < n) {
                 const float2 ml = __ldcg(reinterpret_cast<const float2*>(mlr + (s0 + d) * kRows * 2));
                 const float w = ml.x == -INFINITY ? 0.0f : ex2(ml.x - M);
                 sw[d] = w;
@@ -436,14 +444,16 @@ __global__ void __launch_bounds__(D) merge_rows_kernel(MmaArgs m) {
             }
             __syncthreads();
         }
+        if (col) {
 #pragma unroll 8
-        for (int s = s0 > 0 ? 0 : kMPre; s < n; ++s)
-            acc = fmaf(sw[s], __ldcg(pr + static_cast<int64_t>(s0 + s) * kRows * kD), acc);
+            for (int s = s0 > 0 ? 0 : kMPre; s < n; ++s)
+                acc = fmaf(sw[s], __ldcg(pr + static_cast<int64_t>(s0 + s) * kRows * kD), acc);
+        }
     }
     __syncthreads();
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, o);
-    if (lane == 0) sred[wid] = lsum;
+    if (col && lane == 0) sred[wid] = lsum;
     __syncthreads();
     float L = sred[0];
 #pragma unroll
@@ -454,6 +464,7 @@ __global__ void __launch_bounds__(D) merge_rows_kernel(MmaArgs m) {
     const int64_t oo = (static_cast<int64_t>(b) * a.Hq + h * a.G + gq) * a.Lq + l;
     if (a.part_acc) {
         // a shard's state: max in natural-log units, sum, accumulator
+        if (!col) return;
         a.part_acc[oo * D + d] = acc * (1.0f / vs);
         if (d == 0) {
             a.part_ml[2 * oo] = M == -INFINITY ? -INFINITY : M * 0.6931471805599453f;
@@ -463,10 +474,10 @@ __global__ void __launch_bounds__(D) merge_rows_kernel(MmaArgs m) {
     }
     const float x = L > 0.0f ? acc * (1.0f / (L * vs)) : 0.0f;
     if (!rotate) {
-        a.out[oo * D + d] = x;
+        if (col) a.out[oo * D + d] = x;
         return;
     }
-    so[d] = x;
+    if (col) so[d] = x;
     __syncthreads();
     // out[d] = sum_i row[i] R_v[i][d]: R_v's row i is one contiguous load, the
     // merged row's values are broadcasts (four at a time)
@@ -486,24 +497,36 @@ __global__ void __launch_bounds__(D) merge_rows_kernel(MmaArgs m) {
             y1 = fmaf(v.w, sR[(4 * i4 + 3) * D + d], y1);
         }
     } else {
-        const float* R = a.vc.R;
+        // rows [D quarter / kQ, D (quarter + 1) / kQ) of R_v, from L2
+        const float* R = a.vc.R + static_cast<int64_t>(quarter) * (D / kQ) * D;
+        const float4* sq4 = so4 + quarter * (D / kQ / 4);
 #pragma unroll 8
-        for (int i4 = 0; i4 < D / 4; ++i4) {
-            const float4 v = so4[i4];
+        for (int i4 = 0; i4 < D / kQ / 4; ++i4) {
+            const float4 v = sq4[i4];
             y0 = fmaf(v.x, __ldg(R + (4 * i4) * D + d), y0);
             y1 = fmaf(v.y, __ldg(R + (4 * i4 + 1) * D + d), y1);
             y0 = fmaf(v.z, __ldg(R + (4 * i4 + 2) * D + d), y0);
             y1 = fmaf(v.w, __ldg(R + (4 * i4 + 3) * D + d), y1);
         }
+        if constexpr (kQ > 1) {
+            sq[quarter * D + d] = y0 + y1;
+            __syncthreads();
+            if (!col) return;
+            y0 = sq[d];
+            y1 = 0.0f;
+#pragma unroll
+            for (int k = 1; k < kQ; ++k) y0 += sq[k * D + d];
+        }
     }
     a.out[oo * D + d] = y0 + y1;
-    if (stage_r && d == 0) mbar_inval(&bar);
+    if (stage_r && threadIdx.x == 0) mbar_inval(&bar);
 }
 
 // Dynamic shared memory of merge_rows_kernel.
-template <int D = kD>
+template <bool VGROUP, int D = kD>
 inline size_t merge_rows_smem(bool rotate) {
-    return (rotate && D == kD ? static_cast<size_t>(kD) * kD * 4 : 0) + (2 * D + D / 32) * 4;
+    constexpr int nt = merge_threads<VGROUP, D>();
+    return (rotate && D == kD ? static_cast<size_t>(kD) * kD * 4 : 0) + (2 * D + D / 32 + (nt > D ? nt : 0)) * 4;
 }
 
 // Query fragments of one unit (16 rows) from its fp32 q' and q'' rows, in the
@@ -511,33 +534,60 @@ inline size_t merge_rows_smem(bool rotate) {
 // k-steps: entry (which, k-step 8 c + ks, lane 4 (row % 8) + j, register
 // 2 e + (row >= 8)) holds the pair (pa, pb) of the lane's chunk j D / 128 + c.
 // Slot 1 holds q'' for prod keys and fp16(q') 's rounding remainder otherwise.
-template <int KB, int ORD, int D>
+// A block of NT threads: every thread issues all of its loads (L2) before it
+// converts any, so the rows arrive in one round trip.
+template <int KB, int ORD, int D, int NT>
 __device__ __forceinline__ void frag_from_rows(uint32_t* dst, const float* q1, const float* q2, bool prod, float s1,
-                                               float s2, int tid, int nthreads) {
+                                               float s2, int tid) {
     constexpr int KS = D / 16, NC = D / kD;
     constexpr int kPerRow = 2 * KS * 4 * 2;
-    for (int e = tid; e < kRows * kPerRow; e += nthreads) {
+    constexpr int kTotal = kRows * kPerRow, kIter = (kTotal + NT - 1) / NT;
+    // entry e: (row, which, k-step, lane chunk j, e) and the source pair
+    auto where = [&](int e, int& out, const float*& q, int& pa, int& pb, bool& qjl, bool& rem) {
         const int rr = e / kPerRow, x = e % kPerRow;
         const int which = x / (KS * 8), ksg = (x / 8) % KS, j = (x >> 1) & 3, ee = x & 1;
         const int c = ksg / 8, ks = ksg % 8;
-        const int ln = 4 * (rr & 7) + j;
-        const int reg = 2 * ee + (rr >= 8 ? 1 : 0);
-        const bool qjl = which && prod;
-        int pa, pb;
+        out = ((which * KS + ksg) * 32 + 4 * (rr & 7) + j) * 4 + 2 * ee + (rr >= 8 ? 1 : 0);
+        qjl = which && prod;
+        rem = which && !prod;
         if (qjl ? (ORD & 2) != 0 : (ORD & 1) != 0) {
             pa = 2 * (2 * ks + ee);
             pb = pa + 1;
         } else {
             mse_pair(qjl ? 1 : KB, 2 * ks + ee, pa, pb);
         }
-        const float* q = (qjl ? q2 : q1) + rr * D + 32 * (j * NC + c);
-        const float sc = qjl ? s2 : s1;
-        float va = q[pa] * sc, vb = q[pb] * sc;
-        if (which && !qjl) {
-            va -= __half2float(__float2half_rn(va));
-            vb -= __half2float(__float2half_rn(vb));
+        q = (qjl ? q2 : q1) + rr * D + 32 * (j * NC + c);
+    };
+    float va[kIter], vb[kIter];
+#pragma unroll
+    for (int it = 0; it < kIter; ++it) {
+        const int e = tid + it * NT;
+        va[it] = vb[it] = 0.0f;
+        if (e < kTotal) {
+            int out, pa, pb;
+            const float* q;
+            bool qjl, rem;
+            where(e, out, q, pa, pb, qjl, rem);
+            va[it] = __ldcg(q + pa);
+            vb[it] = __ldcg(q + pb);
         }
-        dst[((which * KS + ksg) * 32 + ln) * 4 + reg] = pack_half2(va, vb);
+    }
+#pragma unroll
+    for (int it = 0; it < kIter; ++it) {
+        const int e = tid + it * NT;
+        if (e < kTotal) {
+            int out, pa, pb;
+            const float* q;
+            bool qjl, rem;
+            where(e, out, q, pa, pb, qjl, rem);
+            const float sc = qjl ? s2 : s1;
+            float a = va[it] * sc, b = vb[it] * sc;
+            if (rem) {
+                a -= __half2float(__float2half_rn(a));
+                b -= __half2float(__float2half_rn(b));
+            }
+            dst[out] = pack_half2(a, b);
+        }
     }
 }
 
@@ -746,10 +796,10 @@ __global__ void __launch_bounds__(kThreads, 1) split_mma_kernel(MmaArgs m) {
         }
     } else {
         // from the unit's fp32 q' and q'' rows (the query prep of this head_dim)
-        frag_from_rows<KB, frag_order(KB, KPROD, VGROUP, VB), D>(
+        frag_from_rows<KB, frag_order(KB, KPROD, VGROUP, VB), D, kThreads>(
             reinterpret_cast<uint32_t*>(smem + st.qs_off), a.qrot + static_cast<int64_t>(unit) * kRows * D,
             a.qjl + static_cast<int64_t>(unit) * kRows * D, KPROD, a.scale * kLog2e / a.kc.cq_scale,
-            a.scale * kLog2e * kSqrtHalfPi / static_cast<float>(D), threadIdx.x, kThreads);
+            a.scale * kLog2e * kSqrtHalfPi / static_cast<float>(D), threadIdx.x);
         if (threadIdx.x == 0) mbar_expect_tx(tbar, 0);
     }
     __syncthreads();  // the barrier's initialisation and any tables and fragments built here
@@ -1100,7 +1150,7 @@ template <bool VGROUP, int D = kD>
 cudaError_t launch_merge(const MmaArgs& m, cudaStream_t s) {
     const DecodeArgs& a = m.a;
     const bool rotate = !VGROUP && !a.part_acc;
-    const size_t smem = merge_rows_smem<D>(rotate);
+    const size_t smem = merge_rows_smem<VGROUP, D>(rotate);
     static std::atomic<uint64_t> attr_set{0};
     int dev = 0;
     cudaGetDevice(&dev);
@@ -1108,7 +1158,7 @@ cudaError_t launch_merge(const MmaArgs& m, cudaStream_t s) {
     if (!(attr_set.load() & bit)) {
         const cudaError_t e = cudaFuncSetAttribute(merge_rows_kernel<VGROUP, D>,
                                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                   static_cast<int>(merge_rows_smem<D>(true)));
+                                                   static_cast<int>(merge_rows_smem<VGROUP, D>(true)));
         if (e != cudaSuccess) {
             (void)cudaGetLastError();
             return e;
@@ -1116,7 +1166,7 @@ cudaError_t launch_merge(const MmaArgs& m, cudaStream_t s) {
         attr_set.fetch_or(bit);
     }
     const int units = a.batch * a.pool.Hkv * a.plan.row_groups;
-    const cudaError_t e = launch_overlapped(merge_rows_kernel<VGROUP, D>, dim3(units, kRows), dim3(D), smem, s, m);
+    const cudaError_t e = launch_overlapped(merge_rows_kernel<VGROUP, D>, dim3(units, kRows), dim3(merge_threads<VGROUP, D>()), smem, s, m);
     g_launches.fetch_add(1, std::memory_order_relaxed);
     return e;
 }
