@@ -233,8 +233,24 @@ def test_decode_plan_split_rule(libtq):
     assert one["splits"] == 19 and one["chunk_tokens"] == 13824
     many = tq.tq_decode_plan(d, 32, 32, 1, 65536, 152)       # 256 units >= 152 SMs: split by length only
     assert many["splits"] == 4 and many["chunk_tokens"] == 16384
-    short = tq.tq_decode_plan(d, 1, 64, 2, 100, 152)         # a short sequence: one 64-token tile per split
-    assert short["chunk_tokens"] == 64 and short["splits"] == 2
+    short = tq.tq_decode_plan(d, 1, 64, 2, 100, 152)         # a short sequence: one 32-token tile per split
+    assert short["chunk_tokens"] == 32 and short["splits"] == 4
+
+
+def test_decode_plan_tile_balances_the_busiest_warp(libtq):
+    # 64-token tiles unless 32-token tiles (each about 0.52 of a 64-token
+    # tile's time) give the busiest of the 12 warps less work: at 256k a split
+    # holds 216 tiles (18 per warp) or 432 half tiles (36 x 0.52 = 18.7); at
+    # 32k, 27 tiles (3 for the busiest warp) or 54 half tiles (5 x 0.52 = 2.6)
+    d = _desc_from_oracle(128, ("prod", 3), ("mse", 3, 0), 256, 8)
+    assert tq.tq_decode_plan(d, 1, 64, 2, 262146, 152)["tile_tokens"] == 64
+    d = _desc_from_oracle(128, ("mse", 4), ("mse", 4, 0), 256, 8)
+    p = tq.tq_decode_plan(d, 1, 64, 2, 32768, 152)
+    assert p["tile_tokens"] == 32 and p["splits"] == 19 and p["chunk_tokens"] == 1728
+    # 32 sequences of up to 64k: splits of 16384 tokens, 256 tiles (22 for the
+    # busiest warp) against 512 half tiles (43 x 0.52 = 22.4)
+    d = _desc_from_oracle(128, ("prod", 3), ("group", 4, 64), 16, 8)
+    assert tq.tq_decode_plan(d, 32, 32, 1, 65536, 152)["tile_tokens"] == 64
 
 
 # ------------------------------------------------------------------ host-side argument checks

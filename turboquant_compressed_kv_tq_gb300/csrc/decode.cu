@@ -510,6 +510,20 @@ DecodePlan make_decode_plan(const tq_cache_desc* d, int batch, int G, int Lq, in
             layout(tile);
         }
         choose_splits(p, units * NH, num_sms, max_seq_len, p.tile, 16384);
+        // A CTA's time is its busiest warp's: ceil(tiles of a split / warps)
+        // tiles. Where 64-token tiles leave that warp a tile more than the
+        // average (short splits), 32-token tiles (each about 0.52 of a 64-token
+        // tile's time, per-tile overheads included) can balance better.
+        if (tile == 64) {
+            auto busiest = [&](const DecodePlan& q) {
+                const int tiles = (q.chunk + q.tile - 1) / q.tile;
+                return (tiles + mmadec::kWarps - 1) / mmadec::kWarps;
+            };
+            const DecodePlan h = p;   // the 64-token plan
+            layout(32);
+            choose_splits(p, units * NH, num_sms, max_seq_len, 32, 16384);
+            if (100 * busiest(h) <= 52 * busiest(p) || p.smem > mmadec::kSmemBudget) p = h;
+        }
         // head_dim 128: the units' query fragments; above it the fp32 q' and
         // q'' rows of the SIMT query prep (two arrays of q_bytes)
         p.q_bytes = NH == 1 ? al256(static_cast<size_t>(units) * 2 * 8 * 32 * 16)
