@@ -381,7 +381,10 @@ typedef struct {
     int row_groups;      /* 16-row groups per (sequence, KV head): ceil(G * q_len / 16)    */
     int splits;          /* token splits per (sequence, KV head, row group)               */
     int chunk_tokens;    /* tokens per split (a multiple of tile_tokens)                  */
-    int tile_tokens;     /* tokens per shared-memory stage (divides block_tokens)         */
+    int tile_tokens;     /* tokens per shared-memory stage: divides block_tokens, or      *
+                          * gathers up to four whole blocks; 64 unless 32 balances the    *
+                          * CTA's warps better or the stages would not fit next to the    *
+                          * lookup tables                                                 */
     size_t smem_bytes;   /* dynamic shared memory of the split kernel (tensor cores)     */
     size_t workspace_bytes; /* as tq_decode_workspace_bytes for num_sms SMs              */
 } tq_decode_plan_info;
