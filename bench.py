@@ -222,13 +222,18 @@ class OracleSample:
                 f"{self.nbytes / 1e6:.1f} MB of compressed records per sample")
 
 
-def cpu_baseline(w, kv_heads=2, device="cuda", repeats=3):
-    """Oracle decode throughput on the host cores (GB/s of compressed bytes),
-    median of `repeats` timed samples. Returns (value, cores, sample, seconds)."""
+def cpu_baseline(w, kv_heads=2, device="cuda", min_repeats=3, min_seconds=10.0, max_repeats=60):
+    """Oracle decode throughput on the host cores (GB/s of compressed bytes):
+    the median of timed samples, repeated until about `min_seconds` of decode
+    work (at least `min_repeats`, at most `max_repeats`). Returns (value,
+    cores, sample, seconds)."""
     smp = OracleSample(w, kv_heads, device)
-    times = [smp.decode_seconds() for _ in range(repeats)]
+    times = []
+    while len(times) < max_repeats and (len(times) < min_repeats or sum(times) < min_seconds):
+        times.append(smp.decode_seconds())
     t = statistics.median(times)
-    return smp.nbytes / t / 1e9, smp.O.num_threads(), smp.describe(), sum(times)
+    desc = smp.describe() + f"; median of {len(times)} timed decodes"
+    return smp.nbytes / t / 1e9, smp.O.num_threads(), desc, sum(times)
 
 
 def _workload(args):

@@ -203,6 +203,22 @@ def test_decode_plan_simt_shapes(libtq):
         assert p["splits"] * p["chunk_tokens"] >= 8192 and p["workspace_bytes"] > 0
 
 
+def test_decode_plan_head_dim_256_codec_set(libtq):
+    # the head_dim-256 tensor-core kernels: prod 3-bit keys with group 2/4-bit
+    # or MSE 3/4-bit values, and MSE 4-bit keys and values; the rest SIMT
+    tc = {(("prod", 3), ("group", 2, 32)), (("prod", 3), ("group", 2, 64)), (("prod", 3), ("group", 4, 32)),
+          (("prod", 3), ("group", 4, 64)), (("prod", 3), ("mse", 3, 0)), (("prod", 3), ("mse", 4, 0)),
+          (("mse", 4), ("mse", 4, 0))}
+    for key in (("prod", 2), ("prod", 3), ("prod", 4), ("mse", 2), ("mse", 3), ("mse", 4)):
+        for value in (("group", 2, 32), ("group", 2, 64), ("group", 4, 32), ("group", 4, 64), ("mse", 2, 0),
+                      ("mse", 3, 0), ("mse", 4, 0)):
+            d = _desc_from_oracle(256, key, value, 64, 2)
+            p = tq.tq_decode_plan(d, 2, 16, 2, 8192, 152)
+            assert p["tensor_cores"] == ((key, value) in tc), (key, value, p)
+            if p["tensor_cores"]:
+                assert p["tile_tokens"] == 32 and 0 < p["smem_bytes"] <= _SMEM_LIMIT - 1024, (key, value, p)
+
+
 @pytest.mark.parametrize("value", [("group", 2, 32), ("mse", 3, 1)])
 def test_decode_plan_head_dim_256_tensor_cores(libtq, value):
     # prod 3-bit keys with group 2-bit or MSE 3-bit values at head_dim 256:

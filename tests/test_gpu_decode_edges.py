@@ -105,11 +105,13 @@ def _plan(w):
     return case, tq.tq_decode_plan(case.cache.desc, w.batch, w.num_q_heads, w.q_len, max(w.seq_lens), sms)
 
 
-@pytest.mark.parametrize("value", [("group", 2, 32), ("mse", 3), ("group", 2, 64)])
-def test_head_dim_256_tile_edges(value):
-    # 32-token tiles at head_dim 256: sequences around one tile, 64-token
-    # blocks, q_len 2 x GQA 8
-    w = _workload(("prod", 3), value, (2, 31, 32, 33, 700), 2, 2, 8, 64, D=256)
+@pytest.mark.parametrize("key,value", [(("prod", 3), ("group", 2, 32)), (("prod", 3), ("mse", 3)),
+                                       (("prod", 3), ("group", 2, 64)), (("prod", 3), ("group", 4, 64)),
+                                       (("prod", 3), ("mse", 4)), (("mse", 4), ("mse", 4))])
+def test_head_dim_256_tile_edges(key, value):
+    # 32-token tiles at head_dim 256, every codec pair of its tensor-core
+    # kernels: sequences around one tile, 64-token blocks, q_len 2 x GQA 8
+    w = _workload(key, value, (2, 31, 32, 33, 700), 2, 2, 8, 64, D=256)
     _, plan = _plan(w)
     assert plan["tensor_cores"] == 1, plan
     _check(w)

@@ -1,12 +1,15 @@
-// Instantiations of the tensor-core decode kernel for head_dim 256: 2-bit key
-// indices (prod 3-bit keys) with 2-bit group values or 3-bit MSE values.
+// Instantiations of the tensor-core decode kernel for head_dim 256: prod
+// 3-bit keys (2-bit indices) with 2- or 4-bit group values or 3- or 4-bit MSE
+// values, and 4-bit MSE keys with 4-bit MSE values.
 #include "decode_mma_impl.cuh"
 
 namespace tq {
 namespace mmadec {
 
 bool wide_supported(int D, int kb, bool prod, bool vgroup, int vb) {
-    return D == 256 && kb == 2 && prod && ((vgroup && vb == 2) || (!vgroup && vb == 3));
+    if (D != 256) return false;
+    if (kb == 2 && prod) return vgroup ? (vb == 2 || vb == 4) : (vb == 3 || vb == 4);
+    return kb == 4 && !prod && !vgroup && vb == 4;
 }
 
 bool dispatch_d(int D, int kb, bool prod, bool vgroup, int vb, const MmaArgs& m, size_t smem, cudaStream_t s,
@@ -17,6 +20,18 @@ bool dispatch_d(int D, int kb, bool prod, bool vgroup, int vb, const MmaArgs& m,
     }
     if (D == 256 && kb == 2 && prod && !vgroup && vb == 3) {
         *err = launch_mma_wide<2, true, false, 3, 256>(m, smem, s);
+        return true;
+    }
+    if (D == 256 && kb == 2 && prod && vgroup && vb == 4) {
+        *err = launch_mma_wide<2, true, true, 4, 256>(m, smem, s);
+        return true;
+    }
+    if (D == 256 && kb == 2 && prod && !vgroup && vb == 4) {
+        *err = launch_mma_wide<2, true, false, 4, 256>(m, smem, s);
+        return true;
+    }
+    if (D == 256 && kb == 4 && !prod && !vgroup && vb == 4) {
+        *err = launch_mma_wide<4, false, false, 4, 256>(m, smem, s);
         return true;
     }
     return false;
