@@ -509,7 +509,11 @@ DecodePlan make_decode_plan(const tq_cache_desc* d, int batch, int G, int Lq, in
             tile /= 2;
             layout(tile);
         }
-        choose_splits(p, units * NH, num_sms, max_seq_len, p.tile, 16384);
+        // At most 16384 tokens per split; where the units alone fill the GPU
+        // (several waves of CTAs) at most 8192, so that the last wave's CTAs,
+        // the grid's tail, are short.
+        const int max_chunk = units * NH >= num_sms ? 8192 : 16384;
+        choose_splits(p, units * NH, num_sms, max_seq_len, p.tile, max_chunk);
         // A CTA's time is its busiest warp's: ceil(tiles of a split / warps)
         // tiles. Where 64-token tiles leave that warp a tile more than the
         // average (short splits), 32-token tiles (each about 0.52 of a 64-token
@@ -521,7 +525,7 @@ DecodePlan make_decode_plan(const tq_cache_desc* d, int batch, int G, int Lq, in
             };
             const DecodePlan h = p;   // the 64-token plan
             layout(32);
-            choose_splits(p, units * NH, num_sms, max_seq_len, 32, 16384);
+            choose_splits(p, units * NH, num_sms, max_seq_len, 32, max_chunk);
             if (100 * busiest(h) <= 52 * busiest(p) || p.smem > mmadec::kSmemBudget) p = h;
         }
         // head_dim 128: the units' query fragments; above it the fp32 q' and
