@@ -243,13 +243,13 @@ def test_decode_plan_head_dim_256_tensor_cores(libtq, value):
 
 def test_decode_plan_split_rule(libtq):
     # splits: enough CTAs to cover the SMs, each split a multiple of the tile
-    # and at most 16384 tokens, or 8192 where the units alone fill the SMs
-    # (several waves of CTAs: short CTAs keep the last wave's tail short)
+    # and at most 16384 tokens, or 12288 where the units alone fill the SMs
+    # (several waves of CTAs: shorter CTAs keep the last wave's tail short)
     d = _desc_from_oracle(128, ("prod", 3), ("mse", 3, 0), 256, 8)
     one = tq.tq_decode_plan(d, 1, 64, 2, 262146, 152)        # 8 units -> 19 splits of 13,824 tokens
     assert one["splits"] == 19 and one["chunk_tokens"] == 13824
     many = tq.tq_decode_plan(d, 32, 32, 1, 65536, 152)       # 256 units >= 152 SMs: split by length only
-    assert many["splits"] == 8 and many["chunk_tokens"] == 8192
+    assert many["splits"] == 6 and many["chunk_tokens"] == 12288
     few = tq.tq_decode_plan(d, 18, 64, 2, 65536, 152)        # 144 units < 152 SMs: 16384-token splits
     assert few["splits"] == 4 and few["chunk_tokens"] == 16384
     short = tq.tq_decode_plan(d, 1, 64, 2, 100, 152)         # a short sequence: one 32-token tile per split
@@ -266,8 +266,8 @@ def test_decode_plan_tile_balances_the_busiest_warp(libtq):
     d = _desc_from_oracle(128, ("mse", 4), ("mse", 4, 0), 256, 8)
     p = tq.tq_decode_plan(d, 1, 64, 2, 32768, 152)
     assert p["tile_tokens"] == 32 and p["splits"] == 19 and p["chunk_tokens"] == 1728
-    # 32 sequences of up to 64k: splits of 8192 tokens, 128 tiles (11 for the
-    # busiest warp) against 256 half tiles (22 x 0.52 = 11.4)
+    # 32 sequences of up to 64k: splits of 12288 tokens, 192 tiles (16 for the
+    # busiest warp) against 384 half tiles (32 x 0.52 = 16.6)
     d = _desc_from_oracle(128, ("prod", 3), ("group", 4, 64), 16, 8)
     assert tq.tq_decode_plan(d, 32, 32, 1, 65536, 152)["tile_tokens"] == 64
 

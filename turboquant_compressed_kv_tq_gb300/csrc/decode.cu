@@ -510,9 +510,9 @@ DecodePlan make_decode_plan(const tq_cache_desc* d, int batch, int G, int Lq, in
             layout(tile);
         }
         // At most 16384 tokens per split; where the units alone fill the GPU
-        // (several waves of CTAs) at most 8192, so that the last wave's CTAs,
+        // (several waves of CTAs) at most 12288, so that the last wave's CTAs,
         // the grid's tail, are short.
-        const int max_chunk = units * NH >= num_sms ? 8192 : 16384;
+        const int max_chunk = units * NH >= num_sms ? 12288 : 16384;
         choose_splits(p, units * NH, num_sms, max_seq_len, p.tile, max_chunk);
         // A CTA's time is its busiest warp's: ceil(tiles of a split / warps)
         // tiles. Where 64-token tiles leave that warp a tile more than the
@@ -552,6 +552,7 @@ DecodePlan make_decode_plan(const tq_cache_desc* d, int batch, int G, int Lq, in
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s, const EncodeAppendArgs* step) {
     if (a.batch == 0) return cudaSuccess;
     if (a.plan.kind == 1) {
+        if (a.plan.splits > 65535) return cudaErrorInvalidValue;  // the split kernel's grid z
         mmadec::MmaArgs m{};
         m.a = a;
         m.st.tt = a.plan.tile;

@@ -605,11 +605,14 @@ __global__ void __launch_bounds__(kThreads, 1) split_mma_kernel(MmaArgs m) {
     // 32-coordinate chunks of each key (scores need all D coordinates)
     static_assert(D % kD == 0, "head_dim a multiple of 128");
     constexpr int NH = D / kD, NC = D / kD;
-    const int split = blockIdx.x;
-    const int h2 = blockIdx.y % NH;
-    const int h = (blockIdx.y / NH) % Hkv;
-    const int rg = blockIdx.y / NH / Hkv;
-    const int b = blockIdx.z;
+    // grid (KV head x row group x half, sequence, split): CTAs are dispatched
+    // split by split, so every unit's full first splits run before the
+    // shorter (last, partial) and empty ones, which make up the last wave
+    const int split = blockIdx.z;
+    const int h2 = blockIdx.x % NH;
+    const int h = (blockIdx.x / NH) % Hkv;
+    const int rg = blockIdx.x / NH / Hkv;
+    const int b = blockIdx.y;
     const int unit = (b * Hkv + h) * RG + rg;
     const int punit = unit * NH + h2;  // the half's partial rows
     const int BT = a.pool.BT;
@@ -1307,7 +1310,7 @@ cudaError_t launch_mma_wide(const MmaArgs& m, size_t smem, cudaStream_t s) {
     g_launches.fetch_add(1, std::memory_order_relaxed);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     e = launch_overlapped(split_mma_kernel<KB, KPROD, VGROUP, VB, D>,
-                          dim3(a.plan.splits, a.pool.Hkv * a.plan.row_groups * (D / kD), a.batch), dim3(kThreads),
+                          dim3(a.pool.Hkv * a.plan.row_groups * (D / kD), a.batch, a.plan.splits), dim3(kThreads),
                           smem, s, m);
     g_launches.fetch_add(1, std::memory_order_relaxed);
     if (e != cudaSuccess) return e;
@@ -1346,7 +1349,7 @@ cudaError_t launch_mma(const MmaArgs& m, size_t smem, cudaStream_t s, const Enco
     if (step) {
         e = launch_step_prep(KB, frag_order(KB, KPROD, VGROUP, VB), m, *step, s);
         if (e != cudaSuccess) return e;
-        e = launch_overlapped(split_mma_kernel<KB, KPROD, VGROUP, VB>, dim3(a.plan.splits, a.pool.Hkv * RG, a.batch),
+        e = launch_overlapped(split_mma_kernel<KB, KPROD, VGROUP, VB>, dim3(a.pool.Hkv * RG, a.batch, a.plan.splits),
                               dim3(kThreads), smem, s, m);
         g_launches.fetch_add(1, std::memory_order_relaxed);
         if (e != cudaSuccess) return e;
@@ -1368,7 +1371,7 @@ cudaError_t launch_mma(const MmaArgs& m, size_t smem, cudaStream_t s, const Enco
                           sizeof(QSmem), s, m);
     g_launches.fetch_add(1, std::memory_order_relaxed);
     if (e != cudaSuccess) return e;
-    e = launch_overlapped(split_mma_kernel<KB, KPROD, VGROUP, VB>, dim3(a.plan.splits, a.pool.Hkv * RG, a.batch),
+    e = launch_overlapped(split_mma_kernel<KB, KPROD, VGROUP, VB>, dim3(a.pool.Hkv * RG, a.batch, a.plan.splits),
                           dim3(kThreads), smem, s, m);
     g_launches.fetch_add(1, std::memory_order_relaxed);
     if (e != cudaSuccess) return e;
