@@ -376,9 +376,9 @@ tq_status tq_decode_workspace_bytes(const tq_cache_desc *cache, int batch, int n
 /* Launch shape tq_decode_attention would use (host arithmetic only; the pages
  * have no counterpart: this exists so callers can inspect and size a decode). */
 typedef struct {
-    int tensor_cores;    /* 1: tensor-core split kernel (head_dim 128; 256 with prod 3-bit
-                          *    keys and group 2/4-bit or MSE 3/4-bit values, or MSE 4-bit
-                          *    keys and values); 0: SIMT kernels                          */
+    int tensor_cores;    /* 1: tensor-core split kernel (head_dim 128; 64 and 256 with prod *
+                          *    3-bit keys and group 2/4-bit or MSE 3/4-bit values, or MSE  *
+                          *    4-bit keys and values); 0: SIMT kernels                     */
     int row_groups;      /* 16-row groups per (sequence, KV head): ceil(G * q_len / 16)    */
     int splits;          /* token splits per (sequence, KV head, row group)               */
     int chunk_tokens;    /* tokens per split (a multiple of tile_tokens)                  */

@@ -203,20 +203,32 @@ def test_decode_plan_simt_shapes(libtq):
         assert p["splits"] * p["chunk_tokens"] >= 8192 and p["workspace_bytes"] > 0
 
 
-def test_decode_plan_head_dim_256_codec_set(libtq):
-    # the head_dim-256 tensor-core kernels: prod 3-bit keys with group 2/4-bit
-    # or MSE 3/4-bit values, and MSE 4-bit keys and values; the rest SIMT
+@pytest.mark.parametrize("D", [64, 256])
+def test_decode_plan_head_dim_64_256_codec_set(libtq, D):
+    # the head_dim-64 and -256 tensor-core kernels: prod 3-bit keys with group
+    # 2/4-bit or MSE 3/4-bit values, and MSE 4-bit keys and values; the rest
+    # SIMT. At 64 the partial rows are 128 columns wide (the head_dim-128
+    # layout); at 256 the stages hold 32 tokens (64-token stages do not fit).
     tc = {(("prod", 3), ("group", 2, 32)), (("prod", 3), ("group", 2, 64)), (("prod", 3), ("group", 4, 32)),
           (("prod", 3), ("group", 4, 64)), (("prod", 3), ("mse", 3, 0)), (("prod", 3), ("mse", 4, 0)),
           (("mse", 4), ("mse", 4, 0))}
     for key in (("prod", 2), ("prod", 3), ("prod", 4), ("mse", 2), ("mse", 3), ("mse", 4)):
         for value in (("group", 2, 32), ("group", 2, 64), ("group", 4, 32), ("group", 4, 64), ("mse", 2, 0),
                       ("mse", 3, 0), ("mse", 4, 0)):
-            d = _desc_from_oracle(256, key, value, 64, 2)
+            if D == 64 and value[0] == "group" and value[2] > 64:
+                continue
+            d = _desc_from_oracle(D, key, value, 64, 2)
             p = tq.tq_decode_plan(d, 2, 16, 2, 8192, 152)
             assert p["tensor_cores"] == ((key, value) in tc), (key, value, p)
             if p["tensor_cores"]:
-                assert p["tile_tokens"] == 32 and 0 < p["smem_bytes"] <= _SMEM_LIMIT - 1024, (key, value, p)
+                assert p["tile_tokens"] in ((32,) if D == 256 else (32, 64)), (key, value, p)
+                assert 0 < p["smem_bytes"] <= _SMEM_LIMIT - 1024, (key, value, p)
+                units, S = 2 * 2, p["splits"]   # 2 sequences x 2 KV heads x 1 row group
+                r = lambda x: (x + 255) // 256 * 256
+                q = r(units * 16 * D * 4)
+                part = r(units * S * 16 * max(D, 128) * 4)
+                ml = r(units * max(D // 128, 1) * S * 16 * 2 * 4)
+                assert p["workspace_bytes"] == 2 * q + part + ml, (key, value, p)
 
 
 @pytest.mark.parametrize("value", [("group", 2, 32), ("mse", 3, 1)])

@@ -4,8 +4,9 @@ Token counts around the 64-token tiles and 128-token blocks (only the query
 positions, a tile minus one, exactly one tile, one over) for every codec pair
 of the prefill kernels, 128- to 512-token blocks in a shuffled order, causal
 query lengths above one, more than 16 query rows (two row groups), a sequence
-long enough for many token splits (past one merge chunk), head_dim 256 on the
-tensor-core path (two 128-column value halves per unit), per-head scales, and inputs with zero,
+long enough for many token splits (past one merge chunk), head_dims 64 and 256
+on the tensor-core path (64 in the head_dim-128 layout, 256 as two 128-column
+value halves per unit), per-head scales, and inputs with zero,
 tiny and one-hot vectors (zero-norm values, zero keys). Every output row is
 compared with the oracle's decode of the same raw inputs (the max abs error
 and cosine bounds of the decode parity rule); the last case checks that two
@@ -105,15 +106,26 @@ def _plan(w):
     return case, tq.tq_decode_plan(case.cache.desc, w.batch, w.num_q_heads, w.q_len, max(w.seq_lens), sms)
 
 
+@pytest.mark.parametrize("D", [64, 256])
 @pytest.mark.parametrize("key,value", [(("prod", 3), ("group", 2, 32)), (("prod", 3), ("mse", 3)),
                                        (("prod", 3), ("group", 2, 64)), (("prod", 3), ("group", 4, 64)),
                                        (("prod", 3), ("mse", 4)), (("mse", 4), ("mse", 4))])
-def test_head_dim_256_tile_edges(key, value):
-    # 32-token tiles at head_dim 256, every codec pair of its tensor-core
-    # kernels: sequences around one tile, 64-token blocks, q_len 2 x GQA 8
-    w = _workload(key, value, (2, 31, 32, 33, 700), 2, 2, 8, 64, D=256)
+def test_head_dim_64_256_tile_edges(D, key, value):
+    # every codec pair of the tensor-core kernels at head_dim 64 (the
+    # head_dim-128 layout, 64-token tiles) and 256 (two value halves, 32-token
+    # tiles): sequences around the tiles, 64-token blocks, q_len 2 x GQA 8
+    w = _workload(key, value, (2, 31, 32, 33, 63, 64, 65, 700), 2, 2, 8, 64, D=D)
     _, plan = _plan(w)
     assert plan["tensor_cores"] == 1, plan
+    _check(w)
+
+
+def test_head_dim_64_many_splits_shuffled_small_blocks():
+    # one KV head over 30000 tokens in 16-token blocks (four per stage) in a
+    # shuffled order, 32 rows (two row groups)
+    w = _workload(("prod", 3), ("mse", 3), (30000, 777), 4, 1, 8, 16, shuffle=True, D=64)
+    _, plan = _plan(w)
+    assert plan["tensor_cores"] == 1 and plan["splits"] > 32, plan
     _check(w)
 
 

@@ -46,6 +46,8 @@ CASES = [
     (256, ("prod", 3), ("group", 2, 32), 2, 8, 1, 1000, (0, 600, 1000)),    # head_dim 256, group values
     (256, ("prod", 3), ("mse", 3), 2, 8, 2, 3000, (0, 1000, 3000)),         # head_dim 256, MSE values
     (256, ("prod", 2), ("group", 4, 64), 1, 4, 1, 800, (0, 400, 800)),      # head_dim 256 on the SIMT kernels
+    (64, ("prod", 3), ("mse", 3), 2, 8, 2, 2000, (0, 900, 2000)),          # head_dim 64, MSE values
+    (64, ("mse", 2), ("mse", 2), 2, 4, 1, 700, (0, 350, 700)),             # head_dim 64 on the SIMT kernels
     (128, ("prod", 3), ("mse", 3), 1, 8, 2, 160000, (0, 10000, 160000)),    # one head: a shard of > 128 splits
 ]
 

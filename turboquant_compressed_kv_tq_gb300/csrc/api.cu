@@ -304,8 +304,9 @@ tq_status tq_codec_create(int head_dim, int bits, tq_mode mode, uint64_t seed, t
     tq_status st = upload(&c->d_R, c->host.rotation);
     if (st == TQ_OK) st = upload(&c->d_Rt, transpose(c->host.rotation, head_dim));
     if (st == TQ_OK && mode == TQ_MODE_PROD) st = upload(&c->d_St, transpose(c->host.qjl, head_dim));
-    // q'' = (S R) q in one pass with q' = R q: the query prep of the wide tensor-core decode
-    if (st == TQ_OK && mode == TQ_MODE_PROD && head_dim > 128)
+    // q'' = (S R) q in one pass with q' = R q: the query prep of the tensor-core
+    // decode at head_dims other than 128
+    if (st == TQ_OK && mode == TQ_MODE_PROD && head_dim != 128)
         st = upload(&c->d_SRt, product_transposed(c->host.qjl, c->host.rotation, head_dim));
     if (st == TQ_OK) st = upload(&c->d_c, c->host.centroids);
     if (st == TQ_OK) st = upload(&c->d_m, c->host.midpoints);

@@ -411,6 +411,7 @@ bool dispatch_b(int, bool, bool, int, const MmaArgs&, size_t, cudaStream_t, cons
 bool dispatch_c(int, bool, bool, int, const MmaArgs&, size_t, cudaStream_t, const EncodeAppendArgs*, cudaError_t*);
 bool wide_supported(int D, int kb, bool prod, bool vgroup, int vb);
 bool dispatch_d(int D, int kb, bool prod, bool vgroup, int vb, const MmaArgs&, size_t, cudaStream_t, cudaError_t*);
+bool dispatch_e(int D, int kb, bool prod, bool vgroup, int vb, const MmaArgs&, size_t, cudaStream_t, cudaError_t*);
 }  // namespace mmadec
 
 namespace {
@@ -435,7 +436,7 @@ void choose_splits(DecodePlan& p, int64_t units, int64_t target_ctas, int max_se
 }
 
 bool mma_supported(const tq_cache_desc* d, DecodePlan& p) {
-    if (d->head_dim != mmadec::kD && d->head_dim != 2 * mmadec::kD) return false;
+    if (d->head_dim != mmadec::kD && d->head_dim != 2 * mmadec::kD && d->head_dim != mmadec::kD / 2) return false;
     p.kprod = d->key_mode == TQ_MODE_PROD;
     p.kb = p.kprod ? d->key_bits - 1 : d->key_bits;
     if (p.kprod ? (p.kb < 1 || p.kb > 3) : (p.kb < 2 || p.kb > 4)) return false;
@@ -446,7 +447,7 @@ bool mma_supported(const tq_cache_desc* d, DecodePlan& p) {
     } else if (p.vb < 2 || p.vb > 4) {
         return false;
     }
-    // head_dim 256: the instantiated codec pairs only
+    // head_dim 64 and 256: the instantiated codec pairs only
     return d->head_dim == mmadec::kD || mmadec::wide_supported(d->head_dim, p.kb, p.kprod, p.vgroup, p.vb);
 }
 
@@ -461,7 +462,7 @@ DecodePlan make_decode_plan(const tq_cache_desc* d, int batch, int G, int Lq, in
     const int64_t units = static_cast<int64_t>(batch) * Hkv * p.row_groups;
     if (mma_supported(d, p)) {
         p.kind = 1;
-        const int NH = D / mmadec::kD;  // 128-column value halves: CTAs per (unit, split)
+        const int NH = D > mmadec::kD ? D / mmadec::kD : 1;  // 128-column value halves: CTAs per (unit, split)
         // stage layout for a tile size; the tile halves (down to 16 tokens)
         // while the split kernel's shared memory would exceed the budget
         auto layout = [&](int tile) {
@@ -528,10 +529,10 @@ DecodePlan make_decode_plan(const tq_cache_desc* d, int batch, int G, int Lq, in
             choose_splits(p, units * NH, num_sms, max_seq_len, 32, max_chunk);
             if (100 * busiest(h) <= 52 * busiest(p) || p.smem > mmadec::kSmemBudget) p = h;
         }
-        // head_dim 128: the units' query fragments; above it the fp32 q' and
-        // q'' rows of the SIMT query prep (two arrays of q_bytes)
-        p.q_bytes = NH == 1 ? al256(static_cast<size_t>(units) * 2 * 8 * 32 * 16)
-                            : al256(static_cast<size_t>(units) * kRows * D * sizeof(float));
+        // head_dim 128: the units' query fragments; otherwise the fp32 q' and
+        // q'' rows of the query prep (two arrays of q_bytes)
+        p.q_bytes = D == mmadec::kD ? al256(static_cast<size_t>(units) * 2 * 8 * 32 * 16)
+                                    : al256(static_cast<size_t>(units) * kRows * D * sizeof(float));
     } else {
         p.kind = 0;
         p.tile = kTile;
@@ -541,9 +542,11 @@ DecodePlan make_decode_plan(const tq_cache_desc* d, int batch, int G, int Lq, in
         choose_splits(p, units, static_cast<int64_t>(num_sms) * 4, max_seq_len, kTile, 1 << 30, kSimtMinChunk);
         p.q_bytes = al256(static_cast<size_t>(units) * kRows * D * sizeof(float));
     }
-    p.part_bytes = al256(static_cast<size_t>(units) * p.splits * kRows * D * sizeof(float));
+    // the tensor-core kernels write 128-column partial rows at head_dim 64
+    const int part_cols = p.kind == 1 && D < mmadec::kD ? mmadec::kD : D;
+    p.part_bytes = al256(static_cast<size_t>(units) * p.splits * kRows * part_cols * sizeof(float));
     // (max, sum) rows: one set per value half of the tensor-core path
-    const int ml_sets = p.kind == 1 ? D / mmadec::kD : 1;
+    const int ml_sets = p.kind == 1 && D > mmadec::kD ? D / mmadec::kD : 1;
     p.ml_bytes = al256(static_cast<size_t>(units) * ml_sets * p.splits * kRows * 2 * sizeof(float));
     p.total = (p.kind == 1 && D == mmadec::kD ? p.q_bytes : 2 * p.q_bytes) + p.part_bytes + p.ml_bytes;
     return p;
@@ -574,6 +577,7 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s, const EncodeAppen
             m.ml = a.ml;
             if (step) return cudaErrorInvalidValue;  // the step's append runs before
             if (mmadec::dispatch_d(a.kc.D, p.kb, p.kprod, p.vgroup, p.vb, m, p.smem, s, &e)) return e;
+            if (mmadec::dispatch_e(a.kc.D, p.kb, p.kprod, p.vgroup, p.vb, m, p.smem, s, &e)) return e;
             return cudaErrorInvalidValue;
         }
         m.qfrag = reinterpret_cast<const uint4*>(ws);

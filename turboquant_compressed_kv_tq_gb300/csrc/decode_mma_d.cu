@@ -6,8 +6,9 @@
 namespace tq {
 namespace mmadec {
 
+// The codec pairs built for head_dim 64 (decode_mma_e.cu) and 256 (here).
 bool wide_supported(int D, int kb, bool prod, bool vgroup, int vb) {
-    if (D != 256) return false;
+    if (D != 64 && D != 256) return false;
     if (kb == 2 && prod) return vgroup ? (vb == 2 || vb == 4) : (vb == 3 || vb == 4);
     return kb == 4 && !prod && !vgroup && vb == 4;
 }

@@ -349,8 +349,8 @@ __device__ __forceinline__ void mse_chunk(const uint32_t* w, const typename MseT
 
 // Merge of a unit's split partials, one CTA per (unit, row), launched after
 // the split kernel with programmatic dependent launch: R_v is staged in shared
-// memory before the CTA waits for the split kernel (head_dim 128; at 256 the
-// rotation reads R_v's rows from L2); then the CTA takes the row's maximum
+// memory before the CTA waits for the split kernel (head_dim 64 and 128; at
+// 256 the rotation reads R_v's rows from L2); then the CTA takes the row's maximum
 // over the splits, weights each split's (sum, accumulator) by 2^(m - max),
 // divides by the merged sum and applies the inverse value rotation (or, for a
 // shard's state, writes the merged (max, sum, accumulator) without the
@@ -361,12 +361,12 @@ __device__ __forceinline__ void mse_chunk(const uint32_t* w, const typename MseT
 // R_v in flight per column instead of one), the quarters' sums added in a
 // fixed order.
 template <bool VGROUP, int D>
-__host__ __device__ constexpr int merge_threads() { return D == kD || VGROUP ? D : 4 * D; }
+__host__ __device__ constexpr int merge_threads() { return D <= kD || VGROUP ? D : 4 * D; }
 
 template <bool VGROUP, int D = kD>
 __global__ void __launch_bounds__(merge_threads<VGROUP, D>()) merge_rows_kernel(MmaArgs m) {
     extern __shared__ __align__(128) unsigned char smem[];
-    constexpr int NH = D / kD, kW = D / 32;
+    constexpr int NH = D > kD ? D / kD : 1, kW = D / 32;
     constexpr int kQ = merge_threads<VGROUP, D>() / D;   // rotation quarters (1: no split of the rotation)
     const DecodeArgs& a = m.a;
     tc::grid_release_dependents();  // the next kernel waits for this grid before the workspace
@@ -380,9 +380,9 @@ __global__ void __launch_bounds__(merge_threads<VGROUP, D>()) merge_rows_kernel(
     const bool col = quarter == 0;   // the threads of the split merge (one per column)
     const int h2 = d / kD, cc = d % kD;
     const bool rotate = !VGROUP && !a.part_acc;
-    const bool stage_r = rotate && D == kD;
+    const bool stage_r = rotate && D <= kD;
     float* sR = reinterpret_cast<float*>(smem);      // [D][D], staged rotation only
-    float* so = sR + (stage_r ? kD * kD : 0);        // [D] the merged row
+    float* so = sR + (stage_r ? D * D : 0);          // [D] the merged row
     float* sw = so + D;                              // [D] weights of a chunk of splits
     float* sred = sw + D;                            // [kW] per-warp maxima / sums
     float* sq = sred + kW;                           // [kQ][D] the rotation quarters' sums
@@ -390,8 +390,8 @@ __global__ void __launch_bounds__(merge_threads<VGROUP, D>()) merge_rows_kernel(
     if (stage_r && threadIdx.x == 0) {
         mbar_init(&bar, 1);
         mbar_fence_init();
-        mbar_expect_tx(&bar, kD * kD * 4);
-        bulk_g2s(sR, a.vc.R, kD * kD * 4, &bar);
+        mbar_expect_tx(&bar, D * D * 4);
+        bulk_g2s(sR, a.vc.R, D * D * 4, &bar);
     }
     tc::grid_wait_prior();  // the split kernel's partials
     const int S = a.plan.splits;
@@ -526,7 +526,7 @@ __global__ void __launch_bounds__(merge_threads<VGROUP, D>()) merge_rows_kernel(
 template <bool VGROUP, int D = kD>
 inline size_t merge_rows_smem(bool rotate) {
     constexpr int nt = merge_threads<VGROUP, D>();
-    return (rotate && D == kD ? static_cast<size_t>(kD) * kD * 4 : 0) + (2 * D + D / 32 + (nt > D ? nt : 0)) * 4;
+    return (rotate && D <= kD ? static_cast<size_t>(D) * D * 4 : 0) + (2 * D + D / 32 + (nt > D ? nt : 0)) * 4;
 }
 
 // Query fragments of one unit (16 rows) from its fp32 q' and q'' rows, in the
@@ -535,11 +535,14 @@ inline size_t merge_rows_smem(bool rotate) {
 // 2 e + (row >= 8)) holds the pair (pa, pb) of the lane's chunk j D / 128 + c.
 // Slot 1 holds q'' for prod keys and fp16(q') 's rounding remainder otherwise.
 // A block of NT threads: every thread issues all of its loads (L2) before it
-// converts any, so the rows arrive in one round trip.
+// converts any, so the rows arrive in one round trip. Head_dim 64 takes the
+// head_dim-128 layout with the coordinates past 64 zero (the lanes whose
+// chunk lies past the vector's end then contribute nothing to a score).
 template <int KB, int ORD, int D, int NT>
 __device__ __forceinline__ void frag_from_rows(uint32_t* dst, const float* q1, const float* q2, bool prod, float s1,
                                                float s2, int tid) {
-    constexpr int KS = D / 16, NC = D / kD;
+    constexpr int DV = D < kD ? kD : D;   // the layout's head_dim
+    constexpr int KS = DV / 16, NC = DV / kD;
     constexpr int kPerRow = 2 * KS * 4 * 2;
     constexpr int kTotal = kRows * kPerRow, kIter = (kTotal + NT - 1) / NT;
     // entry e: (row, which, k-step, lane chunk j, e) and the source pair
@@ -556,7 +559,8 @@ __device__ __forceinline__ void frag_from_rows(uint32_t* dst, const float* q1, c
         } else {
             mse_pair(qjl ? 1 : KB, 2 * ks + ee, pa, pb);
         }
-        q = (qjl ? q2 : q1) + rr * D + 32 * (j * NC + c);
+        const int chunk = j * NC + c;
+        q = chunk < D / 32 ? (qjl ? q2 : q1) + rr * D + 32 * chunk : nullptr;
     };
     float va[kIter], vb[kIter];
 #pragma unroll
@@ -568,8 +572,10 @@ __device__ __forceinline__ void frag_from_rows(uint32_t* dst, const float* q1, c
             const float* q;
             bool qjl, rem;
             where(e, out, q, pa, pb, qjl, rem);
-            va[it] = __ldcg(q + pa);
-            vb[it] = __ldcg(q + pb);
+            if (q) {
+                va[it] = __ldcg(q + pa);
+                vb[it] = __ldcg(q + pb);
+            }
         }
     }
 #pragma unroll
@@ -602,9 +608,15 @@ __global__ void __launch_bounds__(kThreads, 1) split_mma_kernel(MmaArgs m) {
     const int RG = a.plan.row_groups;
     // head_dim D = 128 NH: each CTA takes one 128-column half h2 of the values
     // (the output accumulator of a warp is 16 x 128); every lane decodes NC
-    // 32-coordinate chunks of each key (scores need all D coordinates)
-    static_assert(D % kD == 0, "head_dim a multiple of 128");
-    constexpr int NH = D / kD, NC = D / kD;
+    // 32-coordinate chunks of each key (scores need all D coordinates).
+    // Head_dim 64 runs in the head_dim-128 layout: lanes j >= 2, whose chunk
+    // lies past the vector's end, decode chunk 1 again (finite operands against
+    // zero query coordinates for the scores; their output columns 64..127 are
+    // not merged).
+    static_assert(D == 64 || D % kD == 0, "head_dim 64 or a multiple of 128");
+    constexpr int NH = D > kD ? D / kD : 1, NC = D > kD ? D / kD : 1;
+    constexpr int DV = D < kD ? kD : D;                       // the fragment layout's head_dim
+    const int jc = D < kD ? (j < D / 32 ? j : D / 32 - 1) : j;  // the lane's chunk, clamped
     // grid (KV head x row group x half, sequence, split): CTAs are dispatched
     // split by split, so every unit's full first splits run before the
     // shorter (last, partial) and empty ones, which make up the last wave
@@ -871,8 +883,8 @@ __global__ void __launch_bounds__(kThreads, 1) split_mma_kernel(MmaArgs m) {
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
                 const int tau = base + 8 * nt + g;
-                load_words<KB>(kidx + tau * (D / 32 * KB) + (j * NC + c) * KB, kw[nt]);
-                if constexpr (KPROD) sw[nt] = ksgn[tau * (D / 32) + j * NC + c];
+                load_words<KB>(kidx + tau * (D / 32 * KB) + (jc * NC + c) * KB, kw[nt]);
+                if constexpr (KPROD) sw[nt] = ksgn[tau * (D / 32) + jc * NC + c];
                 else sw[nt] = 0u;
             }
 #pragma unroll
@@ -887,7 +899,7 @@ __global__ void __launch_bounds__(kThreads, 1) split_mma_kernel(MmaArgs m) {
                     {
                         const uint4 v = qsm[(8 * c + ks) * 32 + lane];
                         qa[0] = v.x; qa[1] = v.y; qa[2] = v.z; qa[3] = v.w;
-                        const uint4 w = qsm[(D / 16 + 8 * c + ks) * 32 + lane];
+                        const uint4 w = qsm[(DV / 16 + 8 * c + ks) * 32 + lane];
                         qj[0] = w.x; qj[1] = w.y; qj[2] = w.z; qj[3] = w.w;
                     }
 #pragma unroll
@@ -914,11 +926,11 @@ __global__ void __launch_bounds__(kThreads, 1) split_mma_kernel(MmaArgs m) {
                 const int tA = base + 16 * kg + g, tB = tA + 8;
                 uint32_t wA[VB], wB[VB];
                 // the lane's 32-coordinate chunk 4 h2 + j of the CTA's value half
-                load_words<VB>(vidx + tA * (D / 32 * VB) + (4 * h2 + j) * VB, wA);
-                load_words<VB>(vidx + tB * (D / 32 * VB) + (4 * h2 + j) * VB, wB);
+                load_words<VB>(vidx + tA * (D / 32 * VB) + (4 * h2 + jc) * VB, wA);
+                load_words<VB>(vidx + tB * (D / 32 * VB) + (4 * h2 + jc) * VB, wB);
                 if constexpr (VGROUP) {
                     const int ng = D / a.vc.group;
-                    const int gi = (32 * (4 * h2 + j)) / a.vc.group;
+                    const int gi = (32 * (4 * h2 + jc)) / a.vc.group;
                     const float mulf = VB == 4 ? 16.0f : 4.0f;
                     const bool okA = tA < valid, okB = tB < valid;
                     const float sA = okA ? __half2float(vsc[tA * ng + gi]) : 0.0f;
@@ -1279,12 +1291,12 @@ __global__ void __launch_bounds__(kQRThreads) qrows_kernel(DecodeArgs a) {
 template <int D>
 constexpr size_t qrows_smem() { return static_cast<size_t>(D) * 32 * 4 + static_cast<size_t>(kRows) * D * 4; }
 
-// Head dims above 128 (two 128-column value halves per unit): the query
-// prep writes the fp32 q' and q'' rows, the split kernel builds its fragments
-// from them, then the merge.
+// Head dims other than 128 (above it two 128-column value halves per unit;
+// 64 in the head_dim-128 layout): the query prep writes the fp32 q' and q''
+// rows, the split kernel builds its fragments from them, then the merge.
 template <int KB, bool KPROD, bool VGROUP, int VB, int D>
 cudaError_t launch_mma_wide(const MmaArgs& m, size_t smem, cudaStream_t s) {
-    static_assert(D > kD && D % kD == 0, "a multiple of 128 above it");
+    static_assert(D == 64 || (D > kD && D % kD == 0), "head_dim 64 or a multiple of 128 above 128");
     const DecodeArgs& a = m.a;
     static std::atomic<uint64_t> attr_set{0}, qr_set{0};
     static std::atomic<int> max_dyn[64];
@@ -1310,7 +1322,8 @@ cudaError_t launch_mma_wide(const MmaArgs& m, size_t smem, cudaStream_t s) {
     g_launches.fetch_add(1, std::memory_order_relaxed);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     e = launch_overlapped(split_mma_kernel<KB, KPROD, VGROUP, VB, D>,
-                          dim3(a.pool.Hkv * a.plan.row_groups * (D / kD), a.batch, a.plan.splits), dim3(kThreads),
+                          dim3(a.pool.Hkv * a.plan.row_groups * (D > kD ? D / kD : 1), a.batch, a.plan.splits),
+                          dim3(kThreads),
                           smem, s, m);
     g_launches.fetch_add(1, std::memory_order_relaxed);
     if (e != cudaSuccess) return e;

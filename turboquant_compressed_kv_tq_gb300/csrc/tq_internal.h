@@ -40,7 +40,7 @@ struct CodecDev {
     const float* R;    // [D][D] row-major
     const float* Rt;   // [D][D] transposed rotation (Rt[k*D+i] = R[i][k])
     const float* St;   // [D][D] transposed QJL matrix (prod) or nullptr
-    const float* SRt;  // [D][D] transposed product S R (prod, head_dim above 128) or nullptr
+    const float* SRt;  // [D][D] transposed product S R (prod, head_dim other than 128) or nullptr
     const float* c;    // centroids
     const float* m;    // midpoints
     const float* cq;   // fp16-exact operand levels op_scale * c (see HostTables)
@@ -100,7 +100,7 @@ struct QuantizeArgs {
 
 // Decode plan shared by workspace sizing and the launch.
 struct DecodePlan {
-    int kind;         // 0: SIMT kernels (any shape), 1: tensor-core kernels (head_dim 128, some 256)
+    int kind;         // 0: SIMT kernels (any shape), 1: tensor-core kernels (head_dim 128, some 64 and 256)
     int rows;         // G * Lq
     int row_groups;   // ceil(rows / 16)
     int splits;       // token splits per (sequence, kv head, row group)
@@ -253,7 +253,7 @@ struct tq_codec {
     float* d_R = nullptr;
     float* d_Rt = nullptr;
     float* d_St = nullptr;
-    float* d_SRt = nullptr;  // transposed S R (prod codecs with head_dim above 128)
+    float* d_SRt = nullptr;  // transposed S R (prod codecs with head_dim other than 128)
     float* d_c = nullptr;
     float* d_m = nullptr;
     float* d_cq = nullptr;
