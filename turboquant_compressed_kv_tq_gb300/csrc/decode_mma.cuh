@@ -111,6 +111,13 @@ __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
     return r;
 }
 
+// The 32 bits of an fp16 pair.
+__device__ __forceinline__ uint32_t h2_bits(__half2 x) {
+    uint32_t r;
+    memcpy(&r, &x, sizeof(r));
+    return r;
+}
+
 // prmt.b32 in its default mode: each selector nibble picks a byte of {b, a};
 // a set msb in the nibble replicates that byte's sign bit instead.
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {

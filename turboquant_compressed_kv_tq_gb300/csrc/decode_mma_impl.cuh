@@ -727,6 +727,12 @@ __global__ void __launch_bounds__(kThreads, 1) split_mma_kernel(MmaArgs m) {
     float o[16][4];
 #pragma unroll
     for (int p = 0; p < 16; ++p) o[p][0] = o[p][1] = o[p][2] = o[p][3] = 0.0f;
+    // group values: groups per token, and the group of this lane's value chunk
+    [[maybe_unused]] int vng = 0, vgi = 0;
+    if constexpr (VGROUP) {
+        vng = D / a.vc.group;
+        vgi = (32 * (4 * h2 + jc)) / a.vc.group;
+    }
     float mrow0 = kNoMax, mrow1 = kNoMax, lrow0 = 0.0f, lrow1 = 0.0f;
     bool failed = false;
 
@@ -929,16 +935,17 @@ __global__ void __launch_bounds__(kThreads, 1) split_mma_kernel(MmaArgs m) {
                 load_words<VB>(vidx + tA * (D / 32 * VB) + (4 * h2 + jc) * VB, wA);
                 load_words<VB>(vidx + tB * (D / 32 * VB) + (4 * h2 + jc) * VB, wB);
                 if constexpr (VGROUP) {
-                    const int ng = D / a.vc.group;
-                    const int gi = (32 * (4 * h2 + jc)) / a.vc.group;
-                    const float mulf = VB == 4 ? 16.0f : 4.0f;
+                    // fp16 pairs (2^VB s, 2^VB s) and (min, min) straight from the
+                    // stored halves (the power-of-two product is exact)
+                    const __half z = __float2half_rn(0.0f);
+                    const __half2 mul = __float2half2_rn(VB == 4 ? 16.0f : 4.0f);
                     const bool okA = tA < valid, okB = tB < valid;
-                    const float sA = okA ? __half2float(vsc[tA * ng + gi]) : 0.0f;
-                    const float mA = okA ? __half2float(vmn[tA * ng + gi]) : 0.0f;
-                    const float sB = okB ? __half2float(vsc[tB * ng + gi]) : 0.0f;
-                    const float mB = okB ? __half2float(vmn[tB * ng + gi]) : 0.0f;
-                    GroupChunk<VB>::run(wA, pack_half2(sA * mulf, sA * mulf), pack_half2(mA, mA), hA);
-                    GroupChunk<VB>::run(wB, pack_half2(sB * mulf, sB * mulf), pack_half2(mB, mB), hB);
+                    const __half2 sA = __hmul2(__half2half2(okA ? vsc[tA * vng + vgi] : z), mul);
+                    const __half2 mA = __half2half2(okA ? vmn[tA * vng + vgi] : z);
+                    const __half2 sB = __hmul2(__half2half2(okB ? vsc[tB * vng + vgi] : z), mul);
+                    const __half2 mB = __half2half2(okB ? vmn[tB * vng + vgi] : z);
+                    GroupChunk<VB>::run(wA, h2_bits(sA), h2_bits(mA), hA);
+                    GroupChunk<VB>::run(wB, h2_bits(sB), h2_bits(mB), hB);
                 } else if constexpr (kPairTab) {
                     pair3_chunk(wA, vt_lane, hA);
                     pair3_chunk(wB, vt_lane, hB);
