@@ -748,6 +748,7 @@ __global__ void __launch_bounds__(kThreads, 1) split_mma_kernel(MmaArgs m) {
     // tile into that stream's run of the stage (blocks one after another).
     const int tile_blocks = TT > BT ? TT / BT : 1;
     const int blk_tokens = TT > BT ? BT : TT;   // tokens a lane's copy carries
+    const int blk_shift = __ffs(blk_tokens) - 1;   // a power of two
     const int my_stream = lane % 7, my_blk = lane / 7;
     unsigned blk_tx = 0;                         // bytes of one block's part of a stage
     int s_off = -1, s_field = 0;
@@ -763,19 +764,28 @@ __global__ void __launch_bounds__(kThreads, 1) split_mma_kernel(MmaArgs m) {
     }
     const uint64_t pol = policy_evict_first();
     uint32_t bad_stage = 0;
-    auto issue = [&](int i) {
+    // The physical block of this lane's block of tile i (its table entry): read
+    // a tile ahead of the copy in the main loop, so that the copy does not wait
+    // for the load. Blocks of the tile that hold no token of this split (a
+    // partial last tile may end before the tile's last block) are not read.
+    auto entry = [&](int i) -> int32_t {
+        if (!a.table) return 0;   // contiguous: the block follows from the position
+        const int t0 = t_begin + (warp + i * kWarps) * TT;
+        const int lb = (t0 >> bt_shift) + my_blk;
+        const int live = min(tile_blocks, (t_end - t0 + blk_tokens - 1) >> blk_shift);
+        if (s_off < 0 || my_blk >= live) return 0;
+        return a.table[static_cast<int64_t>(b) * a.max_blocks + lb];
+    };
+    auto issue = [&](int i, int32_t tab) {
         const int t0 = t_begin + (warp + i * kWarps) * TT;
         const int lb = (t0 >> bt_shift) + my_blk;
         const int slot0 = t0 & (BT - 1);
-        // blocks of the tile that hold tokens of this split (a partial last tile
-        // may end before the tile's last block, whose table entry is not read)
-        const int live = min(tile_blocks, (t_end - t0 + blk_tokens - 1) / blk_tokens);
+        const int live = min(tile_blocks, (t_end - t0 + blk_tokens - 1) >> blk_shift);
         const bool mine = s_off >= 0 && my_blk < live;
         int64_t pb = 0;
         bool badb = false;
         if (mine) {
-            pb = a.table ? static_cast<int64_t>(a.table[static_cast<int64_t>(b) * a.max_blocks + lb])
-                         : static_cast<int64_t>(b) * a.max_blocks + lb;
+            pb = a.table ? static_cast<int64_t>(tab) : static_cast<int64_t>(b) * a.max_blocks + lb;
             badb = pb < 0 || pb >= a.pool.num_blocks;
             if (badb) pb = 0;
         }
@@ -802,13 +812,13 @@ __global__ void __launch_bounds__(kThreads, 1) split_mma_kernel(MmaArgs m) {
         return a.len_add == 0 || t_begin + (warp + i * kWarps) * TT + TT <= N - a.len_add;
     };
     for (int i = 0; i < pre; ++i)
-        if (early(i)) issue(i);
+        if (early(i)) issue(i, entry(i));
     // query fragments of this unit, shared by all warps: [2][8][32] uint4
     // (written by the query-prep kernel this one may overlap: wait for it)
     const uint4* qsm = reinterpret_cast<const uint4*>(smem + st.qs_off);
     tc::grid_wait_prior();
     for (int i = 0; i < pre; ++i)
-        if (!early(i)) issue(i);
+        if (!early(i)) issue(i, entry(i));
     if constexpr (D == kD) {
         if (threadIdx.x == 0) {
             tc::fence_proxy_async_global();
@@ -829,10 +839,12 @@ __global__ void __launch_bounds__(kThreads, 1) split_mma_kernel(MmaArgs m) {
         (void)mbar_wait(tbar, 0);  // no copy may still be in flight below
     }
     int waited = 0;
+    int32_t pb_ahead = kStages - 1 < my_n ? entry(kStages - 1) : 0;   // the next copy's table entry
     for (int i = 0; i < my_n; ++i) {
         if (i + kStages - 1 < my_n) {
             __syncwarp();
-            issue(i + kStages - 1);
+            issue(i + kStages - 1, pb_ahead);
+            if (i + kStages < my_n) pb_ahead = entry(i + kStages);
         }
         if (!mbar_wait(&bars[i % kStages], (i / kStages) & 1)) {
             failed = true;
