@@ -33,9 +33,17 @@ def _lib_built():
     assert torch.cuda.is_available()
 
 
-def test_noalloc_matches_workspace_entry_on_two_calls():
-    # the bench's codecs and head layout (8 KV heads, GQA 8, two query positions)
-    w = dataclasses.replace(wl.long_256k(), seq_lens=(5003,))
+@pytest.mark.parametrize("shape", ["long_256k", "layer_d256", "d64"])
+def test_noalloc_matches_workspace_entry_on_two_calls(shape):
+    # the bench's codecs and head layout (8 KV heads, GQA 8, two query
+    # positions); the head_dim-256 layer (its query rows in the scratch); the
+    # same codecs at head_dim 64 (the head_dim-128 layout's wider partials)
+    if shape == "long_256k":
+        w = dataclasses.replace(wl.long_256k(), seq_lens=(5003,))
+    elif shape == "layer_d256":
+        w = dataclasses.replace(wl.layer_d256(4096), num_layers=2, seq_lens=(3001,))
+    else:
+        w = dataclasses.replace(wl.long_256k(), head_dim=64, num_layers=2, seq_lens=(7000,))
     case = GpuCase(w, layers=[0, 1])
     case.prefill()
     sl = torch.tensor(case.seq_lens, dtype=torch.int32, device=DEV)
