@@ -194,8 +194,8 @@ def test_workspace_query_rejects_a_descriptor_without_heads(libtq):
 
 
 def test_decode_plan_simt_shapes(libtq):
-    # head_dim 64, and 256 with codec pairs the tensor-core kernels are not
-    # built for, take the SIMT kernels: no tensor-core shared memory
+    # head_dims 64 and 256 with codec pairs the tensor-core kernels are not
+    # built for take the SIMT kernels: no tensor-core shared memory
     for D, key, value in [(256, ("prod", 2), ("group", 4, 64)), (64, ("mse", 2), ("mse", 2, 0))]:
         d = _desc_from_oracle(D, key, value, 64, 2)
         p = tq.tq_decode_plan(d, 2, 16, 1, 8192, 152)
