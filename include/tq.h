@@ -388,6 +388,9 @@ typedef struct {
                           * lookup tables                                                 */
     size_t smem_bytes;   /* dynamic shared memory of the split kernel (tensor cores)     */
     size_t workspace_bytes; /* as tq_decode_workspace_bytes for num_sms SMs              */
+    int transposed;      /* 1: the tensor-core split kernel in its transposed form        *
+                          * (head_dim 128, at most 8 query rows per KV head, the codec    *
+                          * pairs of the head_dim-64/256 set): tokens on the MMA's M       */
 } tq_decode_plan_info;
 
 /*

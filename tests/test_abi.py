@@ -268,6 +268,24 @@ def test_decode_plan_split_rule(libtq):
     assert short["chunk_tokens"] == 32 and short["splits"] == 4
 
 
+def test_decode_plan_transposed_for_few_rows(libtq):
+    # head_dim 128 with at most 8 query rows per KV head and a codec pair of the
+    # transposed kernel's set: the transposed form; 16 rows, other pairs, or
+    # other head_dims: the 16-row form (or SIMT)
+    few = {(("prod", 3), ("group", 4)), (("prod", 3), ("group", 2)), (("prod", 3), ("mse", 3)),
+           (("prod", 3), ("mse", 4)), (("mse", 4), ("mse", 4))}   # any group size
+    for key in _KEYS:
+        for value in _VALUES:
+            d = _desc_from_oracle(128, key, value, 64, 8)
+            for Hq, Lq in ((32, 1), (64, 1), (16, 3), (64, 2)):
+                p = tq.tq_decode_plan(d, 2, Hq, Lq, 4096, 152)
+                rows = Hq // 8 * Lq
+                want = 1 if rows <= 8 and (key, value[:2]) in few else 0
+                assert p["transposed"] == want, (key, value, Hq, Lq, p)
+    d = _desc_from_oracle(64, ("prod", 3), ("mse", 3, 0), 64, 8)
+    assert tq.tq_decode_plan(d, 2, 32, 1, 4096, 152)["transposed"] == 0
+
+
 def test_decode_plan_tile_balances_the_busiest_warp(libtq):
     # 64-token tiles unless 32-token tiles (each about 0.52 of a 64-token
     # tile's time) give the busiest of the 12 warps less work: at 256k a split

@@ -6,7 +6,8 @@ of the prefill kernels, 128- to 512-token blocks in a shuffled order, causal
 query lengths above one, more than 16 query rows (two row groups), a sequence
 long enough for many token splits (past one merge chunk), head_dims 64 and 256
 on the tensor-core path (64 in the head_dim-128 layout, 256 as two 128-column
-value halves per unit), per-head scales, and inputs with zero,
+value halves per unit), up to 8 query rows per KV head (the transposed
+kernel), per-head scales, and inputs with zero,
 tiny and one-hot vectors (zero-norm values, zero keys). Every output row is
 compared with the oracle's decode of the same raw inputs (the max abs error
 and cosine bounds of the decode parity rule); the last case checks that two
@@ -140,6 +141,18 @@ def test_head_dim_256_many_splits():
     w = _workload(("prod", 3), ("group", 2, 32), (20000,), 1, 1, 8, 256, D=256)
     _, plan = _plan(w)
     assert plan["tensor_cores"] == 1 and plan["splits"] > 32, plan
+    _check(w)
+
+
+@pytest.mark.parametrize("key,value", [(("prod", 3), ("group", 4, 64)), (("prod", 3), ("group", 2, 32)),
+                                       (("prod", 3), ("mse", 3)), (("prod", 3), ("mse", 4)), (("mse", 4), ("mse", 4))])
+@pytest.mark.parametrize("G,Lq", [(1, 1), (4, 1), (2, 3), (4, 2), (8, 1)])
+def test_few_rows_transposed_kernel(key, value, G, Lq):
+    # at most 8 query rows per KV head: the split kernel's transposed form
+    # (tokens on the MMA's M, rows on N), causal for q_len > 1, around the tiles
+    w = _workload(key, value, (3, 31, 64, 65, 700), Lq, 2, G, 64)
+    _, plan = _plan(w)
+    assert plan["tensor_cores"] == 1 and plan["transposed"] == 1, plan
     _check(w)
 
 

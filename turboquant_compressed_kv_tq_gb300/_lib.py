@@ -57,7 +57,8 @@ class tq_codec_info_t(ctypes.Structure):
 class tq_decode_plan_info(ctypes.Structure):
     _fields_ = [("tensor_cores", ctypes.c_int), ("row_groups", ctypes.c_int), ("splits", ctypes.c_int),
                 ("chunk_tokens", ctypes.c_int), ("tile_tokens", ctypes.c_int),
-                ("smem_bytes", ctypes.c_size_t), ("workspace_bytes", ctypes.c_size_t)]
+                ("smem_bytes", ctypes.c_size_t), ("workspace_bytes", ctypes.c_size_t),
+                ("transposed", ctypes.c_int)]
 
 
 class tq_cache_desc(ctypes.Structure):

@@ -17,7 +17,7 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libtq.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-CU_SOURCES = ["api.cu", "encode.cu", "encode_block.cu", "encode_tc.cu", "decode.cu", "decode_mma_a.cu", "decode_mma_b.cu", "decode_mma_c.cu", "decode_mma_d.cu", "decode_mma_e.cu", "decode_noalloc.cu", "decode_step.cu", "prefill_tc.cu", "cache_ops.cu", "decode_split.cu"]
+CU_SOURCES = ["api.cu", "encode.cu", "encode_block.cu", "encode_tc.cu", "decode.cu", "decode_mma_a.cu", "decode_mma_b.cu", "decode_mma_c.cu", "decode_mma_d.cu", "decode_mma_e.cu", "decode_mma_f.cu", "decode_noalloc.cu", "decode_step.cu", "prefill_tc.cu", "cache_ops.cu", "decode_split.cu"]
 CXX_SOURCES = ["codec_build.cpp"]
 HEADERS = sorted(os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".h", ".cuh"))) + \
     [os.path.join(INCLUDE, "tq.h")]

@@ -689,6 +689,7 @@ tq_status tq_decode_plan(const tq_cache_desc* cache, int batch, int num_q_heads,
     info->tile_tokens = p.tile;
     info->smem_bytes = p.kind == 1 ? p.smem : 0;
     info->workspace_bytes = p.total;
+    info->transposed = p.kind == 1 && p.r8 ? 1 : 0;
     return TQ_OK;
 }
 

@@ -412,6 +412,8 @@ bool dispatch_c(int, bool, bool, int, const MmaArgs&, size_t, cudaStream_t, cons
 bool wide_supported(int D, int kb, bool prod, bool vgroup, int vb);
 bool dispatch_d(int D, int kb, bool prod, bool vgroup, int vb, const MmaArgs&, size_t, cudaStream_t, cudaError_t*);
 bool dispatch_e(int D, int kb, bool prod, bool vgroup, int vb, const MmaArgs&, size_t, cudaStream_t, cudaError_t*);
+bool r8_supported(int kb, bool prod, bool vgroup, int vb);
+bool dispatch_f(int, bool, bool, int, const MmaArgs&, size_t, cudaStream_t, const EncodeAppendArgs*, cudaError_t*);
 }  // namespace mmadec
 
 namespace {
@@ -529,6 +531,8 @@ DecodePlan make_decode_plan(const tq_cache_desc* d, int batch, int G, int Lq, in
             choose_splits(p, units * NH, num_sms, max_seq_len, 32, max_chunk);
             if (100 * busiest(h) <= 52 * busiest(p) || p.smem > mmadec::kSmemBudget) p = h;
         }
+        // at most 8 query rows per unit at head_dim 128: the transposed kernel
+        p.r8 = D == mmadec::kD && p.rows <= 8 && mmadec::r8_supported(p.kb, p.kprod, p.vgroup, p.vb) ? 1 : 0;
         // head_dim 128: the units' query fragments; otherwise the fp32 q' and
         // q'' rows of the query prep (two arrays of q_bytes)
         p.q_bytes = D == mmadec::kD ? al256(static_cast<size_t>(units) * 2 * 8 * 32 * 16)
@@ -583,6 +587,10 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s, const EncodeAppen
         m.qfrag = reinterpret_cast<const uint4*>(ws);
         m.part = reinterpret_cast<float*>(ws + a.plan.q_bytes);
         m.ml = reinterpret_cast<float*>(ws + a.plan.q_bytes + a.plan.part_bytes);
+        if (p.r8) {
+            if (mmadec::dispatch_f(p.kb, p.kprod, p.vgroup, p.vb, m, p.smem, s, step, &e)) return e;
+            return cudaErrorInvalidValue;
+        }
         if (mmadec::dispatch_a(p.kb, p.kprod, p.vgroup, p.vb, m, p.smem, s, step, &e)) return e;
         if (mmadec::dispatch_b(p.kb, p.kprod, p.vgroup, p.vb, m, p.smem, s, step, &e)) return e;
         if (mmadec::dispatch_c(p.kb, p.kprod, p.vgroup, p.vb, m, p.smem, s, step, &e)) return e;

@@ -597,8 +597,15 @@ __device__ __forceinline__ void frag_from_rows(uint32_t* dst, const float* q1, c
     }
 }
 
-template <int KB, bool KPROD, bool VGROUP, int VB, int D = kD>
+// R8 (head_dim 128, at most 8 query rows per unit): the transposed form.
+// Scores as S^T = K Q^T with 16 tokens on M and the 8 rows on N (the query
+// fragments' registers 0 and 2 are the B operand of rows 0..7; two 8-token
+// key tiles' operands are the A operand), outputs as O^T = V^T P^T with 16
+// value columns on M: half the MMAs and half the softmax work per token of
+// the 16-row form, whose rows 8..15 would be padding.
+template <int KB, bool KPROD, bool VGROUP, int VB, int D = kD, bool R8 = false>
 __global__ void __launch_bounds__(kThreads, 1) split_mma_kernel(MmaArgs m) {
+    static_assert(!R8 || D == kD, "the transposed form at head_dim 128");
     extern __shared__ __align__(128) unsigned char smem[];
     const DecodeArgs& a = m.a;
     const StageLayout& st = m.st;
@@ -719,14 +726,18 @@ __global__ void __launch_bounds__(kThreads, 1) split_mma_kernel(MmaArgs m) {
     }
 
     // causal limits of this thread's two rows (padding rows see everything)
-    const int r0 = rg * kRows + g, r1 = r0 + 8;
+    // (R8: the lane's rows 2 j and 2 j + 1, its tokens g and g + 8 of each 16)
+    const int r0 = R8 ? rg * kRows + 2 * j : rg * kRows + g, r1 = R8 ? r0 + 1 : r0 + 8;
     const int lim0 = r0 < a.plan.rows ? vis - a.Lq + (r0 % a.Lq) : N - 1;
     const int lim1 = r1 < a.plan.rows ? vis - a.Lq + (r1 % a.Lq) : N - 1;
     const int lim_all = vis - a.Lq;  // every row sees the tokens up to here
 
-    float o[16][4];
+    // output accumulator: 16 n8 tiles of 8 columns x 16 rows, or (R8) 8 m16
+    // tiles of 16 columns x 8 rows
+    constexpr int kOT = R8 ? 8 : 16;
+    float o[kOT][4];
 #pragma unroll
-    for (int p = 0; p < 16; ++p) o[p][0] = o[p][1] = o[p][2] = o[p][3] = 0.0f;
+    for (int p = 0; p < kOT; ++p) o[p][0] = o[p][1] = o[p][2] = o[p][3] = 0.0f;
     // group values: groups per token, and the group of this lane's value chunk
     [[maybe_unused]] int vng = 0, vgi = 0;
     if constexpr (VGROUP) {
@@ -887,11 +898,13 @@ __global__ void __launch_bounds__(kThreads, 1) split_mma_kernel(MmaArgs m) {
             [[maybe_unused]] constexpr uint32_t neg2 = 0xBC00BC00u;  // (-1, -1): a set bit gives +1
             // ---------------- scores: S = Q' K^T (+ Q'' sigma^T), key operands
             // decoded two k-steps at a time
-            float sc[NT][4], sd[NT][4];
+            // (R8: MT m16 tiles of 16 tokens, the n8 tiles 2 mt and 2 mt + 1)
+            constexpr int MT = R8 ? (NT + 1) / 2 : NT;
+            float sc[MT][4], sd[MT][4];
             uint32_t kw[NT][KB];
             uint32_t sw[NT];
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt) {
+            for (int nt = 0; nt < MT; ++nt) {
                 sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.0f;
                 sd[nt][0] = sd[nt][1] = sd[nt][2] = sd[nt][3] = 0.0f;
             }
@@ -920,19 +933,45 @@ __global__ void __launch_bounds__(kThreads, 1) split_mma_kernel(MmaArgs m) {
                         const uint4 w = qsm[(DV / 16 + 8 * c + ks) * 32 + lane];
                         qj[0] = w.x; qj[1] = w.y; qj[2] = w.z; qj[3] = w.w;
                     }
-#pragma unroll
-                    for (int nt = 0; nt < NT; ++nt) {
-                        mma16816(sc[nt], qa, hk[nt][2 * e], hk[nt][2 * e + 1]);
+                    // the QJL sign operands of tile nt, k-step ks (B-operand pairs)
+                    auto signs = [&](int nt, uint32_t& b0, uint32_t& b1) {
                         if constexpr (KPROD && kNibQ) {
                             // sign nibble ks of the lane's word at bits 7..10: a table address
                             const uint32_t x = ks == 0 ? shl_f(sw[nt], 7)
                                                : ks == 1 ? shl_f(sw[nt], 3) : (sw[nt] >> (4 * ks - 7));
                             const uint2 sv = lds_u64((x & 0x780u) | qn_lane);
-                            mma16816(sd[nt], qj, sv.x, sv.y);
-                        } else if constexpr (KPROD)
-                            mma16816(sd[nt], qj, dec1(sw[nt], 15 - ks, neg2), dec1(sw[nt], 7 - ks, neg2));
-                        else
-                            mma16816(sd[nt], qj, hk[nt][2 * e], hk[nt][2 * e + 1]);
+                            b0 = sv.x;
+                            b1 = sv.y;
+                        } else if constexpr (KPROD) {
+                            b0 = dec1(sw[nt], 15 - ks, neg2);
+                            b1 = dec1(sw[nt], 7 - ks, neg2);
+                        } else {
+                            b0 = hk[nt][2 * e];
+                            b1 = hk[nt][2 * e + 1];
+                        }
+                    };
+                    if constexpr (R8) {
+                        // A: tokens g of tiles 2 mt and 2 mt + 1; B: rows 0..7
+                        const uint32_t qb[2] = {qa[0], qa[2]}, jb[2] = {qj[0], qj[2]};
+#pragma unroll
+                        for (int mt = 0; mt < MT; ++mt) {
+                            const int n0 = 2 * mt, n1 = 2 * mt + 1 < NT ? 2 * mt + 1 : 2 * mt;
+                            const uint32_t ka[4] = {hk[n0][2 * e], hk[n1][2 * e], hk[n0][2 * e + 1], hk[n1][2 * e + 1]};
+                            mma16816(sc[mt], ka, qb[0], qb[1]);
+                            uint32_t s00, s01, s10, s11;
+                            signs(n0, s00, s01);
+                            signs(n1, s10, s11);
+                            const uint32_t sa[4] = {s00, s10, s01, s11};
+                            mma16816(sd[mt], sa, jb[0], jb[1]);
+                        }
+                    } else {
+#pragma unroll
+                        for (int nt = 0; nt < NT; ++nt) {
+                            mma16816(sc[nt], qa, hk[nt][2 * e], hk[nt][2 * e + 1]);
+                            uint32_t b0, b1;
+                            signs(nt, b0, b1);
+                            mma16816(sd[nt], qj, b0, b1);
+                        }
                     }
                 }
             }
@@ -967,130 +1006,261 @@ __global__ void __launch_bounds__(kThreads, 1) split_mma_kernel(MmaArgs m) {
                 }
             };
             decode_values(0);
+            if constexpr (R8) {
+                // tokens ta (tile 2 mt) and tb = ta + 8 (tile 2 mt + 1) of the lane,
+                // rows r0 = 2 j and r1 = 2 j + 1: S^T entries (ta, r0), (ta, r1),
+                // (tb, r0), (tb, r1)
+                float2 nv8[MT];
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt) {
-                if constexpr (KPROD) {
-                    // codebook part + residual norm x QJL part, per token column
-                    const float2 gm = *reinterpret_cast<const float2*>(krn + base + 8 * nt + 2 * j);
-                    // (two tokens' columns per packed fp32 pair operation)
-                    const float2 lo = __ffma2_rn(gm, make_float2(sd[nt][0], sd[nt][1]), make_float2(sc[nt][0], sc[nt][1]));
-                    const float2 hi = __ffma2_rn(gm, make_float2(sd[nt][2], sd[nt][3]), make_float2(sc[nt][2], sc[nt][3]));
-                    sc[nt][0] = lo.x; sc[nt][1] = lo.y; sc[nt][2] = hi.x; sc[nt][3] = hi.y;
-                } else {
+                for (int mt = 0; mt < MT; ++mt) {
+                    const int ta = base + 16 * mt + g, tb = ta + 8;
+                    if constexpr (KPROD) {
+                        // codebook part + residual norm x QJL part
+                        const float ga = krn[ta], gb = krn[tb];
+                        sc[mt][0] = fmaf(ga, sd[mt][0], sc[mt][0]);
+                        sc[mt][1] = fmaf(ga, sd[mt][1], sc[mt][1]);
+                        sc[mt][2] = fmaf(gb, sd[mt][2], sc[mt][2]);
+                        sc[mt][3] = fmaf(gb, sd[mt][3], sc[mt][3]);
+                    } else {
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) sc[nt][e] += sd[nt][e];
+                        for (int e = 0; e < 4; ++e) sc[mt][e] += sd[mt][e];
+                    }
+                    const float kna = knorm[ta], knb = knorm[tb];
+                    sc[mt][0] *= kna;
+                    sc[mt][1] *= kna;
+                    sc[mt][2] *= knb;
+                    sc[mt][3] *= knb;
+                    if constexpr (!VGROUP) nv8[mt] = make_float2(vnorm[ta], vnorm[tb]);
+                    else nv8[mt] = make_float2(0.0f, 0.0f);
                 }
-            }
-            // ---------------- scale, mask, online softmax (log2 domain)
-            float2 nv[NT];
+                // masks only where the step reaches past the tile's end or a row's
+                // causal limit (past the end, the stage holds stale bytes: their
+                // value norms become 0)
+                if (base + 8 * NT > valid || t0 + base + 8 * NT - 1 > lim_all) {
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt) {
-                const float2 kn = *reinterpret_cast<const float2*>(knorm + base + 8 * nt + 2 * j);
-                if constexpr (!VGROUP) nv[nt] = *reinterpret_cast<const float2*>(vnorm + base + 8 * nt + 2 * j);
-                else nv[nt] = make_float2(0.0f, 0.0f);
-                const float2 lo = __fmul2_rn(make_float2(sc[nt][0], sc[nt][1]), kn);
-                const float2 hi = __fmul2_rn(make_float2(sc[nt][2], sc[nt][3]), kn);
-                sc[nt][0] = lo.x; sc[nt][1] = lo.y; sc[nt][2] = hi.x; sc[nt][3] = hi.y;
-            }
-            // masks only where the step reaches past the tile's end or a row's
-            // causal limit (past the end, the stage holds stale bytes: their
-            // value norms become 0)
-            if (base + 8 * NT > valid || t0 + base + 8 * NT - 1 > lim_all) {
-#pragma unroll
-                for (int nt = 0; nt < NT; ++nt) {
-                    const int tl = base + 8 * nt + 2 * j;
-                    const int pos = t0 + tl;
-                    const bool v0 = tl < valid, v1 = tl + 1 < valid;
-                    if (!(v0 && pos <= lim0)) sc[nt][0] = -INFINITY;
-                    if (!(v1 && pos + 1 <= lim0)) sc[nt][1] = -INFINITY;
-                    if (!(v0 && pos <= lim1)) sc[nt][2] = -INFINITY;
-                    if (!(v1 && pos + 1 <= lim1)) sc[nt][3] = -INFINITY;
-                    if (!v0) nv[nt].x = 0.0f;
-                    if (!v1) nv[nt].y = 0.0f;
-                }
-            }
-            const float th0 = mrow0 + lag, th1 = mrow1 + lag;
-            bool over = false;
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
-                over |= sc[nt][0] > th0 || sc[nt][1] > th0 || sc[nt][2] > th1 || sc[nt][3] > th1;
-            if (__any_sync(0xffffffffu, over)) {
-                // a score passed m + lag: move m to the exact row maxima
-                float mx0 = fmaxf(sc[0][0], sc[0][1]), mx1 = fmaxf(sc[0][2], sc[0][3]);
-#pragma unroll
-                for (int nt = 1; nt < NT; ++nt) {
-                    mx0 = fmaxf(mx0, fmaxf(sc[nt][0], sc[nt][1]));
-                    mx1 = fmaxf(mx1, fmaxf(sc[nt][2], sc[nt][3]));
-                }
-                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-                const float mn0 = fmaxf(mrow0, mx0), mn1 = fmaxf(mrow1, mx1);
-                const float al0 = ex2(mrow0 - mn0);
-                const float al1 = ex2(mrow1 - mn1);
-                lrow0 *= al0;
-                lrow1 *= al1;
-#pragma unroll
-                for (int p = 0; p < 16; ++p) {
-                    o[p][0] *= al0; o[p][1] *= al0;
-                    o[p][2] *= al1; o[p][3] *= al1;
-                }
-                mrow0 = mn0;
-                mrow1 = mn1;
-            }
-            // P' = fp16(p * value norm); the row sums add the weights actually
-            // multiplied (P' / norm), so the rounding of P' cancels in o = sum/L.
-            // A zero norm gives P' = 0 and a huge finite 1/norm (nothing added);
-            // its p enters the row sums in the rare branch below.
-            uint32_t pa[NT][2];
-            [[maybe_unused]] bool zero = false;
-            const float2 nm0 = make_float2(-mrow0, -mrow0), nm1 = make_float2(-mrow1, -mrow1);
-            float2 lsum = make_float2(0.0f, 0.0f);  // this step's (row g, row g + 8) sums
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt) {
-                const float2 x0 = __fadd2_rn(make_float2(sc[nt][0], sc[nt][1]), nm0);
-                const float2 x1 = __fadd2_rn(make_float2(sc[nt][2], sc[nt][3]), nm1);
-                float2 w01 = make_float2(ex2(x0.x), ex2(x0.y));
-                float2 w23 = make_float2(ex2(x1.x), ex2(x1.y));
-                float r0 = 1.0f, r1 = 1.0f;
-                if constexpr (!VGROUP) {
-                    const float nx = nv[nt].x, ny = nv[nt].y;
-                    zero |= !(fminf(nx, ny) > 0.0f);
-                    r0 = rcp_approx(fmaxf(nx, 1e-30f));
-                    r1 = rcp_approx(fmaxf(ny, 1e-30f));
-                    sc[nt][0] = w01.x;  // keep p for the zero-norm branch
-                    sc[nt][1] = w01.y;
-                    sc[nt][2] = w23.x;
-                    sc[nt][3] = w23.y;
-                    w01 = __fmul2_rn(w01, nv[nt]);
-                    w23 = __fmul2_rn(w23, nv[nt]);
-                }
-                pa[nt][0] = pack_half2(w01.x, w01.y);
-                pa[nt][1] = pack_half2(w23.x, w23.y);
-                const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&pa[nt][0]));
-                const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&pa[nt][1]));
-                lsum = __ffma2_rn(make_float2(f0.x, f1.x), make_float2(r0, r0), lsum);
-                lsum = __ffma2_rn(make_float2(f0.y, f1.y), make_float2(r1, r1), lsum);
-            }
-            lrow0 += lsum.x;
-            lrow1 += lsum.y;
-            if constexpr (!VGROUP) {
-                if (__any_sync(0xffffffffu, zero)) {
-#pragma unroll
-                    for (int nt = 0; nt < NT; ++nt) {
-                        if (!(nv[nt].x > 0.0f)) { lrow0 += sc[nt][0]; lrow1 += sc[nt][2]; }
-                        if (!(nv[nt].y > 0.0f)) { lrow0 += sc[nt][1]; lrow1 += sc[nt][3]; }
+                    for (int mt = 0; mt < MT; ++mt) {
+                        const int ta = base + 16 * mt + g, tb = ta + 8;
+                        const bool va = ta < valid, vb = tb < valid;
+                        if (!(va && t0 + ta <= lim0)) sc[mt][0] = -INFINITY;
+                        if (!(va && t0 + ta <= lim1)) sc[mt][1] = -INFINITY;
+                        if (!(vb && t0 + tb <= lim0)) sc[mt][2] = -INFINITY;
+                        if (!(vb && t0 + tb <= lim1)) sc[mt][3] = -INFINITY;
+                        if (!va) nv8[mt].x = 0.0f;
+                        if (!vb) nv8[mt].y = 0.0f;
                     }
                 }
-            }
-            // ---------------- O += P' V, 16 tokens per k-group
+                const float th0 = mrow0 + lag, th1 = mrow1 + lag;
+                bool over = false;
 #pragma unroll
-            for (int kg = 0; kg < NT / 2; ++kg) {
-                if (kg > 0) decode_values(kg);
-                const uint32_t pk[4] = {pa[2 * kg][0], pa[2 * kg][1], pa[2 * kg + 1][0], pa[2 * kg + 1][1]};
+                for (int mt = 0; mt < MT; ++mt)
+                    over |= sc[mt][0] > th0 || sc[mt][1] > th1 || sc[mt][2] > th0 || sc[mt][3] > th1;
+                if (__any_sync(0xffffffffu, over)) {
+                    // a score passed m + lag: move m to the exact row maxima (the
+                    // lanes g of one j hold the rows' tokens)
+                    float mx0 = fmaxf(sc[0][0], sc[0][2]), mx1 = fmaxf(sc[0][1], sc[0][3]);
 #pragma unroll
-                for (int p = 0; p < 16; ++p) mma16816(o[p], pk, movmatrix_t(hA[p]), movmatrix_t(hB[p]));
+                    for (int mt = 1; mt < MT; ++mt) {
+                        mx0 = fmaxf(mx0, fmaxf(sc[mt][0], sc[mt][2]));
+                        mx1 = fmaxf(mx1, fmaxf(sc[mt][1], sc[mt][3]));
+                    }
+#pragma unroll
+                    for (int o2 = 4; o2 < 32; o2 <<= 1) {
+                        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o2));
+                        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o2));
+                    }
+                    const float mn0 = fmaxf(mrow0, mx0), mn1 = fmaxf(mrow1, mx1);
+                    const float al0 = ex2(mrow0 - mn0);
+                    const float al1 = ex2(mrow1 - mn1);
+                    lrow0 *= al0;
+                    lrow1 *= al1;
+#pragma unroll
+                    for (int p = 0; p < kOT; ++p) {
+                        o[p][0] *= al0; o[p][1] *= al1;
+                        o[p][2] *= al0; o[p][3] *= al1;
+                    }
+                    mrow0 = mn0;
+                    mrow1 = mn1;
+                }
+                // P' = fp16(p * value norm) per token; the row sums add P' / norm
+                // (a zero norm: its p enters the row sums in the branch below)
+                uint32_t pu[MT][2];
+                [[maybe_unused]] bool zero = false;
+                float2 lsum = make_float2(0.0f, 0.0f);  // this step's (row r0, row r1) sums
+#pragma unroll
+                for (int mt = 0; mt < MT; ++mt) {
+                    float2 wa = make_float2(ex2(sc[mt][0] - mrow0), ex2(sc[mt][1] - mrow1));   // token ta
+                    float2 wb = make_float2(ex2(sc[mt][2] - mrow0), ex2(sc[mt][3] - mrow1));   // token tb
+                    float ra = 1.0f, rb = 1.0f;
+                    if constexpr (!VGROUP) {
+                        const float nx = nv8[mt].x, ny = nv8[mt].y;
+                        zero |= !(fminf(nx, ny) > 0.0f);
+                        ra = rcp_approx(fmaxf(nx, 1e-30f));
+                        rb = rcp_approx(fmaxf(ny, 1e-30f));
+                        sc[mt][0] = wa.x;  // keep p for the zero-norm branch
+                        sc[mt][1] = wa.y;
+                        sc[mt][2] = wb.x;
+                        sc[mt][3] = wb.y;
+                        wa = __fmul2_rn(wa, make_float2(nx, nx));
+                        wb = __fmul2_rn(wb, make_float2(ny, ny));
+                    }
+                    pu[mt][0] = pack_half2(wa.x, wa.y);
+                    pu[mt][1] = pack_half2(wb.x, wb.y);
+                    const float2 fa = __half22float2(*reinterpret_cast<const __half2*>(&pu[mt][0]));
+                    const float2 fb = __half22float2(*reinterpret_cast<const __half2*>(&pu[mt][1]));
+                    lsum = __ffma2_rn(fa, make_float2(ra, ra), lsum);
+                    lsum = __ffma2_rn(fb, make_float2(rb, rb), lsum);
+                }
+                lrow0 += lsum.x;
+                lrow1 += lsum.y;
+                if constexpr (!VGROUP) {
+                    if (__any_sync(0xffffffffu, zero)) {
+#pragma unroll
+                        for (int mt = 0; mt < MT; ++mt) {
+                            if (!(nv8[mt].x > 0.0f)) { lrow0 += sc[mt][0]; lrow1 += sc[mt][1]; }
+                            if (!(nv8[mt].y > 0.0f)) { lrow0 += sc[mt][2]; lrow1 += sc[mt][3]; }
+                        }
+                    }
+                }
+                // ---------------- O^T += V^T P'^T, 16 tokens (one m16 tile) per k-group:
+                // A = the value columns of pairs 2 p and 2 p + 1 (16) x the tokens,
+                // B = P'^T (tokens x rows) by transposing the lane's (token, row pair)
+#pragma unroll
+                for (int kg = 0; kg < MT; ++kg) {
+                    if (kg > 0) decode_values(kg);
+                    const uint32_t b0 = movmatrix_t(pu[kg][0]), b1 = movmatrix_t(pu[kg][1]);
+#pragma unroll
+                    for (int p = 0; p < kOT; ++p) {
+                        const uint32_t va[4] = {movmatrix_t(hA[2 * p]), movmatrix_t(hA[2 * p + 1]),
+                                                movmatrix_t(hB[2 * p]), movmatrix_t(hB[2 * p + 1])};
+                        mma16816(o[p], va, b0, b1);
+                    }
+                }
+            } else {
+    #pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    if constexpr (KPROD) {
+                        // codebook part + residual norm x QJL part, per token column
+                        const float2 gm = *reinterpret_cast<const float2*>(krn + base + 8 * nt + 2 * j);
+                        // (two tokens' columns per packed fp32 pair operation)
+                        const float2 lo = __ffma2_rn(gm, make_float2(sd[nt][0], sd[nt][1]), make_float2(sc[nt][0], sc[nt][1]));
+                        const float2 hi = __ffma2_rn(gm, make_float2(sd[nt][2], sd[nt][3]), make_float2(sc[nt][2], sc[nt][3]));
+                        sc[nt][0] = lo.x; sc[nt][1] = lo.y; sc[nt][2] = hi.x; sc[nt][3] = hi.y;
+                    } else {
+    #pragma unroll
+                        for (int e = 0; e < 4; ++e) sc[nt][e] += sd[nt][e];
+                    }
+                }
+                // ---------------- scale, mask, online softmax (log2 domain)
+                float2 nv[NT];
+    #pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    const float2 kn = *reinterpret_cast<const float2*>(knorm + base + 8 * nt + 2 * j);
+                    if constexpr (!VGROUP) nv[nt] = *reinterpret_cast<const float2*>(vnorm + base + 8 * nt + 2 * j);
+                    else nv[nt] = make_float2(0.0f, 0.0f);
+                    const float2 lo = __fmul2_rn(make_float2(sc[nt][0], sc[nt][1]), kn);
+                    const float2 hi = __fmul2_rn(make_float2(sc[nt][2], sc[nt][3]), kn);
+                    sc[nt][0] = lo.x; sc[nt][1] = lo.y; sc[nt][2] = hi.x; sc[nt][3] = hi.y;
+                }
+                // masks only where the step reaches past the tile's end or a row's
+                // causal limit (past the end, the stage holds stale bytes: their
+                // value norms become 0)
+                if (base + 8 * NT > valid || t0 + base + 8 * NT - 1 > lim_all) {
+    #pragma unroll
+                    for (int nt = 0; nt < NT; ++nt) {
+                        const int tl = base + 8 * nt + 2 * j;
+                        const int pos = t0 + tl;
+                        const bool v0 = tl < valid, v1 = tl + 1 < valid;
+                        if (!(v0 && pos <= lim0)) sc[nt][0] = -INFINITY;
+                        if (!(v1 && pos + 1 <= lim0)) sc[nt][1] = -INFINITY;
+                        if (!(v0 && pos <= lim1)) sc[nt][2] = -INFINITY;
+                        if (!(v1 && pos + 1 <= lim1)) sc[nt][3] = -INFINITY;
+                        if (!v0) nv[nt].x = 0.0f;
+                        if (!v1) nv[nt].y = 0.0f;
+                    }
+                }
+                const float th0 = mrow0 + lag, th1 = mrow1 + lag;
+                bool over = false;
+    #pragma unroll
+                for (int nt = 0; nt < NT; ++nt)
+                    over |= sc[nt][0] > th0 || sc[nt][1] > th0 || sc[nt][2] > th1 || sc[nt][3] > th1;
+                if (__any_sync(0xffffffffu, over)) {
+                    // a score passed m + lag: move m to the exact row maxima
+                    float mx0 = fmaxf(sc[0][0], sc[0][1]), mx1 = fmaxf(sc[0][2], sc[0][3]);
+    #pragma unroll
+                    for (int nt = 1; nt < NT; ++nt) {
+                        mx0 = fmaxf(mx0, fmaxf(sc[nt][0], sc[nt][1]));
+                        mx1 = fmaxf(mx1, fmaxf(sc[nt][2], sc[nt][3]));
+                    }
+                    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+                    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+                    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+                    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+                    const float mn0 = fmaxf(mrow0, mx0), mn1 = fmaxf(mrow1, mx1);
+                    const float al0 = ex2(mrow0 - mn0);
+                    const float al1 = ex2(mrow1 - mn1);
+                    lrow0 *= al0;
+                    lrow1 *= al1;
+    #pragma unroll
+                    for (int p = 0; p < 16; ++p) {
+                        o[p][0] *= al0; o[p][1] *= al0;
+                        o[p][2] *= al1; o[p][3] *= al1;
+                    }
+                    mrow0 = mn0;
+                    mrow1 = mn1;
+                }
+                // P' = fp16(p * value norm); the row sums add the weights actually
+                // multiplied (P' / norm), so the rounding of P' cancels in o = sum/L.
+                // A zero norm gives P' = 0 and a huge finite 1/norm (nothing added);
+                // its p enters the row sums in the rare branch below.
+                uint32_t pa[NT][2];
+                [[maybe_unused]] bool zero = false;
+                const float2 nm0 = make_float2(-mrow0, -mrow0), nm1 = make_float2(-mrow1, -mrow1);
+                float2 lsum = make_float2(0.0f, 0.0f);  // this step's (row g, row g + 8) sums
+    #pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    const float2 x0 = __fadd2_rn(make_float2(sc[nt][0], sc[nt][1]), nm0);
+                    const float2 x1 = __fadd2_rn(make_float2(sc[nt][2], sc[nt][3]), nm1);
+                    float2 w01 = make_float2(ex2(x0.x), ex2(x0.y));
+                    float2 w23 = make_float2(ex2(x1.x), ex2(x1.y));
+                    float r0 = 1.0f, r1 = 1.0f;
+                    if constexpr (!VGROUP) {
+                        const float nx = nv[nt].x, ny = nv[nt].y;
+                        zero |= !(fminf(nx, ny) > 0.0f);
+                        r0 = rcp_approx(fmaxf(nx, 1e-30f));
+                        r1 = rcp_approx(fmaxf(ny, 1e-30f));
+                        sc[nt][0] = w01.x;  // keep p for the zero-norm branch
+                        sc[nt][1] = w01.y;
+                        sc[nt][2] = w23.x;
+                        sc[nt][3] = w23.y;
+                        w01 = __fmul2_rn(w01, nv[nt]);
+                        w23 = __fmul2_rn(w23, nv[nt]);
+                    }
+                    pa[nt][0] = pack_half2(w01.x, w01.y);
+                    pa[nt][1] = pack_half2(w23.x, w23.y);
+                    const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&pa[nt][0]));
+                    const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&pa[nt][1]));
+                    lsum = __ffma2_rn(make_float2(f0.x, f1.x), make_float2(r0, r0), lsum);
+                    lsum = __ffma2_rn(make_float2(f0.y, f1.y), make_float2(r1, r1), lsum);
+                }
+                lrow0 += lsum.x;
+                lrow1 += lsum.y;
+                if constexpr (!VGROUP) {
+                    if (__any_sync(0xffffffffu, zero)) {
+    #pragma unroll
+                        for (int nt = 0; nt < NT; ++nt) {
+                            if (!(nv[nt].x > 0.0f)) { lrow0 += sc[nt][0]; lrow1 += sc[nt][2]; }
+                            if (!(nv[nt].y > 0.0f)) { lrow0 += sc[nt][1]; lrow1 += sc[nt][3]; }
+                        }
+                    }
+                }
+                // ---------------- O += P' V, 16 tokens per k-group
+    #pragma unroll
+                for (int kg = 0; kg < NT / 2; ++kg) {
+                    if (kg > 0) decode_values(kg);
+                    const uint32_t pk[4] = {pa[2 * kg][0], pa[2 * kg][1], pa[2 * kg + 1][0], pa[2 * kg + 1][1]};
+    #pragma unroll
+                    for (int p = 0; p < 16; ++p) mma16816(o[p], pk, movmatrix_t(hA[p]), movmatrix_t(hB[p]));
+                }
             }
         };
         if (TT >= 32) {
@@ -1118,38 +1288,59 @@ __global__ void __launch_bounds__(kThreads, 1) split_mma_kernel(MmaArgs m) {
     if (threadIdx.x == 0) mbar_inval(tbar);
 
     // ---------------- merge the warps of this CTA
-    lrow0 += __shfl_xor_sync(0xffffffffu, lrow0, 1);
-    lrow0 += __shfl_xor_sync(0xffffffffu, lrow0, 2);
-    lrow1 += __shfl_xor_sync(0xffffffffu, lrow1, 1);
-    lrow1 += __shfl_xor_sync(0xffffffffu, lrow1, 2);
+    // row sums over the lanes that share the thread's rows (R8: the lanes g of
+    // one j; else the lanes j of one g)
+#pragma unroll
+    for (int o2 = R8 ? 4 : 1; o2 < (R8 ? 32 : 4); o2 <<= 1) {
+        lrow0 += __shfl_xor_sync(0xffffffffu, lrow0, o2);
+        lrow1 += __shfl_xor_sync(0xffffffffu, lrow1, o2);
+    }
     __syncthreads();
     constexpr int kStride = kCoStride;  // column d at d + d / 32
     float* cm = reinterpret_cast<float*>(smem);
     float* cl = cm + kWarps * kRows;
     float* co = cl + kWarps * kRows;
-    if (j == 0) {
-        cm[warp * kRows + g] = mrow0;
-        cm[warp * kRows + g + 8] = mrow1;
-        cl[warp * kRows + g] = lrow0;
-        cl[warp * kRows + g + 8] = lrow1;
+    const int lr0 = r0 - rg * kRows, lr1 = r1 - rg * kRows;   // the thread's rows in the group
+    if (R8 ? g == 0 : j == 0) {
+        cm[warp * kRows + lr0] = mrow0;
+        cm[warp * kRows + lr1] = mrow1;
+        cl[warp * kRows + lr0] = lrow0;
+        cl[warp * kRows + lr1] = lrow1;
     }
+    if constexpr (R8) {
+        // o[p]: O^T of value pairs 2 p (entries 0, 1) and 2 p + 1 (2, 3), column g
+        // of the pair's eight (chunk g / 2, element g % 2), rows lr0 (0, 2) and lr1
 #pragma unroll
-    for (int p = 0; p < 16; ++p) {
-        int pa_, pb_;
-        if constexpr (VGROUP) group_pair(VB, p, pa_, pb_);
-        else mse_pair(VB, p, pa_, pb_);
-        const int d0 = 33 * j + pa_, d1 = 33 * j + pb_;
-        co[(warp * kRows + g) * kStride + d0] = o[p][0];
-        co[(warp * kRows + g) * kStride + d1] = o[p][1];
-        co[(warp * kRows + g + 8) * kStride + d0] = o[p][2];
-        co[(warp * kRows + g + 8) * kStride + d1] = o[p][3];
+        for (int p = 0; p < kOT; ++p) {
+#pragma unroll
+            for (int hp = 0; hp < 2; ++hp) {
+                int pa_, pb_;
+                if constexpr (VGROUP) group_pair(VB, 2 * p + hp, pa_, pb_);
+                else mse_pair(VB, 2 * p + hp, pa_, pb_);
+                const int d = 33 * (g >> 1) + ((g & 1) ? pb_ : pa_);
+                co[(warp * kRows + lr0) * kStride + d] = o[p][2 * hp];
+                co[(warp * kRows + lr1) * kStride + d] = o[p][2 * hp + 1];
+            }
+        }
+    } else {
+#pragma unroll
+        for (int p = 0; p < kOT; ++p) {
+            int pa_, pb_;
+            if constexpr (VGROUP) group_pair(VB, p, pa_, pb_);
+            else mse_pair(VB, p, pa_, pb_);
+            const int d0 = 33 * j + pa_, d1 = 33 * j + pb_;
+            co[(warp * kRows + lr0) * kStride + d0] = o[p][0];
+            co[(warp * kRows + lr0) * kStride + d1] = o[p][1];
+            co[(warp * kRows + lr1) * kStride + d0] = o[p][2];
+            co[(warp * kRows + lr1) * kStride + d1] = o[p][3];
+        }
     }
     __syncthreads();
     const int S = a.plan.splits;
     const int tid = threadIdx.x;
     const int r = tid >> 4;
     const int dbase = (tid & 15) * 8;
-    const bool merger = tid < kRows * 16;  // 16 threads per row, 8 columns each
+    const bool merger = tid < (R8 ? 8 : kRows) * 16;  // 16 threads per row, 8 columns each
     if (merger) {
         float M = -INFINITY;
         for (int w = 0; w < kWarps; ++w) M = fmaxf(M, cm[w * kRows + r]);
@@ -1349,7 +1540,8 @@ cudaError_t launch_mma_wide(const MmaArgs& m, size_t smem, cudaStream_t s) {
     return launch_merge<VGROUP, D>(m, s);
 }
 
-template <int KB, bool KPROD, bool VGROUP, int VB>
+// R8: the transposed split kernel (head_dim 128, at most 8 query rows per unit).
+template <int KB, bool KPROD, bool VGROUP, int VB, bool R8 = false>
 cudaError_t launch_mma(const MmaArgs& m, size_t smem, cudaStream_t s, const EncodeAppendArgs* step) {
     const DecodeArgs& a = m.a;
     static std::atomic<uint64_t> attr_set{0};
@@ -1363,9 +1555,9 @@ cudaError_t launch_mma(const MmaArgs& m, size_t smem, cudaStream_t s, const Enco
         int optin = 0;
         cudaFuncAttributes fa{};
         cudaError_t e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-        if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, split_mma_kernel<KB, KPROD, VGROUP, VB>);
+        if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, split_mma_kernel<KB, KPROD, VGROUP, VB, kD, R8>);
         if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(split_mma_kernel<KB, KPROD, VGROUP, VB>,
+            e = cudaFuncSetAttribute(split_mma_kernel<KB, KPROD, VGROUP, VB, kD, R8>,
                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      optin - static_cast<int>(fa.sharedSizeBytes));
         if (e != cudaSuccess) {
@@ -1381,7 +1573,7 @@ cudaError_t launch_mma(const MmaArgs& m, size_t smem, cudaStream_t s, const Enco
     if (step) {
         e = launch_step_prep(KB, frag_order(KB, KPROD, VGROUP, VB), m, *step, s);
         if (e != cudaSuccess) return e;
-        e = launch_overlapped(split_mma_kernel<KB, KPROD, VGROUP, VB>, dim3(a.pool.Hkv * RG, a.batch, a.plan.splits),
+        e = launch_overlapped(split_mma_kernel<KB, KPROD, VGROUP, VB, kD, R8>, dim3(a.pool.Hkv * RG, a.batch, a.plan.splits),
                               dim3(kThreads), smem, s, m);
         g_launches.fetch_add(1, std::memory_order_relaxed);
         if (e != cudaSuccess) return e;
@@ -1403,7 +1595,7 @@ cudaError_t launch_mma(const MmaArgs& m, size_t smem, cudaStream_t s, const Enco
                           sizeof(QSmem), s, m);
     g_launches.fetch_add(1, std::memory_order_relaxed);
     if (e != cudaSuccess) return e;
-    e = launch_overlapped(split_mma_kernel<KB, KPROD, VGROUP, VB>, dim3(a.pool.Hkv * RG, a.batch, a.plan.splits),
+    e = launch_overlapped(split_mma_kernel<KB, KPROD, VGROUP, VB, kD, R8>, dim3(a.pool.Hkv * RG, a.batch, a.plan.splits),
                           dim3(kThreads), smem, s, m);
     g_launches.fetch_add(1, std::memory_order_relaxed);
     if (e != cudaSuccess) return e;

@@ -101,6 +101,7 @@ struct QuantizeArgs {
 // Decode plan shared by workspace sizing and the launch.
 struct DecodePlan {
     int kind;         // 0: SIMT kernels (any shape), 1: tensor-core kernels (head_dim 128, some 64 and 256)
+    int r8;           // tensor-core kernels in the transposed form (head_dim 128, at most 8 rows per unit)
     int rows;         // G * Lq
     int row_groups;   // ceil(rows / 16)
     int splits;       // token splits per (sequence, kv head, row group)
