@@ -70,6 +70,7 @@ void free_codec(tq_codec* c) {
     cudaFree(c->d_Stc);
     cudaFree(c->d_quad);
     cudaFree(c->d_pair);
+    cudaFree(c->d_pair4);
     if (prev >= 0) cudaSetDevice(prev);
     delete c;
 }
@@ -116,6 +117,16 @@ std::vector<uint32_t> pair_table(const std::vector<float>& cq) {
     return t;
 }
 
+// 4-bit code pairs: entry e (a byte of two codes) at 128 e + 4 c for bank copy c < 32.
+std::vector<uint32_t> pair4_table(const std::vector<float>& cq) {
+    std::vector<uint32_t> t(256 * 32);
+    for (int i = 0; i < 256 * 32; ++i) {
+        const int e = i >> 5;
+        t[i] = half_bits_exact(cq[e & 15]) | (half_bits_exact(cq[e >> 4]) << 16);
+    }
+    return t;
+}
+
 std::vector<float> transpose(const std::vector<float>& a, int D) {
     std::vector<float> t(a.size());
     for (int i = 0; i < D; ++i)
@@ -154,6 +165,7 @@ CodecDev dev_view(const tq_codec* c) {
     d.Stc = c->d_Stc;
     d.quad = c->d_quad;
     d.pair = c->d_pair;
+    d.pair4 = c->d_pair4;
     d.D = c->head_dim;
     d.mode = c->mode;
     d.bits = c->bits;
@@ -313,6 +325,8 @@ tq_status tq_codec_create(int head_dim, int bits, tq_mode mode, uint64_t seed, t
     if (st == TQ_OK) st = upload(&c->d_cq, c->host.op_levels);
     if (st == TQ_OK && c->index_bits == 2) st = upload(&c->d_quad, quad_table(c->host.op_levels));
     if (st == TQ_OK && c->index_bits == 3) st = upload(&c->d_pair, pair_table(c->host.op_levels));
+    if (st == TQ_OK && c->index_bits == 4 && mode == TQ_MODE_MSE)
+        st = upload(&c->d_pair4, pair4_table(c->host.op_levels));
     if (st == TQ_OK && head_dim <= 128) {
         // tensor-core operands for the chunked-prefill encoder: 16 R and S, fp16 hi + lo
         std::vector<uint16_t> op;

@@ -312,6 +312,18 @@ __device__ __forceinline__ void load_words(const uint32_t* p, uint32_t (&w)[NW])
     }
 }
 
+// The fp16 pairs of one word's four bytes (codes 2k, 2k + 1 for byte k) from
+// the 4-bit pair table: entry e (a byte) at 128 e + 4 L for lane L; byte k is
+// shifted to bit 7, masked and added to the lane's address (one shift, one
+// logic op, one add and one load per pair).
+__device__ __forceinline__ void pair4_word(uint32_t w, uint32_t lane_addr, uint32_t (&h)[4]) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const uint32_t f = k == 0 ? shl_f(w, 7) : (w >> (8 * k - 7));
+        h[k] = lds_u32(mad_lo(f & 0x7F80u, kDc.pow2[0], lane_addr));
+    }
+}
+
 template <int B>
 struct MseTable {
     using type = Tab8;
@@ -669,16 +681,38 @@ __global__ void __launch_bounds__(kThreads, 1) split_mma_kernel(MmaArgs m) {
         const uint32_t region = smem_u32(smem + st.vt_off);
         pair_off = st.vt_off + (((region + kVPairBytes - 1) & ~static_cast<uint32_t>(kVPairBytes - 1)) - region);
     }
+    // 4-bit MSE keys / values through the shared 4-bit pair table (MSE keys)
+    constexpr bool kP4K = pair4_keys(KB, KPROD), kP4V = pair4_values(KPROD, VGROUP, VB);
     const bool quad_copy = kQuadTab && a.kc.quad, pair_copy = kPairTab && a.vc.pair;
+    const bool p4k_copy = kP4K && a.kc.pair4, p4v_copy = kP4V && a.vc.pair4;
     if (threadIdx.x == 0) {
         mbar_init(tbar, 2);
         mbar_fence_init();
-        mbar_expect_tx(tbar, (quad_copy ? kKQuadBytes : 0) + (pair_copy ? kVPairBytes : 0));
+        mbar_expect_tx(tbar, (quad_copy ? kKQuadBytes : 0) + (pair_copy ? kVPairBytes : 0) +
+                                 (p4k_copy ? kPair4Bytes : 0) + (p4v_copy ? kPair4Bytes : 0));
         if (quad_copy) bulk_g2s(smem + st.kt_off, a.kc.quad, kKQuadBytes, tbar);
         if (pair_copy) bulk_g2s(smem + pair_off, a.vc.pair, kVPairBytes, tbar);
+        if (p4k_copy) bulk_g2s(smem + st.kt_off, a.kc.pair4, kPair4Bytes, tbar);
+        if (p4v_copy) bulk_g2s(smem + st.vt_off, a.vc.pair4, kPair4Bytes, tbar);
+    }
+    // a codec without the prebuilt table: build it here
+    auto build_pair4 = [&](uint32_t* tab, const float* cq) {
+        for (int i = threadIdx.x; i < 256 * 32; i += kThreads) {
+            const int e = i >> 5;
+            tab[i] = h_bits(__ldg(cq + (e & 15))) | (h_bits(__ldg(cq + (e >> 4))) << 16);
+        }
+    };
+    uint32_t k4_lane = 0, v4_lane = 0;
+    if constexpr (kP4K) {
+        k4_lane = smem_u32(smem + st.kt_off) + 4u * lane;
+        if (!p4k_copy) build_pair4(reinterpret_cast<uint32_t*>(smem + st.kt_off), a.kc.cq);
+    }
+    if constexpr (kP4V) {
+        v4_lane = smem_u32(smem + st.vt_off) + 4u * lane;
+        if (!p4v_copy) build_pair4(reinterpret_cast<uint32_t*>(smem + st.vt_off), a.vc.cq);
     }
     typename MseTable<KB>::type ktab{};
-    if constexpr (!kQuadTab) ktab = mse_table<KB>(a.kc.cq);
+    if constexpr (!kQuadTab && !kP4K) ktab = mse_table<KB>(a.kc.cq);
     uint32_t kt_lane = 0;
     if constexpr (kQuadTab) {
         kt_lane = smem_u32(smem + st.kt_off) + 8u * (lane & 15);
@@ -712,7 +746,7 @@ __global__ void __launch_bounds__(kThreads, 1) split_mma_kernel(MmaArgs m) {
         }
     }
     typename MseTable<VGROUP ? 2 : VB>::type vtab{};
-    if constexpr (!VGROUP && !kPairTab) vtab = mse_table<VB>(a.vc.cq);
+    if constexpr (!VGROUP && !kPairTab && !kP4V) vtab = mse_table<VB>(a.vc.cq);
     uint32_t vt_lane = 0;
     if constexpr (kPairTab) {
         vt_lane = smem_u32(smem + pair_off) + 4u * lane;
@@ -922,7 +956,10 @@ __global__ void __launch_bounds__(kThreads, 1) split_mma_kernel(MmaArgs m) {
             for (int q2 = 0; q2 < 4; ++q2) {
                 uint32_t hk[NT][4];
 #pragma unroll
-                for (int nt = 0; nt < NT; ++nt) key_ks2<KB, kQuadTab>(kw[nt], ktab, kt_lane, q2, hk[nt]);
+                for (int nt = 0; nt < NT; ++nt) {
+                    if constexpr (kP4K) pair4_word(kw[nt][q2 < KB ? q2 : 0], k4_lane, hk[nt]);
+                    else key_ks2<KB, kQuadTab>(kw[nt], ktab, kt_lane, q2, hk[nt]);
+                }
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
                     const int ks = 2 * q2 + e;
@@ -1000,6 +1037,18 @@ __global__ void __launch_bounds__(kThreads, 1) split_mma_kernel(MmaArgs m) {
                 } else if constexpr (kPairTab) {
                     pair3_chunk(wA, vt_lane, hA);
                     pair3_chunk(wB, vt_lane, hB);
+                } else if constexpr (kP4V) {
+#pragma unroll
+                    for (int wi = 0; wi < 4; ++wi) {
+                        uint32_t ga[4], gb[4];
+                        pair4_word(wA[wi < VB ? wi : 0], v4_lane, ga);
+                        pair4_word(wB[wi < VB ? wi : 0], v4_lane, gb);
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            hA[4 * wi + k] = ga[k];
+                            hB[4 * wi + k] = gb[k];
+                        }
+                    }
                 } else {
                     mse_chunk<VB>(wA, vtab, hA);
                     mse_chunk<VB>(wB, vtab, hB);

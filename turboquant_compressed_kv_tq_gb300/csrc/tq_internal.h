@@ -54,6 +54,8 @@ struct CodecDev {
     // 128 e + 4 c for bank copy c < 32, fp16 pair (cq[e & 7], cq[e >> 3])
     const uint32_t* quad;
     const uint32_t* pair;
+    const uint32_t* pair4;  // 4-bit code pairs, entry e (a byte) at 128 e + 4 c for bank copy c < 32:
+                            // fp16 pair (cq[e & 15], cq[e >> 4]); or nullptr
     int D;
     int mode;          // tq_mode
     int bits;          // total bits
@@ -262,4 +264,5 @@ struct tq_codec {
     uint16_t* d_Stc = nullptr;
     uint32_t* d_quad = nullptr;  // decode lookup table of 2-bit code quads (index bits 2)
     uint32_t* d_pair = nullptr;  // decode lookup table of 3-bit code pairs (index bits 3)
+    uint32_t* d_pair4 = nullptr;  // decode lookup table of 4-bit code pairs (MSE, index bits 4)
 };
