@@ -493,12 +493,12 @@ DecodePlan make_decode_plan(const tq_cache_desc* d, int batch, int G, int Lq, in
                 p.vt_off = static_cast<int>(ringq);
                 ringq += mmadec::kVPairRegion;
             }
-            if (mmadec::pair4_values(p.kprod, p.vgroup, p.vb)) {  // pair table of 4-bit value codes
+            if (mmadec::pair4_values(D, p.kprod, p.vgroup, p.vb)) {  // pair table of 4-bit value codes
                 p.vt_off = static_cast<int>(ringq);
                 ringq += mmadec::kPair4Bytes;
             }
             p.kt_off = -1;
-            if (mmadec::pair4_keys(p.kb, p.kprod)) {  // pair table of 4-bit key codes
+            if (mmadec::pair4_keys(D, p.kb, p.kprod)) {  // pair table of 4-bit key codes
                 p.kt_off = static_cast<int>(ringq);
                 ringq += mmadec::kPair4Bytes;
             }

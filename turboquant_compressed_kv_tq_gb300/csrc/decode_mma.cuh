@@ -66,11 +66,14 @@ constexpr int kVPairRegion = 2 * kVPairBytes;
 constexpr int kKQuadBytes = 256 * 16 * 8;
 __host__ __device__ constexpr bool quad_keys(int kb, bool kprod, bool vgroup) { return kb == 2 && !(kprod && vgroup); }
 // Pair table of 4-bit MSE codes: 256 entries (a byte: two codes) x 32 bank
-// copies x 4 bytes. Used with MSE keys: for 4-bit keys, and for 4-bit values
-// (with prod keys the stages would have to drop to 32 tokens to make room).
+// copies x 4 bytes. Used with MSE keys at head_dims up to 128: for 4-bit keys,
+// and for 4-bit values (with prod keys, or at head_dim 256, the stages would
+// have to shrink to make room).
 constexpr int kPair4Bytes = 256 * 32 * 4;
-__host__ __device__ constexpr bool pair4_keys(int kb, bool kprod) { return !kprod && kb == 4; }
-__host__ __device__ constexpr bool pair4_values(bool kprod, bool vgroup, int vb) { return !kprod && !vgroup && vb == 4; }
+__host__ __device__ constexpr bool pair4_keys(int d, int kb, bool kprod) { return d <= kD && !kprod && kb == 4; }
+__host__ __device__ constexpr bool pair4_values(int d, bool kprod, bool vgroup, int vb) {
+    return d <= kD && !kprod && !vgroup && vb == 4;
+}
 // QJL sign operands through a shared table of sign nibbles (16 entries x 16
 // bank copies x 8 bytes), placed in the slack of the value pair table's
 // region: prod keys with 3-bit MSE values.

@@ -682,7 +682,7 @@ __global__ void __launch_bounds__(kThreads, 1) split_mma_kernel(MmaArgs m) {
         pair_off = st.vt_off + (((region + kVPairBytes - 1) & ~static_cast<uint32_t>(kVPairBytes - 1)) - region);
     }
     // 4-bit MSE keys / values through the shared 4-bit pair table (MSE keys)
-    constexpr bool kP4K = pair4_keys(KB, KPROD), kP4V = pair4_values(KPROD, VGROUP, VB);
+    constexpr bool kP4K = pair4_keys(D, KB, KPROD), kP4V = pair4_values(D, KPROD, VGROUP, VB);
     const bool quad_copy = kQuadTab && a.kc.quad, pair_copy = kPairTab && a.vc.pair;
     const bool p4k_copy = kP4K && a.kc.pair4, p4v_copy = kP4V && a.vc.pair4;
     if (threadIdx.x == 0) {
