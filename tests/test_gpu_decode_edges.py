@@ -156,6 +156,22 @@ def test_few_rows_transposed_kernel(key, value, G, Lq):
     _check(w)
 
 
+@pytest.mark.parametrize("G,Lq,bt", [(8, 2, 16), (4, 1, 16), (8, 2, 256), (4, 1, 64)])
+def test_splits_with_partial_warp_rounds(G, Lq, bt):
+    # The 12 warps of a split take its tiles in turn; sequence lengths whose
+    # splits end in a partial round (some warps a tile short), a lone partial
+    # tile and a split of two tokens; 16-token blocks in a shuffled order (a
+    # tile gathers several blocks); 16 query rows per KV head (the 16-row
+    # form) or 4 (transposed)
+    w = _workload(("prod", 3), ("mse", 3), (20000, 1000, 150, 2), Lq, 2, G, bt, shuffle=True)
+    _, plan = _plan(w)
+    assert plan["tensor_cores"] == 1 and plan["transposed"] == (1 if G * Lq <= 8 else 0), plan
+    tile, chunk = plan["tile_tokens"], plan["chunk_tokens"]
+    tiles = {-(-min(chunk, n - t0) // tile) for n in w.seq_lens for t0 in range(0, n, chunk)}
+    assert any(t % 12 for t in tiles) and 1 in tiles, (plan, tiles)
+    _check(w)
+
+
 def test_head_scales_mse4():
     _check(_workload(("mse", 4), ("mse", 4), (5000,), 2, 2, 8, 256, scales=(0.5, 2.0)))
 
