@@ -652,6 +652,17 @@ const char *tq_status_string(tq_status status);
 tq_status tq_device_error(uint32_t *flags);
 /* Number of kernels this library has launched since it was loaded. */
 uint64_t tq_launch_count(void);
+/* Self-test of the bounded-wait error path (the kernels wait for their bulk
+ * copies on mbarriers, each wait bounded; a wait that runs out sets
+ * TQ_DEVERR_TIMEOUT and the kernel returns). Launches one kernel on `stream`
+ * whose single thread waits on an mbarrier nothing arrives on, with a deadline
+ * of `seconds` (0 < seconds <= 1, else TQ_ERR_INVALID_ARG, nothing launched)
+ * on the GPU's global timer; when it passes, the kernel sets
+ * TQ_DEVERR_TIMEOUT in the device error word, invalidates the barrier and
+ * returns. No fault and no hang: the device stays usable, and the next
+ * tq_device_error() reports and clears the bit. Returns TQ_ERR_CUDA if the
+ * launch fails. */
+tq_status tq_selftest_wait_timeout(double seconds, tq_stream_t stream);
 int tq_abi_version(void);
 
 #ifdef __cplusplus

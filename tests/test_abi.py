@@ -182,6 +182,12 @@ def test_decode_plan_rejects_bad_sizes(libtq):
     assert libtq.tq_decode_plan(ctypes.byref(d), 1, 8 * 65, 1, 100, 152, ctypes.byref(info)) == _lib.TQ_ERR_UNSUPPORTED
 
 
+def test_selftest_wait_timeout_rejects_bad_deadlines_without_device(libtq):
+    # the deadline is checked on the host before any CUDA call (none is possible here)
+    for s in (0.0, -0.5, 1.01, float("nan"), float("inf")):
+        assert libtq.tq_selftest_wait_timeout(s, None) == _lib.TQ_ERR_INVALID_ARG
+
+
 def test_workspace_query_rejects_a_descriptor_without_heads(libtq):
     # checked on the host before any division by the head count or device call
     d = _desc_from_oracle(128, ("prod", 3), ("mse", 3, 0), 256, 8)

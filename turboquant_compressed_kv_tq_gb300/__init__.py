@@ -27,7 +27,7 @@ __all__ = [
     "tq_decode_partials", "tq_decode_merge",
     "tq_encode_append_split", "tq_decode_workspace_bytes_split", "tq_decode_attention_split", "SplitCache",
     "tq_batch_filter", "tq_batch_extend", "tq_batch_merge", "tq_batch_extract", "Batch",
-    "tq_device_error",
+    "tq_device_error", "tq_selftest_wait_timeout",
     "tq_launch_count", "tq_abi_version", "Codec", "CompressedKVCache", "TQError",
     "TQ_MODE_MSE", "TQ_MODE_PROD", "TQ_MODE_GROUP", "TQ_F32", "TQ_BF16", "TQ_F16",
     "TQ_ENCODE_AUTO", "TQ_ENCODE_EXACT",
@@ -397,6 +397,10 @@ def tq_device_error() -> int:
     if st not in (TQ_OK, 7):
         check(st, "tq_device_error")
     return flags.value
+
+
+def tq_selftest_wait_timeout(seconds: float, stream=None) -> None:
+    check(lib().tq_selftest_wait_timeout(float(seconds), _stream(stream)), "tq_selftest_wait_timeout")
 
 
 # ----------------------------------------------------------------- helpers

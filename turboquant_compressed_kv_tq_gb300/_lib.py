@@ -137,6 +137,7 @@ SIGNATURES = {
     "tq_batch_merge": (_ST, [ctypes.POINTER(tq_batch), ctypes.POINTER(tq_batch), _I, _P, _I, _P, _P]),
     "tq_batch_extract": (_ST, [ctypes.POINTER(tq_batch), _I, ctypes.POINTER(tq_batch), _P, _I, _P, _P]),
     "tq_device_error": (_ST, [ctypes.POINTER(ctypes.c_uint32)]),
+    "tq_selftest_wait_timeout": (_ST, [ctypes.c_double, _P]),
 }
 
 _lock = threading.Lock()

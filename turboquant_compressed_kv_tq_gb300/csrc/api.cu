@@ -43,6 +43,34 @@ tq_status device_state(unsigned** err, int* num_sms) {
     return TQ_OK;
 }
 
+// The bounded-wait error path, on its own: one thread waits on an mbarrier
+// that nothing arrives on (mbarrier.try_wait.parity in a loop, as the kernels
+// wait for their bulk copies), bounded by a deadline on the global timer (and,
+// as a backstop, by an iteration count); when the deadline passes it sets
+// TQ_DEVERR_TIMEOUT, invalidates the barrier and returns.
+__global__ void wait_timeout_kernel(unsigned* err, unsigned long long limit_ns) {
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x != 0) return;
+    const uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(&bar));
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;\n" ::"r"(a) : "memory");
+    unsigned long long t0, t;
+    asm volatile("mov.u64 %0, %%globaltimer;\n" : "=l"(t0));
+    bool done = false;
+    for (unsigned it = 0; it < (1u << 24) && !done; ++it) {
+        uint32_t ok;
+        asm volatile(
+            "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}\n"
+            : "=r"(ok)
+            : "r"(a), "r"(0u), "r"(1000u)
+            : "memory");
+        done = ok != 0;
+        asm volatile("mov.u64 %0, %%globaltimer;\n" : "=l"(t));
+        if (t - t0 > limit_ns) break;
+    }
+    if (!done) atomicOr(err, TQ_DEVERR_TIMEOUT);
+    asm volatile("mbarrier.inval.shared::cta.b64 [%0];\n" ::"r"(a) : "memory");
+}
+
 int index_bits_of(int bits, int mode) { return mode == TQ_MODE_PROD ? bits - 1 : bits; }
 
 int record_bytes_of(int D, int bits, int mode, int group) {
@@ -1044,6 +1072,16 @@ tq_status tq_prefill_attention(const tq_codec* kc, const tq_codec* vc, const tq_
                    cudaSuccess
                ? TQ_OK
                : TQ_ERR_CUDA;
+}
+
+tq_status tq_selftest_wait_timeout(double seconds, tq_stream_t stream) {
+    if (!(seconds > 0.0 && seconds <= 1.0)) return TQ_ERR_INVALID_ARG;
+    unsigned* err = nullptr;
+    if (device_state(&err, nullptr) != TQ_OK) return TQ_ERR_CUDA;
+    wait_timeout_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+        err, static_cast<unsigned long long>(seconds * 1e9));
+    ++g_launches;
+    return cudaGetLastError() == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
 }
 
 tq_status tq_device_error(uint32_t* flags) {
