@@ -99,6 +99,7 @@ void free_codec(tq_codec* c) {
     cudaFree(c->d_quad);
     cudaFree(c->d_pair);
     cudaFree(c->d_pair4);
+    cudaFree(c->d_pair4w);
     if (prev >= 0) cudaSetDevice(prev);
     delete c;
 }
@@ -155,6 +156,18 @@ std::vector<uint32_t> pair4_table(const std::vector<float>& cq) {
     return t;
 }
 
+// The same pairs in 256-byte entries: entry e at 256 e + 4 c for c < 64 (the
+// byte of codes itself times 256 is the entry's offset: one byte permute
+// forms a lane's address).
+std::vector<uint32_t> pair4w_table(const std::vector<float>& cq) {
+    std::vector<uint32_t> t(256 * 64);
+    for (int i = 0; i < 256 * 64; ++i) {
+        const int e = i >> 6;
+        t[i] = half_bits_exact(cq[e & 15]) | (half_bits_exact(cq[e >> 4]) << 16);
+    }
+    return t;
+}
+
 std::vector<float> transpose(const std::vector<float>& a, int D) {
     std::vector<float> t(a.size());
     for (int i = 0; i < D; ++i)
@@ -194,6 +207,7 @@ CodecDev dev_view(const tq_codec* c) {
     d.quad = c->d_quad;
     d.pair = c->d_pair;
     d.pair4 = c->d_pair4;
+    d.pair4w = c->d_pair4w;
     d.D = c->head_dim;
     d.mode = c->mode;
     d.bits = c->bits;
@@ -355,6 +369,8 @@ tq_status tq_codec_create(int head_dim, int bits, tq_mode mode, uint64_t seed, t
     if (st == TQ_OK && c->index_bits == 3) st = upload(&c->d_pair, pair_table(c->host.op_levels));
     if (st == TQ_OK && c->index_bits == 4 && mode == TQ_MODE_MSE)
         st = upload(&c->d_pair4, pair4_table(c->host.op_levels));
+    if (st == TQ_OK && c->index_bits == 4 && mode == TQ_MODE_MSE)
+        st = upload(&c->d_pair4w, pair4w_table(c->host.op_levels));
     if (st == TQ_OK && head_dim <= 128) {
         // tensor-core operands for the chunked-prefill encoder: 16 R and S, fp16 hi + lo
         std::vector<uint16_t> op;
@@ -788,6 +804,12 @@ tq_status decode_args(const tq_codec* kc, const tq_codec* vc, const tq_cache_des
     a = DecodeArgs{};
     a.kc = dev_view(kc);
     a.vc = dev_view(vc);
+    // 4-bit MSE keys and values of one codebook (the levels depend on the head
+    // dimension and the width only): one wide pair table serves both
+    if (kc->d_pair4w && vc->d_pair4w && kc->host.op_levels.size() == vc->host.op_levels.size() &&
+        std::memcmp(kc->host.op_levels.data(), vc->host.op_levels.data(),
+                    kc->host.op_levels.size() * sizeof(float)) == 0)
+        a.vc.pair4w = a.kc.pair4w;
     a.pool = pool_view(cache, layer);
     a.q = q;
     a.q_dtype = q_dtype;

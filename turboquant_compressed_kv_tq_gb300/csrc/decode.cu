@@ -485,20 +485,23 @@ DecodePlan make_decode_plan(const tq_cache_desc* d, int batch, int G, int Lq, in
                 o += p.tile * p.st_field[k];
             }
             p.st_bytes = (o + 127) / 128 * 128;
-            const size_t ring = static_cast<size_t>(mmadec::kWarps) * mmadec::kStages * p.st_bytes;
+            // 4-bit MSE keys and values: their one table of 256-byte entries at offset 0
+            const bool wide = mmadec::pair4_wide(D, p.kb, p.kprod, p.vgroup, p.vb);
+            p.ring_off = wide ? mmadec::kPair4WBytes : 0;
+            const size_t ring = p.ring_off + static_cast<size_t>(mmadec::kWarps) * mmadec::kStages * p.st_bytes;
             p.qs_off = static_cast<int>(ring);
             size_t ringq = ring + static_cast<size_t>(mmadec::kQFragBytes) * NH;
-            p.vt_off = -1;
+            p.vt_off = wide ? 0 : -1;
             if (!p.vgroup && p.vb == 3) {  // pair table of 3-bit value codes (aligned inside the region)
                 p.vt_off = static_cast<int>(ringq);
                 ringq += mmadec::kVPairRegion;
             }
-            if (mmadec::pair4_values(D, p.kprod, p.vgroup, p.vb)) {  // pair table of 4-bit value codes
+            if (!wide && mmadec::pair4_values(D, p.kprod, p.vgroup, p.vb)) {  // pair table of 4-bit value codes
                 p.vt_off = static_cast<int>(ringq);
                 ringq += mmadec::kPair4Bytes;
             }
-            p.kt_off = -1;
-            if (mmadec::pair4_keys(D, p.kb, p.kprod)) {  // pair table of 4-bit key codes
+            p.kt_off = wide ? 0 : -1;
+            if (!wide && mmadec::pair4_keys(D, p.kb, p.kprod)) {  // pair table of 4-bit key codes
                 p.kt_off = static_cast<int>(ringq);
                 ringq += mmadec::kPair4Bytes;
             }
@@ -576,6 +579,7 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s, const EncodeAppen
         m.st.qs_off = a.plan.qs_off;
         m.st.vt_off = a.plan.vt_off;
         m.st.kt_off = a.plan.kt_off;
+        m.st.ring_off = a.plan.ring_off;
         for (int k = 0; k < 7; ++k) {
             m.st.off[k] = a.plan.st_off[k];
             m.st.field[k] = a.plan.st_field[k];

@@ -74,6 +74,15 @@ __host__ __device__ constexpr bool pair4_keys(int d, int kb, bool kprod) { retur
 __host__ __device__ constexpr bool pair4_values(int d, bool kprod, bool vgroup, int vb) {
     return d <= kD && !kprod && !vgroup && vb == 4;
 }
+// With 4-bit MSE keys and values both: one table of 256-byte entries at
+// shared offset 0 (256 entries x two sets of 32 bank copies x 4 bytes; keys
+// read set 0, values set 1), the lane's address one byte permute of the code
+// word (the byte of codes x 256 + the lane's copy) with the table's base
+// folded into the load.
+constexpr int kPair4WBytes = 256 * 64 * 4;
+__host__ __device__ constexpr bool pair4_wide(int d, int kb, bool kprod, bool vgroup, int vb) {
+    return pair4_keys(d, kb, kprod) && pair4_values(d, kprod, vgroup, vb);
+}
 // QJL sign operands through a shared table of sign nibbles (16 entries x 16
 // bank copies x 8 bytes), placed in the slack of the value pair table's
 // region: prod keys with 3-bit MSE values.

@@ -32,6 +32,7 @@ struct StageLayout {
     int qs_off;             // byte offset of the query fragments (past the ring)
     int vt_off;             // byte offset of the value pair table region (-1: none)
     int kt_off;             // byte offset of the key quad table (-1: none)
+    int ring_off;           // byte offset of the stage rings
 };
 
 struct MmaArgs {
@@ -322,6 +323,15 @@ __device__ __forceinline__ void pair4_word(uint32_t w, uint32_t lane_addr, uint3
         const uint32_t f = k == 0 ? shl_f(w, 7) : (w >> (8 * k - 7));
         h[k] = lds_u32(mad_lo(f & 0x7F80u, kDc.pow2[0], lane_addr));
     }
+}
+
+// The same from the table of 256-byte entries at the start of shared memory:
+// the entry's offset is byte k of w times 256, the lane's copy lane_b (< 256),
+// so one byte permute gives the offset (byte 0 = lane_b, byte 1 = byte k of w).
+__device__ __forceinline__ void pair4w_word(const unsigned char* tab, uint32_t w, uint32_t lane_b, uint32_t (&h)[4]) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+        h[k] = *reinterpret_cast<const uint32_t*>(tab + __byte_perm(w, lane_b, 0x5504u | (k << 4)));
 }
 
 template <int B>
@@ -649,7 +659,9 @@ __global__ void __launch_bounds__(kThreads, 1) split_mma_kernel(MmaArgs m) {
     const int BT = a.pool.BT;
     const int TT = st.tt;
 
-    unsigned char* ring = smem + static_cast<size_t>(warp) * kStages * st.bytes;
+    // (the rings start past a table at offset 0 in the kernels that keep one there)
+    unsigned char* ring = smem + (pair4_wide(D, KB, KPROD, VGROUP, VB) ? st.ring_off : 0) +
+                          static_cast<size_t>(warp) * kStages * st.bytes;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + st.bar_off) + warp * kStages;
 
     const int N = a.seq_lens[b] + a.len_add;
@@ -683,17 +695,22 @@ __global__ void __launch_bounds__(kThreads, 1) split_mma_kernel(MmaArgs m) {
     }
     // 4-bit MSE keys / values through the shared 4-bit pair table (MSE keys)
     constexpr bool kP4K = pair4_keys(D, KB, KPROD), kP4V = pair4_values(D, KPROD, VGROUP, VB);
+    // both: one table of 256-byte entries at offset 0 (keys copy set 0, values set 1)
+    constexpr bool kP4W = pair4_wide(D, KB, KPROD, VGROUP, VB);
     const bool quad_copy = kQuadTab && a.kc.quad, pair_copy = kPairTab && a.vc.pair;
-    const bool p4k_copy = kP4K && a.kc.pair4, p4v_copy = kP4V && a.vc.pair4;
+    const bool p4k_copy = kP4K && !kP4W && a.kc.pair4, p4v_copy = kP4V && !kP4W && a.vc.pair4;
+    const bool p4w_copy = kP4W && a.kc.pair4w && a.kc.pair4w == a.vc.pair4w;   // one codebook
     if (threadIdx.x == 0) {
         mbar_init(tbar, 2);
         mbar_fence_init();
         mbar_expect_tx(tbar, (quad_copy ? kKQuadBytes : 0) + (pair_copy ? kVPairBytes : 0) +
-                                 (p4k_copy ? kPair4Bytes : 0) + (p4v_copy ? kPair4Bytes : 0));
+                                 (p4k_copy ? kPair4Bytes : 0) + (p4v_copy ? kPair4Bytes : 0) +
+                                 (p4w_copy ? kPair4WBytes : 0));
         if (quad_copy) bulk_g2s(smem + st.kt_off, a.kc.quad, kKQuadBytes, tbar);
         if (pair_copy) bulk_g2s(smem + pair_off, a.vc.pair, kVPairBytes, tbar);
         if (p4k_copy) bulk_g2s(smem + st.kt_off, a.kc.pair4, kPair4Bytes, tbar);
         if (p4v_copy) bulk_g2s(smem + st.vt_off, a.vc.pair4, kPair4Bytes, tbar);
+        if (p4w_copy) bulk_g2s(smem, a.kc.pair4w, kPair4WBytes, tbar);
     }
     // a codec without the prebuilt table: build it here
     auto build_pair4 = [&](uint32_t* tab, const float* cq) {
@@ -703,13 +720,27 @@ __global__ void __launch_bounds__(kThreads, 1) split_mma_kernel(MmaArgs m) {
         }
     };
     uint32_t k4_lane = 0, v4_lane = 0;
-    if constexpr (kP4K) {
-        k4_lane = smem_u32(smem + st.kt_off) + 4u * lane;
-        if (!p4k_copy) build_pair4(reinterpret_cast<uint32_t*>(smem + st.kt_off), a.kc.cq);
-    }
-    if constexpr (kP4V) {
-        v4_lane = smem_u32(smem + st.vt_off) + 4u * lane;
-        if (!p4v_copy) build_pair4(reinterpret_cast<uint32_t*>(smem + st.vt_off), a.vc.cq);
+    if constexpr (kP4W) {
+        // the lanes' copies: bytes 4 lane (keys) and 128 + 4 lane (values) of an entry
+        k4_lane = 4u * lane;
+        v4_lane = 128u + 4u * lane;
+        if (!p4w_copy) {   // codecs without one shared prebuilt table: build it here
+            uint32_t* tab = reinterpret_cast<uint32_t*>(smem);
+            for (int i = threadIdx.x; i < 256 * 64; i += kThreads) {
+                const int e = i >> 6;
+                const float* cq = (i & 63) < 32 ? a.kc.cq : a.vc.cq;
+                tab[i] = h_bits(__ldg(cq + (e & 15))) | (h_bits(__ldg(cq + (e >> 4))) << 16);
+            }
+        }
+    } else {
+        if constexpr (kP4K) {
+            k4_lane = smem_u32(smem + st.kt_off) + 4u * lane;
+            if (!p4k_copy) build_pair4(reinterpret_cast<uint32_t*>(smem + st.kt_off), a.kc.cq);
+        }
+        if constexpr (kP4V) {
+            v4_lane = smem_u32(smem + st.vt_off) + 4u * lane;
+            if (!p4v_copy) build_pair4(reinterpret_cast<uint32_t*>(smem + st.vt_off), a.vc.cq);
+        }
     }
     typename MseTable<KB>::type ktab{};
     if constexpr (!kQuadTab && !kP4K) ktab = mse_table<KB>(a.kc.cq);
@@ -957,7 +988,8 @@ __global__ void __launch_bounds__(kThreads, 1) split_mma_kernel(MmaArgs m) {
                 uint32_t hk[NT][4];
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) {
-                    if constexpr (kP4K) pair4_word(kw[nt][q2 < KB ? q2 : 0], k4_lane, hk[nt]);
+                    if constexpr (kP4W) pair4w_word(smem, kw[nt][q2 < KB ? q2 : 0], k4_lane, hk[nt]);
+                    else if constexpr (kP4K) pair4_word(kw[nt][q2 < KB ? q2 : 0], k4_lane, hk[nt]);
                     else key_ks2<KB, kQuadTab>(kw[nt], ktab, kt_lane, q2, hk[nt]);
                 }
 #pragma unroll
@@ -1041,8 +1073,13 @@ __global__ void __launch_bounds__(kThreads, 1) split_mma_kernel(MmaArgs m) {
 #pragma unroll
                     for (int wi = 0; wi < 4; ++wi) {
                         uint32_t ga[4], gb[4];
-                        pair4_word(wA[wi < VB ? wi : 0], v4_lane, ga);
-                        pair4_word(wB[wi < VB ? wi : 0], v4_lane, gb);
+                        if constexpr (kP4W) {
+                            pair4w_word(smem, wA[wi < VB ? wi : 0], v4_lane, ga);
+                            pair4w_word(smem, wB[wi < VB ? wi : 0], v4_lane, gb);
+                        } else {
+                            pair4_word(wA[wi < VB ? wi : 0], v4_lane, ga);
+                            pair4_word(wB[wi < VB ? wi : 0], v4_lane, gb);
+                        }
 #pragma unroll
                         for (int k = 0; k < 4; ++k) {
                             hA[4 * wi + k] = ga[k];

@@ -56,6 +56,8 @@ struct CodecDev {
     const uint32_t* pair;
     const uint32_t* pair4;  // 4-bit code pairs, entry e (a byte) at 128 e + 4 c for bank copy c < 32:
                             // fp16 pair (cq[e & 15], cq[e >> 4]); or nullptr
+    const uint32_t* pair4w; // the same pairs in 256-byte entries (e at 256 e + 4 c for c < 64: two
+                            // sets of bank copies, for keys and values), or nullptr
     int D;
     int mode;          // tq_mode
     int bits;          // total bits
@@ -118,6 +120,7 @@ struct DecodePlan {
     int qs_off;       // shared-memory offset of the query fragments
     int vt_off;       // shared-memory offset of the 3-bit value pair table region (-1: unused)
     int kt_off;       // shared-memory offset of the 2-bit key quad table (-1: unused)
+    int ring_off;     // shared-memory offset of the stage rings (after a table at offset 0)
     size_t smem;      // dynamic shared memory of the split kernel
     size_t q_bytes;   // SIMT and head_dim 256: q' and q'' buffers (each); tensor cores at 128: query fragments
     size_t part_bytes;// partial accumulators
@@ -265,4 +268,5 @@ struct tq_codec {
     uint32_t* d_quad = nullptr;  // decode lookup table of 2-bit code quads (index bits 2)
     uint32_t* d_pair = nullptr;  // decode lookup table of 3-bit code pairs (index bits 3)
     uint32_t* d_pair4 = nullptr;  // decode lookup table of 4-bit code pairs (MSE, index bits 4)
+    uint32_t* d_pair4w = nullptr; // the same in 256-byte entries
 };
