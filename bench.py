@@ -236,6 +236,19 @@ def cpu_baseline(w, kv_heads=2, device="cuda", min_repeats=3, min_seconds=10.0, 
     return smp.nbytes / t / 1e9, smp.O.num_threads(), desc, sum(times)
 
 
+def cpu_baseline_one_core(w, device="cuda"):
+    """The same oracle decode on one host core: one KV head of the sample,
+    timed once. Returns (value, sample)."""
+    smp = OracleSample(w, 1, device)
+    cores = smp.O.num_threads()
+    smp.O.set_num_threads(1)
+    try:
+        t = smp.decode_seconds()
+    finally:
+        smp.O.set_num_threads(cores)
+    return smp.nbytes / t / 1e9, smp.describe() + "; one timed decode on 1 thread"
+
+
 def _workload(args):
     from turboquant_compressed_kv_tq_gb300 import workloads as wl
     w = wl.WORKLOADS[args.workload]()
@@ -535,8 +548,9 @@ def run_gpu(args):
         cpu = None
         if world == 1 and not args.no_cpu_baseline:
             v, cores, sample, secs = cpu_baseline(w, kv_heads=2, device=dev)
+            v1, sample1 = cpu_baseline_one_core(w, device=dev)
             cpu = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample,
-                   "seconds": round(secs, 2)}
+                   "seconds": round(secs, 2), "one_core": {"value": v1, "unit": UNIT, "cores": 1, "sample": sample1}}
         clocks = clk.summary()
         plan = tq.tq_decode_plan(cache.desc, B, Hq, Lq, cap,
                                  torch.cuda.get_device_properties(dev).multi_processor_count)

@@ -94,6 +94,7 @@ def _declare(L):
         "tqo_pool_write": (None, [_P, _I, _I, _I, _P, _I, _I, _I, _I64, _I64, _I, _I, _I, _I, _I,
                                   _P, _P, _P, _P, _P, _P, _P, _P]),
         "tqo_num_threads": (_I, []),
+        "tqo_set_num_threads": (None, [_I]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -335,3 +336,7 @@ def pool_write(pool: np.ndarray, kc: Codec, vc: Codec, Hkv: int, BT: int, table,
 
 def num_threads() -> int:
     return lib().tqo_num_threads()
+
+
+def set_num_threads(n: int) -> None:
+    lib().tqo_set_num_threads(int(n))

@@ -65,6 +65,15 @@ int tqo_num_threads(void) {
 #endif
 }
 
+/* Threads of the parallel loops that follow (timing on one core and on all). */
+void tqo_set_num_threads(int n) {
+#ifdef _OPENMP
+    if (n > 0) omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}
+
 /* ------------------------------------------------------------------ */
 /* [R1] SplitMix64 (Vigna): state += golden gamma, then the mix.       */
 /* ------------------------------------------------------------------ */

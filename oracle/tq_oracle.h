@@ -117,6 +117,7 @@ void tqo_pool_write(uint8_t *pool, int D, int Hkv, int BT, const int32_t *table,
                     const uint16_t *vscale, const uint16_t *vmin);
 
 int tqo_num_threads(void);
+void tqo_set_num_threads(int n);
 
 #ifdef __cplusplus
 }
