@@ -33,6 +33,16 @@
  *     table, a block id outside the pool) skip the offending access and set
  *     bits in a per-device error word read by tq_device_error().
  *   - Shapes are row-major and contiguous.
+ *   - Consecutive calls on one stream overlap at their boundaries (programmatic
+ *     dependent launch): a call's first kernel may start, and read its plain
+ *     inputs (q, k, v, k_new, v_new), while the previous call's last kernel
+ *     is still finishing. Every read of cache records, block tables, lengths
+ *     and workspaces waits for the kernels before it; the plain inputs do not.
+ *     So q, k, v, k_new and v_new must not be the output (out, or a shard's
+ *     state) of the immediately preceding decode call (tq_decode_attention,
+ *     tq_decode_attention_noalloc, tq_decode_step, tq_decode_partials) on the
+ *     same stream: any other kernel or memory copy enqueued between the two
+ *     calls (as a model's projections are) restores plain stream order.
  */
 #ifndef TQ_H
 #define TQ_H
