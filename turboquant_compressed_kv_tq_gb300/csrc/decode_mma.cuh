@@ -1,26 +1,35 @@
-// Tensor-core split-K decode attention over the TurboQuant cache, head_dim 128.
+// Tensor-core split-K decode attention over the TurboQuant cache (head_dims
+// 64, 128 and 256; 64 runs in the 128 layout, 256 as two CTAs per unit, one
+// per 128-column half of the values).
 //
 // Per (token split, kv head, row group of 16 query rows, sequence) one CTA of
 // kWarps warps. Every warp streams its own tiles of compressed records from
 // HBM into a private ring of shared-memory stages with 1-D bulk copies
-// (cp.async.bulk, completion on an mbarrier), and runs, 16 tokens at a time:
+// (cp.async.bulk, completion on an mbarrier), and runs, 32 tokens at a time:
 //   scores  S = Q' K_hat^T (+ Q'' sigma^T for prod keys) on mma.sync
 //           m16n8k16 (fp16 operands, fp32 accumulate); the key operand is
 //           decoded from the packed indices straight into MMA fragments:
 //           2-bit indices through a shared table of code quads (one 64-bit
-//           load per four levels), other widths with byte-permute lookups in
-//           registers; QJL signs as exact +-1 operands, their products
-//           weighted by the residual norm in fp32; codebook operands are the
-//           fp16 numbers nearest to op_scale * level (a per-codebook scale
-//           that keeps the rounding error small), op_scale divided out in the
+//           load per four levels), 4-bit MSE indices through a shared table
+//           of code pairs, other widths with byte-permute lookups in
+//           registers; QJL signs as exact +-1 operands (with 3-bit MSE values
+//           through a shared table of sign nibbles), their products weighted
+//           by the residual norm in fp32; codebook operands are the fp16
+//           numbers nearest to op_scale * level (a per-codebook scale that
+//           keeps the rounding error small), op_scale divided out in the
 //           query (keys) and in the merge (values);
 //   softmax online, in log2 units (scale * log2(e) folded into the query),
 //           with a lagging row maximum;
 //   values  O += P' V_hat on mma.sync, P' = p * value norm, V_hat decoded per
-//           token into registers (3-bit indices through a shared table of
-//           code pairs) and transposed to the MMA operand layout with movmatrix.
-// Warps merge in shared memory; the CTA writes (max, sum, acc) partials and
-// the last CTA of each (sequence, head, row group) merges the splits, applies
+//           token into registers (3- and 4-bit MSE indices through shared
+//           tables of code pairs; group codes or-ed into the mantissa of an
+//           fp16 1.0, then one subtraction and one multiply-add by the
+//           group's scale and minimum) and transposed to the MMA operand
+//           layout with movmatrix.
+// With at most 8 query rows per KV head a transposed form puts 16 tokens on
+// the MMA's M and the rows on N (S^T = K Q^T, O^T = V^T P^T). Warps merge in
+// shared memory; each CTA writes its split's (max, sum, acc) rows, and a
+// separate merge kernel (one CTA per output row) combines the splits, applies
 // the inverse value rotation and writes the output.
 //
 // Query fragments are prepared by a separate kernel (or inside the fused
