@@ -496,6 +496,10 @@ DecodePlan make_decode_plan(const tq_cache_desc* d, int batch, int G, int Lq, in
                 p.vt_off = static_cast<int>(ringq);
                 ringq += mmadec::kVPairRegion;
             }
+            if (p.vgroup && mmadec::nibble_qjl(p.kprod, p.vgroup, p.vb)) {  // QJL sign nibbles (aligned inside)
+                p.vt_off = static_cast<int>(ringq);
+                ringq += mmadec::kQNibRegion;
+            }
             if (!wide && mmadec::pair4_values(D, p.kprod, p.vgroup, p.vb)) {  // pair table of 4-bit value codes
                 p.vt_off = static_cast<int>(ringq);
                 ringq += mmadec::kPair4Bytes;

@@ -93,10 +93,14 @@ __host__ __device__ constexpr bool pair4_wide(int d, int kb, bool kprod, bool vg
     return pair4_keys(d, kb, kprod) && pair4_values(d, kprod, vgroup, vb);
 }
 // QJL sign operands through a shared table of sign nibbles (16 entries x 16
-// bank copies x 8 bytes), placed in the slack of the value pair table's
-// region: prod keys with 3-bit MSE values.
+// bank copies x 8 bytes) at a 2 KB-aligned shared address: prod keys with
+// 3-bit MSE values (in the slack of the value pair table's region) or with
+// group values (in a 4 KB region of its own).
 constexpr int kQNibBytes = 16 * 16 * 8;
-__host__ __device__ constexpr bool nibble_qjl(bool kprod, bool vgroup, int vb) { return kprod && !vgroup && vb == 3; }
+constexpr int kQNibRegion = 4096;
+__host__ __device__ constexpr bool nibble_qjl(bool kprod, bool vgroup, int vb) {
+    return kprod && (vgroup || vb == 3);
+}
 // Coordinate order of the query fragments: bit 0 natural pair order of the
 // codebook part (quad-table keys), bit 1 natural pair order of the QJL part
 // (nibble-table signs); otherwise the byte-permute decoders' orders.

@@ -766,8 +766,13 @@ __global__ void __launch_bounds__(kThreads, 1) split_mma_kernel(MmaArgs m) {
     uint32_t qn_lane = 0;
     if constexpr (kNibQ) {
         const uint32_t region = smem_u32(smem + st.vt_off);
-        const uint32_t pair_at = smem_u32(smem + pair_off);
-        const uint32_t nib = pair_at - region >= 4096u ? (region + 2047u) & ~2047u : pair_at + kVPairBytes;
+        uint32_t nib;
+        if constexpr (kPairTab) {
+            const uint32_t pair_at = smem_u32(smem + pair_off);
+            nib = pair_at - region >= 4096u ? (region + 2047u) & ~2047u : pair_at + kVPairBytes;
+        } else {
+            nib = (region + 2047u) & ~2047u;   // group values: a 4 KB region of its own
+        }
         qn_lane = nib + 8u * (lane & 15);
         uint2* tab = reinterpret_cast<uint2*>(smem + st.vt_off + (nib - region));
         for (int i = threadIdx.x; i < 16 * 16; i += kThreads) {
