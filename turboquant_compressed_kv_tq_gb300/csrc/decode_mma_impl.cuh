@@ -1530,6 +1530,11 @@ __global__ void __launch_bounds__(kQRThreads) qrows_kernel(DecodeArgs a) {
     float* ms = qr_smem;        // [D][32] the matrix slice
     float* qs = ms + D * 32;    // [16][D] query rows
     __shared__ uint64_t bar;
+    // This kernel is a plain launch (it starts after everything before it on
+    // the stream is complete, the records included), so the split kernel may
+    // start its prologue (tables, first record copies) at once; it waits for
+    // this grid before it reads the rows written below.
+    tc::grid_release_dependents();
     const int unit = blockIdx.x, c0 = 32 * blockIdx.y;
     const bool qjl = blockIdx.z != 0;
     const float* M = qjl ? a.kc.SRt : a.kc.Rt;
